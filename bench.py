@@ -1,0 +1,350 @@
+"""Benchmark: CSA prefill of 1 x 8192 tokens on one B300 (tokens/s).
+
+One step = the whole CSA hot path over one batch of synthetic input, through
+the C ABI of libcsa_b300.so: block compression of the KV cache (m = 4, mixed
+FP8/BF16 rows) and of the window cache (m = 1), compression of the FP4
+indexer keys, lightning-indexer scores + top-k (k = 512), and sparse MQA over
+the selected entries plus the 128-token window (64 heads, D = 512).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With torchrun (N > 1) every rank runs its own sequence (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+CFG = wl.CONFIGS["c2_csa_prefill_8k"]
+METRIC = "CSA prefill tokens/s (1x8192, m=4, top-k 512, window 128, 64 heads, D=512)"
+
+
+def attn_flops(cfg) -> float:
+    """Algorithmic flops of the sparse MQA step: per query and head 4D per key
+    (QK^T and PV), keys = min(k, visible entries) + min(W, t + 1)."""
+    t = np.arange(cfg.T, dtype=np.int64)
+    keys = np.minimum(cfg.k, np.minimum(cfg.N, (t + 1) // cfg.m)) + np.minimum(cfg.W, t + 1)
+    return float(keys.sum()) * cfg.H * 4 * cfg.D
+
+
+def indexer_flops(cfg) -> float:
+    t = np.arange(cfg.T, dtype=np.int64)
+    pairs = np.minimum(cfg.N, (t + 1) // cfg.m).sum()
+    return float(pairs) * 2 * cfg.HI * cfg.dI
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thr = threading.Thread(target=self._read, daemon=True)
+            self.thr.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+
+    def summary(self):
+        sm = [float(r[0]) for r in self.rows if len(r) >= 7 and r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if len(r) >= 7 and r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows if len(r) >= 7 for i in range(4)
+                          if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# inputs
+# --------------------------------------------------------------------------
+def host_inputs(seed: int):
+    toks = wl.gen_tokens(CFG, 0, seed=seed)
+    qry = wl.gen_queries(CFG, 0, seed=seed)
+    sc = wl.gen_channel_scales(CFG, seed=seed)
+    return {"kv": toks["kv"][None], "z": toks["z"][None], "kI": toks["kI"][None], "zI": toks["zI"][None],
+            "q": qry["q"][None], "qI": qry["qI"][None], "w": qry["w"][None], "s": sc["s"], "sI": sc["sI"],
+            "q_pos": np.arange(CFG.T, dtype=np.int64)[None], "swa_pos0": np.zeros(1, np.int64)}
+
+
+BF16_KEYS = ("kv", "kI", "q", "qI")
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import long_context_sparse_29_b300 as csa
+    from long_context_sparse_29_b300 import build as csa_build
+
+    csa_build.build()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    h = host_inputs(seed=rank)
+    pinned = {}
+    for kname, a in h.items():
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if kname in BF16_KEYS else a)
+        if kname in BF16_KEYS:
+            t = t.view(torch.bfloat16)
+        pinned[kname] = t.pin_memory()
+    d = {kname: t.cuda() for kname, t in pinned.items()}
+    rope = csa.rope_table(CFG.T + 1, CFG.R)
+    scale = 1.0 / math.sqrt(CFG.D)
+    T, N, m, k, W = CFG.T, CFG.N, CFG.m, CFG.k, CFG.W
+    dev = torch.device("cuda", local_rank)
+    cache = torch.empty((1, N, 592), dtype=torch.uint8, device=dev)
+    swa = torch.empty((1, T, 592), dtype=torch.uint8, device=dev)
+    kcodes = torch.empty((1, N, CFG.dI // 2), dtype=torch.uint8, device=dev)
+    kscales = torch.empty((1, N, CFG.dI // 32), dtype=torch.uint8, device=dev)
+    idx = torch.empty((1, T, k), dtype=torch.int32, device=dev)
+    out = torch.empty((1, T, CFG.H, CFG.D), dtype=torch.bfloat16, device=dev)
+    ws = csa.Workspace(dev)
+    stream = torch.cuda.current_stream(dev)
+    ev_attn = []
+
+    def step(x, timed=False):
+        csa.compress_kv(x["kv"], x["z"], x["s"], m, csa.FMT_MIXED592, CFG.R, rope, out=cache)
+        csa.compress_kv(x["kv"], x["z"], None, 1, csa.FMT_MIXED592, CFG.R, rope, out=swa)
+        csa.compress_kv(x["kI"], x["zI"], x["sI"], m, csa.FMT_MXFP4, 0, out=kcodes, out_scales=kscales)
+        csa.indexer_topk(x["qI"], x["w"], kcodes, kscales, x["q_pos"], N, m, k, scores=False,
+                         idx_out=idx, ws=ws)
+        if timed:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        csa.sparse_mqa(x["q"], x["q_pos"], cache, m, idx, swa, x["swa_pos0"], W, scale, rope,
+                       CFG.R, out=out, ws=ws)
+        if timed:
+            e1.record(stream)
+            ev_attn.append((e0, e1))
+
+    for _ in range(args.warmup):
+        step(d)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(d, timed=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_attn)
+    flags = ws.flags()
+    if flags:
+        raise RuntimeError(f"device check flags {flags} during the benchmark")
+
+    # end to end through the public API with host buffers: H2D of the step's inputs,
+    # the step, D2H of the output
+    in_keys = ("kv", "z", "kI", "zI", "q", "qI", "w", "s", "sI", "q_pos", "swa_pos0")
+    h2d = sum(pinned[kname].numel() * pinned[kname].element_size() for kname in in_keys)
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(2, min(args.steps, 5))
+    dd = {kname: torch.empty_like(d[kname]) for kname in in_keys}
+
+    def e2e_step():
+        for kname in in_keys:
+            dd[kname].copy_(pinned[kname], non_blocking=True)
+        step(dd)
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    if dist:
+        t = torch.tensor([ms, e2e_ms, attn_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms, attn_ms = (float(x) for x in t.tolist())
+    pk = peaks()
+    af = attn_flops(CFG)
+    achieved = af / (attn_ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops"]
+    ms_step = ms / args.steps
+    res = {
+        "metric": METRIC, "value": world * T / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": CFG.name, "B": 1, "T": T, "m": m, "N": N, "k": k, "W": W, "H": CFG.H,
+                   "D": CFG.D, "HI": CFG.HI, "dI": CFG.dI, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (q and out 512 MiB each per step)"},
+        "roofline": {"kernel": "sparse_mqa", "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_src": f"bf16 dense, {pk['src']} (burst)",
+                     "algorithmic_flops_per_launch": af, "avg_launch_ms": attn_ms},
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(h, budget_s=args.cpu_budget)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return res
+
+
+# kernels launched per step: 3 compress, indexer scores + top-k, attention
+LAUNCHES_PER_STEP = 6
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores
+# --------------------------------------------------------------------------
+def oracle_sample(h, rows, rope):
+    """One bounded oracle step: compression of all tokens, then top-k and
+    attention for the given query rows.  Returns (compress s, rows s)."""
+    import oracle
+    t0 = time.perf_counter()
+    x = wl.bf16_bits_to_f32(h["kv"])
+    cache = oracle.compress_kv(x, h["z"], h["s"], CFG.m, "mixed592", CFG.R, 0, rope)
+    swa = oracle.compress_kv(x, h["z"], None, 1, "mixed592", CFG.R, 0, rope)
+    keys = oracle.compress_kv(wl.bf16_bits_to_f32(h["kI"]), h["zI"], h["sI"], CFG.m, "mxfp4", 0)
+    t1 = time.perf_counter()
+    idx, _ = oracle.indexer_topk(wl.bf16_bits_to_f32(h["qI"])[:, rows], h["w"][:, rows], keys,
+                                 h["q_pos"][:, rows], CFG.N, CFG.m, CFG.k)
+    oracle.attention(wl.bf16_bits_to_f32(h["q"])[:, rows], h["q_pos"][:, rows], cache, CFG.N, CFG.m,
+                     idx, swa, h["swa_pos0"], CFG.W, 1.0 / math.sqrt(CFG.D), rope, CFG.R)
+    return t1 - t0, time.perf_counter() - t1
+
+
+def _full_step_seconds(t_comp, t_rows, n_rows):
+    """Estimated oracle time of a whole 8192-token step from a sampled one."""
+    return t_comp + t_rows * CFG.T / n_rows
+
+
+def cpu_baseline(h, budget_s=20.0):
+    """Time the oracle on a bounded sample: compression of all tokens, then
+    top-k and attention for a seeded set of query rows; scaled to tokens/s."""
+    import oracle
+    oracle.build()
+    oracle.set_threads(os.cpu_count() or 1)
+    rope = oracle.rope_table(CFG.T + 1, CFG.R)
+    rng = np.random.default_rng(123)
+    n_rows = 16
+    rows = np.sort(rng.choice(CFG.T, n_rows, replace=False))
+    tc, tr = oracle_sample(h, rows, rope)
+    if tc + tr < budget_s / 4:
+        n_rows = int(min(CFG.T, n_rows * max(1.0, (budget_s / 2 - tc) / max(tr, 1e-3))))
+        rows = np.sort(rng.choice(CFG.T, n_rows, replace=False))
+        tc, tr = oracle_sample(h, rows, rope)
+    full = _full_step_seconds(tc, tr, n_rows)
+    return {"value": CFG.T / full, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": f"compression of all {CFG.T} tokens ({tc:.2f} s) + top-k and sparse MQA for "
+                      f"{n_rows} seeded query rows ({tr:.2f} s); rows scaled to {CFG.T}"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    h = host_inputs(seed=0)
+    import oracle
+    oracle.build()
+    oracle.set_threads(os.cpu_count() or 1)
+    rope = oracle.rope_table(CFG.T + 1, CFG.R)
+    n_rows = 16
+    rng = np.random.default_rng(7)
+    fulls = []
+    for i in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(CFG.T, n_rows, replace=False))
+        tc, tr = oracle_sample(h, rows, rope)
+        if i >= args.warmup:
+            fulls.append(_full_step_seconds(tc, tr, n_rows))
+    ms = 1e3 * statistics.mean(fulls)
+    value = CFG.T / (ms * 1e-3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": CFG.name, "B": 1, "T": CFG.T, "m": CFG.m, "N": CFG.N, "k": CFG.k,
+                   "W": CFG.W, "H": CFG.H, "D": CFG.D, "HI": CFG.HI, "dI": CFG.dI},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
+                         "sample": f"per step: compression of all {CFG.T} tokens + top-k and sparse MQA "
+                                   f"for {n_rows} seeded query rows, row time scaled to {CFG.T} rows"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+/*
+ * csa_b300.h -- C ABI of the B300 (sm_103a) compressed-attention library
+ * libcsa_b300.so: DeepSeek-V4's hybrid attention, compressed sparse
+ * attention (CSA) and heavily compressed attention (HCA).
+ *
+ * Sources (page title, section) cited below:
+ *  [XM] xmsumi.com DeepSeek-V4 article: "CSA（压缩稀疏注意力）",
+ *       "HCA（重度压缩注意力）", "关键技术细节" (key technical details), and the
+ *       heterogeneous KV cache paragraph under "百万Token 长上下文真实表现".
+ *  [HU] "DeepSeek-V4 — MoE nyelvmodellek milliós kontextussal" (hortopato.cc
+ *       wiki): the CSA list (Tömörítés, Lightning Indexer, Sliding Window
+ *       figyelem) and "Heavily Compressed Attention (HCA)".
+ *  [ZC] zcldvi.com DeepSeek-V4 news article: FP4 indexer, lossless FP4->FP8,
+ *       the window branch in both attentions.
+ *
+ * Conventions shared by every call
+ *  - Return value: CSA_OK or a negative csa status.  CSA_ERR_INVALID_ARG and
+ *    CSA_ERR_UNSUPPORTED are returned before anything is enqueued; the text
+ *    of the last error of the calling thread is in csa_last_error().
+ *  - Device calls are asynchronous on `stream` (a cudaStream_t passed as
+ *    void*; NULL is the legacy default stream).  They never allocate, free or
+ *    synchronise.
+ *  - Every pointer marked (device) is a device pointer owned by the caller;
+ *    arrays are dense, row-major, in the shapes given, and must not overlap
+ *    the outputs.  Pointers marked (host) are host memory.
+ *  - Scratch: calls that need it take `ws` (device, at least the size given
+ *    by csa_workspace_size, 256-byte aligned) and its size `ws_bytes`.  The
+ *    first 16 bytes of ws are a status block of sticky device-check flags:
+ *    clear it with csa_status_reset once before first use, read it with
+ *    csa_status_read.  A kernel that meets an index it must not follow (an
+ *    entry >= N or not yet visible, a window row outside the window cache)
+ *    skips that key and sets CSA_FLAG_DEVICE_CHECK; a bounded wait that
+ *    expires sets CSA_FLAG_TIMEOUT.  Calls that overlap on the GPU must use
+ *    different workspaces.
+ *  - Formats: CSA_FMT_F32 rows are C fp32 channels.  CSA_FMT_MIXED592 rows
+ *    (C = 512, the last 64 channels RoPE) are 592 bytes: [0,448) E4M3 codes
+ *    of the 448 non-RoPE channels, each scaled by 2^-e_g of its 128-channel
+ *    group g (groups of 128,128,128,64); [448,576) the 64 RoPE channels as
+ *    bf16 (little endian, nearest-even); [576,592) four fp32 scales 2^e_g,
+ *    e_g the smallest integer with max|v| / 2^e_g <= 448 (>= -126; 0 for an
+ *    all-zero group).  [XM] key technical details: RoPE dims in BF16, the
+ *    rest in FP8.  CSA_FMT_MXFP4 (indexer keys, C a multiple of 32): C/2
+ *    bytes of E2M1 codes (even element in the low nibble) per row plus C/32
+ *    UE8M0 scale bytes per row in a separate array; scale exponent =
+ *    floor(log2 max|v|) - 2 over each block of 32 (OCP MX v1.0).
+ *  - RoPE: rope_cos / rope_sin (device, fp32 [rope_rows, R/2]) hold
+ *    cos/sin(p * base^(-2i/R)); pairs (2i, 2i+1) of the last R channels
+ *    rotate by angle p*theta_i.  Build them with csa_rope_table.
+ *    [XM] key technical details: RoPE acts on the last 64 dims of q and of
+ *    the KV entries, and the attention output gets the inverse rotation.
+ */
+#ifndef CSA_B300_H
+#define CSA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CSA_OK 0
+#define CSA_ERR_INVALID_ARG (-1)
+#define CSA_ERR_UNSUPPORTED (-2)
+#define CSA_ERR_CUDA (-3)
+#define CSA_ERR_DEVICE_CHECK (-4)
+#define CSA_ERR_TIMEOUT (-5)
+
+#define CSA_FLAG_DEVICE_CHECK 1u
+#define CSA_FLAG_TIMEOUT 2u
+
+#define CSA_DTYPE_F32 0
+#define CSA_DTYPE_BF16 1
+
+#define CSA_FMT_F32 0
+#define CSA_FMT_MIXED592 1
+#define CSA_FMT_MXFP4 2
+
+#define CSA_OP_INDEXER_TOPK 1
+#define CSA_OP_SPARSE_MQA 2
+#define CSA_OP_HCA_DENSE 3
+
+/* Text of the last error returned on the calling thread ("" if none). */
+const char *csa_last_error(void);
+
+/* Library version string. */
+const char *csa_version(void);
+
+/*
+ * csa_rope_table (host): fill cos_out / sin_out (host, fp32 [P, R/2]) with
+ * the nearest fp32 of cos / sin(p * base^(-2i/R)), evaluated in fp64.
+ * [XM] key technical details (RoPE on the last 64 dims).
+ * Errors: INVALID_ARG for P < 1, odd or non-positive R, NULL pointers.
+ */
+int csa_rope_table(int64_t P, int R, double base, float *cos_out, float *sin_out);
+
+/*
+ * csa_workspace_size: bytes of `ws` that `op` (CSA_OP_*) needs for B
+ * sequences of Tq queries, N entries per sequence, top-k k (CSA) and the
+ * largest key count per query max_keys (attention: k + W for CSA, entries +
+ * W for HCA).  Never less than 256 (the status block).  Returns -1 for an
+ * unknown op.
+ */
+int64_t csa_workspace_size(int op, int B, int64_t Tq, int64_t N, int k, int H, int D,
+                           int64_t max_keys);
+
+/* Clear the status block of ws (async on stream). */
+int csa_status_reset(void *ws, void *stream);
+
+/* Copy the status flags of ws to *flags (host) and wait for stream. */
+int csa_status_read(const void *ws, void *stream, uint32_t *flags);
+
+/*
+ * kvcache_pack_fp8_bf16: pack n post-RoPE rows of 512 fp32 channels
+ * (v, device [n, 512]) into the mixed FP8/BF16 layout (out, device
+ * [n, 592] bytes, CSA_FMT_MIXED592 above).  [XM] key technical details
+ * (KV cache in mixed precision).  Used for the window ("state") cache and
+ * standalone packing; csa_compress_kv packs its own output.
+ * Errors: INVALID_ARG for n < 0 or NULL pointers with n > 0.
+ */
+int kvcache_pack_fp8_bf16(const float *v, int64_t n, uint8_t *out, void *stream);
+
+/*
+ * csa_compress_kv: block compression of KV (or of indexer keys) into
+ * compressed entries, with RoPE and storage packing fused.
+ * [XM] CSA: the KV entries of every m tokens are fused into one compressed
+ * entry by a weighted sum; [HU] Tömörítés (m = 4); [XM]/[HU] HCA: m' = 128.
+ *  x         (device) [B, T, C] activations, x_dtype CSA_DTYPE_BF16 or _F32
+ *  z         (device) fp32 [B, T] compression logits, one per token
+ *  s         (device) fp32 [C] per-channel scale, or NULL for all ones
+ *  rope_cos/sin, rope_rows: RoPE tables (needed when R > 0)
+ *  pos0      absolute position of x's first token; a multiple of m
+ *  R         RoPE channels (the last R of C); 0 for indexer keys
+ *  m         block size (1..128); N = floor(T / m) entries are written
+ *  out_fmt   CSA_FMT_F32 (out fp32 [B, N, C]), CSA_FMT_MIXED592 (C = 512,
+ *            R = 64; out [B, N, 592] bytes) or CSA_FMT_MXFP4 (R = 0, C a
+ *            multiple of 32, at most 64; out [B, N, C/2] codes and
+ *            out_scales [B, N, C/32] bytes)
+ * Entry j (of this call) covers tokens [jm, jm + m); its weights are
+ * a = softmax(z over the block), computed as mu = max z, e_i = sexp(z_i -
+ * mu) (the library's fp32 exponential), S = e_0 + ... + e_{m-1} in order,
+ * a_i = e_i / S; channel c is (sum_i fma order) a_i x_{i,c}, times s_c; the
+ * last R channels then rotate at position pos0 + jm + m - 1, the block's
+ * last token.  With m = 1 and s = NULL this stores the tokens themselves
+ * (the sliding-window cache).
+ * Errors: INVALID_ARG (NULL pointers, bad dtype/format, pos0 % m != 0,
+ * RoPE rows not covering the last position); UNSUPPORTED (m > 128, format
+ * and C/R combinations not listed).
+ */
+int csa_compress_kv(const void *x, int x_dtype, const float *z, const float *s,
+                    const float *rope_cos, const float *rope_sin, int64_t rope_rows,
+                    int64_t pos0, int B, int64_t T, int C, int R, int m, int out_fmt, void *out,
+                    uint8_t *out_scales, void *stream);
+
+/*
+ * csa_indexer_topk: lightning-indexer scores of every visible compressed
+ * entry for every query, and the top-k of them.
+ * [XM] CSA: the lightning indexer picks the top-k compressed entries per
+ * query token; [HU] Lightning Indexer (k = 1024); [XM] key technical details:
+ * the indexer's attention runs in FP4.
+ *  qI        (device) [B, Tq, HI, dI] indexer queries: CSA_DTYPE_BF16 with
+ *            kI_fmt CSA_FMT_MXFP4 (quantised to MXFP4 per 32-block inside),
+ *            or CSA_DTYPE_F32 with kI_fmt CSA_FMT_F32
+ *  w         (device) fp32 [B, Tq, HI] head weights
+ *  kI        (device) keys: MXFP4 codes [B, N, dI/2] with kI_scales
+ *            [B, N, dI/32], or fp32 [B, N, dI] (kI_scales NULL)
+ *  q_pos     (device) int64 [B, Tq] absolute position t of each query
+ *  N, m      entries per sequence and their block size
+ *  k         entries to keep (1..4096)
+ *  idx_out   (device) int32 [B, Tq, k]: entry indices, best first, -1 pad
+ *  score_out (device) fp32 [B, Tq, k] or NULL: their scores (-inf pad)
+ * score(t, j) = sum over heads h, ascending, of s = fma(w_h, relu(d_h), s)
+ * from +0; d_h is the exact dot of the dequantised MXFP4 vectors rounded
+ * once to fp32 (FP4) or the fma chain over dI from +0 (fp32).  Candidates:
+ * j < N with (j + 1) m - 1 <= t.  Order: score descending, then index
+ * ascending.
+ * Errors: INVALID_ARG, UNSUPPORTED (dI not 32/64, HI > 64, k > 4096),
+ * CUDA; needs csa_workspace_size(CSA_OP_INDEXER_TOPK, ...) bytes of ws.
+ */
+int csa_indexer_topk(const void *qI, int qI_dtype, const float *w, const void *kI,
+                     const uint8_t *kI_scales, int kI_fmt, const int64_t *q_pos, int B,
+                     int64_t Tq, int HI, int dI, int64_t N, int m, int k, int32_t *idx_out,
+                     float *score_out, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * csa_sparse_mqa: multi-query attention of every query over its selected
+ * compressed entries and its sliding window, in one softmax.
+ * [XM] CSA: attention runs only over the selected entries, with a sliding
+ * window branch for the nearest tokens; [HU] Sliding Window figyelem (128);
+ * [ZC] both attentions carry the window branch; [XM] key technical details:
+ * partial RoPE and inverse rotation of the output.
+ *  q         (device) [B, Tq, H, D] queries before RoPE (q_dtype BF16 with
+ *            cache_fmt MIXED592, D = 512, R = 64; or F32 with cache_fmt F32)
+ *  q_pos     (device) int64 [B, Tq] absolute positions t
+ *  cache     (device) [B, N, row] compressed entries (cache_fmt rows)
+ *  idx       (device) int32 [B, Tq, k] selected entries (-1 = none)
+ *  swa       (device) [B, Ts, row] window cache: token u of sequence b is
+ *            row u - swa_pos0[b]; swa_pos0 (device) int64 [B]
+ *  W         window: tokens t - W < u <= t, u >= 0
+ *  softmax_scale  multiplies q.k
+ *  out       (device) [B, Tq, H, D], same dtype as q
+ *  lse       (device) fp32 [B, Tq, H] natural-log sum-exp, or NULL
+ * All H heads share one KV; the value of a key is its entry (V = K).
+ * Logits = scale * RoPE_t(q_h) . kappa over the union of the selected
+ * entries and the window (an entry that also lies in the window is not
+ * removed), one softmax, o_h = sum p kappa, then the last R channels of o_h
+ * rotate by -t.  No keys: o = 0, lse = -inf.
+ * Errors: INVALID_ARG, UNSUPPORTED (shapes other than listed, k + W >
+ * 8192), CUDA; device check flag for indices >= N, not yet visible, or
+ * window rows outside swa.
+ */
+int csa_sparse_mqa(const void *q, int q_dtype, const int64_t *q_pos, int B, int64_t Tq, int H,
+                   int D, int R, int cache_fmt, const void *cache, int64_t N, int m,
+                   const int32_t *idx, int k, const void *swa, const int64_t *swa_pos0,
+                   int64_t Ts, int W, float softmax_scale, const float *rope_cos,
+                   const float *rope_sin, int64_t rope_rows, void *out, float *lse, void *ws,
+                   size_t ws_bytes, void *stream);
+
+/*
+ * hca_dense_attn: as csa_sparse_mqa, with every visible entry
+ * (j < min(N, floor((t + 1) / m))) in place of the selected ones.
+ * [XM] HCA: a larger compression ratio m' and dense attention over all
+ * compressed entries, no selection; [HU] Heavily Compressed Attention
+ * (m' = 128).
+ * Errors: as csa_sparse_mqa (UNSUPPORTED when visible entries + W > 16384).
+ */
+int hca_dense_attn(const void *q, int q_dtype, const int64_t *q_pos, int B, int64_t Tq, int H,
+                   int D, int R, int cache_fmt, const void *cache, int64_t N, int m,
+                   const void *swa, const int64_t *swa_pos0, int64_t Ts, int W,
+                   float softmax_scale, const float *rope_cos, const float *rope_sin,
+                   int64_t rope_rows, void *out, float *lse, void *ws, size_t ws_bytes,
+                   void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_B300_H */

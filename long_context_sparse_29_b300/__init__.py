@@ -1,0 +1,229 @@
+"""B300 (sm_103a) compressed attention: DeepSeek-V4's CSA and HCA.
+
+Thin Python binding over the C ABI of libcsa_b300.so (include/csa_b300.h):
+argument marshalling only.  Every step of the computation runs in the
+library's CUDA kernels; torch provides device memory and streams.
+
+Calls (same names as the C ABI):
+  compress_kv            block compression + RoPE + packing of KV / indexer keys
+  kvcache_pack_fp8_bf16  standalone mixed FP8/BF16 row packing
+  indexer_topk           lightning-indexer scores and top-k entry selection
+  sparse_mqa             CSA: MQA over selected entries + sliding window
+  hca_dense_attn         HCA: MQA over all visible entries + sliding window
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from ._lib import CsaError, check, lib
+
+__all__ = ["CsaError", "Workspace", "rope_table", "compress_kv", "kvcache_pack_fp8_bf16",
+           "indexer_topk", "sparse_mqa", "hca_dense_attn", "workspace_size",
+           "DTYPE_F32", "DTYPE_BF16", "FMT_F32", "FMT_MIXED592", "FMT_MXFP4"]
+
+DTYPE_F32, DTYPE_BF16 = 0, 1
+FMT_F32, FMT_MIXED592, FMT_MXFP4 = 0, 1, 2
+OP_INDEXER_TOPK, OP_SPARSE_MQA, OP_HCA_DENSE = 1, 2, 3
+FLAG_DEVICE_CHECK, FLAG_TIMEOUT = 1, 2
+MIXED_ROW = 592
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _dt(t):
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def workspace_size(op: int, B: int, Tq: int, N: int, k: int, H: int, D: int, max_keys: int) -> int:
+    return int(lib().csa_workspace_size(op, B, Tq, N, k, H, D, max_keys))
+
+
+class Workspace:
+    """Device scratch for the library calls (first 16 bytes: status flags).
+
+    Grows on demand; `flags()` reads the sticky device-check / timeout flags.
+    """
+
+    def __init__(self, device=None, nbytes: int = 1 << 20):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+        self._alloc(nbytes)
+
+    def _alloc(self, nbytes):
+        self.buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
+        check(lib().csa_status_reset(_ptr(self.buf), _stream(self.device)))
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf.numel() < nbytes:
+            self._alloc(nbytes + (nbytes >> 3))
+        return self.buf
+
+    def reset(self):
+        check(lib().csa_status_reset(_ptr(self.buf), _stream(self.device)))
+
+    def flags(self) -> int:
+        f = ctypes.c_uint32(0)
+        code = lib().csa_status_read(_ptr(self.buf), _stream(self.device), ctypes.byref(f))
+        if code not in (0, -4, -5):
+            check(code)
+        return int(f.value)
+
+
+_default_ws: dict = {}
+
+
+def _ws(ws, device):
+    if ws is not None:
+        return ws
+    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(torch.device("cuda", key))
+    return _default_ws[key]
+
+
+def rope_table(P: int, R: int = 64, base: float = 10000.0, device="cuda"):
+    """cos/sin tables fp32 [P, R/2] on `device` (built on the host by the library)."""
+    c = np.empty((P, R // 2), np.float32)
+    s = np.empty((P, R // 2), np.float32)
+    check(lib().csa_rope_table(P, R, float(base), c.ctypes.data_as(ctypes.c_void_p),
+                               s.ctypes.data_as(ctypes.c_void_p)))
+    return torch.from_numpy(c).to(device), torch.from_numpy(s).to(device)
+
+
+def compress_kv(x, z, s, m: int, out_fmt: int, R: int = 0, rope=None, pos0: int = 0, out=None,
+                out_scales=None):
+    """Compress x [B, T, C] (bf16 or fp32) in blocks of m; see csa_compress_kv.
+
+    Returns fp32 [B, N, C] (FMT_F32), uint8 [B, N, 592] (FMT_MIXED592) or
+    (codes uint8 [B, N, C/2], scales uint8 [B, N, C/32]) (FMT_MXFP4).
+    """
+    _need(x, "x")
+    B, T, C = x.shape
+    _need(z, "z", torch.float32)
+    if s is not None:
+        _need(s, "s", torch.float32)
+    N = T // m
+    dev = x.device
+    if out is None:
+        if out_fmt == FMT_F32:
+            out = torch.empty((B, N, C), dtype=torch.float32, device=dev)
+        elif out_fmt == FMT_MIXED592:
+            out = torch.empty((B, N, MIXED_ROW), dtype=torch.uint8, device=dev)
+        else:
+            out = torch.empty((B, N, C // 2), dtype=torch.uint8, device=dev)
+            out_scales = torch.empty((B, N, C // 32), dtype=torch.uint8, device=dev)
+    rc, rs = (rope if rope is not None else (None, None))
+    rows = rc.shape[0] if rc is not None else 0
+    check(lib().csa_compress_kv(_ptr(x), _dt(x), _ptr(z), _ptr(s), _ptr(rc), _ptr(rs), rows, pos0,
+                                B, T, C, R, m, out_fmt, _ptr(out), _ptr(out_scales), _stream(dev)))
+    return (out, out_scales) if out_fmt == FMT_MXFP4 else out
+
+
+def kvcache_pack_fp8_bf16(v, out=None):
+    """Pack post-RoPE rows v fp32 [..., 512] into uint8 [..., 592]."""
+    _need(v, "v", torch.float32)
+    lead = v.shape[:-1]
+    n = int(np.prod(lead)) if len(lead) else 1
+    if out is None:
+        out = torch.empty(tuple(lead) + (MIXED_ROW,), dtype=torch.uint8, device=v.device)
+    check(lib().kvcache_pack_fp8_bf16(_ptr(v), n, _ptr(out), _stream(v.device)))
+    return out
+
+
+def indexer_topk(qI, w, kI, kI_scales, q_pos, N: int, m: int, k: int, scores: bool = True,
+                 idx_out=None, score_out=None, ws: Workspace | None = None):
+    """Top-k entries per query.  qI [B, Tq, HI, dI] bf16 (MXFP4 keys) or fp32 (fp32 keys)."""
+    _need(qI, "qI")
+    _need(w, "w", torch.float32)
+    _need(q_pos, "q_pos", torch.int64)
+    _need(kI, "kI")
+    B, Tq, HI, dI = qI.shape
+    fmt = FMT_MXFP4 if kI_scales is not None else FMT_F32
+    dev = qI.device
+    if idx_out is None:
+        idx_out = torch.empty((B, Tq, k), dtype=torch.int32, device=dev)
+    if scores and score_out is None:
+        score_out = torch.empty((B, Tq, k), dtype=torch.float32, device=dev)
+    ws = _ws(ws, dev)
+    need = workspace_size(OP_INDEXER_TOPK, B, Tq, N, k, 0, 0, 0)
+    buf = ws.get(need)
+    check(lib().csa_indexer_topk(_ptr(qI), _dt(qI), _ptr(w), _ptr(kI), _ptr(kI_scales), fmt,
+                                 _ptr(q_pos), B, Tq, HI, dI, N, m, k, _ptr(idx_out),
+                                 _ptr(score_out if scores else None), _ptr(buf), buf.numel(),
+                                 _stream(dev)))
+    return (idx_out, score_out) if scores else idx_out
+
+
+def _attn(q, q_pos, cache, N, m, idx, swa, swa_pos0, W, scale, rope, R, want_lse, out, ws):
+    _need(q, "q")
+    _need(q_pos, "q_pos", torch.int64)
+    B, Tq, H, D = q.shape
+    fmt = FMT_MIXED592 if q.dtype == torch.bfloat16 else FMT_F32
+    dev = q.device
+    if swa is not None:
+        _need(swa, "swa")
+        _need(swa_pos0, "swa_pos0", torch.int64)
+    Ts = swa.shape[1] if swa is not None else 0
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((B, Tq, H), dtype=torch.float32, device=dev) if want_lse else None
+    rc, rs = rope
+    ws = _ws(ws, dev)
+    k = idx.shape[-1] if idx is not None else 0
+    max_keys = (k if idx is not None else N) + W
+    op = OP_SPARSE_MQA if idx is not None else OP_HCA_DENSE
+    buf = ws.get(workspace_size(op, B, Tq, N, k, H, D, max_keys))
+    st = _stream(dev)
+    if idx is not None:
+        _need(idx, "idx", torch.int32)
+        check(lib().csa_sparse_mqa(_ptr(q), _dt(q), _ptr(q_pos), B, Tq, H, D, R, fmt, _ptr(cache), N,
+                                   m, _ptr(idx), k, _ptr(swa), _ptr(swa_pos0), Ts, W, float(scale),
+                                   _ptr(rc), _ptr(rs), rc.shape[0], _ptr(out), _ptr(lse), _ptr(buf),
+                                   buf.numel(), st))
+    else:
+        check(lib().hca_dense_attn(_ptr(q), _dt(q), _ptr(q_pos), B, Tq, H, D, R, fmt, _ptr(cache), N,
+                                   m, _ptr(swa), _ptr(swa_pos0), Ts, W, float(scale), _ptr(rc),
+                                   _ptr(rs), rc.shape[0], _ptr(out), _ptr(lse), _ptr(buf),
+                                   buf.numel(), st))
+    return (out, lse) if want_lse else out
+
+
+def sparse_mqa(q, q_pos, cache, m: int, idx, swa, swa_pos0, W: int, scale: float, rope,
+               R: int = 64, lse: bool = False, out=None, ws: Workspace | None = None):
+    """CSA: attention of q [B, Tq, H, D] over the idx-selected entries of cache
+    [B, N, row] (block size m) and the window rows of swa; see csa_sparse_mqa."""
+    return _attn(q, q_pos, cache, cache.shape[1], m, idx, swa, swa_pos0, W, scale, rope, R, lse,
+                 out, ws)
+
+
+def hca_dense_attn(q, q_pos, cache, m: int, swa, swa_pos0, W: int, scale: float, rope,
+                   R: int = 64, lse: bool = False, out=None, ws: Workspace | None = None):
+    """HCA: attention of q over every visible entry of cache [B, N, row] (block size m)
+    and the window rows of swa; see hca_dense_attn."""
+    return _attn(q, q_pos, cache, cache.shape[1], m, None, swa, swa_pos0, W, scale, rope, R, lse,
+                 out, ws)

@@ -1,0 +1,365 @@
+// indexer.cu -- lightning-indexer scores and top-k selection.
+//
+// xmsumi.com DeepSeek-V4 article, section "CSA（压缩稀疏注意力）": a light
+// lightning indexer picks the top-k compressed entries for each query token;
+// section "关键技术细节": the indexer's attention runs in FP4.
+// "DeepSeek-V4 — MoE nyelvmodellek milliós kontextussal", CSA list item
+// "Lightning Indexer" (k = 1024 in V4-Pro).
+//
+// score(t, j) = sum_h w_{t,h} relu(q_{t,h} . k_j) with the head sum as an fma
+// chain from +0 in ascending h.  In the FP4 path q and k are MXFP4 (E2M1
+// elements, power-of-two scales per 32-block): every E2M1 value times 2 is a
+// small integer, so each 32-block dot is an exact integer (dp4a on int8) and
+// the head dot is the exact sum of the two scaled block dots rounded once
+// (both terms are exact fp32 values, so one IEEE add gives the nearest fp32
+// of the exact sum).  The fp32 path runs the fma chain over the head dim.
+//
+// Selection: per query, radix select on order-preserving 32-bit keys of the
+// scores (4 passes of 8 bits) finds the k-th largest value; every larger key
+// is taken and ties at the threshold are taken in ascending index order; the
+// chosen (score, index) pairs are then bitonic-sorted by score descending,
+// index ascending.
+#include "csa_common.cuh"
+#include "launch.h"
+
+namespace csa {
+
+constexpr int kScoreThreads = 256;   // entries per CTA
+constexpr int kScoreQT = 16;         // queries per CTA
+constexpr int kMaxHI = 32;
+
+__device__ __forceinline__ int64_t visible_entries(int64_t t, int m, int64_t N) {
+  int64_t nv = (t + 1) / m;
+  nv = nv < 0 ? 0 : nv;
+  return nv < N ? nv : N;
+}
+
+// E2M1 code -> 2 * value as a signed int8 (exact)
+__device__ __forceinline__ int e2m1_x2(uint32_t c) {
+  const int mag = (c & 7) < 4 ? (int)(c & 7) : (c & 7) == 4 ? 4 : (c & 7) == 5 ? 6 : (c & 7) == 6 ? 8 : 12;
+  return (c & 8) ? -mag : mag;
+}
+
+// d = P0 * 2^e0 + P1 * 2^e1, one rounding (the block dots are exact integers)
+__device__ __forceinline__ float combine_blocks(int P0, int e0, int P1, int e1) {
+  return __fadd_rn(scale_pow2((float)P0, e0), scale_pow2((float)P1, e1));
+}
+
+// ---------------------------------------------------------------------------
+// FP4 scores: grid (entry chunks, query tiles, B); one thread per entry.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScoreThreads)
+scores_fp4_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
+                  const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
+                  const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
+                  float* __restrict__ scores) {
+  // int8 (2 * E2M1) query values, 64 per head; block exponents; weights
+  __shared__ __align__(16) int32_t qv_s[kScoreQT][kMaxHI][16];
+  __shared__ int8_t qe_s[kScoreQT][kMaxHI][2];
+  __shared__ float w_s[kScoreQT][kMaxHI];
+  __shared__ int64_t nv_s[kScoreQT];
+  const int b = blockIdx.z;
+  const int64_t q0 = (int64_t)blockIdx.y * kScoreQT;
+  const int nq = (int)(Tq - q0 < kScoreQT ? Tq - q0 : kScoreQT);
+  const int64_t j0 = (int64_t)blockIdx.x * kScoreThreads;
+  const int tid = threadIdx.x;
+
+  if (tid < kScoreQT) nv_s[tid] = tid < nq ? visible_entries(q_pos[b * Tq + q0 + tid], m, N) : 0;
+  __syncthreads();
+  int64_t nv_max = 0;
+  for (int q = 0; q < nq; ++q) nv_max = nv_max > nv_s[q] ? nv_max : nv_s[q];
+  if (j0 >= nv_max) return;   // no query of the tile sees this chunk
+
+  // quantise the tile's queries: one (query, head, block) of 32 elements per step
+  for (int u = tid; u < nq * HI * 2; u += kScoreThreads) {
+    const int q = u / (HI * 2), h = (u / 2) % HI, blk = u & 1;
+    const __nv_bfloat16* src = qI + (((b * Tq + q0 + q) * HI + h) * 64 + 32 * blk);
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] = __bfloat162float(src[i]);
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const int sx = mx_block_exp(amax);
+    const float inv = pow2i(-sx);
+#pragma unroll
+    for (int wd = 0; wd < 8; ++wd) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int val = e2m1_x2(e2m1_encode(__fmul_rn(v[4 * wd + e], inv)));
+        word |= ((uint32_t)(val & 0xff)) << (8 * e);
+      }
+      qv_s[q][h][8 * blk + wd] = (int32_t)word;
+    }
+    qe_s[q][h][blk] = (int8_t)sx;
+  }
+  for (int u = tid; u < nq * HI; u += kScoreThreads)
+    w_s[u / HI][u % HI] = w[(b * Tq + q0) * HI + u];
+  __syncthreads();
+
+  const int64_t j = j0 + tid;
+  if (j >= nv_max) return;
+  // the key: 64 E2M1 codes -> 16 words of 4 int8, and its two block exponents
+  int32_t kv[16];
+  const uint4* kc4 = reinterpret_cast<const uint4*>(kc + (b * N + j) * 32);
+  const uint4 c_lo = kc4[0], c_hi = kc4[1];
+  const uint32_t cw[8] = {c_lo.x, c_lo.y, c_lo.z, c_lo.w, c_hi.x, c_hi.y, c_hi.z, c_hi.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      lo |= ((uint32_t)(e2m1_x2((cw[i] >> (4 * e)) & 15) & 0xff)) << (8 * e);
+      hi |= ((uint32_t)(e2m1_x2((cw[i] >> (16 + 4 * e)) & 15) & 0xff)) << (8 * e);
+    }
+    kv[2 * i] = (int32_t)lo;
+    kv[2 * i + 1] = (int32_t)hi;
+  }
+  const int ke0 = (int)ks[(b * N + j) * 2] - 127, ke1 = (int)ks[(b * N + j) * 2 + 1] - 127;
+
+  for (int q = 0; q < nq; ++q) {
+    if (j >= nv_s[q]) continue;
+    float s = 0.0f;
+    for (int h = 0; h < HI; ++h) {
+      const int4* qv4 = reinterpret_cast<const int4*>(qv_s[q][h]);
+      int P0 = 0, P1 = 0;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int4 a = qv4[i];
+        P0 = __dp4a(kv[4 * i + 0], a.x, P0);
+        P0 = __dp4a(kv[4 * i + 1], a.y, P0);
+        P0 = __dp4a(kv[4 * i + 2], a.z, P0);
+        P0 = __dp4a(kv[4 * i + 3], a.w, P0);
+      }
+#pragma unroll
+      for (int i = 2; i < 4; ++i) {
+        const int4 a = qv4[i];
+        P1 = __dp4a(kv[4 * i + 0], a.x, P1);
+        P1 = __dp4a(kv[4 * i + 1], a.y, P1);
+        P1 = __dp4a(kv[4 * i + 2], a.z, P1);
+        P1 = __dp4a(kv[4 * i + 3], a.w, P1);
+      }
+      const float d = combine_blocks(P0, qe_s[q][h][0] + ke0 - 2, P1, qe_s[q][h][1] + ke1 - 2);
+      const float r = d > 0.0f ? d : 0.0f;
+      s = __fmaf_rn(w_s[q][h], r, s);
+    }
+    scores[(b * Tq + q0 + q) * N + j] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fp32 scores (dI <= 64): fma chain over the head dim.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScoreThreads)
+scores_f32_kernel(const float* __restrict__ qI, const float* __restrict__ w,
+                  const float* __restrict__ kI, const int64_t* __restrict__ q_pos, int64_t Tq,
+                  int HI, int dI, int64_t N, int m, float* __restrict__ scores) {
+  __shared__ float q_s[kScoreQT][512];   // HI * dI <= 512
+  __shared__ float w_s[kScoreQT][kMaxHI];
+  __shared__ int64_t nv_s[kScoreQT];
+  const int b = blockIdx.z;
+  const int64_t q0 = (int64_t)blockIdx.y * kScoreQT;
+  const int nq = (int)(Tq - q0 < kScoreQT ? Tq - q0 : kScoreQT);
+  const int64_t j0 = (int64_t)blockIdx.x * kScoreThreads;
+  const int tid = threadIdx.x;
+  if (tid < kScoreQT) nv_s[tid] = tid < nq ? visible_entries(q_pos[b * Tq + q0 + tid], m, N) : 0;
+  for (int u = tid; u < nq * HI * dI; u += kScoreThreads)
+    q_s[u / (HI * dI)][u % (HI * dI)] = qI[(b * Tq + q0) * HI * dI + u];
+  for (int u = tid; u < nq * HI; u += kScoreThreads) w_s[u / HI][u % HI] = w[(b * Tq + q0) * HI + u];
+  __syncthreads();
+  const int64_t j = j0 + tid;
+  float kv[64];
+  const float* kr = kI + (b * N + (j < N - 1 ? j : N - 1)) * dI;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) kv[i] = i < dI ? kr[i] : 0.0f;
+  for (int q = 0; q < nq; ++q) {
+    if (j >= nv_s[q]) continue;
+    float s = 0.0f;
+    for (int h = 0; h < HI; ++h) {
+      float d = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        if (i < dI) d = __fmaf_rn(q_s[q][h * dI + i], kv[i], d);
+      const float r = d > 0.0f ? d : 0.0f;
+      s = __fmaf_rn(w_s[q][h], r, s);
+    }
+    scores[(b * Tq + q0 + q) * N + j] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// top-k: one CTA per query row
+// ---------------------------------------------------------------------------
+constexpr int kTopkThreads = 512;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;   // -0 ranks as +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float order_key_value(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+__global__ void __launch_bounds__(kTopkThreads)
+topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m,
+            int k, int kpad, int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
+  extern __shared__ unsigned long long keys_s[];   // kpad composite keys
+  __shared__ unsigned int hist[256];
+  __shared__ unsigned int warp_cnt[kTopkThreads / 32];
+  __shared__ unsigned int sh_prefix, sh_remaining, sh_slots;
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t nv = visible_entries(q_pos[row], m, N);
+  const int kk = (int)((int64_t)k < nv ? (int64_t)k : nv);
+  const float* sr = scores + row * N;
+
+  for (int i = tid; i < kpad; i += kTopkThreads) keys_s[i] = 0ull;
+  if (tid == 0) {
+    sh_prefix = 0;
+    sh_remaining = (unsigned)kk;
+    sh_slots = 0;
+  }
+  __syncthreads();
+
+  if (kk > 0) {
+    uint32_t mask = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+      __syncthreads();
+      const uint32_t prefix = sh_prefix;
+      for (int64_t jj = tid; jj < nv; jj += kTopkThreads) {
+        const uint32_t u = order_key(sr[jj]);
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane L holds bins 255-8L .. 248-8L (descending); find the digit where
+        // the count of larger keys first reaches `remaining`
+        const unsigned int rem = sh_remaining;
+        unsigned int c[8], tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = hist[255 - 8 * lane - i];
+          tot += c[i];
+        }
+        unsigned int incl = tot;   // inclusive prefix over lanes 0..L
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const unsigned int excl = incl - tot;
+        const bool here = excl < rem && incl >= rem;
+        const unsigned int who = __ballot_sync(0xffffffffu, here);
+        if (lane == __ffs(who) - 1) {
+          unsigned int acc = excl;
+          int d = 255 - 8 * lane;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (acc + c[i] >= rem) { d = 255 - 8 * lane - i; break; }
+            acc += c[i];
+          }
+          sh_remaining = rem - acc;
+          sh_prefix = prefix | ((uint32_t)d << shift);
+        }
+      }
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+    // collect: all keys above the threshold, and the first `remaining` equal ones by index
+    const uint32_t thr = sh_prefix;
+    const unsigned int need_eq = sh_remaining;
+    unsigned int taken_eq = 0;
+    for (int64_t base = 0; base < nv; base += kTopkThreads) {
+      const int64_t jj = base + tid;
+      const uint32_t u = jj < nv ? order_key(sr[jj]) : 0u;
+      const bool gt = jj < nv && u > thr;
+      const bool eq = jj < nv && u == thr;
+      const unsigned int bal = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) warp_cnt[warp] = __popc(bal);
+      __syncthreads();
+      unsigned int before = taken_eq;
+      for (int w2 = 0; w2 < warp; ++w2) before += warp_cnt[w2];
+      before += __popc(bal & ((1u << lane) - 1u));
+      if (gt || (eq && before < need_eq)) {
+        const unsigned int slot = atomicAdd(&sh_slots, 1u);
+        keys_s[slot] = ((unsigned long long)u << 32) | (unsigned long long)(0xffffffffu - (uint32_t)jj);
+      }
+      unsigned int blk = 0;
+      for (int w2 = 0; w2 < kTopkThreads / 32; ++w2) blk += warp_cnt[w2];
+      taken_eq += blk;
+      __syncthreads();
+    }
+    // bitonic sort, descending
+    for (int size = 2; size <= kpad; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < kpad; i += kTopkThreads) {
+          const int p = i ^ stride;
+          if (p > i) {
+            const bool desc = (i & size) == 0;
+            const unsigned long long a = keys_s[i], c = keys_s[p];
+            if ((a < c) == desc) {
+              keys_s[i] = c;
+              keys_s[p] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
+  for (int r = tid; r < k; r += kTopkThreads) {
+    int32_t j = -1;
+    float sc = -INFINITY;
+    if (r < kk) {
+      const unsigned long long key = keys_s[r];
+      j = (int32_t)(0xffffffffu - (uint32_t)(key & 0xffffffffull));
+      sc = order_key_value((uint32_t)(key >> 32));
+    }
+    idx_out[row * k + r] = j;
+    if (score_out) score_out[row * k + r] = sc;
+  }
+}
+
+int topk_pad(int k) {
+  int p = 1;
+  while (p < k) p <<= 1;
+  return p < 2 ? 2 : p;
+}
+
+cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
+                                const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
+                                int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
+                                float* score_out, float* scores_ws, cudaStream_t st) {
+  if ((int64_t)B * Tq == 0) return cudaSuccess;
+  if (N > 0) {
+    const dim3 grid((unsigned)((N + kScoreThreads - 1) / kScoreThreads),
+                    (unsigned)((Tq + kScoreQT - 1) / kScoreQT), (unsigned)B);
+    if (fp4)
+      scores_fp4_kernel<<<grid, kScoreThreads, 0, st>>>(
+          reinterpret_cast<const __nv_bfloat16*>(qI), w, reinterpret_cast<const uint8_t*>(kI),
+          kI_scales, q_pos, Tq, HI, N, m, scores_ws);
+    else
+      scores_f32_kernel<<<grid, kScoreThreads, 0, st>>>(reinterpret_cast<const float*>(qI), w,
+                                                        reinterpret_cast<const float*>(kI), q_pos,
+                                                        Tq, HI, dI, N, m, scores_ws);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int kpad = topk_pad(k);
+  const size_t smem = sizeof(unsigned long long) * (size_t)kpad;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    attr_set = true;
+  }
+  topk_kernel<<<(unsigned)(B * Tq), kTopkThreads, smem, st>>>(scores_ws, q_pos, N, m, k, kpad,
+                                                             idx_out, score_out);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,51 @@
+// launch.h -- internal launchers of libcsa_b300 (not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace csa {
+
+struct AttnArgs {
+  const void* q;
+  bool q_bf16;
+  const int64_t* q_pos;
+  int B;
+  int64_t Tq;
+  int H, D, R;
+  int cache_fmt;
+  const void* cache;
+  int64_t N;
+  int m;
+  const int32_t* idx;   // NULL: dense (every visible entry)
+  int k;
+  const void* swa;
+  const int64_t* swa_pos0;
+  int64_t Ts;
+  int W;
+  float scale;
+  const float* rcos;
+  const float* rsin;
+  int64_t rope_rows;
+  void* out;
+  float* lse;
+  void* ws;             // status block at ws; scratch after kWsHeader
+  size_t ws_bytes;
+  int max_keys;         // upper bound of keys per query (list length)
+};
+
+constexpr size_t kWsHeader = 256;
+
+cudaError_t launch_compress(const void* x, bool x_bf16, const float* z, const float* s,
+                            const float* rcos, const float* rsin, int64_t pos0, int B, int64_t T,
+                            int C, int R, int m, int fmt, void* out, uint8_t* out_scales,
+                            cudaStream_t st);
+cudaError_t launch_pack_mixed(const float* v, int64_t n, uint8_t* out, cudaStream_t st);
+cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
+                                const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
+                                int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
+                                float* score_out, float* scores_ws, cudaStream_t st);
+cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st);
+size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys);
+
+}  // namespace csa

@@ -1,0 +1,344 @@
+"""GPU parity of every call against the CPU oracle, through the C ABI.
+
+Bar: bit-exact compressed cache bytes, FP4 key bytes, top-k indices and
+scores; attention outputs within max|err| <= 1e-2 max|ref| (bf16 out, fp32
+accumulation) or 1e-5 (fp32 configuration).  Full-size runs use the launch
+configuration of the benchmark and compare sampled query rows, which the
+oracle computes one by one from its own cache and its own top-k.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_common import act_dev, dev, max_rel_err, softmax_scale, tol, widen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csa():
+    from long_context_sparse_29_b300 import build
+    build.build()
+    import long_context_sparse_29_b300 as m
+    return m
+
+
+_ROPE = {}
+
+
+def ropes(csa, oracle_mod, P):
+    if P not in _ROPE:
+        _ROPE.clear()
+        _ROPE[P] = (oracle_mod.rope_table(P, 64), csa.rope_table(P, 64))
+    return _ROPE[P]
+
+
+# --------------------------------------------------------------------------
+# compression and packing: bit-exact bytes
+# --------------------------------------------------------------------------
+COMPRESS_CASES = [
+    # (config, sequence, tokens, m, pos0, part)
+    ("c2_csa_prefill_8k", 0, 8192, 4, 0, "kv"),          # CSA cache, full size
+    ("c2_csa_prefill_8k", 0, 8192 - 3, 4, 4096, "kv"),   # ragged tail, shifted positions
+    ("c2_csa_prefill_8k", 0, 8192, 1, 0, "kv"),          # window (state) cache
+    ("c2_csa_prefill_8k", 0, 8192, 4, 0, "kI"),          # FP4 indexer keys
+    ("c4_hca_prefill_64k", 0, 65536, 128, 0, "kv"),      # HCA cache, full size
+    ("c3_csa_decode_128k", 7, 131072, 4, 0, "kv"),       # one sequence of the 128K decode cache
+    ("c5_hybrid_csa_decode_1m", 1, 1 << 20, 4, 0, "kI"),  # 1M-token FP4 keys
+    ("c1_tiny_csa_prefill", 0, 512, 4, 0, "kv"),         # fp32 format
+    ("c1_tiny_csa_prefill", 0, 512, 4, 0, "kI"),
+    ("c1_tiny_csa_prefill", 0, 510, 1, 0, "kv"),
+]
+
+
+@pytest.mark.parametrize("name,b,T,m,pos0,part", COMPRESS_CASES)
+def test_compress_bitexact(csa, oracle_mod, name, b, T, m, pos0, part):
+    cfg = wl.CONFIGS[name]
+    toks = wl.gen_tokens(cfg, b, 0, T, parts=(part, "z" if part == "kv" else "zI"))
+    sc = wl.gen_channel_scales(cfg)
+    x = toks[part]
+    z = toks["z" if part == "kv" else "zI"]
+    s = None if m == 1 else (sc["s"] if part == "kv" else sc["sI"])
+    R = cfg.R if part == "kv" else 0
+    if cfg.fp32:
+        fmt, ofmt = csa.FMT_F32, "f32"
+    elif part == "kv":
+        fmt, ofmt = csa.FMT_MIXED592, "mixed592"
+    else:
+        fmt, ofmt = csa.FMT_MXFP4, "mxfp4"
+    P = pos0 + T + 1
+    rope_np, rope_dev = ropes(csa, oracle_mod, P)
+    out = csa.compress_kv(act_dev(x, cfg)[None], dev(z)[None], None if s is None else dev(s), m, fmt,
+                          R, rope_dev if R else None, pos0)
+    ref = oracle_mod.compress_kv(widen(x, cfg)[None], z[None], s, m, ofmt, R, pos0, rope_np)
+    if ofmt == "mxfp4":
+        np.testing.assert_array_equal(out[0].cpu().numpy(), ref[0])
+        np.testing.assert_array_equal(out[1].cpu().numpy(), ref[1])
+    elif ofmt == "f32":
+        np.testing.assert_array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    else:
+        np.testing.assert_array_equal(out.cpu().numpy(), ref)
+
+
+def test_pack_fp8_bf16_bitexact(csa, oracle_mod):
+    rng = np.random.default_rng(40)
+    v = (rng.standard_normal((5000, 512)) * np.exp(rng.uniform(-20, 12, (5000, 1)))).astype(np.float32)
+    v[3, :128] = 0.0
+    v[4, 5] = -0.0
+    v[9, 100] = 1e30
+    out = csa.kvcache_pack_fp8_bf16(dev(v))
+    np.testing.assert_array_equal(out.cpu().numpy(), oracle_mod.pack_mixed(v))
+
+
+# --------------------------------------------------------------------------
+# indexer + top-k: bit-exact indices and scores
+# --------------------------------------------------------------------------
+def _keys(csa, oracle_mod, cfg, b, T):
+    toks = wl.gen_tokens(cfg, b, 0, T, parts=("kI", "zI"))
+    sI = wl.gen_channel_scales(cfg)["sI"]
+    if cfg.fp32:
+        kd = csa.compress_kv(dev(toks["kI"])[None], dev(toks["zI"])[None], dev(sI), cfg.m, csa.FMT_F32, 0)
+        kn = oracle_mod.compress_kv(toks["kI"][None], toks["zI"][None], sI, cfg.m, "f32", 0)
+        return (kd, None), kn
+    kd = csa.compress_kv(act_dev(toks["kI"], cfg)[None], dev(toks["zI"])[None], dev(sI), cfg.m,
+                         csa.FMT_MXFP4, 0)
+    kn = oracle_mod.compress_kv(widen(toks["kI"], cfg)[None], toks["zI"][None], sI, cfg.m, "mxfp4", 0)
+    return kd, kn
+
+
+@pytest.mark.parametrize("name,rows", [("c1_tiny_csa_prefill", None), ("c2_csa_prefill_8k", 384)])
+def test_indexer_topk_prefill(csa, oracle_mod, name, rows):
+    cfg = wl.CONFIGS[name]
+    (kd, ksd), kn = _keys(csa, oracle_mod, cfg, 0, cfg.T)
+    qry = wl.gen_queries(cfg, 0)
+    q_pos = np.arange(cfg.Tq, dtype=np.int64)[None]
+    idx, sc = csa.indexer_topk(act_dev(qry["qI"], cfg)[None], dev(qry["w"])[None], kd, ksd, dev(q_pos),
+                               cfg.N, cfg.m, cfg.k)
+    idx, sc = idx.cpu().numpy(), sc.cpu().numpy()
+    sel = np.arange(cfg.Tq) if rows is None else np.unique(np.concatenate([
+        np.arange(0, 12), np.arange(cfg.k * cfg.m - 8, cfg.k * cfg.m + 8), [cfg.Tq - 1],
+        np.random.default_rng(41).choice(cfg.Tq, rows, replace=False)]))
+    oidx, osc = oracle_mod.indexer_topk(widen(qry["qI"], cfg)[sel][None], qry["w"][sel][None], kn,
+                                        q_pos[:, sel], cfg.N, cfg.m, cfg.k)
+    np.testing.assert_array_equal(idx[:, sel], oidx)
+    np.testing.assert_array_equal(sc[:, sel], osc)
+
+
+@pytest.mark.parametrize("name", ["c3_csa_decode_128k", "c5_hybrid_csa_decode_1m"])
+def test_indexer_topk_decode_full(csa, oracle_mod, name):
+    cfg = wl.CONFIGS[name]
+    B = cfg.B
+    keys_d = [_keys(csa, oracle_mod, cfg, b, cfg.T) for b in range(B)]
+    kd = torch.cat([k[0][0] for k in keys_d])
+    ksd = torch.cat([k[0][1] for k in keys_d])
+    kn = (np.concatenate([k[1][0] for k in keys_d]), np.concatenate([k[1][1] for k in keys_d]))
+    qry = [wl.gen_queries(cfg, b) for b in range(B)]
+    qI = np.stack([q["qI"] for q in qry])
+    w = np.stack([q["w"] for q in qry])
+    q_pos = np.full((B, 1), cfg.T - 1, np.int64)
+    idx, sc = csa.indexer_topk(act_dev(qI, cfg), dev(w), kd, ksd, dev(q_pos), cfg.N, cfg.m, cfg.k)
+    oidx, osc = oracle_mod.indexer_topk(widen(qI, cfg), w, kn, q_pos, cfg.N, cfg.m, cfg.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+    np.testing.assert_array_equal(sc.cpu().numpy(), osc)
+
+
+# --------------------------------------------------------------------------
+# whole CSA prefill pipeline: compress -> indexer/top-k -> sparse MQA
+# --------------------------------------------------------------------------
+def _prefill_pipeline(csa, oracle_mod, cfg, sample_rows):
+    T = cfg.T
+    toks = wl.gen_tokens(cfg, 0)
+    sc = wl.gen_channel_scales(cfg)
+    qry = wl.gen_queries(cfg, 0)
+    rope_np, rope_dev = ropes(csa, oracle_mod, T + 1)
+    fmt = csa.FMT_F32 if cfg.fp32 else csa.FMT_MIXED592
+    ofmt = "f32" if cfg.fp32 else "mixed592"
+    kv_d, z_d = act_dev(toks["kv"], cfg)[None], dev(toks["z"])[None]
+    cache = csa.compress_kv(kv_d, z_d, dev(sc["s"]), cfg.m, fmt, cfg.R, rope_dev)
+    swa = csa.compress_kv(kv_d, z_d, None, 1, fmt, cfg.R, rope_dev)
+    (kd, ksd), kn = _keys(csa, oracle_mod, cfg, 0, T)
+    q_pos = np.arange(T, dtype=np.int64)[None]
+    qpos_d = dev(q_pos)
+    idx = csa.indexer_topk(act_dev(qry["qI"], cfg)[None], dev(qry["w"])[None], kd, ksd, qpos_d, cfg.N,
+                           cfg.m, cfg.k, scores=False)
+    out, lse = csa.sparse_mqa(act_dev(qry["q"], cfg)[None], qpos_d, cache, cfg.m, idx, swa,
+                              dev(np.zeros(1, np.int64)), cfg.W, softmax_scale(cfg), rope_dev, cfg.R,
+                              lse=True)
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    # oracle from its own cache and its own top-k, on the sampled rows
+    xw = widen(toks["kv"], cfg)[None]
+    ocache = oracle_mod.compress_kv(xw, toks["z"][None], sc["s"], cfg.m, ofmt, cfg.R, 0, rope_np)
+    oswa = oracle_mod.compress_kv(xw, toks["z"][None], None, 1, ofmt, cfg.R, 0, rope_np)
+    rows = np.arange(T) if sample_rows is None else sample_rows
+    oidx, _ = oracle_mod.indexer_topk(widen(qry["qI"], cfg)[rows][None], qry["w"][rows][None], kn,
+                                      q_pos[:, rows], cfg.N, cfg.m, cfg.k)
+    oout, olse, bad = oracle_mod.attention(widen(qry["q"], cfg)[rows][None], q_pos[:, rows], ocache,
+                                           cfg.N, cfg.m, oidx, oswa, np.zeros(1, np.int64), cfg.W,
+                                           softmax_scale(cfg), rope_np, cfg.R,
+                                           oracle_mod.FMT_F32 if cfg.fp32 else oracle_mod.FMT_MIXED592)
+    assert bad == 0
+    return out[0, rows], lse[0, rows], oout[0], olse[0]
+
+
+def test_csa_prefill_tiny_fp32_full(csa, oracle_mod):
+    cfg = wl.CONFIGS["c1_tiny_csa_prefill"]
+    got, glse, ref, rlse = _prefill_pipeline(csa, oracle_mod, cfg, None)
+    assert max_rel_err(got, ref) <= tol(cfg)
+    np.testing.assert_allclose(glse, rlse, rtol=0, atol=1e-4)
+
+
+def test_csa_prefill_8k_sampled(csa, oracle_mod):
+    cfg = wl.CONFIGS["c2_csa_prefill_8k"]
+    rows = np.unique(np.concatenate([np.arange(0, 6), [127, 128, 129, 2046, 2047, 2048, 2051],
+                                     np.random.default_rng(42).choice(cfg.T, 40, replace=False),
+                                     [cfg.T - 1]]))
+    got, glse, ref, rlse = _prefill_pipeline(csa, oracle_mod, cfg, rows)
+    err = max_rel_err(got, ref)
+    assert err <= tol(cfg), err
+    np.testing.assert_allclose(glse, rlse, rtol=0, atol=2e-2)
+
+
+# --------------------------------------------------------------------------
+# decode: caches built from 128K / 1M tokens, sampled sequences checked
+# --------------------------------------------------------------------------
+def _decode_caches(csa, oracle_mod, cfg, oracle_seqs):
+    """GPU caches for all B sequences; oracle caches for oracle_seqs."""
+    T, W = cfg.T, cfg.W
+    rope_np, rope_dev = ropes(csa, oracle_mod, T + 1)
+    sc = wl.gen_channel_scales(cfg)
+    s_d = dev(sc["s"])
+    cache = torch.empty((cfg.B, cfg.N, 592), dtype=torch.uint8, device="cuda")
+    swa = torch.empty((cfg.B, W, 592), dtype=torch.uint8, device="cuda")
+    ocache, oswa = {}, {}
+    for b in range(cfg.B):
+        toks = wl.gen_tokens(cfg, b, parts=("kv", "z"))
+        kv_d, z_d = act_dev(toks["kv"], cfg)[None], dev(toks["z"])[None]
+        csa.compress_kv(kv_d, z_d, s_d, cfg.m, csa.FMT_MIXED592, cfg.R, rope_dev, out=cache[b:b + 1])
+        csa.compress_kv(kv_d[:, T - W:], z_d[:, T - W:], None, 1, csa.FMT_MIXED592, cfg.R, rope_dev,
+                        pos0=T - W, out=swa[b:b + 1])
+        if b in oracle_seqs:
+            xw = widen(toks["kv"], cfg)[None]
+            ocache[b] = oracle_mod.compress_kv(xw, toks["z"][None], sc["s"], cfg.m, "mixed592", cfg.R, 0,
+                                               rope_np)
+            oswa[b] = oracle_mod.compress_kv(xw[:, T - W:], toks["z"][None, T - W:], None, 1, "mixed592",
+                                             cfg.R, T - W, rope_np)
+        del kv_d, z_d
+    return cache, swa, ocache, oswa, rope_np, rope_dev
+
+
+@pytest.mark.parametrize("name", ["c3_csa_decode_128k", "c5_hybrid_csa_decode_1m",
+                                  "c4_hca_decode_1m", "c5_hybrid_hca_decode_1m"])
+def test_decode_sampled(csa, oracle_mod, name):
+    cfg = wl.CONFIGS[name]
+    B, T, W = cfg.B, cfg.T, cfg.W
+    check = sorted({0, B - 1})
+    cache, swa, ocache, oswa, rope_np, rope_dev = _decode_caches(csa, oracle_mod, cfg, check)
+    qry = [wl.gen_queries(cfg, b) for b in range(B)]
+    q = np.stack([x["q"] for x in qry])
+    q_pos = np.full((B, 1), T - 1, np.int64)
+    pos0 = np.full(B, T - W, np.int64)
+    if cfg.k:
+        keys = [_keys(csa, oracle_mod, cfg, b, T) for b in range(B)]
+        kd = torch.cat([k[0][0] for k in keys])
+        ksd = torch.cat([k[0][1] for k in keys])
+        qI = np.stack([x["qI"] for x in qry])
+        w = np.stack([x["w"] for x in qry])
+        idx = csa.indexer_topk(act_dev(qI, cfg), dev(w), kd, ksd, dev(q_pos), cfg.N, cfg.m, cfg.k,
+                               scores=False)
+        out = csa.sparse_mqa(act_dev(q, cfg), dev(q_pos), cache, cfg.m, idx, swa, dev(pos0), W,
+                             softmax_scale(cfg), rope_dev, cfg.R)
+    else:
+        out = csa.hca_dense_attn(act_dev(q, cfg), dev(q_pos), cache, cfg.m, swa, dev(pos0), W,
+                                 softmax_scale(cfg), rope_dev, cfg.R)
+    out = out.float().cpu().numpy()
+    for b in check:
+        oidx = None
+        if cfg.k:
+            oidx, _ = oracle_mod.indexer_topk(widen(qI, cfg)[b:b + 1], w[b:b + 1], keys[b][1], q_pos[b:b + 1],
+                                              cfg.N, cfg.m, cfg.k)
+        ref, _, bad = oracle_mod.attention(widen(q, cfg)[b:b + 1], q_pos[b:b + 1], ocache[b], cfg.N, cfg.m,
+                                           oidx, oswa[b], pos0[b:b + 1], W, softmax_scale(cfg), rope_np,
+                                           cfg.R)
+        assert bad == 0
+        err = max_rel_err(out[b:b + 1], ref)
+        assert err <= tol(cfg), (b, err)
+
+
+# --------------------------------------------------------------------------
+# properties: determinism, device checks, edge cases
+# --------------------------------------------------------------------------
+def _small_mixed(csa, oracle_mod, T=512, m=4, H=64, seed=50):
+    rng = np.random.default_rng(seed)
+    N = T // m
+    rope_np, rope_dev = ropes(csa, oracle_mod, T + 1)
+    ent = rng.standard_normal((1, N, 512)).astype(np.float32)
+    tok = rng.standard_normal((1, T, 512)).astype(np.float32)
+    cache = oracle_mod.pack_mixed(ent)
+    swa = oracle_mod.pack_mixed(tok)
+    q = wl.f32_to_bf16_bits(rng.standard_normal((1, T, H, 512)).astype(np.float32))
+    return rope_np, rope_dev, cache, swa, q, N
+
+
+def test_attention_is_deterministic(csa, oracle_mod):
+    rope_np, rope_dev, cache, swa, q, N = _small_mixed(csa, oracle_mod)
+    T, m, k = 512, 4, 64
+    rng = np.random.default_rng(51)
+    idx = np.full((1, T, k), -1, np.int32)
+    for t in range(T):
+        nv = min(N, (t + 1) // m)
+        p = rng.permutation(nv)[:k]
+        idx[0, t, :len(p)] = p
+    args = (dev(np.arange(T, dtype=np.int64)[None]), dev(cache), m, dev(idx), dev(swa),
+            dev(np.zeros(1, np.int64)), 128, 1 / math.sqrt(512), rope_dev)
+    from gpu_common import dev_bf16
+    a = csa.sparse_mqa(dev_bf16(q), *args)
+    b = csa.sparse_mqa(dev_bf16(q), *args)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_invalid_index_sets_device_check(csa, oracle_mod):
+    rope_np, rope_dev, cache, swa, q, N = _small_mixed(csa, oracle_mod, T=64, H=64)
+    from gpu_common import dev_bf16
+    ws = csa.Workspace()
+    q_pos = np.array([[40]], np.int64)
+    good = np.array([[[0, 5, 9, -1]]], np.int32)
+    bad = np.array([[[0, 5, 9, 10]]], np.int32)       # entry 10 covers tokens 40..43: not visible at 40
+    qd = dev_bf16(q[:, 40:41])
+    args = (dev(cache), 4)
+    rest = (dev(swa), dev(np.zeros(1, np.int64)), 16, 0.05, rope_dev)
+    o_good = csa.sparse_mqa(qd, dev(q_pos), *args, dev(good), *rest, ws=ws)
+    assert ws.flags() == 0
+    o_bad = csa.sparse_mqa(qd, dev(q_pos), *args, dev(bad), *rest, ws=ws)
+    assert ws.flags() & csa.FLAG_DEVICE_CHECK
+    assert torch.equal(o_good.view(torch.int16), o_bad.view(torch.int16))
+    ws.reset()
+    assert ws.flags() == 0
+
+
+def test_no_keys_gives_zero(csa, oracle_mod):
+    rope_np, rope_dev, cache, swa, q, N = _small_mixed(csa, oracle_mod, T=64, H=64)
+    from gpu_common import dev_bf16
+    none = np.full((1, 1, 8), -1, np.int32)
+    out, lse = csa.sparse_mqa(dev_bf16(q[:, :1]), dev(np.array([[0]], np.int64)), dev(cache), 4, dev(none),
+                              dev(swa), dev(np.zeros(1, np.int64)), 0, 0.05, rope_dev, lse=True)
+    assert torch.all(out.float() == 0) and torch.all(torch.isinf(lse))
+
+
+def test_hca_equals_sparse_with_all_entries(csa, oracle_mod):
+    """k >= visible entries: the sparse call over all visible entries equals the dense call."""
+    rope_np, rope_dev, cache, swa, q, N = _small_mixed(csa, oracle_mod, T=512, m=8, H=64)
+    T, m = 512, 8
+    idx = np.full((1, T, N), -1, np.int32)
+    for t in range(T):
+        nv = min(N, (t + 1) // m)
+        idx[0, t, :nv] = np.arange(nv)
+    from gpu_common import dev_bf16
+    qp = dev(np.arange(T, dtype=np.int64)[None])
+    rest = (dev(swa), dev(np.zeros(1, np.int64)), 32, 1 / math.sqrt(512), rope_dev)
+    a = csa.sparse_mqa(dev_bf16(q), qp, dev(cache), m, dev(idx), *rest).float()
+    b = csa.hca_dense_attn(dev_bf16(q), qp, dev(cache), m, *rest).float()
+    assert float((a - b).abs().max()) <= 1e-2 * float(b.abs().max())

@@ -25,7 +25,9 @@ of the fp32 draw); fp32 tensors as ``float32``.
 """
 from __future__ import annotations
 
+import concurrent.futures as _cf
 import dataclasses
+import os
 import zlib
 
 import numpy as np
@@ -138,31 +140,36 @@ def gen_channel_scales(cfg: Config, seed: int = 0) -> dict:
     return out
 
 
-def gen_tokens(cfg: Config, b: int, t0: int = 0, t1: int | None = None, seed: int = 0) -> dict:
+def gen_tokens(cfg: Config, b: int, t0: int = 0, t1: int | None = None, seed: int = 0,
+               parts=("kv", "z", "kI", "zI")) -> dict:
     """Per-token activations of sequence b, tokens [t0, t1) of the context.
 
-    Returns kv [n, D], z [n] and, when the layer has an indexer, kI [n, dI], zI [n].
-    Tokens are drawn in fixed blocks of 4096 so that any sub-range is the same
-    slice of the full sequence.
+    kv [n, D] and z [n]; with an indexer also kI [n, dI] and zI [n].  Each
+    tensor has its own generator, drawn in fixed blocks of 4096 tokens, so any
+    sub-range or subset of tensors is the same slice of the full sequence.
     """
     t1 = cfg.T if t1 is None else t1
     blk = 4096
-    parts = {"kv": [], "z": [], "kI": [], "zI": []}
-    for c in range(t0 // blk, (t1 + blk - 1) // blk):
+    widths = {"kv": cfg.D, "kI": cfg.dI}
+    out = {}
+    def block(name, c):
         lo, hi = c * blk, min((c + 1) * blk, cfg.T)
         a, e = max(t0, lo) - lo, min(t1, hi) - lo
-        r = rng_for(seed, cfg.name, "tok", b, c)
-        kv = _act(cfg, r, (hi - lo, cfg.D))
-        z = (r.standard_normal(size=hi - lo, dtype=np.float32) * np.float32(cfg.z_std))
-        parts["kv"].append(kv[a:e])
-        parts["z"].append(z[a:e])
-        if cfg.dI:
-            kI = _act(cfg, r, (hi - lo, cfg.dI))
-            zI = (r.standard_normal(size=hi - lo, dtype=np.float32) * np.float32(cfg.z_std))
-            parts["kI"].append(kI[a:e])
-            parts["zI"].append(zI[a:e])
-    out = {k: np.concatenate(v) for k, v in parts.items() if v}
-    return out
+        r = rng_for(seed, cfg.name, name, b, c)
+        if name in ("kv", "kI"):
+            v = _act(cfg, r, (hi - lo, widths[name]))
+        else:
+            v = r.standard_normal(size=hi - lo, dtype=np.float32) * np.float32(cfg.z_std)
+        return v[a:e]
+
+    jobs = [(name, c) for name in parts if not (name in ("kI", "zI") and not cfg.dI)
+            for c in range(t0 // blk, (t1 + blk - 1) // blk)]
+    with _cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+        res = list(ex.map(lambda jc: block(*jc), jobs))
+    out = {}
+    for (name, _), v in zip(jobs, res):
+        out.setdefault(name, []).append(v)
+    return {k: np.concatenate(v) for k, v in out.items()}
 
 
 def gen_queries(cfg: Config, b: int, q0: int = 0, q1: int | None = None, seed: int = 0) -> dict:
