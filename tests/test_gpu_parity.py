@@ -342,3 +342,95 @@ def test_hca_equals_sparse_with_all_entries(csa, oracle_mod):
     a = csa.sparse_mqa(dev_bf16(q), qp, dev(cache), m, dev(idx), *rest).float()
     b = csa.hca_dense_attn(dev_bf16(q), qp, dev(cache), m, *rest).float()
     assert float((a - b).abs().max()) <= 1e-2 * float(b.abs().max())
+
+
+# --------------------------------------------------------------------------
+# tensor-core attention: tile edges, rescale path, agreement with the CUDA-core kernel
+# --------------------------------------------------------------------------
+def _oracle_attn(oracle_mod, q, q_pos, cache, N, m, idx, swa, pos0, W, scale, rope_np):
+    out, lse, bad = oracle_mod.attention(wl.bf16_bits_to_f32(q), q_pos, cache, N, m, idx, swa, pos0, W,
+                                         scale, rope_np, 64)
+    assert bad == 0
+    return out, lse
+
+
+@pytest.mark.parametrize("k,W", [(1, 0), (127, 1), (128, 0), (300, 37), (1024, 128), (4000, 128)])
+def test_tc_tile_edges(csa, oracle_mod, k, W):
+    """Key counts around the 128-key tile: empty tail, exact multiples, ragged."""
+    from gpu_common import dev_bf16
+    rng = np.random.default_rng(60 + k)
+    T, m = 4 * 4096, 4
+    N = T // m
+    rope_np, rope_dev = ropes(csa, oracle_mod, T + 1)
+    cache = oracle_mod.pack_mixed(rng.standard_normal((1, N, 512)).astype(np.float32))
+    swa = oracle_mod.pack_mixed(rng.standard_normal((1, 256, 512)).astype(np.float32))
+    Tq = 6
+    q = wl.f32_to_bf16_bits(rng.standard_normal((1, Tq, 64, 512)).astype(np.float32))
+    q_pos = np.array([[T - 1, T - 2, 4 * k + 3, 200, 3, T - 100]], np.int64)
+    pos0 = np.array([T - 256], np.int64)
+    idx = np.full((1, Tq, k), -1, np.int32)
+    for i, t in enumerate(q_pos[0]):
+        nv = min(N, (t + 1) // m)
+        p = rng.permutation(nv)[:k]
+        idx[0, i, :len(p)] = p
+    # window rows exist only for the last 256 positions: keep W-windows inside them
+    q_pos_w = q_pos.copy()
+    if W:
+        q_pos_w[0] = np.maximum(q_pos[0], T - 256 + W)
+        q_pos_w[0] = np.minimum(q_pos_w[0], T - 1)
+    scale = 1 / math.sqrt(512)
+    got = csa.sparse_mqa(dev_bf16(q), dev(q_pos_w), dev(cache), m, dev(idx), dev(swa), dev(pos0), W, scale,
+                         rope_dev).float().cpu().numpy()
+    ref, _ = _oracle_attn(oracle_mod, q, q_pos_w, cache, N, m, idx, swa, pos0, W, scale, rope_np)
+    assert max_rel_err(got, ref) <= 1e-2
+
+
+def test_tc_rescale_path(csa, oracle_mod):
+    """Later key tiles with much larger logits force the lazy rescale of O."""
+    from gpu_common import dev_bf16
+    rng = np.random.default_rng(70)
+    T, m, k = 4096, 4, 640
+    N = T // m
+    rope_np, rope_dev = ropes(csa, oracle_mod, T + 1)
+    q32 = rng.standard_normal((1, 1, 64, 512)).astype(np.float32)
+    base = rng.standard_normal((1, N, 512)).astype(np.float32)
+    # entries aligned with q (head-averaged) get growing weight: logits rise tile by tile
+    dirn = q32[0, 0].mean(0)
+    grow = np.linspace(0, 6, N).astype(np.float32)[None, :, None]
+    ent = base + grow * dirn[None, None, :] / np.linalg.norm(dirn) * 8
+    cache = oracle_mod.pack_mixed(ent.astype(np.float32))
+    swa = oracle_mod.pack_mixed(rng.standard_normal((1, 128, 512)).astype(np.float32))
+    q = wl.f32_to_bf16_bits(q32)
+    q_pos = np.array([[T - 1]], np.int64)
+    idx = np.arange(N - k, N, dtype=np.int32)[None, None, :]         # increasing logits
+    pos0 = np.array([T - 128], np.int64)
+    scale = 1 / math.sqrt(512)
+    got, glse = csa.sparse_mqa(dev_bf16(q), dev(q_pos), dev(cache), m, dev(idx), dev(swa), dev(pos0), 128,
+                               scale, rope_dev, lse=True)
+    ref, rlse = _oracle_attn(oracle_mod, q, q_pos, cache, N, m, idx, swa, pos0, 128, scale, rope_np)
+    assert max_rel_err(got.float().cpu().numpy(), ref) <= 1e-2
+    np.testing.assert_allclose(glse.cpu().numpy(), rlse, rtol=0, atol=2e-2)
+
+
+def test_simt_and_tc_kernels_agree(csa, oracle_mod, monkeypatch):
+    from gpu_common import dev_bf16
+    rope_np, rope_dev, cache, swa, q, N = _small_mixed(csa, oracle_mod, T=1024, m=4, H=64, seed=80)
+    T, m, k = 1024, 4, 96
+    rng = np.random.default_rng(81)
+    idx = np.full((1, T, k), -1, np.int32)
+    for t in range(T):
+        nv = min(N, (t + 1) // m)
+        p = rng.permutation(nv)[:k]
+        idx[0, t, :len(p)] = p
+    args = (dev(np.arange(T, dtype=np.int64)[None]), dev(cache), m, dev(idx), dev(swa),
+            dev(np.zeros(1, np.int64)), 64, 1 / math.sqrt(512), rope_dev)
+    tc = csa.sparse_mqa(dev_bf16(q), *args).float()
+    monkeypatch.setenv("CSA_ATTN_IMPL", "simt")
+    simt = csa.sparse_mqa(dev_bf16(q), *args).float()
+    monkeypatch.delenv("CSA_ATTN_IMPL")
+    rows = np.array([0, 1, 100, 511, 1023])
+    ref, _ = _oracle_attn(oracle_mod, q[:, rows], np.arange(T, dtype=np.int64)[None][:, rows], cache, N, m,
+                          idx[:, rows], swa, np.zeros(1, np.int64), 64, 1 / math.sqrt(512), rope_np)
+    assert max_rel_err(tc.cpu().numpy()[:, rows], ref) <= 1e-2
+    assert max_rel_err(simt.cpu().numpy()[:, rows], ref) <= 1e-2
+    assert float((tc - simt).abs().max()) <= 1e-2 * float(simt.abs().max())
