@@ -231,6 +231,31 @@ int hca_dense_attn(const void *q, int q_dtype, const int64_t *q_pos, int B, int6
                    int64_t rope_rows, void *out, float *lse, void *ws, size_t ws_bytes,
                    void *stream);
 
+/*
+ * csa_indexer_topk_noalloc: csa_indexer_topk without a caller workspace.
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot allocate device memory.  Serving runtimes that plan every device
+ * buffer before they start and refuse allocation afterwards, and plugins
+ * that such a runtime hands the tensors of one call but no allocator,
+ * cannot provide the score scratch that csa_indexer_topk needs; this call
+ * keeps that scratch in a fixed device array owned by the library.
+ * Arguments, results and errors are those of csa_indexer_topk, without
+ * ws / ws_bytes.  Rules:
+ *  - the array holds 16 MiB (B * Tq * N <= 4194304 scores); larger calls
+ *    return CSA_ERR_UNSUPPORTED before anything is enqueued;
+ *  - every GPU that loads the library holds the array until exit;
+ *  - all calls share the array and it keeps the last call's contents:
+ *    calls that overlap on the GPU race, so order them on one stream;
+ *  - the first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ * It calls no cudaMalloc / cudaFree and no allocating library routine.
+ */
+int csa_indexer_topk_noalloc(const void *qI, int qI_dtype, const float *w, const void *kI,
+                             const uint8_t *kI_scales, int kI_fmt, const int64_t *q_pos, int B,
+                             int64_t Tq, int HI, int dI, int64_t N, int m, int k,
+                             int32_t *idx_out, float *score_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

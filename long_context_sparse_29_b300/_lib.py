@@ -31,6 +31,8 @@ SIGNATURES = {
                                P, SZ, P]),
     "csa_sparse_mqa": (I32, [P, I32, P, I32, I64, I32, I32, I32, I32, P, I64, I32, P, I32, P, P,
                              I64, I32, F32, P, P, I64, P, P, P, SZ, P]),
+    "csa_indexer_topk_noalloc": (I32, [P, I32, P, P, P, I32, P, I32, I64, I32, I32, I64, I32, I32, P,
+                                       P, P]),
     "hca_dense_attn": (I32, [P, I32, P, I32, I64, I32, I32, I32, I32, P, I64, I32, P, P, I64, I32,
                              F32, P, P, I64, P, P, P, SZ, P]),
 }

@@ -273,3 +273,10 @@ int hca_dense_attn(const void* q, int q_dtype, const int64_t* q_pos, int B, int6
 }
 
 }  // extern "C"
+
+namespace csa {
+
+// Records an error for csa_last_error() from other translation units.
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+}  // namespace csa
