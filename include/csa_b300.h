@@ -96,13 +96,16 @@ int csa_rope_table(int64_t P, int R, double base, float *cos_out, float *sin_out
 
 /*
  * csa_workspace_size: bytes of `ws` that `op` (CSA_OP_*) needs for B
- * sequences of Tq queries, N entries per sequence, top-k k (CSA) and the
- * largest key count per query max_keys (attention: k + W for CSA, entries +
- * W for HCA).  Never less than 256 (the status block).  Returns -1 for an
- * unknown op.
+ * sequences of Tq queries, N entries per sequence, top-k k (CSA), H heads of
+ * dim D, the largest key count per query max_keys (attention: k + W for CSA,
+ * entries + W for HCA) and Ts window-cache rows per sequence.  Never less
+ * than 256 (the status block).  Returns -1 for an unknown op.  The attention
+ * calls use the space for split-softmax partial states (few queries) and
+ * for a bf16 copy of the cache rows when every row serves many queries
+ * (prefill); with less workspace they fall back to slower plans.
  */
 int64_t csa_workspace_size(int op, int B, int64_t Tq, int64_t N, int k, int H, int D,
-                           int64_t max_keys);
+                           int64_t max_keys, int64_t Ts);
 
 /* Clear the status block of ws (async on stream). */
 int csa_status_reset(void *ws, void *stream);

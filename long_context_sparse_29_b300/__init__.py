@@ -59,8 +59,9 @@ def _dt(t):
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
-def workspace_size(op: int, B: int, Tq: int, N: int, k: int, H: int, D: int, max_keys: int) -> int:
-    return int(lib().csa_workspace_size(op, B, Tq, N, k, H, D, max_keys))
+def workspace_size(op: int, B: int, Tq: int, N: int, k: int, H: int, D: int, max_keys: int,
+                   Ts: int = 0) -> int:
+    return int(lib().csa_workspace_size(op, B, Tq, N, k, H, D, max_keys, Ts))
 
 
 class Workspace:
@@ -170,7 +171,7 @@ def indexer_topk(qI, w, kI, kI_scales, q_pos, N: int, m: int, k: int, scores: bo
     if scores and score_out is None:
         score_out = torch.empty((B, Tq, k), dtype=torch.float32, device=dev)
     ws = _ws(ws, dev)
-    need = workspace_size(OP_INDEXER_TOPK, B, Tq, N, k, 0, 0, 0)
+    need = workspace_size(OP_INDEXER_TOPK, B, Tq, N, k, 0, 0, 0, 0)
     buf = ws.get(need)
     check(lib().csa_indexer_topk(_ptr(qI), _dt(qI), _ptr(w), _ptr(kI), _ptr(kI_scales), fmt,
                                  _ptr(q_pos), B, Tq, HI, dI, N, m, k, _ptr(idx_out),
@@ -197,7 +198,7 @@ def _attn(q, q_pos, cache, N, m, idx, swa, swa_pos0, W, scale, rope, R, want_lse
     k = idx.shape[-1] if idx is not None else 0
     max_keys = (k if idx is not None else N) + W
     op = OP_SPARSE_MQA if idx is not None else OP_HCA_DENSE
-    buf = ws.get(workspace_size(op, B, Tq, N, k, H, D, max_keys))
+    buf = ws.get(workspace_size(op, B, Tq, N, k, H, D, max_keys, Ts))
     st = _stream(dev)
     if idx is not None:
         _need(idx, "idx", torch.int32)

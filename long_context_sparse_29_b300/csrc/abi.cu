@@ -102,8 +102,7 @@ int attn_prepare(csa::AttnArgs& a, const void* q, int q_dtype, const int64_t* q_
   a.ws = ws;
   a.ws_bytes = ws_bytes;
   a.max_keys = (int)max_keys;
-  const size_t need = csa_workspace_size(idx ? CSA_OP_SPARSE_MQA : CSA_OP_HCA_DENSE, B, Tq, N, k,
-                                         H, D, max_keys);
+  const size_t need = csa::kWsHeader;   // more is used when given (see csa_workspace_size)
   if (ws_bytes < need)
     return fail(CSA_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name, ws_bytes, need);
   return CSA_OK;
@@ -141,7 +140,7 @@ int csa_rope_table(int64_t P, int R, double base, float* cos_out, float* sin_out
 }
 
 int64_t csa_workspace_size(int op, int B, int64_t Tq, int64_t N, int k, int H, int D,
-                           int64_t max_keys) {
+                           int64_t max_keys, int64_t Ts) {
   (void)k;
   if (B < 0 || Tq < 0 || N < 0) return -1;
   switch (op) {
@@ -149,7 +148,7 @@ int64_t csa_workspace_size(int op, int B, int64_t Tq, int64_t N, int k, int H, i
       return (int64_t)indexer_ws(B, Tq, N);
     case CSA_OP_SPARSE_MQA:
     case CSA_OP_HCA_DENSE:
-      return (int64_t)(csa::kWsHeader + align256(csa::attn_tc_workspace(B, Tq, H, D, max_keys)));
+      return (int64_t)(csa::kWsHeader + align256(csa::attn_tc_workspace(B, Tq, H, D, max_keys, N, Ts)));
     default:
       return -1;
   }

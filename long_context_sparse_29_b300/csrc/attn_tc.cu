@@ -7,22 +7,31 @@
 // section "关键技术细节": RoPE on the last 64 dims with inverse rotation of
 // the output, RoPE dims BF16 and the rest FP8 in the KV cache.
 //
-// One CTA per query token, all 64 heads (they share the KV: MQA).  Keys run
-// in tiles of 128:
-//   producer warps 4-7  gather the tile's 592-byte rows from HBM/L2,
-//                       dequantise FP8 x 2^e (exact in bf16) and write a
-//                       128 x 512 bf16 tile, 128-byte swizzled, into smem;
-//   MMA warp 8          S = Q K^T   (M = 64 heads, N = 128 keys, K = 512)
-//                       into TMEM, then O^T += V^T P^T (M = 128 dims x 4,
-//                       N = 64 heads, K = 128 keys) into TMEM -- the value
-//                       of a key is the key itself, so the same smem tile is
-//                       read K-major for QK^T and MN-major for PV;
+// Persistent kernel, one CTA per SM.  A work item is one query token (all
+// 64 heads share the KV: MQA) or, for small batches, a contiguous range of
+// its key tiles (split-K; a second kernel merges the partial softmaxes).
+// Keys run in tiles of 64 through a two-deep smem ring:
+//   producer warps 4-7  gather each tile's 592-byte rows (16 rows per warp in
+//                       flight), dequantise FP8 x 2^e to bf16 (exact) and
+//                       write a 64 x 512 bf16 tile, 128-byte swizzled; the
+//                       bf16 RoPE columns and the query are copied with
+//                       cp.async;
+//   MMA warp 8          S = Q K^T   (M = 64 heads, N = 64 keys, K = 512) into
+//                       TMEM, and O^T += V^T P^T (M = 128 dims x 4, N = 64
+//                       heads, K = 64 keys) into TMEM -- V = K, so the same
+//                       smem tile is read K-major for QK^T and MN-major for
+//                       PV; QK^T of the next tile is issued before PV of the
+//                       current one so the softmax overlaps the tensor core;
 //   softmax warps 0-3   read S from TMEM, online softmax in the exp2 domain
 //                       with a lazy rescale of O^T (only when a running max
-//                       grows by more than 2^8), write bf16 P to smem, and in
-//                       the end normalise O, rotate its RoPE dims back and
-//                       store bf16.
-// Waits are bounded; on expiry the CTA records a timeout and returns.
+//                       grows by more than 2^8), write bf16 P to smem; at the
+//                       end of an item normalise O, rotate its RoPE dims back
+//                       and store bf16 (or store the partial state).
+// Every ring slot has its own full / empty mbarrier, so a waiter is never
+// more than one phase behind.  Waits are bounded: on expiry the CTA records a
+// timeout flag in the workspace and gives up.
+#include <cuda.h>
+
 #include "csa_common.cuh"
 #include "launch.h"
 #include "tc_ptx.cuh"
@@ -35,70 +44,225 @@ namespace {
 
 constexpr int kH = 64;
 constexpr int kD = 512;
-constexpr int kTile = 128;
+constexpr int kTile = 64;
 constexpr int kThreads = 9 * 32;
 constexpr int kMmaWarp = 8;
 
-constexpr uint32_t kQOff = 0;                     // 8 x [64 x 128 B]
-constexpr uint32_t kKVOff = 65536;                // 8 x [128 x 128 B]
-constexpr uint32_t kPOff = kKVOff + 131072;       // 2 x [64 x 128 B]
-constexpr uint32_t kMiscOff = kPOff + 16384;      // 1 KB of barriers and per-head state
-constexpr uint32_t kListOff = kMiscOff + 1024;    // int32 key list
-constexpr uint32_t kSmemLimit = 232448;
-constexpr int kMaxList = (int)((kSmemLimit - 1024 - kListOff) / 4);
+constexpr uint32_t kQOff = 0;                     // 8 chunks x [64 heads x 128 B]
+constexpr uint32_t kKVOff = 65536;                // 2 buffers x 8 chunks x [64 keys x 128 B]
+constexpr uint32_t kPOff = kKVOff + 131072;       // 2 buffers x [64 heads x 64 keys bf16]
+constexpr uint32_t kMiscOff = kPOff + 16384;      // barriers and per-head state
+constexpr uint32_t kListOff = kMiscOff + 1024;    // int32 key list of the current item
+constexpr uint32_t kSmemBytes = 232448;           // 227 KiB
+constexpr int kMaxList = (int)((kSmemBytes - 1024 - kListOff) / 8);   // per buffer (two buffers)
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;      // O^T: 4 blocks of 64 columns (heads), lanes = dims
-constexpr uint32_t kTmemS = 256;    // S: 2 buffers of 128 columns (keys)
+constexpr uint32_t kTmemO = 0;       // O^T: 4 blocks of 64 columns (heads); lanes = dims
+constexpr uint32_t kTmemS = 256;     // S: 2 buffers of 64 columns (keys); M = 64 layout
 
 constexpr uint32_t kWaitLimit = 1u << 20;
-constexpr float kLazy = 8.0f;       // log2 growth of a running max that forces a rescale
-
-// rows of a 64-row (M = 64) accumulator: warp quadrant q, lanes 0-15 hold rows 16 q + lane
-__device__ __forceinline__ bool s_row_valid(int lane) { return lane < 16; }
-__device__ __forceinline__ int s_row(int q, int lane) { return 16 * q + lane; }
+constexpr float kLazy = 8.0f;        // log2 growth of a running max that forces a rescale
 
 struct Misc {
-  uint64_t bar_full, bar_s, bar_p, bar_o;
+  uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
+  uint64_t q_full, q_ready, q_empty, o_full, o_empty;
+  uint64_t sm_sync[2];           // softmax group syncs (4 warps), alternating
+  uint64_t list_full[2], list_empty[2];  // producer key list handover, double-buffered
   uint32_t tmem;
   int abort;
-  int any_rescale[2];
-  int nkeys;
-  float alpha[kH];
-  float l_fin[kH];
+  int any_rescale[4];
+  float alpha[2][kH];
+  float lsum[kH];
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk16) {
   return row * 128u + (((chunk16 ^ row) & 7u) << 4);
 }
 
-// 16 E4M3 codes (one uint4) times 2^e -> 16 bf16 (two uint4), exact
+// Bounded barrier of the four softmax warps: every warp arrives once on
+// sm_sync[n & 1] and waits for its phase.  Returns false on expiry.
+__device__ __forceinline__ bool group_sync(Misc* ms, uint32_t& n, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ms->sm_sync[n & 1]);
+  const bool ok = mbar_wait(&ms->sm_sync[n & 1], (n >> 1) & 1, kWaitLimit);
+  ++n;
+  return ok;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+// 16 E4M3 codes times 2^e -> 16 bf16, exact, without the conversion pipe.
+// A code's 7 magnitude bits placed at bits 20..26 of an fp32 read as
+// 2^(E-127) (1 + m/8) for exponent field E >= 1 and as m 2^-129 for E = 0:
+// the E4M3 value times 2^-120 in both cases.  One fp32 multiply by
+// 2^(120 + e) (two when 2^(120 + e) is not a finite fp32) gives the value
+// times the group scale 2^e exactly -- it has at most 4 significant bits --
+// so the top half of the fp32 is the bf16.
+__device__ __forceinline__ uint32_t e4m3_bits(uint32_t x, int byte) {
+  // fp32 bit pattern holding the magnitude bits of code `byte` of x at bits
+  // 20..26 and its sign at bit 31
+  switch (byte) {
+    case 0: return ((x << 20) & 0x07F00000u) | ((x << 24) & 0x80000000u);
+    case 1: return ((x << 12) & 0x07F00000u) | ((x << 16) & 0x80000000u);
+    case 2: return ((x << 4) & 0x07F00000u) | ((x << 8) & 0x80000000u);
+    default: return ((x >> 4) & 0x07F00000u) | (x & 0x80000000u);
+  }
+}
+
 __device__ __forceinline__ void dequant16(const uint4 c, float sc, uint4& o0, uint4& o1) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
   uint32_t r[8];
+  if (sc <= 128.0f) {                       // 2^(120 + e) is a finite fp32: one multiply
+    const float s120 = __fmul_rn(sc, 0x1p120f);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 4; ++i) {
+      const float f0 = __fmul_rn(__uint_as_float(e4m3_bits(w[i], 0)), s120);
+      const float f1 = __fmul_rn(__uint_as_float(e4m3_bits(w[i], 1)), s120);
+      const float f2 = __fmul_rn(__uint_as_float(e4m3_bits(w[i], 2)), s120);
+      const float f3 = __fmul_rn(__uint_as_float(e4m3_bits(w[i], 3)), s120);
+      r[2 * i] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+      r[2 * i + 1] = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+    }
+  } else {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[i] >> (16 * h)) & 0xffffu);
-      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-      const float2 f = __half22float2(__half2(hr));
-      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
-      r[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b);
+    for (int i = 0; i < 4; ++i) {
+      float f[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) f[j] = __fmul_rn(__fmul_rn(__uint_as_float(e4m3_bits(w[i], j)), 0x1p120f), sc);
+      r[2 * i] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632);
+      r[2 * i + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632);
     }
   }
   o0 = make_uint4(r[0], r[1], r[2], r[3]);
   o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
+// Mixed 592-byte rows -> bf16 rows of 512 (exact), one warp per row.  Used
+// when every row serves many queries, so the expansion is paid once.
+__global__ void __launch_bounds__(256) expand_rows_kernel(const uint8_t* __restrict__ rows, int64_t n,
+                                                          __nv_bfloat16* __restrict__ out) {
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= n) return;
+  const uint8_t* row = rows + r * kMixRow;
+  uint4* dst = reinterpret_cast<uint4*>(out + r * kD);
+  if (lane < 28) {
+    const uint4 c = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+    const float sc = __ldg(reinterpret_cast<const float*>(row + kMixScaleOff) + (lane >> 3));
+    uint4 o0, o1;
+    dequant16(c, sc, o0, o1);
+    dst[2 * lane] = o0;
+    dst[2 * lane + 1] = o1;
+  } else {
+    const int l4 = lane - 28;
+    dst[56 + 2 * l4] = __ldg(reinterpret_cast<const uint4*>(row + kMixRopeOff) + 2 * l4);
+    dst[56 + 2 * l4 + 1] = __ldg(reinterpret_cast<const uint4*>(row + kMixRopeOff) + 2 * l4 + 1);
+  }
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+struct Params {
+  const __nv_bfloat16* q;
+  const int64_t* q_pos;
+  int64_t Tq;
+  const uint8_t* cache;
+  int64_t N;
+  int m;
+  const int32_t* idx;
+  int k;
+  const uint8_t* swa;
+  const int64_t* swa_pos0;
+  int64_t Ts;
+  int W;
+  float scale_log2;
+  const float* rcos;
+  const float* rsin;
+  int64_t rope_rows;
+  __nv_bfloat16* out;
+  float* lse;
+  void* ws;
+  int64_t items;      // rows * nsplit
+  int nsplit;
+  float* part_o;      // [items, 64, 512] unnormalised O (split mode)
+  float* part_ml;     // [items, 64, 2] running max (log2 units) and sum
+  const __nv_bfloat16* xcache;   // bf16 copy of the cache rows [B, N, 512], or NULL
+  const __nv_bfloat16* xswa;     // bf16 copy of the window rows [B, Ts, 512]
+  int64_t xrows;                 // rows of the bf16 copy (cache rows, then window rows)
+  int64_t xwin0;                 // first window row in the copy (= B * N)
+};
+
+// Keys of one work item: entries first (selected, in idx order, or all
+// visible ones), then the window tokens; this split owns tiles [tlo, thi).
+struct Item {
+  int64_t row, b, t;
+  bool t_ok;
+  int ne, nwin, nkeys;
+  int64_t w_lo, p0;
+  int tlo, thi;
+  int key_hi;
+};
+
+constexpr int kIdxBatch = 16;   // selected indices loaded per lane before any is used
+
+__device__ __forceinline__ bool entry_ok(int32_t j, int64_t t, const Params& p) {
+  return j >= 0 && (int64_t)j < p.N && (int64_t)(j + 1) * p.m - 1 <= t;
+}
+
+template <bool DENSE>
+__device__ __forceinline__ int count_valid(const Params& p, int64_t row, int64_t t, int lane) {
+  if (DENSE) {
+    const int64_t nv = (t + 1) / p.m;
+    return (int)(nv < p.N ? nv : p.N);
+  }
+  int cnt = 0;
+  for (int base = 0; base < p.k; base += 32 * kIdxBatch) {
+    int32_t js[kIdxBatch];
+#pragma unroll
+    for (int i = 0; i < kIdxBatch; ++i) {
+      const int r = base + 32 * i + lane;
+      js[i] = r < p.k ? __ldg(p.idx + row * p.k + r) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kIdxBatch; ++i) cnt += __popc(__ballot_sync(0xffffffffu, entry_ok(js[i], t, p)));
+  }
+  return cnt < kMaxList ? cnt : kMaxList;
+}
+
+// Warp-uniform description of work item `it` (every lane of the warp calls it).
+template <bool DENSE>
+__device__ __forceinline__ Item make_item(const Params& p, int64_t it, int lane) {
+  Item I;
+  I.row = it / p.nsplit;
+  const int split = (int)(it % p.nsplit);
+  I.b = I.row / p.Tq;
+  I.t = p.q_pos[I.row];
+  I.t_ok = I.t >= 0 && I.t < p.rope_rows;
+  I.ne = I.t_ok ? count_valid<DENSE>(p, I.row, I.t, lane) : 0;
+  const int64_t u_lo = I.t - p.W + 1 < 0 ? 0 : I.t - p.W + 1;
+  I.p0 = p.W > 0 ? p.swa_pos0[I.b] : 0;
+  I.w_lo = u_lo < I.p0 ? I.p0 : u_lo;
+  const int64_t w_hi = I.t < I.p0 + p.Ts - 1 ? I.t : I.p0 + p.Ts - 1;
+  I.nwin = (I.t_ok && p.W > 0 && w_hi >= I.w_lo) ? (int)(w_hi - I.w_lo + 1) : 0;
+  I.nkeys = I.ne + I.nwin;
+  const int ntiles = (I.nkeys + kTile - 1) / kTile;
+  const int per = (ntiles + p.nsplit - 1) / p.nsplit;
+  I.tlo = min(ntiles, split * per);
+  I.thi = min(ntiles, I.tlo + per);
+  I.key_hi = min(I.nkeys, I.thi * kTile);
+  return I;
+}
+
 template <bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __nv_bfloat16* __restrict__ q, const int64_t* __restrict__ q_pos, int64_t Tq,
-               const uint8_t* __restrict__ cache, int64_t N, int m, const int32_t* __restrict__ idx,
-               int k, const uint8_t* __restrict__ swa, const int64_t* __restrict__ swa_pos0,
-               int64_t Ts, int W, float scale_log2, const float* __restrict__ rcos,
-               const float* __restrict__ rsin, int64_t rope_rows, __nv_bfloat16* __restrict__ out,
-               float* __restrict__ lse, void* ws) {
+attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm + kQOff;
@@ -106,304 +270,535 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ q, const int64_t* __restrict__ 
   uint8_t* sP = sm + kPOff;
   Misc* ms = reinterpret_cast<Misc*>(sm + kMiscOff);
   int32_t* list = reinterpret_cast<int32_t*>(sm + kListOff);
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t row_q = blockIdx.x;
-  const int64_t b = row_q / Tq;
-  const int64_t t = q_pos[row_q];
-  const bool t_ok = t >= 0 && t < rope_rows;
 
-  // ---------------- set-up: key list, window range, Q with RoPE ----------------
   if (tid == 0) {
     ms->abort = 0;
-    ms->any_rescale[0] = 0;
-    ms->any_rescale[1] = 0;
-    if (!t_ok) flag_device_check(ws, 0x40000000u);
-    mbar_init(&ms->bar_full, 4);
-    mbar_init(&ms->bar_s, 1);
-    mbar_init(&ms->bar_p, 4);
-    mbar_init(&ms->bar_o, 1);
+    for (int i = 0; i < 4; ++i) ms->any_rescale[i] = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->kv_full[i], 4);
+      mbar_init(&ms->kv_empty[i], 1);
+      mbar_init(&ms->s_full[i], 1);
+      mbar_init(&ms->p_full[i], 4);
+    }
+    mbar_init(&ms->q_full, 1);
+    mbar_init(&ms->q_ready, 4);
+    mbar_init(&ms->q_empty, 1);
+    mbar_init(&ms->o_full, 1);
+    mbar_init(&ms->o_empty, 4);
+    mbar_init(&ms->sm_sync[0], 4);
+    mbar_init(&ms->sm_sync[1], 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->list_full[i], 1);
+      mbar_init(&ms->list_empty[i], 4);
+    }
     mbar_fence_init();
   }
-  int ne = 0;                       // entries in the key list (sparse) or visible (dense)
-  if (!DENSE) {
-    if (warp == 0 && t_ok) {        // ordered compaction of the valid selected entries
-      int cnt = 0;
-      for (int base = 0; base < k; base += 32) {
-        const int r = base + lane;
-        int32_t j = r < k ? idx[row_q * k + r] : -1;
-        if (j >= 0 && ((int64_t)j >= N || (int64_t)(j + 1) * m - 1 > t)) {
-          flag_device_check(ws, (unsigned)j);
-          j = -1;
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, j >= 0);
-        const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
-        if (j >= 0 && pos < kMaxList) list[pos] = j;
-        cnt += __popc(bal);
-      }
-      if (lane == 0) ms->nkeys = cnt < kMaxList ? cnt : kMaxList;
-    }
-  } else if (tid == 0) {
-    int64_t nv = t_ok ? (t + 1) / m : 0;
-    ms->nkeys = (int)(nv < N ? nv : N);
-  }
-  // window tokens u in [max(0, t-W+1), t] held by the window cache
-  int64_t u_lo = t - W + 1 < 0 ? 0 : t - W + 1;
-  const int64_t p0 = W > 0 ? swa_pos0[b] : 0;
-  int64_t w_lo = u_lo < p0 ? p0 : u_lo;
-  int64_t w_hi = t < p0 + Ts - 1 ? t : p0 + Ts - 1;
-  int nwin = (t_ok && W > 0 && w_hi >= w_lo) ? (int)(w_hi - w_lo + 1) : 0;
-  if (tid == 0 && t_ok && W > 0 && (w_lo > u_lo || w_hi < t)) flag_device_check(ws, 0x80000000u);
-  if (t_ok) {
-    // Q: 64 heads x 512 dims bf16 -> smem (8 chunks of 64 dims, SW128); RoPE on chunk 7
-    const uint4* qg = reinterpret_cast<const uint4*>(q + row_q * (int64_t)(kH * kD));
-    const float* cs = rcos + t * 32;
-    const float* sn = rsin + t * 32;
-    for (int v = tid; v < kH * kD / 8; v += kThreads) {
-      const int h = v >> 6, c16 = v & 63;       // 16-byte vector c16 of head h (8 dims)
-      uint4 x = qg[v];
-      if (c16 >= 56) {                          // dims 448..511: rotate 4 pairs
-        uint32_t wd[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int i = (c16 - 56) * 4 + p;     // pair index within the RoPE slice
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[p]));
-          const float y0 = __fsub_rn(__fmul_rn(f.x, cs[i]), __fmul_rn(f.y, sn[i]));
-          const float y1 = __fadd_rn(__fmul_rn(f.x, sn[i]), __fmul_rn(f.y, cs[i]));
-          const __nv_bfloat162 r = __floats2bfloat162_rn(y0, y1);
-          wd[p] = *reinterpret_cast<const uint32_t*>(&r);
-        }
-        x = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-      }
-      const int chunk = c16 >> 3, sub = c16 & 7;
-      *reinterpret_cast<uint4*>(sQ + chunk * 8192 + sw128(h, sub)) = x;
-    }
-  }
   if (warp == kMmaWarp) tmem_alloc(&ms->tmem, kTmemCols);
-  fence_proxy_async();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = ms->tmem;
-  ne = ms->nkeys;
-  const int nkeys = ne + nwin;
-  const int ntiles = (nkeys + kTile - 1) / kTile;
 
   if (warp >= 4 && warp < 8) {
-    // ============================ producers ============================
-    const int pw = warp - 4;
-    for (int i = 0; i < ntiles; ++i) {
-      if (i > 0 && !mbar_wait(&ms->bar_o, (i - 1) & 1, kWaitLimit)) {
+    // ================================ producers ================================
+    const int pw = warp - 4, ptid = tid - 128;
+    uint32_t g = 0, nq = 0;      // tiles and non-empty items produced so far
+    for (int64_t it = blockIdx.x; it < p.items && !ms->abort; it += gridDim.x) {
+      const Item I = make_item<DENSE>(p, it, lane);
+      if (I.thi <= I.tlo) continue;
+      if (pw == 0 && lane == 0 && it + gridDim.x < p.items) {   // warm L2 for the next item
+        const int64_t nrow = (it + gridDim.x) / p.nsplit;
+        if (nrow != I.row) {
+          prefetch_l2(p.q + nrow * (int64_t)(kH * kD), kH * kD * 2);
+          if (!DENSE && ((p.k * 4) & 15) == 0) prefetch_l2(p.idx + nrow * p.k, (uint32_t)p.k * 4);
+        }
+      }
+      // ordered list of the valid selected entries, built by producer warp 0
+      // into list buffer nq & 1 (the other buffer may still feed the
+      // previous item's last tiles)
+      int32_t* lst = list + (nq & 1) * kMaxList;
+      if (!DENSE) {
+        if (pw == 0) {
+          if (nq >= 2 && !mbar_wait(&ms->list_empty[nq & 1], ((nq >> 1) - 1) & 1, kWaitLimit)) {
+            ms->abort = 1;
+            flag_timeout(p.ws);
+            break;
+          }
+          int cnt = 0;
+          for (int base = 0; base < p.k; base += 32 * kIdxBatch) {
+            int32_t js[kIdxBatch];
+#pragma unroll
+            for (int i = 0; i < kIdxBatch; ++i) {
+              const int r = base + 32 * i + lane;
+              js[i] = r < p.k ? __ldg(p.idx + I.row * p.k + r) : -1;
+            }
+#pragma unroll
+            for (int i = 0; i < kIdxBatch; ++i) {
+              int32_t j = js[i];
+              if (j >= 0 && !entry_ok(j, I.t, p)) {
+                if (I.row * p.nsplit == it) flag_device_check(p.ws, (unsigned)j);   // once per row
+                j = -1;
+              }
+              const unsigned bal = __ballot_sync(0xffffffffu, j >= 0);
+              const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
+              if (j >= 0 && pos < kMaxList) lst[pos] = j;
+              cnt += __popc(bal);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ms->list_full[nq & 1]);
+        }
+        if (!mbar_wait(&ms->list_full[nq & 1], (nq >> 1) & 1, kWaitLimit)) {
+          ms->abort = 1;
+          flag_timeout(p.ws);
+          break;
+        }
+      }
+      // ---- the query: 64 heads x 512 dims -> smem, RoPE on dims 448..511 ----
+      if (nq > 0 && !mbar_wait(&ms->q_empty, (nq - 1) & 1, kWaitLimit)) {
         ms->abort = 1;
-        flag_timeout(ws);
+        flag_timeout(p.ws);
         break;
       }
-      if (ms->abort) break;
-      for (int r = pw; r < kTile; r += 4) {
-        const int key = i * kTile + r;
-        const uint8_t* row = nullptr;
-        if (key < ne) {
-          const int64_t j = DENSE ? (int64_t)key : (int64_t)list[key];
-          row = cache + ((size_t)b * N + j) * kMixRow;
-        } else if (key < nkeys) {
-          row = swa + ((size_t)b * Ts + (w_lo - p0 + (key - ne))) * kMixRow;
+      {
+        // TMA: 8 boxes of 64 heads x 64 dims, 128-byte swizzled, then RoPE
+        // of the last box (dims 448..511) in place
+        if (pw == 0 && lane == 0) {
+          mbar_arrive_expect_tx(&ms->q_full, kH * kD * 2);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) tma_load_2d(smem_u32(sQ + c * 8192), &tm_q, 64 * c, (int)(I.row * kH), &ms->q_full);
         }
-        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-        if (lane < 28) {
-          if (row) {
-            const uint4 c = __ldg(reinterpret_cast<const uint4*>(row) + lane);
-            const float sc = __ldg(reinterpret_cast<const float*>(row + kMixScaleOff) + (lane >> 3));
-            dequant16(c, sc, o0, o1);
-          }
-          const int chunk = lane >> 2, sub = 2 * (lane & 3);
-          uint8_t* dst = sKV + chunk * 16384;
-          *reinterpret_cast<uint4*>(dst + sw128(r, sub)) = o0;
-          *reinterpret_cast<uint4*>(dst + sw128(r, sub + 1)) = o1;
-        } else {
-          const int l4 = lane - 28;
-          if (row) {
-            o0 = __ldg(reinterpret_cast<const uint4*>(row + kMixRopeOff) + 2 * l4);
-            o1 = __ldg(reinterpret_cast<const uint4*>(row + kMixRopeOff) + 2 * l4 + 1);
-          }
-          uint8_t* dst = sKV + 7 * 16384;
-          *reinterpret_cast<uint4*>(dst + sw128(r, 2 * l4)) = o0;
-          *reinterpret_cast<uint4*>(dst + sw128(r, 2 * l4 + 1)) = o1;
+        if (!mbar_wait(&ms->q_full, nq & 1, kWaitLimit)) {
+          ms->abort = 1;
+          flag_timeout(p.ws);
+          break;
         }
+        const float* cs = p.rcos + (I.t_ok ? I.t : 0) * 32;
+        const float* sn = p.rsin + (I.t_ok ? I.t : 0) * 32;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = ptid + 128 * u, h = v >> 3, c = v & 7;
+          uint4* slot = reinterpret_cast<uint4*>(sQ + 7 * 8192 + sw128(h, c));
+          const uint4 x = *slot;
+          uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            const int i = c * 4 + pp;
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[pp]));
+            const float y0 = __fsub_rn(__fmul_rn(f.x, cs[i]), __fmul_rn(f.y, sn[i]));
+            const float y1 = __fadd_rn(__fmul_rn(f.x, sn[i]), __fmul_rn(f.y, cs[i]));
+            const __nv_bfloat162 r = __floats2bfloat162_rn(y0, y1);
+            wd[pp] = *reinterpret_cast<const uint32_t*>(&r);
+          }
+          *slot = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->q_ready);
       }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ms->bar_full);
+      ++nq;
+      // ---- key tiles ----
+      bool ok = true;
+      if (p.xcache) {
+        // bf16 rows are ready: each producer warp gathers 16 of the tile's 64
+        // rows with TMA (4 rows x 128 bytes per instruction, 8 column boxes)
+        for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
+          const int buf = g & 1;
+          if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * kD * 2);
+            const uint32_t kvb = smem_u32(sKV + buf * 65536);
+#pragma unroll 1
+            for (int grp = 0; grp < 4; ++grp) {
+              int y[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int r = 16 * pw + 4 * grp + e;
+                const int key = tl * kTile + r;
+                int64_t row = p.xrows;            // out of range: the box reads zeros
+                if (key < I.key_hi) {
+                  if (key < I.ne) row = (int64_t)I.b * p.N + (DENSE ? (int64_t)key : (int64_t)lst[key]);
+                  else row = p.xwin0 + (int64_t)I.b * p.Ts + (I.w_lo - I.p0 + (key - I.ne));
+                }
+                y[e] = (int)row;
+              }
+              const uint32_t roff = (uint32_t)(16 * pw + 4 * grp) * 128u;
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                tma_gather4(kvb + c * 8192 + roff, &tm_rows, 64 * c, y[0], y[1], y[2], y[3], &ms->kv_full[buf]);
+            }
+          }
+          __syncwarp();
+        }
+      } else {
+      for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
+        const int buf = g & 1;
+        const int kbase = tl * kTile;
+        uint4 c[16];
+        float sc[16];
+        const uint8_t* rowp[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          const int key = kbase + pw + 4 * rr;
+          const uint8_t* row = nullptr;
+          if (key < I.key_hi) {
+            if (key < I.ne) {
+              const int64_t j = DENSE ? (int64_t)key : (int64_t)lst[key];
+              row = p.cache + ((size_t)I.b * p.N + j) * kMixRow;
+            } else {
+              row = p.swa + ((size_t)I.b * p.Ts + (I.w_lo - I.p0 + (key - I.ne))) * kMixRow;
+            }
+          }
+          rowp[rr] = row;
+          c[rr] = make_uint4(0, 0, 0, 0);
+          sc[rr] = 0.0f;
+          if (lane < 28 && row) {
+            c[rr] = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+            sc[rr] = __ldg(reinterpret_cast<const float*>(row + kMixScaleOff) + (lane >> 3));
+          }
+        }
+        if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          break;
+        }
+        uint8_t* kv = sKV + buf * 65536;
+        const uint32_t aKV = smem_u32(kv);
+        if (lane >= 28) {                 // bf16 RoPE columns: async copies first
+          const int l4 = lane - 28;
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) {
+            const int r = pw + 4 * rr;
+            if (rowp[rr]) {
+              cp_async16(aKV + 7 * 8192 + sw128(r, 2 * l4), rowp[rr] + kMixRopeOff + 32 * l4);
+              cp_async16(aKV + 7 * 8192 + sw128(r, 2 * l4 + 1), rowp[rr] + kMixRopeOff + 32 * l4 + 16);
+            } else {
+              *reinterpret_cast<uint4*>(kv + 7 * 8192 + sw128(r, 2 * l4)) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(kv + 7 * 8192 + sw128(r, 2 * l4 + 1)) = make_uint4(0, 0, 0, 0);
+            }
+          }
+        } else {                          // FP8 columns: dequantise
+          uint8_t* dst = kv + (lane >> 2) * 8192;
+          const uint32_t sub = 2 * (lane & 3);
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) {
+            const int r = pw + 4 * rr;
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+            if (rowp[rr]) dequant16(c[rr], sc[rr], o0, o1);
+            *reinterpret_cast<uint4*>(dst + sw128(r, sub)) = o0;
+            *reinterpret_cast<uint4*>(dst + sw128(r, sub + 1)) = o1;
+          }
+        }
+        cp_async_wait_all();
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->kv_full[buf]);
+      }
+      }
+      if (!ok) {
+        ms->abort = 1;
+        flag_timeout(p.ws);
+        break;
+      }
+      if (!DENSE) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->list_empty[(nq - 1) & 1]);
+      }
     }
   } else if (warp == kMmaWarp) {
-    // ============================ MMA issue ============================
-    if (lane == 0) {
-      const uint32_t aQ = smem_u32(sQ), aKV = smem_u32(sKV), aP = smem_u32(sP);
-      constexpr uint32_t idQK = idesc_bf16(64, kTile, 0, 0);
-      constexpr uint32_t idPV = idesc_bf16(128, kH, 1, 0);
-      for (int i = 0; i < ntiles; ++i) {
-        if (!mbar_wait(&ms->bar_full, i & 1, kWaitLimit)) {
-          ms->abort = 1;
-          flag_timeout(ws);
-          break;
-        }
-        fence_after_sync();
-        const uint32_t dS = tmem + kTmemS + 128u * (i & 1);
-#pragma unroll 4
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk & 3) * 32u;
-          mma_bf16(dS, sdesc_sw128(aQ + (kk >> 2) * 8192 + off, 16, 1024),
-                   sdesc_sw128(aKV + (kk >> 2) * 16384 + off, 16, 1024), idQK, kk > 0);
-        }
-        mma_commit(&ms->bar_s);
-        if (!mbar_wait(&ms->bar_p, i & 1, kWaitLimit)) {
-          ms->abort = 1;
-          flag_timeout(ws);
-          break;
-        }
-        fence_after_sync();
-#pragma unroll 1
+    // ================================ MMA issue ================================
+    const uint32_t aQ = smem_u32(sQ), aKV = smem_u32(sKV), aP = smem_u32(sP);
+    constexpr uint32_t idQK = idesc_bf16(64, kTile, 0, 0);
+    constexpr uint32_t idPV = idesc_bf16(128, kH, 1, 0);
+    uint32_t g = 0, nq = 0;
+    int pend = -1;             // tile whose PV is not issued yet
+    bool pend_first = false, pend_last = false;
+    uint32_t pend_q = 0;       // ordinal of its item
+    bool ok = true;
+    auto do_pv = [&](uint32_t gg, bool first, bool last, uint32_t qord) -> bool {
+      if (!mbar_wait(&ms->p_full[gg & 1], (gg >> 1) & 1, kWaitLimit)) return false;
+      if (first && qord > 0 && !mbar_wait(&ms->o_empty, (qord - 1) & 1, kWaitLimit)) return false;
+      fence_after_sync();
+      {
+        const uint64_t vd0 = sdesc_sw128(aKV + (gg & 1) * 65536, 8192, 1024);
+        const uint64_t pd0 = sdesc_sw128(aP + (gg & 1) * 8192, 16, 1024);
+#pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks) {
-            const uint64_t a = sdesc_sw128(aKV + (2 * mt) * 16384 + ks * 2048, 16384, 1024);
-            const uint64_t bb = sdesc_sw128(aP + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-            mma_bf16(tmem + kTmemO + 64u * mt, a, bb, idPV, (i > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_bf16_elect(tmem + kTmemO + 64u * mt, vd0 + (uint64_t)((2 * mt * 8192 + ks * 2048) >> 4),
+                           pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!first || ks > 0) ? 1u : 0u);
+        }
+        mma_commit_elect(&ms->kv_empty[gg & 1]);
+        if (last) mma_commit_elect(&ms->o_full);
+      }
+      __syncwarp();
+      return true;
+    };
+    // next non-empty item at or after `it`
+    auto next_item = [&](int64_t it, Item& I) -> int64_t {
+      for (; it < p.items; it += gridDim.x) {
+        I = make_item<DENSE>(p, it, lane);
+        if (I.thi > I.tlo) return it;
+      }
+      return p.items;
+    };
+    Item I;
+    int64_t it = next_item(blockIdx.x, I);
+    while (it < p.items && ok && !ms->abort) {
+      if (!mbar_wait(&ms->q_ready, nq & 1, kWaitLimit)) {
+        ok = false;
+        break;
+      }
+      for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
+        if (!mbar_wait(&ms->kv_full[g & 1], (g >> 1) & 1, kWaitLimit)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        {
+          const uint32_t dS = tmem + kTmemS + 64u * (g & 1);
+          const uint64_t qd0 = sdesc_sw128(aQ, 16, 1024);
+          const uint64_t kd0 = sdesc_sw128(aKV + (g & 1) * 65536, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
+            mma_bf16_elect(dS, qd0 + off, kd0 + off, idQK, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_elect(&ms->s_full[g & 1]);
+          if (tl == I.thi - 1) mma_commit_elect(&ms->q_empty);
+        }
+        __syncwarp();
+        if (pend >= 0) {
+          ok = do_pv((uint32_t)pend, pend_first, pend_last, pend_q);
+          if (!ok) break;
+        }
+        pend = (int)g;
+        pend_first = tl == I.tlo;
+        pend_last = tl == I.thi - 1;
+        pend_q = nq;
+      }
+      if (!ok) break;
+      ++nq;
+      // describe the next item while the tensor core drains this one, then
+      // issue this item's last PV
+      Item J;
+      const int64_t it2 = next_item(it + gridDim.x, J);
+      if (pend >= 0) {
+        ok = do_pv((uint32_t)pend, pend_first, pend_last, pend_q);
+        pend = -1;
+      }
+      it = it2;
+      I = J;
+    }
+    if (ok && pend >= 0) ok = do_pv((uint32_t)pend, pend_first, pend_last, pend_q);
+    if (!ok) {
+      ms->abort = 1;
+      if (lane == 0) flag_timeout(p.ws);
+    }
+  } else {
+    // ============================ softmax / epilogue ============================
+    // S (64 heads x 64 keys) sits in lanes 0-15 of every TMEM quadrant; the
+    // 16x256b load spreads those 16 rows over all 32 lanes: lane t holds rows
+    // ra = t / 4 and rb = 8 + t / 4 of its quadrant, keys 8j + 2 (t % 4) and
+    // 8j + 2 (t % 4) + 1, j = 0..7.  Row maxima reduce over the 4 lanes of a
+    // row; row sums stay per lane until the epilogue.
+    const int qd = warp;
+    const int cq = 2 * (lane & 3);
+    const int ha = 16 * qd + (lane >> 2), hb = ha + 8;
+    const bool leader = (lane & 3) == 0;
+    const bool split = p.part_o != nullptr;
+    uint32_t g = 0, nq = 0, ns = 0;
+    for (int64_t it = blockIdx.x; it < p.items && !ms->abort; it += gridDim.x) {
+      const Item I = make_item<DENSE>(p, it, lane);
+      if (tid == 0 && I.row * p.nsplit == it) {
+        if (!I.t_ok) flag_device_check(p.ws, 0x40000000u);
+        const int64_t u_lo = I.t - p.W + 1 < 0 ? 0 : I.t - p.W + 1;
+        if (I.t_ok && p.W > 0 && I.nwin < I.t - u_lo + 1) flag_device_check(p.ws, 0x80000000u);
+      }
+      const float* cs = p.rcos + (I.t_ok ? I.t : 0) * 32;
+      const float* sn = p.rsin + (I.t_ok ? I.t : 0) * 32;
+      if (I.thi <= I.tlo) {           // no keys: zero output / empty partial state
+        if (split) {
+          for (int e = tid; e < kH * kD; e += 128) p.part_o[it * (kH * kD) + e] = 0.0f;
+          if (tid < kH) {
+            p.part_ml[(it * kH + tid) * 2] = -INFINITY;
+            p.part_ml[(it * kH + tid) * 2 + 1] = 0.0f;
+          }
+        } else {
+          for (int e = tid; e < kH * kD; e += 128) p.out[I.row * (kH * kD) + e] = __float2bfloat16_rn(0.0f);
+          if (p.lse && tid < kH) p.lse[I.row * kH + tid] = -INFINITY;
+        }
+        continue;
+      }
+      float ma = -INFINITY, mb = -INFINITY, la = 0.0f, lb = 0.0f;
+      bool ok = true;
+      for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
+        if (!mbar_wait(&ms->s_full[g & 1], (g >> 1) & 1, kWaitLimit)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const int nvalid = min(kTile, I.key_hi - tl * kTile);
+        uint32_t v[32];
+        tmem_ld16x256b_x8(tmem + ((uint32_t)(32 * qd) << 16) + kTmemS + 64u * (g & 1), v);
+        tmem_wait_ld();
+        float xa[16], xb[16];
+        float ta = -INFINITY, tb = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool valid = 8 * j + cq + e < nvalid;
+            xa[2 * j + e] = valid ? __uint_as_float(v[4 * j + e]) * p.scale_log2 : -INFINITY;
+            xb[2 * j + e] = valid ? __uint_as_float(v[4 * j + 2 + e]) * p.scale_log2 : -INFINITY;
+            ta = fmaxf(ta, xa[2 * j + e]);
+            tb = fmaxf(tb, xb[2 * j + e]);
           }
         }
-        mma_commit(&ms->bar_o);
+        ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 1));
+        ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 2));
+        tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 1));
+        tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 2));
+        const bool need_a = ta > ma + kLazy, need_b = tb > mb + kLazy;
+        const float na = need_a ? ta : ma, nb = need_b ? tb : mb;
+        const float aa = need_a ? exp2f(ma - na) : 1.0f;   // exp2(-inf) = 0 on the first tile
+        const float ab = need_b ? exp2f(mb - nb) : 1.0f;
+        if (tl > I.tlo) {
+          if (__any_sync(0xffffffffu, need_a || need_b) && lane == 0) atomicOr(&ms->any_rescale[g & 3], 1);
+          if (leader) {
+            ms->alpha[g & 1][ha] = aa;
+            ms->alpha[g & 1][hb] = ab;
+          }
+          if (!group_sync(ms, ns, lane)) {
+            ok = false;
+            break;
+          }
+          if (tid == 0) ms->any_rescale[(g + 2) & 3] = 0;   // slot of tile g + 2, read by nobody now
+          if (ms->any_rescale[g & 3]) {
+            // the previous tile's PV must be complete before O^T is touched
+            const uint32_t gp = g - 1;
+            if (!mbar_wait(&ms->kv_empty[gp & 1], (gp >> 1) & 1, kWaitLimit)) ok = false;
+            fence_after_sync();
+            if (ok) {
+#pragma unroll 1
+              for (int c = 0; c < 8; ++c) {
+                uint32_t o[32];
+                const uint32_t oa = tmem + ((uint32_t)(32 * qd) << 16) + kTmemO + 32u * c;
+                tmem_ld32(oa, o);
+                tmem_wait_ld();
+                const int h0 = 32 * (c & 1);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * ms->alpha[g & 1][h0 + j]);
+                tmem_st32(oa, o);
+              }
+              tmem_wait_st();
+            }
+          }
+          if (!ok) break;
+        }
+        ma = na;
+        mb = nb;
+        float sa = 0.0f, sb2 = 0.0f;
+        uint8_t* dst = sP + (g & 1) * 8192;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float pa0 = exp2f(xa[2 * j] - ma), pa1 = exp2f(xa[2 * j + 1] - ma);
+          const float pb0 = exp2f(xb[2 * j] - mb), pb1 = exp2f(xb[2 * j + 1] - mb);
+          sa += pa0 + pa1;
+          sb2 += pb0 + pb1;
+          const __nv_bfloat162 qa = __floats2bfloat162_rn(pa0, pa1);
+          const __nv_bfloat162 qb = __floats2bfloat162_rn(pb0, pb1);
+          *reinterpret_cast<uint32_t*>(dst + sw128(ha, j) + 2 * cq) = *reinterpret_cast<const uint32_t*>(&qa);
+          *reinterpret_cast<uint32_t*>(dst + sw128(hb, j) + 2 * cq) = *reinterpret_cast<const uint32_t*>(&qb);
+        }
+        la = la * aa + sa;
+        lb = lb * ab + sb2;
+        fence_proxy_async();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->p_full[g & 1]);
       }
-    }
-    __syncwarp();
-  } else {
-    // ============================ softmax ============================
-    const int qd = warp;                 // TMEM lane quadrant
-    const bool hv = s_row_valid(lane);
-    const int h = s_row(qd, lane);
-    float m_run = -INFINITY, l_run = 0.0f;
-    for (int i = 0; i < ntiles; ++i) {
-      if (!mbar_wait(&ms->bar_s, i & 1, kWaitLimit)) {
+      if (!ok) {
         ms->abort = 1;
-        flag_timeout(ws);
+        flag_timeout(p.ws);
+        break;
+      }
+      // ---- epilogue: the item's O^T is complete after its last PV ----
+      la += __shfl_xor_sync(0xffffffffu, la, 1);
+      la += __shfl_xor_sync(0xffffffffu, la, 2);
+      lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+      lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+      if (!mbar_wait(&ms->o_full, nq & 1, kWaitLimit)) {
+        ms->abort = 1;
+        flag_timeout(p.ws);
         break;
       }
       fence_after_sync();
-      const int nvalid = min(kTile, nkeys - i * kTile);
-      const uint32_t sbase = tmem + ((uint32_t)(32 * qd) << 16) + kTmemS + 128u * (i & 1);
-      // pass 1: tile max
-      float tmax = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < kTile; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(sbase + c, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c + j < nvalid) tmax = fmaxf(tmax, __uint_as_float(v[j]) * scale_log2);
-      }
-      const bool need = hv && tmax > m_run + kLazy;
-      const float m_new = need ? tmax : m_run;
-      const float alpha = need ? exp2f(m_run - m_new) : 1.0f;   // exp2(-inf) = 0 on the first tile
-      if (i > 0) {
-        // rescale O^T when any head's running max jumped
-        if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&ms->any_rescale[i & 1], 1);
-        if (hv) ms->alpha[h] = alpha;
-        named_bar_sync(1, 128);
-        if (tid == 0) ms->any_rescale[(i + 1) & 1] = 0;
-        if (ms->any_rescale[i & 1]) {
-          float al[kH];
-#pragma unroll
-          for (int hh = 0; hh < kH; ++hh) al[hh] = ms->alpha[hh];
-#pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint32_t v[32];
-              const uint32_t oa = tmem + ((uint32_t)(32 * qd) << 16) + kTmemO + 64u * mt + 32u * half;
-              tmem_ld32(oa, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * al[32 * half + j]);
-              tmem_st32(oa, v);
-            }
-          }
-          tmem_wait_st();
-        }
-        named_bar_sync(1, 128);
-      }
-      m_run = m_new;
-      // pass 2: probabilities -> bf16 P rows (head h, 128 keys), row sums
-      float psum = 0.0f;
-#pragma unroll 1
-      for (int c = 0; c < kTile; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(sbase + c, v);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = (c + j < nvalid) ? exp2f(__uint_as_float(v[j]) * scale_log2 - m_run) : 0.0f;
-          const float p1 = (c + j + 1 < nvalid) ? exp2f(__uint_as_float(v[j + 1]) * scale_log2 - m_run) : 0.0f;
-          psum += p0 + p1;
-          const __nv_bfloat162 bp = __floats2bfloat162_rn(p0, p1);
-          pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&bp);
-        }
-        if (hv) {
-          uint8_t* dst = sP + (c >> 6) * 8192;
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint32_t sub = ((c & 63) >> 3) + s;
-            *reinterpret_cast<uint4*>(dst + sw128(h, sub)) =
-                make_uint4(pk[4 * s], pk[4 * s + 1], pk[4 * s + 2], pk[4 * s + 3]);
-          }
+      if (leader) {
+        ms->lsum[ha] = la > 0.0f ? 1.0f / la : 0.0f;   // per-head 1/sum for every lane
+        ms->lsum[hb] = lb > 0.0f ? 1.0f / lb : 0.0f;
+        if (split) {
+          p.part_ml[(it * kH + ha) * 2] = ma;
+          p.part_ml[(it * kH + ha) * 2 + 1] = la;
+          p.part_ml[(it * kH + hb) * 2] = mb;
+          p.part_ml[(it * kH + hb) * 2 + 1] = lb;
+        } else if (p.lse) {
+          p.lse[I.row * kH + ha] = la > 0.0f ? (ma + log2f(la)) * 0.69314718055994531f : -INFINITY;
+          p.lse[I.row * kH + hb] = lb > 0.0f ? (mb + log2f(lb)) * 0.69314718055994531f : -INFINITY;
         }
       }
-      l_run = l_run * alpha + psum;
-      fence_proxy_async();
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ms->bar_p);
-    }
-    // ============================ epilogue ============================
-    if (hv) ms->l_fin[h] = l_run;
-    if (hv && lse) lse[row_q * kH + h] = l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-    bool ok = ntiles > 0;
-    if (ok && !mbar_wait(&ms->bar_o, (ntiles - 1) & 1, kWaitLimit)) {
-      ms->abort = 1;
-      flag_timeout(ws);
-      ok = false;
-    }
-    named_bar_sync(1, 128);
-    fence_after_sync();
-    float inv[kH];
-#pragma unroll
-    for (int hh = 0; hh < kH; ++hh) inv[hh] = (ok && ms->l_fin[hh] > 0.0f) ? 1.0f / ms->l_fin[hh] : 0.0f;
-    const float* cs = rcos + (t_ok ? t : 0) * 32;
-    const float* sn = rsin + (t_ok ? t : 0) * 32;
-    __nv_bfloat16* og = out + row_q * (int64_t)(kH * kD);
+      if (!group_sync(ms, ns, lane)) {
+        ms->abort = 1;
+        flag_timeout(p.ws);
+        break;
+      }
+      if (split) {
+        float* po = p.part_o + it * (int64_t)(kH * kD);
 #pragma unroll 1
-    for (int mt = 0; mt < 4; ++mt) {
-      const int d = 128 * mt + 32 * qd + lane;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        if (ok) {
-          tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + kTmemO + 64u * mt + 32u * half, v);
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + kTmemO + 32u * c, o);
           tmem_wait_ld();
-        } else {
+          const int d = 128 * (c >> 1) + 32 * qd + lane;
+          const int h0 = 32 * (c & 1);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0u;
+          for (int j = 0; j < 32; ++j) po[(h0 + j) * kD + d] = __uint_as_float(o[j]);
         }
+      } else {
+        __nv_bfloat16* og = p.out + I.row * (int64_t)(kH * kD);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + kTmemO + 32u * c, o);
+          tmem_wait_ld();
+          const int d = 128 * (c >> 1) + 32 * qd + lane;
+          const int h0 = 32 * (c & 1);
+          const bool rope = d >= kMixDn;          // warp-uniform
+          const int pi = rope ? (d - kMixDn) >> 1 : 0;
+          const float cc = rope ? cs[pi] : 1.0f, ss = rope ? sn[pi] : 0.0f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float o = __uint_as_float(v[j]) * inv[32 * half + j];
-          if (d >= kMixDn) {          // inverse rotation of the RoPE dims (pairs in adjacent lanes)
-            const float other = __shfl_xor_sync(0xffffffffu, o, 1);
-            const int pi = (d - kMixDn) >> 1;
-            o = (d & 1) ? (-other * sn[pi] + o * cs[pi]) : (o * cs[pi] + other * sn[pi]);
+          for (int j = 0; j < 32; ++j) {
+            float o1 = __uint_as_float(o[j]) * ms->lsum[h0 + j];
+            if (rope) {
+              const float other = __shfl_xor_sync(0xffffffffu, o1, 1);
+              o1 = (d & 1) ? (-other * ss + o1 * cc) : (o1 * cc + other * ss);
+            }
+            og[(h0 + j) * kD + d] = __float2bfloat16_rn(o1);
           }
-          og[(32 * half + j) * kD + d] = __float2bfloat16_rn(o);
         }
       }
+      fence_before_sync();
+      if (!group_sync(ms, ns, lane)) {      // every O^T read done; lsum free again
+        ms->abort = 1;
+        flag_timeout(p.ws);
+        break;
+      }
+      if (lane == 0) mbar_arrive(&ms->o_empty);
+      ++nq;
     }
   }
   fence_before_sync();
@@ -414,32 +809,207 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ q, const int64_t* __restrict__ 
   }
 }
 
+// Merge the split partial softmax states of one query row into out and lse.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const Params p) {
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int64_t t = p.q_pos[row];
+  const bool t_ok = t >= 0 && t < p.rope_rows;
+  const float* cs = p.rcos + (t_ok ? t : 0) * 32;
+  const float* sn = p.rsin + (t_ok ? t : 0) * 32;
+  const int d0 = 2 * tid;   // dims d0, d0 + 1 (a RoPE pair when d0 >= 448)
+  for (int h = 0; h < kH; ++h) {
+    float M = -INFINITY;
+    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.part_ml[((row * p.nsplit + s) * kH + h) * 2]);
+    float L = 0.0f, o0 = 0.0f, o1 = 0.0f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < p.nsplit; ++s) {
+        const int64_t it = row * p.nsplit + s;
+        const float mi = p.part_ml[(it * kH + h) * 2];
+        if (mi == -INFINITY) continue;
+        const float w = exp2f(mi - M);
+        L += w * p.part_ml[(it * kH + h) * 2 + 1];
+        const float2 v = *reinterpret_cast<const float2*>(p.part_o + it * (int64_t)(kH * kD) + h * kD + d0);
+        o0 += w * v.x;
+        o1 += w * v.y;
+      }
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    o0 *= inv;
+    o1 *= inv;
+    if (d0 >= kMixDn) {
+      const int pi = (d0 - kMixDn) >> 1;
+      const float y0 = o0 * cs[pi] + o1 * sn[pi];
+      const float y1 = -o0 * sn[pi] + o1 * cs[pi];
+      o0 = y0;
+      o1 = y1;
+    }
+    *reinterpret_cast<__nv_bfloat162*>(p.out + row * (int64_t)(kH * kD) + h * kD + d0) =
+        __floats2bfloat162_rn(o0, o1);
+    if (tid == 0 && p.lse) p.lse[row * kH + h] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// Split count: 1 when there are enough rows to fill the GPU, else enough
+// splits to give every SM an item (at most one per 64-key tile).
+int choose_splits(int64_t rows, int64_t max_keys) {
+  const int sms = num_sms();
+  if (rows >= sms) return 1;
+  const int64_t tiles = (max_keys + kTile - 1) / kTile;
+  int64_t s = (sms + rows - 1) / rows;
+  if (s > tiles) s = tiles;
+  return (int)(s < 1 ? 1 : s);
+}
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// How a call runs: the split count (partial states in the workspace) and
+// whether the cache and window rows are first expanded to bf16 in the
+// workspace -- worth it when every row serves many queries (prefill), not
+// when each is read about once (decode).
+struct Plan {
+  int nsplit;
+  bool expand;
+  size_t part_bytes, x_bytes;
+};
+
+Plan make_plan(int B, int64_t Tq, int64_t max_keys, int64_t N, int64_t Ts) {
+  Plan pl;
+  const int64_t rows = (int64_t)B * Tq;
+  pl.nsplit = choose_splits(rows, max_keys);
+  pl.part_bytes = pl.nsplit > 1 ? al256((size_t)rows * pl.nsplit * ((size_t)kH * kD * 4 + (size_t)kH * 2 * 4)) : 0;
+  const double uses = (double)rows * (double)max_keys;
+  const double nrows = (double)B * (double)(N + Ts);
+  pl.expand = nrows > 0 && uses >= 8.0 * nrows;
+  pl.x_bytes = pl.expand ? al256((size_t)B * (size_t)(N + Ts) * kD * 2) : 0;
+  return pl;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver once
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// Tensor map over bf16 rows of 512 (1 KiB apart): boxes of 64 columns x box_rows
+// rows, 128-byte swizzle, zero fill outside.
+bool make_row_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
-size_t attn_tc_workspace(int, int64_t, int, int, int64_t) { return 0; }
+size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys, int64_t N, int64_t Ts) {
+  if (H != kH || D != kD) return 0;
+  const Plan pl = make_plan(B, Tq, max_keys, N, Ts);
+  return pl.part_bytes + pl.x_bytes;
+}
 
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
   const int64_t rows = (int64_t)a.B * a.Tq;
   if (rows == 0) return cudaSuccess;
   if (a.H != kH || a.D != kD || a.R != 64) return launch_attn_simt(a, st);
   if (a.idx && a.k > kMaxList) return launch_attn_simt(a, st);
-  const size_t smem = kSmemLimit;
-  const float scale_log2 = a.scale * 1.4426950408889634f;
-  if (a.idx) {
-    cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attn_tc_kernel<false><<<(unsigned)rows, kThreads, smem, st>>>(
-        reinterpret_cast<const __nv_bfloat16*>(a.q), a.q_pos, a.Tq,
-        reinterpret_cast<const uint8_t*>(a.cache), a.N, a.m, a.idx, a.k,
-        reinterpret_cast<const uint8_t*>(a.swa), a.swa_pos0, a.Ts, a.W, scale_log2, a.rcos, a.rsin,
-        a.rope_rows, reinterpret_cast<__nv_bfloat16*>(a.out), a.lse, a.ws);
-  } else {
-    cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attn_tc_kernel<true><<<(unsigned)rows, kThreads, smem, st>>>(
-        reinterpret_cast<const __nv_bfloat16*>(a.q), a.q_pos, a.Tq,
-        reinterpret_cast<const uint8_t*>(a.cache), a.N, a.m, nullptr, 0,
-        reinterpret_cast<const uint8_t*>(a.swa), a.swa_pos0, a.Ts, a.W, scale_log2, a.rcos, a.rsin,
-        a.rope_rows, reinterpret_cast<__nv_bfloat16*>(a.out), a.lse, a.ws);
+  Params p;
+  p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  p.q_pos = a.q_pos;
+  p.Tq = a.Tq;
+  p.cache = reinterpret_cast<const uint8_t*>(a.cache);
+  p.N = a.N;
+  p.m = a.m;
+  p.idx = a.idx;
+  p.k = a.idx ? a.k : 0;
+  p.swa = reinterpret_cast<const uint8_t*>(a.swa);
+  p.swa_pos0 = a.swa_pos0;
+  p.Ts = a.Ts;
+  p.W = a.W;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.rcos = a.rcos;
+  p.rsin = a.rsin;
+  p.rope_rows = a.rope_rows;
+  p.out = reinterpret_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.ws = a.ws;
+  p.part_o = nullptr;
+  p.part_ml = nullptr;
+  p.xcache = nullptr;
+  p.xswa = nullptr;
+  Plan pl = make_plan(a.B, a.Tq, a.max_keys, a.N, a.W > 0 ? a.Ts : 0);
+  size_t avail = a.ws_bytes > csa::kWsHeader ? a.ws_bytes - csa::kWsHeader : 0;
+  uint8_t* base = reinterpret_cast<uint8_t*>(a.ws) + csa::kWsHeader;
+  if (pl.nsplit > 1 && pl.part_bytes > avail) {   // too little scratch: no split
+    pl.nsplit = 1;
+    pl.part_bytes = 0;
   }
+  if (pl.expand && pl.part_bytes + pl.x_bytes > avail) pl.expand = false;
+  p.nsplit = pl.nsplit;
+  p.items = rows * p.nsplit;
+  if (p.nsplit > 1) {
+    p.part_o = reinterpret_cast<float*>(base);
+    p.part_ml = reinterpret_cast<float*>(base + (size_t)p.items * kH * kD * 4);
+    base += pl.part_bytes;
+  }
+  CUtensorMap tm_q, tm_rows;
+  if (!make_row_map(&tm_q, a.q, (uint64_t)rows * kH, 64)) return cudaErrorInvalidValue;
+  tm_rows = tm_q;
+  p.xrows = 0;
+  p.xwin0 = 0;
+  if (pl.expand) {
+    const int64_t nc = (int64_t)a.B * a.N, nw = (a.W > 0) ? (int64_t)a.B * a.Ts : 0;
+    __nv_bfloat16* xc = reinterpret_cast<__nv_bfloat16*>(base);
+    __nv_bfloat16* xs = xc + nc * kD;
+    if (nc > 0) expand_rows_kernel<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(p.cache, nc, xc);
+    if (nw > 0) expand_rows_kernel<<<(unsigned)((nw + 7) / 8), 256, 0, st>>>(p.swa, nw, xs);
+    p.xcache = xc;
+    p.xswa = xs;
+    p.xrows = nc + nw;
+    p.xwin0 = nc;
+    if (!make_row_map(&tm_rows, xc, (uint64_t)(nc + nw), 1)) return cudaErrorInvalidValue;
+  }
+  const int grid = (int)(p.items < num_sms() ? p.items : num_sms());
+  if (a.idx) {
+    cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q);
+  } else {
+    cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.nsplit == 1) return e;
+  attn_combine_kernel<<<(unsigned)rows, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -97,8 +97,8 @@ def test_validation_errors_before_launch(csa):
                          ctypes.c_void_p(16), ctypes.c_void_p(16), 1, ctypes.c_void_p(16), None, ws,
                          1 << 20, None)
     assert r == -2
-    assert L.csa_workspace_size(99, 1, 1, 1, 1, 1, 1, 1) == -1
-    assert L.csa_workspace_size(1, 1, 8, 2048, 512, 0, 0, 0) >= 256 + 8 * 2048 * 4
+    assert L.csa_workspace_size(99, 1, 1, 1, 1, 1, 1, 1, 0) == -1
+    assert L.csa_workspace_size(1, 1, 8, 2048, 512, 0, 0, 0, 0) >= 256 + 8 * 2048 * 4
 
 
 def test_binding_requires_cuda_tensors(csa):

@@ -434,3 +434,30 @@ def test_simt_and_tc_kernels_agree(csa, oracle_mod, monkeypatch):
     assert max_rel_err(tc.cpu().numpy()[:, rows], ref) <= 1e-2
     assert max_rel_err(simt.cpu().numpy()[:, rows], ref) <= 1e-2
     assert float((tc - simt).abs().max()) <= 1e-2 * float(simt.abs().max())
+
+
+def test_tc_dequant_is_exact(csa, oracle_mod):
+    """One selected key and no window: softmax weight 1, so the FP8 columns of
+    the output are the dequantised key itself (bf16 of code x 2^e, exact)."""
+    from gpu_common import dev_bf16
+    rng = np.random.default_rng(90)
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    exps = [-117, -60, -20, -9, -7, -1, 0, 3, 7, 8, 10]
+    n = len(exps) * 2
+    rows = np.zeros((1, n, 592), np.uint8)
+    for r in range(n):
+        rows[0, r, :448] = np.roll(np.resize(codes, 448), 37 * r)
+        e = exps[r % len(exps)]
+        sc = np.array([2.0 ** e, 2.0 ** (e - (r & 1)), 2.0 ** min(e + 1, 10), 2.0 ** e], np.float32)
+        rows[0, r, 576:592] = sc.view(np.uint8)
+        rows[0, r, 448:576] = wl.f32_to_bf16_bits(rng.standard_normal(64).astype(np.float32)).view(np.uint8)
+    m, T = 1, n
+    rope_np, rope_dev = ropes(csa, oracle_mod, T + 1)
+    q = wl.f32_to_bf16_bits(rng.standard_normal((1, n, 64, 512)).astype(np.float32))
+    q_pos = np.arange(n, dtype=np.int64)[None]
+    idx = np.arange(n, dtype=np.int32)[None, :, None]               # query r selects entry r only
+    out = csa.sparse_mqa(dev_bf16(q), dev(q_pos), dev(rows), m, dev(idx), dev(rows), dev(np.zeros(1, np.int64)),
+                         0, 0.05, rope_dev).float().cpu().numpy()
+    want = oracle_mod.unpack_mixed(rows)[0, :, :448]
+    for r in range(n):
+        np.testing.assert_array_equal(out[0, r, :, :448], np.broadcast_to(want[r], (64, 448)))
