@@ -141,14 +141,14 @@ int csa_rope_table(int64_t P, int R, double base, float* cos_out, float* sin_out
 
 int64_t csa_workspace_size(int op, int B, int64_t Tq, int64_t N, int k, int H, int D,
                            int64_t max_keys, int64_t Ts) {
-  (void)k;
   if (B < 0 || Tq < 0 || N < 0) return -1;
   switch (op) {
     case CSA_OP_INDEXER_TOPK:
       return (int64_t)indexer_ws(B, Tq, N);
     case CSA_OP_SPARSE_MQA:
     case CSA_OP_HCA_DENSE:
-      return (int64_t)(csa::kWsHeader + align256(csa::attn_tc_workspace(B, Tq, H, D, max_keys, N, Ts)));
+      return (int64_t)(csa::kWsHeader +
+                       align256(csa::attn_tc_workspace(B, Tq, H, D, max_keys, N, Ts, op == CSA_OP_SPARSE_MQA ? k : 0)));
     default:
       return -1;
   }

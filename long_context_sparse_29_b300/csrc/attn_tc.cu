@@ -197,6 +197,9 @@ struct Params {
   const __nv_bfloat16* xswa;     // bf16 copy of the window rows [B, Ts, 512]
   int64_t xrows;                 // rows of the bf16 copy (cache rows, then window rows)
   int64_t xwin0;                 // first window row in the copy (= B * N)
+  const int32_t* clist;          // [rows, kpad] valid selected entries of each row, in idx order
+  const int32_t* ccount;         // [rows] their number
+  int kpad;                      // row stride of clist (multiple of 4)
 };
 
 // Keys of one work item: entries first (selected, in idx order, or all
@@ -245,7 +248,7 @@ __device__ __forceinline__ Item make_item(const Params& p, int64_t it, int lane)
   I.b = I.row / p.Tq;
   I.t = p.q_pos[I.row];
   I.t_ok = I.t >= 0 && I.t < p.rope_rows;
-  I.ne = I.t_ok ? count_valid<DENSE>(p, I.row, I.t, lane) : 0;
+  I.ne = !I.t_ok ? 0 : DENSE ? count_valid<DENSE>(p, I.row, I.t, lane) : min(p.ccount[I.row], kMaxList);
   const int64_t u_lo = I.t - p.W + 1 < 0 ? 0 : I.t - p.W + 1;
   I.p0 = p.W > 0 ? p.swa_pos0[I.b] : 0;
   I.w_lo = u_lo < I.p0 ? I.p0 : u_lo;
@@ -258,6 +261,39 @@ __device__ __forceinline__ Item make_item(const Params& p, int64_t it, int lane)
   I.thi = min(ntiles, I.tlo + per);
   I.key_hi = min(I.nkeys, I.thi * kTile);
   return I;
+}
+
+// Ordered compaction of each row's valid selected entries (idx >= 0, < N,
+// block complete at the query's position); invalid ones set the device-check
+// flag.  One warp per query row.
+__global__ void __launch_bounds__(256)
+compact_idx_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ q_pos, int64_t rows, int k,
+                   int kpad, int64_t N, int m, int64_t rope_rows, int32_t* __restrict__ clist,
+                   int32_t* __restrict__ ccount, void* ws) {
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int64_t t = q_pos[row];
+  const bool t_ok = t >= 0 && t < rope_rows;
+  int cnt = 0;
+  for (int base = 0; base < k; base += 32 * kIdxBatch) {
+    int32_t js[kIdxBatch];
+#pragma unroll
+    for (int i = 0; i < kIdxBatch; ++i) {
+      const int r = base + 32 * i + lane;
+      js[i] = r < k ? __ldg(idx + row * k + r) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kIdxBatch; ++i) {
+      const int32_t j = js[i];
+      const bool ok = t_ok && j >= 0 && (int64_t)j < N && (int64_t)(j + 1) * m - 1 <= t;
+      if (t_ok && j >= 0 && !ok) flag_device_check(ws, (unsigned)j);
+      const unsigned bal = __ballot_sync(0xffffffffu, ok);
+      if (ok) clist[row * kpad + cnt + __popc(bal & ((1u << lane) - 1u))] = j;
+      cnt += __popc(bal);
+    }
+  }
+  if (lane == 0) ccount[row] = cnt;
 }
 
 template <bool DENSE>
@@ -314,42 +350,22 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
           if (!DENSE && ((p.k * 4) & 15) == 0) prefetch_l2(p.idx + nrow * p.k, (uint32_t)p.k * 4);
         }
       }
-      // ordered list of the valid selected entries, built by producer warp 0
-      // into list buffer nq & 1 (the other buffer may still feed the
-      // previous item's last tiles)
+      // the row's compacted entry list -> smem buffer nq & 1 (the other buffer
+      // may still feed the previous item's last tiles)
       int32_t* lst = list + (nq & 1) * kMaxList;
       if (!DENSE) {
-        if (pw == 0) {
+        if (pw == 0 && lane == 0) {
           if (nq >= 2 && !mbar_wait(&ms->list_empty[nq & 1], ((nq >> 1) - 1) & 1, kWaitLimit)) {
             ms->abort = 1;
             flag_timeout(p.ws);
-            break;
+          } else {
+            const uint32_t bytes = (uint32_t)((I.ne + 3) & ~3) * 4u;
+            mbar_arrive_expect_tx(&ms->list_full[nq & 1], bytes);
+            if (bytes) bulk_copy_g2s(smem_u32(lst), p.clist + I.row * p.kpad, bytes, &ms->list_full[nq & 1]);
           }
-          int cnt = 0;
-          for (int base = 0; base < p.k; base += 32 * kIdxBatch) {
-            int32_t js[kIdxBatch];
-#pragma unroll
-            for (int i = 0; i < kIdxBatch; ++i) {
-              const int r = base + 32 * i + lane;
-              js[i] = r < p.k ? __ldg(p.idx + I.row * p.k + r) : -1;
-            }
-#pragma unroll
-            for (int i = 0; i < kIdxBatch; ++i) {
-              int32_t j = js[i];
-              if (j >= 0 && !entry_ok(j, I.t, p)) {
-                if (I.row * p.nsplit == it) flag_device_check(p.ws, (unsigned)j);   // once per row
-                j = -1;
-              }
-              const unsigned bal = __ballot_sync(0xffffffffu, j >= 0);
-              const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
-              if (j >= 0 && pos < kMaxList) lst[pos] = j;
-              cnt += __popc(bal);
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ms->list_full[nq & 1]);
         }
-        if (!mbar_wait(&ms->list_full[nq & 1], (nq >> 1) & 1, kWaitLimit)) {
+        __syncwarp();
+        if (ms->abort || !mbar_wait(&ms->list_full[nq & 1], (nq >> 1) & 1, kWaitLimit)) {
           ms->abort = 1;
           flag_timeout(p.ws);
           break;
@@ -364,10 +380,10 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
       {
         // TMA: 8 boxes of 64 heads x 64 dims, 128-byte swizzled, then RoPE
         // of the last box (dims 448..511) in place
-        if (pw == 0 && lane == 0) {
-          mbar_arrive_expect_tx(&ms->q_full, kH * kD * 2);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) tma_load_2d(smem_u32(sQ + c * 8192), &tm_q, 64 * c, (int)(I.row * kH), &ms->q_full);
+        if (pw == 0) {
+          if (lane == 0) mbar_arrive_expect_tx(&ms->q_full, kH * kD * 2);
+          __syncwarp();
+          if (lane < 8) tma_load_2d(smem_u32(sQ + lane * 8192), &tm_q, 64 * lane, (int)(I.row * kH), &ms->q_full);
         }
         if (!mbar_wait(&ms->q_full, nq & 1, kWaitLimit)) {
           ms->abort = 1;
@@ -409,28 +425,24 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
             ok = false;
             break;
           }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * kD * 2);
-            const uint32_t kvb = smem_u32(sKV + buf * 65536);
-#pragma unroll 1
-            for (int grp = 0; grp < 4; ++grp) {
-              int y[4];
+          if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * kD * 2);
+          __syncwarp();
+          {
+            // lane: 4-row group (lane / 8) of this warp's 16 rows, column box lane % 8
+            const int r0 = 16 * pw + 4 * (lane >> 3), cb = lane & 7;
+            int y[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int r = 16 * pw + 4 * grp + e;
-                const int key = tl * kTile + r;
-                int64_t row = p.xrows;            // out of range: the box reads zeros
-                if (key < I.key_hi) {
-                  if (key < I.ne) row = (int64_t)I.b * p.N + (DENSE ? (int64_t)key : (int64_t)lst[key]);
-                  else row = p.xwin0 + (int64_t)I.b * p.Ts + (I.w_lo - I.p0 + (key - I.ne));
-                }
-                y[e] = (int)row;
+            for (int e = 0; e < 4; ++e) {
+              const int key = tl * kTile + r0 + e;
+              int64_t row = p.xrows;            // out of range: the box reads zeros
+              if (key < I.key_hi) {
+                if (key < I.ne) row = (int64_t)I.b * p.N + (DENSE ? (int64_t)key : (int64_t)lst[key]);
+                else row = p.xwin0 + (int64_t)I.b * p.Ts + (I.w_lo - I.p0 + (key - I.ne));
               }
-              const uint32_t roff = (uint32_t)(16 * pw + 4 * grp) * 128u;
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                tma_gather4(kvb + c * 8192 + roff, &tm_rows, 64 * c, y[0], y[1], y[2], y[3], &ms->kv_full[buf]);
+              y[e] = (int)row;
             }
+            tma_gather4(smem_u32(sKV + buf * 65536) + cb * 8192 + (uint32_t)r0 * 128u, &tm_rows, 64 * cb, y[0], y[1],
+                        y[2], y[3], &ms->kv_full[buf]);
           }
           __syncwarp();
         }
@@ -881,12 +893,15 @@ size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Plan {
   int nsplit;
   bool expand;
-  size_t part_bytes, x_bytes;
+  int kpad;
+  size_t list_bytes, part_bytes, x_bytes;
 };
 
-Plan make_plan(int B, int64_t Tq, int64_t max_keys, int64_t N, int64_t Ts) {
+Plan make_plan(int B, int64_t Tq, int64_t max_keys, int64_t N, int64_t Ts, int k) {
   Plan pl;
   const int64_t rows = (int64_t)B * Tq;
+  pl.kpad = (k + 3) & ~3;
+  pl.list_bytes = k > 0 ? al256((size_t)rows * pl.kpad * 4) + al256((size_t)rows * 4) : 0;
   pl.nsplit = choose_splits(rows, max_keys);
   pl.part_bytes = pl.nsplit > 1 ? al256((size_t)rows * pl.nsplit * ((size_t)kH * kD * 4 + (size_t)kH * 2 * 4)) : 0;
   const double uses = (double)rows * (double)max_keys;
@@ -932,10 +947,10 @@ bool make_row_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_
 
 }  // namespace
 
-size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys, int64_t N, int64_t Ts) {
+size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys, int64_t N, int64_t Ts, int k) {
   if (H != kH || D != kD) return 0;
-  const Plan pl = make_plan(B, Tq, max_keys, N, Ts);
-  return pl.part_bytes + pl.x_bytes;
+  const Plan pl = make_plan(B, Tq, max_keys, N, Ts, k);
+  return pl.list_bytes + pl.part_bytes + pl.x_bytes;
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
@@ -967,9 +982,23 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
   p.part_ml = nullptr;
   p.xcache = nullptr;
   p.xswa = nullptr;
-  Plan pl = make_plan(a.B, a.Tq, a.max_keys, a.N, a.W > 0 ? a.Ts : 0);
+  Plan pl = make_plan(a.B, a.Tq, a.max_keys, a.N, a.W > 0 ? a.Ts : 0, a.idx ? a.k : 0);
   size_t avail = a.ws_bytes > csa::kWsHeader ? a.ws_bytes - csa::kWsHeader : 0;
   uint8_t* base = reinterpret_cast<uint8_t*>(a.ws) + csa::kWsHeader;
+  if (pl.list_bytes > avail) return launch_attn_simt(a, st);   // no room for the entry lists
+  p.kpad = pl.kpad;
+  p.clist = nullptr;
+  p.ccount = nullptr;
+  if (a.idx) {
+    int32_t* cl = reinterpret_cast<int32_t*>(base);
+    int32_t* cc = reinterpret_cast<int32_t*>(base + al256((size_t)rows * pl.kpad * 4));
+    compact_idx_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a.idx, a.q_pos, rows, a.k, pl.kpad, a.N, a.m,
+                                                                  a.rope_rows, cl, cc, a.ws);
+    p.clist = cl;
+    p.ccount = cc;
+    base += pl.list_bytes;
+    avail -= pl.list_bytes;
+  }
   if (pl.nsplit > 1 && pl.part_bytes > avail) {   // too little scratch: no split
     pl.nsplit = 1;
     pl.part_bytes = 0;

@@ -46,6 +46,6 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
                                 float* score_out, float* scores_ws, cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st);
-size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys, int64_t N, int64_t Ts);
+size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys, int64_t N, int64_t Ts, int k);
 
 }  // namespace csa

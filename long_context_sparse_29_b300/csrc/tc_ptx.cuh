@@ -161,6 +161,14 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes (16-byte aligned, multiple of 16)
+// from global into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, void* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Wait for the phase with the given parity to complete; gives up after
 // `limit` polls and returns false (the caller records a timeout).
 __device__ __forceinline__ bool mbar_wait(void* bar, uint32_t parity, uint32_t limit) {
