@@ -245,8 +245,10 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
-# kernels launched per step: 3 compress, indexer scores + top-k, attention
-LAUNCHES_PER_STEP = 6
+# kernels launched per step: 3 compress, indexer scores + top-k, and for the
+# attention the per-row prep (rotated query dims, entry lists), the bf16
+# expansion of the cache and of the window rows, and the attention kernel
+LAUNCHES_PER_STEP = 9
 
 
 # --------------------------------------------------------------------------

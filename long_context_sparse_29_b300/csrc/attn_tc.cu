@@ -11,17 +11,20 @@
 // 64 heads share the KV: MQA) or, for small batches, a contiguous range of
 // its key tiles (split-K; a second kernel merges the partial softmaxes).
 // Keys run in tiles of 64 through a two-deep smem ring:
-//   producer warps 4-7  gather each tile's 592-byte rows (16 rows per warp in
-//                       flight), dequantise FP8 x 2^e to bf16 (exact) and
-//                       write a 64 x 512 bf16 tile, 128-byte swizzled; the
-//                       bf16 RoPE columns and the query are copied with
-//                       cp.async;
-//   MMA warp 8          S = Q K^T   (M = 64 heads, N = 64 keys, K = 512) into
-//                       TMEM, and O^T += V^T P^T (M = 128 dims x 4, N = 64
-//                       heads, K = 64 keys) into TMEM -- V = K, so the same
-//                       smem tile is read K-major for QK^T and MN-major for
-//                       PV; QK^T of the next tile is issued before PV of the
-//                       current one so the softmax overlaps the tensor core;
+//   producer warps 4-7  fetch each tile's rows: TMA gathers of bf16 rows
+//                       (prefill: the rows are expanded once up front) or
+//                       loads of the 592-byte mixed rows dequantised in
+//                       registers (decode), into a 64 x 512 bf16 tile,
+//                       128-byte swizzled; the compacted entry list of the
+//                       next item is bulk-copied one item ahead;
+//   MMA warp 8          an event loop over two kinds of work, whichever is
+//                       ready: S = Q K^T (M = 64 heads, N = 64 keys, K = 512)
+//                       into TMEM, and O^T += V^T P^T (M = 128 dims x 4,
+//                       N = 64 heads, K = 64 keys) into TMEM -- V = K, so
+//                       the same smem tile is read K-major for QK^T and
+//                       MN-major for PV; it also loads each item's query
+//                       with TMA (dims 448..511 pre-rotated by a small
+//                       per-row kernel);
 //   softmax warps 0-3   read S from TMEM, online softmax in the exp2 domain
 //                       with a lazy rescale of O^T (only when a running max
 //                       grows by more than 2^8), write bf16 P to smem; at the
@@ -29,7 +32,8 @@
 //                       and store bf16 (or store the partial state).
 // Every ring slot has its own full / empty mbarrier, so a waiter is never
 // more than one phase behind.  Waits are bounded: on expiry the CTA records a
-// timeout flag in the workspace and gives up.
+// timeout flag in the workspace and gives up; the four softmax warps take
+// that decision together, through a reducing named barrier.
 #include <cuda.h>
 
 #include "csa_common.cuh"
@@ -52,7 +56,7 @@ constexpr uint32_t kQOff = 0;                     // 8 chunks x [64 heads x 128 
 constexpr uint32_t kKVOff = 65536;                // 2 buffers x 8 chunks x [64 keys x 128 B]
 constexpr uint32_t kPOff = kKVOff + 131072;       // 2 buffers x [64 heads x 64 keys bf16]
 constexpr uint32_t kMiscOff = kPOff + 16384;      // barriers and per-head state
-constexpr uint32_t kListOff = kMiscOff + 1024;    // int32 key list of the current item
+constexpr uint32_t kListOff = kMiscOff + 2048;    // int32 entry lists, two buffers
 constexpr uint32_t kSmemBytes = 232448;           // 227 KiB
 constexpr int kMaxList = (int)((kSmemBytes - 1024 - kListOff) / 8);   // per buffer (two buffers)
 
@@ -60,33 +64,60 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O^T: 4 blocks of 64 columns (heads); lanes = dims
 constexpr uint32_t kTmemS = 256;     // S: 2 buffers of 64 columns (keys); M = 64 layout
 
-constexpr uint32_t kWaitLimit = 1u << 20;
+constexpr uint32_t kWaitLimit = 1u << 20;    // suspending polls of one mbarrier wait
+constexpr uint32_t kIdleLimit = 1u << 24;    // idle rounds of the MMA event loop
 constexpr float kLazy = 8.0f;        // log2 growth of a running max that forces a rescale
 
 struct Misc {
   uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
-  uint64_t q_full, q_ready, q_empty, o_full, o_empty;
-  uint64_t sm_sync[2];           // softmax group syncs (4 warps), alternating
-  uint64_t list_full[2], list_empty[2];  // producer key list handover, double-buffered
+  uint64_t q_full, q_empty, o_full, o_empty, drain;
+  uint64_t list_full[2], list_empty[2];  // entry list handover, double-buffered
   uint32_t tmem;
   int abort;
-  int any_rescale[4];
-  float alpha[2][kH];
-  float lsum[kH];
+  float alpha[2][kH];            // per-head rescale factors of a tile, double-buffered
+  float lsum[2][kH];             // per-head 1 / sum of an item, double-buffered
 };
+static_assert(sizeof(Misc) <= 2048, "Misc overflows its smem slot");
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk16) {
   return row * 128u + (((chunk16 ^ row) & 7u) << 4);
 }
 
-// Bounded barrier of the four softmax warps: every warp arrives once on
-// sm_sync[n & 1] and waits for its phase.  Returns false on expiry.
-__device__ __forceinline__ bool group_sync(Misc* ms, uint32_t& n, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&ms->sm_sync[n & 1]);
-  const bool ok = mbar_wait(&ms->sm_sync[n & 1], (n >> 1) & 1, kWaitLimit);
-  ++n;
-  return ok;
+// Barrier of the four softmax warps (named barrier 1, 128 threads) that
+// returns how many of them voted: every softmax warp executes the same
+// sequence of these, and exits only on a count read from one of them, so no
+// warp can be left waiting at a barrier the others never reach.
+__device__ __forceinline__ uint32_t group_vote(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %1, 0;\n bar.red.popc.u32 %0, 1, 128, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ bool vabort(const Misc* ms) {
+  return *reinterpret_cast<const volatile int*>(&ms->abort) != 0;
+}
+
+// Non-blocking test of an mbarrier phase, decided by lane 0 for the warp.
+__device__ __forceinline__ bool mbar_test_w(void* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return __shfl_sync(0xffffffffu, done, 0) != 0;
+}
+
+// 2^x by the hardware approximation (a few ulp; P is rounded to bf16 next).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -165,10 +196,6 @@ __global__ void __launch_bounds__(256) expand_rows_kernel(const uint8_t* __restr
   }
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
-
 struct Params {
   const __nv_bfloat16* q;
   const int64_t* q_pos;
@@ -176,7 +203,6 @@ struct Params {
   const uint8_t* cache;
   int64_t N;
   int m;
-  const int32_t* idx;
   int k;
   const uint8_t* swa;
   const int64_t* swa_pos0;
@@ -194,7 +220,6 @@ struct Params {
   float* part_o;      // [items, 64, 512] unnormalised O (split mode)
   float* part_ml;     // [items, 64, 2] running max (log2 units) and sum
   const __nv_bfloat16* xcache;   // bf16 copy of the cache rows [B, N, 512], or NULL
-  const __nv_bfloat16* xswa;     // bf16 copy of the window rows [B, Ts, 512]
   int64_t xrows;                 // rows of the bf16 copy (cache rows, then window rows)
   int64_t xwin0;                 // first window row in the copy (= B * N)
   const int32_t* clist;          // [rows, kpad] valid selected entries of each row, in idx order
@@ -205,7 +230,7 @@ struct Params {
 // Keys of one work item: entries first (selected, in idx order, or all
 // visible ones), then the window tokens; this split owns tiles [tlo, thi).
 struct Item {
-  int64_t row, b, t;
+  int64_t it, row, b, t;
   bool t_ok;
   int ne, nwin, nkeys;
   int64_t w_lo, p0;
@@ -213,44 +238,48 @@ struct Item {
   int key_hi;
 };
 
-constexpr int kIdxBatch = 16;   // selected indices loaded per lane before any is used
+// The global loads an item description needs, issued one item ahead.
+struct ItemPre {
+  int64_t t, p0;
+  int cnt;
+};
 
-__device__ __forceinline__ bool entry_ok(int32_t j, int64_t t, const Params& p) {
-  return j >= 0 && (int64_t)j < p.N && (int64_t)(j + 1) * p.m - 1 <= t;
+template <bool DENSE>
+__device__ __forceinline__ ItemPre item_fetch(const Params& p, int64_t it) {
+  ItemPre r;
+  r.t = -1;
+  r.p0 = 0;
+  r.cnt = 0;
+  if (it < p.items) {
+    const int64_t row = it / p.nsplit;
+    r.t = p.q_pos[row];
+    if (p.W > 0) r.p0 = p.swa_pos0[row / p.Tq];
+    if (!DENSE) r.cnt = p.ccount[row];
+  }
+  return r;
 }
 
 template <bool DENSE>
-__device__ __forceinline__ int count_valid(const Params& p, int64_t row, int64_t t, int lane) {
-  if (DENSE) {
-    const int64_t nv = (t + 1) / p.m;
-    return (int)(nv < p.N ? nv : p.N);
-  }
-  int cnt = 0;
-  for (int base = 0; base < p.k; base += 32 * kIdxBatch) {
-    int32_t js[kIdxBatch];
-#pragma unroll
-    for (int i = 0; i < kIdxBatch; ++i) {
-      const int r = base + 32 * i + lane;
-      js[i] = r < p.k ? __ldg(p.idx + row * p.k + r) : -1;
-    }
-#pragma unroll
-    for (int i = 0; i < kIdxBatch; ++i) cnt += __popc(__ballot_sync(0xffffffffu, entry_ok(js[i], t, p)));
-  }
-  return cnt < kMaxList ? cnt : kMaxList;
-}
-
-// Warp-uniform description of work item `it` (every lane of the warp calls it).
-template <bool DENSE>
-__device__ __forceinline__ Item make_item(const Params& p, int64_t it, int lane) {
+__device__ __forceinline__ Item item_make(const Params& p, int64_t it, const ItemPre& r) {
   Item I;
+  I.it = it;
   I.row = it / p.nsplit;
-  const int split = (int)(it % p.nsplit);
+  const int split = (int)(it - I.row * p.nsplit);
   I.b = I.row / p.Tq;
-  I.t = p.q_pos[I.row];
+  I.t = r.t;
   I.t_ok = I.t >= 0 && I.t < p.rope_rows;
-  I.ne = !I.t_ok ? 0 : DENSE ? count_valid<DENSE>(p, I.row, I.t, lane) : min(p.ccount[I.row], kMaxList);
+  int ne = 0;
+  if (I.t_ok) {
+    if (DENSE) {
+      const int64_t nv = (I.t + 1) / p.m;   // entries whose block ends at or before t
+      ne = (int)(nv < p.N ? nv : p.N);
+    } else {
+      ne = min(r.cnt, kMaxList);
+    }
+  }
+  I.ne = ne;
   const int64_t u_lo = I.t - p.W + 1 < 0 ? 0 : I.t - p.W + 1;
-  I.p0 = p.W > 0 ? p.swa_pos0[I.b] : 0;
+  I.p0 = r.p0;
   I.w_lo = u_lo < I.p0 ? I.p0 : u_lo;
   const int64_t w_hi = I.t < I.p0 + p.Ts - 1 ? I.t : I.p0 + p.Ts - 1;
   I.nwin = (I.t_ok && p.W > 0 && w_hi >= I.w_lo) ? (int)(w_hi - I.w_lo + 1) : 0;
@@ -263,18 +292,69 @@ __device__ __forceinline__ Item make_item(const Params& p, int64_t it, int lane)
   return I;
 }
 
-// Ordered compaction of each row's valid selected entries (idx >= 0, < N,
-// block complete at the query's position); invalid ones set the device-check
-// flag.  One warp per query row.
+// This CTA's items in order (blockIdx.x, + gridDim.x, ...), the loads of
+// the next one in flight while the current one is worked on.
+template <bool DENSE>
+struct Cursor {
+  int64_t next;
+  ItemPre pre;
+  __device__ __forceinline__ explicit Cursor(const Params& p) : next(blockIdx.x) { pre = item_fetch<DENSE>(p, next); }
+  __device__ __forceinline__ bool any(const Params& p, Item& I) {
+    if (next >= p.items) return false;
+    I = item_make<DENSE>(p, next, pre);
+    next += gridDim.x;
+    pre = item_fetch<DENSE>(p, next);
+    return true;
+  }
+  __device__ __forceinline__ bool nonempty(const Params& p, Item& I) {
+    while (any(p, I))
+      if (I.thi > I.tlo) return true;
+    return false;
+  }
+  // like nonempty, but keeps only the item's index and loads (few registers)
+  __device__ __forceinline__ int64_t seek(const Params& p, ItemPre& out) {
+    Item I;
+    while (next < p.items) {
+      const int64_t it = next;
+      out = pre;
+      if (!any(p, I)) break;
+      if (I.thi > I.tlo) return it;
+    }
+    return p.items;
+  }
+};
+
+constexpr int kIdxBatch = 16;   // selected indices loaded per lane before any is used
+
+// Per query row, ahead of the attention: the query's RoPE dims rotated to
+// its position and rounded to bf16 (qr, [rows, 64 heads, 64 dims]), and for
+// sparse attention the ordered list of its valid selected entries (idx >= 0,
+// < N, block complete at the query's position); invalid ones set the
+// device-check flag.  One block of 8 warps per row.
 __global__ void __launch_bounds__(256)
-compact_idx_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ q_pos, int64_t rows, int k,
-                   int kpad, int64_t N, int m, int64_t rope_rows, int32_t* __restrict__ clist,
-                   int32_t* __restrict__ ccount, void* ws) {
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
+prep_rows_kernel(const __nv_bfloat16* __restrict__ q, const int64_t* __restrict__ q_pos, const float* __restrict__ rcos,
+                 const float* __restrict__ rsin, int64_t rope_rows, __nv_bfloat16* __restrict__ qr,
+                 const int32_t* __restrict__ idx, int k, int kpad, int64_t N, int m, int32_t* __restrict__ clist,
+                 int32_t* __restrict__ ccount, void* ws) {
+  const int64_t row = blockIdx.x;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = q_pos[row];
   const bool t_ok = t >= 0 && t < rope_rows;
+  {
+    const float c = rcos[(t_ok ? t : 0) * 32 + lane], s = rsin[(t_ok ? t : 0) * 32 + lane];
+    __nv_bfloat162 x[8];
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh)
+      x[hh] = *reinterpret_cast<const __nv_bfloat162*>(q + (row * kH + 8 * w + hh) * kD + kMixDn + 2 * lane);
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh) {
+      const float2 f = __bfloat1622float2(x[hh]);
+      const float y0 = __fsub_rn(__fmul_rn(f.x, c), __fmul_rn(f.y, s));
+      const float y1 = __fadd_rn(__fmul_rn(f.x, s), __fmul_rn(f.y, c));
+      *reinterpret_cast<__nv_bfloat162*>(qr + (row * kH + 8 * w + hh) * 64 + 2 * lane) = __floats2bfloat162_rn(y0, y1);
+    }
+  }
+  if (!idx || w != 0) return;
   int cnt = 0;
   for (int base = 0; base < k; base += 32 * kIdxBatch) {
     int32_t js[kIdxBatch];
@@ -298,7 +378,8 @@ compact_idx_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ 
 
 template <bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_q) {
+attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_q,
+               const __grid_constant__ CUtensorMap tm_qr) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm + kQOff;
@@ -310,24 +391,19 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
 
   if (tid == 0) {
     ms->abort = 0;
-    for (int i = 0; i < 4; ++i) ms->any_rescale[i] = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->kv_full[i], 4);
       mbar_init(&ms->kv_empty[i], 1);
       mbar_init(&ms->s_full[i], 1);
       mbar_init(&ms->p_full[i], 4);
-    }
-    mbar_init(&ms->q_full, 1);
-    mbar_init(&ms->q_ready, 4);
-    mbar_init(&ms->q_empty, 1);
-    mbar_init(&ms->o_full, 1);
-    mbar_init(&ms->o_empty, 4);
-    mbar_init(&ms->sm_sync[0], 4);
-    mbar_init(&ms->sm_sync[1], 4);
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->list_full[i], 1);
       mbar_init(&ms->list_empty[i], 4);
     }
+    mbar_init(&ms->q_full, 1);
+    mbar_init(&ms->q_empty, 1);
+    mbar_init(&ms->o_full, 1);
+    mbar_init(&ms->o_empty, 4);
+    mbar_init(&ms->drain, 1);
     mbar_fence_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&ms->tmem, kTmemCols);
@@ -338,84 +414,42 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
 
   if (warp >= 4 && warp < 8) {
     // ================================ producers ================================
-    const int pw = warp - 4, ptid = tid - 128;
+    const int pw = warp - 4;
+    Cursor<DENSE> cur(p);
+    Item I;
+    bool have = cur.nonempty(p, I);
+    ItemPre pj;                  // the next item (for its list): index jn, loads pj
+    int64_t jn = (!DENSE && have) ? cur.seek(p, pj) : p.items;
     uint32_t g = 0, nq = 0;      // tiles and non-empty items produced so far
-    for (int64_t it = blockIdx.x; it < p.items && !ms->abort; it += gridDim.x) {
-      const Item I = make_item<DENSE>(p, it, lane);
-      if (I.thi <= I.tlo) continue;
-      if (pw == 0 && lane == 0 && it + gridDim.x < p.items) {   // warm L2 for the next item
-        const int64_t nrow = (it + gridDim.x) / p.nsplit;
-        if (nrow != I.row) {
-          prefetch_l2(p.q + nrow * (int64_t)(kH * kD), kH * kD * 2);
-          if (!DENSE && ((p.k * 4) & 15) == 0) prefetch_l2(p.idx + nrow * p.k, (uint32_t)p.k * 4);
+    uint32_t nl = 0;             // entry lists issued (warp 0)
+    bool ok = true;
+    // entry list of item ordinal n -> smem buffer n & 1, once every producer
+    // warp is done with item n - 2 (warp 0 issues)
+    auto issue_list = [&](const Item& L, uint32_t n) -> bool {
+      int good = 1;
+      if (lane == 0) {
+        if (n >= 2 && !mbar_wait(&ms->list_empty[n & 1], ((n >> 1) - 1) & 1, kWaitLimit)) {
+          good = 0;
+        } else {
+          const uint32_t bytes = (uint32_t)((L.ne + 3) & ~3) * 4u;
+          mbar_arrive_expect_tx(&ms->list_full[n & 1], bytes);
+          if (bytes)
+            bulk_copy_g2s(smem_u32(list + (n & 1) * kMaxList), p.clist + L.row * p.kpad, bytes,
+                          &ms->list_full[n & 1]);
         }
       }
-      // the row's compacted entry list -> smem buffer nq & 1 (the other buffer
-      // may still feed the previous item's last tiles)
-      int32_t* lst = list + (nq & 1) * kMaxList;
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (good) nl = n + 1;
+      return good != 0;
+    };
+    if (!DENSE && have && pw == 0) ok = issue_list(I, 0);
+    while (have && ok && !vabort(ms)) {
+      const int32_t* lst = list + (nq & 1) * kMaxList;
       if (!DENSE) {
-        if (pw == 0 && lane == 0) {
-          if (nq >= 2 && !mbar_wait(&ms->list_empty[nq & 1], ((nq >> 1) - 1) & 1, kWaitLimit)) {
-            ms->abort = 1;
-            flag_timeout(p.ws);
-          } else {
-            const uint32_t bytes = (uint32_t)((I.ne + 3) & ~3) * 4u;
-            mbar_arrive_expect_tx(&ms->list_full[nq & 1], bytes);
-            if (bytes) bulk_copy_g2s(smem_u32(lst), p.clist + I.row * p.kpad, bytes, &ms->list_full[nq & 1]);
-          }
-        }
-        __syncwarp();
-        if (ms->abort || !mbar_wait(&ms->list_full[nq & 1], (nq >> 1) & 1, kWaitLimit)) {
-          ms->abort = 1;
-          flag_timeout(p.ws);
-          break;
-        }
+        if (jn < p.items && pw == 0) ok = issue_list(item_make<DENSE>(p, jn, pj), nq + 1);
+        if (ok && !mbar_wait(&ms->list_full[nq & 1], (nq >> 1) & 1, kWaitLimit)) ok = false;
+        if (!ok) break;
       }
-      // ---- the query: 64 heads x 512 dims -> smem, RoPE on dims 448..511 ----
-      if (nq > 0 && !mbar_wait(&ms->q_empty, (nq - 1) & 1, kWaitLimit)) {
-        ms->abort = 1;
-        flag_timeout(p.ws);
-        break;
-      }
-      {
-        // TMA: 8 boxes of 64 heads x 64 dims, 128-byte swizzled, then RoPE
-        // of the last box (dims 448..511) in place
-        if (pw == 0) {
-          if (lane == 0) mbar_arrive_expect_tx(&ms->q_full, kH * kD * 2);
-          __syncwarp();
-          if (lane < 8) tma_load_2d(smem_u32(sQ + lane * 8192), &tm_q, 64 * lane, (int)(I.row * kH), &ms->q_full);
-        }
-        if (!mbar_wait(&ms->q_full, nq & 1, kWaitLimit)) {
-          ms->abort = 1;
-          flag_timeout(p.ws);
-          break;
-        }
-        const float* cs = p.rcos + (I.t_ok ? I.t : 0) * 32;
-        const float* sn = p.rsin + (I.t_ok ? I.t : 0) * 32;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int v = ptid + 128 * u, h = v >> 3, c = v & 7;
-          uint4* slot = reinterpret_cast<uint4*>(sQ + 7 * 8192 + sw128(h, c));
-          const uint4 x = *slot;
-          uint32_t wd[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-          for (int pp = 0; pp < 4; ++pp) {
-            const int i = c * 4 + pp;
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[pp]));
-            const float y0 = __fsub_rn(__fmul_rn(f.x, cs[i]), __fmul_rn(f.y, sn[i]));
-            const float y1 = __fadd_rn(__fmul_rn(f.x, sn[i]), __fmul_rn(f.y, cs[i]));
-            const __nv_bfloat162 r = __floats2bfloat162_rn(y0, y1);
-            wd[pp] = *reinterpret_cast<const uint32_t*>(&r);
-          }
-          *slot = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ms->q_ready);
-      }
-      ++nq;
-      // ---- key tiles ----
-      bool ok = true;
       if (p.xcache) {
         // bf16 rows are ready: each producer warp gathers 16 of the tile's 64
         // rows with TMA (4 rows x 128 bytes per instruction, 8 column boxes)
@@ -447,170 +481,206 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
           __syncwarp();
         }
       } else {
-      for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
-        const int buf = g & 1;
-        const int kbase = tl * kTile;
-        uint4 c[16];
-        float sc[16];
-        const uint8_t* rowp[16];
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          const int key = kbase + pw + 4 * rr;
-          const uint8_t* row = nullptr;
-          if (key < I.key_hi) {
-            if (key < I.ne) {
-              const int64_t j = DENSE ? (int64_t)key : (int64_t)lst[key];
-              row = p.cache + ((size_t)I.b * p.N + j) * kMixRow;
-            } else {
-              row = p.swa + ((size_t)I.b * p.Ts + (I.w_lo - I.p0 + (key - I.ne))) * kMixRow;
-            }
-          }
-          rowp[rr] = row;
-          c[rr] = make_uint4(0, 0, 0, 0);
-          sc[rr] = 0.0f;
-          if (lane < 28 && row) {
-            c[rr] = __ldg(reinterpret_cast<const uint4*>(row) + lane);
-            sc[rr] = __ldg(reinterpret_cast<const float*>(row + kMixScaleOff) + (lane >> 3));
-          }
-        }
-        if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
-          ok = false;
-          break;
-        }
-        uint8_t* kv = sKV + buf * 65536;
-        const uint32_t aKV = smem_u32(kv);
-        if (lane >= 28) {                 // bf16 RoPE columns: async copies first
-          const int l4 = lane - 28;
+        // mixed rows, dequantised here: this warp takes rows pw + 4 rr of the
+        // tile, 16 of them in flight per lane
+        for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
+          const int buf = g & 1;
+          const int kbase = tl * kTile;
+          uint4 c[16];
+          float sc[16];
+          const uint8_t* rowp[16];
 #pragma unroll
           for (int rr = 0; rr < 16; ++rr) {
-            const int r = pw + 4 * rr;
-            if (rowp[rr]) {
-              cp_async16(aKV + 7 * 8192 + sw128(r, 2 * l4), rowp[rr] + kMixRopeOff + 32 * l4);
-              cp_async16(aKV + 7 * 8192 + sw128(r, 2 * l4 + 1), rowp[rr] + kMixRopeOff + 32 * l4 + 16);
-            } else {
-              *reinterpret_cast<uint4*>(kv + 7 * 8192 + sw128(r, 2 * l4)) = make_uint4(0, 0, 0, 0);
-              *reinterpret_cast<uint4*>(kv + 7 * 8192 + sw128(r, 2 * l4 + 1)) = make_uint4(0, 0, 0, 0);
+            const int key = kbase + pw + 4 * rr;
+            const uint8_t* row = nullptr;
+            if (key < I.key_hi) {
+              if (key < I.ne) {
+                const int64_t j = DENSE ? (int64_t)key : (int64_t)lst[key];
+                row = p.cache + ((size_t)I.b * p.N + j) * kMixRow;
+              } else {
+                row = p.swa + ((size_t)I.b * p.Ts + (I.w_lo - I.p0 + (key - I.ne))) * kMixRow;
+              }
+            }
+            rowp[rr] = row;
+            c[rr] = make_uint4(0, 0, 0, 0);
+            sc[rr] = 0.0f;
+            if (lane < 28 && row) {
+              c[rr] = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+              sc[rr] = __ldg(reinterpret_cast<const float*>(row + kMixScaleOff) + (lane >> 3));
             }
           }
-        } else {                          // FP8 columns: dequantise
-          uint8_t* dst = kv + (lane >> 2) * 8192;
-          const uint32_t sub = 2 * (lane & 3);
-#pragma unroll
-          for (int rr = 0; rr < 16; ++rr) {
-            const int r = pw + 4 * rr;
-            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-            if (rowp[rr]) dequant16(c[rr], sc[rr], o0, o1);
-            *reinterpret_cast<uint4*>(dst + sw128(r, sub)) = o0;
-            *reinterpret_cast<uint4*>(dst + sw128(r, sub + 1)) = o1;
+          if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
+            ok = false;
+            break;
           }
+          uint8_t* kv = sKV + buf * 65536;
+          const uint32_t aKV = smem_u32(kv);
+          if (lane >= 28) {                 // bf16 RoPE columns: async copies first
+            const int l4 = lane - 28;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+              const int r = pw + 4 * rr;
+              if (rowp[rr]) {
+                cp_async16(aKV + 7 * 8192 + sw128(r, 2 * l4), rowp[rr] + kMixRopeOff + 32 * l4);
+                cp_async16(aKV + 7 * 8192 + sw128(r, 2 * l4 + 1), rowp[rr] + kMixRopeOff + 32 * l4 + 16);
+              } else {
+                *reinterpret_cast<uint4*>(kv + 7 * 8192 + sw128(r, 2 * l4)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(kv + 7 * 8192 + sw128(r, 2 * l4 + 1)) = make_uint4(0, 0, 0, 0);
+              }
+            }
+          } else {                          // FP8 columns: dequantise
+            uint8_t* dst = kv + (lane >> 2) * 8192;
+            const uint32_t sub = 2 * (lane & 3);
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+              const int r = pw + 4 * rr;
+              uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+              if (rowp[rr]) dequant16(c[rr], sc[rr], o0, o1);
+              *reinterpret_cast<uint4*>(dst + sw128(r, sub)) = o0;
+              *reinterpret_cast<uint4*>(dst + sw128(r, sub + 1)) = o1;
+            }
+          }
+          cp_async_wait_all();
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ms->kv_full[buf]);
         }
-        cp_async_wait_all();
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ms->kv_full[buf]);
       }
-      }
-      if (!ok) {
-        ms->abort = 1;
-        flag_timeout(p.ws);
-        break;
-      }
+      if (!ok) break;
       if (!DENSE) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ms->list_empty[(nq - 1) & 1]);
+        if (lane == 0) mbar_arrive(&ms->list_empty[nq & 1]);
+      }
+      ++nq;
+      if (DENSE) {
+        have = cur.nonempty(p, I);
+      } else {
+        have = jn < p.items;
+        if (have) {
+          I = item_make<DENSE>(p, jn, pj);
+          jn = cur.seek(p, pj);
+        }
       }
     }
+    if (!ok) {
+      ms->abort = 1;
+      if (lane == 0) flag_timeout(p.ws);
+    }
+    // copies of this warp still in flight land before the CTA can exit
+    if (p.xcache && g > 0) mbar_wait(&ms->kv_full[(g - 1) & 1], ((g - 1) >> 1) & 1, kWaitLimit);
+    if (nl > 0) mbar_wait(&ms->list_full[(nl - 1) & 1], ((nl - 1) >> 1) & 1, kWaitLimit);
   } else if (warp == kMmaWarp) {
     // ================================ MMA issue ================================
+    // Event loop: PV of the oldest tile whose P is ready, else the next
+    // query load, else QK of the next tile whose keys and query are in.
+    // QK of tile g reuses the S buffer and ring slot of tile g - 2, so it
+    // waits until PV of tile g - 2 is issued (the softmax has read S, and
+    // the tensor core runs in order); the first PV of an item overwrites
+    // O^T, so it waits for the previous item's epilogue.
     const uint32_t aQ = smem_u32(sQ), aKV = smem_u32(sKV), aP = smem_u32(sP);
     constexpr uint32_t idQK = idesc_bf16(64, kTile, 0, 0);
     constexpr uint32_t idPV = idesc_bf16(128, kH, 1, 0);
-    uint32_t g = 0, nq = 0;
-    int pend = -1;             // tile whose PV is not issued yet
-    bool pend_first = false, pend_last = false;
-    uint32_t pend_q = 0;       // ordinal of its item
-    bool ok = true;
-    auto do_pv = [&](uint32_t gg, bool first, bool last, uint32_t qord) -> bool {
-      if (!mbar_wait(&ms->p_full[gg & 1], (gg >> 1) & 1, kWaitLimit)) return false;
-      if (first && qord > 0 && !mbar_wait(&ms->o_empty, (qord - 1) & 1, kWaitLimit)) return false;
-      fence_after_sync();
-      {
-        const uint64_t vd0 = sdesc_sw128(aKV + (gg & 1) * 65536, 8192, 1024);
-        const uint64_t pd0 = sdesc_sw128(aP + (gg & 1) * 8192, 16, 1024);
+    Cursor<DENSE> cur(p);
+    Item I;
+    bool have = cur.nonempty(p, I);
+    int tq = have ? I.tlo : 0;
+    uint32_t gq = 0, gp = 0, nq = 0;        // next QK tile, next PV tile, ordinal of item I
+    bool f0 = false, l0 = false, f1 = false, l1 = false;   // first / last of tiles gp, gp + 1
+    uint32_t q0 = 0, q1 = 0;                // their item ordinals
+    bool q_load = have, q_in = false, q_pending = false, ok = true;
+    uint32_t idle = 0;
+    auto issue_q = [&](int64_t row) {
+      if (lane == 0) mbar_arrive_expect_tx(&ms->q_full, kH * kD * 2);
+      __syncwarp();
+      if (lane < 7) tma_load_2d(aQ + lane * 8192, &tm_q, 64 * lane, (int)(row * kH), &ms->q_full);
+      else if (lane == 7) tma_load_2d(aQ + 7 * 8192, &tm_qr, 0, (int)(row * kH), &ms->q_full);
+      __syncwarp();
+    };
+    while (have || gp != gq) {
+      bool did = false;
+      if (gp != gq && mbar_test_w(&ms->p_full[gp & 1], (gp >> 1) & 1) &&
+          (!f0 || q0 == 0 || mbar_test_w(&ms->o_empty, (q0 - 1) & 1))) {
+        fence_after_sync();
+        const uint64_t vd0 = sdesc_sw128(aKV + (gp & 1) * 65536, 8192, 1024);
+        const uint64_t pd0 = sdesc_sw128(aP + (gp & 1) * 8192, 16, 1024);
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
             mma_bf16_elect(tmem + kTmemO + 64u * mt, vd0 + (uint64_t)((2 * mt * 8192 + ks * 2048) >> 4),
-                           pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!first || ks > 0) ? 1u : 0u);
+                           pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!f0 || ks > 0) ? 1u : 0u);
         }
-        mma_commit_elect(&ms->kv_empty[gg & 1]);
-        if (last) mma_commit_elect(&ms->o_full);
-      }
-      __syncwarp();
-      return true;
-    };
-    // next non-empty item at or after `it`
-    auto next_item = [&](int64_t it, Item& I) -> int64_t {
-      for (; it < p.items; it += gridDim.x) {
-        I = make_item<DENSE>(p, it, lane);
-        if (I.thi > I.tlo) return it;
-      }
-      return p.items;
-    };
-    Item I;
-    int64_t it = next_item(blockIdx.x, I);
-    while (it < p.items && ok && !ms->abort) {
-      if (!mbar_wait(&ms->q_ready, nq & 1, kWaitLimit)) {
-        ok = false;
-        break;
-      }
-      for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
-        if (!mbar_wait(&ms->kv_full[g & 1], (g >> 1) & 1, kWaitLimit)) {
-          ok = false;
-          break;
+        mma_commit_elect(&ms->kv_empty[gp & 1]);
+        if (l0) mma_commit_elect(&ms->o_full);
+        __syncwarp();
+        f0 = f1;
+        l0 = l1;
+        q0 = q1;
+        ++gp;
+        did = true;
+      } else if (q_load) {
+        if (nq == 0 || mbar_test_w(&ms->q_empty, (nq - 1) & 1)) {
+          issue_q(I.row);
+          q_load = false;
+          q_pending = true;
+          did = true;
         }
-        fence_after_sync();
-        {
-          const uint32_t dS = tmem + kTmemS + 64u * (g & 1);
+      } else if (have && gq - gp < 2) {
+        if (!q_in) q_in = mbar_test_w(&ms->q_full, nq & 1);
+        if (q_in && mbar_test_w(&ms->kv_full[gq & 1], (gq >> 1) & 1)) {
+          q_pending = false;
+          fence_after_sync();
+          const bool first = tq == I.tlo, last = tq == I.thi - 1;
+          const uint32_t dS = tmem + kTmemS + 64u * (gq & 1);
           const uint64_t qd0 = sdesc_sw128(aQ, 16, 1024);
-          const uint64_t kd0 = sdesc_sw128(aKV + (g & 1) * 65536, 16, 1024);
+          const uint64_t kd0 = sdesc_sw128(aKV + (gq & 1) * 65536, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint64_t off = (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
             mma_bf16_elect(dS, qd0 + off, kd0 + off, idQK, kk > 0 ? 1u : 0u);
           }
-          mma_commit_elect(&ms->s_full[g & 1]);
-          if (tl == I.thi - 1) mma_commit_elect(&ms->q_empty);
+          mma_commit_elect(&ms->s_full[gq & 1]);
+          if (last) mma_commit_elect(&ms->q_empty);
+          __syncwarp();
+          if (gq == gp) {
+            f0 = first;
+            l0 = last;
+            q0 = nq;
+          } else {
+            f1 = first;
+            l1 = last;
+            q1 = nq;
+          }
+          ++gq;
+          ++tq;
+          if (last) {
+            ++nq;
+            q_in = false;
+            have = cur.nonempty(p, I);
+            if (have) {
+              tq = I.tlo;
+              q_load = true;
+            }
+          }
+          did = true;
         }
-        __syncwarp();
-        if (pend >= 0) {
-          ok = do_pv((uint32_t)pend, pend_first, pend_last, pend_q);
-          if (!ok) break;
-        }
-        pend = (int)g;
-        pend_first = tl == I.tlo;
-        pend_last = tl == I.thi - 1;
-        pend_q = nq;
       }
-      if (!ok) break;
-      ++nq;
-      // describe the next item while the tensor core drains this one, then
-      // issue this item's last PV
-      Item J;
-      const int64_t it2 = next_item(it + gridDim.x, J);
-      if (pend >= 0) {
-        ok = do_pv((uint32_t)pend, pend_first, pend_last, pend_q);
-        pend = -1;
+      if (did) {
+        idle = 0;
+      } else if (++idle > kIdleLimit || vabort(ms)) {
+        ok = false;
+        break;
       }
-      it = it2;
-      I = J;
     }
-    if (ok && pend >= 0) ok = do_pv((uint32_t)pend, pend_first, pend_last, pend_q);
     if (!ok) {
       ms->abort = 1;
       if (lane == 0) flag_timeout(p.ws);
+      if (q_pending) mbar_wait(&ms->q_full, nq & 1, kWaitLimit);   // the query copy in flight
     }
+    // every MMA this warp issued completes before TMEM is released
+    mma_commit_elect(&ms->drain);
+    __syncwarp();
+    mbar_wait(&ms->drain, 0, kWaitLimit);
   } else {
     // ============================ softmax / epilogue ============================
     // S (64 heads x 64 keys) sits in lanes 0-15 of every TMEM quadrant; the
@@ -623,9 +693,13 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
     const int ha = 16 * qd + (lane >> 2), hb = ha + 8;
     const bool leader = (lane & 3) == 0;
     const bool split = p.part_o != nullptr;
-    uint32_t g = 0, nq = 0, ns = 0;
-    for (int64_t it = blockIdx.x; it < p.items && !ms->abort; it += gridDim.x) {
-      const Item I = make_item<DENSE>(p, it, lane);
+    const uint32_t tq_lane = (uint32_t)(32 * qd) << 16;   // this warp's TMEM lane quadrant
+    Cursor<DENSE> cur(p);
+    Item I;
+    uint32_t g = 0, nq = 0;
+    bool fail = false, stop = false;
+    while (!stop && cur.any(p, I)) {
+      const int64_t it = I.it;
       if (tid == 0 && I.row * p.nsplit == it) {
         if (!I.t_ok) flag_device_check(p.ws, 0x40000000u);
         const int64_t u_lo = I.t - p.W + 1 < 0 ? 0 : I.t - p.W + 1;
@@ -647,16 +721,12 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         continue;
       }
       float ma = -INFINITY, mb = -INFINITY, la = 0.0f, lb = 0.0f;
-      bool ok = true;
       for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
-        if (!mbar_wait(&ms->s_full[g & 1], (g >> 1) & 1, kWaitLimit)) {
-          ok = false;
-          break;
-        }
+        if (!fail && !mbar_wait(&ms->s_full[g & 1], (g >> 1) & 1, kWaitLimit)) fail = true;
         fence_after_sync();
         const int nvalid = min(kTile, I.key_hi - tl * kTile);
         uint32_t v[32];
-        tmem_ld16x256b_x8(tmem + ((uint32_t)(32 * qd) << 16) + kTmemS + 64u * (g & 1), v);
+        tmem_ld16x256b_x8(tmem + tq_lane + kTmemS + 64u * (g & 1), v);
         tmem_wait_ld();
         float xa[16], xb[16];
         float ta = -INFINITY, tb = -INFINITY;
@@ -677,40 +747,41 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 2));
         const bool need_a = ta > ma + kLazy, need_b = tb > mb + kLazy;
         const float na = need_a ? ta : ma, nb = need_b ? tb : mb;
-        const float aa = need_a ? exp2f(ma - na) : 1.0f;   // exp2(-inf) = 0 on the first tile
-        const float ab = need_b ? exp2f(mb - nb) : 1.0f;
+        const float aa = need_a ? ex2(ma - na) : 1.0f;   // 2^-inf = 0 on the first tile
+        const float ab = need_b ? ex2(mb - nb) : 1.0f;
         if (tl > I.tlo) {
-          if (__any_sync(0xffffffffu, need_a || need_b) && lane == 0) atomicOr(&ms->any_rescale[g & 3], 1);
           if (leader) {
             ms->alpha[g & 1][ha] = aa;
             ms->alpha[g & 1][hb] = ab;
           }
-          if (!group_sync(ms, ns, lane)) {
-            ok = false;
+          // one vote per warp that must rescale, 32 per warp that failed
+          const bool wfail = __any_sync(0xffffffffu, fail || vabort(ms));
+          const bool wresc = __any_sync(0xffffffffu, need_a || need_b);
+          const uint32_t votes = group_vote(wfail || (lane == 0 && wresc));
+          if (votes >= 32) {
+            stop = true;
             break;
           }
-          if (tid == 0) ms->any_rescale[(g + 2) & 3] = 0;   // slot of tile g + 2, read by nobody now
-          if (ms->any_rescale[g & 3]) {
+          if (votes > 0) {
             // the previous tile's PV must be complete before O^T is touched
-            const uint32_t gp = g - 1;
-            if (!mbar_wait(&ms->kv_empty[gp & 1], (gp >> 1) & 1, kWaitLimit)) ok = false;
+            const uint32_t gv = g - 1;
+            if (!fail && !mbar_wait(&ms->kv_empty[gv & 1], (gv >> 1) & 1, kWaitLimit)) fail = true;
             fence_after_sync();
-            if (ok) {
+            if (!fail) {
 #pragma unroll 1
               for (int c = 0; c < 8; ++c) {
                 uint32_t o[32];
-                const uint32_t oa = tmem + ((uint32_t)(32 * qd) << 16) + kTmemO + 32u * c;
+                const uint32_t oa = tmem + tq_lane + kTmemO + 32u * c;
                 tmem_ld32(oa, o);
                 tmem_wait_ld();
-                const int h0 = 32 * (c & 1);
+                const float* al = ms->alpha[g & 1] + 32 * (c & 1);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * ms->alpha[g & 1][h0 + j]);
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al[j]);
                 tmem_st32(oa, o);
               }
               tmem_wait_st();
             }
           }
-          if (!ok) break;
         }
         ma = na;
         mb = nb;
@@ -718,8 +789,8 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         uint8_t* dst = sP + (g & 1) * 8192;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float pa0 = exp2f(xa[2 * j] - ma), pa1 = exp2f(xa[2 * j + 1] - ma);
-          const float pb0 = exp2f(xb[2 * j] - mb), pb1 = exp2f(xb[2 * j + 1] - mb);
+          const float pa0 = ex2(xa[2 * j] - ma), pa1 = ex2(xa[2 * j + 1] - ma);
+          const float pb0 = ex2(xb[2 * j] - mb), pb1 = ex2(xb[2 * j + 1] - mb);
           sa += pa0 + pa1;
           sb2 += pb0 + pb1;
           const __nv_bfloat162 qa = __floats2bfloat162_rn(pa0, pa1);
@@ -734,25 +805,18 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         __syncwarp();
         if (lane == 0) mbar_arrive(&ms->p_full[g & 1]);
       }
-      if (!ok) {
-        ms->abort = 1;
-        flag_timeout(p.ws);
-        break;
-      }
+      if (stop) break;
       // ---- epilogue: the item's O^T is complete after its last PV ----
       la += __shfl_xor_sync(0xffffffffu, la, 1);
       la += __shfl_xor_sync(0xffffffffu, la, 2);
       lb += __shfl_xor_sync(0xffffffffu, lb, 1);
       lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-      if (!mbar_wait(&ms->o_full, nq & 1, kWaitLimit)) {
-        ms->abort = 1;
-        flag_timeout(p.ws);
-        break;
-      }
+      if (!fail && !mbar_wait(&ms->o_full, nq & 1, kWaitLimit)) fail = true;
       fence_after_sync();
+      float* lsv = ms->lsum[nq & 1];
       if (leader) {
-        ms->lsum[ha] = la > 0.0f ? 1.0f / la : 0.0f;   // per-head 1/sum for every lane
-        ms->lsum[hb] = lb > 0.0f ? 1.0f / lb : 0.0f;
+        lsv[ha] = la > 0.0f ? 1.0f / la : 0.0f;   // per-head 1/sum for every lane
+        lsv[hb] = lb > 0.0f ? 1.0f / lb : 0.0f;
         if (split) {
           p.part_ml[(it * kH + ha) * 2] = ma;
           p.part_ml[(it * kH + ha) * 2 + 1] = la;
@@ -763,17 +827,13 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
           p.lse[I.row * kH + hb] = lb > 0.0f ? (mb + log2f(lb)) * 0.69314718055994531f : -INFINITY;
         }
       }
-      if (!group_sync(ms, ns, lane)) {
-        ms->abort = 1;
-        flag_timeout(p.ws);
-        break;
-      }
+      if (group_vote(__any_sync(0xffffffffu, fail || vabort(ms))) != 0) break;
       if (split) {
         float* po = p.part_o + it * (int64_t)(kH * kD);
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           uint32_t o[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + kTmemO + 32u * c, o);
+          tmem_ld32(tmem + tq_lane + kTmemO + 32u * c, o);
           tmem_wait_ld();
           const int d = 128 * (c >> 1) + 32 * qd + lane;
           const int h0 = 32 * (c & 1);
@@ -781,36 +841,49 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
           for (int j = 0; j < 32; ++j) po[(h0 + j) * kD + d] = __uint_as_float(o[j]);
         }
       } else {
+        // lane pairs swap values so that each lane holds two adjacent dims of
+        // one head: lane 2i takes head j, lane 2i + 1 head j + 1; a RoPE pair
+        // is then rotated back within one lane and stored as one bf16x2
         __nv_bfloat16* og = p.out + I.row * (int64_t)(kH * kD);
+        const int odd = lane & 1;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + kTmemO + 32u * c, o);
-          tmem_wait_ld();
-          const int d = 128 * (c >> 1) + 32 * qd + lane;
-          const int h0 = 32 * (c & 1);
-          const bool rope = d >= kMixDn;          // warp-uniform
-          const int pi = rope ? (d - kMixDn) >> 1 : 0;
-          const float cc = rope ? cs[pi] : 1.0f, ss = rope ? sn[pi] : 0.0f;
+        for (int hh = 0; hh < 2; ++hh) {
+          const float* inv = lsv + 32 * hh;
+#pragma unroll 1
+          for (int mt = 0; mt < 4; ++mt) {
+            uint32_t o[32];
+            tmem_ld32(tmem + tq_lane + kTmemO + 64u * mt + 32u * hh, o);
+            tmem_wait_ld();
+            const int de = 128 * mt + 32 * qd + (lane & ~1);
+            const bool rope = de >= kMixDn;          // warp-uniform
+            const int pi = rope ? (de - kMixDn) >> 1 : 0;
+            const float cc = rope ? cs[pi] : 1.0f, ss = rope ? sn[pi] : 0.0f;
+            __nv_bfloat16* orow = og + (int64_t)(32 * hh + odd) * kD + de;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float o1 = __uint_as_float(o[j]) * ms->lsum[h0 + j];
-            if (rope) {
-              const float other = __shfl_xor_sync(0xffffffffu, o1, 1);
-              o1 = (d & 1) ? (-other * ss + o1 * cc) : (o1 * cc + other * ss);
+            for (int j = 0; j < 32; j += 2) {
+              const float v0 = __uint_as_float(o[j]) * inv[j];
+              const float v1 = __uint_as_float(o[j + 1]) * inv[j + 1];
+              const float r = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+              float x = odd ? r : v0, y = odd ? v1 : r;   // even / odd dim of head 32 hh + j + odd
+              if (rope) {
+                const float x2 = x * cc + y * ss;
+                const float y2 = y * cc - x * ss;
+                x = x2;
+                y = y2;
+              }
+              *reinterpret_cast<__nv_bfloat162*>(orow + (int64_t)j * kD) = __floats2bfloat162_rn(x, y);
             }
-            og[(h0 + j) * kD + d] = __float2bfloat16_rn(o1);
           }
         }
       }
       fence_before_sync();
-      if (!group_sync(ms, ns, lane)) {      // every O^T read done; lsum free again
-        ms->abort = 1;
-        flag_timeout(p.ws);
-        break;
-      }
+      __syncwarp();
       if (lane == 0) mbar_arrive(&ms->o_empty);
       ++nq;
+    }
+    if (fail) {
+      ms->abort = 1;
+      if (lane == 0) flag_timeout(p.ws);
     }
   }
   fence_before_sync();
@@ -894,13 +967,14 @@ struct Plan {
   int nsplit;
   bool expand;
   int kpad;
-  size_t list_bytes, part_bytes, x_bytes;
+  size_t qr_bytes, list_bytes, part_bytes, x_bytes;
 };
 
 Plan make_plan(int B, int64_t Tq, int64_t max_keys, int64_t N, int64_t Ts, int k) {
   Plan pl;
   const int64_t rows = (int64_t)B * Tq;
   pl.kpad = (k + 3) & ~3;
+  pl.qr_bytes = al256((size_t)rows * kH * 64 * 2);
   pl.list_bytes = k > 0 ? al256((size_t)rows * pl.kpad * 4) + al256((size_t)rows * 4) : 0;
   pl.nsplit = choose_splits(rows, max_keys);
   pl.part_bytes = pl.nsplit > 1 ? al256((size_t)rows * pl.nsplit * ((size_t)kH * kD * 4 + (size_t)kH * 2 * 4)) : 0;
@@ -931,13 +1005,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Tensor map over bf16 rows of 512 (1 KiB apart): boxes of 64 columns x box_rows
-// rows, 128-byte swizzle, zero fill outside.
-bool make_row_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+// Tensor map over packed bf16 rows of `width` elements: boxes of 64 columns
+// x box_rows rows, 128-byte swizzle, zero fill outside.
+bool make_row_map(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows == 0) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)width * 2};
   const cuuint32_t box[2] = {64u, box_rows};
   const cuuint32_t estr[2] = {1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -950,7 +1024,7 @@ bool make_row_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_
 size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys, int64_t N, int64_t Ts, int k) {
   if (H != kH || D != kD) return 0;
   const Plan pl = make_plan(B, Tq, max_keys, N, Ts, k);
-  return pl.list_bytes + pl.part_bytes + pl.x_bytes;
+  return pl.qr_bytes + pl.list_bytes + pl.part_bytes + pl.x_bytes;
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
@@ -965,7 +1039,6 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
   p.cache = reinterpret_cast<const uint8_t*>(a.cache);
   p.N = a.N;
   p.m = a.m;
-  p.idx = a.idx;
   p.k = a.idx ? a.k : 0;
   p.swa = reinterpret_cast<const uint8_t*>(a.swa);
   p.swa_pos0 = a.swa_pos0;
@@ -981,24 +1054,26 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
   p.part_o = nullptr;
   p.part_ml = nullptr;
   p.xcache = nullptr;
-  p.xswa = nullptr;
   Plan pl = make_plan(a.B, a.Tq, a.max_keys, a.N, a.W > 0 ? a.Ts : 0, a.idx ? a.k : 0);
   size_t avail = a.ws_bytes > csa::kWsHeader ? a.ws_bytes - csa::kWsHeader : 0;
   uint8_t* base = reinterpret_cast<uint8_t*>(a.ws) + csa::kWsHeader;
-  if (pl.list_bytes > avail) return launch_attn_simt(a, st);   // no room for the entry lists
+  // the rotated query dims and the entry lists are required
+  if (pl.qr_bytes + pl.list_bytes > avail) return launch_attn_simt(a, st);
+  __nv_bfloat16* qr = reinterpret_cast<__nv_bfloat16*>(base);
+  base += pl.qr_bytes;
+  avail -= pl.qr_bytes;
   p.kpad = pl.kpad;
   p.clist = nullptr;
   p.ccount = nullptr;
   if (a.idx) {
-    int32_t* cl = reinterpret_cast<int32_t*>(base);
-    int32_t* cc = reinterpret_cast<int32_t*>(base + al256((size_t)rows * pl.kpad * 4));
-    compact_idx_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a.idx, a.q_pos, rows, a.k, pl.kpad, a.N, a.m,
-                                                                  a.rope_rows, cl, cc, a.ws);
-    p.clist = cl;
-    p.ccount = cc;
+    p.clist = reinterpret_cast<int32_t*>(base);
+    p.ccount = reinterpret_cast<int32_t*>(base + al256((size_t)rows * pl.kpad * 4));
     base += pl.list_bytes;
     avail -= pl.list_bytes;
   }
+  prep_rows_kernel<<<(unsigned)rows, 256, 0, st>>>(p.q, a.q_pos, a.rcos, a.rsin, a.rope_rows, qr, a.idx, p.k, pl.kpad,
+                                                   a.N, a.m, const_cast<int32_t*>(p.clist),
+                                                   const_cast<int32_t*>(p.ccount), a.ws);
   if (pl.nsplit > 1 && pl.part_bytes > avail) {   // too little scratch: no split
     pl.nsplit = 1;
     pl.part_bytes = 0;
@@ -1011,30 +1086,29 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
     p.part_ml = reinterpret_cast<float*>(base + (size_t)p.items * kH * kD * 4);
     base += pl.part_bytes;
   }
-  CUtensorMap tm_q, tm_rows;
-  if (!make_row_map(&tm_q, a.q, (uint64_t)rows * kH, 64)) return cudaErrorInvalidValue;
+  CUtensorMap tm_q, tm_qr, tm_rows;
+  if (!make_row_map(&tm_q, a.q, kD, (uint64_t)rows * kH, 64)) return cudaErrorInvalidValue;
+  if (!make_row_map(&tm_qr, qr, 64, (uint64_t)rows * kH, 64)) return cudaErrorInvalidValue;
   tm_rows = tm_q;
   p.xrows = 0;
   p.xwin0 = 0;
   if (pl.expand) {
     const int64_t nc = (int64_t)a.B * a.N, nw = (a.W > 0) ? (int64_t)a.B * a.Ts : 0;
     __nv_bfloat16* xc = reinterpret_cast<__nv_bfloat16*>(base);
-    __nv_bfloat16* xs = xc + nc * kD;
     if (nc > 0) expand_rows_kernel<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(p.cache, nc, xc);
-    if (nw > 0) expand_rows_kernel<<<(unsigned)((nw + 7) / 8), 256, 0, st>>>(p.swa, nw, xs);
+    if (nw > 0) expand_rows_kernel<<<(unsigned)((nw + 7) / 8), 256, 0, st>>>(p.swa, nw, xc + nc * kD);
     p.xcache = xc;
-    p.xswa = xs;
     p.xrows = nc + nw;
     p.xwin0 = nc;
-    if (!make_row_map(&tm_rows, xc, (uint64_t)(nc + nw), 1)) return cudaErrorInvalidValue;
+    if (!make_row_map(&tm_rows, xc, kD, (uint64_t)(nc + nw), 1)) return cudaErrorInvalidValue;
   }
   const int grid = (int)(p.items < num_sms() ? p.items : num_sms());
   if (a.idx) {
     cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q);
+    attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q, tm_qr);
   } else {
     cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q);
+    attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q, tm_qr);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.nsplit == 1) return e;
