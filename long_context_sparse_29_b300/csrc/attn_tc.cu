@@ -65,7 +65,8 @@ constexpr uint32_t kTmemO = 0;       // O^T: 4 blocks of 64 columns (heads); lan
 constexpr uint32_t kTmemS = 256;     // S: 2 buffers of 64 columns (keys); M = 64 layout
 
 constexpr uint32_t kWaitLimit = 1u << 20;    // suspending polls of one mbarrier wait
-constexpr uint32_t kIdleLimit = 1u << 24;    // idle rounds of the MMA event loop
+constexpr uint32_t kIdleLimit = 1u << 22;    // idle rounds of the MMA event loop
+constexpr uint32_t kNapNs = 256;             // longest nap of an idle MMA warp
 constexpr float kLazy = 8.0f;        // log2 growth of a running max that forces a rescale
 
 struct Misc {
@@ -113,6 +114,15 @@ __device__ __forceinline__ bool mbar_test_w(void* bar, uint32_t parity) {
   return __shfl_sync(0xffffffffu, done, 0) != 0;
 }
 
+// Suspend (up to about `ns` nanoseconds) until the phase completes; the
+// result is not needed, the caller tests again.
+__device__ __forceinline__ void mbar_nap(void* bar, uint32_t parity, uint32_t ns) {
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%0], %1, %2;\n}\n" ::"r"(smem_u32(bar)),
+      "r"(parity), "r"(ns)
+      : "memory");
+}
+
 // 2^x by the hardware approximation (a few ulp; P is rounded to bf16 next).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -122,6 +132,16 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// cp.async of 16 bytes, of which the first `src_bytes` (0 or 16) are read
+// and the rest zero-filled.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// An arrive on `bar` once this thread's cp.async copies so far have landed
+// (the pending count is raised now, so the phase waits for it).
+__device__ __forceinline__ void cp_async_mbar_arrive(void* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
@@ -451,32 +471,51 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         if (!ok) break;
       }
       if (p.xcache) {
-        // bf16 rows are ready: each producer warp gathers 16 of the tile's 64
-        // rows with TMA (4 rows x 128 bytes per instruction, 8 column boxes)
+        // bf16 rows are ready.  Producer warp pw fetches rows 16 pw .. 16 pw + 15
+        // of each tile: dims 0..255 by TMA gathers (4 rows x 128 bytes per
+        // instruction, lanes 0..15) and dims 256..511 by 16-byte cp.async
+        // (lane l: 16-byte unit l of each row's upper half) -- the TMA unit
+        // alone cannot gather rows as fast as the tensor core consumes them.
+        // Both complete on kv_full: the TMA by its byte count, the cp.async
+        // through an asynchronous arrive of every lane.
         for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
           const int buf = g & 1;
+          int myrow = (int)p.xrows;          // lane i < 16: row of key 16 pw + i (xrows: none)
+          if (lane < 16) {
+            const int key = tl * kTile + 16 * pw + lane;
+            if (key < I.key_hi) {
+              if (key < I.ne) myrow = (int)((int64_t)I.b * p.N + (DENSE ? (int64_t)key : (int64_t)lst[key]));
+              else myrow = (int)(p.xwin0 + (int64_t)I.b * p.Ts + (I.w_lo - I.p0 + (key - I.ne)));
+            }
+          }
           if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
             ok = false;
             break;
           }
-          if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * kD * 2);
+          const uint32_t tb = smem_u32(sKV + buf * 65536);
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) {
+            const int row = __shfl_sync(0xffffffffu, myrow, rr);
+            const uint32_t r = (uint32_t)(16 * pw + rr);
+            const bool v = row < p.xrows;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.xcache) + (size_t)(v ? row : 0) * (kD * 2) +
+                                 kD + 16 * lane;
+            cp_async16_zfill(tb + (4 + (lane >> 3)) * 8192 + r * 128u + ((((uint32_t)lane & 7u) ^ (r & 7u)) << 4), src,
+                             v ? 16u : 0u);
+          }
+          cp_async_mbar_arrive(&ms->kv_full[buf]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * (kD / 2) * 2);
           __syncwarp();
           {
-            // lane: 4-row group (lane / 8) of this warp's 16 rows, column box lane % 8
-            const int r0 = 16 * pw + 4 * (lane >> 3), cb = lane & 7;
-            int y[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int key = tl * kTile + r0 + e;
-              int64_t row = p.xrows;            // out of range: the box reads zeros
-              if (key < I.key_hi) {
-                if (key < I.ne) row = (int64_t)I.b * p.N + (DENSE ? (int64_t)key : (int64_t)lst[key]);
-                else row = p.xwin0 + (int64_t)I.b * p.Ts + (I.w_lo - I.p0 + (key - I.ne));
-              }
-              y[e] = (int)row;
-            }
-            tma_gather4(smem_u32(sKV + buf * 65536) + cb * 8192 + (uint32_t)r0 * 128u, &tm_rows, 64 * cb, y[0], y[1],
-                        y[2], y[3], &ms->kv_full[buf]);
+            const int rg = (lane >> 2) & 3, cb = lane & 3;
+            const int y0 = __shfl_sync(0xffffffffu, myrow, 4 * rg);
+            const int y1 = __shfl_sync(0xffffffffu, myrow, 4 * rg + 1);
+            const int y2 = __shfl_sync(0xffffffffu, myrow, 4 * rg + 2);
+            const int y3 = __shfl_sync(0xffffffffu, myrow, 4 * rg + 3);
+            if (lane < 16)
+              tma_gather4(tb + cb * 8192 + (uint32_t)(16 * pw + 4 * rg) * 128u, &tm_rows, 64 * cb, y0, y1, y2, y3,
+                          &ms->kv_full[buf]);
           }
           __syncwarp();
         }
@@ -598,38 +637,62 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
     };
     while (have || gp != gq) {
       bool did = false;
-      if (gp != gq && mbar_test_w(&ms->p_full[gp & 1], (gp >> 1) & 1) &&
-          (!f0 || q0 == 0 || mbar_test_w(&ms->o_empty, (q0 - 1) & 1))) {
-        fence_after_sync();
-        const uint64_t vd0 = sdesc_sw128(aKV + (gp & 1) * 65536, 8192, 1024);
-        const uint64_t pd0 = sdesc_sw128(aP + (gp & 1) * 8192, 16, 1024);
+      void* nap = nullptr;                  // the barrier that blocks the oldest candidate
+      uint32_t nap_par = 0;
+      if (gp != gq) {
+        if (!mbar_test_w(&ms->p_full[gp & 1], (gp >> 1) & 1)) {
+          nap = &ms->p_full[gp & 1];
+          nap_par = (gp >> 1) & 1;
+        } else if (f0 && q0 > 0 && !mbar_test_w(&ms->o_empty, (q0 - 1) & 1)) {
+          nap = &ms->o_empty;
+          nap_par = (q0 - 1) & 1;
+        } else {
+          fence_after_sync();
+          const uint64_t vd0 = sdesc_sw128(aKV + (gp & 1) * 65536, 8192, 1024);
+          const uint64_t pd0 = sdesc_sw128(aP + (gp & 1) * 8192, 16, 1024);
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
+          for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            mma_bf16_elect(tmem + kTmemO + 64u * mt, vd0 + (uint64_t)((2 * mt * 8192 + ks * 2048) >> 4),
-                           pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!f0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < kTile / 16; ++ks)
+              mma_bf16_elect(tmem + kTmemO + 64u * mt, vd0 + (uint64_t)((2 * mt * 8192 + ks * 2048) >> 4),
+                             pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!f0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit_elect(&ms->kv_empty[gp & 1]);
+          if (l0) mma_commit_elect(&ms->o_full);
+          __syncwarp();
+          f0 = f1;
+          l0 = l1;
+          q0 = q1;
+          ++gp;
+          did = true;
         }
-        mma_commit_elect(&ms->kv_empty[gp & 1]);
-        if (l0) mma_commit_elect(&ms->o_full);
-        __syncwarp();
-        f0 = f1;
-        l0 = l1;
-        q0 = q1;
-        ++gp;
-        did = true;
-      } else if (q_load) {
+      }
+      if (!did && q_load) {
         if (nq == 0 || mbar_test_w(&ms->q_empty, (nq - 1) & 1)) {
           issue_q(I.row);
           q_load = false;
           q_pending = true;
           did = true;
+        } else if (!nap) {
+          nap = &ms->q_empty;
+          nap_par = (nq - 1) & 1;
         }
-      } else if (have && gq - gp < 2) {
+      } else if (!did && have && gq - gp < 2) {
         if (!q_in) q_in = mbar_test_w(&ms->q_full, nq & 1);
-        if (q_in && mbar_test_w(&ms->kv_full[gq & 1], (gq >> 1) & 1)) {
+        if (!q_in) {
+          if (!nap) {
+            nap = &ms->q_full;
+            nap_par = nq & 1;
+          }
+        } else if (!mbar_test_w(&ms->kv_full[gq & 1], (gq >> 1) & 1)) {
+          if (!nap) {
+            nap = &ms->kv_full[gq & 1];
+            nap_par = (gq >> 1) & 1;
+          }
+        } else {
           q_pending = false;
           fence_after_sync();
+          fence_proxy_async();   // the tile's cp.async part was written through the generic proxy
           const bool first = tq == I.tlo, last = tq == I.thi - 1;
           const uint32_t dS = tmem + kTmemS + 64u * (gq & 1);
           const uint64_t qd0 = sdesc_sw128(aQ, 16, 1024);
@@ -670,6 +733,10 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
       } else if (++idle > kIdleLimit || vabort(ms)) {
         ok = false;
         break;
+      } else if (nap) {
+        // nothing to issue: sleep on the blocking barrier instead of spinning,
+        // so the softmax warp sharing this SM sub-partition keeps its issue slots
+        mbar_nap(nap, nap_par, kNapNs);
       }
     }
     if (!ok) {
@@ -843,37 +910,51 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
       } else {
         // lane pairs swap values so that each lane holds two adjacent dims of
         // one head: lane 2i takes head j, lane 2i + 1 head j + 1; a RoPE pair
-        // is then rotated back within one lane and stored as one bf16x2
+        // is then rotated back within one lane and stored as one bf16x2.  The
+        // phases (scale all, swap all, store all) keep the latencies overlapped.
         __nv_bfloat16* og = p.out + I.row * (int64_t)(kH * kD);
         const int odd = lane & 1;
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          const float* inv = lsv + 32 * hh;
-#pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
-            uint32_t o[32];
-            tmem_ld32(tmem + tq_lane + kTmemO + 64u * mt + 32u * hh, o);
-            tmem_wait_ld();
-            const int de = 128 * mt + 32 * qd + (lane & ~1);
-            const bool rope = de >= kMixDn;          // warp-uniform
-            const int pi = rope ? (de - kMixDn) >> 1 : 0;
-            const float cc = rope ? cs[pi] : 1.0f, ss = rope ? sn[pi] : 0.0f;
-            __nv_bfloat16* orow = og + (int64_t)(32 * hh + odd) * kD + de;
+        for (int c = 0; c < 8; ++c) {
+          const int mt = c >> 1, hh = c & 1;
+          uint32_t o[32];
+          tmem_ld32(tmem + tq_lane + kTmemO + 64u * mt + 32u * hh, o);
+          float inv[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float v0 = __uint_as_float(o[j]) * inv[j];
-              const float v1 = __uint_as_float(o[j + 1]) * inv[j + 1];
-              const float r = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-              float x = odd ? r : v0, y = odd ? v1 : r;   // even / odd dim of head 32 hh + j + odd
-              if (rope) {
-                const float x2 = x * cc + y * ss;
-                const float y2 = y * cc - x * ss;
-                x = x2;
-                y = y2;
-              }
-              *reinterpret_cast<__nv_bfloat162*>(orow + (int64_t)j * kD) = __floats2bfloat162_rn(x, y);
-            }
+          for (int j = 0; j < 32; j += 4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(lsv + 32 * hh + j);
+            inv[j] = v4.x;
+            inv[j + 1] = v4.y;
+            inv[j + 2] = v4.z;
+            inv[j + 3] = v4.w;
           }
+          const int de = 128 * mt + 32 * qd + (lane & ~1);
+          const bool rope = de >= kMixDn;          // warp-uniform
+          const int pi = rope ? (de - kMixDn) >> 1 : 0;
+          const float cc = rope ? cs[pi] : 1.0f, ss = rope ? sn[pi] : 0.0f;
+          tmem_wait_ld();
+          float f[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(o[j]) * inv[j];
+          float r[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) r[j] = __shfl_xor_sync(0xffffffffu, odd ? f[2 * j] : f[2 * j + 1], 1);
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float x = odd ? r[j] : f[2 * j], y = odd ? f[2 * j + 1] : r[j];   // even / odd dim
+            if (rope) {
+              const float x2 = x * cc + y * ss;
+              const float y2 = y * cc - x * ss;
+              x = x2;
+              y = y2;
+            }
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(x, y);
+            pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          uint32_t* orow = reinterpret_cast<uint32_t*>(og + (int64_t)(32 * hh + odd) * kD + de);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) orow[(int64_t)j * kD] = pk[j];   // head 32 hh + 2 j + odd
         }
       }
       fence_before_sync();
@@ -1079,6 +1160,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
     pl.part_bytes = 0;
   }
   if (pl.expand && pl.part_bytes + pl.x_bytes > avail) pl.expand = false;
+  if ((int64_t)a.B * (a.N + (a.W > 0 ? a.Ts : 0)) >= INT32_MAX) pl.expand = false;   // TMA rows are int32
   p.nsplit = pl.nsplit;
   p.items = rows * p.nsplit;
   if (p.nsplit > 1) {
