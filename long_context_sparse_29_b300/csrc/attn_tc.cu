@@ -138,10 +138,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-// An arrive on `bar` once this thread's cp.async copies so far have landed
-// (the pending count is raised now, so the phase waits for it).
-__device__ __forceinline__ void cp_async_mbar_arrive(void* bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+// An arrive on `bar` once this thread's cp.async copies so far have landed;
+// it is one of the arrivals the barrier's count expects.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(void* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
@@ -412,7 +412,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
   if (tid == 0) {
     ms->abort = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms->kv_full[i], 4);
+      mbar_init(&ms->kv_full[i], 4 + 128);   // per producer warp: one arrival, + one per lane
       mbar_init(&ms->kv_empty[i], 1);
       mbar_init(&ms->s_full[i], 1);
       mbar_init(&ms->p_full[i], 4);
@@ -477,7 +477,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         // (lane l: 16-byte unit l of each row's upper half) -- the TMA unit
         // alone cannot gather rows as fast as the tensor core consumes them.
         // Both complete on kv_full: the TMA by its byte count, the cp.async
-        // through an asynchronous arrive of every lane.
+        // through a counted asynchronous arrive of every lane.
         for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
           const int buf = g & 1;
           int myrow = (int)p.xrows;          // lane i < 16: row of key 16 pw + i (xrows: none)
@@ -493,18 +493,6 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
             break;
           }
           const uint32_t tb = smem_u32(sKV + buf * 65536);
-#pragma unroll
-          for (int rr = 0; rr < 16; ++rr) {
-            const int row = __shfl_sync(0xffffffffu, myrow, rr);
-            const uint32_t r = (uint32_t)(16 * pw + rr);
-            const bool v = row < p.xrows;
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.xcache) + (size_t)(v ? row : 0) * (kD * 2) +
-                                 kD + 16 * lane;
-            cp_async16_zfill(tb + (4 + (lane >> 3)) * 8192 + r * 128u + ((((uint32_t)lane & 7u) ^ (r & 7u)) << 4), src,
-                             v ? 16u : 0u);
-          }
-          cp_async_mbar_arrive(&ms->kv_full[buf]);
-          __syncwarp();
           if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * (kD / 2) * 2);
           __syncwarp();
           {
@@ -517,6 +505,17 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
               tma_gather4(tb + cb * 8192 + (uint32_t)(16 * pw + 4 * rg) * 128u, &tm_rows, 64 * cb, y0, y1, y2, y3,
                           &ms->kv_full[buf]);
           }
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) {
+            const int row = __shfl_sync(0xffffffffu, myrow, rr);
+            const uint32_t r = (uint32_t)(16 * pw + rr);
+            const bool v = row < p.xrows;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.xcache) + (size_t)(v ? row : 0) * (kD * 2) +
+                                 kD + 16 * lane;
+            cp_async16_zfill(tb + (4 + (lane >> 3)) * 8192 + r * 128u + ((((uint32_t)lane & 7u) ^ (r & 7u)) << 4), src,
+                             v ? 16u : 0u);
+          }
+          cp_async_mbar_arrive_noinc(&ms->kv_full[buf]);
           __syncwarp();
         }
       } else {
@@ -581,6 +580,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
           }
           cp_async_wait_all();
           fence_proxy_async();
+          cp_async_mbar_arrive_noinc(&ms->kv_full[buf]);   // nothing in flight: arrives at once
           __syncwarp();
           if (lane == 0) mbar_arrive(&ms->kv_full[buf]);
         }
@@ -635,37 +635,47 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
       else if (lane == 7) tma_load_2d(aQ + 7 * 8192, &tm_qr, 0, (int)(row * kH), &ms->q_full);
       __syncwarp();
     };
+    // PV of tile gp: P in smem (and, first tile of an item, O^T free)?  Sets
+    // the barrier to nap on when not.
+    auto pv_ready = [&](void*& nap, uint32_t& nap_par) -> bool {
+      if (!mbar_test_w(&ms->p_full[gp & 1], (gp >> 1) & 1)) {
+        nap = &ms->p_full[gp & 1];
+        nap_par = (gp >> 1) & 1;
+        return false;
+      }
+      if (f0 && q0 > 0 && !mbar_test_w(&ms->o_empty, (q0 - 1) & 1)) {
+        nap = &ms->o_empty;
+        nap_par = (q0 - 1) & 1;
+        return false;
+      }
+      return true;
+    };
+    auto issue_pv = [&]() {
+      fence_after_sync();
+      const uint64_t vd0 = sdesc_sw128(aKV + (gp & 1) * 65536, 8192, 1024);
+      const uint64_t pd0 = sdesc_sw128(aP + (gp & 1) * 8192, 16, 1024);
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_bf16_elect(tmem + kTmemO + 64u * mt, vd0 + (uint64_t)((2 * mt * 8192 + ks * 2048) >> 4),
+                         pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!f0 || ks > 0) ? 1u : 0u);
+      }
+      mma_commit_elect(&ms->kv_empty[gp & 1]);
+      if (l0) mma_commit_elect(&ms->o_full);
+      __syncwarp();
+      f0 = f1;
+      l0 = l1;
+      q0 = q1;
+      ++gp;
+    };
     while (have || gp != gq) {
       bool did = false;
       void* nap = nullptr;                  // the barrier that blocks the oldest candidate
       uint32_t nap_par = 0;
-      if (gp != gq) {
-        if (!mbar_test_w(&ms->p_full[gp & 1], (gp >> 1) & 1)) {
-          nap = &ms->p_full[gp & 1];
-          nap_par = (gp >> 1) & 1;
-        } else if (f0 && q0 > 0 && !mbar_test_w(&ms->o_empty, (q0 - 1) & 1)) {
-          nap = &ms->o_empty;
-          nap_par = (q0 - 1) & 1;
-        } else {
-          fence_after_sync();
-          const uint64_t vd0 = sdesc_sw128(aKV + (gp & 1) * 65536, 8192, 1024);
-          const uint64_t pd0 = sdesc_sw128(aP + (gp & 1) * 8192, 16, 1024);
-#pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks)
-              mma_bf16_elect(tmem + kTmemO + 64u * mt, vd0 + (uint64_t)((2 * mt * 8192 + ks * 2048) >> 4),
-                             pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!f0 || ks > 0) ? 1u : 0u);
-          }
-          mma_commit_elect(&ms->kv_empty[gp & 1]);
-          if (l0) mma_commit_elect(&ms->o_full);
-          __syncwarp();
-          f0 = f1;
-          l0 = l1;
-          q0 = q1;
-          ++gp;
-          did = true;
-        }
+      if (gp != gq && pv_ready(nap, nap_par)) {
+        issue_pv();
+        did = true;
       }
       if (!did && q_load) {
         if (nq == 0 || mbar_test_w(&ms->q_empty, (nq - 1) & 1)) {
