@@ -49,8 +49,9 @@ namespace {
 constexpr int kH = 64;
 constexpr int kD = 512;
 constexpr int kTile = 64;
-constexpr int kThreads = 9 * 32;
-constexpr int kMmaWarp = 8;
+constexpr int kThreads = 10 * 32;
+constexpr int kMmaWarp = 8;       // QK^T issue, query loads, TMEM owner
+constexpr int kPvWarp = 9;        // PV issue
 
 constexpr uint32_t kQOff = 0;                     // 8 chunks x [64 heads x 128 B]
 constexpr uint32_t kKVOff = 65536;                // 2 buffers x 8 chunks x [64 keys x 128 B]
@@ -65,20 +66,19 @@ constexpr uint32_t kTmemO = 0;       // O^T: 4 blocks of 64 columns (heads); lan
 constexpr uint32_t kTmemS = 256;     // S: 2 buffers of 64 columns (keys); M = 64 layout
 
 constexpr uint32_t kWaitLimit = 1u << 20;    // suspending polls of one mbarrier wait
-constexpr uint32_t kIdleLimit = 1u << 22;    // idle rounds of the MMA event loop
-constexpr uint32_t kNapNs = 256;             // longest nap of an idle MMA warp
 constexpr float kLazy = 8.0f;        // log2 growth of a running max that forces a rescale
 
 struct Misc {
   uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
-  uint64_t q_full, q_empty, o_full, o_empty, drain;
+  uint64_t q_full, q_empty, o_full, o_empty, drain[2];
   uint64_t list_full[2], list_empty[2];  // entry list handover, double-buffered
   uint32_t tmem;
   int abort;
-  float alpha[2][kH];            // per-head rescale factors of a tile, double-buffered
-  float lsum[2][kH];             // per-head 1 / sum of an item, double-buffered
+  alignas(16) float alpha[2][kH];   // per-head rescale factors of a tile, double-buffered
+  alignas(16) float lsum[2][kH];    // per-head 1 / sum of an item, double-buffered (read as float4)
 };
 static_assert(sizeof(Misc) <= 2048, "Misc overflows its smem slot");
+static_assert(offsetof(Misc, lsum) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0, "vector reads of Misc");
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk16) {
   return row * 128u + (((chunk16 ^ row) & 7u) << 4);
@@ -102,27 +102,6 @@ __device__ __forceinline__ bool vabort(const Misc* ms) {
   return *reinterpret_cast<const volatile int*>(&ms->abort) != 0;
 }
 
-// Non-blocking test of an mbarrier phase, decided by lane 0 for the warp.
-__device__ __forceinline__ bool mbar_test_w(void* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return __shfl_sync(0xffffffffu, done, 0) != 0;
-}
-
-// Suspend (up to about `ns` nanoseconds) until the phase completes; the
-// result is not needed, the caller tests again.
-__device__ __forceinline__ void mbar_nap(void* bar, uint32_t parity, uint32_t ns) {
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%0], %1, %2;\n}\n" ::"r"(smem_u32(bar)),
-      "r"(parity), "r"(ns)
-      : "memory");
-}
-
 // 2^x by the hardware approximation (a few ulp; P is rounded to bf16 next).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -133,6 +112,10 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 // cp.async of 16 bytes, of which the first `src_bytes` (0 or 16) are read
 // and the rest zero-filled.
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -423,7 +406,8 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
     mbar_init(&ms->q_empty, 1);
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->o_empty, 4);
-    mbar_init(&ms->drain, 1);
+    mbar_init(&ms->drain[0], 1);
+    mbar_init(&ms->drain[1], 1);
     mbar_fence_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&ms->tmem, kTmemCols);
@@ -609,25 +593,19 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
     if (p.xcache && g > 0) mbar_wait(&ms->kv_full[(g - 1) & 1], ((g - 1) >> 1) & 1, kWaitLimit);
     if (nl > 0) mbar_wait(&ms->list_full[(nl - 1) & 1], ((nl - 1) >> 1) & 1, kWaitLimit);
   } else if (warp == kMmaWarp) {
-    // ================================ MMA issue ================================
-    // Event loop: PV of the oldest tile whose P is ready, else the next
-    // query load, else QK of the next tile whose keys and query are in.
-    // QK of tile g reuses the S buffer and ring slot of tile g - 2, so it
-    // waits until PV of tile g - 2 is issued (the softmax has read S, and
-    // the tensor core runs in order); the first PV of an item overwrites
-    // O^T, so it waits for the previous item's epilogue.
-    const uint32_t aQ = smem_u32(sQ), aKV = smem_u32(sKV), aP = smem_u32(sP);
+    // ============================== QK^T issue ==============================
+    // S of tile g goes to TMEM buffer g & 1; it is written once the softmax
+    // has released the buffer's previous tile (its P is ready) and the keys
+    // are in.  The query of the next item is loaded when the last QK^T of
+    // this one has completed, and pulled into L2 one item earlier.
+    const uint32_t aQ = smem_u32(sQ), aKV = smem_u32(sKV);
     constexpr uint32_t idQK = idesc_bf16(64, kTile, 0, 0);
-    constexpr uint32_t idPV = idesc_bf16(128, kH, 1, 0);
     Cursor<DENSE> cur(p);
-    Item I;
+    Item I, In;
     bool have = cur.nonempty(p, I);
-    int tq = have ? I.tlo : 0;
-    uint32_t gq = 0, gp = 0, nq = 0;        // next QK tile, next PV tile, ordinal of item I
-    bool f0 = false, l0 = false, f1 = false, l1 = false;   // first / last of tiles gp, gp + 1
-    uint32_t q0 = 0, q1 = 0;                // their item ordinals
-    bool q_load = have, q_in = false, q_pending = false, ok = true;
-    uint32_t idle = 0;
+    bool have_n = have && cur.nonempty(p, In);
+    uint32_t g = 0, nq = 0;
+    bool ok = true, q_pending = false;
     auto issue_q = [&](int64_t row) {
       if (lane == 0) mbar_arrive_expect_tx(&ms->q_full, kH * kD * 2);
       __syncwarp();
@@ -635,119 +613,50 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
       else if (lane == 7) tma_load_2d(aQ + 7 * 8192, &tm_qr, 0, (int)(row * kH), &ms->q_full);
       __syncwarp();
     };
-    // PV of tile gp: P in smem (and, first tile of an item, O^T free)?  Sets
-    // the barrier to nap on when not.
-    auto pv_ready = [&](void*& nap, uint32_t& nap_par) -> bool {
-      if (!mbar_test_w(&ms->p_full[gp & 1], (gp >> 1) & 1)) {
-        nap = &ms->p_full[gp & 1];
-        nap_par = (gp >> 1) & 1;
-        return false;
-      }
-      if (f0 && q0 > 0 && !mbar_test_w(&ms->o_empty, (q0 - 1) & 1)) {
-        nap = &ms->o_empty;
-        nap_par = (q0 - 1) & 1;
-        return false;
-      }
-      return true;
-    };
-    auto issue_pv = [&]() {
-      fence_after_sync();
-      const uint64_t vd0 = sdesc_sw128(aKV + (gp & 1) * 65536, 8192, 1024);
-      const uint64_t pd0 = sdesc_sw128(aP + (gp & 1) * 8192, 16, 1024);
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_bf16_elect(tmem + kTmemO + 64u * mt, vd0 + (uint64_t)((2 * mt * 8192 + ks * 2048) >> 4),
-                         pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!f0 || ks > 0) ? 1u : 0u);
-      }
-      mma_commit_elect(&ms->kv_empty[gp & 1]);
-      if (l0) mma_commit_elect(&ms->o_full);
-      __syncwarp();
-      f0 = f1;
-      l0 = l1;
-      q0 = q1;
-      ++gp;
-    };
-    while (have || gp != gq) {
-      bool did = false;
-      void* nap = nullptr;                  // the barrier that blocks the oldest candidate
-      uint32_t nap_par = 0;
-      if (gp != gq && pv_ready(nap, nap_par)) {
-        issue_pv();
-        did = true;
-      }
-      if (!did && q_load) {
-        if (nq == 0 || mbar_test_w(&ms->q_empty, (nq - 1) & 1)) {
-          issue_q(I.row);
-          q_load = false;
-          q_pending = true;
-          did = true;
-        } else if (!nap) {
-          nap = &ms->q_empty;
-          nap_par = (nq - 1) & 1;
-        }
-      } else if (!did && have && gq - gp < 2) {
-        if (!q_in) q_in = mbar_test_w(&ms->q_full, nq & 1);
-        if (!q_in) {
-          if (!nap) {
-            nap = &ms->q_full;
-            nap_par = nq & 1;
-          }
-        } else if (!mbar_test_w(&ms->kv_full[gq & 1], (gq >> 1) & 1)) {
-          if (!nap) {
-            nap = &ms->kv_full[gq & 1];
-            nap_par = (gq >> 1) & 1;
-          }
-        } else {
-          q_pending = false;
-          fence_after_sync();
-          fence_proxy_async();   // the tile's cp.async part was written through the generic proxy
-          const bool first = tq == I.tlo, last = tq == I.thi - 1;
-          const uint32_t dS = tmem + kTmemS + 64u * (gq & 1);
-          const uint64_t qd0 = sdesc_sw128(aQ, 16, 1024);
-          const uint64_t kd0 = sdesc_sw128(aKV + (gq & 1) * 65536, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint64_t off = (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
-            mma_bf16_elect(dS, qd0 + off, kd0 + off, idQK, kk > 0 ? 1u : 0u);
-          }
-          mma_commit_elect(&ms->s_full[gq & 1]);
-          if (last) mma_commit_elect(&ms->q_empty);
-          __syncwarp();
-          if (gq == gp) {
-            f0 = first;
-            l0 = last;
-            q0 = nq;
-          } else {
-            f1 = first;
-            l1 = last;
-            q1 = nq;
-          }
-          ++gq;
-          ++tq;
-          if (last) {
-            ++nq;
-            q_in = false;
-            have = cur.nonempty(p, I);
-            if (have) {
-              tq = I.tlo;
-              q_load = true;
-            }
-          }
-          did = true;
-        }
-      }
-      if (did) {
-        idle = 0;
-      } else if (++idle > kIdleLimit || vabort(ms)) {
+    while (have && ok && !vabort(ms)) {
+      if (nq > 0 && !mbar_wait(&ms->q_empty, (nq - 1) & 1, kWaitLimit)) {
         ok = false;
         break;
-      } else if (nap) {
-        // nothing to issue: sleep on the blocking barrier instead of spinning,
-        // so the softmax warp sharing this SM sub-partition keeps its issue slots
-        mbar_nap(nap, nap_par, kNapNs);
       }
+      issue_q(I.row);
+      q_pending = true;
+      if (have_n && lane == 0) {   // the next item's query: into L2 now
+        prefetch_l2(p.q + In.row * (int64_t)(kH * kD), kH * kD * 2);
+      }
+      if (!mbar_wait(&ms->q_full, nq & 1, kWaitLimit)) {
+        ok = false;
+        break;
+      }
+      q_pending = false;
+      for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
+        // S buffer g & 1 is free once the softmax of tile g - 2 has made its P
+        if (g >= 2 && !mbar_wait(&ms->p_full[g & 1], ((g >> 1) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&ms->kv_full[g & 1], (g >> 1) & 1, kWaitLimit)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        fence_proxy_async();   // the tile's cp.async part was written through the generic proxy
+        const uint32_t dS = tmem + kTmemS + 64u * (g & 1);
+        const uint64_t qd0 = sdesc_sw128(aQ, 16, 1024);
+        const uint64_t kd0 = sdesc_sw128(aKV + (g & 1) * 65536, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t off = (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
+          mma_bf16_elect(dS, qd0 + off, kd0 + off, idQK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_elect(&ms->s_full[g & 1]);
+        if (tl == I.thi - 1) mma_commit_elect(&ms->q_empty);
+        __syncwarp();
+      }
+      if (!ok) break;
+      ++nq;
+      I = In;
+      have = have_n;
+      if (have) have_n = cur.nonempty(p, In);
     }
     if (!ok) {
       ms->abort = 1;
@@ -755,9 +664,51 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
       if (q_pending) mbar_wait(&ms->q_full, nq & 1, kWaitLimit);   // the query copy in flight
     }
     // every MMA this warp issued completes before TMEM is released
-    mma_commit_elect(&ms->drain);
+    mma_commit_elect(&ms->drain[0]);
     __syncwarp();
-    mbar_wait(&ms->drain, 0, kWaitLimit);
+    mbar_wait(&ms->drain[0], 0, kWaitLimit);
+  } else if (warp == kPvWarp) {
+    // ================================ PV issue ================================
+    // O^T += V^T P^T as soon as P of the tile is in smem; the first tile of
+    // an item overwrites O^T, so it waits for the previous item's epilogue.
+    // Its completion frees the tile's ring slot (kv_empty).
+    const uint32_t aKV = smem_u32(sKV), aP = smem_u32(sP);
+    constexpr uint32_t idPV = idesc_bf16(128, kH, 1, 0);
+    Cursor<DENSE> cur(p);
+    Item I;
+    uint32_t g = 0, nq = 0;
+    bool ok = true;
+    while (ok && !vabort(ms) && cur.nonempty(p, I)) {
+      for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
+        const bool first = tl == I.tlo, last = tl == I.thi - 1;
+        if (!mbar_wait(&ms->p_full[g & 1], (g >> 1) & 1, kWaitLimit) ||
+            (first && nq > 0 && !mbar_wait(&ms->o_empty, (nq - 1) & 1, kWaitLimit))) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const uint64_t vd0 = sdesc_sw128(aKV + (g & 1) * 65536, 8192, 1024);
+        const uint64_t pd0 = sdesc_sw128(aP + (g & 1) * 8192, 16, 1024);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_bf16_elect(tmem + kTmemO + 64u * mt, vd0 + (uint64_t)((2 * mt * 8192 + ks * 2048) >> 4),
+                           pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!first || ks > 0) ? 1u : 0u);
+        }
+        mma_commit_elect(&ms->kv_empty[g & 1]);
+        if (last) mma_commit_elect(&ms->o_full);
+        __syncwarp();
+      }
+      ++nq;
+    }
+    if (!ok) {
+      ms->abort = 1;
+      if (lane == 0) flag_timeout(p.ws);
+    }
+    mma_commit_elect(&ms->drain[1]);
+    __syncwarp();
+    mbar_wait(&ms->drain[1], 0, kWaitLimit);
   } else {
     // ============================ softmax / epilogue ============================
     // S (64 heads x 64 keys) sits in lanes 0-15 of every TMEM quadrant; the
@@ -862,6 +813,9 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         }
         ma = na;
         mb = nb;
+        // P buffer g & 1 was last read by PV of tile g - 2 (another warp's
+        // MMAs: S being ready does not imply it), so wait for that PV
+        if (g >= 2 && !fail && !mbar_wait(&ms->kv_empty[g & 1], ((g >> 1) - 1) & 1, kWaitLimit)) fail = true;
         float sa = 0.0f, sb2 = 0.0f;
         uint8_t* dst = sP + (g & 1) * 8192;
 #pragma unroll
