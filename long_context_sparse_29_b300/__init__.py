@@ -171,7 +171,7 @@ def indexer_topk(qI, w, kI, kI_scales, q_pos, N: int, m: int, k: int, scores: bo
     if scores and score_out is None:
         score_out = torch.empty((B, Tq, k), dtype=torch.float32, device=dev)
     ws = _ws(ws, dev)
-    need = workspace_size(OP_INDEXER_TOPK, B, Tq, N, k, 0, 0, 0, 0)
+    need = workspace_size(OP_INDEXER_TOPK, B, Tq, N, k, HI, dI, 0, 0)
     buf = ws.get(need)
     check(lib().csa_indexer_topk(_ptr(qI), _dt(qI), _ptr(w), _ptr(kI), _ptr(kI_scales), fmt,
                                  _ptr(q_pos), B, Tq, HI, dI, N, m, k, _ptr(idx_out),

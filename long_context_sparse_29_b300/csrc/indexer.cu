@@ -334,20 +334,27 @@ int topk_pad(int k) {
 cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
                                 const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
                                 int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
-                                float* score_out, float* scores_ws, cudaStream_t st) {
+                                float* score_out, float* scores_ws, void* tc_ws, void* flags_ws,
+                                cudaStream_t st) {
   if ((int64_t)B * Tq == 0) return cudaSuccess;
   if (N > 0) {
-    const dim3 grid((unsigned)((N + kScoreThreads - 1) / kScoreThreads),
-                    (unsigned)((Tq + kScoreQT - 1) / kScoreQT), (unsigned)B);
-    if (fp4)
-      scores_fp4_kernel<<<grid, kScoreThreads, 0, st>>>(
-          reinterpret_cast<const __nv_bfloat16*>(qI), w, reinterpret_cast<const uint8_t*>(kI),
-          kI_scales, q_pos, Tq, HI, N, m, scores_ws);
-    else
-      scores_f32_kernel<<<grid, kScoreThreads, 0, st>>>(reinterpret_cast<const float*>(qI), w,
-                                                        reinterpret_cast<const float*>(kI), q_pos,
-                                                        Tq, HI, dI, N, m, scores_ws);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (fp4 && tc_ws && indexer_tc_applies(B, Tq, HI, dI, N)) {
+      e = launch_indexer_scores_tc(qI, w, reinterpret_cast<const uint8_t*>(kI), kI_scales, q_pos, B, Tq, HI, N,
+                                   m, scores_ws, tc_ws, flags_ws, st);
+    } else {
+      const dim3 grid((unsigned)((N + kScoreThreads - 1) / kScoreThreads),
+                      (unsigned)((Tq + kScoreQT - 1) / kScoreQT), (unsigned)B);
+      if (fp4)
+        scores_fp4_kernel<<<grid, kScoreThreads, 0, st>>>(
+            reinterpret_cast<const __nv_bfloat16*>(qI), w, reinterpret_cast<const uint8_t*>(kI),
+            kI_scales, q_pos, Tq, HI, N, m, scores_ws);
+      else
+        scores_f32_kernel<<<grid, kScoreThreads, 0, st>>>(reinterpret_cast<const float*>(qI), w,
+                                                          reinterpret_cast<const float*>(kI), q_pos,
+                                                          Tq, HI, dI, N, m, scores_ws);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
   }
   const int kpad = topk_pad(k);

@@ -1,0 +1,481 @@
+// indexer_tc.cu -- lightning-indexer scores on the FP8 tensor cores.
+//
+// xmsumi.com DeepSeek-V4 article, section "CSA（压缩稀疏注意力）": a lightning
+// indexer scores every visible compressed entry for each query token, and
+// section "关键技术细节": its attention runs in FP4.
+//
+// score(t, j) = sum_h w_{t,h} relu(d_{t,h,j}), the head sum an fma chain from
+// +0 in ascending h, and d = P0 2^(e_q0 + e_k0 - 2) + P1 2^(e_q1 + e_k1 - 2)
+// rounded once, where P_b is the dot of the two 32-element MXFP4 blocks b
+// with every E2M1 value doubled (an integer in [-12, 12]).  These are the
+// same numbers as the dp4a kernel in indexer.cu computes.
+//
+// Here P_b comes from tcgen05.mma kind::f8f6f4: the doubled E2M1 values are
+// small integers, exact in E4M3, and every partial sum of 32 products of
+// them is an integer below 2^13, exact in the fp32 accumulator whatever the
+// order of the additions -- so P_b is the exact integer, and the scores are
+// bit-identical to the integer path.
+//
+// Work: one CTA per (128 query rows, 256 entries) of a sequence, entries past
+// the last visible one skipped.  Warp 8 loads the quantised queries (all
+// heads, 128 KiB) once and a ring of entry tiles (64 entries) with TMA;
+// warp 9 issues, per tile and head, the two block MMAs (M = 128 rows, N = 64
+// entries, K = 32) into one of four TMEM buffers; warps 0-7 (row quadrant
+// w % 4, entry half w / 4) combine the blocks, apply relu and the head
+// weights in ascending head order and store the scores.
+#include <cuda.h>
+
+#include "csa_common.cuh"
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace csa {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kIxRows = 128;       // query rows per CTA (MMA M)
+constexpr int kIxKeys = 64;        // entries per tile (MMA N)
+constexpr int kIxChunk = 256;      // entries per CTA
+constexpr int kIxStages = 4;       // entry-tile ring
+constexpr int kIxBufs = 4;         // TMEM head buffers, 128 columns each (block 0 | block 1)
+constexpr int kIxMaxHeads = 16;
+constexpr int kIxThreads = 10 * 32;
+constexpr int kIxProducer = 8, kIxMma = 9;
+
+constexpr uint32_t kIxQChunk = kIxRows * 128;                 // two heads x 64 dims, 128 rows
+constexpr uint32_t kIxKTile = kIxKeys * 128;                  // 64 entries x 128 B (64 data + 64 zero)
+constexpr uint32_t kIxKOff = (kIxMaxHeads / 2) * kIxQChunk;   // 128 KiB of queries
+constexpr uint32_t kIxMiscOff = kIxKOff + kIxStages * kIxKTile;
+constexpr uint32_t kIxSmem = kIxMiscOff + 1024 + 1024;        // + slack for 1 KiB alignment
+
+constexpr uint32_t kIxWait = 1u << 20;
+
+struct IxMisc {
+  uint64_t q_full, k_full[kIxStages], k_empty[kIxStages], t_full[kIxBufs], t_empty[kIxBufs], drain;
+  uint32_t tmem;
+  int nv_max;
+};
+
+// 2 x E2M1 value of a code, as the E4M3 byte that holds it exactly
+// (magnitudes 0, 1, 2, 3, 4, 6, 8, 12; bit 3 of the code is the sign)
+__device__ __forceinline__ uint32_t e2m1x2_e4m3(uint32_t code) {
+  const uint32_t mag = 0x54504C4844403800ull >> (8 * (code & 7)) & 0xffu;   // (lookup in a 64-bit word)
+  return mag | ((code & 8u) << 4);
+}
+
+// kind::f8f6f4 instruction descriptor: E4M3 A and B (format 0), fp32 D,
+// both K-major; N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_e4m3_elect(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, 0, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc));
+}
+
+__device__ __forceinline__ int64_t visible(int64_t t, int m, int64_t N) {
+  int64_t nv = (t + 1) / m;
+  nv = nv < 0 ? 0 : nv;
+  return nv < N ? nv : N;
+}
+
+}  // namespace
+
+// Query quantisation: one thread per (row, head, 32-block); MXFP4 with the
+// block exponent floor(log2 amax) - 2, each value stored as the E4M3 byte of
+// twice its E2M1 value.  qx: [rows, HI * 64] bytes; qe: [rows, HI, 2].
+__global__ void __launch_bounds__(256)
+ix_quant_q_kernel(const __nv_bfloat16* __restrict__ qI, int64_t rows, int HI, uint8_t* __restrict__ qx,
+                  int8_t* __restrict__ qe) {
+  const int64_t u = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (u >= rows * HI * 2) return;
+  const int64_t rh = u >> 1;        // row * HI + h
+  const int blk = (int)(u & 1);
+  const uint4* src = reinterpret_cast<const uint4*>(qI + rh * 64 + 32 * blk);
+  float v[32];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 x = __ldg(src + i);
+    const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[8 * i + 2 * e] = __uint_as_float(wd[e] << 16);
+      v[8 * i + 2 * e + 1] = __uint_as_float(wd[e] & 0xffff0000u);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int sx = mx_block_exp(amax);
+  const float inv = pow2i(-sx);
+  uint32_t wq[8];
+#pragma unroll
+  for (int wd = 0; wd < 8; ++wd) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) word |= e2m1x2_e4m3(e2m1_encode(__fmul_rn(v[4 * wd + e], inv))) << (8 * e);
+    wq[wd] = word;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(qx + rh * 64 + 32 * blk);
+  dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+  dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+  qe[u] = (int8_t)sx;
+}
+
+// Entry expansion: 64 E2M1 codes (byte c/2, low nibble first) -> 64 E4M3
+// bytes of the doubled values, then 64 zero bytes (128-byte rows for the
+// swizzled TMA layout).  One thread per (entry, 16-byte output unit).
+__global__ void __launch_bounds__(256)
+ix_expand_k_kernel(const uint8_t* __restrict__ kc, int64_t n, uint8_t* __restrict__ kx) {
+  const int64_t u = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (u >= n * 8) return;
+  const int64_t key = u >> 3;
+  const int part = (int)(u & 7);
+  uint4 out = make_uint4(0, 0, 0, 0);
+  if (part < 4) {   // codes 16 part .. 16 part + 15 from bytes 8 part .. 8 part + 7
+    const uint2 c = __ldg(reinterpret_cast<const uint2*>(kc + key * 32) + part);
+    const uint32_t cw[2] = {c.x, c.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t src = cw[i >> 1] >> (16 * (i & 1));   // codes 4i .. 4i + 3 of this unit
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) word |= e2m1x2_e4m3((src >> (4 * e)) & 15u) << (8 * e);
+      o[i] = word;
+    }
+    out = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  reinterpret_cast<uint4*>(kx + key * 128)[part] = out;
+}
+
+struct IxParams {
+  const int8_t* qe;         // [B * Tq, HI, 2]
+  const float* w;           // [B * Tq, HI]
+  const uint8_t* ks;        // [B * N, 2] E8M0 entry block scales
+  const int64_t* q_pos;
+  int64_t Tq, N;
+  int HI, m;
+  float* scores;            // [B * Tq, N]
+  void* ws;                 // status flags
+};
+
+__global__ void __launch_bounds__(kIxThreads, 1)
+ix_scores_tc_kernel(const IxParams p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  IxMisc* ms = reinterpret_cast<IxMisc*>(sm + kIxMiscOff);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z;
+  const int64_t t0 = (int64_t)blockIdx.y * kIxRows;
+  const int64_t c0 = (int64_t)blockIdx.x * kIxChunk;
+
+  if (tid == 0) ms->nv_max = 0;
+  __syncthreads();
+  if (tid < kIxRows && t0 + tid < p.Tq) {
+    const int nv = (int)visible(p.q_pos[b * p.Tq + t0 + tid], p.m, p.N);
+    atomicMax(&ms->nv_max, nv);
+  }
+  __syncthreads();
+  const int64_t nv_max = ms->nv_max;
+  if (c0 >= nv_max) return;   // no row of the tile sees this chunk (uniform exit)
+  const int nt = (int)(((nv_max - c0 < kIxChunk ? nv_max - c0 : kIxChunk) + kIxKeys - 1) / kIxKeys);
+
+  if (tid == 0) {
+    mbar_init(&ms->q_full, 1);
+    for (int i = 0; i < kIxStages; ++i) {
+      mbar_init(&ms->k_full[i], 1);
+      mbar_init(&ms->k_empty[i], 1);
+    }
+    for (int i = 0; i < kIxBufs; ++i) {
+      mbar_init(&ms->t_full[i], 1);
+      mbar_init(&ms->t_empty[i], 8);
+    }
+    mbar_init(&ms->drain, 1);
+    mbar_fence_init();
+  }
+  if (warp == kIxMma) tmem_alloc(&ms->tmem, 512);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = ms->tmem;
+  const uint32_t aQ = smem_u32(sm), aK = smem_u32(sm + kIxKOff);
+  const int nchunks = p.HI / 2;
+
+  if (warp == kIxProducer) {
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(&ms->q_full, (uint32_t)nchunks * kIxQChunk);
+      for (int c = 0; c < nchunks; ++c)
+        tma_load_2d(aQ + c * kIxQChunk, &tm_q, 128 * c, (int)(b * p.Tq + t0), &ms->q_full);
+      for (int kt = 0; kt < nt && ok; ++kt) {
+        const int s = kt % kIxStages;
+        if (kt >= kIxStages && !mbar_wait(&ms->k_empty[s], ((kt / kIxStages) - 1) & 1, kIxWait)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&ms->k_full[s], kIxKTile);
+        tma_load_2d(aK + s * kIxKTile, &tm_k, 0, (int)(b * p.N + c0 + (int64_t)kIxKeys * kt), &ms->k_full[s]);
+      }
+      if (!ok) flag_timeout(p.ws);
+      // copies still in flight land before the CTA exits
+      mbar_wait(&ms->q_full, 0, kIxWait);
+      if (nt > 0) mbar_wait(&ms->k_full[(nt - 1) % kIxStages], ((nt - 1) / kIxStages) & 1, kIxWait);
+    }
+    __syncwarp();
+  } else if (warp == kIxMma) {
+    constexpr uint32_t id = idesc_e4m3(kIxRows, kIxKeys);
+    bool ok = mbar_wait(&ms->q_full, 0, kIxWait);
+    fence_after_sync();
+    uint32_t u = 0;   // head steps issued
+    for (int kt = 0; kt < nt && ok; ++kt) {
+      const int s = kt % kIxStages;
+      if (!mbar_wait(&ms->k_full[s], (kt / kIxStages) & 1, kIxWait)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      const uint64_t kd = sdesc_sw128(aK + s * kIxKTile, 16, 1024);
+      for (int h = 0; h < p.HI; ++h, ++u) {
+        const uint32_t hb = u % kIxBufs;
+        if (u >= kIxBufs && !mbar_wait(&ms->t_empty[hb], ((u / kIxBufs) - 1) & 1, kIxWait)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const uint64_t qd = sdesc_sw128(aQ + (h >> 1) * kIxQChunk, 16, 1024);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk)
+          mma_e4m3_elect(tmem + 128u * hb + 64u * blk, qd + (uint64_t)((64 * (h & 1) + 32 * blk) >> 4),
+                         kd + (uint64_t)((32 * blk) >> 4), id);
+        mma_commit_elect(&ms->t_full[hb]);
+        __syncwarp();
+      }
+      if (!ok) break;
+      mma_commit_elect(&ms->k_empty[s]);
+      __syncwarp();
+    }
+    if (!ok && lane == 0) flag_timeout(p.ws);
+    mma_commit_elect(&ms->drain);
+    __syncwarp();
+    mbar_wait(&ms->drain, 0, kIxWait);
+  } else {
+    // ============ epilogue: warp w = rows 32 (w % 4) + lane, entries 32 (w / 4) + j of a tile ============
+    const int qd = warp & 3, kh = warp >> 2;
+    const int64_t t = t0 + 32 * qd + lane;
+    const bool row_ok = t < p.Tq;
+    const int64_t row = b * p.Tq + (row_ok ? t : 0);
+    const float* wrow = p.w + row * p.HI;            // head weights of the row
+    const int8_t* qerow = p.qe + row * p.HI * 2;      // its block exponents (read per head, L1-resident)
+    const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+    bool ok = true;
+    uint32_t u = 0;
+    for (int kt = 0; kt < nt && ok; ++kt) {
+      const int64_t j0 = c0 + (int64_t)kIxKeys * kt + 32 * kh;
+      // the 32 entries' raw E8M0 block exponents (e_k + 127): ek0w / ek1w hold
+      // those of blocks 0 / 1, entry j at byte j % 4 of word j / 4
+      uint32_t ek0w[8], ek1w[8];
+      {
+        const uint8_t* src = p.ks + (b * p.N + j0) * 2;
+        uint32_t raw[16];
+        if (j0 + 32 <= p.N && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>(src) + i);
+            raw[4 * i] = x.x;
+            raw[4 * i + 1] = x.y;
+            raw[4 * i + 2] = x.z;
+            raw[4 * i + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int64_t jj = 2 * i + e / 2;   // entry of byte 4 i + e
+              word |= (j0 + jj < p.N ? (uint32_t)__ldg(src + 4 * i + e) : 127u) << (8 * e);
+            }
+            raw[i] = word;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          ek0w[i] = __byte_perm(raw[2 * i], raw[2 * i + 1], 0x6420);
+          ek1w[i] = __byte_perm(raw[2 * i], raw[2 * i + 1], 0x7531);
+        }
+      }
+      uint32_t lo0 = 255, hi0 = 0, lo1 = 255, hi1 = 0;   // exponent ranges of the tile's entries
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t x0 = (ek0w[j >> 2] >> (8 * (j & 3))) & 0xffu, x1 = (ek1w[j >> 2] >> (8 * (j & 3))) & 0xffu;
+        lo0 = min(lo0, x0);
+        hi0 = max(hi0, x0);
+        lo1 = min(lo1, x1);
+        hi1 = max(hi1, x1);
+      }
+      float sc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sc[j] = 0.0f;
+      for (int h = 0; h < p.HI; ++h, ++u) {
+        const uint32_t hb = u % kIxBufs;
+        if (!mbar_wait(&ms->t_full[hb], (u / kIxBufs) & 1, kIxWait)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const int eq0 = __ldg(qerow + 2 * h), eq1 = __ldg(qerow + 2 * h + 1);
+        const float wh = __ldg(wrow + h);
+        // block b of entry j is scaled by 2^(e_qb + x_bj - 129), x = raw exponent
+        // byte; when every such power lies in [2^-100, 2^100] one multiply by
+        // it is exact, as is the two-step scale_pow2 otherwise
+        const bool fast = eq0 + (int)lo0 >= 29 && eq0 + (int)hi0 <= 229 && eq1 + (int)lo1 >= 29 && eq1 + (int)hi1 <= 229;
+        const int c0 = (eq0 - 2) << 23, c1 = (eq1 - 2) << 23;   // + (x << 23): fp32 bits of the power
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {   // 16 entries at a time (registers)
+          uint32_t P0[16], P1[16];
+          tmem_ld32x16(tmem + lane_base + 128u * hb + 32u * kh + 16u * half, P0);
+          tmem_ld32x16(tmem + lane_base + 128u * hb + 64u + 32u * kh + 16u * half, P1);
+          tmem_wait_ld();
+          if (half == 1) {   // the buffer is read: release it to the MMA warp
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms->t_empty[hb]);
+          }
+          if (fast) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = 16 * half + i;
+              const int x0 = (int)((ek0w[j >> 2] >> (8 * (j & 3))) & 0xffu);
+              const int x1 = (int)((ek1w[j >> 2] >> (8 * (j & 3))) & 0xffu);
+              const float d = __fadd_rn(__fmul_rn(__uint_as_float(P0[i]), __int_as_float(x0 * (1 << 23) + c0)),
+                                        __fmul_rn(__uint_as_float(P1[i]), __int_as_float(x1 * (1 << 23) + c1)));
+              sc[j] = __fmaf_rn(wh, d > 0.0f ? d : 0.0f, sc[j]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = 16 * half + i;
+              const int x0 = (int)((ek0w[j >> 2] >> (8 * (j & 3))) & 0xffu);
+              const int x1 = (int)((ek1w[j >> 2] >> (8 * (j & 3))) & 0xffu);
+              const float d = __fadd_rn(scale_pow2(__uint_as_float(P0[i]), eq0 + x0 - 129),
+                                        scale_pow2(__uint_as_float(P1[i]), eq1 + x1 - 129));
+              sc[j] = __fmaf_rn(wh, d > 0.0f ? d : 0.0f, sc[j]);
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      if (row_ok) {
+        float* dst = p.scores + row * p.N + j0;
+        if (j0 + 32 <= p.N && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(dst + j) = make_float4(sc[j], sc[j + 1], sc[j + 2], sc[j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j0 + j < p.N) dst[j] = sc[j];
+        }
+      }
+    }
+    if (!ok && lane == 0) flag_timeout(p.ws);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == kIxMma) {
+    fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn ix_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// byte rows of `width` bytes, boxes of 128 bytes x box_rows, 128-byte swizzle
+bool ix_byte_map(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = ix_encode_fn();
+  if (!fn || rows == 0) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)width};
+  const cuuint32_t box[2] = {128u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+bool indexer_tc_applies(int B, int64_t Tq, int HI, int dI, int64_t N) {
+  return Tq >= 64 && dI == 64 && HI >= 2 && HI <= kIxMaxHeads && HI % 2 == 0 && N > 0 &&
+         (int64_t)B * Tq < INT32_MAX && (int64_t)B * N < INT32_MAX;
+}
+
+size_t indexer_tc_workspace(int B, int64_t Tq, int HI, int64_t N) {
+  const size_t rows = (size_t)B * (size_t)Tq;
+  return al256(rows * (size_t)HI * 64) + al256(rows * (size_t)HI * 2) + al256((size_t)B * (size_t)N * 128);
+}
+
+cudaError_t launch_indexer_scores_tc(const void* qI, const float* w, const uint8_t* kc, const uint8_t* ks,
+                                     const int64_t* q_pos, int B, int64_t Tq, int HI, int64_t N, int m,
+                                     float* scores, void* tc_ws, void* flags_ws, cudaStream_t st) {
+  const int64_t rows = (int64_t)B * Tq;
+  uint8_t* base = reinterpret_cast<uint8_t*>(tc_ws);
+  uint8_t* qx = base;
+  int8_t* qe = reinterpret_cast<int8_t*>(base + al256((size_t)rows * HI * 64));
+  uint8_t* kx = base + al256((size_t)rows * HI * 64) + al256((size_t)rows * HI * 2);
+  const int64_t nq = rows * HI * 2, nk = (int64_t)B * N * 8;
+  ix_quant_q_kernel<<<(unsigned)((nq + 255) / 256), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(qI), rows,
+                                                                 HI, qx, qe);
+  ix_expand_k_kernel<<<(unsigned)((nk + 255) / 256), 256, 0, st>>>(kc, (int64_t)B * N, kx);
+  CUtensorMap tm_q, tm_k;
+  if (!ix_byte_map(&tm_q, qx, (uint64_t)HI * 64, (uint64_t)rows, kIxRows)) return cudaErrorInvalidValue;
+  if (!ix_byte_map(&tm_k, kx, 128, (uint64_t)B * N, kIxKeys)) return cudaErrorInvalidValue;
+  IxParams p;
+  p.qe = qe;
+  p.w = w;
+  p.ks = ks;
+  p.q_pos = q_pos;
+  p.Tq = Tq;
+  p.N = N;
+  p.HI = HI;
+  p.m = m;
+  p.scores = scores;
+  p.ws = flags_ws;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(ix_scores_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIxSmem);
+    attr = true;
+  }
+  const dim3 grid((unsigned)((N + kIxChunk - 1) / kIxChunk), (unsigned)((Tq + kIxRows - 1) / kIxRows), (unsigned)B);
+  ix_scores_tc_kernel<<<grid, kIxThreads, kIxSmem, st>>>(p, tm_q, tm_k);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -43,7 +43,15 @@ cudaError_t launch_pack_mixed(const float* v, int64_t n, uint8_t* out, cudaStrea
 cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
                                 const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
                                 int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
-                                float* score_out, float* scores_ws, cudaStream_t st);
+                                float* score_out, float* scores_ws, void* tc_ws, void* flags_ws,
+                                cudaStream_t st);
+// FP8 tensor-core scoring (indexer_tc.cu): whether it applies, its extra
+// scratch, and the launch (scores only; top-k follows in indexer.cu)
+bool indexer_tc_applies(int B, int64_t Tq, int HI, int dI, int64_t N);
+size_t indexer_tc_workspace(int B, int64_t Tq, int HI, int64_t N);
+cudaError_t launch_indexer_scores_tc(const void* qI, const float* w, const uint8_t* kc, const uint8_t* ks,
+                                     const int64_t* q_pos, int B, int64_t Tq, int HI, int64_t N, int m,
+                                     float* scores, void* tc_ws, void* flags_ws, cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st);
 size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys, int64_t N, int64_t Ts, int k);

@@ -93,6 +93,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "r"(taddr));
 }
 
+// 32 lanes x 32 bit, 16 consecutive columns -> v[0..15]
+__device__ __forceinline__ void tmem_ld32x16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+
 // 16 lanes x 256 bit, 8 repetitions along the columns -> v[0..31]: lane t of
 // the warp gets rows t/4 and 8 + t/4 of the 16, columns 8j + 2 (t % 4) and
 // the next one, in the order (row t/4: 2 columns, row 8 + t/4: 2 columns) per j.

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import workloads as wl
-from gpu_common import act_dev, dev, max_rel_err, softmax_scale, tol, widen
+from gpu_common import act_dev, dev, dev_bf16, max_rel_err, softmax_scale, tol, widen
 
 pytestmark = pytest.mark.gpu
 
@@ -461,3 +461,40 @@ def test_tc_dequant_is_exact(csa, oracle_mod):
     want = oracle_mod.unpack_mixed(rows)[0, :, :448]
     for r in range(n):
         np.testing.assert_array_equal(out[0, r, :, :448], np.broadcast_to(want[r], (64, 448)))
+
+
+# --------------------------------------------------------------------------
+# indexer: FP8 tensor-core scoring against the exact integer (dp4a) kernel
+# --------------------------------------------------------------------------
+def _mxfp4_keys_random(rng, n, exps):
+    """Random E2M1 codes (all 16) and E8M0 scale bytes drawn from `exps`."""
+    codes = rng.integers(0, 256, size=(n, 32), dtype=np.uint8)
+    scales = rng.choice(np.asarray(exps, np.uint8), size=(n, 2)).astype(np.uint8)
+    return codes, scales
+
+
+@pytest.mark.parametrize("B,Tq,N,m,key_exps,q_scale", [
+    (2, 300, 700, 1, list(range(120, 135)), 1.0),      # ragged rows and entries, two sequences
+    (1, 256, 256, 1, [0, 1, 2, 250, 254], 1e-30),      # block powers far outside [2^-100, 2^100]
+    (1, 129, 64, 2, list(range(100, 160)), 3e4),       # one row past a 128-row tile; m = 2
+])
+def test_indexer_tc_scores_match_dp4a(csa, monkeypatch, B, Tq, N, m, key_exps, q_scale):
+    """The FP8 tensor-core scores (exact block dots) equal the dp4a kernel's bit
+    for bit: all visible scores, read back through a top-k of k = N."""
+    rng = np.random.default_rng(7 + Tq + N)
+    HI, dI = 16, 64
+    codes, scales = _mxfp4_keys_random(rng, B * N, key_exps)
+    kd = dev(codes.reshape(B, N, 32))
+    ksd = dev(scales.reshape(B, N, 2))
+    qI = (rng.standard_normal((B, Tq, HI, dI)) * q_scale).astype(np.float32)
+    qI[:, :, 0, :32] = 0.0                                 # an all-zero block (exponent 0)
+    qbits = wl.f32_to_bf16_bits(qI)
+    w = rng.standard_normal((B, Tq, HI)).astype(np.float32)
+    q_pos = np.tile(np.arange(Tq, dtype=np.int64), (B, 1)) + rng.integers(0, 3, size=(B, 1))
+    args = (dev_bf16(qbits), dev(w), kd, ksd, dev(q_pos), N, m, N)
+    idx_tc, sc_tc = csa.indexer_topk(*args)
+    monkeypatch.setenv("CSA_INDEXER_IMPL", "dp4a")
+    idx_dp, sc_dp = csa.indexer_topk(*args)
+    monkeypatch.delenv("CSA_INDEXER_IMPL")
+    np.testing.assert_array_equal(idx_tc.cpu().numpy(), idx_dp.cpu().numpy())
+    np.testing.assert_array_equal(sc_tc.cpu().numpy().view(np.uint32), sc_dp.cpu().numpy().view(np.uint32))
