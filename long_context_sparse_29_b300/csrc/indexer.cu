@@ -294,21 +294,66 @@ topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos,
       taken_eq += blk;
       __syncthreads();
     }
-    // bitonic sort, descending
-    for (int size = 2; size <= kpad; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = tid; i < kpad; i += kTopkThreads) {
-          const int p = i ^ stride;
-          if (p > i) {
-            const bool desc = (i & size) == 0;
-            const unsigned long long a = keys_s[i], c = keys_s[p];
-            if ((a < c) == desc) {
-              keys_s[i] = c;
-              keys_s[p] = a;
-            }
-          }
+    // sort, descending
+    if (kpad <= kTopkThreads && kpad >= 32) {
+      // every warp sorts its 32 keys with shuffles; the sorted runs are then
+      // merged pairwise (32 -> 64 -> ... -> kpad), each key moving to its own
+      // position plus the count of larger keys in the partner run (binary
+      // search).  Empty slots get distinct keys below every real one.
+      unsigned long long* buf0 = keys_s;
+      unsigned long long* buf1 = keys_s + kpad;
+      unsigned long long v = 0;
+      if (tid < kpad) {
+        v = keys_s[tid];
+        if (v == 0ull) v = (unsigned long long)(kpad - tid);
+      }
+#pragma unroll
+      for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, stride);
+          const bool desc = size == 32 || (lane & size) == 0, lower = (lane & stride) == 0;
+          v = (desc == lower) ? (v > o ? v : o) : (v < o ? v : o);
+        }
+      }
+      __syncthreads();
+      if (tid < kpad) buf0[tid] = v;
+      __syncthreads();
+      for (int L = 32; L < kpad; L <<= 1) {
+        if (tid < kpad) {
+          const unsigned long long x = buf0[tid];
+          const int r = tid / L, pos = tid - r * L;
+          const unsigned long long* part = buf0 + (r ^ 1) * L;
+          int c = 0;   // keys of the partner run larger than x (a prefix: runs are descending)
+          for (int st = L; st > 0; st >>= 1)
+            if (c + st <= L && part[c + st - 1] > x) c += st;
+          buf1[(r & ~1) * L + pos + c] = x;
         }
         __syncthreads();
+        unsigned long long* t = buf0;
+        buf0 = buf1;
+        buf1 = t;
+      }
+      if (buf0 != keys_s) {
+        if (tid < kpad) keys_s[tid] = buf0[tid];
+        __syncthreads();
+      }
+    } else {
+      for (int size = 2; size <= kpad; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int i = tid; i < kpad; i += kTopkThreads) {
+            const int p = i ^ stride;
+            if (p > i) {
+              const bool desc = (i & size) == 0;
+              const unsigned long long a = keys_s[i], c = keys_s[p];
+              if ((a < c) == desc) {
+                keys_s[i] = c;
+                keys_s[p] = a;
+              }
+            }
+          }
+          __syncthreads();
+        }
       }
     }
   }
@@ -358,7 +403,7 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
     if (e != cudaSuccess) return e;
   }
   const int kpad = topk_pad(k);
-  const size_t smem = sizeof(unsigned long long) * (size_t)kpad;
+  const size_t smem = sizeof(unsigned long long) * (size_t)kpad * (kpad <= kTopkThreads ? 2 : 1);
   static bool attr_set = false;
   if (!attr_set) {
     cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
