@@ -229,7 +229,7 @@ def run_ours(args, rank, world, local_rank):
                    "D": CFG.D, "HI": CFG.HI, "dI": CFG.dI, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (q and out 512 MiB each per step)"},
         "roofline": {"kernel": "sparse_mqa", "bound": "tensor", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ATTN_TRAFFIC,
                      "peak_src": f"bf16 dense, {pk['src']} (burst)",
                      "algorithmic_flops_per_launch": af, "avg_launch_ms": attn_ms},
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -245,10 +245,16 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
-# kernels launched per step: 3 compress, indexer scores + top-k, and for the
-# attention the per-row prep (rotated query dims, entry lists), the bf16
-# expansion of the cache and of the window rows, and the attention kernel
-LAUNCHES_PER_STEP = 9
+# kernels launched per step: 3 compress; the indexer's query quantisation,
+# entry expansion, tensor-core scores and top-k; for the attention the per-row
+# prep (rotated query dims, entry lists), the bf16 expansion of the cache and
+# of the window rows, and the attention kernel
+LAUNCHES_PER_STEP = 11
+
+# DRAM bytes (read + write) of one attn_tc_kernel launch on this workload, from
+# one ncu capture of it (dram__bytes_read.sum + dram__bytes_write.sum); to be
+# set to None when the kernel changes, until it is captured again
+ATTN_TRAFFIC = 631651584 + 495853312
 
 
 # --------------------------------------------------------------------------
@@ -328,6 +334,163 @@ def run_reference(args, rank, world):
     }
 
 
+# --------------------------------------------------------------------------
+# the other configurations (--config): decode steps against resident caches,
+# and the 64K HCA prefill
+# --------------------------------------------------------------------------
+def _bf16_dev(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _f_dev(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def decode_layer(csa, cfg, dev, rope):
+    """Resident caches of one decode layer (every sequence's full context run
+    through the library's compression), and the step's inputs on the host."""
+    import torch
+    B, T, W, N, m = cfg.B, cfg.T, cfg.W, cfg.N, cfg.m
+    sc = wl.gen_channel_scales(cfg)
+    s_d = _f_dev(sc["s"], dev)
+    cache = torch.empty((B, N, 592), dtype=torch.uint8, device=dev)
+    swa = torch.empty((B, W, 592), dtype=torch.uint8, device=dev)
+    kc = torch.empty((B, N, 32), dtype=torch.uint8, device=dev) if cfg.k else None
+    ks = torch.empty((B, N, 2), dtype=torch.uint8, device=dev) if cfg.k else None
+    for b in range(B):
+        toks = wl.gen_tokens(cfg, b, parts=("kv", "z", "kI", "zI") if cfg.k else ("kv", "z"))
+        kv, z = _bf16_dev(toks["kv"], dev)[None], _f_dev(toks["z"], dev)[None]
+        csa.compress_kv(kv, z, s_d, m, csa.FMT_MIXED592, cfg.R, rope, out=cache[b:b + 1])
+        csa.compress_kv(kv[:, T - W:], z[:, T - W:], None, 1, csa.FMT_MIXED592, cfg.R, rope, pos0=T - W,
+                        out=swa[b:b + 1])
+        if cfg.k:
+            csa.compress_kv(_bf16_dev(toks["kI"], dev)[None], _f_dev(toks["zI"], dev)[None],
+                            _f_dev(sc["sI"], dev), m, csa.FMT_MXFP4, 0, out=kc[b:b + 1], out_scales=ks[b:b + 1])
+        del kv, z, toks
+    qry = [wl.gen_queries(cfg, b) for b in range(B)]
+    host = {"q": np.stack([x["q"] for x in qry]), "q_pos": np.full((B, 1), T - 1, np.int64),
+            "swa_pos0": np.full(B, T - W, np.int64)}
+    if cfg.k:
+        host["qI"] = np.stack([x["qI"] for x in qry])
+        host["w"] = np.stack([x["w"] for x in qry])
+    return {"cache": cache, "swa": swa, "kc": kc, "ks": ks}, host
+
+
+def decode_bytes(cfg) -> float:
+    """Algorithmic HBM bytes of one decode step: every resident byte the step
+    must read once (indexer keys 34 B per entry; the k + W gathered or all
+    visible rows, 592 B each) plus the query and the output (64 KiB each)."""
+    rows = (cfg.k if cfg.k else cfg.N) + cfg.W
+    per_q = rows * 592 + 2 * cfg.H * cfg.D * 2 + (cfg.N * 34 if cfg.k else 0)
+    return float(cfg.B * per_q)
+
+
+def run_config(args, name):
+    import torch
+    import long_context_sparse_29_b300 as csa
+    from long_context_sparse_29_b300 import build as csa_build
+
+    csa_build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    stream = torch.cuda.current_stream(dev)
+    if name in ("c3_csa_decode_128k", "c4_hca_decode_1m", "c5_hybrid_csa_decode_1m"):
+        layers = [wl.CONFIGS[name]]
+        if name == "c5_hybrid_csa_decode_1m":
+            layers.append(wl.CONFIGS["c5_hybrid_hca_decode_1m"])
+        rope = csa.rope_table(layers[0].T + 1, 64)
+        built = []
+        for cfg in layers:
+            res, host = decode_layer(csa, cfg, dev, rope)
+            d = {kk: (_bf16_dev(v, dev) if kk in ("q", "qI") else _f_dev(v, dev)) for kk, v in host.items()}
+            out = torch.empty((cfg.B, 1, cfg.H, cfg.D), dtype=torch.bfloat16, device=dev)
+            idx = torch.empty((cfg.B, 1, cfg.k), dtype=torch.int32, device=dev) if cfg.k else None
+            built.append((cfg, res, d, out, idx, csa.Workspace(dev), csa.Workspace(dev)))
+        torch.cuda.synchronize()
+
+        def step():
+            for cfg, res, d, out, idx, ws1, ws2 in built:
+                scale = 1.0 / math.sqrt(cfg.D)
+                if cfg.k:
+                    csa.indexer_topk(d["qI"], d["w"], res["kc"], res["ks"], d["q_pos"], cfg.N, cfg.m, cfg.k,
+                                     scores=False, idx_out=idx, ws=ws1)
+                    csa.sparse_mqa(d["q"], d["q_pos"], res["cache"], cfg.m, idx, res["swa"], d["swa_pos0"], cfg.W,
+                                   scale, rope, cfg.R, out=out, ws=ws2)
+                else:
+                    csa.hca_dense_attn(d["q"], d["q_pos"], res["cache"], cfg.m, res["swa"], d["swa_pos0"], cfg.W,
+                                       scale, rope, cfg.R, out=out, ws=ws2)
+
+        units, unit = float(layers[0].B), "queries/s"
+        metric = {"c3_csa_decode_128k": "CSA decode queries/s (32 sequences at 128K context, top-k 1024)",
+                  "c4_hca_decode_1m": "HCA decode queries/s (16 sequences at 1M context, m'=128)",
+                  "c5_hybrid_csa_decode_1m": "hybrid CSA+HCA decode layer-pair steps/s (4 sequences at 1M)"}[name]
+        alg = sum(decode_bytes(c) for c in layers)
+        roof = {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s", "algorithmic_bytes_per_step": alg}
+        l2 = "caches resident; each step reads them once (larger than L2 except the HCA-only step)"
+    elif name == "c4_hca_prefill_64k":
+        cfg = wl.CONFIGS[name]
+        T, W, N, m = cfg.T, cfg.W, cfg.N, cfg.m
+        rope = csa.rope_table(T + 1, 64)
+        sc = wl.gen_channel_scales(cfg)
+        toks = wl.gen_tokens(cfg, 0, parts=("kv", "z"))
+        qry = wl.gen_queries(cfg, 0)
+        kv, z = _bf16_dev(toks["kv"], dev)[None], _f_dev(toks["z"], dev)[None]
+        q = _bf16_dev(qry["q"], dev)[None]
+        q_pos = _f_dev(np.arange(T, dtype=np.int64)[None], dev)
+        pos0 = _f_dev(np.zeros(1, np.int64), dev)
+        s_d = _f_dev(sc["s"], dev)
+        cache = torch.empty((1, N, 592), dtype=torch.uint8, device=dev)
+        swa = torch.empty((1, T, 592), dtype=torch.uint8, device=dev)
+        out = torch.empty((1, T, cfg.H, cfg.D), dtype=torch.bfloat16, device=dev)
+        ws = csa.Workspace(dev)
+        scale = 1.0 / math.sqrt(cfg.D)
+
+        def step():
+            csa.compress_kv(kv, z, s_d, m, csa.FMT_MIXED592, cfg.R, rope, out=cache)
+            csa.compress_kv(kv, z, None, 1, csa.FMT_MIXED592, cfg.R, rope, out=swa)
+            csa.hca_dense_attn(q, q_pos, cache, m, swa, pos0, W, scale, rope, cfg.R, out=out, ws=ws)
+
+        units, unit = float(T), "tokens/s"
+        metric = "HCA prefill tokens/s (1x65536, m'=128, window 128, 64 heads, D=512)"
+        t = np.arange(T, dtype=np.int64)
+        keys = np.minimum(N, (t + 1) // m) + np.minimum(W, t + 1)
+        alg = float(keys.sum()) * cfg.H * 4 * cfg.D
+        roof = {"bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "algorithmic_flops_per_step": alg}
+        l2 = "inputs larger than L2 (q and out 4 GiB each)"
+        layers = [cfg]
+    else:
+        raise SystemExit(f"unknown config {name}")
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    if roof["bound"] == "hbm":
+        ach = roof["algorithmic_bytes_per_step"] / (ms * 1e-3) / 1e9
+    else:
+        ach = roof["algorithmic_flops_per_step"] / (ms * 1e-3) / 1e12
+    roof.update({"achieved": ach, "frac": ach / roof["peak"], "traffic": None,
+                 "peak_src": f"{pk['src']} ({'HBM copy' if roof['bound'] == 'hbm' else 'bf16 dense, burst'})",
+                 "note": "the whole step (all its launches) timed with CUDA events"})
+    cfg0 = layers[0]
+    return {"metric": metric, "value": units / (ms * 1e-3), "unit": unit, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": name, "B": cfg0.B, "T": cfg0.T, "N": cfg0.N, "m": cfg0.m, "k": cfg0.k,
+                       "W": cfg0.W, "H": cfg0.H, "D": cfg0.D, "l2": l2},
+            "roofline": roof, "clocks": clk.summary()}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -336,7 +499,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--config", default=CFG.name,
+                    help="workload; the default is the 8K CSA prefill, the others are measured on one GPU")
     args = ap.parse_args()
+    if args.config != CFG.name:
+        if args.impl != "ours":
+            raise SystemExit("--config applies to --impl ours only")
+        print(json.dumps(run_config(args, args.config)), flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
