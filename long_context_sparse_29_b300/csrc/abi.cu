@@ -41,9 +41,13 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 size_t indexer_ws(int B, int64_t Tq, int64_t N) {
   return csa::kWsHeader + align256(sizeof(float) * (size_t)B * (size_t)Tq * (size_t)N);
 }
-// + the quantised queries and expanded entries of the tensor-core scoring, when it applies
-size_t indexer_ws_full(int B, int64_t Tq, int64_t N, int HI, int dI) {
-  const size_t base = indexer_ws(B, Tq, N);
+// + the chunk winners of the two-stage top-k (few long rows) and the quantised
+// queries and expanded entries of the tensor-core scoring, where they apply
+size_t indexer_cand_ws(int B, int64_t Tq, int64_t N, int k) {
+  return csa::topk_two_stage(B, Tq, N) ? align256(csa::topk_cand_bytes(B, Tq, N, k)) : 0;
+}
+size_t indexer_ws_full(int B, int64_t Tq, int64_t N, int HI, int dI, int k) {
+  const size_t base = indexer_ws(B, Tq, N) + indexer_cand_ws(B, Tq, N, k);
   return csa::indexer_tc_applies(B, Tq, HI, dI, N) ? base + align256(csa::indexer_tc_workspace(B, Tq, HI, N)) : base;
 }
 
@@ -155,7 +159,7 @@ int64_t csa_workspace_size(int op, int B, int64_t Tq, int64_t N, int k, int H, i
   if (B < 0 || Tq < 0 || N < 0) return -1;
   switch (op) {
     case CSA_OP_INDEXER_TOPK:   // H, D: indexer heads and head dim (0: the minimum)
-      return (int64_t)indexer_ws_full(B, Tq, N, H, D);
+      return (int64_t)indexer_ws_full(B, Tq, N, H, D, k);
     case CSA_OP_SPARSE_MQA:
     case CSA_OP_HCA_DENSE:
       return (int64_t)(csa::kWsHeader +
@@ -248,12 +252,18 @@ int csa_indexer_topk(const void* qI, int qI_dtype, const float* w, const void* k
                 indexer_ws(B, Tq, N));
   if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(CSA_ERR_INVALID_ARG, "%s: ws not 256-byte aligned", nm);
   float* scores = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + csa::kWsHeader);
-  void* tc_ws = nullptr;   // tensor-core scoring when its scratch was given
-  if (fp4 && !indexer_use_dp4a() && ws_bytes >= indexer_ws_full(B, Tq, N, HI, dI) &&
-      indexer_ws_full(B, Tq, N, HI, dI) > indexer_ws(B, Tq, N))
-    tc_ws = reinterpret_cast<char*>(ws) + indexer_ws(B, Tq, N);
+  // the optional parts when the whole plan fits: [scores | chunk winners | tensor-core scratch]
+  void* cand_ws = nullptr;
+  void* tc_ws = nullptr;
+  const size_t full = indexer_ws_full(B, Tq, N, HI, dI, k);
+  if (ws_bytes >= full) {
+    char* p = reinterpret_cast<char*>(ws) + indexer_ws(B, Tq, N);
+    if (indexer_cand_ws(B, Tq, N, k)) cand_ws = p;
+    p += indexer_cand_ws(B, Tq, N, k);
+    if (fp4 && !indexer_use_dp4a() && csa::indexer_tc_applies(B, Tq, HI, dI, N)) tc_ws = p;
+  }
   return cuda_result(csa::launch_indexer_topk(qI, fp4, w, kI, kI_scales, q_pos, B, Tq, HI, dI, N,
-                                              m, k, idx_out, score_out, scores, tc_ws, ws,
+                                              m, k, idx_out, score_out, scores, tc_ws, cand_ws, ws,
                                               as_stream(stream)),
                      nm);
 }

@@ -939,45 +939,46 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
   }
 }
 
-// Merge the split partial softmax states of one query row into out and lse.
+// Merge the split partial softmax states of one (query row, head) into out
+// and lse: one CTA per pair, thread t owns dims 2t and 2t + 1 (a RoPE pair when
+// 2t >= 448); the partial states are weighted by 2^(m_s - max m) in split order.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const Params p) {
   const int64_t row = blockIdx.x;
+  const int h = blockIdx.y;
   const int tid = threadIdx.x;
   const int64_t t = p.q_pos[row];
   const bool t_ok = t >= 0 && t < p.rope_rows;
-  const float* cs = p.rcos + (t_ok ? t : 0) * 32;
-  const float* sn = p.rsin + (t_ok ? t : 0) * 32;
-  const int d0 = 2 * tid;   // dims d0, d0 + 1 (a RoPE pair when d0 >= 448)
-  for (int h = 0; h < kH; ++h) {
-    float M = -INFINITY;
-    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.part_ml[((row * p.nsplit + s) * kH + h) * 2]);
-    float L = 0.0f, o0 = 0.0f, o1 = 0.0f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < p.nsplit; ++s) {
-        const int64_t it = row * p.nsplit + s;
-        const float mi = p.part_ml[(it * kH + h) * 2];
-        if (mi == -INFINITY) continue;
-        const float w = exp2f(mi - M);
-        L += w * p.part_ml[(it * kH + h) * 2 + 1];
-        const float2 v = *reinterpret_cast<const float2*>(p.part_o + it * (int64_t)(kH * kD) + h * kD + d0);
-        o0 += w * v.x;
-        o1 += w * v.y;
-      }
+  const int d0 = 2 * tid;
+  const float* ml = p.part_ml + (row * p.nsplit * kH + h) * 2;   // split s at + s * kH * 2
+  float M = -INFINITY;
+  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, ml[s * kH * 2]);
+  float L = 0.0f, o0 = 0.0f, o1 = 0.0f;
+  if (M != -INFINITY) {
+    const float* po = p.part_o + row * p.nsplit * (int64_t)(kH * kD) + h * kD + d0;
+    for (int s = 0; s < p.nsplit; ++s) {
+      const float mi = ml[s * kH * 2];
+      if (mi == -INFINITY) continue;
+      const float w = exp2f(mi - M);
+      L += w * ml[s * kH * 2 + 1];
+      const float2 v = *reinterpret_cast<const float2*>(po + s * (int64_t)(kH * kD));
+      o0 += w * v.x;
+      o1 += w * v.y;
     }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    o0 *= inv;
-    o1 *= inv;
-    if (d0 >= kMixDn) {
-      const int pi = (d0 - kMixDn) >> 1;
-      const float y0 = o0 * cs[pi] + o1 * sn[pi];
-      const float y1 = -o0 * sn[pi] + o1 * cs[pi];
-      o0 = y0;
-      o1 = y1;
-    }
-    *reinterpret_cast<__nv_bfloat162*>(p.out + row * (int64_t)(kH * kD) + h * kD + d0) =
-        __floats2bfloat162_rn(o0, o1);
-    if (tid == 0 && p.lse) p.lse[row * kH + h] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  o0 *= inv;
+  o1 *= inv;
+  if (d0 >= kMixDn) {
+    const float* cs = p.rcos + (t_ok ? t : 0) * 32;
+    const float* sn = p.rsin + (t_ok ? t : 0) * 32;
+    const int pi = (d0 - kMixDn) >> 1;
+    const float y0 = o0 * cs[pi] + o1 * sn[pi];
+    const float y1 = -o0 * sn[pi] + o1 * cs[pi];
+    o0 = y0;
+    o1 = y1;
+  }
+  *reinterpret_cast<__nv_bfloat162*>(p.out + row * (int64_t)(kH * kD) + h * kD + d0) = __floats2bfloat162_rn(o0, o1);
+  if (tid == 0 && p.lse) p.lse[row * kH + h] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 int num_sms() {
@@ -1158,7 +1159,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  attn_combine_kernel<<<(unsigned)rows, 256, 0, st>>>(p);
+  attn_combine_kernel<<<dim3((unsigned)rows, kH), 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -190,9 +190,20 @@ scores_f32_kernel(const float* __restrict__ qI, const float* __restrict__ w,
 }
 
 // ---------------------------------------------------------------------------
-// top-k: one CTA per query row
+// top-k.  A row's candidates are visited in index order; the k-th largest
+// order key is found by radix select (4 passes of 8 bits over shared-memory
+// histograms); the chosen keys -- every key above that threshold and the first
+// `remaining` keys equal to it, in index order -- are compacted in index order
+// (per-warp segments: count, prefix, write); then sorted by (score desc, index
+// asc) as 64-bit composite keys: warps sort runs of 32 with shuffles, runs are
+// merged pairwise by binary search.  Rows longer than kTkChunk go in two
+// stages: every chunk of kTkChunk candidates keeps its own top-k (the global
+// top-k lies in their union: the order is total), then one CTA per row
+// selects among the chunk winners.
 // ---------------------------------------------------------------------------
 constexpr int kTopkThreads = 512;
+constexpr int kTkWarps = kTopkThreads / 32;
+constexpr int kTkChunk = 8192;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -204,164 +215,192 @@ __device__ __forceinline__ float order_key_value(uint32_t u) {
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
-topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m,
-            int k, int kpad, int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
-  extern __shared__ unsigned long long keys_s[];   // kpad composite keys
-  __shared__ unsigned int hist[256];
-  __shared__ unsigned int warp_cnt[kTopkThreads / 32];
-  __shared__ unsigned int sh_prefix, sh_remaining, sh_slots;
-  const int64_t row = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t nv = visible_entries(q_pos[row], m, N);
-  const int kk = (int)((int64_t)k < nv ? (int64_t)k : nv);
-  const float* sr = scores + row * N;
+__device__ __forceinline__ unsigned long long composite(uint32_t key, uint32_t idx) {
+  return ((unsigned long long)key << 32) | (unsigned long long)(0xffffffffu - idx);
+}
 
-  for (int i = tid; i < kpad; i += kTopkThreads) keys_s[i] = 0ull;
-  if (tid == 0) {
-    sh_prefix = 0;
-    sh_remaining = (unsigned)kk;
-    sh_slots = 0;
+struct TkShared {
+  unsigned int hist[256];
+  unsigned int cnt_gt[kTkWarps], cnt_eq[kTkWarps];
+  unsigned int prefix, remaining;
+};
+
+// Candidate streams: get(i, key, idx) for i in [0, n), false when slot i holds
+// no candidate.  Order keys of real scores are never 0.
+struct DenseRow {   // scores[base + i], index base + i, for i < n
+  const float* s;
+  int64_t base;
+  __device__ __forceinline__ bool get(int64_t i, uint32_t& key, uint32_t& idx) const {
+    key = order_key(s[base + i]);
+    idx = (uint32_t)(base + i);
+    return true;
   }
-  __syncthreads();
+};
+struct CandList {   // composite keys, 0 = empty slot
+  const unsigned long long* c;
+  __device__ __forceinline__ bool get(int64_t i, uint32_t& key, uint32_t& idx) const {
+    const unsigned long long v = c[i];
+    key = (uint32_t)(v >> 32);
+    idx = 0xffffffffu - (uint32_t)(v & 0xffffffffull);
+    return key != 0u;
+  }
+};
 
-  if (kk > 0) {
-    uint32_t mask = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
-      __syncthreads();
-      const uint32_t prefix = sh_prefix;
-      for (int64_t jj = tid; jj < nv; jj += kTopkThreads) {
-        const uint32_t u = order_key(sr[jj]);
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+// The kk-th largest key of the stream (kk >= 1 and at most the number of
+// candidates): returns its value; sh.remaining = how many keys equal to it
+// are taken.
+template <class Src>
+__device__ uint32_t radix_threshold(const Src& src, int64_t n, int kk, TkShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    sh.prefix = 0;
+    sh.remaining = (unsigned)kk;
+  }
+  uint32_t mask = 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    if (tid < 256) sh.hist[tid] = 0;
+    __syncthreads();
+    const uint32_t prefix = sh.prefix;
+    for (int64_t i = tid; i < n; i += kTopkThreads) {
+      uint32_t u, id;
+      if (src.get(i, u, id) && (u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane L holds bins 255-8L .. 248-8L (descending); find the digit where
+      // the count of larger keys first reaches `remaining`
+      const unsigned int rem = sh.remaining;
+      unsigned int c[8], tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = sh.hist[255 - 8 * lane - i];
+        tot += c[i];
       }
-      __syncthreads();
-      if (warp == 0) {
-        // lane L holds bins 255-8L .. 248-8L (descending); find the digit where
-        // the count of larger keys first reaches `remaining`
-        const unsigned int rem = sh_remaining;
-        unsigned int c[8], tot = 0;
+      unsigned int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const unsigned int excl = incl - tot;
+      const bool here = excl < rem && incl >= rem;
+      const unsigned int who = __ballot_sync(0xffffffffu, here);
+      if (lane == __ffs(who) - 1) {
+        unsigned int acc = excl;
+        int d = 255 - 8 * lane;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          c[i] = hist[255 - 8 * lane - i];
-          tot += c[i];
-        }
-        unsigned int incl = tot;   // inclusive prefix over lanes 0..L
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const unsigned int excl = incl - tot;
-        const bool here = excl < rem && incl >= rem;
-        const unsigned int who = __ballot_sync(0xffffffffu, here);
-        if (lane == __ffs(who) - 1) {
-          unsigned int acc = excl;
-          int d = 255 - 8 * lane;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (acc + c[i] >= rem) { d = 255 - 8 * lane - i; break; }
-            acc += c[i];
+          if (acc + c[i] >= rem) {
+            d = 255 - 8 * lane - i;
+            break;
           }
-          sh_remaining = rem - acc;
-          sh_prefix = prefix | ((uint32_t)d << shift);
+          acc += c[i];
         }
-      }
-      mask |= 255u << shift;
-      __syncthreads();
-    }
-    // collect: all keys above the threshold, and the first `remaining` equal ones by index
-    const uint32_t thr = sh_prefix;
-    const unsigned int need_eq = sh_remaining;
-    unsigned int taken_eq = 0;
-    for (int64_t base = 0; base < nv; base += kTopkThreads) {
-      const int64_t jj = base + tid;
-      const uint32_t u = jj < nv ? order_key(sr[jj]) : 0u;
-      const bool gt = jj < nv && u > thr;
-      const bool eq = jj < nv && u == thr;
-      const unsigned int bal = __ballot_sync(0xffffffffu, eq);
-      if (lane == 0) warp_cnt[warp] = __popc(bal);
-      __syncthreads();
-      unsigned int before = taken_eq;
-      for (int w2 = 0; w2 < warp; ++w2) before += warp_cnt[w2];
-      before += __popc(bal & ((1u << lane) - 1u));
-      if (gt || (eq && before < need_eq)) {
-        const unsigned int slot = atomicAdd(&sh_slots, 1u);
-        keys_s[slot] = ((unsigned long long)u << 32) | (unsigned long long)(0xffffffffu - (uint32_t)jj);
-      }
-      unsigned int blk = 0;
-      for (int w2 = 0; w2 < kTopkThreads / 32; ++w2) blk += warp_cnt[w2];
-      taken_eq += blk;
-      __syncthreads();
-    }
-    // sort, descending
-    if (kpad <= kTopkThreads && kpad >= 32) {
-      // every warp sorts its 32 keys with shuffles; the sorted runs are then
-      // merged pairwise (32 -> 64 -> ... -> kpad), each key moving to its own
-      // position plus the count of larger keys in the partner run (binary
-      // search).  Empty slots get distinct keys below every real one.
-      unsigned long long* buf0 = keys_s;
-      unsigned long long* buf1 = keys_s + kpad;
-      unsigned long long v = 0;
-      if (tid < kpad) {
-        v = keys_s[tid];
-        if (v == 0ull) v = (unsigned long long)(kpad - tid);
-      }
-#pragma unroll
-      for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, stride);
-          const bool desc = size == 32 || (lane & size) == 0, lower = (lane & stride) == 0;
-          v = (desc == lower) ? (v > o ? v : o) : (v < o ? v : o);
-        }
-      }
-      __syncthreads();
-      if (tid < kpad) buf0[tid] = v;
-      __syncthreads();
-      for (int L = 32; L < kpad; L <<= 1) {
-        if (tid < kpad) {
-          const unsigned long long x = buf0[tid];
-          const int r = tid / L, pos = tid - r * L;
-          const unsigned long long* part = buf0 + (r ^ 1) * L;
-          int c = 0;   // keys of the partner run larger than x (a prefix: runs are descending)
-          for (int st = L; st > 0; st >>= 1)
-            if (c + st <= L && part[c + st - 1] > x) c += st;
-          buf1[(r & ~1) * L + pos + c] = x;
-        }
-        __syncthreads();
-        unsigned long long* t = buf0;
-        buf0 = buf1;
-        buf1 = t;
-      }
-      if (buf0 != keys_s) {
-        if (tid < kpad) keys_s[tid] = buf0[tid];
-        __syncthreads();
-      }
-    } else {
-      for (int size = 2; size <= kpad; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int i = tid; i < kpad; i += kTopkThreads) {
-            const int p = i ^ stride;
-            if (p > i) {
-              const bool desc = (i & size) == 0;
-              const unsigned long long a = keys_s[i], c = keys_s[p];
-              if ((a < c) == desc) {
-                keys_s[i] = c;
-                keys_s[p] = a;
-              }
-            }
-          }
-          __syncthreads();
-        }
+        sh.remaining = rem - acc;
+        sh.prefix = prefix | ((uint32_t)d << shift);
       }
     }
+    mask |= 255u << shift;
+    __syncthreads();
   }
-  for (int r = tid; r < k; r += kTopkThreads) {
+  return sh.prefix;
+}
+
+// Writes the chosen candidates (key > thr, and the first need_eq keys == thr in
+// stream order) to dst[0..) in stream order as composite keys.  Warp w scans
+// slots [w seg, (w + 1) seg).
+template <class Src>
+__device__ void ordered_collect(const Src& src, int64_t n, uint32_t thr, unsigned int need_eq,
+                                unsigned long long* dst, TkShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t seg = ((n + kTkWarps - 1) / kTkWarps + 31) & ~int64_t(31);
+  const int64_t lo = warp * seg, hi = lo + seg < n ? lo + seg : n;
+  unsigned int ngt = 0, neq = 0;
+  for (int64_t b = lo; b < hi; b += 32) {
+    const int64_t i = b + lane;
+    uint32_t u = 0, id = 0;
+    const bool ok = i < hi && src.get(i, u, id);
+    ngt += __popc(__ballot_sync(0xffffffffu, ok && u > thr));
+    neq += __popc(__ballot_sync(0xffffffffu, ok && u == thr));
+  }
+  if (lane == 0) {
+    sh.cnt_gt[warp] = ngt;
+    sh.cnt_eq[warp] = neq;
+  }
+  __syncthreads();
+  unsigned int eq_before = 0, out = 0;
+  for (int w2 = 0; w2 < warp; ++w2) {
+    const unsigned int e = sh.cnt_eq[w2];
+    const unsigned int te = eq_before >= need_eq ? 0u : (need_eq - eq_before < e ? need_eq - eq_before : e);
+    out += sh.cnt_gt[w2] + te;
+    eq_before += e;
+  }
+  unsigned int eq_seen = eq_before;   // equal keys before this warp's current chunk
+  const unsigned int lt = (1u << lane) - 1u;
+  for (int64_t b = lo; b < hi; b += 32) {
+    const int64_t i = b + lane;
+    uint32_t u = 0, id = 0;
+    const bool ok = i < hi && src.get(i, u, id);
+    const bool gt = ok && u > thr, eq = ok && u == thr;
+    const unsigned int beq = __ballot_sync(0xffffffffu, eq);
+    const bool take = gt || (eq && eq_seen + __popc(beq & lt) < need_eq);
+    const unsigned int bt = __ballot_sync(0xffffffffu, take);
+    if (take) dst[out + __popc(bt & lt)] = composite(u, id);
+    out += __popc(bt);
+    eq_seen += __popc(beq);
+  }
+  __syncthreads();
+}
+
+// Sorts buf[0..P) descending (P a power of two >= 32, slots past `count` are
+// padded with distinct keys below every real one); buf has 2 P slots.
+// Returns the buffer that holds the result.
+__device__ unsigned long long* merge_sort_desc(unsigned long long* buf, int count, int P) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long* b0 = buf;
+  unsigned long long* b1 = buf + P;
+  for (int i = tid; i < P; i += kTopkThreads)
+    if (i >= count) b0[i] = (unsigned long long)(P - i);
+  __syncthreads();
+  for (int r = warp; r < P / 32; r += kTkWarps) {
+    unsigned long long v = b0[r * 32 + lane];
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, stride);
+        const bool desc = size == 32 || (lane & size) == 0, lower = (lane & stride) == 0;
+        v = (desc == lower) ? (v > o ? v : o) : (v < o ? v : o);
+      }
+    }
+    b0[r * 32 + lane] = v;
+  }
+  __syncthreads();
+  for (int L = 32; L < P; L <<= 1) {
+    for (int i = tid; i < P; i += kTopkThreads) {
+      const unsigned long long x = b0[i];
+      const int r = i / L, pos = i - r * L;
+      const unsigned long long* part = b0 + (r ^ 1) * L;
+      int c = 0;   // keys of the partner run larger than x (a prefix: runs are descending)
+      for (int st = L; st > 0; st >>= 1)
+        if (c + st <= L && part[c + st - 1] > x) c += st;
+      b1[(r & ~1) * L + pos + c] = x;
+    }
+    __syncthreads();
+    unsigned long long* t = b0;
+    b0 = b1;
+    b1 = t;
+  }
+  return b0;
+}
+
+__device__ __forceinline__ void emit_topk(const unsigned long long* sorted, int kk, int k, int64_t row,
+                                          int32_t* idx_out, float* score_out) {
+  for (int r = threadIdx.x; r < k; r += kTopkThreads) {
     int32_t j = -1;
     float sc = -INFINITY;
     if (r < kk) {
-      const unsigned long long key = keys_s[r];
+      const unsigned long long key = sorted[r];
       j = (int32_t)(0xffffffffu - (uint32_t)(key & 0xffffffffull));
       sc = order_key_value((uint32_t)(key >> 32));
     }
@@ -370,16 +409,86 @@ topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos,
   }
 }
 
+// One CTA per query row over its visible scores (rows of any length).
+__global__ void __launch_bounds__(kTopkThreads)
+topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int P,
+            int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
+  extern __shared__ unsigned long long keys_s[];   // 2 P composite keys
+  __shared__ TkShared sh;
+  const int64_t row = blockIdx.x;
+  const int64_t nv = visible_entries(q_pos[row], m, N);
+  const int kk = (int)((int64_t)k < nv ? (int64_t)k : nv);
+  const DenseRow src{scores + row * N, 0};
+  if (kk > 0) {
+    const uint32_t thr = radix_threshold(src, nv, kk, sh);
+    ordered_collect(src, nv, thr, sh.remaining, keys_s, sh);
+  }
+  const unsigned long long* sorted = merge_sort_desc(keys_s, kk, P);
+  emit_topk(sorted, kk, k, row, idx_out, score_out);
+}
+
+// Stage 1 of long rows: grid (rows, chunks); chunk c keeps the top-k of its
+// visible candidates [c C, (c + 1) C) in index order, at cand[(row chunks + c) k].
+__global__ void __launch_bounds__(kTopkThreads)
+topk_stage1_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m, int k,
+                   int chunks, unsigned long long* __restrict__ cand) {
+  __shared__ TkShared sh;
+  const int64_t row = blockIdx.x;
+  const int c = blockIdx.y;
+  const int64_t nv = visible_entries(q_pos[row], m, N);
+  const int64_t c0 = (int64_t)c * kTkChunk;
+  const int64_t n = nv - c0 < 0 ? 0 : (nv - c0 < kTkChunk ? nv - c0 : kTkChunk);
+  const int kk = (int)((int64_t)k < n ? (int64_t)k : n);
+  unsigned long long* dst = cand + ((int64_t)row * chunks + c) * k;
+  if (kk > 0) {
+    const DenseRow src{scores + row * N, c0};
+    const uint32_t thr = radix_threshold(src, n, kk, sh);
+    ordered_collect(src, n, thr, sh.remaining, dst, sh);
+  }
+  for (int i = kk + threadIdx.x; i < k; i += kTopkThreads) dst[i] = 0ull;   // empty slots
+}
+
+// Stage 2: one CTA per row selects among its chunks' winners (in index order).
+__global__ void __launch_bounds__(kTopkThreads)
+topk_stage2_kernel(const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int chunks, int P,
+                   const unsigned long long* __restrict__ cand, int32_t* __restrict__ idx_out,
+                   float* __restrict__ score_out) {
+  extern __shared__ unsigned long long keys_s[];   // 2 P composite keys
+  __shared__ TkShared sh;
+  const int64_t row = blockIdx.x;
+  const int64_t nv = visible_entries(q_pos[row], m, N);
+  const int kk = (int)((int64_t)k < nv ? (int64_t)k : nv);
+  const CandList src{cand + (int64_t)row * chunks * k};
+  const int64_t n = (int64_t)chunks * k;
+  if (kk > 0) {
+    const uint32_t thr = radix_threshold(src, n, kk, sh);
+    ordered_collect(src, n, thr, sh.remaining, keys_s, sh);
+  }
+  const unsigned long long* sorted = merge_sort_desc(keys_s, kk, P);
+  emit_topk(sorted, kk, k, row, idx_out, score_out);
+}
+
 int topk_pad(int k) {
-  int p = 1;
+  int p = 32;
   while (p < k) p <<= 1;
-  return p < 2 ? 2 : p;
+  return p;
+}
+
+int topk_chunks(int64_t N) { return N > kTkChunk ? (int)((N + kTkChunk - 1) / kTkChunk) : 0; }
+
+size_t topk_cand_bytes(int B, int64_t Tq, int64_t N, int k) {
+  const int ch = topk_chunks(N);
+  return ch ? (size_t)B * (size_t)Tq * (size_t)ch * (size_t)k * 8 : 0;
+}
+
+bool topk_two_stage(int B, int64_t Tq, int64_t N) {
+  return topk_chunks(N) > 0 && (int64_t)B * Tq < 4 * 148;
 }
 
 cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
                                 const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
                                 int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
-                                float* score_out, float* scores_ws, void* tc_ws, void* flags_ws,
+                                float* score_out, float* scores_ws, void* tc_ws, void* cand_ws, void* flags_ws,
                                 cudaStream_t st) {
   if ((int64_t)B * Tq == 0) return cudaSuccess;
   if (N > 0) {
@@ -402,15 +511,25 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
     }
     if (e != cudaSuccess) return e;
   }
-  const int kpad = topk_pad(k);
-  const size_t smem = sizeof(unsigned long long) * (size_t)kpad * (kpad <= kTopkThreads ? 2 : 1);
+  const int P = topk_pad(k);
+  const size_t smem = sizeof(unsigned long long) * 2 * (size_t)P;
   static bool attr_set = false;
   if (!attr_set) {
     cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(topk_stage2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     attr_set = true;
   }
-  topk_kernel<<<(unsigned)(B * Tq), kTopkThreads, smem, st>>>(scores_ws, q_pos, N, m, k, kpad,
-                                                             idx_out, score_out);
+  const int64_t rows = (int64_t)B * Tq;
+  if (cand_ws && topk_two_stage(B, Tq, N)) {
+    const int ch = topk_chunks(N);
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(cand_ws);
+    topk_stage1_kernel<<<dim3((unsigned)rows, (unsigned)ch), kTopkThreads, 0, st>>>(scores_ws, q_pos, N, m, k, ch,
+                                                                                  cand);
+    topk_stage2_kernel<<<(unsigned)rows, kTopkThreads, smem, st>>>(q_pos, N, m, k, ch, P, cand, idx_out,
+                                                                   score_out);
+  } else {
+    topk_kernel<<<(unsigned)rows, kTopkThreads, smem, st>>>(scores_ws, q_pos, N, m, k, P, idx_out, score_out);
+  }
   return cudaGetLastError();
 }
 

@@ -43,8 +43,11 @@ cudaError_t launch_pack_mixed(const float* v, int64_t n, uint8_t* out, cudaStrea
 cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
                                 const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
                                 int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
-                                float* score_out, float* scores_ws, void* tc_ws, void* flags_ws,
+                                float* score_out, float* scores_ws, void* tc_ws, void* cand_ws, void* flags_ws,
                                 cudaStream_t st);
+// two-stage top-k for long rows when there are few of them, and its scratch
+bool topk_two_stage(int B, int64_t Tq, int64_t N);
+size_t topk_cand_bytes(int B, int64_t Tq, int64_t N, int k);
 // FP8 tensor-core scoring (indexer_tc.cu): whether it applies, its extra
 // scratch, and the launch (scores only; top-k follows in indexer.cu)
 bool indexer_tc_applies(int B, int64_t Tq, int HI, int dI, int64_t N);
