@@ -223,6 +223,8 @@ struct Params {
   float* part_o;      // [items, 64, 512] unnormalised O (split mode)
   float* part_ml;     // [items, 64, 2] running max (log2 units) and sum
   const __nv_bfloat16* xcache;   // bf16 copy of the cache rows [B, N, 512], or NULL
+  const __nv_bfloat16* xg;       // or: every row's own keys in bf16, [rows, kp, 512], zero padded
+  int64_t kp;                    // key slots per row of xg (a multiple of the tile)
   int64_t xrows;                 // rows of the bf16 copy (cache rows, then window rows)
   int64_t xwin0;                 // first window row in the copy (= B * N)
   const int32_t* clist;          // [rows, kpad] valid selected entries of each row, in idx order
@@ -379,6 +381,54 @@ prep_rows_kernel(const __nv_bfloat16* __restrict__ q, const int64_t* __restrict_
   if (lane == 0) ccount[row] = cnt;
 }
 
+// Per-row key rows in bf16 (decode): slot (r, key) of xg holds key `key` of
+// query row r -- its selected (or, dense, visible) entries in order, then its
+// window tokens -- expanded exactly from the mixed rows; slots past the row's
+// keys are zero.  One warp per slot.
+__global__ void __launch_bounds__(256)
+gather_expand_kernel(const Params p, int64_t rows, int dense, __nv_bfloat16* __restrict__ xg) {
+  const int64_t slot = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t r = slot / p.kp;
+  if (r >= rows) return;
+  const int64_t key = slot - r * p.kp;
+  const int64_t b = r / p.Tq, t = p.q_pos[r];
+  const bool t_ok = t >= 0 && t < p.rope_rows;
+  int64_t ne = 0;
+  if (t_ok) {
+    if (dense) {
+      const int64_t nv = (t + 1) / p.m;
+      ne = nv < p.N ? nv : p.N;
+    } else {
+      ne = p.ccount[r];
+    }
+  }
+  const int64_t u_lo = t - p.W + 1 < 0 ? 0 : t - p.W + 1;
+  const int64_t p0 = p.W > 0 ? p.swa_pos0[b] : 0;
+  const int64_t w_lo = u_lo < p0 ? p0 : u_lo;
+  const int64_t w_hi = t < p0 + p.Ts - 1 ? t : p0 + p.Ts - 1;
+  const int64_t nwin = (t_ok && p.W > 0 && w_hi >= w_lo) ? w_hi - w_lo + 1 : 0;
+  const uint8_t* row = nullptr;
+  if (key < ne) row = p.cache + (b * p.N + (dense ? key : (int64_t)p.clist[r * p.kpad + key])) * kMixRow;
+  else if (key < ne + nwin) row = p.swa + (b * p.Ts + (w_lo - p0 + (key - ne))) * kMixRow;
+  uint4* dst = reinterpret_cast<uint4*>(xg + slot * kD);
+  if (!row) {
+    dst[2 * lane] = make_uint4(0, 0, 0, 0);
+    dst[2 * lane + 1] = make_uint4(0, 0, 0, 0);
+  } else if (lane < 28) {
+    const uint4 c = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+    const float sc = __ldg(reinterpret_cast<const float*>(row + kMixScaleOff) + (lane >> 3));
+    uint4 o0, o1;
+    dequant16(c, sc, o0, o1);
+    dst[2 * lane] = o0;
+    dst[2 * lane + 1] = o1;
+  } else {
+    const int l4 = lane - 28;
+    dst[56 + 2 * l4] = __ldg(reinterpret_cast<const uint4*>(row + kMixRopeOff) + 2 * l4);
+    dst[56 + 2 * l4 + 1] = __ldg(reinterpret_cast<const uint4*>(row + kMixRopeOff) + 2 * l4 + 1);
+  }
+}
+
 template <bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_q,
@@ -454,7 +504,29 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         if (ok && !mbar_wait(&ms->list_full[nq & 1], (nq >> 1) & 1, kWaitLimit)) ok = false;
         if (!ok) break;
       }
-      if (p.xcache) {
+      if (p.xg) {
+        // the row's keys are contiguous bf16 rows: 8 TMA boxes of 64 rows x
+        // 64 columns per tile from producer warp 0; the others only arrive
+        for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
+          const int buf = g & 1;
+          if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
+            ok = false;
+            break;
+          }
+          const uint32_t tb = smem_u32(sKV + buf * 65536);
+          if (pw == 0) {
+            if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], kTile * kD * 2);
+            __syncwarp();
+            if (lane < 8)
+              tma_load_2d(tb + lane * 8192, &tm_rows, 64 * lane, (int)(I.row * p.kp + (int64_t)tl * kTile),
+                          &ms->kv_full[buf]);
+          } else if (lane == 0) {
+            mbar_arrive(&ms->kv_full[buf]);
+          }
+          cp_async_mbar_arrive_noinc(&ms->kv_full[buf]);   // no copies of this lane: arrives at once
+          __syncwarp();
+        }
+      } else if (p.xcache) {
         // bf16 rows are ready.  Producer warp pw fetches rows 16 pw .. 16 pw + 15
         // of each tile: dims 0..255 by TMA gathers (4 rows x 128 bytes per
         // instruction, lanes 0..15) and dims 256..511 by 16-byte cp.async
@@ -1011,9 +1083,11 @@ size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 // when each is read about once (decode).
 struct Plan {
   int nsplit;
-  bool expand;
+  bool expand;              // shared bf16 copy of all cache and window rows (prefill)
+  bool gather;              // or every row's own keys in bf16 (decode)
   int kpad;
-  size_t qr_bytes, list_bytes, part_bytes, x_bytes;
+  int64_t kp;               // key slots per row when gathered
+  size_t qr_bytes, list_bytes, part_bytes, x_bytes, g_bytes;
 };
 
 Plan make_plan(int B, int64_t Tq, int64_t max_keys, int64_t N, int64_t Ts, int k) {
@@ -1028,6 +1102,10 @@ Plan make_plan(int B, int64_t Tq, int64_t max_keys, int64_t N, int64_t Ts, int k
   const double nrows = (double)B * (double)(N + Ts);
   pl.expand = nrows > 0 && uses >= 8.0 * nrows;
   pl.x_bytes = pl.expand ? al256((size_t)B * (size_t)(N + Ts) * kD * 2) : 0;
+  pl.kp = (max_keys + kTile - 1) / kTile * kTile;
+  const double gbytes = (double)rows * (double)pl.kp * kD * 2;
+  pl.gather = !pl.expand && pl.kp > 0 && gbytes <= (double)(2ull << 30) && (double)rows * pl.kp < 2147483647.0;
+  pl.g_bytes = pl.gather ? al256((size_t)gbytes) : 0;
   return pl;
 }
 
@@ -1070,7 +1148,7 @@ bool make_row_map(CUtensorMap* m, const void* base, uint64_t width, uint64_t row
 size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys, int64_t N, int64_t Ts, int k) {
   if (H != kH || D != kD) return 0;
   const Plan pl = make_plan(B, Tq, max_keys, N, Ts, k);
-  return pl.qr_bytes + pl.list_bytes + pl.part_bytes + pl.x_bytes;
+  return pl.qr_bytes + pl.list_bytes + pl.part_bytes + pl.x_bytes + pl.g_bytes;
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
@@ -1125,6 +1203,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
     pl.part_bytes = 0;
   }
   if (pl.expand && pl.part_bytes + pl.x_bytes > avail) pl.expand = false;
+  if (pl.gather && pl.part_bytes + pl.g_bytes > avail) pl.gather = false;
   if ((int64_t)a.B * (a.N + (a.W > 0 ? a.Ts : 0)) >= INT32_MAX) pl.expand = false;   // TMA rows are int32
   p.nsplit = pl.nsplit;
   p.items = rows * p.nsplit;
@@ -1139,7 +1218,15 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
   tm_rows = tm_q;
   p.xrows = 0;
   p.xwin0 = 0;
-  if (pl.expand) {
+  p.xg = nullptr;
+  p.kp = pl.kp;
+  if (pl.gather) {
+    __nv_bfloat16* xg = reinterpret_cast<__nv_bfloat16*>(base);
+    const int64_t slots = rows * pl.kp;
+    gather_expand_kernel<<<(unsigned)((slots + 7) / 8), 256, 0, st>>>(p, rows, a.idx ? 0 : 1, xg);
+    p.xg = xg;
+    if (!make_row_map(&tm_rows, xg, kD, (uint64_t)slots, 64)) return cudaErrorInvalidValue;
+  } else if (pl.expand) {
     const int64_t nc = (int64_t)a.B * a.N, nw = (a.W > 0) ? (int64_t)a.B * a.Ts : 0;
     __nv_bfloat16* xc = reinterpret_cast<__nv_bfloat16*>(base);
     if (nc > 0) expand_rows_kernel<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(p.cache, nc, xc);

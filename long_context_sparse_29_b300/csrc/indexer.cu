@@ -150,6 +150,126 @@ scores_fp4_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict_
 }
 
 // ---------------------------------------------------------------------------
+// FP4 scores for few query rows against long entry lists (decode): grid
+// (entry chunks of kDecChunk, rows); the row's query is quantised by the CTA
+// (while its first entries are in flight); each thread scores kDecKPT
+// entries per round, their loads issued together.  Codes become doubled
+// values by a byte-permute table; the even and odd elements of each 8-element
+// group are dotted separately (an integer sum: same result).
+// ---------------------------------------------------------------------------
+constexpr int kDecKPT = 4;
+constexpr int kDecChunk = kScoreThreads * kDecKPT * 2;
+
+// four E2M1 codes (one per byte, low nibble) -> their doubled values as int8x4
+__device__ __forceinline__ uint32_t e2m1x2_int8x4(uint32_t b4) {
+  const uint32_t mg = b4 & 0x07070707u;
+  const uint32_t sel = (mg & 0x7u) | ((mg >> 4) & 0x70u) | ((mg >> 8) & 0x700u) | ((mg >> 12) & 0x7000u);
+  const uint32_t mag = __byte_perm(0x03020100u, 0x0C080604u, sel);   // 0,1,2,3,4,6,8,12
+  const uint32_t neg = ((b4 >> 3) & 0x01010101u) * 0xFFu;          // 0xFF in negative bytes
+  return __vsub4(mag ^ neg, neg);
+}
+
+__global__ void __launch_bounds__(kScoreThreads)
+scores_fp4_decode_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
+                         const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
+                         const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
+                         float* __restrict__ scores) {
+  // doubled query values: head h, block b, group i (8 elements): word [h][b][0][i] even
+  // elements, [h][b][1][i] odd elements of the group
+  __shared__ __align__(16) int32_t qv_s[kMaxHI][2][2][4];
+  __shared__ int8_t qe_s[kMaxHI][2];
+  __shared__ float w_s[kMaxHI];
+  const int64_t row = blockIdx.y;
+  const int64_t b = row / Tq;
+  const int tid = threadIdx.x;
+  const int64_t nv = visible_entries(q_pos[row], m, N);
+  const int64_t c0 = (int64_t)blockIdx.x * kDecChunk;
+  if (c0 >= nv) return;
+  const int64_t c1 = c0 + kDecChunk < nv ? c0 + kDecChunk : nv;
+  // the first round's entries, in flight during the query quantisation
+  uint4 cw[kDecKPT][2];
+  uint32_t se[kDecKPT];
+#pragma unroll
+  for (int i = 0; i < kDecKPT; ++i) {
+    const int64_t j = c0 + tid + kScoreThreads * i;
+    const int64_t jj = j < c1 ? j : c0;
+    cw[i][0] = __ldg(reinterpret_cast<const uint4*>(kc + (b * N + jj) * 32));
+    cw[i][1] = __ldg(reinterpret_cast<const uint4*>(kc + (b * N + jj) * 32) + 1);
+    se[i] = __ldg(reinterpret_cast<const uint16_t*>(ks + (b * N + jj) * 2));
+  }
+  if (tid < HI * 2) {   // quantise block (h, blk) of the query
+    const int h = tid >> 1, blk = tid & 1;
+    const __nv_bfloat16* src = qI + (row * HI + h) * 64 + 32 * blk;
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] = __bfloat162float(src[i]);
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const int sx = mx_block_exp(amax);
+    const float inv = pow2i(-sx);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t ev = 0, od = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ev |= ((uint32_t)(e2m1_x2(e2m1_encode(__fmul_rn(v[8 * g + 2 * e], inv))) & 0xff)) << (8 * e);
+        od |= ((uint32_t)(e2m1_x2(e2m1_encode(__fmul_rn(v[8 * g + 2 * e + 1], inv))) & 0xff)) << (8 * e);
+      }
+      qv_s[h][blk][0][g] = (int32_t)ev;
+      qv_s[h][blk][1][g] = (int32_t)od;
+    }
+    qe_s[h][blk] = (int8_t)sx;
+  }
+  if (tid < HI) w_s[tid] = w[row * HI + tid];
+  __syncthreads();
+  for (int64_t base = c0; base < c1; base += (int64_t)kScoreThreads * kDecKPT) {
+#pragma unroll
+    for (int i = 0; i < kDecKPT; ++i) {
+      const int64_t j = base + tid + kScoreThreads * i;
+      if (base > c0) {   // this round's entries (the first round's were loaded above)
+        const int64_t jj = j < c1 ? j : c0;
+        cw[i][0] = __ldg(reinterpret_cast<const uint4*>(kc + (b * N + jj) * 32));
+        cw[i][1] = __ldg(reinterpret_cast<const uint4*>(kc + (b * N + jj) * 32) + 1);
+        se[i] = __ldg(reinterpret_cast<const uint16_t*>(ks + (b * N + jj) * 2));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kDecKPT; ++i) {
+      const int64_t j = base + tid + kScoreThreads * i;
+      // entry words: block b = codes 32 b .. 32 b + 31 = words 4 b .. 4 b + 3 (8 codes each)
+      const uint32_t wd[8] = {cw[i][0].x, cw[i][0].y, cw[i][0].z, cw[i][0].w,
+                              cw[i][1].x, cw[i][1].y, cw[i][1].z, cw[i][1].w};
+      int32_t kev[8], kod[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        kev[g] = (int32_t)e2m1x2_int8x4(wd[g] & 0x0F0F0F0Fu);
+        kod[g] = (int32_t)e2m1x2_int8x4((wd[g] >> 4) & 0x0F0F0F0Fu);
+      }
+      const int ke0 = (int)(se[i] & 0xff) - 127, ke1 = (int)(se[i] >> 8) - 127;
+      float sc = 0.0f;
+      for (int h = 0; h < HI; ++h) {
+        const int4* q4 = reinterpret_cast<const int4*>(&qv_s[h][0][0][0]);
+        const int4 q0e = q4[0], q0o = q4[1], q1e = q4[2], q1o = q4[3];
+        int P0 = 0, P1 = 0;
+        P0 = __dp4a(kev[0], q0e.x, P0); P0 = __dp4a(kod[0], q0o.x, P0);
+        P0 = __dp4a(kev[1], q0e.y, P0); P0 = __dp4a(kod[1], q0o.y, P0);
+        P0 = __dp4a(kev[2], q0e.z, P0); P0 = __dp4a(kod[2], q0o.z, P0);
+        P0 = __dp4a(kev[3], q0e.w, P0); P0 = __dp4a(kod[3], q0o.w, P0);
+        P1 = __dp4a(kev[4], q1e.x, P1); P1 = __dp4a(kod[4], q1o.x, P1);
+        P1 = __dp4a(kev[5], q1e.y, P1); P1 = __dp4a(kod[5], q1o.y, P1);
+        P1 = __dp4a(kev[6], q1e.z, P1); P1 = __dp4a(kod[6], q1o.z, P1);
+        P1 = __dp4a(kev[7], q1e.w, P1); P1 = __dp4a(kod[7], q1o.w, P1);
+        const float d = combine_blocks(P0, qe_s[h][0] + ke0 - 2, P1, qe_s[h][1] + ke1 - 2);
+        sc = __fmaf_rn(w_s[h], d > 0.0f ? d : 0.0f, sc);
+      }
+      if (j < c1) scores[row * N + j] = sc;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // fp32 scores (dI <= 64): fma chain over the head dim.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kScoreThreads)
@@ -496,6 +616,12 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
     if (fp4 && tc_ws && indexer_tc_applies(B, Tq, HI, dI, N)) {
       e = launch_indexer_scores_tc(qI, w, reinterpret_cast<const uint8_t*>(kI), kI_scales, q_pos, B, Tq, HI, N,
                                    m, scores_ws, tc_ws, flags_ws, st);
+    } else if (fp4 && Tq <= 4 && HI <= kMaxHI && N >= 4 * kDecChunk) {
+      const dim3 grid((unsigned)((N + kDecChunk - 1) / kDecChunk), (unsigned)(B * Tq));
+      scores_fp4_decode_kernel<<<grid, kScoreThreads, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(qI), w,
+                                                               reinterpret_cast<const uint8_t*>(kI), kI_scales,
+                                                               q_pos, Tq, HI, N, m, scores_ws);
+      e = cudaGetLastError();
     } else {
       const dim3 grid((unsigned)((N + kScoreThreads - 1) / kScoreThreads),
                       (unsigned)((Tq + kScoreQT - 1) / kScoreQT), (unsigned)B);
