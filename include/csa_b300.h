@@ -156,6 +156,45 @@ int csa_compress_kv(const void *x, int x_dtype, const float *z, const float *s,
                     uint8_t *out_scales, void *stream);
 
 /*
+ * csa_decode_append: decode-time maintenance of one layer's caches -- one new
+ * token per sequence.  [XM] CSA / HCA: every m tokens become one compressed
+ * entry; [XM] "百万Token 长上下文真实表现" (state cache for the uncompressed
+ * tail) and [HU] Sliding Window: the newest tokens stay uncompressed in a
+ * window cache.  Per sequence b, with t = t_pos[b] (device) the new token's
+ * position:
+ *  - kv [b] (C = 512 bf16) and z [b] go to ring slot t mod m of kv_tail
+ *    [B, m, C] bf16 / z_tail [B, m] fp32 (the raw tokens of the block being
+ *    filled); likewise kI [b] (CI bf16) and zI [b] to kI_tail / zI_tail when
+ *    kI is not NULL (indexer keys, CSA layers);
+ *  - the token is packed into the window cache swa [B, Ts, 592] at row
+ *    t - swa_pos0[b] exactly as csa_compress_kv with m = 1 and s = NULL
+ *    stores it (RoPE at t).  When that row is Ts, the last W - 1 rows first
+ *    move to rows 0 .. W - 2 and swa_pos0[b] (device, updated) becomes
+ *    t - W + 1; so the window cache always holds tokens swa_pos0[b] .. t,
+ *    the form csa_sparse_mqa / hca_dense_attn read.  Requires Ts >= 2 W;
+ *  - when (t + 1) mod m == 0 the block [t - m + 1, t] is compressed from the
+ *    ring into entry j = (t + 1) / m - 1 of cache [B, nmax, 592] (RoPE at t)
+ *    and, when kI is given, of kI_codes [B, nmax, CI/2] / kI_scales
+ *    [B, nmax, CI/32] (MXFP4, no RoPE), with the very operations of
+ *    csa_compress_kv (s, sI: the channel scales, or NULL); entries j >= nmax
+ *    are not stored.
+ * Tokens of a sequence must be appended in order (t = previous t + 1; the
+ * first one at t = swa_pos0[b], with the ring slots of its block filled by
+ * earlier calls), so that after the call for token t the caches equal those
+ * csa_compress_kv builds from tokens 0 .. t.  A sequence whose t has no RoPE
+ * row (t < 0 or t >= rope_rows) is left unchanged; rows outside the window
+ * buffer are never written.
+ * Errors: INVALID_ARG (NULL pointers, m outside 1..128, Ts < 2 W);
+ * UNSUPPORTED (C != 512, R != 64, CI not 32 or 64 with kI given).
+ */
+int csa_decode_append(const void *kv, const float *z, const void *kI, const float *zI, const float *s,
+                      const float *sI, const float *rope_cos, const float *rope_sin, int64_t rope_rows,
+                      const int64_t *t_pos,
+                      int B, int C, int R, int CI, int m, void *kv_tail, float *z_tail, void *kI_tail,
+                      float *zI_tail, uint8_t *cache, int64_t nmax, uint8_t *kI_codes, uint8_t *kI_scales,
+                      uint8_t *swa, int64_t Ts, int W, int64_t *swa_pos0, void *stream);
+
+/*
  * csa_indexer_topk: lightning-indexer scores of every visible compressed
  * entry for every query, and the top-k of them.
  * [XM] CSA: the lightning indexer picks the top-k compressed entries per

@@ -21,7 +21,7 @@ import torch
 from ._lib import CsaError, check, lib
 
 __all__ = ["CsaError", "Workspace", "rope_table", "compress_kv", "kvcache_pack_fp8_bf16",
-           "indexer_topk", "sparse_mqa", "hca_dense_attn", "workspace_size",
+           "indexer_topk", "sparse_mqa", "hca_dense_attn", "workspace_size", "LayerCache", "decode_append",
            "DTYPE_F32", "DTYPE_BF16", "FMT_F32", "FMT_MIXED592", "FMT_MXFP4"]
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
@@ -143,6 +143,44 @@ def compress_kv(x, z, s, m: int, out_fmt: int, R: int = 0, rope=None, pos0: int 
     check(lib().csa_compress_kv(_ptr(x), _dt(x), _ptr(z), _ptr(s), _ptr(rc), _ptr(rs), rows, pos0,
                                 B, T, C, R, m, out_fmt, _ptr(out), _ptr(out_scales), _stream(dev)))
     return (out, out_scales) if out_fmt == FMT_MXFP4 else out
+
+
+class LayerCache:
+    """Device state of one attention layer's decode caches (csa_decode_append):
+    compressed entries [B, nmax, 592], indexer keys (CSA layers: CI > 0), the
+    window cache [B, Ts, 592] with its first position per sequence, and the
+    rings of the last m raw tokens."""
+
+    def __init__(self, B: int, nmax: int, m: int, W: int, Ts: int | None = None, CI: int = 0, C: int = 512,
+                 pos0: int = 0, device="cuda"):
+        dev = torch.device(device)
+        self.B, self.nmax, self.m, self.W, self.CI, self.C = B, nmax, m, W, CI, C
+        self.Ts = Ts if Ts is not None else 2 * W
+        self.cache = torch.zeros((B, nmax, MIXED_ROW), dtype=torch.uint8, device=dev)
+        self.kI_codes = torch.zeros((B, nmax, CI // 2), dtype=torch.uint8, device=dev) if CI else None
+        self.kI_scales = torch.zeros((B, nmax, CI // 32), dtype=torch.uint8, device=dev) if CI else None
+        self.swa = torch.zeros((B, self.Ts, MIXED_ROW), dtype=torch.uint8, device=dev)
+        self.swa_pos0 = torch.full((B,), pos0, dtype=torch.int64, device=dev)
+        self.kv_tail = torch.zeros((B, m, C), dtype=torch.bfloat16, device=dev)
+        self.z_tail = torch.zeros((B, m), dtype=torch.float32, device=dev)
+        self.kI_tail = torch.zeros((B, m, CI), dtype=torch.bfloat16, device=dev) if CI else None
+        self.zI_tail = torch.zeros((B, m), dtype=torch.float32, device=dev) if CI else None
+
+
+def decode_append(lc: LayerCache, kv, z, t_pos, rope, kI=None, zI=None, s=None, sI=None, R: int = 64):
+    """Append one token per sequence to lc (see csa_decode_append): kv [B, C]
+    bf16, z [B] fp32, t_pos [B] int64 (device), kI [B, CI] bf16 / zI [B] for
+    CSA layers."""
+    _need(kv, "kv", torch.bfloat16)
+    _need(z, "z", torch.float32)
+    _need(t_pos, "t_pos", torch.int64)
+    B, C = kv.shape
+    rc, rs = rope
+    check(lib().csa_decode_append(_ptr(kv), _ptr(z), _ptr(kI), _ptr(zI), _ptr(s), _ptr(sI), _ptr(rc), _ptr(rs),
+                                  rc.shape[0], _ptr(t_pos), B, C, R, lc.CI, lc.m, _ptr(lc.kv_tail), _ptr(lc.z_tail),
+                                  _ptr(lc.kI_tail), _ptr(lc.zI_tail), _ptr(lc.cache), lc.nmax, _ptr(lc.kI_codes),
+                                  _ptr(lc.kI_scales), _ptr(lc.swa), lc.Ts, lc.W, _ptr(lc.swa_pos0),
+                                  _stream(kv.device)))
 
 
 def kvcache_pack_fp8_bf16(v, out=None):

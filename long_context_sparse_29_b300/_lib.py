@@ -35,6 +35,8 @@ SIGNATURES = {
                                        P, P]),
     "hca_dense_attn": (I32, [P, I32, P, I32, I64, I32, I32, I32, I32, P, I64, I32, P, P, I64, I32,
                              F32, P, P, I64, P, P, P, SZ, P]),
+    "csa_decode_append": (I32, [P, P, P, P, P, P, P, P, I64, P, I32, I32, I32, I32, I32, P, P, P, P, P, I64, P,
+                                P, P, I64, I32, P, P]),
 }
 
 _lib = None

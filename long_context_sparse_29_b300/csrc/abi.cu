@@ -230,6 +230,29 @@ int csa_compress_kv(const void* x, int x_dtype, const float* z, const float* s,
                      nm);
 }
 
+int csa_decode_append(const void* kv, const float* z, const void* kI, const float* zI, const float* s,
+                      const float* sI, const float* rope_cos, const float* rope_sin, int64_t rope_rows,
+                      const int64_t* t_pos,
+                      int B, int C, int R, int CI, int m, void* kv_tail, float* z_tail, void* kI_tail,
+                      float* zI_tail, uint8_t* cache, int64_t nmax, uint8_t* kI_codes, uint8_t* kI_scales,
+                      uint8_t* swa, int64_t Ts, int W, int64_t* swa_pos0, void* stream) {
+  const char* nm = "csa_decode_append";
+  if (B < 0 || m < 1 || m > 128 || nmax < 0 || W < 0 || Ts < 0)
+    return fail(CSA_ERR_INVALID_ARG, "%s: bad sizes", nm);
+  if (C != 512 || R != 64) return fail(CSA_ERR_UNSUPPORTED, "%s: needs C = 512 and R = 64", nm);
+  if (kI && CI != 32 && CI != 64) return fail(CSA_ERR_UNSUPPORTED, "%s: CI must be 32 or 64", nm);
+  if (W > 0 && Ts < 2 * (int64_t)W) return fail(CSA_ERR_INVALID_ARG, "%s: Ts must be >= 2 W", nm);
+  if (B == 0) return ok();
+  if (!kv || !z || !t_pos || !kv_tail || !z_tail || !rope_cos || !rope_sin || (nmax > 0 && !cache) ||
+      (W > 0 && (!swa || !swa_pos0)) || (kI && (!zI || !kI_tail || !zI_tail || (nmax > 0 && (!kI_codes || !kI_scales)))))
+    return fail(CSA_ERR_INVALID_ARG, "%s: NULL pointer", nm);
+  return cuda_result(csa::launch_decode_append(kv, z, kI, zI, s, sI, rope_cos, rope_sin, rope_rows, t_pos, B, C, R,
+                                               kI ? CI : 0, m,
+                                               kv_tail, z_tail, kI_tail, zI_tail, cache, nmax, kI_codes, kI_scales,
+                                               swa, Ts, W, swa_pos0, as_stream(stream)),
+                     nm);
+}
+
 int csa_indexer_topk(const void* qI, int qI_dtype, const float* w, const void* kI,
                      const uint8_t* kI_scales, int kI_fmt, const int64_t* q_pos, int B, int64_t Tq,
                      int HI, int dI, int64_t N, int m, int k, int32_t* idx_out, float* score_out,

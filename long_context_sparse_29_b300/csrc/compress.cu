@@ -66,34 +66,33 @@ __device__ __forceinline__ void pack_mixed_row(const float2 (&v)[kMaxPairs], int
   }
 }
 
+// One compressed entry by one warp: the m token rows at x (row stride C
+// elements), their logits z[0..m), the channel scale s (or NULL), RoPE of the
+// last R channels at position P, stored in format FMT at out (entry 0 of out)
+// and out_scales.  alpha is m floats of warp-private shared memory.  The same
+// code serves block compression and the decode-time append, so both store the
+// same bytes.
 template <int FMT, bool BF16>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
-                const float* __restrict__ s, const float* __restrict__ rcos,
-                const float* __restrict__ rsin, int64_t pos0, int B, int64_t T, int C, int R,
-                int m, int64_t N, void* __restrict__ out, uint8_t* __restrict__ out_scales) {
-  __shared__ float alpha_s[kWarpsPerBlock][128];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ent = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
-  if (ent >= (int64_t)B * N) return;
-  const int64_t b = ent / N, j = ent % N;
-  const int64_t tok0 = b * T + j * m;   // first token row of the block
-
+__device__ __forceinline__ void compress_entry(const void* __restrict__ x, const float* __restrict__ z,
+                                               const float* __restrict__ s, const float* __restrict__ rcos,
+                                               const float* __restrict__ rsin, int64_t P, int C, int R, int m,
+                                               void* __restrict__ out, uint8_t* __restrict__ out_scales,
+                                               float* alpha, int lane) {
   // ---- weights of the block: a = softmax(z) with the library exponential ----
   float mu = -INFINITY;
-  for (int i = lane; i < m; i += 32) mu = fmaxf(mu, z[tok0 + i]);
+  for (int i = lane; i < m; i += 32) mu = fmaxf(mu, z[i]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, o));
-  for (int i = lane; i < m; i += 32) alpha_s[warp][i] = sexp(__fsub_rn(z[tok0 + i], mu));
+  for (int i = lane; i < m; i += 32) alpha[i] = sexp(__fsub_rn(z[i], mu));
   __syncwarp();
   float S = 0.0f;
   if (lane == 0) {
-    S = alpha_s[warp][0];
-    for (int i = 1; i < m; ++i) S = __fadd_rn(S, alpha_s[warp][i]);
+    S = alpha[0];
+    for (int i = 1; i < m; ++i) S = __fadd_rn(S, alpha[i]);
   }
   S = __shfl_sync(0xffffffffu, S, 0);
   __syncwarp();
-  for (int i = lane; i < m; i += 32) alpha_s[warp][i] = __fdiv_rn(alpha_s[warp][i], S);
+  for (int i = lane; i < m; i += 32) alpha[i] = __fdiv_rn(alpha[i], S);
   __syncwarp();
 
   // ---- weighted sum over the block's tokens, channel pairs per lane ----
@@ -102,8 +101,8 @@ compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
 #pragma unroll
   for (int r = 0; r < kMaxPairs; ++r) v[r] = make_float2(0.0f, 0.0f);
   for (int i = 0; i < m; ++i) {
-    const float a = alpha_s[warp][i];
-    const int64_t row = (tok0 + i) * C;
+    const float a = alpha[i];
+    const int64_t row = (int64_t)i * C;
 #pragma unroll
     for (int r = 0; r < kMaxPairs; ++r) {
       const int p = lane + 32 * r;
@@ -124,7 +123,6 @@ compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
     }
   }
   const int half = R >> 1;
-  const int64_t P = pos0 + j * m + m - 1;   // RoPE position: the block's last token
 #pragma unroll
   for (int r = 0; r < kMaxPairs; ++r) {
     const int p = lane + 32 * r;
@@ -145,14 +143,14 @@ compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
 
   // ---- store ----
   if (FMT == CSA_FMT_F32) {
-    float2* o = reinterpret_cast<float2*>(out) + ent * npairs;
+    float2* o = reinterpret_cast<float2*>(out);
 #pragma unroll
     for (int r = 0; r < kMaxPairs; ++r) {
       const int p = lane + 32 * r;
       if (p < npairs) o[p] = v[r];
     }
   } else if (FMT == CSA_FMT_MIXED592) {
-    pack_mixed_row(v, lane, reinterpret_cast<uint8_t*>(out) + ent * kMixRow);
+    pack_mixed_row(v, lane, reinterpret_cast<uint8_t*>(out));
   } else {  // MXFP4, C in {32, 64}: block of lane's pair = p / 16 = lane / 16
     float amax = (lane < npairs) ? fmaxf(fabsf(v[0].x), fabsf(v[0].y)) : 0.0f;
 #pragma unroll
@@ -162,8 +160,105 @@ compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
       const float inv = pow2i(-sx);
       const uint32_t c0 = e2m1_encode(__fmul_rn(v[0].x, inv));
       const uint32_t c1 = e2m1_encode(__fmul_rn(v[0].y, inv));
-      reinterpret_cast<uint8_t*>(out)[ent * npairs + lane] = (uint8_t)(c0 | (c1 << 4));
-      if ((lane & 15) == 0) out_scales[ent * (C / 32) + (lane >> 4)] = (uint8_t)(sx + 127);
+      reinterpret_cast<uint8_t*>(out)[lane] = (uint8_t)(c0 | (c1 << 4));
+      if ((lane & 15) == 0) out_scales[lane >> 4] = (uint8_t)(sx + 127);
+    }
+  }
+}
+
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
+                const float* __restrict__ s, const float* __restrict__ rcos,
+                const float* __restrict__ rsin, int64_t pos0, int B, int64_t T, int C, int R,
+                int m, int64_t N, void* __restrict__ out, uint8_t* __restrict__ out_scales) {
+  __shared__ float alpha_s[kWarpsPerBlock][128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t ent = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+  if (ent >= (int64_t)B * N) return;
+  const int64_t b = ent / N, j = ent % N;
+  const int64_t tok0 = b * T + j * m;   // first token row of the block
+  const int64_t P = pos0 + j * m + m - 1;   // RoPE position: the block's last token
+  const size_t esz = BF16 ? 2 : 4;
+  void* o = FMT == CSA_FMT_F32 ? (void*)(reinterpret_cast<float*>(out) + ent * C)
+            : FMT == CSA_FMT_MIXED592 ? (void*)(reinterpret_cast<uint8_t*>(out) + ent * kMixRow)
+                                      : (void*)(reinterpret_cast<uint8_t*>(out) + ent * (C / 2));
+  compress_entry<FMT, BF16>(reinterpret_cast<const uint8_t*>(x) + tok0 * C * esz, z + tok0, s, rcos, rsin, P, C, R,
+                            m, o, FMT == CSA_FMT_MXFP4 ? out_scales + ent * (C / 32) : nullptr, alpha_s[warp],
+                            lane);
+}
+
+// Decode-time cache maintenance, one CTA per sequence: the new token at
+// position t (t_pos[b]) enters the ring of the sequence's last m raw tokens
+// (slot t mod m), is packed into the window cache at row t - swa_pos0[b]
+// (when that row is past the buffer, the last W - 1 rows first move to the
+// front and swa_pos0[b] becomes t - W + 1), and when t closes a block
+// ((t + 1) mod m == 0) the block is compressed into entry (t + 1) / m - 1 of
+// the cache and, with its own ring, of the indexer keys.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restrict__ z,
+                     const __nv_bfloat16* __restrict__ kI, const float* __restrict__ zI,
+                     const float* __restrict__ s, const float* __restrict__ sI,
+                     const float* __restrict__ rcos, const float* __restrict__ rsin, int64_t rope_rows,
+                     const int64_t* __restrict__ t_pos, int C, int R, int CI, int m,
+                     __nv_bfloat16* __restrict__ kv_tail, float* __restrict__ z_tail,
+                     __nv_bfloat16* __restrict__ kI_tail, float* __restrict__ zI_tail,
+                     uint8_t* __restrict__ cache, int64_t nmax, uint8_t* __restrict__ kI_codes,
+                     uint8_t* __restrict__ kI_scales, uint8_t* __restrict__ swa, int64_t Ts, int W,
+                     int64_t* __restrict__ swa_pos0) {
+  __shared__ float alpha_s[3][128];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t t = t_pos[b];
+  if (t < 0 || t >= rope_rows) return;   // no RoPE row for it: nothing is stored
+  const int slot = (int)(t % m);
+  // ---- the raw token into its ring slot ----
+  for (int c = tid; c < C; c += blockDim.x) kv_tail[((int64_t)b * m + slot) * C + c] = kv[(int64_t)b * C + c];
+  if (kI)
+    for (int c = tid; c < CI; c += blockDim.x) kI_tail[((int64_t)b * m + slot) * CI + c] = kI[(int64_t)b * CI + c];
+  if (tid == 0) {
+    z_tail[(int64_t)b * m + slot] = z[b];
+    if (kI) zI_tail[(int64_t)b * m + slot] = zI[b];
+  }
+  // ---- window: slide when the row is past the buffer ----
+  if (W > 0) {
+    const int64_t old0 = swa_pos0[b];
+    const bool slide = t - old0 >= Ts;
+    __syncthreads();   // every thread has read swa_pos0[b]
+    if (slide) {
+      // rows of tokens t - W + 1 .. t - 1 move to rows 0 .. W - 2; source rows
+      // are >= Ts - W + 1 >= W + 1 (Ts >= 2 W): no overlap.  Rows past the
+      // buffer (appends out of order) are not read.
+      const int64_t keep0 = t - W + 1, src0 = keep0 - old0;
+      const int per = kMixRow / 16;
+      const uint4* src = reinterpret_cast<const uint4*>(swa + (int64_t)b * Ts * kMixRow);
+      uint4* dst = reinterpret_cast<uint4*>(swa + (int64_t)b * Ts * kMixRow);
+      for (int i = tid; i < (W - 1) * per; i += blockDim.x) {
+        const int64_t sr = src0 + i / per;
+        if (sr >= 0 && sr < Ts) dst[i] = src[sr * per + i % per];
+      }
+      __syncthreads();
+      if (tid == 0) swa_pos0[b] = keep0;
+    }
+    const int64_t row = slide ? (int64_t)W - 1 : t - old0;
+    if (warp == 0 && row >= 0 && row < Ts) {   // the token itself: m = 1, no channel scale, RoPE at t
+      const float zz = 0.0f;
+      compress_entry<CSA_FMT_MIXED592, true>(kv + (int64_t)b * C, &zz, nullptr, rcos, rsin, t, C, R, 1,
+                                             swa + ((int64_t)b * Ts + row) * kMixRow, nullptr, alpha_s[0], lane);
+    }
+  }
+  __syncthreads();   // the ring slots are written
+  if ((t + 1) % m == 0) {
+    const int64_t j = (t + 1) / m - 1;
+    if (j < nmax) {
+      if (warp == 1)
+        compress_entry<CSA_FMT_MIXED592, true>(kv_tail + (int64_t)b * m * C, z_tail + (int64_t)b * m, s, rcos,
+                                               rsin, t, C, R, m, cache + ((int64_t)b * nmax + j) * kMixRow,
+                                               nullptr, alpha_s[1], lane);
+      if (warp == 2 && kI)
+        compress_entry<CSA_FMT_MXFP4, true>(kI_tail + (int64_t)b * m * CI, zI_tail + (int64_t)b * m, sI, rcos,
+                                            rsin, t, CI, 0, m, kI_codes + ((int64_t)b * nmax + j) * (CI / 2),
+                                            kI_scales + ((int64_t)b * nmax + j) * (CI / 32), alpha_s[2], lane);
     }
   }
 }
@@ -199,6 +294,21 @@ cudaError_t launch_compress(const void* x, bool x_bf16, const float* z, const fl
     if (x_bf16) CSA_CK(CSA_FMT_MXFP4, true); else CSA_CK(CSA_FMT_MXFP4, false);
   }
 #undef CSA_CK
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_append(const void* kv, const float* z, const void* kI, const float* zI, const float* s,
+                                 const float* sI, const float* rcos, const float* rsin, int64_t rope_rows,
+                                 const int64_t* t_pos, int B,
+                                 int C, int R, int CI, int m, void* kv_tail, float* z_tail, void* kI_tail,
+                                 float* zI_tail, uint8_t* cache, int64_t nmax, uint8_t* kI_codes,
+                                 uint8_t* kI_scales, uint8_t* swa, int64_t Ts, int W, int64_t* swa_pos0,
+                                 cudaStream_t st) {
+  if (B == 0) return cudaSuccess;
+  decode_append_kernel<<<(unsigned)B, kWarpsPerBlock * 32, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(kv), z, reinterpret_cast<const __nv_bfloat16*>(kI), zI, s, sI, rcos,
+      rsin, rope_rows, t_pos, C, R, CI, m, reinterpret_cast<__nv_bfloat16*>(kv_tail), z_tail,
+      reinterpret_cast<__nv_bfloat16*>(kI_tail), zI_tail, cache, nmax, kI_codes, kI_scales, swa, Ts, W, swa_pos0);
   return cudaGetLastError();
 }
 

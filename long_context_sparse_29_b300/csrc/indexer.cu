@@ -317,7 +317,8 @@ scores_f32_kernel(const float* __restrict__ qI, const float* __restrict__ w,
 // (per-warp segments: count, prefix, write); then sorted by (score desc, index
 // asc) as 64-bit composite keys: warps sort runs of 32 with shuffles, runs are
 // merged pairwise by binary search.  Rows longer than kTkChunk go in two
-// stages: every chunk of kTkChunk candidates keeps its own top-k (the global
+// stages: every chunk of C candidates (C ~ sqrt(N k), at least kTkChunk, so
+// both stages get similar work) keeps its own top-k (the global
 // top-k lies in their union: the order is total), then one CTA per row
 // selects among the chunk winners.
 // ---------------------------------------------------------------------------
@@ -551,13 +552,13 @@ topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos,
 // visible candidates [c C, (c + 1) C) in index order, at cand[(row chunks + c) k].
 __global__ void __launch_bounds__(kTopkThreads)
 topk_stage1_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m, int k,
-                   int chunks, unsigned long long* __restrict__ cand) {
+                   int chunks, int64_t C, unsigned long long* __restrict__ cand) {
   __shared__ TkShared sh;
   const int64_t row = blockIdx.x;
   const int c = blockIdx.y;
   const int64_t nv = visible_entries(q_pos[row], m, N);
-  const int64_t c0 = (int64_t)c * kTkChunk;
-  const int64_t n = nv - c0 < 0 ? 0 : (nv - c0 < kTkChunk ? nv - c0 : kTkChunk);
+  const int64_t c0 = (int64_t)c * C;
+  const int64_t n = nv - c0 < 0 ? 0 : (nv - c0 < C ? nv - c0 : C);
   const int kk = (int)((int64_t)k < n ? (int64_t)k : n);
   unsigned long long* dst = cand + ((int64_t)row * chunks + c) * k;
   if (kk > 0) {
@@ -594,15 +595,25 @@ int topk_pad(int k) {
   return p;
 }
 
-int topk_chunks(int64_t N) { return N > kTkChunk ? (int)((N + kTkChunk - 1) / kTkChunk) : 0; }
+// candidates per stage-1 chunk: a power of two near sqrt(N k), at least kTkChunk
+int64_t topk_chunk_size(int64_t N, int k) {
+  int64_t c = kTkChunk;
+  while (c * c < N * (int64_t)k && c < N) c <<= 1;
+  return c;
+}
+int topk_chunks(int64_t N, int k) {
+  if (N <= kTkChunk) return 0;
+  const int64_t c = topk_chunk_size(N, k);
+  return (int)((N + c - 1) / c);
+}
 
 size_t topk_cand_bytes(int B, int64_t Tq, int64_t N, int k) {
-  const int ch = topk_chunks(N);
+  const int ch = topk_chunks(N, k);
   return ch ? (size_t)B * (size_t)Tq * (size_t)ch * (size_t)k * 8 : 0;
 }
 
 bool topk_two_stage(int B, int64_t Tq, int64_t N) {
-  return topk_chunks(N) > 0 && (int64_t)B * Tq < 4 * 148;
+  return N > kTkChunk && (int64_t)B * Tq < 4 * 148;
 }
 
 cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
@@ -647,10 +658,10 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
   }
   const int64_t rows = (int64_t)B * Tq;
   if (cand_ws && topk_two_stage(B, Tq, N)) {
-    const int ch = topk_chunks(N);
+    const int ch = topk_chunks(N, k);
     unsigned long long* cand = reinterpret_cast<unsigned long long*>(cand_ws);
     topk_stage1_kernel<<<dim3((unsigned)rows, (unsigned)ch), kTopkThreads, 0, st>>>(scores_ws, q_pos, N, m, k, ch,
-                                                                                  cand);
+                                                                                  topk_chunk_size(N, k), cand);
     topk_stage2_kernel<<<(unsigned)rows, kTopkThreads, smem, st>>>(q_pos, N, m, k, ch, P, cand, idx_out,
                                                                    score_out);
   } else {

@@ -40,6 +40,13 @@ cudaError_t launch_compress(const void* x, bool x_bf16, const float* z, const fl
                             int C, int R, int m, int fmt, void* out, uint8_t* out_scales,
                             cudaStream_t st);
 cudaError_t launch_pack_mixed(const float* v, int64_t n, uint8_t* out, cudaStream_t st);
+cudaError_t launch_decode_append(const void* kv, const float* z, const void* kI, const float* zI, const float* s,
+                                 const float* sI, const float* rcos, const float* rsin, int64_t rope_rows,
+                                 const int64_t* t_pos, int B,
+                                 int C, int R, int CI, int m, void* kv_tail, float* z_tail, void* kI_tail,
+                                 float* zI_tail, uint8_t* cache, int64_t nmax, uint8_t* kI_codes,
+                                 uint8_t* kI_scales, uint8_t* swa, int64_t Ts, int W, int64_t* swa_pos0,
+                                 cudaStream_t st);
 cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
                                 const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
                                 int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
