@@ -349,42 +349,59 @@ def _f_dev(a, dev):
 
 
 def decode_layer(csa, cfg, dev, rope):
-    """Resident caches of one decode layer (every sequence's full context run
-    through the library's compression), and the step's inputs on the host."""
+    """Resident decode state of one layer (every sequence's full context run
+    through the library's compression into a LayerCache: entries, indexer
+    keys, the last W tokens in a 2W-row window buffer, the ring of the last m
+    raw tokens) and the step's inputs on the host: the query of position T-1
+    and that token's activations, which the step appends again (closing block
+    N-1, so every step does the append's full work and leaves the same bytes)."""
     import torch
     B, T, W, N, m = cfg.B, cfg.T, cfg.W, cfg.N, cfg.m
     sc = wl.gen_channel_scales(cfg)
-    s_d = _f_dev(sc["s"], dev)
-    cache = torch.empty((B, N, 592), dtype=torch.uint8, device=dev)
-    swa = torch.empty((B, W, 592), dtype=torch.uint8, device=dev)
-    kc = torch.empty((B, N, 32), dtype=torch.uint8, device=dev) if cfg.k else None
-    ks = torch.empty((B, N, 2), dtype=torch.uint8, device=dev) if cfg.k else None
+    CI = cfg.dI if cfg.k else 0
+    lc = csa.LayerCache(B, N, m, W, 2 * W, CI=CI, C=cfg.D, pos0=T - W, device=dev)
+    new = {"kv": [], "z": [], "kI": [], "zI": []}
     for b in range(B):
         toks = wl.gen_tokens(cfg, b, parts=("kv", "z", "kI", "zI") if cfg.k else ("kv", "z"))
         kv, z = _bf16_dev(toks["kv"], dev)[None], _f_dev(toks["z"], dev)[None]
-        csa.compress_kv(kv, z, s_d, m, csa.FMT_MIXED592, cfg.R, rope, out=cache[b:b + 1])
+        csa.compress_kv(kv, z, _f_dev(sc["s"], dev), m, csa.FMT_MIXED592, cfg.R, rope, out=lc.cache[b:b + 1])
         csa.compress_kv(kv[:, T - W:], z[:, T - W:], None, 1, csa.FMT_MIXED592, cfg.R, rope, pos0=T - W,
-                        out=swa[b:b + 1])
+                        out=lc.swa[b:b + 1, :W])
+        lc.kv_tail[b] = kv[0, T - m:]
+        lc.z_tail[b] = z[0, T - m:]
         if cfg.k:
-            csa.compress_kv(_bf16_dev(toks["kI"], dev)[None], _f_dev(toks["zI"], dev)[None],
-                            _f_dev(sc["sI"], dev), m, csa.FMT_MXFP4, 0, out=kc[b:b + 1], out_scales=ks[b:b + 1])
+            kI, zI = _bf16_dev(toks["kI"], dev)[None], _f_dev(toks["zI"], dev)[None]
+            csa.compress_kv(kI, zI, _f_dev(sc["sI"], dev), m, csa.FMT_MXFP4, 0, out=lc.kI_codes[b:b + 1],
+                            out_scales=lc.kI_scales[b:b + 1])
+            lc.kI_tail[b] = kI[0, T - m:]
+            lc.zI_tail[b] = zI[0, T - m:]
+        for kk in new:
+            if kk in toks:
+                new[kk].append(toks[kk][T - 1])
         del kv, z, toks
     qry = [wl.gen_queries(cfg, b) for b in range(B)]
     host = {"q": np.stack([x["q"] for x in qry]), "q_pos": np.full((B, 1), T - 1, np.int64),
-            "swa_pos0": np.full(B, T - W, np.int64)}
+            "t_pos": np.full(B, T - 1, np.int64), "s": sc["s"],
+            "kv_new": np.stack(new["kv"]), "z_new": np.array(new["z"], np.float32)}
     if cfg.k:
         host["qI"] = np.stack([x["qI"] for x in qry])
         host["w"] = np.stack([x["w"] for x in qry])
-    return {"cache": cache, "swa": swa, "kc": kc, "ks": ks}, host
+        host["kI_new"] = np.stack(new["kI"])
+        host["zI_new"] = np.array(new["zI"], np.float32)
+        host["sI"] = sc["sI"]
+    return lc, host
 
 
 def decode_bytes(cfg) -> float:
     """Algorithmic HBM bytes of one decode step: every resident byte the step
     must read once (indexer keys 34 B per entry; the k + W gathered or all
-    visible rows, 592 B each) plus the query and the output (64 KiB each)."""
+    visible rows, 592 B each) plus the query and the output (64 KiB each),
+    and the append: the new token in, the m ring rows read, one window row and
+    one entry (+ its 34-byte key) written."""
     rows = (cfg.k if cfg.k else cfg.N) + cfg.W
     per_q = rows * 592 + 2 * cfg.H * cfg.D * 2 + (cfg.N * 34 if cfg.k else 0)
-    return float(cfg.B * per_q)
+    append = (cfg.m + 1) * (2 * cfg.D + 4) + 2 * 592 + ((cfg.m + 1) * (2 * cfg.dI + 4) + 34 if cfg.k else 0)
+    return float(cfg.B * (per_q + append))
 
 
 def run_config(args, name):
@@ -404,25 +421,29 @@ def run_config(args, name):
         rope = csa.rope_table(layers[0].T + 1, 64)
         built = []
         for cfg in layers:
-            res, host = decode_layer(csa, cfg, dev, rope)
-            d = {kk: (_bf16_dev(v, dev) if kk in ("q", "qI") else _f_dev(v, dev)) for kk, v in host.items()}
+            lc, host = decode_layer(csa, cfg, dev, rope)
+            d = {kk: (_bf16_dev(v, dev) if kk in ("q", "qI", "kv_new", "kI_new") else _f_dev(v, dev))
+                 for kk, v in host.items()}
             out = torch.empty((cfg.B, 1, cfg.H, cfg.D), dtype=torch.bfloat16, device=dev)
             idx = torch.empty((cfg.B, 1, cfg.k), dtype=torch.int32, device=dev) if cfg.k else None
-            built.append((cfg, res, d, out, idx, csa.Workspace(dev), csa.Workspace(dev)))
+            built.append((cfg, lc, d, out, idx, csa.Workspace(dev), csa.Workspace(dev)))
         torch.cuda.synchronize()
 
         def step():
-            for cfg, res, d, out, idx, ws1, ws2 in built:
+            for cfg, lc, d, out, idx, ws1, ws2 in built:
                 scale = 1.0 / math.sqrt(cfg.D)
+                csa.decode_append(lc, d["kv_new"], d["z_new"], d["t_pos"], rope, d.get("kI_new"), d.get("zI_new"),
+                                  d["s"], d.get("sI"), cfg.R)
                 if cfg.k:
-                    csa.indexer_topk(d["qI"], d["w"], res["kc"], res["ks"], d["q_pos"], cfg.N, cfg.m, cfg.k,
+                    csa.indexer_topk(d["qI"], d["w"], lc.kI_codes, lc.kI_scales, d["q_pos"], cfg.N, cfg.m, cfg.k,
                                      scores=False, idx_out=idx, ws=ws1)
-                    csa.sparse_mqa(d["q"], d["q_pos"], res["cache"], cfg.m, idx, res["swa"], d["swa_pos0"], cfg.W,
+                    csa.sparse_mqa(d["q"], d["q_pos"], lc.cache, cfg.m, idx, lc.swa, lc.swa_pos0, cfg.W,
                                    scale, rope, cfg.R, out=out, ws=ws2)
                 else:
-                    csa.hca_dense_attn(d["q"], d["q_pos"], res["cache"], cfg.m, res["swa"], d["swa_pos0"], cfg.W,
+                    csa.hca_dense_attn(d["q"], d["q_pos"], lc.cache, cfg.m, lc.swa, lc.swa_pos0, cfg.W,
                                        scale, rope, cfg.R, out=out, ws=ws2)
 
+        graph = True
         units, unit = float(layers[0].B), "queries/s"
         metric = {"c3_csa_decode_128k": "CSA decode queries/s (32 sequences at 128K context, top-k 1024)",
                   "c4_hca_decode_1m": "HCA decode queries/s (16 sequences at 1M context, m'=128)",
@@ -430,6 +451,8 @@ def run_config(args, name):
         alg = sum(decode_bytes(c) for c in layers)
         roof = {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s", "algorithmic_bytes_per_step": alg}
         l2 = "caches resident; each step reads them once (larger than L2 except the HCA-only step)"
+        step_desc = "decode_append + indexer_topk + sparse_mqa (CSA) / decode_append + hca_dense_attn (HCA), " \
+                    "one CUDA graph per step"
     elif name == "c4_hca_prefill_64k":
         cfg = wl.CONFIGS[name]
         T, W, N, m = cfg.T, cfg.W, cfg.N, cfg.m
@@ -461,17 +484,31 @@ def run_config(args, name):
         roof = {"bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "algorithmic_flops_per_step": alg}
         l2 = "inputs larger than L2 (q and out 4 GiB each)"
         layers = [cfg]
+        graph = False
+        step_desc = "compress (entries and window rows) + hca_dense_attn"
     else:
         raise SystemExit(f"unknown config {name}")
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    run = step
+    if graph:
+        # the step's launches captured once (workspaces already sized by the
+        # warm-up steps) and replayed: no host work between kernels
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        run = g.replay
     with ClockSampler(0) as clk:
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for _ in range(args.steps):
-            step()
+            run()
         t1.record(stream)
         torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / args.steps
@@ -487,7 +524,7 @@ def run_config(args, name):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": name, "B": cfg0.B, "T": cfg0.T, "N": cfg0.N, "m": cfg0.m, "k": cfg0.k,
-                       "W": cfg0.W, "H": cfg0.H, "D": cfg0.D, "l2": l2},
+                       "W": cfg0.W, "H": cfg0.H, "D": cfg0.D, "l2": l2, "step": step_desc},
             "roofline": roof, "clocks": clk.summary()}
 
 

@@ -184,8 +184,9 @@ int csa_compress_kv(const void *x, int x_dtype, const float *z, const float *s,
  * csa_compress_kv builds from tokens 0 .. t.  A sequence whose t has no RoPE
  * row (t < 0 or t >= rope_rows) is left unchanged; rows outside the window
  * buffer are never written.
- * Errors: INVALID_ARG (NULL pointers, m outside 1..128, Ts < 2 W);
- * UNSUPPORTED (C != 512, R != 64, CI not 32 or 64 with kI given).
+ * Errors: INVALID_ARG (NULL pointers, m outside 1..128, Ts < 2 W, kv / kI /
+ * kv_tail / kI_tail not 16-byte aligned); UNSUPPORTED (C != 512, R != 64, CI
+ * not 32 or 64 with kI given).
  */
 int csa_decode_append(const void *kv, const float *z, const void *kI, const float *zI, const float *s,
                       const float *sI, const float *rope_cos, const float *rope_sin, int64_t rope_rows,

@@ -246,6 +246,9 @@ int csa_decode_append(const void* kv, const float* z, const void* kI, const floa
   if (!kv || !z || !t_pos || !kv_tail || !z_tail || !rope_cos || !rope_sin || (nmax > 0 && !cache) ||
       (W > 0 && (!swa || !swa_pos0)) || (kI && (!zI || !kI_tail || !zI_tail || (nmax > 0 && (!kI_codes || !kI_scales)))))
     return fail(CSA_ERR_INVALID_ARG, "%s: NULL pointer", nm);
+  if (((reinterpret_cast<uintptr_t>(kv) | reinterpret_cast<uintptr_t>(kv_tail) | reinterpret_cast<uintptr_t>(kI) |
+        reinterpret_cast<uintptr_t>(kI_tail)) & 15))
+    return fail(CSA_ERR_INVALID_ARG, "%s: kv, kI and their rings must be 16-byte aligned", nm);
   return cuda_result(csa::launch_decode_append(kv, z, kI, zI, s, sI, rope_cos, rope_sin, rope_rows, t_pos, B, C, R,
                                                kI ? CI : 0, m,
                                                kv_tail, z_tail, kI_tail, zI_tail, cache, nmax, kI_codes, kI_scales,
@@ -287,7 +290,7 @@ int csa_indexer_topk(const void* qI, int qI_dtype, const float* w, const void* k
   }
   return cuda_result(csa::launch_indexer_topk(qI, fp4, w, kI, kI_scales, q_pos, B, Tq, HI, dI, N,
                                               m, k, idx_out, score_out, scores, tc_ws, cand_ws, ws,
-                                              as_stream(stream)),
+                                              !indexer_use_dp4a(), as_stream(stream)),
                      nm);
 }
 

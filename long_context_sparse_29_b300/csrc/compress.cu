@@ -66,19 +66,10 @@ __device__ __forceinline__ void pack_mixed_row(const float2 (&v)[kMaxPairs], int
   }
 }
 
-// One compressed entry by one warp: the m token rows at x (row stride C
-// elements), their logits z[0..m), the channel scale s (or NULL), RoPE of the
-// last R channels at position P, stored in format FMT at out (entry 0 of out)
-// and out_scales.  alpha is m floats of warp-private shared memory.  The same
-// code serves block compression and the decode-time append, so both store the
-// same bytes.
-template <int FMT, bool BF16>
-__device__ __forceinline__ void compress_entry(const void* __restrict__ x, const float* __restrict__ z,
-                                               const float* __restrict__ s, const float* __restrict__ rcos,
-                                               const float* __restrict__ rsin, int64_t P, int C, int R, int m,
-                                               void* __restrict__ out, uint8_t* __restrict__ out_scales,
-                                               float* alpha, int lane) {
-  // ---- weights of the block: a = softmax(z) with the library exponential ----
+// The compression weights of one block, by one warp: alpha[i] = softmax(z)[i]
+// for i < m with the library exponential (max, exponentials, their sum in
+// token order, one division each).  alpha is m floats of shared memory.
+__device__ __forceinline__ void entry_weights(const float* __restrict__ z, int m, float* alpha, int lane) {
   float mu = -INFINITY;
   for (int i = lane; i < m; i += 32) mu = fmaxf(mu, z[i]);
 #pragma unroll
@@ -94,35 +85,28 @@ __device__ __forceinline__ void compress_entry(const void* __restrict__ x, const
   __syncwarp();
   for (int i = lane; i < m; i += 32) alpha[i] = __fdiv_rn(alpha[i], S);
   __syncwarp();
+}
 
-  // ---- weighted sum over the block's tokens, channel pairs per lane ----
-  const int npairs = C >> 1;
-  float2 v[kMaxPairs];
-#pragma unroll
-  for (int r = 0; r < kMaxPairs; ++r) v[r] = make_float2(0.0f, 0.0f);
-  for (int i = 0; i < m; ++i) {
-    const float a = alpha[i];
-    const int64_t row = (int64_t)i * C;
-#pragma unroll
-    for (int r = 0; r < kMaxPairs; ++r) {
-      const int p = lane + 32 * r;
-      if (p < npairs) {
-        float x0, x1;
-        if (BF16) {
-          const uint32_t w = reinterpret_cast<const uint32_t*>(x)[(row >> 1) + p];
-          x0 = __uint_as_float(w << 16);
-          x1 = __uint_as_float(w & 0xffff0000u);
-        } else {
-          const float2 w = reinterpret_cast<const float2*>(x)[(row >> 1) + p];
-          x0 = w.x;
-          x1 = w.y;
-        }
-        v[r].x = __fmaf_rn(a, x0, v[r].x);
-        v[r].y = __fmaf_rn(a, x1, v[r].y);
-      }
-    }
+// Channels 2p, 2p+1 of x (m rows, row stride C elements) under the weights:
+// fma over the tokens in order, the only order the stored bytes allow.
+template <bool BF16>
+__device__ __forceinline__ float2 load_pair(const void* __restrict__ x, int64_t row, int p) {
+  if (BF16) {
+    const uint32_t w = reinterpret_cast<const uint32_t*>(x)[(row >> 1) + p];
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   }
-  const int half = R >> 1;
+  return reinterpret_cast<const float2*>(x)[(row >> 1) + p];
+}
+
+// The weighted sum, the channel scale s (or NULL), RoPE of the last R
+// channels at position P and the store in format FMT at out / out_scales, by
+// one warp whose lane holds pairs p = lane + 32 r in v.
+template <int FMT>
+__device__ __forceinline__ void entry_finish(float2 (&v)[kMaxPairs], const float* __restrict__ s,
+                                             const float* __restrict__ rcos, const float* __restrict__ rsin,
+                                             int64_t P, int C, int R, void* __restrict__ out,
+                                             uint8_t* __restrict__ out_scales, int lane) {
+  const int npairs = C >> 1, half = R >> 1;
 #pragma unroll
   for (int r = 0; r < kMaxPairs; ++r) {
     const int p = lane + 32 * r;
@@ -140,8 +124,6 @@ __device__ __forceinline__ void compress_entry(const void* __restrict__ x, const
       }
     }
   }
-
-  // ---- store ----
   if (FMT == CSA_FMT_F32) {
     float2* o = reinterpret_cast<float2*>(out);
 #pragma unroll
@@ -164,6 +146,36 @@ __device__ __forceinline__ void compress_entry(const void* __restrict__ x, const
       if ((lane & 15) == 0) out_scales[lane >> 4] = (uint8_t)(sx + 127);
     }
   }
+}
+
+// One compressed entry by one warp: the m token rows at x (row stride C
+// elements), their logits z[0..m), the channel scale s (or NULL), RoPE of the
+// last R channels at position P, stored in format FMT at out (entry 0 of out)
+// and out_scales.  alpha is m floats of warp-private shared memory.
+template <int FMT, bool BF16>
+__device__ __forceinline__ void compress_entry(const void* __restrict__ x, const float* __restrict__ z,
+                                               const float* __restrict__ s, const float* __restrict__ rcos,
+                                               const float* __restrict__ rsin, int64_t P, int C, int R, int m,
+                                               void* __restrict__ out, uint8_t* __restrict__ out_scales,
+                                               float* alpha, int lane) {
+  entry_weights(z, m, alpha, lane);
+  const int npairs = C >> 1;
+  float2 v[kMaxPairs];
+#pragma unroll
+  for (int r = 0; r < kMaxPairs; ++r) v[r] = make_float2(0.0f, 0.0f);
+  for (int i = 0; i < m; ++i) {
+    const float a = alpha[i];
+#pragma unroll
+    for (int r = 0; r < kMaxPairs; ++r) {
+      const int p = lane + 32 * r;
+      if (p < npairs) {
+        const float2 w = load_pair<BF16>(x, (int64_t)i * C, p);
+        v[r].x = __fmaf_rn(a, w.x, v[r].x);
+        v[r].y = __fmaf_rn(a, w.y, v[r].y);
+      }
+    }
+  }
+  entry_finish<FMT>(v, s, rcos, rsin, P, C, R, out, out_scales, lane);
 }
 
 template <int FMT, bool BF16>
@@ -194,7 +206,9 @@ compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
 // (when that row is past the buffer, the last W - 1 rows first move to the
 // front and swa_pos0[b] becomes t - W + 1), and when t closes a block
 // ((t + 1) mod m == 0) the block is compressed into entry (t + 1) / m - 1 of
-// the cache and, with its own ring, of the indexer keys.
+// the cache and, with its own ring, of the indexer keys: one thread per
+// channel pair sums the m ring rows (the same fma order as compress_entry, so
+// the same bytes), then one warp scales, rotates and packs.
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restrict__ z,
                      const __nv_bfloat16* __restrict__ kI, const float* __restrict__ zI,
@@ -207,11 +221,34 @@ decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restri
                      uint8_t* __restrict__ kI_scales, uint8_t* __restrict__ swa, int64_t Ts, int W,
                      int64_t* __restrict__ swa_pos0) {
   __shared__ float alpha_s[3][128];
+  __shared__ float z_s[2][128];              // the closing block's logits (cache, key)
+  __shared__ float2 acc_s[(512 + 64) / 2];   // the closing block's pair sums: C/2 of the cache, CI/2 of the key
+  extern __shared__ __align__(16) uint8_t ring_s[];   // closing block: m rows of C, then m rows of CI (bf16)
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t t = t_pos[b];
   if (t < 0 || t >= rope_rows) return;   // no RoPE row for it: nothing is stored
   const int slot = (int)(t % m);
+  const bool closes = (t + 1) % m == 0 && (t + 1) / m - 1 < nmax;
+  if (closes) {
+    // stage the block's rows: slots 0 .. m-2 from the ring, slot m-1 is this
+    // token; 16-byte asynchronous copies, all in flight together
+    const int rk = C * 2 / 16, ri = CI * 2 / 16;   // 16-byte pieces per row
+    for (int q = tid; q < m * (rk + ri); q += blockDim.x) {
+      const bool key = q >= m * rk;
+      const int qq = key ? q - m * rk : q, per = key ? ri : rk;
+      const int i = qq / per, c = qq - i * per;
+      const uint8_t* src = key ? (i == m - 1 ? reinterpret_cast<const uint8_t*>(kI + (int64_t)b * CI)
+                                             : reinterpret_cast<const uint8_t*>(kI_tail + ((int64_t)b * m + i) * CI))
+                               : (i == m - 1 ? reinterpret_cast<const uint8_t*>(kv + (int64_t)b * C)
+                                             : reinterpret_cast<const uint8_t*>(kv_tail + ((int64_t)b * m + i) * C));
+      uint8_t* dst = ring_s + (key ? (size_t)m * C * 2 : 0) + ((size_t)i * per + c) * 16;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                   "l"(src + c * 16)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  }
   // ---- the raw token into its ring slot ----
   for (int c = tid; c < C; c += blockDim.x) kv_tail[((int64_t)b * m + slot) * C + c] = kv[(int64_t)b * C + c];
   if (kI)
@@ -247,18 +284,54 @@ decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restri
                                              swa + ((int64_t)b * Ts + row) * kMixRow, nullptr, alpha_s[0], lane);
     }
   }
-  __syncthreads();   // the ring slots are written
-  if ((t + 1) % m == 0) {
+  if (closes) {   // CTA-wide, the same fma order per channel as compress_entry
     const int64_t j = (t + 1) / m - 1;
-    if (j < nmax) {
-      if (warp == 1)
-        compress_entry<CSA_FMT_MIXED592, true>(kv_tail + (int64_t)b * m * C, z_tail + (int64_t)b * m, s, rcos,
-                                               rsin, t, C, R, m, cache + ((int64_t)b * nmax + j) * kMixRow,
-                                               nullptr, alpha_s[1], lane);
-      if (warp == 2 && kI)
-        compress_entry<CSA_FMT_MXFP4, true>(kI_tail + (int64_t)b * m * CI, zI_tail + (int64_t)b * m, sI, rcos,
-                                            rsin, t, CI, 0, m, kI_codes + ((int64_t)b * nmax + j) * (CI / 2),
-                                            kI_scales + ((int64_t)b * nmax + j) * (CI / 32), alpha_s[2], lane);
+    // the logits: slots 0 .. m-2 from the ring, slot m-1 this token's
+    if (warp == 1) {
+      for (int i = lane; i < m; i += 32) z_s[0][i] = i == m - 1 ? z[b] : z_tail[(int64_t)b * m + i];
+      __syncwarp();
+      entry_weights(z_s[0], m, alpha_s[1], lane);
+    }
+    if (warp == 2 && kI) {
+      for (int i = lane; i < m; i += 32) z_s[1][i] = i == m - 1 ? zI[b] : zI_tail[(int64_t)b * m + i];
+      __syncwarp();
+      entry_weights(z_s[1], m, alpha_s[2], lane);
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    __syncthreads();
+    const void* xk = ring_s;
+    const void* xi = ring_s + (size_t)m * C * 2;
+    for (int p = tid; p < (C >> 1) + (CI >> 1); p += blockDim.x) {
+      const bool key = p >= (C >> 1);
+      const int q = key ? p - (C >> 1) : p;
+      const float* a = alpha_s[key ? 2 : 1];
+      const void* x = key ? xi : xk;
+      const int cc = key ? CI : C;
+      float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll 8
+      for (int i = 0; i < m; ++i) {
+        const float2 w = load_pair<true>(x, (int64_t)i * cc, q);
+        acc.x = __fmaf_rn(a[i], w.x, acc.x);
+        acc.y = __fmaf_rn(a[i], w.y, acc.y);
+      }
+      acc_s[p] = acc;
+    }
+    __syncthreads();
+    if (warp == 1 || (warp == 2 && kI)) {
+      const bool key = warp == 2;
+      const int off = key ? (C >> 1) : 0, np = key ? (CI >> 1) : (C >> 1);
+      float2 v[kMaxPairs];
+#pragma unroll
+      for (int r = 0; r < kMaxPairs; ++r) {
+        const int p = lane + 32 * r;
+        v[r] = p < np ? acc_s[off + p] : make_float2(0.0f, 0.0f);
+      }
+      if (key)
+        entry_finish<CSA_FMT_MXFP4>(v, sI, rcos, rsin, t, CI, 0, kI_codes + ((int64_t)b * nmax + j) * (CI / 2),
+                                    kI_scales + ((int64_t)b * nmax + j) * (CI / 32), lane);
+      else
+        entry_finish<CSA_FMT_MIXED592>(v, s, rcos, rsin, t, C, R, cache + ((int64_t)b * nmax + j) * kMixRow,
+                                       nullptr, lane);
     }
   }
 }
@@ -305,7 +378,13 @@ cudaError_t launch_decode_append(const void* kv, const float* z, const void* kI,
                                  uint8_t* kI_scales, uint8_t* swa, int64_t Ts, int W, int64_t* swa_pos0,
                                  cudaStream_t st) {
   if (B == 0) return cudaSuccess;
-  decode_append_kernel<<<(unsigned)B, kWarpsPerBlock * 32, 0, st>>>(
+  const size_t ring = (size_t)m * (C + CI) * 2;   // staged rows of a closing block
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(decode_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * (512 + 64) * 2);
+    attr_set = true;
+  }
+  decode_append_kernel<<<(unsigned)B, kWarpsPerBlock * 32, ring, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(kv), z, reinterpret_cast<const __nv_bfloat16*>(kI), zI, s, sI, rcos,
       rsin, rope_rows, t_pos, C, R, CI, m, reinterpret_cast<__nv_bfloat16*>(kv_tail), z_tail,
       reinterpret_cast<__nv_bfloat16*>(kI_tail), zI_tail, cache, nmax, kI_codes, kI_scales, swa, Ts, W, swa_pos0);

@@ -151,14 +151,18 @@ scores_fp4_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict_
 
 // ---------------------------------------------------------------------------
 // FP4 scores for few query rows against long entry lists (decode): grid
-// (entry chunks of kDecChunk, rows); the row's query is quantised by the CTA
-// (while its first entries are in flight); each thread scores kDecKPT
-// entries per round, their loads issued together.  Codes become doubled
-// values by a byte-permute table; the even and odd elements of each 8-element
-// group are dotted separately (an integer sum: same result).
+// (entry chunks, rows), the chunk length chosen by the host so that the grid
+// fills the resident CTA slots of the GPU about once; the row's query is
+// quantised by all threads of the CTA (four elements each) while the first
+// entries are in flight; each thread scores kDecKPT entries per round, their
+// loads issued together.  Codes become doubled values by a byte-permute
+// table; the even and odd elements of each 8-element group are dotted
+// separately (an integer sum: same result).  The two block dots of a head
+// meet as one integer when their scales are within 2^17 of each other, so the
+// head's dot is one conversion (the single rounding) and one exact scaling.
 // ---------------------------------------------------------------------------
 constexpr int kDecKPT = 4;
-constexpr int kDecChunk = kScoreThreads * kDecKPT * 2;
+constexpr int kDecRound = kScoreThreads * kDecKPT;   // entries per CTA round
 
 // four E2M1 codes (one per byte, low nibble) -> their doubled values as int8x4
 __device__ __forceinline__ uint32_t e2m1x2_int8x4(uint32_t b4) {
@@ -169,23 +173,36 @@ __device__ __forceinline__ uint32_t e2m1x2_int8x4(uint32_t b4) {
   return __vsub4(mag ^ neg, neg);
 }
 
-__global__ void __launch_bounds__(kScoreThreads)
+// RN(P0 2^e0 + P1 2^e1) for integer block dots |P| < 2^13: one integer when
+// |e1 - e0| <= 17 (|sum| < 2^31) and the result stays normal, else the
+// two-product form.  Both give the correctly rounded sum.
+__device__ __forceinline__ float combine_blocks_fast(int P0, int e0, int P1, int dl) {
+  const bool up = dl >= 0;
+  const int sh = min(up ? dl : -dl, 17);
+  const int S = up ? P0 + P1 * (1 << sh) : P1 + P0 * (1 << sh);
+  const int base = up ? e0 : e0 + dl;
+  if ((up ? dl : -dl) <= 17 && base >= -126 && base <= 96) return __fmul_rn((float)S, pow2i(base));
+  return combine_blocks(P0, e0, P1, e0 + dl);
+}
+
+__global__ void __launch_bounds__(kScoreThreads, 3)
 scores_fp4_decode_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
                          const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
                          const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
-                         float* __restrict__ scores) {
+                         int64_t chunk, float* __restrict__ scores) {
   // doubled query values: head h, block b, group i (8 elements): word [h][b][0][i] even
   // elements, [h][b][1][i] odd elements of the group
   __shared__ __align__(16) int32_t qv_s[kMaxHI][2][2][4];
-  __shared__ int8_t qe_s[kMaxHI][2];
-  __shared__ float w_s[kMaxHI];
+  // per head: {qe0 - 2, qe1 - qe0, w bits, 0}
+  __shared__ __align__(16) int4 hx_s[kMaxHI];
+  __shared__ int qe_s[kMaxHI][2];
   const int64_t row = blockIdx.y;
   const int64_t b = row / Tq;
   const int tid = threadIdx.x;
   const int64_t nv = visible_entries(q_pos[row], m, N);
-  const int64_t c0 = (int64_t)blockIdx.x * kDecChunk;
+  const int64_t c0 = (int64_t)blockIdx.x * chunk;
   if (c0 >= nv) return;
-  const int64_t c1 = c0 + kDecChunk < nv ? c0 + kDecChunk : nv;
+  const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
   // the first round's entries, in flight during the query quantisation
   uint4 cw[kDecKPT][2];
   uint32_t se[kDecKPT];
@@ -197,34 +214,36 @@ scores_fp4_decode_kernel(const __nv_bfloat16* __restrict__ qI, const float* __re
     cw[i][1] = __ldg(reinterpret_cast<const uint4*>(kc + (b * N + jj) * 32) + 1);
     se[i] = __ldg(reinterpret_cast<const uint16_t*>(ks + (b * N + jj) * 2));
   }
-  if (tid < HI * 2) {   // quantise block (h, blk) of the query
-    const int h = tid >> 1, blk = tid & 1;
-    const __nv_bfloat16* src = qI + (row * HI + h) * 64 + 32 * blk;
-    float v[32];
+  // quantise the query: thread t takes elements 4u .. 4u+3 (u = t mod 8) of blocks t / 8 + 32 r
+  for (int blkid = tid >> 3; blkid < 2 * kMaxHI; blkid += kScoreThreads / 8) {
+    const int u = tid & 7;
+    const int h = blkid >> 1, blk = blkid & 1;
+    const bool act = h < HI;
+    float v[4];
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = __bfloat162float(src[i]);
+    for (int i = 0; i < 4; ++i) {
+      v[i] = act ? __bfloat162float(qI[(row * HI + h) * 64 + 32 * blk + 4 * u + i]) : 0.0f;
       amax = fmaxf(amax, fabsf(v[i]));
     }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const int sx = mx_block_exp(amax);
     const float inv = pow2i(-sx);
+    if (act) {
+      // element 4u + i is byte 2 (u & 1) + i / 2 of word [h][blk][i & 1][u / 2]
+      int8_t* qb = reinterpret_cast<int8_t*>(&qv_s[h][blk][0][0]);
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint32_t ev = 0, od = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        ev |= ((uint32_t)(e2m1_x2(e2m1_encode(__fmul_rn(v[8 * g + 2 * e], inv))) & 0xff)) << (8 * e);
-        od |= ((uint32_t)(e2m1_x2(e2m1_encode(__fmul_rn(v[8 * g + 2 * e + 1], inv))) & 0xff)) << (8 * e);
-      }
-      qv_s[h][blk][0][g] = (int32_t)ev;
-      qv_s[h][blk][1][g] = (int32_t)od;
+      for (int i = 0; i < 4; ++i)
+        qb[((i & 1) * 4 + (u >> 1)) * 4 + 2 * (u & 1) + (i >> 1)] =
+            (int8_t)(e2m1_x2(e2m1_encode(__fmul_rn(v[i], inv))) & 0xff);
+      if (u == 0) qe_s[h][blk] = sx;
     }
-    qe_s[h][blk] = (int8_t)sx;
   }
-  if (tid < HI) w_s[tid] = w[row * HI + tid];
   __syncthreads();
-  for (int64_t base = c0; base < c1; base += (int64_t)kScoreThreads * kDecKPT) {
+  if (tid < HI) hx_s[tid] = make_int4(qe_s[tid][0] - 2, qe_s[tid][1] - qe_s[tid][0], __float_as_int(w[row * HI + tid]), 0);
+  __syncthreads();
+  for (int64_t base = c0; base < c1; base += kDecRound) {
 #pragma unroll
     for (int i = 0; i < kDecKPT; ++i) {
       const int64_t j = base + tid + kScoreThreads * i;
@@ -247,11 +266,12 @@ scores_fp4_decode_kernel(const __nv_bfloat16* __restrict__ qI, const float* __re
         kev[g] = (int32_t)e2m1x2_int8x4(wd[g] & 0x0F0F0F0Fu);
         kod[g] = (int32_t)e2m1x2_int8x4((wd[g] >> 4) & 0x0F0F0F0Fu);
       }
-      const int ke0 = (int)(se[i] & 0xff) - 127, ke1 = (int)(se[i] >> 8) - 127;
+      const int ke0 = (int)(se[i] & 0xff) - 127, dk = (int)(se[i] >> 8) - 127 - ke0;
       float sc = 0.0f;
       for (int h = 0; h < HI; ++h) {
         const int4* q4 = reinterpret_cast<const int4*>(&qv_s[h][0][0][0]);
         const int4 q0e = q4[0], q0o = q4[1], q1e = q4[2], q1o = q4[3];
+        const int4 hx = hx_s[h];
         int P0 = 0, P1 = 0;
         P0 = __dp4a(kev[0], q0e.x, P0); P0 = __dp4a(kod[0], q0o.x, P0);
         P0 = __dp4a(kev[1], q0e.y, P0); P0 = __dp4a(kod[1], q0o.y, P0);
@@ -261,12 +281,30 @@ scores_fp4_decode_kernel(const __nv_bfloat16* __restrict__ qI, const float* __re
         P1 = __dp4a(kev[5], q1e.y, P1); P1 = __dp4a(kod[5], q1o.y, P1);
         P1 = __dp4a(kev[6], q1e.z, P1); P1 = __dp4a(kod[6], q1o.z, P1);
         P1 = __dp4a(kev[7], q1e.w, P1); P1 = __dp4a(kod[7], q1o.w, P1);
-        const float d = combine_blocks(P0, qe_s[h][0] + ke0 - 2, P1, qe_s[h][1] + ke1 - 2);
-        sc = __fmaf_rn(w_s[h], d > 0.0f ? d : 0.0f, sc);
+        const float d = combine_blocks_fast(P0, hx.x + ke0, P1, hx.y + dk);
+        sc = __fmaf_rn(__int_as_float(hx.z), d > 0.0f ? d : 0.0f, sc);
       }
       if (j < c1) scores[row * N + j] = sc;
     }
   }
+}
+
+// entries per decode-scoring CTA: a multiple of kScoreThreads, so that the
+// grid (chunks x rows) is about one CTA per resident slot (at least 2 rounds)
+int64_t decode_chunk(int64_t N, int64_t rows) {
+  static int slots = 0;
+  if (!slots) {
+    int dev = 0, sms = 148, per = 2;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    per = resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_kernel), kScoreThreads, 0);
+    slots = sms * per;
+  }
+  int64_t per_row = slots / rows;
+  if (per_row < 1) per_row = 1;
+  int64_t c = (N + per_row - 1) / per_row;
+  c = (c + kScoreThreads - 1) / kScoreThreads * kScoreThreads;
+  return c < 2 * kDecRound ? 2 * kDecRound : c;
 }
 
 // ---------------------------------------------------------------------------
@@ -325,6 +363,7 @@ scores_f32_kernel(const float* __restrict__ qI, const float* __restrict__ w,
 constexpr int kTopkThreads = 512;
 constexpr int kTkWarps = kTopkThreads / 32;
 constexpr int kTkChunk = 8192;
+constexpr size_t kTkStageMax = 200 * 1024;   // dynamic shared memory for staged candidates
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -366,6 +405,33 @@ struct CandList {   // composite keys, 0 = empty slot
     return key != 0u;
   }
 };
+
+struct SmemDense {   // staged scores: s[i] (shared memory), index base + i
+  const float* s;
+  int64_t base;
+  __device__ __forceinline__ bool get(int64_t i, uint32_t& key, uint32_t& idx) const {
+    key = order_key(s[i]);
+    idx = (uint32_t)(base + i);
+    return true;
+  }
+};
+
+// Copies n elements of E bytes (4 or 8) from global src to shared dst, every
+// copy in flight at once (asynchronous copies), then waits and syncs the CTA.
+template <int E>
+__device__ __forceinline__ void stage_to_smem(void* dst, const void* src, int64_t n) {
+  const uint32_t d0 = (uint32_t)__cvta_generic_to_shared(dst);
+  for (int64_t i = threadIdx.x; i < n; i += kTopkThreads) {
+    const char* g = reinterpret_cast<const char*>(src) + i * E;
+    if (E == 8)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d0 + (uint32_t)(i * E)), "l"(g) : "memory");
+    else
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d0 + (uint32_t)(i * E)), "l"(g) : "memory");
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
+  __syncthreads();
+}
 
 // The kk-th largest key of the stream (kk >= 1 and at most the number of
 // candidates): returns its value; sh.remaining = how many keys equal to it
@@ -541,8 +607,9 @@ topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos,
   const int kk = (int)((int64_t)k < nv ? (int64_t)k : nv);
   const DenseRow src{scores + row * N, 0};
   if (kk > 0) {
-    const uint32_t thr = radix_threshold(src, nv, kk, sh);
-    ordered_collect(src, nv, thr, sh.remaining, keys_s, sh);
+    // every visible key taken: no selection (real order keys are never 0)
+    const uint32_t thr = kk == nv ? 0u : radix_threshold(src, nv, kk, sh);
+    ordered_collect(src, nv, thr, kk == nv ? 0u : sh.remaining, keys_s, sh);
   }
   const unsigned long long* sorted = merge_sort_desc(keys_s, kk, P);
   emit_topk(sorted, kk, k, row, idx_out, score_out);
@@ -550,9 +617,12 @@ topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos,
 
 // Stage 1 of long rows: grid (rows, chunks); chunk c keeps the top-k of its
 // visible candidates [c C, (c + 1) C) in index order, at cand[(row chunks + c) k].
+// With stage set, the chunk's scores are first copied to shared memory (C
+// floats of dynamic shared memory) and every pass reads them there.
 __global__ void __launch_bounds__(kTopkThreads)
 topk_stage1_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m, int k,
-                   int chunks, int64_t C, unsigned long long* __restrict__ cand) {
+                   int chunks, int64_t C, bool stage, unsigned long long* __restrict__ cand) {
+  extern __shared__ __align__(16) float chunk_s[];
   __shared__ TkShared sh;
   const int64_t row = blockIdx.x;
   const int c = blockIdx.y;
@@ -562,28 +632,38 @@ topk_stage1_kernel(const float* __restrict__ scores, const int64_t* __restrict__
   const int kk = (int)((int64_t)k < n ? (int64_t)k : n);
   unsigned long long* dst = cand + ((int64_t)row * chunks + c) * k;
   if (kk > 0) {
-    const DenseRow src{scores + row * N, c0};
-    const uint32_t thr = radix_threshold(src, n, kk, sh);
-    ordered_collect(src, n, thr, sh.remaining, dst, sh);
+    if (stage) {
+      stage_to_smem<4>(chunk_s, scores + row * N + c0, n);
+      const SmemDense src{chunk_s, c0};
+      const uint32_t thr = kk == n ? 0u : radix_threshold(src, n, kk, sh);
+      ordered_collect(src, n, thr, kk == n ? 0u : sh.remaining, dst, sh);
+    } else {
+      const DenseRow src{scores + row * N, c0};
+      const uint32_t thr = kk == n ? 0u : radix_threshold(src, n, kk, sh);
+      ordered_collect(src, n, thr, kk == n ? 0u : sh.remaining, dst, sh);
+    }
   }
   for (int i = kk + threadIdx.x; i < k; i += kTopkThreads) dst[i] = 0ull;   // empty slots
 }
 
 // Stage 2: one CTA per row selects among its chunks' winners (in index order).
 __global__ void __launch_bounds__(kTopkThreads)
-topk_stage2_kernel(const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int chunks, int P,
+topk_stage2_kernel(const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int chunks, int P, bool stage,
                    const unsigned long long* __restrict__ cand, int32_t* __restrict__ idx_out,
                    float* __restrict__ score_out) {
-  extern __shared__ unsigned long long keys_s[];   // 2 P composite keys
+  // 2 P composite keys, then (stage) the row's chunks x k candidates
+  extern __shared__ __align__(16) unsigned long long keys_s[];
   __shared__ TkShared sh;
   const int64_t row = blockIdx.x;
   const int64_t nv = visible_entries(q_pos[row], m, N);
   const int kk = (int)((int64_t)k < nv ? (int64_t)k : nv);
-  const CandList src{cand + (int64_t)row * chunks * k};
   const int64_t n = (int64_t)chunks * k;
+  if (stage) stage_to_smem<8>(keys_s + 2 * P, cand + (int64_t)row * n, n);
+  const CandList src{stage ? keys_s + 2 * P : cand + (int64_t)row * n};
   if (kk > 0) {
-    const uint32_t thr = radix_threshold(src, n, kk, sh);
-    ordered_collect(src, n, thr, sh.remaining, keys_s, sh);
+    // kk == nv: every chunk kept all its visible candidates, all are taken
+    const uint32_t thr = kk == nv ? 0u : radix_threshold(src, n, kk, sh);
+    ordered_collect(src, n, thr, kk == nv ? 0u : sh.remaining, keys_s, sh);
   }
   const unsigned long long* sorted = merge_sort_desc(keys_s, kk, P);
   emit_topk(sorted, kk, k, row, idx_out, score_out);
@@ -620,18 +700,22 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
                                 const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
                                 int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
                                 float* score_out, float* scores_ws, void* tc_ws, void* cand_ws, void* flags_ws,
-                                cudaStream_t st) {
+                                bool tensor_cores, cudaStream_t st) {
   if ((int64_t)B * Tq == 0) return cudaSuccess;
   if (N > 0) {
     cudaError_t e;
     if (fp4 && tc_ws && indexer_tc_applies(B, Tq, HI, dI, N)) {
       e = launch_indexer_scores_tc(qI, w, reinterpret_cast<const uint8_t*>(kI), kI_scales, q_pos, B, Tq, HI, N,
                                    m, scores_ws, tc_ws, flags_ws, st);
-    } else if (fp4 && Tq <= 4 && HI <= kMaxHI && N >= 4 * kDecChunk) {
-      const dim3 grid((unsigned)((N + kDecChunk - 1) / kDecChunk), (unsigned)(B * Tq));
+    } else if (fp4 && tensor_cores && decode_tc_applies(Tq, HI, dI, N)) {
+      e = launch_scores_fp4_decode_tc(qI, w, reinterpret_cast<const uint8_t*>(kI), kI_scales, q_pos, B, Tq, HI, N,
+                                      m, scores_ws, flags_ws, st);
+    } else if (fp4 && dI == 64 && Tq <= 4 && HI <= kMaxHI && N >= 8 * kDecRound) {
+      const int64_t chunk = decode_chunk(N, (int64_t)B * Tq);
+      const dim3 grid((unsigned)((N + chunk - 1) / chunk), (unsigned)(B * Tq));
       scores_fp4_decode_kernel<<<grid, kScoreThreads, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(qI), w,
                                                                reinterpret_cast<const uint8_t*>(kI), kI_scales,
-                                                               q_pos, Tq, HI, N, m, scores_ws);
+                                                               q_pos, Tq, HI, N, m, chunk, scores_ws);
       e = cudaGetLastError();
     } else {
       const dim3 grid((unsigned)((N + kScoreThreads - 1) / kScoreThreads),
@@ -653,17 +737,21 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
   static bool attr_set = false;
   if (!attr_set) {
     cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    cudaFuncSetAttribute(topk_stage2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(topk_stage1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTkStageMax);
+    cudaFuncSetAttribute(topk_stage2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTkStageMax);
     attr_set = true;
   }
   const int64_t rows = (int64_t)B * Tq;
   if (cand_ws && topk_two_stage(B, Tq, N)) {
     const int ch = topk_chunks(N, k);
     unsigned long long* cand = reinterpret_cast<unsigned long long*>(cand_ws);
-    topk_stage1_kernel<<<dim3((unsigned)rows, (unsigned)ch), kTopkThreads, 0, st>>>(scores_ws, q_pos, N, m, k, ch,
-                                                                                  topk_chunk_size(N, k), cand);
-    topk_stage2_kernel<<<(unsigned)rows, kTopkThreads, smem, st>>>(q_pos, N, m, k, ch, P, cand, idx_out,
-                                                                   score_out);
+    // stage a chunk's scores / a row's candidates in shared memory when they fit
+    const int64_t C = topk_chunk_size(N, k);
+    const bool st1 = (size_t)C * 4 <= kTkStageMax, st2 = smem + (size_t)ch * k * 8 <= kTkStageMax;
+    topk_stage1_kernel<<<dim3((unsigned)rows, (unsigned)ch), kTopkThreads, st1 ? (size_t)C * 4 : 0, st>>>(
+        scores_ws, q_pos, N, m, k, ch, C, st1, cand);
+    topk_stage2_kernel<<<(unsigned)rows, kTopkThreads, st2 ? smem + (size_t)ch * k * 8 : smem, st>>>(
+        q_pos, N, m, k, ch, P, st2, cand, idx_out, score_out);
   } else {
     topk_kernel<<<(unsigned)rows, kTopkThreads, smem, st>>>(scores_ws, q_pos, N, m, k, P, idx_out, score_out);
   }

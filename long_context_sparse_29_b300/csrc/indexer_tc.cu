@@ -394,6 +394,240 @@ ix_scores_tc_kernel(const IxParams p, const __grid_constant__ CUtensorMap tm_q, 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Decode scoring on the tensor cores: few query rows, long entry lists.
+//
+// The same numbers as above with the roles of the operands swapped: 128
+// entries of one sequence form the MMA's M side (A, one row per entry), the
+// row's quantised query the N side (B, one row per head, 16 rows), and
+// kind::f8f6f4 takes the E2M1 codes as they are stored: a 16-element run of
+// K is 8 bytes of packed codes followed by 8 bytes of padding in shared
+// memory, so an entry's 32 code bytes become its 64-byte operand row without
+// any conversion.  Products of E2M1 values are multiples of 1/4 and a block
+// dot is below 2^11 in magnitude: exact in the fp32 accumulator.  Block b of
+// all heads lands in TMEM columns 16 b .. 16 b + 15 of the tile's buffer.
+//
+// One CTA of 4 warps walks a chunk of entries in 128-entry tiles: every
+// thread loads one entry's codes and scales, writes the operand row, one
+// elected lane issues the two block MMAs; while tile u + 1 is multiplied
+// the threads combine tile u from the other TMEM buffer (lane = entry) and
+// store its scores.  All waits have iteration limits and their outcome is
+// made uniform by the CTA barrier before the next step.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kDtThreads = 128;             // entries per tile (MMA M) = threads
+constexpr int kDtHeads = 16;                // MMA N
+constexpr uint32_t kDtBOff = 0;             // query operand, 16 rows x 128 B
+constexpr uint32_t kDtAOff = 2048;          // entry operand, 128 rows x 128 B
+constexpr uint32_t kDtMiscOff = kDtAOff + 128 * 128;
+constexpr uint32_t kDtSmem = kDtMiscOff + 512 + 1024;   // + alignment slack
+
+struct DtMisc {
+  uint64_t mma_done;
+  uint32_t tmem;
+  int qlo0, qhi0, qlo1, qhi1;   // range of the query's block exponents over the heads
+  int4 hx[kDtHeads];            // per head: {eq0 << 23, eq1 << 23, w bits, 0}
+};
+
+// kind::f8f6f4 with E2M1 A and B (format 5), fp32 D, both K-major
+__host__ __device__ constexpr uint32_t idesc_e2m1(int M, int N) {
+  return (1u << 4) | (5u << 7) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f8f6f4_elect(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, 0, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc));
+}
+
+// byte offset of logical 16-byte chunk c of row r in a 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kDtThreads, 6)
+scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
+                            const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
+                            const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
+                            int64_t chunk, float* __restrict__ scores, void* ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DtMisc* ms = reinterpret_cast<DtMisc*>(sm + kDtMiscOff);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t row = blockIdx.y;
+  const int64_t b = row / Tq;
+  const int64_t nv = visible(q_pos[row], m, N);
+  const int64_t c0 = (int64_t)blockIdx.x * chunk;
+  if (c0 >= nv) return;   // uniform
+  const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
+  const int ntiles = (int)((c1 - c0 + kDtThreads - 1) / kDtThreads);
+
+  // the first tile's entry (codes and scales) in flight during the set-up
+  auto load_entry = [&](int u, uint4& lo, uint4& hi, uint32_t& sc) {
+    int64_t j = c0 + (int64_t)u * kDtThreads + tid;
+    j = j < c1 ? j : c0;
+    const uint4* src = reinterpret_cast<const uint4*>(kc + (b * N + j) * 32);
+    lo = __ldg(src);
+    hi = __ldg(src + 1);
+    sc = __ldg(reinterpret_cast<const uint16_t*>(ks + (b * N + j) * 2));
+  };
+  uint4 klo, khi;
+  uint32_t ksc;
+  load_entry(0, klo, khi, ksc);
+
+  // ---- set-up: TMEM, barrier, zeroed query operand ----
+  for (int i = tid; i < 2048 / 16; i += kDtThreads) reinterpret_cast<uint4*>(sm + kDtBOff)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    mbar_init(&ms->mma_done, 1);
+    mbar_fence_init();
+    ms->qlo0 = ms->qlo1 = 1 << 30;
+    ms->qhi0 = ms->qhi1 = -(1 << 30);
+  }
+  if (warp == 0) tmem_alloc(&ms->tmem, 64);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = ms->tmem;
+
+  // ---- the query: MXFP4 codes into the B operand, block exponents ----
+  // thread t: elements 4u .. 4u + 3 (u = t mod 8) of blocks t / 8 + 16 r
+  for (int blkid = tid >> 3; blkid < 2 * kDtHeads; blkid += kDtThreads / 8) {
+    const int u = tid & 7, h = blkid >> 1, blk = blkid & 1;
+    const bool act = h < HI;
+    float v[4];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] = act ? __bfloat162float(qI[(row * HI + h) * 64 + 32 * blk + 4 * u + i]) : 0.0f;
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int sx = mx_block_exp(amax);
+    const float inv = pow2i(-sx);
+    if (act) {
+      uint32_t cd = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cd |= e2m1_encode(__fmul_rn(v[i], inv)) << (4 * i);
+      // element 32 blk + 4 u + i: run 2 blk + u / 4 of the head's row, data bytes 2 (u mod 4) .. + 1
+      *reinterpret_cast<uint16_t*>(sm + kDtBOff + sw128_off(h, 2 * blk + (u >> 2)) + 2 * (u & 3)) = (uint16_t)cd;
+      if (u == 0) {
+        if (blk == 0) {
+          atomicMin(&ms->qlo0, sx);
+          atomicMax(&ms->qhi0, sx);
+          ms->hx[h].x = sx << 23;
+          ms->hx[h].z = __float_as_int(w[row * HI + h]);
+        } else {
+          atomicMin(&ms->qlo1, sx);
+          atomicMax(&ms->qhi1, sx);
+          ms->hx[h].y = sx << 23;
+        }
+      }
+    }
+  }
+  const uint32_t aA = smem_u32(sm + kDtAOff), aB = smem_u32(sm + kDtBOff);
+  constexpr uint32_t id = idesc_e2m1(kDtThreads, kDtHeads);
+  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  bool ok = true;
+  int issued = 0, waited = 0;   // MMA tile pairs issued / seen complete
+  uint32_t sc_cur = 0;   // scales of the tile in the TMEM buffer being combined
+  // tile u: operand row written from the registers, then multiplied
+  auto put_tile = [&]() {
+    uint8_t* a = sm + kDtAOff;
+    *reinterpret_cast<uint4*>(a + sw128_off(tid, 0)) = make_uint4(klo.x, klo.y, 0, 0);
+    *reinterpret_cast<uint4*>(a + sw128_off(tid, 1)) = make_uint4(klo.z, klo.w, 0, 0);
+    *reinterpret_cast<uint4*>(a + sw128_off(tid, 2)) = make_uint4(khi.x, khi.y, 0, 0);
+    *reinterpret_cast<uint4*>(a + sw128_off(tid, 3)) = make_uint4(khi.z, khi.w, 0, 0);
+    fence_proxy_async();
+  };
+  auto issue = [&](int u) {
+    if (warp == 0) {
+      fence_after_sync();
+      const uint64_t ad = sdesc_sw128(aA, 16, 1024), bd = sdesc_sw128(aB, 16, 1024);
+      const uint32_t d = tmem + 32u * (u & 1);
+      mma_f8f6f4_elect(d, ad, bd, id);
+      mma_f8f6f4_elect(d + 16u, ad + 2, bd + 2, id);
+      mma_commit_elect(&ms->mma_done);
+      __syncwarp();
+    }
+  };
+  put_tile();
+  sc_cur = ksc;
+  fence_before_sync();
+  __syncthreads();   // query operand, exponent ranges, tile 0 written
+  const int qlo0 = ms->qlo0, qhi0 = ms->qhi0, qlo1 = ms->qlo1, qhi1 = ms->qhi1;
+  issue(0);
+  issued = 1;
+  if (ntiles > 1) load_entry(1, klo, khi, ksc);
+
+  for (int u = 0; u < ntiles; ++u) {
+    const bool done = mbar_wait(&ms->mma_done, (uint32_t)(u & 1), kIxWait);
+    waited += done ? 1 : 0;
+    fence_after_sync();
+    const uint32_t sc_this = sc_cur;
+    if (u + 1 < ntiles) {   // the operand is free: write tile u + 1
+      put_tile();
+      sc_cur = ksc;
+    }
+    fence_before_sync();
+    ok = __syncthreads_and(ok && done) != 0;
+    if (!ok) break;
+    if (u + 1 < ntiles) {
+      issue(u + 1);
+      ++issued;
+      if (u + 2 < ntiles) load_entry(u + 2, klo, khi, ksc);
+    }
+    // ---- combine tile u: lane = entry, 16 heads x 2 blocks from TMEM ----
+    uint32_t P[32];
+    tmem_ld32(tmem + lane_base + 32u * (u & 1), P);
+    tmem_wait_ld();
+    const int x0 = (int)(sc_this & 0xffu), x1 = (int)(sc_this >> 8);
+    const int X0 = x0 << 23, X1 = x1 << 23;
+    // block b of head h is scaled by 2^(eq_bh + x_b - 127): one exact multiply
+    // when every such power of the entry lies in [2^-100, 2^100]
+    const bool fast = qlo0 + x0 >= 27 && qhi0 + x0 <= 227 && qlo1 + x1 >= 27 && qhi1 + x1 <= 227;
+    float s = 0.0f;
+    if (fast) {
+#pragma unroll
+      for (int h = 0; h < kDtHeads; ++h) {
+        if (h < HI) {
+          const int4 hx = ms->hx[h];
+          const float d = __fadd_rn(__fmul_rn(__uint_as_float(P[h]), __int_as_float(hx.x + X0)),
+                                    __fmul_rn(__uint_as_float(P[16 + h]), __int_as_float(hx.y + X1)));
+          s = __fmaf_rn(__int_as_float(hx.z), d > 0.0f ? d : 0.0f, s);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < kDtHeads; ++h) {
+        if (h < HI) {
+          const int4 hx = ms->hx[h];
+          const float d = __fadd_rn(scale_pow2(__uint_as_float(P[h]), (hx.x >> 23) + x0 - 127),
+                                    scale_pow2(__uint_as_float(P[16 + h]), (hx.y >> 23) + x1 - 127));
+          s = __fmaf_rn(__int_as_float(hx.z), d > 0.0f ? d : 0.0f, s);
+        }
+      }
+    }
+    const int64_t j = c0 + (int64_t)u * kDtThreads + tid;
+    if (j < c1) scores[row * N + j] = s;
+  }
+  if (!ok) {
+    if (tid == 0) flag_timeout(ws);
+    // an MMA still in flight finishes (bounded wait) before its TMEM is freed
+    if (issued > waited) mbar_wait(&ms->mma_done, (uint32_t)((issued - 1) & 1), kIxWait);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
 namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -475,6 +709,36 @@ cudaError_t launch_indexer_scores_tc(const void* qI, const float* w, const uint8
   }
   const dim3 grid((unsigned)((N + kIxChunk - 1) / kIxChunk), (unsigned)((Tq + kIxRows - 1) / kIxRows), (unsigned)B);
   ix_scores_tc_kernel<<<grid, kIxThreads, kIxSmem, st>>>(p, tm_q, tm_k);
+  return cudaGetLastError();
+}
+
+bool decode_tc_applies(int64_t Tq, int HI, int dI, int64_t N) {
+  return Tq <= 4 && dI == 64 && HI >= 1 && HI <= kDtHeads && N >= 8 * kDtThreads * 8;
+}
+
+cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const uint8_t* kc, const uint8_t* ks,
+                                        const int64_t* q_pos, int B, int64_t Tq, int HI, int64_t N, int m,
+                                        float* scores, void* flags_ws, cudaStream_t st) {
+  static int slots = 0;
+  if (!slots) {
+    int dev = 0, sms = 148, per = 4;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaFuncSetAttribute(scores_fp4_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDtSmem);
+    per = resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_tc_kernel), kDtThreads, kDtSmem);
+    per = per > 8 ? 8 : per;   // 64 TMEM columns each: at most 8 per SM
+    slots = sms * per;
+  }
+  const int64_t rows = (int64_t)B * Tq;
+  // chunks of whole tiles, about one CTA per resident slot, at least 2 tiles each
+  int64_t per_row = slots / rows;
+  if (per_row < 1) per_row = 1;
+  int64_t chunk = (N + per_row - 1) / per_row;
+  chunk = (chunk + kDtThreads - 1) / kDtThreads * kDtThreads;
+  if (chunk < 2 * kDtThreads) chunk = 2 * kDtThreads;
+  const dim3 grid((unsigned)((N + chunk - 1) / chunk), (unsigned)rows);
+  scores_fp4_decode_tc_kernel<<<grid, kDtThreads, kDtSmem, st>>>(reinterpret_cast<const __nv_bfloat16*>(qI), w, kc,
+                                                                 ks, q_pos, Tq, HI, N, m, chunk, scores, flags_ws);
   return cudaGetLastError();
 }
 

@@ -51,7 +51,29 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
                                 const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
                                 int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
                                 float* score_out, float* scores_ws, void* tc_ws, void* cand_ws, void* flags_ws,
-                                cudaStream_t st);
+                                bool tensor_cores, cudaStream_t st);
+// CTAs of `kernel` that fit on one SM at once: the tightest of its register,
+// shared-memory (228 KiB per SM, 1 KiB reserved per CTA), thread (2048) and
+// block (32) limits, from the compiled kernel's attributes
+inline int resident_ctas(const void* kernel, int threads, size_t dyn_smem) {
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return 1;
+  const int warps = (threads + 31) / 32;
+  const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;   // allocated per warp in units of 256
+  const int by_regs = regs_warp > 0 ? 65536 / (regs_warp * warps) : 32;
+  const int by_smem = (int)((size_t)233472 / (fa.sharedSizeBytes + dyn_smem + 1024));
+  const int by_threads = 2048 / (warps * 32);
+  int n = by_regs < by_smem ? by_regs : by_smem;
+  n = n < by_threads ? n : by_threads;
+  n = n < 32 ? n : 32;
+  return n < 1 ? 1 : n;
+}
+
+// decode scoring on the tensor cores (few query rows, long entry lists)
+bool decode_tc_applies(int64_t Tq, int HI, int dI, int64_t N);
+cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const uint8_t* kc, const uint8_t* ks,
+                                        const int64_t* q_pos, int B, int64_t Tq, int HI, int64_t N, int m,
+                                        float* scores, void* flags_ws, cudaStream_t st);
 // two-stage top-k for long rows when there are few of them, and its scratch
 bool topk_two_stage(int B, int64_t Tq, int64_t N);
 size_t topk_cand_bytes(int B, int64_t Tq, int64_t N, int k);

@@ -97,7 +97,8 @@ extern "C" int csa_indexer_topk_noalloc(const void* qI, int qI_dtype, const floa
   if (r != CSA_OK) return r;
   const cudaError_t e = csa::launch_indexer_topk(qI, fp4, w, kI, kI_scales, q_pos, B, Tq, HI, dI, N, m,
                                                  k, idx_out, score_out, reinterpret_cast<float*>(scratch),
-                                                 nullptr, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+                                                 nullptr, nullptr, nullptr, true,
+                                                 reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return csa::report_error(CSA_ERR_CUDA, cudaGetErrorString(e));
   return CSA_OK;
 }

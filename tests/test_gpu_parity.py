@@ -498,3 +498,53 @@ def test_indexer_tc_scores_match_dp4a(csa, monkeypatch, B, Tq, N, m, key_exps, q
     monkeypatch.delenv("CSA_INDEXER_IMPL")
     np.testing.assert_array_equal(idx_tc.cpu().numpy(), idx_dp.cpu().numpy())
     np.testing.assert_array_equal(sc_tc.cpu().numpy().view(np.uint32), sc_dp.cpu().numpy().view(np.uint32))
+
+
+def test_indexer_decode_scores_wide_scale_spread(csa, oracle_mod):
+    """Decode-shaped scoring (one query row per sequence, N past the decode
+    kernel's threshold) with block scales far apart, so the two block
+    dots of a head meet both as one integer and through the two-product form
+    (scale exponents up to ~33 apart);
+    top-k of k = 4096 in two stages (chunk winners staged in shared memory)
+    against the oracle, bit for bit.  Spreads stay where the oracle's fp64 dot
+    is exact (13-bit block dots, shifts below 40)."""
+    rng = np.random.default_rng(2024)
+    B, N, HI, dI, k = 2, 9000, 16, 64, 4096
+    codes, scales = _mxfp4_keys_random(rng, B * N, list(range(118, 143)))
+    qI = rng.standard_normal((B, 1, HI, dI)).astype(np.float32)
+    qI[:, :, 3, 32:] *= np.float32(2.0 ** 6)                 # one head's blocks 2^6 apart
+    qbits = wl.f32_to_bf16_bits(qI)
+    w = rng.uniform(0.0, 1.0, (B, 1, HI)).astype(np.float32)
+    q_pos = np.array([[N - 1], [N - 700]], np.int64)          # the second row sees fewer entries
+    idx, sc = csa.indexer_topk(dev_bf16(qbits), dev(w), dev(codes.reshape(B, N, 32)),
+                               dev(scales.reshape(B, N, 2)), dev(q_pos), N, 1, k)
+    oidx, osc = oracle_mod.indexer_topk(wl.bf16_bits_to_f32(qbits), w,
+                                        (codes.reshape(B, N, 32), scales.reshape(B, N, 2)), q_pos, N, 1, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), osc.view(np.uint32))
+
+
+@pytest.mark.parametrize("B,N,HI,key_exps,q_scale", [
+    (2, 9000, 16, list(range(120, 135)), 1.0),          # ordinary scales (one-multiply epilogue)
+    (1, 8192 + 77, 16, [0, 1, 2, 250, 254], 1e-30),     # powers far outside [2^-100, 2^100]
+    (3, 8200, 12, list(range(100, 160)), 3e4),         # fewer heads than the MMA's 16 columns
+])
+def test_indexer_decode_tc_matches_dp4a(csa, monkeypatch, B, N, HI, key_exps, q_scale):
+    """Decode scoring on the tensor cores (E2M1 operands straight from the
+    stored codes) equals the integer decode kernel bit for bit: indices and
+    scores of a top-4096 per row."""
+    rng = np.random.default_rng(11 + N + HI)
+    codes, scales = _mxfp4_keys_random(rng, B * N, key_exps)
+    qI = (rng.standard_normal((B, 1, HI, 64)) * q_scale).astype(np.float32)
+    qI[:, :, 0, :32] = 0.0                                 # an all-zero block (exponent 0)
+    qbits = wl.f32_to_bf16_bits(qI)
+    w = rng.standard_normal((B, 1, HI)).astype(np.float32)
+    q_pos = (N - 1 - rng.integers(0, 300, size=(B, 1))).astype(np.int64)
+    args = (dev_bf16(qbits), dev(w), dev(codes.reshape(B, N, 32)), dev(scales.reshape(B, N, 2)), dev(q_pos), N, 1,
+            4096)
+    idx_tc, sc_tc = csa.indexer_topk(*args)
+    monkeypatch.setenv("CSA_INDEXER_IMPL", "dp4a")
+    idx_dp, sc_dp = csa.indexer_topk(*args)
+    monkeypatch.delenv("CSA_INDEXER_IMPL")
+    np.testing.assert_array_equal(idx_tc.cpu().numpy(), idx_dp.cpu().numpy())
+    np.testing.assert_array_equal(sc_tc.cpu().numpy().view(np.uint32), sc_dp.cpu().numpy().view(np.uint32))
