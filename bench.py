@@ -254,7 +254,7 @@ LAUNCHES_PER_STEP = 11
 # DRAM bytes (read + write) of one attn_tc_kernel launch on this workload, from
 # one ncu capture of it (dram__bytes_read.sum + dram__bytes_write.sum); to be
 # set to None when the kernel changes, until it is captured again
-ATTN_TRAFFIC = 631651584 + 495853312
+ATTN_TRAFFIC = 631670784 + 493387264
 
 
 # --------------------------------------------------------------------------

@@ -360,8 +360,8 @@ scores_f32_kernel(const float* __restrict__ qI, const float* __restrict__ w,
 // top-k lies in their union: the order is total), then one CTA per row
 // selects among the chunk winners.
 // ---------------------------------------------------------------------------
-constexpr int kTopkThreads = 512;
-constexpr int kTkWarps = kTopkThreads / 32;
+constexpr int kTopkThreads = 512;        // CTA of the two-stage kernels (few long rows)
+constexpr int kTopkRowThreads = 128;     // CTA of the one-row kernel (many rows of at most kTkChunk)
 constexpr int kTkChunk = 8192;
 constexpr size_t kTkStageMax = 200 * 1024;   // dynamic shared memory for staged candidates
 
@@ -379,9 +379,10 @@ __device__ __forceinline__ unsigned long long composite(uint32_t key, uint32_t i
   return ((unsigned long long)key << 32) | (unsigned long long)(0xffffffffu - idx);
 }
 
+template <int NT>
 struct TkShared {
   unsigned int hist[256];
-  unsigned int cnt_gt[kTkWarps], cnt_eq[kTkWarps];
+  unsigned int cnt_gt[NT / 32], cnt_eq[NT / 32];
   unsigned int prefix, remaining;
 };
 
@@ -418,10 +419,10 @@ struct SmemDense {   // staged scores: s[i] (shared memory), index base + i
 
 // Copies n elements of E bytes (4 or 8) from global src to shared dst, every
 // copy in flight at once (asynchronous copies), then waits and syncs the CTA.
-template <int E>
+template <int NT, int E>
 __device__ __forceinline__ void stage_to_smem(void* dst, const void* src, int64_t n) {
   const uint32_t d0 = (uint32_t)__cvta_generic_to_shared(dst);
-  for (int64_t i = threadIdx.x; i < n; i += kTopkThreads) {
+  for (int64_t i = threadIdx.x; i < n; i += NT) {
     const char* g = reinterpret_cast<const char*>(src) + i * E;
     if (E == 8)
       asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d0 + (uint32_t)(i * E)), "l"(g) : "memory");
@@ -436,8 +437,8 @@ __device__ __forceinline__ void stage_to_smem(void* dst, const void* src, int64_
 // The kk-th largest key of the stream (kk >= 1 and at most the number of
 // candidates): returns its value; sh.remaining = how many keys equal to it
 // are taken.
-template <class Src>
-__device__ uint32_t radix_threshold(const Src& src, int64_t n, int kk, TkShared& sh) {
+template <int NT, class Src>
+__device__ uint32_t radix_threshold(const Src& src, int64_t n, int kk, TkShared<NT>& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     sh.prefix = 0;
@@ -445,10 +446,10 @@ __device__ uint32_t radix_threshold(const Src& src, int64_t n, int kk, TkShared&
   }
   uint32_t mask = 0;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    if (tid < 256) sh.hist[tid] = 0;
+    for (int i = tid; i < 256; i += NT) sh.hist[i] = 0;
     __syncthreads();
     const uint32_t prefix = sh.prefix;
-    for (int64_t i = tid; i < n; i += kTopkThreads) {
+    for (int64_t i = tid; i < n; i += NT) {
       uint32_t u, id;
       if (src.get(i, u, id) && (u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & 255u], 1u);
     }
@@ -496,11 +497,11 @@ __device__ uint32_t radix_threshold(const Src& src, int64_t n, int kk, TkShared&
 // Writes the chosen candidates (key > thr, and the first need_eq keys == thr in
 // stream order) to dst[0..) in stream order as composite keys.  Warp w scans
 // slots [w seg, (w + 1) seg).
-template <class Src>
+template <int NT, class Src>
 __device__ void ordered_collect(const Src& src, int64_t n, uint32_t thr, unsigned int need_eq,
-                                unsigned long long* dst, TkShared& sh) {
+                                unsigned long long* dst, TkShared<NT>& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t seg = ((n + kTkWarps - 1) / kTkWarps + 31) & ~int64_t(31);
+  const int64_t seg = ((n + (NT / 32) - 1) / (NT / 32) + 31) & ~int64_t(31);
   const int64_t lo = warp * seg, hi = lo + seg < n ? lo + seg : n;
   unsigned int ngt = 0, neq = 0;
   for (int64_t b = lo; b < hi; b += 32) {
@@ -542,14 +543,15 @@ __device__ void ordered_collect(const Src& src, int64_t n, uint32_t thr, unsigne
 // Sorts buf[0..P) descending (P a power of two >= 32, slots past `count` are
 // padded with distinct keys below every real one); buf has 2 P slots.
 // Returns the buffer that holds the result.
+template <int NT>
 __device__ unsigned long long* merge_sort_desc(unsigned long long* buf, int count, int P) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned long long* b0 = buf;
   unsigned long long* b1 = buf + P;
-  for (int i = tid; i < P; i += kTopkThreads)
+  for (int i = tid; i < P; i += NT)
     if (i >= count) b0[i] = (unsigned long long)(P - i);
   __syncthreads();
-  for (int r = warp; r < P / 32; r += kTkWarps) {
+  for (int r = warp; r < P / 32; r += (NT / 32)) {
     unsigned long long v = b0[r * 32 + lane];
 #pragma unroll
     for (int size = 2; size <= 32; size <<= 1) {
@@ -564,7 +566,7 @@ __device__ unsigned long long* merge_sort_desc(unsigned long long* buf, int coun
   }
   __syncthreads();
   for (int L = 32; L < P; L <<= 1) {
-    for (int i = tid; i < P; i += kTopkThreads) {
+    for (int i = tid; i < P; i += NT) {
       const unsigned long long x = b0[i];
       const int r = i / L, pos = i - r * L;
       const unsigned long long* part = b0 + (r ^ 1) * L;
@@ -581,9 +583,10 @@ __device__ unsigned long long* merge_sort_desc(unsigned long long* buf, int coun
   return b0;
 }
 
+template <int NT>
 __device__ __forceinline__ void emit_topk(const unsigned long long* sorted, int kk, int k, int64_t row,
                                           int32_t* idx_out, float* score_out) {
-  for (int r = threadIdx.x; r < k; r += kTopkThreads) {
+  for (int r = threadIdx.x; r < k; r += NT) {
     int32_t j = -1;
     float sc = -INFINITY;
     if (r < kk) {
@@ -597,22 +600,23 @@ __device__ __forceinline__ void emit_topk(const unsigned long long* sorted, int 
 }
 
 // One CTA per query row over its visible scores (rows of any length).
-__global__ void __launch_bounds__(kTopkThreads)
+__global__ void __launch_bounds__(kTopkRowThreads)
 topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int P,
             int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
+  constexpr int NT = kTopkRowThreads;
   extern __shared__ unsigned long long keys_s[];   // 2 P composite keys
-  __shared__ TkShared sh;
+  __shared__ TkShared<NT> sh;
   const int64_t row = blockIdx.x;
   const int64_t nv = visible_entries(q_pos[row], m, N);
   const int kk = (int)((int64_t)k < nv ? (int64_t)k : nv);
   const DenseRow src{scores + row * N, 0};
   if (kk > 0) {
     // every visible key taken: no selection (real order keys are never 0)
-    const uint32_t thr = kk == nv ? 0u : radix_threshold(src, nv, kk, sh);
-    ordered_collect(src, nv, thr, kk == nv ? 0u : sh.remaining, keys_s, sh);
+    const uint32_t thr = kk == nv ? 0u : radix_threshold<NT>(src, nv, kk, sh);
+    ordered_collect<NT>(src, nv, thr, kk == nv ? 0u : sh.remaining, keys_s, sh);
   }
-  const unsigned long long* sorted = merge_sort_desc(keys_s, kk, P);
-  emit_topk(sorted, kk, k, row, idx_out, score_out);
+  const unsigned long long* sorted = merge_sort_desc<NT>(keys_s, kk, P);
+  emit_topk<NT>(sorted, kk, k, row, idx_out, score_out);
 }
 
 // Stage 1 of long rows: grid (rows, chunks); chunk c keeps the top-k of its
@@ -622,8 +626,9 @@ topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos,
 __global__ void __launch_bounds__(kTopkThreads)
 topk_stage1_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m, int k,
                    int chunks, int64_t C, bool stage, unsigned long long* __restrict__ cand) {
+  constexpr int NT = kTopkThreads;
   extern __shared__ __align__(16) float chunk_s[];
-  __shared__ TkShared sh;
+  __shared__ TkShared<NT> sh;
   const int64_t row = blockIdx.x;
   const int c = blockIdx.y;
   const int64_t nv = visible_entries(q_pos[row], m, N);
@@ -633,17 +638,17 @@ topk_stage1_kernel(const float* __restrict__ scores, const int64_t* __restrict__
   unsigned long long* dst = cand + ((int64_t)row * chunks + c) * k;
   if (kk > 0) {
     if (stage) {
-      stage_to_smem<4>(chunk_s, scores + row * N + c0, n);
+      stage_to_smem<NT, 4>(chunk_s, scores + row * N + c0, n);
       const SmemDense src{chunk_s, c0};
-      const uint32_t thr = kk == n ? 0u : radix_threshold(src, n, kk, sh);
-      ordered_collect(src, n, thr, kk == n ? 0u : sh.remaining, dst, sh);
+      const uint32_t thr = kk == n ? 0u : radix_threshold<NT>(src, n, kk, sh);
+      ordered_collect<NT>(src, n, thr, kk == n ? 0u : sh.remaining, dst, sh);
     } else {
       const DenseRow src{scores + row * N, c0};
-      const uint32_t thr = kk == n ? 0u : radix_threshold(src, n, kk, sh);
-      ordered_collect(src, n, thr, kk == n ? 0u : sh.remaining, dst, sh);
+      const uint32_t thr = kk == n ? 0u : radix_threshold<NT>(src, n, kk, sh);
+      ordered_collect<NT>(src, n, thr, kk == n ? 0u : sh.remaining, dst, sh);
     }
   }
-  for (int i = kk + threadIdx.x; i < k; i += kTopkThreads) dst[i] = 0ull;   // empty slots
+  for (int i = kk + threadIdx.x; i < k; i += NT) dst[i] = 0ull;   // empty slots
 }
 
 // Stage 2: one CTA per row selects among its chunks' winners (in index order).
@@ -651,22 +656,23 @@ __global__ void __launch_bounds__(kTopkThreads)
 topk_stage2_kernel(const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int chunks, int P, bool stage,
                    const unsigned long long* __restrict__ cand, int32_t* __restrict__ idx_out,
                    float* __restrict__ score_out) {
+  constexpr int NT = kTopkThreads;
   // 2 P composite keys, then (stage) the row's chunks x k candidates
   extern __shared__ __align__(16) unsigned long long keys_s[];
-  __shared__ TkShared sh;
+  __shared__ TkShared<NT> sh;
   const int64_t row = blockIdx.x;
   const int64_t nv = visible_entries(q_pos[row], m, N);
   const int kk = (int)((int64_t)k < nv ? (int64_t)k : nv);
   const int64_t n = (int64_t)chunks * k;
-  if (stage) stage_to_smem<8>(keys_s + 2 * P, cand + (int64_t)row * n, n);
+  if (stage) stage_to_smem<NT, 8>(keys_s + 2 * P, cand + (int64_t)row * n, n);
   const CandList src{stage ? keys_s + 2 * P : cand + (int64_t)row * n};
   if (kk > 0) {
     // kk == nv: every chunk kept all its visible candidates, all are taken
-    const uint32_t thr = kk == nv ? 0u : radix_threshold(src, n, kk, sh);
-    ordered_collect(src, n, thr, kk == nv ? 0u : sh.remaining, keys_s, sh);
+    const uint32_t thr = kk == nv ? 0u : radix_threshold<NT>(src, n, kk, sh);
+    ordered_collect<NT>(src, n, thr, kk == nv ? 0u : sh.remaining, keys_s, sh);
   }
-  const unsigned long long* sorted = merge_sort_desc(keys_s, kk, P);
-  emit_topk(sorted, kk, k, row, idx_out, score_out);
+  const unsigned long long* sorted = merge_sort_desc<NT>(keys_s, kk, P);
+  emit_topk<NT>(sorted, kk, k, row, idx_out, score_out);
 }
 
 int topk_pad(int k) {
@@ -753,7 +759,7 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
     topk_stage2_kernel<<<(unsigned)rows, kTopkThreads, st2 ? smem + (size_t)ch * k * 8 : smem, st>>>(
         q_pos, N, m, k, ch, P, st2, cand, idx_out, score_out);
   } else {
-    topk_kernel<<<(unsigned)rows, kTopkThreads, smem, st>>>(scores_ws, q_pos, N, m, k, P, idx_out, score_out);
+    topk_kernel<<<(unsigned)rows, kTopkRowThreads, smem, st>>>(scores_ws, q_pos, N, m, k, P, idx_out, score_out);
   }
   return cudaGetLastError();
 }
