@@ -78,6 +78,7 @@ def _declare(L):
         "orc_e4m3_decode": (F64, [ctypes.c_uint8]),
         "orc_e2m1_decode": (F64, [ctypes.c_uint8]),
         "orc_compress": (None, [P, P, P, I64, I64, I32, I32, I32, I64, P, P, I64, P]),
+        "orc_compress_channel_logits": (None, [P, P, P, I64, I64, I32, I32, I32, I64, P, P, I64, P]),
         "orc_pack_mixed": (None, [P, I64, P]),
         "orc_unpack_mixed": (None, [P, I64, P]),
         "orc_mxfp4_quant": (None, [P, I64, I32, P, P]),
@@ -157,10 +158,14 @@ def e2m1_decode(codes) -> np.ndarray:
 # compression and cache formats
 # --------------------------------------------------------------------------
 def compress(x, z, s, m: int, R: int, pos0: int = 0, rope=None) -> np.ndarray:
-    """Block compression + RoPE of the last R channels: x fp32 [B, T, C] -> [B, T//m, C]."""
+    """Block compression + RoPE of the last R channels: x fp32 [B, T, C] -> [B, T//m, C].
+
+    z [B, T]: one logit per token; z [B, T, C]: one logit per token and channel.
+    """
     x = _c(x, np.float32)
     B, T, C = x.shape
-    z = _c(z, np.float32).reshape(B, T)
+    per_channel = np.ndim(z) == 3
+    z = _c(z, np.float32).reshape((B, T, C) if per_channel else (B, T))
     s = None if s is None else _c(s, np.float32)
     N = T // m
     out = np.empty((B, N, C), np.float32)
@@ -170,8 +175,8 @@ def compress(x, z, s, m: int, R: int, pos0: int = 0, rope=None) -> np.ndarray:
     else:
         rc = rs = None
         rows = 0
-    lib().orc_compress(_p(x), _p(z), _p(s), B, T, C, m, R, int(pos0), _p(rc), _p(rs), rows,
-                       _p(out))
+    fn = lib().orc_compress_channel_logits if per_channel else lib().orc_compress
+    fn(_p(x), _p(z), _p(s), B, T, C, m, R, int(pos0), _p(rc), _p(rs), rows, _p(out))
     return out
 
 

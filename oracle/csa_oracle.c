@@ -235,6 +235,53 @@ void orc_compress(const float *x, const float *z, const float *s, int64_t B, int
 }
 
 /* ------------------------------------------------------------------------ */
+/* Block compression with per-channel logits (the other plain reading of     */
+/* [XM] CSA's weighted sum: one learned logit per token and channel).  Each   */
+/* channel c of block j takes its own softmax over the block's m logits       */
+/* z_{jm+i, c}, with the fp32 sequence of orc_compress written per channel:   */
+/*   mu_c = max_i z_{i,c};  e_i = sexp(z_{i,c} - mu_c);  S_c = e_0 + e_1 + ...*/
+/*   (in order);  a_i = e_i / S_c;  acc = fma(a_i, x_{jm+i,c}, acc) over i;  */
+/*   C_c = acc * s_c;  then the same RoPE of the last R channels.            */
+/* With z_{t,c} equal across c this is orc_compress exactly.                 */
+/* x: fp32 [B, T, C]; z: [B, T, C]; out: fp32 [B, N, C].                      */
+/* ------------------------------------------------------------------------ */
+void orc_compress_channel_logits(const float *x, const float *z, const float *s, int64_t B, int64_t T,
+                                 int C, int m, int R, int64_t pos0, const float *rcos,
+                                 const float *rsin, int64_t rope_rows, float *out) {
+    int64_t N = T / m;
+    int half = R / 2;
+    float *e = (float *)malloc(sizeof(float) * (size_t)m);
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t j = 0; j < N; ++j) {
+            float *o = out + (b * N + j) * C;
+            for (int c = 0; c < C; ++c) {
+                const float *zc = z + (b * T + j * m) * C + c;   /* z_{jm+i, c} = zc[i * C] */
+                float mu = zc[0];
+                for (int i = 1; i < m; ++i) mu = fmaxf(mu, zc[(int64_t)i * C]);
+                for (int i = 0; i < m; ++i) e[i] = orc_sexp(zc[(int64_t)i * C] - mu);
+                float S = e[0];
+                for (int i = 1; i < m; ++i) S = S + e[i];
+                float acc = 0.0f;
+                for (int i = 0; i < m; ++i) acc = fmaf(e[i] / S, x[(b * T + j * m + i) * C + c], acc);
+                o[c] = acc * (s ? s[c] : 1.0f);
+            }
+            if (R > 0) {
+                int64_t p = pos0 + j * m + m - 1;
+                if (p < 0 || p >= rope_rows) abort();
+                for (int i = 0; i < half; ++i) {
+                    float cs = rcos[p * half + i], sn = rsin[p * half + i];
+                    float x0 = o[C - R + 2 * i], x1 = o[C - R + 2 * i + 1];
+                    float a0 = x0 * cs, a1 = x1 * sn, b0 = x0 * sn, b1 = x1 * cs;
+                    o[C - R + 2 * i] = a0 - a1;
+                    o[C - R + 2 * i + 1] = b0 + b1;
+                }
+            }
+        }
+    }
+    free(e);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Mixed FP8/BF16 cache row.  [XM] key technical details: the KV cache keeps  */
 /* the RoPE dims in BF16 and the other dims in FP8, close to half the size  */
 /* of a pure BF16 cache.  Row of D = 512 post-RoPE values (448 nope + 64     */
