@@ -156,6 +156,24 @@ int csa_compress_kv(const void *x, int x_dtype, const float *z, const float *s,
                     uint8_t *out_scales, void *stream);
 
 /*
+ * csa_compress_kv_channel_logits: csa_compress_kv with one logit per token
+ * and channel -- the other plain reading of [XM] CSA's weighted sum of every
+ * m tokens' KV entries (a learned weight per slot and channel).
+ *  z         (device) fp32 [B, T, C] compression logits
+ *  every other argument, the layout of out / out_scales and the errors as
+ *  csa_compress_kv.
+ * Channel c of entry j has its own weights a_{i,c} = softmax over the block
+ * of z_{jm+i, c}, by the sequence above written per channel (mu_c = max,
+ * e_i = sexp(z_{i,c} - mu_c), S_c in token order, a_i = e_i / S_c); then
+ * (sum_i fma order) a_{i,c} x_{i,c}, times s_c, and the same RoPE and
+ * packing.  Logits equal across channels give csa_compress_kv's bytes.
+ */
+int csa_compress_kv_channel_logits(const void *x, int x_dtype, const float *z, const float *s,
+                                   const float *rope_cos, const float *rope_sin, int64_t rope_rows,
+                                   int64_t pos0, int B, int64_t T, int C, int R, int m, int out_fmt,
+                                   void *out, uint8_t *out_scales, void *stream);
+
+/*
  * csa_decode_append: decode-time maintenance of one layer's caches -- one new
  * token per sequence.  [XM] CSA / HCA: every m tokens become one compressed
  * entry; [XM] "百万Token 长上下文真实表现" (state cache for the uncompressed

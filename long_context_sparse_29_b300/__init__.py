@@ -120,12 +120,17 @@ def compress_kv(x, z, s, m: int, out_fmt: int, R: int = 0, rope=None, pos0: int 
                 out_scales=None):
     """Compress x [B, T, C] (bf16 or fp32) in blocks of m; see csa_compress_kv.
 
-    Returns fp32 [B, N, C] (FMT_F32), uint8 [B, N, 592] (FMT_MIXED592) or
-    (codes uint8 [B, N, C/2], scales uint8 [B, N, C/32]) (FMT_MXFP4).
+    z fp32 [B, T] (one logit per token), or [B, T, C] (one per token and
+    channel: csa_compress_kv_channel_logits).  Returns fp32 [B, N, C]
+    (FMT_F32), uint8 [B, N, 592] (FMT_MIXED592) or (codes uint8 [B, N, C/2],
+    scales uint8 [B, N, C/32]) (FMT_MXFP4).
     """
     _need(x, "x")
     B, T, C = x.shape
     _need(z, "z", torch.float32)
+    per_channel = z.dim() == 3
+    if tuple(z.shape) != ((B, T, C) if per_channel else (B, T)):
+        raise CsaError(f"z has shape {tuple(z.shape)}; [B, T] or [B, T, C] expected")
     if s is not None:
         _need(s, "s", torch.float32)
     N = T // m
@@ -140,8 +145,9 @@ def compress_kv(x, z, s, m: int, out_fmt: int, R: int = 0, rope=None, pos0: int 
             out_scales = torch.empty((B, N, C // 32), dtype=torch.uint8, device=dev)
     rc, rs = (rope if rope is not None else (None, None))
     rows = rc.shape[0] if rc is not None else 0
-    check(lib().csa_compress_kv(_ptr(x), _dt(x), _ptr(z), _ptr(s), _ptr(rc), _ptr(rs), rows, pos0,
-                                B, T, C, R, m, out_fmt, _ptr(out), _ptr(out_scales), _stream(dev)))
+    fn = lib().csa_compress_kv_channel_logits if per_channel else lib().csa_compress_kv
+    check(fn(_ptr(x), _dt(x), _ptr(z), _ptr(s), _ptr(rc), _ptr(rs), rows, pos0,
+             B, T, C, R, m, out_fmt, _ptr(out), _ptr(out_scales), _stream(dev)))
     return (out, out_scales) if out_fmt == FMT_MXFP4 else out
 
 

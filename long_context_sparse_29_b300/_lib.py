@@ -27,6 +27,8 @@ SIGNATURES = {
     "csa_status_read": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
     "kvcache_pack_fp8_bf16": (I32, [P, I64, P, P]),
     "csa_compress_kv": (I32, [P, I32, P, P, P, P, I64, I64, I32, I64, I32, I32, I32, I32, P, P, P]),
+    "csa_compress_kv_channel_logits": (I32, [P, I32, P, P, P, P, I64, I64, I32, I64, I32, I32, I32, I32, P, P,
+                                             P]),
     "csa_indexer_topk": (I32, [P, I32, P, P, P, I32, P, I32, I64, I32, I32, I64, I32, I32, P, P,
                                P, SZ, P]),
     "csa_sparse_mqa": (I32, [P, I32, P, I32, I64, I32, I32, I32, I32, P, I64, I32, P, I32, P, P,

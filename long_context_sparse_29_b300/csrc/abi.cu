@@ -193,11 +193,10 @@ int kvcache_pack_fp8_bf16(const float* v, int64_t n, uint8_t* out, void* stream)
   return cuda_result(csa::launch_pack_mixed(v, n, out, as_stream(stream)), "kvcache_pack_fp8_bf16");
 }
 
-int csa_compress_kv(const void* x, int x_dtype, const float* z, const float* s,
-                    const float* rope_cos, const float* rope_sin, int64_t rope_rows, int64_t pos0,
-                    int B, int64_t T, int C, int R, int m, int out_fmt, void* out,
-                    uint8_t* out_scales, void* stream) {
-  const char* nm = "csa_compress_kv";
+static int compress_call(const char* nm, bool z_per_channel, const void* x, int x_dtype, const float* z,
+                         const float* s, const float* rope_cos, const float* rope_sin, int64_t rope_rows,
+                         int64_t pos0, int B, int64_t T, int C, int R, int m, int out_fmt, void* out,
+                         uint8_t* out_scales, void* stream) {
   if (B < 0 || T < 0 || C < 2 || (C & 1) || m < 1 || pos0 < 0 || R < 0 || (R & 1) || R > C)
     return fail(CSA_ERR_INVALID_ARG, "%s: bad sizes (B=%d T=%lld C=%d R=%d m=%d pos0=%lld)", nm, B,
                 (long long)T, C, R, m, (long long)pos0);
@@ -224,10 +223,26 @@ int csa_compress_kv(const void* x, int x_dtype, const float* z, const float* s,
   } else if (out_fmt != CSA_FMT_F32) {
     return fail(CSA_ERR_INVALID_ARG, "%s: unknown output format %d", nm, out_fmt);
   }
-  return cuda_result(csa::launch_compress(x, x_dtype == CSA_DTYPE_BF16, z, s, rope_cos, rope_sin,
+  return cuda_result(csa::launch_compress(x, x_dtype == CSA_DTYPE_BF16, z, z_per_channel, s, rope_cos, rope_sin,
                                           pos0, B, T, C, R, m, out_fmt, out, out_scales,
                                           as_stream(stream)),
                      nm);
+}
+
+int csa_compress_kv(const void* x, int x_dtype, const float* z, const float* s,
+                    const float* rope_cos, const float* rope_sin, int64_t rope_rows, int64_t pos0,
+                    int B, int64_t T, int C, int R, int m, int out_fmt, void* out,
+                    uint8_t* out_scales, void* stream) {
+  return compress_call("csa_compress_kv", false, x, x_dtype, z, s, rope_cos, rope_sin, rope_rows, pos0, B, T, C, R,
+                       m, out_fmt, out, out_scales, stream);
+}
+
+int csa_compress_kv_channel_logits(const void* x, int x_dtype, const float* z, const float* s,
+                                   const float* rope_cos, const float* rope_sin, int64_t rope_rows, int64_t pos0,
+                                   int B, int64_t T, int C, int R, int m, int out_fmt, void* out,
+                                   uint8_t* out_scales, void* stream) {
+  return compress_call("csa_compress_kv_channel_logits", true, x, x_dtype, z, s, rope_cos, rope_sin, rope_rows,
+                       pos0, B, T, C, R, m, out_fmt, out, out_scales, stream);
 }
 
 int csa_decode_append(const void* kv, const float* z, const void* kI, const float* zI, const float* s,

@@ -178,7 +178,55 @@ __device__ __forceinline__ void compress_entry(const void* __restrict__ x, const
   entry_finish<FMT>(v, s, rcos, rsin, P, C, R, out, out_scales, lane);
 }
 
+// The same with one logit per token and channel: z holds the m blocks' rows
+// with stride C (z[i C + c]); channel c's weights are the softmax of its own m
+// logits, by the sequence of entry_weights written per channel (max, the
+// exponentials, their sum in token order, one division each), then the same
+// fma over the tokens.  The exponentials are evaluated twice (sum, weights):
+// the same fp32 values both times.
 template <int FMT, bool BF16>
+__device__ __forceinline__ void compress_entry_channel_logits(const void* __restrict__ x,
+                                                              const float* __restrict__ z,
+                                                              const float* __restrict__ s,
+                                                              const float* __restrict__ rcos,
+                                                              const float* __restrict__ rsin, int64_t P, int C,
+                                                              int R, int m, void* __restrict__ out,
+                                                              uint8_t* __restrict__ out_scales, int lane) {
+  const int npairs = C >> 1;
+  float2 v[kMaxPairs];
+#pragma unroll
+  for (int r = 0; r < kMaxPairs; ++r) {
+    v[r] = make_float2(0.0f, 0.0f);
+    const int p = lane + 32 * r;
+    if (p < npairs) {
+      const float2* z2 = reinterpret_cast<const float2*>(z);
+      float2 mu = make_float2(-INFINITY, -INFINITY);
+      for (int i = 0; i < m; ++i) {
+        const float2 w = z2[((int64_t)i * C >> 1) + p];
+        mu.x = fmaxf(mu.x, w.x);
+        mu.y = fmaxf(mu.y, w.y);
+      }
+      float2 S = make_float2(0.0f, 0.0f);
+      for (int i = 0; i < m; ++i) {
+        const float2 w = z2[((int64_t)i * C >> 1) + p];
+        const float ex = sexp(__fsub_rn(w.x, mu.x)), ey = sexp(__fsub_rn(w.y, mu.y));
+        S.x = i == 0 ? ex : __fadd_rn(S.x, ex);
+        S.y = i == 0 ? ey : __fadd_rn(S.y, ey);
+      }
+      for (int i = 0; i < m; ++i) {
+        const float2 w = z2[((int64_t)i * C >> 1) + p];
+        const float ax = __fdiv_rn(sexp(__fsub_rn(w.x, mu.x)), S.x);
+        const float ay = __fdiv_rn(sexp(__fsub_rn(w.y, mu.y)), S.y);
+        const float2 xv = load_pair<BF16>(x, (int64_t)i * C, p);
+        v[r].x = __fmaf_rn(ax, xv.x, v[r].x);
+        v[r].y = __fmaf_rn(ay, xv.y, v[r].y);
+      }
+    }
+  }
+  entry_finish<FMT>(v, s, rcos, rsin, P, C, R, out, out_scales, lane);
+}
+
+template <int FMT, bool BF16, bool ZC>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
                 const float* __restrict__ s, const float* __restrict__ rcos,
@@ -195,9 +243,14 @@ compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
   void* o = FMT == CSA_FMT_F32 ? (void*)(reinterpret_cast<float*>(out) + ent * C)
             : FMT == CSA_FMT_MIXED592 ? (void*)(reinterpret_cast<uint8_t*>(out) + ent * kMixRow)
                                       : (void*)(reinterpret_cast<uint8_t*>(out) + ent * (C / 2));
-  compress_entry<FMT, BF16>(reinterpret_cast<const uint8_t*>(x) + tok0 * C * esz, z + tok0, s, rcos, rsin, P, C, R,
-                            m, o, FMT == CSA_FMT_MXFP4 ? out_scales + ent * (C / 32) : nullptr, alpha_s[warp],
-                            lane);
+  if (ZC)
+    compress_entry_channel_logits<FMT, BF16>(reinterpret_cast<const uint8_t*>(x) + tok0 * C * esz, z + tok0 * C, s,
+                                             rcos, rsin, P, C, R, m, o,
+                                             FMT == CSA_FMT_MXFP4 ? out_scales + ent * (C / 32) : nullptr, lane);
+  else
+    compress_entry<FMT, BF16>(reinterpret_cast<const uint8_t*>(x) + tok0 * C * esz, z + tok0, s, rcos, rsin, P, C,
+                              R, m, o, FMT == CSA_FMT_MXFP4 ? out_scales + ent * (C / 32) : nullptr, alpha_s[warp],
+                              lane);
 }
 
 // Decode-time cache maintenance, one CTA per sequence: the new token at
@@ -348,7 +401,7 @@ pack_mixed_kernel(const float* __restrict__ v, int64_t n, uint8_t* __restrict__ 
   pack_mixed_row(x, lane, out + row * kMixRow);
 }
 
-cudaError_t launch_compress(const void* x, bool x_bf16, const float* z, const float* s,
+cudaError_t launch_compress(const void* x, bool x_bf16, const float* z, bool z_per_channel, const float* s,
                             const float* rcos, const float* rsin, int64_t pos0, int B, int64_t T,
                             int C, int R, int m, int fmt, void* out, uint8_t* out_scales,
                             cudaStream_t st) {
@@ -356,9 +409,15 @@ cudaError_t launch_compress(const void* x, bool x_bf16, const float* z, const fl
   const int64_t ents = (int64_t)B * N;
   if (ents == 0) return cudaSuccess;
   const dim3 grid((unsigned)((ents + kWarpsPerBlock - 1) / kWarpsPerBlock)), block(kWarpsPerBlock * 32);
-#define CSA_CK(F, BF)                                                                         \
-  compress_kernel<F, BF><<<grid, block, 0, st>>>(x, z, s, rcos, rsin, pos0, B, T, C, R, m, N, \
-                                                 out, out_scales)
+#define CSA_CK(F, BF)                                                                                 \
+  do {                                                                                                \
+    if (z_per_channel)                                                                                \
+      compress_kernel<F, BF, true><<<grid, block, 0, st>>>(x, z, s, rcos, rsin, pos0, B, T, C, R, m, N, out, \
+                                                           out_scales);                               \
+    else                                                                                              \
+      compress_kernel<F, BF, false><<<grid, block, 0, st>>>(x, z, s, rcos, rsin, pos0, B, T, C, R, m, N, out, \
+                                                            out_scales);                              \
+  } while (0)
   if (fmt == CSA_FMT_F32) {
     if (x_bf16) CSA_CK(CSA_FMT_F32, true); else CSA_CK(CSA_FMT_F32, false);
   } else if (fmt == CSA_FMT_MIXED592) {

@@ -35,7 +35,7 @@ struct AttnArgs {
 
 constexpr size_t kWsHeader = 256;
 
-cudaError_t launch_compress(const void* x, bool x_bf16, const float* z, const float* s,
+cudaError_t launch_compress(const void* x, bool x_bf16, const float* z, bool z_per_channel, const float* s,
                             const float* rcos, const float* rsin, int64_t pos0, int B, int64_t T,
                             int C, int R, int m, int fmt, void* out, uint8_t* out_scales,
                             cudaStream_t st);

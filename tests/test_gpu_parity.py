@@ -548,3 +548,49 @@ def test_indexer_decode_tc_matches_dp4a(csa, monkeypatch, B, N, HI, key_exps, q_
     monkeypatch.delenv("CSA_INDEXER_IMPL")
     np.testing.assert_array_equal(idx_tc.cpu().numpy(), idx_dp.cpu().numpy())
     np.testing.assert_array_equal(sc_tc.cpu().numpy().view(np.uint32), sc_dp.cpu().numpy().view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# per-channel compression logits: bit-exact bytes against the oracle
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("name,T,m,pos0,part,fmt", [
+    ("c2_csa_prefill_8k", 8192 - 3, 4, 4096, "kv", "mixed592"),   # ragged tail, shifted positions
+    ("c4_hca_prefill_64k", 16384 + 100, 128, 0, "kv", "mixed592"),  # HCA ratio
+    ("c2_csa_prefill_8k", 4096, 1, 0, "kv", "mixed592"),           # m = 1: the tokens, scaled
+    ("c2_csa_prefill_8k", 8192, 4, 0, "kI", "mxfp4"),              # FP4 indexer keys
+    ("c1_tiny_csa_prefill", 510, 4, 0, "kv", "f32"),               # fp32 input and output
+])
+def test_compress_channel_logits_bitexact(csa, oracle_mod, name, T, m, pos0, part, fmt):
+    cfg = wl.CONFIGS[name]
+    toks = wl.gen_tokens(cfg, 0, 0, T, parts=(part,))
+    x = toks[part]
+    C = x.shape[1]
+    zc = wl.gen_channel_logits(cfg, 0, C, 0, T)
+    sc = wl.gen_channel_scales(cfg)
+    s = sc["s"] if part == "kv" else sc["sI"]
+    R = 64 if part == "kv" else 0
+    rope_np, rope_dev = ropes(csa, oracle_mod, pos0 + T + 1)
+    dfmt = {"mixed592": csa.FMT_MIXED592, "mxfp4": csa.FMT_MXFP4, "f32": csa.FMT_F32}[fmt]
+    got = csa.compress_kv(act_dev(x, cfg)[None], dev(zc)[None], dev(s), m, dfmt, R, rope_dev if R else None,
+                          pos0=pos0)
+    ref = oracle_mod.compress_kv(widen(x, cfg)[None], zc[None], s, m, fmt, R, pos0, rope_np if R else None)
+    if fmt == "mxfp4":
+        np.testing.assert_array_equal(got[0].cpu().numpy(), ref[0])
+        np.testing.assert_array_equal(got[1].cpu().numpy(), ref[1])
+    elif fmt == "f32":
+        np.testing.assert_array_equal(got.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    else:
+        np.testing.assert_array_equal(got.cpu().numpy(), ref)
+
+
+def test_compress_channel_logits_equal_channels_is_per_token(csa):
+    """On the GPU too: logits repeated over channels store the per-token bytes."""
+    cfg = wl.CONFIGS["c2_csa_prefill_8k"]
+    toks = wl.gen_tokens(cfg, 0, 0, 2048, parts=("kv", "z"))
+    x = act_dev(toks["kv"], cfg)[None]
+    z = dev(toks["z"])[None]
+    s = dev(wl.gen_channel_scales(cfg)["s"])
+    rope = csa.rope_table(2049, 64)
+    a = csa.compress_kv(x, z, s, 4, csa.FMT_MIXED592, 64, rope)
+    b = csa.compress_kv(x, z[..., None].expand(1, 2048, 512).contiguous(), s, 4, csa.FMT_MIXED592, 64, rope)
+    assert torch.equal(a, b)

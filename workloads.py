@@ -172,6 +172,21 @@ def gen_tokens(cfg: Config, b: int, t0: int = 0, t1: int | None = None, seed: in
     return {k: np.concatenate(v) for k, v in out.items()}
 
 
+def gen_channel_logits(cfg: Config, b: int, width: int, t0: int = 0, t1: int | None = None,
+                       seed: int = 0) -> np.ndarray:
+    """Per-token, per-channel compression logits of sequence b, tokens [t0, t1):
+    fp32 [n, width] ~ N(0, z_std^2), drawn in blocks of 4096 tokens like gen_tokens."""
+    t1 = cfg.T if t1 is None else t1
+    blk = 4096
+    parts = []
+    for c in range(t0 // blk, (t1 + blk - 1) // blk):
+        lo, hi = c * blk, min((c + 1) * blk, cfg.T)
+        r = rng_for(seed, cfg.name, "zc", width, b, c)
+        v = r.standard_normal(size=(hi - lo, width), dtype=np.float32) * np.float32(cfg.z_std)
+        parts.append(v[max(t0, lo) - lo:min(t1, hi) - lo])
+    return np.concatenate(parts)
+
+
 def gen_queries(cfg: Config, b: int, q0: int = 0, q1: int | None = None, seed: int = 0) -> dict:
     """Query-side tensors of sequence b, query rows [q0, q1).
 
