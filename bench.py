@@ -453,6 +453,51 @@ def run_config(args, name):
         l2 = "caches resident; each step reads them once (larger than L2 except the HCA-only step)"
         step_desc = "decode_append + indexer_topk + sparse_mqa (CSA) / decode_append + hca_dense_attn (HCA), " \
                     "one CUDA graph per step"
+    elif name == "c2_csa_prefill_128k":
+        cfg = wl.CONFIGS[name]
+        T, W, m, Tc = cfg.T, cfg.W, cfg.m, 8192
+        rope = csa.rope_table(T + 1, 64)
+        sc = wl.gen_channel_scales(cfg)
+        s_d, sI_d = _f_dev(sc["s"], dev), _f_dev(sc["sI"], dev)
+        kv = torch.empty((1, T, cfg.D), dtype=torch.bfloat16, device=dev)
+        kI = torch.empty((1, T, cfg.dI), dtype=torch.bfloat16, device=dev)
+        z = torch.empty((1, T), dtype=torch.float32, device=dev)
+        zI = torch.empty((1, T), dtype=torch.float32, device=dev)
+        q = torch.empty((1, T, cfg.H, cfg.D), dtype=torch.bfloat16, device=dev)
+        qI = torch.empty((1, T, cfg.HI, cfg.dI), dtype=torch.bfloat16, device=dev)
+        w = torch.empty((1, T, cfg.HI), dtype=torch.float32, device=dev)
+        for t0 in range(0, T, Tc):   # seeded inputs, generated chunk by chunk
+            toks = wl.gen_tokens(cfg, 0, t0, t0 + Tc)
+            qry = wl.gen_queries(cfg, 0, t0, t0 + Tc)
+            kv[0, t0:t0 + Tc] = _bf16_dev(toks["kv"], dev)
+            kI[0, t0:t0 + Tc] = _bf16_dev(toks["kI"], dev)
+            z[0, t0:t0 + Tc] = _f_dev(toks["z"], dev)
+            zI[0, t0:t0 + Tc] = _f_dev(toks["zI"], dev)
+            q[0, t0:t0 + Tc] = _bf16_dev(qry["q"], dev)
+            qI[0, t0:t0 + Tc] = _bf16_dev(qry["qI"], dev)
+            w[0, t0:t0 + Tc] = _f_dev(qry["w"], dev)
+            del toks, qry
+        out = torch.empty_like(q)
+        cp = csa.ChunkedPrefill(T, m, cfg.k, W, rope, device=dev)
+        scale = 1.0 / math.sqrt(cfg.D)
+
+        def step():
+            for t0 in range(0, T, Tc):
+                t1 = t0 + Tc
+                cp.run(t0, t1, kv[:, t0:t1], z[:, t0:t1], kI[:, t0:t1], zI[:, t0:t1], s_d, sI_d, q[:, t0:t1],
+                       qI[:, t0:t1], w[:, t0:t1], scale, out=out[:, t0:t1])
+
+        units, unit = float(T), "tokens/s"
+        metric = "CSA prefill tokens/s (1x131072 in chunks of 8192, m=4, top-k 512, window 128, 64 heads, D=512)"
+        t = np.arange(T, dtype=np.int64)
+        keys = np.minimum(cfg.k, (t + 1) // m) + np.minimum(W, t + 1)
+        alg = float(keys.sum()) * cfg.H * 4 * cfg.D
+        roof = {"bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "algorithmic_flops_per_step": alg}
+        l2 = "inputs larger than L2 (q and out 8 GiB each)"
+        layers = [cfg]
+        graph = False
+        step_desc = ("16 chunks of 8192 tokens, each: compress (entries, window rows, keys) + indexer_topk + "
+                     "sparse_mqa against the caches so far; roofline = attention flops over the whole step")
     elif name == "c4_hca_prefill_64k":
         cfg = wl.CONFIGS[name]
         T, W, N, m = cfg.T, cfg.W, cfg.N, cfg.m

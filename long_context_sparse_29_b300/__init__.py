@@ -20,7 +20,7 @@ import torch
 
 from ._lib import CsaError, check, lib
 
-__all__ = ["CsaError", "Workspace", "rope_table", "compress_kv", "kvcache_pack_fp8_bf16",
+__all__ = ["CsaError", "Workspace", "ChunkedPrefill", "rope_table", "compress_kv", "kvcache_pack_fp8_bf16",
            "indexer_topk", "sparse_mqa", "hca_dense_attn", "workspace_size", "LayerCache", "decode_append",
            "DTYPE_F32", "DTYPE_BF16", "FMT_F32", "FMT_MIXED592", "FMT_MXFP4"]
 
@@ -187,6 +187,57 @@ def decode_append(lc: LayerCache, kv, z, t_pos, rope, kI=None, zI=None, s=None, 
                                   _ptr(lc.kI_tail), _ptr(lc.zI_tail), _ptr(lc.cache), lc.nmax, _ptr(lc.kI_codes),
                                   _ptr(lc.kI_scales), _ptr(lc.swa), lc.Ts, lc.W, _ptr(lc.swa_pos0),
                                   _stream(kv.device)))
+
+
+class ChunkedPrefill:
+    """Prefill of one sequence in query chunks against resident caches that
+    grow chunk by chunk (entries [1, N, 592], window rows [1, T, 592], MXFP4
+    indexer keys).  run(t0, t1, ...) stores the chunk's tokens at their
+    positions (csa_compress_kv: entries, window rows with m = 1, keys), then
+    the chunk's queries select among and attend over everything visible so
+    far (csa_indexer_topk, csa_sparse_mqa on views of the caches that end at
+    the chunk's last visible entry / start at its first window token).  Each
+    step is one library call; nothing is computed here."""
+
+    def __init__(self, T: int, m: int, k: int, W: int, rope, C: int = 512, CI: int = 64, R: int = 64,
+                 device="cuda"):
+        dev = torch.device(device)
+        self.T, self.m, self.k, self.W, self.C, self.CI, self.R, self.rope = T, m, k, W, C, CI, R, rope
+        N = T // m
+        self.cache = torch.zeros((1, N, MIXED_ROW), dtype=torch.uint8, device=dev)
+        self.swa = torch.zeros((1, T, MIXED_ROW), dtype=torch.uint8, device=dev)
+        self.kc = torch.zeros((1, N, CI // 2), dtype=torch.uint8, device=dev)
+        self.ks = torch.zeros((1, N, CI // 32), dtype=torch.uint8, device=dev)
+        self.q_pos = torch.arange(T, dtype=torch.int64, device=dev)[None]
+        self.ws_ix, self.ws_attn = Workspace(dev), Workspace(dev)
+        self._pos0 = {}
+        self._idx = None
+
+    def _window_start(self, t0: int):
+        lo = max(0, t0 - self.W + 1)   # the first window token of query t0
+        if lo not in self._pos0:
+            self._pos0[lo] = torch.full((1,), lo, dtype=torch.int64, device=self.cache.device)
+        return lo, self._pos0[lo]
+
+    def run(self, t0: int, t1: int, kv, z, kI, zI, s, sI, q, qI, w, scale: float, out=None):
+        """Tokens and queries [t0, t1) (t0 a multiple of m; chunk tensors [1, t1 - t0, ...])."""
+        m = self.m
+        if t0 % m or t1 <= t0 or t1 > self.T:
+            raise CsaError(f"chunk [{t0}, {t1}) must start at a multiple of m = {m} and lie in [0, {self.T}]")
+        e0, e1 = t0 // m, t1 // m
+        compress_kv(kv, z, s, m, FMT_MIXED592, self.R, self.rope, pos0=t0, out=self.cache[:, e0:e1])
+        compress_kv(kv, z, None, 1, FMT_MIXED592, self.R, self.rope, pos0=t0, out=self.swa[:, t0:t1])
+        compress_kv(kI, zI, sI, m, FMT_MXFP4, 0, out=self.kc[:, e0:e1], out_scales=self.ks[:, e0:e1])
+        n = t1 - t0
+        if self._idx is None or self._idx.shape[1] < n:
+            self._idx = torch.empty((1, n, self.k), dtype=torch.int32, device=self.cache.device)
+        idx = self._idx[:, :n]
+        qp = self.q_pos[:, t0:t1]
+        indexer_topk(qI, w, self.kc[:, :e1], self.ks[:, :e1], qp, e1, m, self.k, scores=False, idx_out=idx,
+                     ws=self.ws_ix)
+        lo, pos0 = self._window_start(t0)
+        return sparse_mqa(q, qp, self.cache[:, :e1], m, idx, self.swa[:, lo:t1], pos0, self.W, scale, self.rope,
+                          self.R, out=out, ws=self.ws_attn)
 
 
 def kvcache_pack_fp8_bf16(v, out=None):

@@ -594,3 +594,58 @@ def test_compress_channel_logits_equal_channels_is_per_token(csa):
     a = csa.compress_kv(x, z, s, 4, csa.FMT_MIXED592, 64, rope)
     b = csa.compress_kv(x, z[..., None].expand(1, 2048, 512).contiguous(), s, 4, csa.FMT_MIXED592, 64, rope)
     assert torch.equal(a, b)
+
+
+# --------------------------------------------------------------------------
+# chunked prefill against a resident cache (the 128K configuration's inputs)
+# --------------------------------------------------------------------------
+def test_chunked_prefill_equals_one_shot_and_oracle(csa, oracle_mod):
+    """The first 16384 tokens of the 128K prefill in 4 chunks of 4096: the
+    caches and the outputs equal one call over all tokens, byte for byte, and
+    sampled rows of the last chunk match the oracle (its own caches and
+    top-k) within the attention tolerance."""
+    cfg = wl.CONFIGS["c2_csa_prefill_128k"]
+    T, Tc, m = 16384, 4096, cfg.m
+    toks = wl.gen_tokens(cfg, 0, 0, T)
+    qry = wl.gen_queries(cfg, 0, 0, T)
+    sc = wl.gen_channel_scales(cfg)
+    rope_np, rope_dev = ropes(csa, oracle_mod, T + 1)
+    kv, z = dev_bf16(toks["kv"])[None], dev(toks["z"])[None]
+    kI, zI = dev_bf16(toks["kI"])[None], dev(toks["zI"])[None]
+    s, sI = dev(sc["s"]), dev(sc["sI"])
+    q, qI, w = dev_bf16(qry["q"])[None], dev_bf16(qry["qI"])[None], dev(qry["w"])[None]
+    scale = softmax_scale(cfg)
+    # one call over all tokens
+    cache = csa.compress_kv(kv, z, s, m, csa.FMT_MIXED592, cfg.R, rope_dev)
+    swa = csa.compress_kv(kv, z, None, 1, csa.FMT_MIXED592, cfg.R, rope_dev)
+    kc, ks = csa.compress_kv(kI, zI, sI, m, csa.FMT_MXFP4, 0)
+    q_pos = torch.arange(T, dtype=torch.int64, device="cuda")[None]
+    idx = csa.indexer_topk(qI, w, kc, ks, q_pos, T // m, m, cfg.k, scores=False)
+    out1 = csa.sparse_mqa(q, q_pos, cache, m, idx, swa, dev(np.zeros(1, np.int64)), cfg.W, scale, rope_dev, cfg.R)
+    # the same in chunks
+    cp = csa.ChunkedPrefill(T, m, cfg.k, cfg.W, rope_dev)
+    out2 = torch.empty_like(q)
+    for t0 in range(0, T, Tc):
+        t1 = t0 + Tc
+        cp.run(t0, t1, kv[:, t0:t1], z[:, t0:t1], kI[:, t0:t1], zI[:, t0:t1], s, sI, q[:, t0:t1], qI[:, t0:t1],
+               w[:, t0:t1], scale, out=out2[:, t0:t1])
+    torch.cuda.synchronize()
+    assert torch.equal(cp.cache, cache) and torch.equal(cp.swa, swa)
+    assert torch.equal(cp.kc, kc) and torch.equal(cp.ks, ks)
+    assert torch.equal(out2, out1)
+    # sampled rows of the last chunk against the oracle
+    rows = np.array([T - Tc, T - Tc + 1, T - 1000, T - 129, T - 2, T - 1])
+    xw = widen(toks["kv"], cfg)[None]
+    ocache = oracle_mod.compress_kv(xw, toks["z"][None], sc["s"], m, "mixed592", cfg.R, 0, rope_np)
+    oswa = oracle_mod.compress_kv(xw, toks["z"][None], None, 1, "mixed592", cfg.R, 0, rope_np)
+    okeys = oracle_mod.compress_kv(widen(toks["kI"], cfg)[None], toks["zI"][None], sc["sI"], m, "mxfp4", 0)
+    qp = np.arange(T, dtype=np.int64)[None]
+    oidx, _ = oracle_mod.indexer_topk(widen(qry["qI"], cfg)[rows][None], qry["w"][rows][None], okeys,
+                                      qp[:, rows], T // m, m, cfg.k)
+    np.testing.assert_array_equal(idx[0, rows].cpu().numpy(), oidx[0])
+    oout, _, bad = oracle_mod.attention(widen(qry["q"], cfg)[rows][None], qp[:, rows], ocache, T // m, m, oidx, oswa,
+                                        np.zeros(1, np.int64), cfg.W, scale, rope_np, cfg.R,
+                                        oracle_mod.FMT_MIXED592)
+    assert bad == 0
+    got = out2[0, rows].float().cpu().numpy()
+    assert max_rel_err(got, oout[0]) <= tol(cfg)

@@ -79,6 +79,10 @@ CONFIGS: dict[str, Config] = {
     "c2_csa_prefill_8k": _c(name="c2_csa_prefill_8k", kind="csa_prefill", B=1, T=8192, Tq=8192,
                             m=4, k=512, W=128, H=64, D=512, R=64, HI=16, dI=64, fp32=False,
                             z_std=0.5),
+    # CSA prefill of 1 x 131072 tokens, run in query chunks against the growing cache.
+    "c2_csa_prefill_128k": _c(name="c2_csa_prefill_128k", kind="csa_prefill", B=1, T=131072, Tq=131072,
+                              m=4, k=512, W=128, H=64, D=512, R=64, HI=16, dI=64, fp32=False,
+                              z_std=0.5),
     # CSA decode, batch 32 at 128K context.
     "c3_csa_decode_128k": _c(name="c3_csa_decode_128k", kind="csa_decode", B=32, T=131072, Tq=1,
                              m=4, k=1024, W=128, H=64, D=512, R=64, HI=16, dI=64, fp32=False,
