@@ -49,6 +49,7 @@ namespace {
 constexpr int kH = 64;
 constexpr int kD = 512;
 constexpr int kTile = 64;
+constexpr int kMaxSplits = 256;   // split-K partial states per row (the combine stages their statistics)
 constexpr int kThreads = 10 * 32;
 constexpr int kMmaWarp = 8;       // QK^T issue, query loads, TMEM owner
 constexpr int kPvWarp = 9;        // PV issue
@@ -1015,26 +1016,37 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
 // and lse: one CTA per pair, thread t owns dims 2t and 2t + 1 (a RoPE pair when
 // 2t >= 448); the partial states are weighted by 2^(m_s - max m) in split order.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const Params p) {
+  __shared__ float m_s[kMaxSplits], l_s[kMaxSplits];
   const int64_t row = blockIdx.x;
   const int h = blockIdx.y;
   const int tid = threadIdx.x;
   const int64_t t = p.q_pos[row];
   const bool t_ok = t >= 0 && t < p.rope_rows;
   const int d0 = 2 * tid;
-  const float* ml = p.part_ml + (row * p.nsplit * kH + h) * 2;   // split s at + s * kH * 2
+  const int ns = p.nsplit;
+  // the splits' running max and sum, read once by the CTA
+  const float* ml = p.part_ml + (row * ns * kH + h) * 2;   // split s at + s * kH * 2
+  for (int s = tid; s < ns; s += 256) {
+    m_s[s] = ml[s * kH * 2];
+    l_s[s] = ml[s * kH * 2 + 1];
+  }
+  __syncthreads();
   float M = -INFINITY;
-  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, ml[s * kH * 2]);
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, m_s[s]);
   float L = 0.0f, o0 = 0.0f, o1 = 0.0f;
   if (M != -INFINITY) {
-    const float* po = p.part_o + row * p.nsplit * (int64_t)(kH * kD) + h * kD + d0;
-    for (int s = 0; s < p.nsplit; ++s) {
-      const float mi = ml[s * kH * 2];
-      if (mi == -INFINITY) continue;
-      const float w = exp2f(mi - M);
-      L += w * ml[s * kH * 2 + 1];
-      const float2 v = *reinterpret_cast<const float2*>(po + s * (int64_t)(kH * kD));
-      o0 += w * v.x;
-      o1 += w * v.y;
+    const float* po = p.part_o + row * ns * (int64_t)(kH * kD) + h * kD + d0;
+    // in split order as before; the partial rows' loads of 8 splits issued together
+#pragma unroll 8
+    for (int s = 0; s < ns; ++s) {
+      const float mi = m_s[s];
+      if (mi != -INFINITY) {
+        const float w = exp2f(mi - M);
+        L += w * l_s[s];
+        const float2 v = *reinterpret_cast<const float2*>(po + s * (int64_t)(kH * kD));
+        o0 += w * v.x;
+        o1 += w * v.y;
+      }
     }
   }
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
@@ -1070,8 +1082,11 @@ int choose_splits(int64_t rows, int64_t max_keys) {
   const int sms = num_sms();
   if (rows >= sms) return 1;
   const int64_t tiles = (max_keys + kTile - 1) / kTile;
-  int64_t s = (sms + rows - 1) / rows;
+  // rows x splits at most one item per SM: a second round for a few items
+  // would double the time of the call
+  int64_t s = sms / rows;
   if (s > tiles) s = tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
   return (int)(s < 1 ? 1 : s);
 }
 
