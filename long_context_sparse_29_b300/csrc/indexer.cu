@@ -360,7 +360,7 @@ scores_f32_kernel(const float* __restrict__ qI, const float* __restrict__ w,
 // top-k lies in their union: the order is total), then one CTA per row
 // selects among the chunk winners.
 // ---------------------------------------------------------------------------
-constexpr int kTopkThreads = 512;        // CTA of the two-stage kernels (few long rows)
+constexpr int kTopkThreads = 1024;       // CTA of the two-stage kernels (few long rows)
 constexpr int kTopkRowThreads = 128;     // CTA of the one-row kernel (many rows of at most kTkChunk)
 constexpr int kTkChunk = 8192;
 constexpr size_t kTkStageMax = 200 * 1024;   // dynamic shared memory for staged candidates

@@ -353,9 +353,11 @@ ix_scores_tc_kernel(const IxParams p, const __grid_constant__ CUtensorMap tm_q, 
               const int j = 16 * half + i;
               const int x0 = (int)((ek0w[j >> 2] >> (8 * (j & 3))) & 0xffu);
               const int x1 = (int)((ek1w[j >> 2] >> (8 * (j & 3))) & 0xffu);
-              const float d = __fadd_rn(__fmul_rn(__uint_as_float(P0[i]), __int_as_float(x0 * (1 << 23) + c0)),
+              // both products are exact here, so one fma rounds their sum once, as the add did;
+              // relu by fmaxf: a -0 can only add a zero product to a sum that starts at +0
+              const float d = __fmaf_rn(__uint_as_float(P0[i]), __int_as_float(x0 * (1 << 23) + c0),
                                         __fmul_rn(__uint_as_float(P1[i]), __int_as_float(x1 * (1 << 23) + c1)));
-              sc[j] = __fmaf_rn(wh, d > 0.0f ? d : 0.0f, sc[j]);
+              sc[j] = __fmaf_rn(wh, fmaxf(d, 0.0f), sc[j]);
             }
           } else {
 #pragma unroll
@@ -596,9 +598,9 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
       for (int h = 0; h < kDtHeads; ++h) {
         if (h < HI) {
           const int4 hx = ms->hx[h];
-          const float d = __fadd_rn(__fmul_rn(__uint_as_float(P[h]), __int_as_float(hx.x + X0)),
+          const float d = __fmaf_rn(__uint_as_float(P[h]), __int_as_float(hx.x + X0),
                                     __fmul_rn(__uint_as_float(P[16 + h]), __int_as_float(hx.y + X1)));
-          s = __fmaf_rn(__int_as_float(hx.z), d > 0.0f ? d : 0.0f, s);
+          s = __fmaf_rn(__int_as_float(hx.z), fmaxf(d, 0.0f), s);
         }
       }
     } else {
