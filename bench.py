@@ -100,6 +100,23 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
+# ranks (torchrun, N > 1): each rank runs its own sequence; the times are
+# reduced by max, the value counts every rank's tokens
+# --------------------------------------------------------------------------
+def max_over_ranks(values, dist, device):
+    """The per-rank times, each replaced by its maximum over the ranks."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def aggregate_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job throughput: all ranks' tokens over the slowest rank's step."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
+# --------------------------------------------------------------------------
 # inputs
 # --------------------------------------------------------------------------
 def host_inputs(seed: int):
@@ -213,16 +230,14 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     if dist:
-        t = torch.tensor([ms, e2e_ms, attn_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms, attn_ms = (float(x) for x in t.tolist())
+        ms, e2e_ms, attn_ms = max_over_ranks([ms, e2e_ms, attn_ms], dist, dev)
     pk = peaks()
     af = attn_flops(CFG)
     achieved = af / (attn_ms * 1e-3) / 1e12
     peak = pk["bf16_tflops"]
     ms_step = ms / args.steps
     res = {
-        "metric": METRIC, "value": world * T / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": aggregate_tokens_per_s(world, T, ms_step), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": CFG.name, "B": 1, "T": T, "m": m, "N": N, "k": k, "W": W, "H": CFG.H,
@@ -232,7 +247,7 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ATTN_TRAFFIC,
                      "peak_src": f"bf16 dense, {pk['src']} (burst)",
                      "algorithmic_flops_per_launch": af, "avg_launch_ms": attn_ms},
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": aggregate_tokens_per_s(world, T, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk.summary(),
