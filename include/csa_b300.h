@@ -235,8 +235,14 @@ int csa_decode_append(const void *kv, const float *z, const void *kI, const floa
  * once to fp32 (FP4) or the fma chain over dI from +0 (fp32).  Candidates:
  * j < N with (j + 1) m - 1 <= t.  Order: score descending, then index
  * ascending.
- * Errors: INVALID_ARG, UNSUPPORTED (dI not 32/64, HI > 64, k > 4096),
- * CUDA; needs csa_workspace_size(CSA_OP_INDEXER_TOPK, ...) bytes of ws.
+ * Errors: INVALID_ARG (sizes, NULL pointers, ws smaller than the scores or
+ * not 256-byte aligned); UNSUPPORTED (k outside 1..4096; FP4: dI != 64 or
+ * HI > 32; fp32: dI > 64, HI > 32 or HI * dI > 512); CUDA.
+ * Workspace: csa_workspace_size(CSA_OP_INDEXER_TOPK, ...) bytes give every
+ * path (the tensor-core prefill scores, the two-stage top-k of few long
+ * rows); the status block plus B * Tq * N fp32 scores is the least accepted,
+ * and then prefill scores run on the CUDA cores and the top-k one CTA per
+ * row.  Same indices and scores on every path.
  */
 int csa_indexer_topk(const void *qI, int qI_dtype, const float *w, const void *kI,
                      const uint8_t *kI_scales, int kI_fmt, const int64_t *q_pos, int B,
