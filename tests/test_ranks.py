@@ -58,3 +58,21 @@ def test_two_gloo_ranks_reduce_by_max():
         assert got == [2.5, 10.0, 0.5]
         assert value == pytest.approx(2 * 8192 / 2.5e-3)
     assert res[1][2] is None   # the reference arm does no work on rank 1
+
+
+def test_reference_arm_line_on_cpu():
+    """The reference arm (the oracle on the host cores, a bounded sample of the
+    8K workload per step) prints the benchmark's line: same metric and unit,
+    impl = reference, a cpu_baseline describing the run, and an e2e object
+    with no host-device copies."""
+    import types
+    sys.path.insert(0, ROOT)
+    import bench
+    res = bench.run_reference(types.SimpleNamespace(steps=1, warmup=0), 0, 1)
+    assert res["impl"] == "reference" and res["metric"] == bench.METRIC and res["unit"] == "tokens/s"
+    assert res["higher_is_better"] is True and res["value"] > 0
+    cb = res["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == res["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert res["e2e"] == {"value": res["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
+    assert res["config"]["workload"] == "c2_csa_prefill_8k"
