@@ -279,8 +279,21 @@ decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restri
   extern __shared__ __align__(16) uint8_t ring_s[];   // closing block: m rows of C, then m rows of CI (bf16)
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ float rope_s[2][32];            // cos, sin of position t (R = 64)
+  __shared__ float s_s[512], sI_s[64];       // the channel scales
   const int64_t t = t_pos[b];
+  const int64_t old0 = W > 0 ? swa_pos0[b] : 0;   // read with t, before anything waits on either
   if (t < 0 || t >= rope_rows) return;   // no RoPE row for it: nothing is stored
+  // the RoPE row of t and the channel scales, read into shared memory now:
+  // the window row and the entry use them only at the ends of their chains
+  for (int i = tid; i < (R >> 1); i += blockDim.x) {
+    rope_s[0][i] = rcos[t * (R >> 1) + i];
+    rope_s[1][i] = rsin[t * (R >> 1) + i];
+  }
+  if (s)
+    for (int i = tid; i < C; i += blockDim.x) s_s[i] = s[i];
+  if (kI && sI)
+    for (int i = tid; i < CI; i += blockDim.x) sI_s[i] = sI[i];
   const int slot = (int)(t % m);
   const bool closes = (t + 1) % m == 0 && (t + 1) / m - 1 < nmax;
   if (closes) {
@@ -312,9 +325,8 @@ decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restri
   }
   // ---- window: slide when the row is past the buffer ----
   if (W > 0) {
-    const int64_t old0 = swa_pos0[b];
     const bool slide = t - old0 >= Ts;
-    __syncthreads();   // every thread has read swa_pos0[b]
+    __syncthreads();   // every thread has read swa_pos0[b]; the RoPE row and scales are in
     if (slide) {
       // rows of tokens t - W + 1 .. t - 1 move to rows 0 .. W - 2; source rows
       // are >= Ts - W + 1 >= W + 1 (Ts >= 2 W): no overlap.  Rows past the
@@ -333,7 +345,7 @@ decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restri
     const int64_t row = slide ? (int64_t)W - 1 : t - old0;
     if (warp == 0 && row >= 0 && row < Ts) {   // the token itself: m = 1, no channel scale, RoPE at t
       const float zz = 0.0f;
-      compress_entry<CSA_FMT_MIXED592, true>(kv + (int64_t)b * C, &zz, nullptr, rcos, rsin, t, C, R, 1,
+      compress_entry<CSA_FMT_MIXED592, true>(kv + (int64_t)b * C, &zz, nullptr, rope_s[0], rope_s[1], 0, C, R, 1,
                                              swa + ((int64_t)b * Ts + row) * kMixRow, nullptr, alpha_s[0], lane);
     }
   }
@@ -380,11 +392,12 @@ decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restri
         v[r] = p < np ? acc_s[off + p] : make_float2(0.0f, 0.0f);
       }
       if (key)
-        entry_finish<CSA_FMT_MXFP4>(v, sI, rcos, rsin, t, CI, 0, kI_codes + ((int64_t)b * nmax + j) * (CI / 2),
+        entry_finish<CSA_FMT_MXFP4>(v, sI ? sI_s : nullptr, rope_s[0], rope_s[1], 0, CI, 0,
+                                    kI_codes + ((int64_t)b * nmax + j) * (CI / 2),
                                     kI_scales + ((int64_t)b * nmax + j) * (CI / 32), lane);
       else
-        entry_finish<CSA_FMT_MIXED592>(v, s, rcos, rsin, t, C, R, cache + ((int64_t)b * nmax + j) * kMixRow,
-                                       nullptr, lane);
+        entry_finish<CSA_FMT_MIXED592>(v, s ? s_s : nullptr, rope_s[0], rope_s[1], 0, C, R,
+                                       cache + ((int64_t)b * nmax + j) * kMixRow, nullptr, lane);
     }
   }
 }
