@@ -106,3 +106,31 @@ def test_binding_requires_cuda_tensors(csa):
     x = torch.zeros(1, 8, 512, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         csa.compress_kv(x, torch.zeros(1, 8), None, 4, csa.FMT_MIXED592, 64)
+
+
+def test_decode_append_and_channel_logits_validation(csa):
+    """Every case is refused on the host (or has nothing to do): no launch."""
+    L = csa._lib.lib()
+    P = ctypes.c_void_p
+    ok16 = P(16)   # stand-in pointers, never dereferenced: each call below fails validation first
+
+    def append(kv=ok16, kI=None, C=512, R=64, CI=0, m=4, B=1, Ts=64, W=32, nmax=4):
+        return L.csa_decode_append(kv, ok16, kI, ok16 if kI else None, None, None, ok16, ok16, 100, ok16, B, C, R,
+                                   CI, m, ok16, ok16, ok16 if kI else None, ok16 if kI else None, ok16, nmax,
+                                   ok16 if kI else None, ok16 if kI else None, ok16, Ts, W, ok16, None)
+
+    assert append(m=0) == -1 and b"bad sizes" in L.csa_last_error()
+    assert append(m=129) == -1
+    assert append(C=256) == -2
+    assert append(R=32) == -2
+    assert append(kI=ok16, CI=48) == -2
+    assert append(Ts=40, W=32) == -1 and b"Ts" in L.csa_last_error()
+    assert append(kv=None) == -1 and b"NULL" in L.csa_last_error()
+    assert append(kv=P(24)) == -1 and b"aligned" in L.csa_last_error()
+    assert append(kv=None, B=0) == 0      # nothing to append
+    r = L.csa_compress_kv_channel_logits(None, 1, None, None, None, None, 0, 0, 1, 8, 512, 64, 4, 1, None, None,
+                                         None)
+    assert r == -1 and b"csa_compress_kv_channel_logits" in L.csa_last_error()
+    r = L.csa_compress_kv_channel_logits(None, 1, None, None, None, None, 0, 0, 1, 1024, 512, 64, 256, 1, None,
+                                         None, None)
+    assert r == -2
