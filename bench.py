@@ -468,6 +468,10 @@ def run_config(args, name):
         l2 = "caches resident; each step reads them once (larger than L2 except the HCA-only step)"
         step_desc = "decode_append + indexer_topk + sparse_mqa (CSA) / decode_append + hca_dense_attn (HCA), " \
                     "one CUDA graph per step"
+        # kernels per step: CSA layer 8 (append; scores, top-k stages 1 and 2;
+        # row prep, row gather, attention, split merge), HCA layer 5 (append;
+        # row prep, row gather, attention, split merge)
+        launches = sum(8 if c.k else 5 for c in layers)
     elif name == "c2_csa_prefill_128k":
         cfg = wl.CONFIGS[name]
         T, W, m, Tc = cfg.T, cfg.W, cfg.m, 8192
@@ -513,6 +517,7 @@ def run_config(args, name):
         graph = False
         step_desc = ("16 chunks of 8192 tokens, each: compress (entries, window rows, keys) + indexer_topk + "
                      "sparse_mqa against the caches so far; roofline = attention flops over the whole step")
+        launches = 16 * LAUNCHES_PER_STEP   # the 8K step's 11 kernels per chunk
     elif name == "c4_hca_prefill_64k":
         cfg = wl.CONFIGS[name]
         T, W, N, m = cfg.T, cfg.W, cfg.N, cfg.m
@@ -546,6 +551,7 @@ def run_config(args, name):
         layers = [cfg]
         graph = False
         step_desc = "compress (entries and window rows) + hca_dense_attn"
+        launches = 6   # 2 compress; row prep, cache and window expansion, attention
     else:
         raise SystemExit(f"unknown config {name}")
     for _ in range(args.warmup):
@@ -585,7 +591,7 @@ def run_config(args, name):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": name, "B": cfg0.B, "T": cfg0.T, "N": cfg0.N, "m": cfg0.m, "k": cfg0.k,
                        "W": cfg0.W, "H": cfg0.H, "D": cfg0.D, "l2": l2, "step": step_desc},
-            "roofline": roof, "clocks": clk.summary()}
+            "roofline": roof, "gpu_launches": launches * args.steps, "clocks": clk.summary()}
 
 
 def main():
