@@ -459,7 +459,7 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DtMisc* ms = reinterpret_cast<DtMisc*>(sm + kDtMiscOff);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int64_t row = blockIdx.y;
   const int64_t b = row / Tq;
   const int64_t nv = visible(q_pos[row], m, N);
