@@ -297,6 +297,18 @@ def _full_step_seconds(t_comp, t_rows, n_rows):
     return t_comp + t_rows * CFG.T / n_rows
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo; "unknown" elsewhere)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(h, budget_s=20.0):
     """Time the oracle on a bounded sample: compression of all tokens, then
     top-k and attention for a seeded set of query rows; scaled to tokens/s."""
@@ -314,6 +326,7 @@ def cpu_baseline(h, budget_s=20.0):
         tc, tr = oracle_sample(h, rows, rope)
     full = _full_step_seconds(tc, tr, n_rows)
     return {"value": CFG.T / full, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
+            "cpu": host_cpu_model(),
             "sample": f"compression of all {CFG.T} tokens ({tc:.2f} s) + top-k and sparse MQA for "
                       f"{n_rows} seeded query rows ({tr:.2f} s); rows scaled to {CFG.T}"}
 
@@ -343,6 +356,7 @@ def run_reference(args, rank, world):
         "config": {"workload": CFG.name, "B": 1, "T": CFG.T, "m": CFG.m, "N": CFG.N, "k": CFG.k,
                    "W": CFG.W, "H": CFG.H, "D": CFG.D, "HI": CFG.HI, "dI": CFG.dI},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
+                         "cpu": host_cpu_model(),
                          "sample": f"per step: compression of all {CFG.T} tokens + top-k and sparse MQA "
                                    f"for {n_rows} seeded query rows, row time scaled to {CFG.T} rows"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
