@@ -134,3 +134,12 @@ def test_decode_append_and_channel_logits_validation(csa):
     r = L.csa_compress_kv_channel_logits(None, 1, None, None, None, None, 0, 0, 1, 1024, 512, 64, 256, 1, None,
                                          None, None)
     assert r == -2
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """No fallback: with the CUDA library absent, the first call raises."""
+    from long_context_sparse_29_b300 import _lib
+    monkeypatch.setattr(_lib, "SO_PATH", os.path.join(ROOT, "no_such_dir", "libcsa_b300.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.lib()
