@@ -114,6 +114,17 @@ int csa_status_reset(void *ws, void *stream);
 int csa_status_read(const void *ws, void *stream, uint32_t *flags);
 
 /*
+ * csa_selftest_wait_timeout: exercise the expiry of the library's bounded
+ * device waits (failure detection).  One CTA waits at most `polls` times on
+ * an mbarrier phase that nothing completes, gives up and sets
+ * CSA_FLAG_TIMEOUT in ws, as any kernel of the library does when one of its
+ * waits expires; csa_status_read then reports CSA_ERR_TIMEOUT.  No fault and
+ * no hang: the context stays usable.  Async on stream.
+ * Errors: INVALID_ARG (NULL ws, polls outside [1, 2^20]); CUDA.
+ */
+int csa_selftest_wait_timeout(void *ws, uint32_t polls, void *stream);
+
+/*
  * kvcache_pack_fp8_bf16: pack n post-RoPE rows of 512 fp32 channels
  * (v, device [n, 512]) into the mixed FP8/BF16 layout (out, device
  * [n, 592] bytes, CSA_FMT_MIXED592 above).  [XM] key technical details

@@ -107,6 +107,12 @@ def _ws(ws, device):
     return _default_ws[key]
 
 
+def selftest_wait_timeout(ws: Workspace, polls: int = 1000) -> None:
+    """Make one bounded device wait expire on purpose; ws's timeout flag is
+    then set (see csa_selftest_wait_timeout)."""
+    check(lib().csa_selftest_wait_timeout(_ptr(ws.buf), int(polls), _stream(ws.device)))
+
+
 def rope_table(P: int, R: int = 64, base: float = 10000.0, device="cuda"):
     """cos/sin tables fp32 [P, R/2] on `device` (built on the host by the library)."""
     c = np.empty((P, R // 2), np.float32)

@@ -22,6 +22,7 @@ SIGNATURES = {
     "csa_last_error": (ctypes.c_char_p, []),
     "csa_version": (ctypes.c_char_p, []),
     "csa_rope_table": (I32, [I64, I32, F64, P, P]),
+    "csa_selftest_wait_timeout": (I32, [P, ctypes.c_uint32, P]),
     "csa_workspace_size": (I64, [I32, I32, I64, I64, I32, I32, I32, I64, I64]),
     "csa_status_reset": (I32, [P, P]),
     "csa_status_read": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32)]),

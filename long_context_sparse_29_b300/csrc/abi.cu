@@ -174,6 +174,13 @@ int csa_status_reset(void* ws, void* stream) {
   return cuda_result(cudaMemsetAsync(ws, 0, sizeof(csa::Status), as_stream(stream)), "csa_status_reset");
 }
 
+int csa_selftest_wait_timeout(void* ws, uint32_t polls, void* stream) {
+  const char* nm = "csa_selftest_wait_timeout";
+  if (!ws) return fail(CSA_ERR_INVALID_ARG, "%s: NULL ws", nm);
+  if (polls < 1 || polls > (1u << 20)) return fail(CSA_ERR_INVALID_ARG, "%s: polls must be in [1, 2^20]", nm);
+  return cuda_result(csa::launch_wait_selftest(ws, polls, as_stream(stream)), nm);
+}
+
 int csa_status_read(const void* ws, void* stream, uint32_t* flags) {
   if (!ws || !flags) return fail(CSA_ERR_INVALID_ARG, "csa_status_read: NULL argument");
   csa::Status st;

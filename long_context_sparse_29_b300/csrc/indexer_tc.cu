@@ -714,6 +714,24 @@ cudaError_t launch_indexer_scores_tc(const void* qI, const float* w, const uint8
   return cudaGetLastError();
 }
 
+// Failure-detection self-test: one thread waits on an mbarrier whose phase
+// nothing completes, with the same bounded wait every kernel here uses, and
+// records the expiry in the workspace's status flags.
+__global__ void wait_selftest_kernel(void* ws, uint32_t polls) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, polls)) flag_timeout(ws);
+}
+
+cudaError_t launch_wait_selftest(void* ws, uint32_t polls, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(ws, polls);
+  return cudaGetLastError();
+}
+
 bool decode_tc_applies(int64_t Tq, int HI, int dI, int64_t N) {
   return Tq <= 4 && dI == 64 && HI >= 1 && HI <= kDtHeads && N >= 8 * kDtThreads * 8;
 }

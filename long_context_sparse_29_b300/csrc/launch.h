@@ -69,6 +69,9 @@ inline int resident_ctas(const void* kernel, int threads, size_t dyn_smem) {
   return n < 1 ? 1 : n;
 }
 
+// a bounded device wait that expires on purpose (failure-detection self-test)
+cudaError_t launch_wait_selftest(void* ws, uint32_t polls, cudaStream_t st);
+
 // decode scoring on the tensor cores (few query rows, long entry lists)
 bool decode_tc_applies(int64_t Tq, int HI, int dI, int64_t N);
 cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const uint8_t* kc, const uint8_t* ks,
