@@ -143,3 +143,23 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         _lib.lib()
+
+
+def test_calls_with_nothing_to_do_return_ok(csa):
+    """Empty work is not an error and launches nothing: no complete block, no
+    queries, no sequences.  (Pointers are NULL; the workspace pointer is
+    only checked for alignment, never used.)"""
+    L = csa._lib.lib()
+    ws = ctypes.c_void_p(256)
+    # T < m: no complete block
+    assert L.csa_compress_kv(None, 1, None, None, None, None, 0, 0, 1, 3, 512, 64, 4, 1, None, None, None) == 0
+    assert L.csa_compress_kv_channel_logits(None, 1, None, None, None, None, 0, 0, 1, 3, 512, 64, 4, 1, None,
+                                            None, None) == 0
+    # no queries
+    assert L.csa_indexer_topk(None, 1, None, None, None, 2, None, 1, 0, 16, 64, 2048, 4, 512, None, None, None,
+                              0, None) == 0
+    assert L.csa_sparse_mqa(None, 1, None, 1, 0, 64, 512, 64, 1, None, 0, 4, None, 0, None, None, 0, 0, 0.1,
+                            None, None, 1, None, None, ws, 1 << 20, None) == 0
+    # no sequences
+    assert L.hca_dense_attn(None, 1, None, 0, 5, 64, 512, 64, 1, None, 0, 128, None, None, 0, 0, 0.1, None, None,
+                            1, None, None, ws, 1 << 20, None) == 0
