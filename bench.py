@@ -131,6 +131,13 @@ def host_inputs(seed: int):
 BF16_KEYS = ("kv", "kI", "q", "qI")
 
 
+def bench_config(world: int) -> dict:
+    """The workload description both arms print (identical dicts)."""
+    return {"workload": CFG.name, "B": 1, "T": CFG.T, "m": CFG.m, "N": CFG.N, "k": CFG.k, "W": CFG.W,
+            "H": CFG.H, "D": CFG.D, "HI": CFG.HI, "dI": CFG.dI, "parallelism": f"replicas{world}",
+            "l2": "inputs larger than L2 (q and out 512 MiB each per step)"}
+
+
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
@@ -235,25 +242,44 @@ def run_ours(args, rank, world, local_rank):
     af = attn_flops(CFG)
     achieved = af / (attn_ms * 1e-3) / 1e12
     peak = pk["bf16_tflops"]
+    fp8_peak = 2.0 * peak   # dense FP8 = the measured bf16 burst x the nominal 2x ratio
     ms_step = ms / args.steps
+    step_flops = af + indexer_flops(CFG)
     res = {
         "metric": METRIC, "value": aggregate_tokens_per_s(world, T, ms_step), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": CFG.name, "B": 1, "T": T, "m": m, "N": N, "k": k, "W": W, "H": CFG.H,
-                   "D": CFG.D, "HI": CFG.HI, "dI": CFG.dI, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2 (q and out 512 MiB each per step)"},
+        "config": bench_config(world),
         "roofline": {"kernel": "sparse_mqa", "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ATTN_TRAFFIC,
                      "peak_src": f"bf16 dense, {pk['src']} (burst)",
                      "algorithmic_flops_per_launch": af, "avg_launch_ms": attn_ms},
+        # the same attention launch against the dense FP8 tensor roofline, and the
+        # whole step (indexer + attention flops over the step time) against it
+        "roofline_fp8": {"kernel": "sparse_mqa", "bound": "tensor", "achieved": achieved, "peak": fp8_peak,
+                         "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                         "peak_src": f"dense FP8 = 2 x bf16 dense, {pk['src']} (burst)"},
+        "step_frac_fp8": step_flops / (ms_step * 1e-3) / 1e12 / fp8_peak,
+        "step_flops": step_flops,
         "e2e": {"value": aggregate_tokens_per_s(world, T, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk.summary(),
     }
+    if world == 1 and not args.no_decode:
+        # the 1M-context decode target, measured in the same run: the hybrid
+        # CSA + HCA layer pair, 4 sequences, one CUDA graph per step
+        dec = run_config(argparse.Namespace(steps=max(args.steps, 20), warmup=max(args.warmup, 3)),
+                         "c5_hybrid_csa_decode_1m")
+        r = dec["roofline"]
+        res["decode_1m"] = {"workload": dec["config"]["workload"], "metric": dec["metric"], "value": dec["value"],
+                            "unit": dec["unit"], "ms_per_step": dec["ms_per_step"], "steps": dec["steps"],
+                            "algorithmic_bytes_per_step": r["algorithmic_bytes_per_step"],
+                            "achieved_gbs": r["achieved"], "peak_gbs": r["peak"], "hbm_frac": r["frac"],
+                            "peak_src": r["peak_src"], "gpu_launches": dec["gpu_launches"],
+                            "clocks": dec["clocks"], "step": dec["config"]["step"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(h, budget_s=args.cpu_budget)
+        res["cpu_baseline"] = cpu_baseline(h)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -285,9 +311,10 @@ def oracle_sample(h, rows, rope):
     swa = oracle.compress_kv(x, h["z"], None, 1, "mixed592", CFG.R, 0, rope)
     keys = oracle.compress_kv(wl.bf16_bits_to_f32(h["kI"]), h["zI"], h["sI"], CFG.m, "mxfp4", 0)
     t1 = time.perf_counter()
-    idx, _ = oracle.indexer_topk(wl.bf16_bits_to_f32(h["qI"])[:, rows], h["w"][:, rows], keys,
+    # only the sampled rows' queries are widened to fp32
+    idx, _ = oracle.indexer_topk(wl.bf16_bits_to_f32(h["qI"][:, rows]), h["w"][:, rows], keys,
                                  h["q_pos"][:, rows], CFG.N, CFG.m, CFG.k)
-    oracle.attention(wl.bf16_bits_to_f32(h["q"])[:, rows], h["q_pos"][:, rows], cache, CFG.N, CFG.m,
+    oracle.attention(wl.bf16_bits_to_f32(h["q"][:, rows]), h["q_pos"][:, rows], cache, CFG.N, CFG.m,
                      idx, swa, h["swa_pos0"], CFG.W, 1.0 / math.sqrt(CFG.D), rope, CFG.R)
     return t1 - t0, time.perf_counter() - t1
 
@@ -309,26 +336,33 @@ def host_cpu_model() -> str:
     return "unknown"
 
 
-def cpu_baseline(h, budget_s=20.0):
-    """Time the oracle on a bounded sample: compression of all tokens, then
-    top-k and attention for a seeded set of query rows; scaled to tokens/s."""
+ORACLE_ROWS = 256   # query rows per sampled oracle step (both CPU arms)
+
+
+def oracle_step_seconds(h, rope, rng, n_rows=ORACLE_ROWS):
+    """One sampled oracle step, scaled to the whole 8192-token step (seconds)."""
+    rows = np.sort(rng.choice(CFG.T, n_rows, replace=False))
+    tc, tr = oracle_sample(h, rows, rope)
+    return _full_step_seconds(tc, tr, n_rows)
+
+
+def oracle_sample_desc(n_rows: int) -> str:
+    return (f"per step: compression of all {CFG.T} tokens + top-k and sparse MQA for {n_rows} seeded "
+            f"query rows, row time scaled to {CFG.T} rows")
+
+
+def cpu_baseline(h, steps=3):
+    """The oracle on the host cores: the mean of `steps` sampled steps (the
+    same sample as the reference arm's steps), as tokens/s."""
     import oracle
     oracle.build()
     oracle.set_threads(os.cpu_count() or 1)
     rope = oracle.rope_table(CFG.T + 1, CFG.R)
     rng = np.random.default_rng(123)
-    n_rows = 16
-    rows = np.sort(rng.choice(CFG.T, n_rows, replace=False))
-    tc, tr = oracle_sample(h, rows, rope)
-    if tc + tr < budget_s / 4:
-        n_rows = int(min(CFG.T, n_rows * max(1.0, (budget_s / 2 - tc) / max(tr, 1e-3))))
-        rows = np.sort(rng.choice(CFG.T, n_rows, replace=False))
-        tc, tr = oracle_sample(h, rows, rope)
-    full = _full_step_seconds(tc, tr, n_rows)
-    return {"value": CFG.T / full, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
-            "cpu": host_cpu_model(),
-            "sample": f"compression of all {CFG.T} tokens ({tc:.2f} s) + top-k and sparse MQA for "
-                      f"{n_rows} seeded query rows ({tr:.2f} s); rows scaled to {CFG.T}"}
+    secs = statistics.mean(oracle_step_seconds(h, rope, rng) for _ in range(steps))
+    return {"value": CFG.T / secs, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
+            "cpu": host_cpu_model(), "rows_sampled": ORACLE_ROWS, "steps": steps,
+            "sample": oracle_sample_desc(ORACLE_ROWS)}
 
 
 def run_reference(args, rank, world):
@@ -339,26 +373,22 @@ def run_reference(args, rank, world):
     oracle.build()
     oracle.set_threads(os.cpu_count() or 1)
     rope = oracle.rope_table(CFG.T + 1, CFG.R)
-    n_rows = 16
     rng = np.random.default_rng(7)
     fulls = []
     for i in range(args.warmup + args.steps):
-        rows = np.sort(rng.choice(CFG.T, n_rows, replace=False))
-        tc, tr = oracle_sample(h, rows, rope)
+        s = oracle_step_seconds(h, rope, rng)
         if i >= args.warmup:
-            fulls.append(_full_step_seconds(tc, tr, n_rows))
+            fulls.append(s)
     ms = 1e3 * statistics.mean(fulls)
     value = CFG.T / (ms * 1e-3)
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": CFG.name, "B": 1, "T": CFG.T, "m": CFG.m, "N": CFG.N, "k": CFG.k,
-                   "W": CFG.W, "H": CFG.H, "D": CFG.D, "HI": CFG.HI, "dI": CFG.dI},
+        "config": bench_config(world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
-                         "cpu": host_cpu_model(),
-                         "sample": f"per step: compression of all {CFG.T} tokens + top-k and sparse MQA "
-                                   f"for {n_rows} seeded query rows, row time scaled to {CFG.T} rows"},
+                         "cpu": host_cpu_model(), "rows_sampled": ORACLE_ROWS,
+                         "sample": oracle_sample_desc(ORACLE_ROWS)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -615,7 +645,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-decode", action="store_true", help="skip the 1M-context decode measurement")
     ap.add_argument("--config", default=CFG.name,
                     help="workload; the default is the 8K CSA prefill, the others are measured on one GPU")
     args = ap.parse_args()

@@ -76,3 +76,6 @@ def test_reference_arm_line_on_cpu():
     assert res["e2e"] == {"value": res["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
     assert res["config"]["workload"] == "c2_csa_prefill_8k"
+    # the same config dict as the GPU arm prints, and the sample size stated
+    assert res["config"] == bench.bench_config(1)
+    assert cb["rows_sampled"] >= 1 and str(cb["rows_sampled"]) in cb["sample"]
