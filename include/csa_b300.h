@@ -326,7 +326,11 @@ int hca_dense_attn(const void *q, int q_dtype, const int64_t *q_pos, int B, int6
  *    calls that overlap on the GPU race, so order them on one stream;
  *  - the first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress); make that first call
- *    before any stream capture.
+ *    before any stream capture;
+ *  - the scores come from the library's integer (CUDA-core) kernels, which
+ *    have no device-side waits, so no wait can expire and CSA_OK covers the
+ *    whole call (no status block is needed); results are bit-identical to
+ *    csa_indexer_topk's.
  * It calls no cudaMalloc / cudaFree and no allocating library routine.
  */
 int csa_indexer_topk_noalloc(const void *qI, int qI_dtype, const float *w, const void *kI,

@@ -1066,14 +1066,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const Params p) {
 }
 
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
+  const int n = device_sms();
+  return n > 0 ? n : 148;
 }
 
 // Split count: 1 when there are enough rows to fill the GPU, else enough
@@ -1252,11 +1246,12 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
     if (!make_row_map(&tm_rows, xc, kD, (uint64_t)(nc + nw), 1)) return cudaErrorInvalidValue;
   }
   const int grid = (int)(p.items < num_sms() ? p.items : num_sms());
+  static PerDevice attr_sparse, attr_dense;
   if (a.idx) {
-    cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    smem_limit_once(attr_sparse, reinterpret_cast<const void*>(attn_tc_kernel<false>), (int)kSmemBytes);
     attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q, tm_qr);
   } else {
-    cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    smem_limit_once(attr_dense, reinterpret_cast<const void*>(attn_tc_kernel<true>), (int)kSmemBytes);
     attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q, tm_qr);
   }
   cudaError_t e = cudaGetLastError();

@@ -451,11 +451,8 @@ cudaError_t launch_decode_append(const void* kv, const float* z, const void* kI,
                                  cudaStream_t st) {
   if (B == 0) return cudaSuccess;
   const size_t ring = (size_t)m * (C + CI) * 2;   // staged rows of a closing block
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(decode_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * (512 + 64) * 2);
-    attr_set = true;
-  }
+  static PerDevice attr;
+  smem_limit_once(attr, reinterpret_cast<const void*>(decode_append_kernel), 128 * (512 + 64) * 2);
   decode_append_kernel<<<(unsigned)B, kWarpsPerBlock * 32, ring, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(kv), z, reinterpret_cast<const __nv_bfloat16*>(kI), zI, s, sI, rcos,
       rsin, rope_rows, t_pos, C, R, CI, m, reinterpret_cast<__nv_bfloat16*>(kv_tail), z_tail,

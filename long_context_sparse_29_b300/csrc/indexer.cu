@@ -292,14 +292,10 @@ scores_fp4_decode_kernel(const __nv_bfloat16* __restrict__ qI, const float* __re
 // entries per decode-scoring CTA: a multiple of kScoreThreads, so that the
 // grid (chunks x rows) is about one CTA per resident slot (at least 2 rounds)
 int64_t decode_chunk(int64_t N, int64_t rows) {
-  static int slots = 0;
-  if (!slots) {
-    int dev = 0, sms = 148, per = 2;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    per = resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_kernel), kScoreThreads, 0);
-    slots = sms * per;
-  }
+  static PerDevice slots_dev;
+  const int slots = slots_dev.get([] {
+    return device_sms() * resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_kernel), kScoreThreads, 0);
+  });
   int64_t per_row = slots / rows;
   if (per_row < 1) per_row = 1;
   int64_t c = (N + per_row - 1) / per_row;
@@ -740,13 +736,10 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
   }
   const int P = topk_pad(k);
   const size_t smem = sizeof(unsigned long long) * 2 * (size_t)P;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    cudaFuncSetAttribute(topk_stage1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTkStageMax);
-    cudaFuncSetAttribute(topk_stage2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTkStageMax);
-    attr_set = true;
-  }
+  static PerDevice attr_row, attr_s1, attr_s2;
+  smem_limit_once(attr_row, reinterpret_cast<const void*>(topk_kernel), 64 * 1024);
+  smem_limit_once(attr_s1, reinterpret_cast<const void*>(topk_stage1_kernel), (int)kTkStageMax);
+  smem_limit_once(attr_s2, reinterpret_cast<const void*>(topk_stage2_kernel), (int)kTkStageMax);
   const int64_t rows = (int64_t)B * Tq;
   if (cand_ws && topk_two_stage(B, Tq, N)) {
     const int ch = topk_chunks(N, k);

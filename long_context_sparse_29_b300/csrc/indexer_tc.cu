@@ -704,11 +704,8 @@ cudaError_t launch_indexer_scores_tc(const void* qI, const float* w, const uint8
   p.m = m;
   p.scores = scores;
   p.ws = flags_ws;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(ix_scores_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIxSmem);
-    attr = true;
-  }
+  static PerDevice attr;
+  smem_limit_once(attr, reinterpret_cast<const void*>(ix_scores_tc_kernel), (int)kIxSmem);
   const dim3 grid((unsigned)((N + kIxChunk - 1) / kIxChunk), (unsigned)((Tq + kIxRows - 1) / kIxRows), (unsigned)B);
   ix_scores_tc_kernel<<<grid, kIxThreads, kIxSmem, st>>>(p, tm_q, tm_k);
   return cudaGetLastError();
@@ -739,16 +736,13 @@ bool decode_tc_applies(int64_t Tq, int HI, int dI, int64_t N) {
 cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const uint8_t* kc, const uint8_t* ks,
                                         const int64_t* q_pos, int B, int64_t Tq, int HI, int64_t N, int m,
                                         float* scores, void* flags_ws, cudaStream_t st) {
-  static int slots = 0;
-  if (!slots) {
-    int dev = 0, sms = 148, per = 4;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(scores_fp4_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDtSmem);
-    per = resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_tc_kernel), kDtThreads, kDtSmem);
+  static PerDevice attr, slots_dev;
+  smem_limit_once(attr, reinterpret_cast<const void*>(scores_fp4_decode_tc_kernel), (int)kDtSmem);
+  const int slots = slots_dev.get([] {
+    int per = resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_tc_kernel), kDtThreads, kDtSmem);
     per = per > 8 ? 8 : per;   // 64 TMEM columns each: at most 8 per SM
-    slots = sms * per;
-  }
+    return device_sms() * per;
+  });
   const int64_t rows = (int64_t)B * Tq;
   // chunks of whole tiles, about one CTA per resident slot, at least 2 tiles each
   int64_t per_row = slots / rows;

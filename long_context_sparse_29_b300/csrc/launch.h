@@ -3,7 +3,51 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace csa {
+
+// A nonzero int per device, computed by f() the first time it is asked for
+// with that device current, then read.  Thread-safe: threads that race on the
+// first use each compute it (f must give the same value every time); a zero
+// from f (a failed query) is not stored, so the next call tries again.
+constexpr int kMaxDevices = 64;
+class PerDevice {
+ public:
+  template <class F>
+  int get(F f) {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return f();
+    int v = v_[d].load(std::memory_order_acquire);
+    if (v == 0) {
+      v = f();
+      if (v != 0) v_[d].store(v, std::memory_order_release);
+    }
+    return v;
+  }
+
+ private:
+  std::atomic<int> v_[kMaxDevices]{};
+};
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device and call site (`once`).
+inline void smem_limit_once(PerDevice& once, const void* kernel, int bytes) {
+  once.get([&] {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess ? 1 : 0;
+  });
+}
+
+// Streaming multiprocessors of the current device.
+inline int device_sms() {
+  static PerDevice sms;
+  return sms.get([] {
+    int d = 0, n = 0;
+    cudaGetDevice(&d);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    return n;
+  });
+}
 
 struct AttnArgs {
   const void* q;

@@ -20,6 +20,12 @@
 //    race on it, so the caller must order them;
 //  * nothing in it has to start at zero: each call writes every score it
 //    later reads;
+//  * the scores are computed by the library's integer (CUDA-core) kernels,
+//    which have no device-side waits: nothing in this call can expire, so
+//    CSA_OK from it covers the whole call (the workspace call's tensor-core
+//    scorers wait on mbarriers and report an expired wait in the caller's
+//    workspace, which this call does not have).  The indices and scores are
+//    bit-identical to csa_indexer_topk's on every path;
 //  * the first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (the device must be current); make that first
 //    call before any stream capture.
@@ -97,7 +103,7 @@ extern "C" int csa_indexer_topk_noalloc(const void* qI, int qI_dtype, const floa
   if (r != CSA_OK) return r;
   const cudaError_t e = csa::launch_indexer_topk(qI, fp4, w, kI, kI_scales, q_pos, B, Tq, HI, dI, N, m,
                                                  k, idx_out, score_out, reinterpret_cast<float*>(scratch),
-                                                 nullptr, nullptr, nullptr, true,
+                                                 nullptr, nullptr, nullptr, /*tensor_cores=*/false,
                                                  reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return csa::report_error(CSA_ERR_CUDA, cudaGetErrorString(e));
   return CSA_OK;

@@ -235,7 +235,7 @@ def _decode_caches(csa, oracle_mod, cfg, oracle_seqs):
 def test_decode_sampled(csa, oracle_mod, name):
     cfg = wl.CONFIGS[name]
     B, T, W = cfg.B, cfg.T, cfg.W
-    check = sorted({0, B - 1})
+    check = sorted({0, B // 3, (2 * B) // 3, B - 1})   # first, two middle and last sequences
     cache, swa, ocache, oswa, rope_np, rope_dev = _decode_caches(csa, oracle_mod, cfg, check)
     qry = [wl.gen_queries(cfg, b) for b in range(B)]
     q = np.stack([x["q"] for x in qry])

@@ -79,6 +79,34 @@ def test_noalloc_topk_matches_workspace_call():
             assert torch.equal(idx, ref_idx)
             assert torch.equal(sc.view(torch.int32), ref_sc.view(torch.int32))
 
+    # exactly the scratch's 4,194,304 scores (the last 2048 rows of the 8K
+    # prefill against all 2048 entries) fill it and still match; one row
+    # more is refused before any launch
+    T8 = cfg2.T
+    tok = wl.gen_tokens(cfg2, 0, 0, T8, parts=("kI", "zI"))
+    kc8, ks8 = csa.compress_kv(_bf16(tok["kI"])[None], torch.from_numpy(tok["zI"]).cuda()[None],
+                               torch.from_numpy(wl.gen_channel_scales(cfg2)["sI"]).cuda(), cfg2.m,
+                               csa.FMT_MXFP4, 0)
+    qry = wl.gen_queries(cfg2, 0, T8 - 2049, T8)
+    N8 = T8 // cfg2.m
+    for Tq in (2048, 2049):
+        qI_d = _bf16(qry["qI"][2049 - Tq:])[None]
+        w_d = torch.from_numpy(qry["w"][2049 - Tq:]).cuda()[None]
+        qpos = torch.arange(T8 - Tq, T8, dtype=torch.int64, device="cuda")[None]
+        idx = torch.full((1, Tq, cfg2.k), -7, dtype=torch.int32, device="cuda")
+        sc = torch.full((1, Tq, cfg2.k), 7.0, dtype=torch.float32, device="cuda")
+        r = L.csa_indexer_topk_noalloc(_ptr(qI_d), csa.DTYPE_BF16, _ptr(w_d), _ptr(kc8), _ptr(ks8),
+                                       csa.FMT_MXFP4, _ptr(qpos), 1, Tq, 16, 64, N8, cfg2.m, cfg2.k, _ptr(idx),
+                                       _ptr(sc), stream)
+        if Tq * N8 <= 4194304:
+            assert r == 0, L.csa_last_error()
+            ref_idx, ref_sc = csa.indexer_topk(qI_d, w_d, kc8, ks8, qpos, N8, cfg2.m, cfg2.k)
+            torch.cuda.synchronize()
+            assert torch.equal(idx, ref_idx)
+            assert torch.equal(sc.view(torch.int32), ref_sc.view(torch.int32))
+        else:
+            assert r == -2 and b"16 MiB" in L.csa_last_error()
+
     # more scores than the built-in scratch holds: refused before any launch
     kc, ks, qI_d, w_d, qpos, N, m, k = cases[0]
     idx = torch.empty((1, 8192, 16), dtype=torch.int32, device="cuda")

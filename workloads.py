@@ -198,13 +198,19 @@ def gen_queries(cfg: Config, b: int, q0: int = 0, q1: int | None = None, seed: i
     """
     q1 = cfg.Tq if q1 is None else q1
     blk = 256
-    parts = {"q": [], "qI": [], "w": []}
-    for c in range(q0 // blk, (q1 + blk - 1) // blk):
+
+    def block(c):
         lo, hi = c * blk, min((c + 1) * blk, cfg.Tq)
         a, e = max(q0, lo) - lo, min(q1, hi) - lo
         r = rng_for(seed, cfg.name, "qry", b, c)
-        parts["q"].append(_act(cfg, r, (hi - lo, cfg.H, cfg.D))[a:e])
+        got = {"q": _act(cfg, r, (hi - lo, cfg.H, cfg.D))[a:e]}
         if cfg.dI:
-            parts["qI"].append(_act(cfg, r, (hi - lo, cfg.HI, cfg.dI), cfg.qI_dist)[a:e])
-            parts["w"].append(r.uniform(0.0, 1.0, size=(hi - lo, cfg.HI)).astype(np.float32)[a:e])
-    return {k: np.concatenate(v) for k, v in parts.items() if v}
+            got["qI"] = _act(cfg, r, (hi - lo, cfg.HI, cfg.dI), cfg.qI_dist)[a:e]
+            got["w"] = r.uniform(0.0, 1.0, size=(hi - lo, cfg.HI)).astype(np.float32)[a:e]
+        return got
+
+    # blocks are independent generators: drawn in parallel, joined in order
+    blocks = range(q0 // blk, (q1 + blk - 1) // blk)
+    with _cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+        res = list(ex.map(block, blocks))
+    return {k: np.concatenate([r[k] for r in res]) for k in res[0]} if res else {}
