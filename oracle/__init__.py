@@ -85,6 +85,9 @@ def _declare(L):
         "orc_mxfp4_dot": (ctypes.c_float, [P, P, P, P, I32]),
         "orc_indexer_topk_fp4": (None, [P, P, P, P, P, I64, I64, I32, I32, I64, I32, I32, P, P]),
         "orc_indexer_topk_f32": (None, [P, P, P, P, I64, I64, I32, I32, I64, I32, I32, P, P]),
+        "orc_fp8b32_quant": (None, [P, I64, I32, P, P]),
+        "orc_fp4q_fp8k_dot": (ctypes.c_float, [P, P, P, P, I32]),
+        "orc_indexer_topk_fp4q_fp8k": (None, [P, P, P, P, P, I64, I64, I32, I32, I64, I32, I32, P, P]),
         "orc_attention": (None, [P, P, I64, I64, I32, I32, I32, I32, P, I64, I32, P, I32,
                                  P, P, I64, I32, F64, P, P, I64, P, P, P]),
     }
@@ -232,12 +235,52 @@ def compress_kv(x, z, s, m: int, fmt: str, R: int, pos0: int = 0, rope=None):
         return pack_mixed(e)
     if fmt == "mxfp4":
         return mxfp4_quant(e)
+    if fmt == "fp8b32":
+        return fp8b32_quant(e)
     raise ValueError(fmt)
+
+
+def fp8b32_quant(v):
+    """FP8 indexer keys: E4M3 codes with a power-of-two scale per 32 channels
+    (the smallest 2^e with max|v| / 2^e <= 448; byte e + 127).
+    v fp32 [..., d] -> (codes uint8 [..., d], scales uint8 [..., d/32])."""
+    v = _c(v, np.float32)
+    d = v.shape[-1]
+    n = v.size // d
+    codes = np.empty(v.shape, np.uint8)
+    scales = np.empty(v.shape[:-1] + (d // 32,), np.uint8)
+    lib().orc_fp8b32_quant(_p(v), n, d, _p(codes), _p(scales))
+    return codes, scales
+
+
+def fp8b32_dequant(codes, scales) -> np.ndarray:
+    """fp64 values of FP8 keys (exact)."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    d = codes.shape[-1]
+    vals = e4m3_decode(codes.ravel()).reshape(codes.shape)
+    sc = np.ldexp(1.0, scales.astype(np.int64) - 127)
+    return vals * np.repeat(sc, 32, axis=-1)[..., :d]
 
 
 # --------------------------------------------------------------------------
 # indexer + top-k
 # --------------------------------------------------------------------------
+def indexer_topk_fp8k(qI, w, keys, q_pos, N: int, m: int, k: int):
+    """Top-k with MXFP4 queries and FP8 keys (codes [B, N, dI], scales
+    [B, N, dI/32]); same order and padding as indexer_topk."""
+    qI = _c(qI, np.float32)
+    B, Tq, HI, dI = qI.shape
+    w = _c(w, np.float32)
+    q_pos = _c(q_pos, np.int64)
+    kc, ks = _c(keys[0], np.uint8), _c(keys[1], np.uint8)
+    idx = np.empty((B, Tq, k), np.int32)
+    sc = np.empty((B, Tq, k), np.float32)
+    lib().orc_indexer_topk_fp4q_fp8k(_p(qI), _p(w), _p(kc), _p(ks), _p(q_pos), B, Tq, HI, dI, N, m, k,
+                                     _p(idx), _p(sc))
+    return idx, sc
+
+
 def indexer_topk(qI, w, keys, q_pos, N: int, m: int, k: int):
     """Top-k entry indices per query (score desc, index asc), -1 padded.
 

@@ -481,6 +481,97 @@ void orc_indexer_topk_fp4(const float *qI, const float *w, const uint8_t *kc, co
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* FP8 indexer keys (the scope's next row: an FP4-query x FP8-key indexer).   */
+/* [XM] "算力与内存效率": an FP4 x FP8 product runs at the FP8 x FP8 rate;    */
+/* [ZC]: dequantising FP4 to FP8 is lossless (E4M3 holds every E2M1 value    */
+/* times a power of two in its range).                                       */
+/* Reading taken for the key format: E4M3 codes with one power-of-two scale  */
+/* per block of 32 channels, the mixed cache's group rule -- the smallest     */
+/* integer e with amax / 2^e <= 448 (no element saturates), 0 for an         */
+/* all-zero block, clamped to >= -126 -- stored as a UE8M0 byte e + 127.      */
+/* v: fp32 [n, d] -> codes [n, d] (one byte per element), scales [n, d/32].   */
+/* ------------------------------------------------------------------------ */
+void orc_fp8b32_quant(const float *v, int64_t n, int d, uint8_t *codes, uint8_t *scales) {
+    int nb = d / 32;
+    for (int64_t r = 0; r < n; ++r) {
+        for (int b = 0; b < nb; ++b) {
+            const float *x = v + r * d + 32 * b;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+            int e = fp8_group_exp(amax);
+            scales[r * nb + b] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; ++i) codes[r * d + 32 * b + i] = orc_e4m3_encode(ldexp((double)x[i], -e));
+        }
+    }
+}
+
+/* Exact dot of a dequantised MXFP4 query head (qc, qs) with a dequantised   */
+/* FP8 key (kc8: d E4M3 codes, ks8: d/32 scale bytes), rounded once to fp32. */
+/* Per block b the integer P_b = sum_i (2 q_i / 2^eq) (512 k_i / 2^ek): twice */
+/* an E2M1 value is an integer in [-12, 12] and 512 times an E4M3 value an   */
+/* integer below 2^18, so |P_b| < 2^28 and the block's value is               */
+/* P_b 2^(eq + ek - 10).  The two blocks are summed exactly in a 64-bit       */
+/* significand (their exponents may differ by at most 36 here) and the cast  */
+/* to fp32 is the one rounding.                                              */
+float orc_fp4q_fp8k_dot(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc8, const uint8_t *ks8, int d) {
+    long double acc = 0.0L;
+    int nb = d / 32;
+    int emin = 1 << 30, emax = -(1 << 30);
+    for (int b = 0; b < nb; ++b) {
+        long long P = 0;
+        for (int i = 32 * b; i < 32 * b + 32; ++i) {
+            int cq = (qc[i / 2] >> (4 * (i & 1))) & 15;
+            long long vq = (long long)(2.0 * orc_e2m1_decode((uint8_t)cq));
+            long long vk = (long long)ldexp(orc_e4m3_decode(kc8[i]), 9);
+            P += vq * vk;
+        }
+        int e = ((int)qs[b] - 127) + ((int)ks8[b] - 127) - 10;
+        if (P != 0) {
+            if (e < emin) emin = e;
+            if (e > emax) emax = e;
+        }
+        acc += ldexpl((long double)P, e);
+    }
+    if (emax - emin > 36) abort();
+    return (float)acc;
+}
+
+/* Lightning-indexer top-k with MXFP4 queries (quantised per head and 32-block */
+/* exactly as orc_indexer_topk_fp4 does) and FP8 keys: the same head sum,      */
+/* visibility rule and order, with d from orc_fp4q_fp8k_dot.                   */
+/* kc8: [B, N, dI] codes; ks8: [B, N, dI/32] scale bytes.                      */
+void orc_indexer_topk_fp4q_fp8k(const float *qI, const float *w, const uint8_t *kc8, const uint8_t *ks8,
+                                const int64_t *q_pos, int64_t B, int64_t Tq, int HI, int dI, int64_t N,
+                                int m, int k, int32_t *idx_out, float *score_out) {
+    int nb = dI / 32;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bt = 0; bt < B * Tq; ++bt) {
+        int64_t b = bt / Tq;
+        int64_t nv = n_visible(q_pos[bt], m, N);
+        uint8_t *qc = (uint8_t *)malloc((size_t)(HI * dI / 2));
+        uint8_t *qs = (uint8_t *)malloc((size_t)(HI * nb));
+        orc_mxfp4_quant(qI + bt * HI * dI, HI, dI, qc, qs);
+        cand_t *c = (cand_t *)malloc(sizeof(cand_t) * (size_t)(nv > 0 ? nv : 1));
+        for (int64_t j = 0; j < nv; ++j) {
+            const uint8_t *kj = kc8 + (b * N + j) * dI;
+            const uint8_t *sj = ks8 + (b * N + j) * nb;
+            float s = 0.0f;
+            for (int h = 0; h < HI; ++h) {
+                float dd = orc_fp4q_fp8k_dot(qc + h * (dI / 2), qs + h * nb, kj, sj, dI);
+                float r = dd > 0.0f ? dd : 0.0f;
+                s = fmaf(w[bt * HI + h], r, s);
+            }
+            c[j].s = s;
+            c[j].j = (int32_t)j;
+        }
+        topk_emit(c, nv, k, idx_out + bt * k, score_out ? score_out + bt * k : NULL);
+        free(c);
+        free(qc);
+        free(qs);
+    }
+}
+
 /* fp32 indexer: kI fp32 [B, N, dI] */
 void orc_indexer_topk_f32(const float *qI, const float *w, const float *kI, const int64_t *q_pos,
                           int64_t B, int64_t Tq, int HI, int dI, int64_t N, int m, int k,
