@@ -43,6 +43,12 @@
  *    bytes of E2M1 codes (even element in the low nibble) per row plus C/32
  *    UE8M0 scale bytes per row in a separate array; scale exponent =
  *    floor(log2 max|v|) - 2 over each block of 32 (OCP MX v1.0).
+ *    CSA_FMT_FP8B32 (FP8 indexer keys, C = 32 or 64): C E4M3 codes per row
+ *    (one byte each) plus C/32 scale bytes per row in a separate array,
+ *    e + 127 with e the smallest integer such that max|v| / 2^e <= 448 over
+ *    the block of 32 (the mixed rows' group rule: no element saturates; 0 for
+ *    an all-zero block, >= -126).  [XM] "算力与内存效率": an FP4 x FP8
+ *    product runs at the FP8 x FP8 rate; [ZC]: FP4 -> FP8 is lossless.
  *  - RoPE: rope_cos / rope_sin (device, fp32 [rope_rows, R/2]) hold
  *    cos/sin(p * base^(-2i/R)); pairs (2i, 2i+1) of the last R channels
  *    rotate by angle p*theta_i.  Build them with csa_rope_table.
@@ -75,6 +81,7 @@ extern "C" {
 #define CSA_FMT_F32 0
 #define CSA_FMT_MIXED592 1
 #define CSA_FMT_MXFP4 2
+#define CSA_FMT_FP8B32 3
 
 #define CSA_OP_INDEXER_TOPK 1
 #define CSA_OP_SPARSE_MQA 2
@@ -147,9 +154,10 @@ int kvcache_pack_fp8_bf16(const float *v, int64_t n, uint8_t *out, void *stream)
  *  R         RoPE channels (the last R of C); 0 for indexer keys
  *  m         block size (1..128); N = floor(T / m) entries are written
  *  out_fmt   CSA_FMT_F32 (out fp32 [B, N, C]), CSA_FMT_MIXED592 (C = 512,
- *            R = 64; out [B, N, 592] bytes) or CSA_FMT_MXFP4 (R = 0, C a
+ *            R = 64; out [B, N, 592] bytes), CSA_FMT_MXFP4 (R = 0, C a
  *            multiple of 32, at most 64; out [B, N, C/2] codes and
- *            out_scales [B, N, C/32] bytes)
+ *            out_scales [B, N, C/32] bytes) or CSA_FMT_FP8B32 (R = 0, C =
+ *            32 or 64; out [B, N, C] codes and out_scales [B, N, C/32])
  * Entry j (of this call) covers tokens [jm, jm + m); its weights are
  * a = softmax(z over the block), computed as mu = max z, e_i = sexp(z_i -
  * mu) (the library's fp32 exponential), S = e_0 + ... + e_{m-1} in order,
@@ -231,24 +239,27 @@ int csa_decode_append(const void *kv, const float *z, const void *kI, const floa
  * query token; [HU] Lightning Indexer (k = 1024); [XM] key technical details:
  * the indexer's attention runs in FP4.
  *  qI        (device) [B, Tq, HI, dI] indexer queries: CSA_DTYPE_BF16 with
- *            kI_fmt CSA_FMT_MXFP4 (quantised to MXFP4 per 32-block inside),
- *            or CSA_DTYPE_F32 with kI_fmt CSA_FMT_F32
+ *            kI_fmt CSA_FMT_MXFP4 or CSA_FMT_FP8B32 (quantised to MXFP4
+ *            per 32-block inside), or CSA_DTYPE_F32 with kI_fmt CSA_FMT_F32
  *  w         (device) fp32 [B, Tq, HI] head weights
  *  kI        (device) keys: MXFP4 codes [B, N, dI/2] with kI_scales
- *            [B, N, dI/32], or fp32 [B, N, dI] (kI_scales NULL)
+ *            [B, N, dI/32], FP8 codes [B, N, dI] with kI_scales [B, N,
+ *            dI/32] (CSA_FMT_FP8B32: the FP4-query x FP8-key indexer), or
+ *            fp32 [B, N, dI] (kI_scales NULL)
  *  q_pos     (device) int64 [B, Tq] absolute position t of each query
  *  N, m      entries per sequence and their block size
  *  k         entries to keep (1..4096)
  *  idx_out   (device) int32 [B, Tq, k]: entry indices, best first, -1 pad
  *  score_out (device) fp32 [B, Tq, k] or NULL: their scores (-inf pad)
  * score(t, j) = sum over heads h, ascending, of s = fma(w_h, relu(d_h), s)
- * from +0; d_h is the exact dot of the dequantised MXFP4 vectors rounded
- * once to fp32 (FP4) or the fma chain over dI from +0 (fp32).  Candidates:
+ * from +0; d_h is the exact dot of the dequantised MXFP4 query with the
+ * dequantised MXFP4 or FP8 key, rounded once to fp32, or the fma chain over
+ * dI from +0 (fp32).  Candidates:
  * j < N with (j + 1) m - 1 <= t.  Order: score descending, then index
  * ascending.
  * Errors: INVALID_ARG (sizes, NULL pointers, ws smaller than the scores or
- * not 256-byte aligned); UNSUPPORTED (k outside 1..4096; FP4: dI != 64 or
- * HI > 32; fp32: dI > 64, HI > 32 or HI * dI > 512); CUDA.
+ * not 256-byte aligned); UNSUPPORTED (k outside 1..4096; FP4 or FP8 keys:
+ * dI != 64 or HI > 32; fp32: dI > 64, HI > 32 or HI * dI > 512); CUDA.
  * Workspace: csa_workspace_size(CSA_OP_INDEXER_TOPK, ...) bytes give every
  * path (the tensor-core prefill scores, the two-stage top-k of few long
  * rows); the status block plus B * Tq * N fp32 scores is the least accepted,

@@ -22,10 +22,10 @@ from ._lib import CsaError, check, lib
 
 __all__ = ["CsaError", "Workspace", "ChunkedPrefill", "rope_table", "compress_kv", "kvcache_pack_fp8_bf16",
            "indexer_topk", "sparse_mqa", "hca_dense_attn", "workspace_size", "LayerCache", "decode_append",
-           "DTYPE_F32", "DTYPE_BF16", "FMT_F32", "FMT_MIXED592", "FMT_MXFP4"]
+           "DTYPE_F32", "DTYPE_BF16", "FMT_F32", "FMT_MIXED592", "FMT_MXFP4", "FMT_FP8B32"]
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
-FMT_F32, FMT_MIXED592, FMT_MXFP4 = 0, 1, 2
+FMT_F32, FMT_MIXED592, FMT_MXFP4, FMT_FP8B32 = 0, 1, 2, 3
 OP_INDEXER_TOPK, OP_SPARSE_MQA, OP_HCA_DENSE = 1, 2, 3
 FLAG_DEVICE_CHECK, FLAG_TIMEOUT = 1, 2
 MIXED_ROW = 592
@@ -128,8 +128,9 @@ def compress_kv(x, z, s, m: int, out_fmt: int, R: int = 0, rope=None, pos0: int 
 
     z fp32 [B, T] (one logit per token), or [B, T, C] (one per token and
     channel: csa_compress_kv_channel_logits).  Returns fp32 [B, N, C]
-    (FMT_F32), uint8 [B, N, 592] (FMT_MIXED592) or (codes uint8 [B, N, C/2],
-    scales uint8 [B, N, C/32]) (FMT_MXFP4).
+    (FMT_F32), uint8 [B, N, 592] (FMT_MIXED592), (codes uint8 [B, N, C/2],
+    scales uint8 [B, N, C/32]) (FMT_MXFP4) or (codes uint8 [B, N, C], scales
+    uint8 [B, N, C/32]) (FMT_FP8B32).
     """
     _need(x, "x")
     B, T, C = x.shape
@@ -147,14 +148,14 @@ def compress_kv(x, z, s, m: int, out_fmt: int, R: int = 0, rope=None, pos0: int 
         elif out_fmt == FMT_MIXED592:
             out = torch.empty((B, N, MIXED_ROW), dtype=torch.uint8, device=dev)
         else:
-            out = torch.empty((B, N, C // 2), dtype=torch.uint8, device=dev)
+            out = torch.empty((B, N, C if out_fmt == FMT_FP8B32 else C // 2), dtype=torch.uint8, device=dev)
             out_scales = torch.empty((B, N, C // 32), dtype=torch.uint8, device=dev)
     rc, rs = (rope if rope is not None else (None, None))
     rows = rc.shape[0] if rc is not None else 0
     fn = lib().csa_compress_kv_channel_logits if per_channel else lib().csa_compress_kv
     check(fn(_ptr(x), _dt(x), _ptr(z), _ptr(s), _ptr(rc), _ptr(rs), rows, pos0,
              B, T, C, R, m, out_fmt, _ptr(out), _ptr(out_scales), _stream(dev)))
-    return (out, out_scales) if out_fmt == FMT_MXFP4 else out
+    return (out, out_scales) if out_fmt in (FMT_MXFP4, FMT_FP8B32) else out
 
 
 class LayerCache:
@@ -259,13 +260,15 @@ def kvcache_pack_fp8_bf16(v, out=None):
 
 def indexer_topk(qI, w, kI, kI_scales, q_pos, N: int, m: int, k: int, scores: bool = True,
                  idx_out=None, score_out=None, ws: Workspace | None = None):
-    """Top-k entries per query.  qI [B, Tq, HI, dI] bf16 (MXFP4 keys) or fp32 (fp32 keys)."""
+    """Top-k entries per query.  qI [B, Tq, HI, dI] bf16 with MXFP4 keys (codes
+    [B, N, dI/2]) or FP8 keys (codes [B, N, dI]), both with kI_scales
+    [B, N, dI/32]; or qI fp32 with fp32 keys (kI_scales None)."""
     _need(qI, "qI")
     _need(w, "w", torch.float32)
     _need(q_pos, "q_pos", torch.int64)
     _need(kI, "kI")
     B, Tq, HI, dI = qI.shape
-    fmt = FMT_MXFP4 if kI_scales is not None else FMT_F32
+    fmt = FMT_F32 if kI_scales is None else (FMT_FP8B32 if kI.shape[-1] == dI else FMT_MXFP4)
     dev = qI.device
     if idx_out is None:
         idx_out = torch.empty((B, Tq, k), dtype=torch.int32, device=dev)

@@ -223,9 +223,9 @@ static int compress_call(const char* nm, bool z_per_channel, const void* x, int 
   }
   if (out_fmt == CSA_FMT_MIXED592) {
     if (C != 512 || R != 64) return fail(CSA_ERR_UNSUPPORTED, "%s: mixed rows need C=512, R=64", nm);
-  } else if (out_fmt == CSA_FMT_MXFP4) {
+  } else if (out_fmt == CSA_FMT_MXFP4 || out_fmt == CSA_FMT_FP8B32) {
     if (R != 0 || (C != 32 && C != 64))
-      return fail(CSA_ERR_UNSUPPORTED, "%s: MXFP4 keys need R=0 and C in {32, 64}", nm);
+      return fail(CSA_ERR_UNSUPPORTED, "%s: MXFP4 / FP8 keys need R=0 and C in {32, 64}", nm);
     if (!out_scales) return fail(CSA_ERR_INVALID_ARG, "%s: NULL out_scales", nm);
   } else if (out_fmt != CSA_FMT_F32) {
     return fail(CSA_ERR_INVALID_ARG, "%s: unknown output format %d", nm, out_fmt);
@@ -287,13 +287,15 @@ int csa_indexer_topk(const void* qI, int qI_dtype, const float* w, const void* k
     return fail(CSA_ERR_INVALID_ARG, "%s: bad sizes", nm);
   if (k < 1 || k > 4096) return fail(CSA_ERR_UNSUPPORTED, "%s: k must be in [1, 4096]", nm);
   const bool fp4 = qI_dtype == CSA_DTYPE_BF16 && kI_fmt == CSA_FMT_MXFP4;
+  const bool fp8k = qI_dtype == CSA_DTYPE_BF16 && kI_fmt == CSA_FMT_FP8B32;
   const bool f32 = qI_dtype == CSA_DTYPE_F32 && kI_fmt == CSA_FMT_F32;
-  if (!fp4 && !f32) return fail(CSA_ERR_UNSUPPORTED, "%s: dtype/format pair not supported", nm);
-  if (fp4 && (dI != 64 || HI > 32)) return fail(CSA_ERR_UNSUPPORTED, "%s: FP4 path needs dI=64, HI<=32", nm);
+  if (!fp4 && !fp8k && !f32) return fail(CSA_ERR_UNSUPPORTED, "%s: dtype/format pair not supported", nm);
+  if ((fp4 || fp8k) && (dI != 64 || HI > 32))
+    return fail(CSA_ERR_UNSUPPORTED, "%s: FP4 / FP8 keys need dI=64, HI<=32", nm);
   if (f32 && (dI > 64 || HI > 32 || HI * dI > 512))
     return fail(CSA_ERR_UNSUPPORTED, "%s: fp32 path needs dI<=64, HI<=32, HI*dI<=512", nm);
   if ((int64_t)B * Tq == 0) return ok();
-  if (!qI || !w || !q_pos || !idx_out || (N > 0 && !kI) || (fp4 && N > 0 && !kI_scales))
+  if (!qI || !w || !q_pos || !idx_out || (N > 0 && !kI) || ((fp4 || fp8k) && N > 0 && !kI_scales))
     return fail(CSA_ERR_INVALID_ARG, "%s: NULL pointer", nm);
   if (!ws || ws_bytes < indexer_ws(B, Tq, N))
     return fail(CSA_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", nm, ws_bytes,
@@ -310,7 +312,7 @@ int csa_indexer_topk(const void* qI, int qI_dtype, const float* w, const void* k
     p += indexer_cand_ws(B, Tq, N, k);
     if (fp4 && !indexer_use_dp4a() && csa::indexer_tc_applies(B, Tq, HI, dI, N)) tc_ws = p;
   }
-  return cuda_result(csa::launch_indexer_topk(qI, fp4, w, kI, kI_scales, q_pos, B, Tq, HI, dI, N,
+  return cuda_result(csa::launch_indexer_topk(qI, kI_fmt, w, kI, kI_scales, q_pos, B, Tq, HI, dI, N,
                                               m, k, idx_out, score_out, scores, tc_ws, cand_ws, ws,
                                               !indexer_use_dp4a(), as_stream(stream)),
                      nm);

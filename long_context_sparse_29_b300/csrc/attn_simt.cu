@@ -64,6 +64,7 @@ attn_simt_kernel(const void* __restrict__ q, const int64_t* __restrict__ q_pos, 
                  const float* __restrict__ rcos, const float* __restrict__ rsin,
                  int64_t rope_rows, void* __restrict__ out, float* __restrict__ lse, void* ws,
                  int max_keys) {
+  pdl_begin();
   extern __shared__ float sm[];
   float* qr = sm;                       // [D]
   float* pt = qr + D;                   // [kSimtThreads] probabilities of the tile
@@ -199,7 +200,7 @@ cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t st) {
   do {                                                                                          \
     cudaFuncSetAttribute(attn_simt_kernel<MX, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                          (int)smem);                                                            \
-    attn_simt_kernel<MX, BF><<<(unsigned)rows, kSimtThreads, smem, st>>>(                       \
+    launch_pdl(attn_simt_kernel<MX, BF>, dim3((unsigned)rows), dim3(kSimtThreads), smem, st,                        \
         a.q, a.q_pos, a.Tq, a.H, a.D, a.R, reinterpret_cast<const uint8_t*>(a.cache), a.N, a.m, \
         a.idx, a.k, reinterpret_cast<const uint8_t*>(a.swa), a.swa_pos0, a.Ts, a.W, a.scale,    \
         a.rcos, a.rsin, a.rope_rows, a.out, a.lse, a.ws, a.max_keys);                                        \

@@ -181,6 +181,7 @@ __device__ __forceinline__ void dequant16(const uint4 c, float sc, uint4& o0, ui
 // when every row serves many queries, so the expansion is paid once.
 __global__ void __launch_bounds__(256) expand_rows_kernel(const uint8_t* __restrict__ rows, int64_t n,
                                                           __nv_bfloat16* __restrict__ out) {
+  pdl_begin();
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= n) return;
@@ -342,6 +343,7 @@ prep_rows_kernel(const __nv_bfloat16* __restrict__ q, const int64_t* __restrict_
                  const float* __restrict__ rsin, int64_t rope_rows, __nv_bfloat16* __restrict__ qr,
                  const int32_t* __restrict__ idx, int k, int kpad, int64_t N, int m, int32_t* __restrict__ clist,
                  int32_t* __restrict__ ccount, void* ws) {
+  pdl_begin();
   const int64_t row = blockIdx.x;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = q_pos[row];
@@ -388,6 +390,7 @@ prep_rows_kernel(const __nv_bfloat16* __restrict__ q, const int64_t* __restrict_
 // keys are zero.  One warp per slot.
 __global__ void __launch_bounds__(256)
 gather_expand_kernel(const Params p, int64_t rows, int dense, __nv_bfloat16* __restrict__ xg) {
+  pdl_begin();
   const int64_t slot = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int64_t r = slot / p.kp;
@@ -434,6 +437,7 @@ template <bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_qr) {
+  pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm + kQOff;
@@ -1016,6 +1020,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
 // and lse: one CTA per pair, thread t owns dims 2t and 2t + 1 (a RoPE pair when
 // 2t >= 448); the partial states are weighted by 2^(m_s - max m) in split order.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const Params p) {
+  pdl_begin();
   __shared__ float m_s[kMaxSplits], l_s[kMaxSplits];
   const int64_t row = blockIdx.x;
   const int h = blockIdx.y;
@@ -1204,7 +1209,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
     base += pl.list_bytes;
     avail -= pl.list_bytes;
   }
-  prep_rows_kernel<<<(unsigned)rows, 256, 0, st>>>(p.q, a.q_pos, a.rcos, a.rsin, a.rope_rows, qr, a.idx, p.k, pl.kpad,
+  launch_pdl(prep_rows_kernel, dim3((unsigned)rows), dim3(256), 0, st, p.q, a.q_pos, a.rcos, a.rsin, a.rope_rows, qr, a.idx, p.k, pl.kpad,
                                                    a.N, a.m, const_cast<int32_t*>(p.clist),
                                                    const_cast<int32_t*>(p.ccount), a.ws);
   if (pl.nsplit > 1 && pl.part_bytes > avail) {   // too little scratch: no split
@@ -1232,14 +1237,14 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
   if (pl.gather) {
     __nv_bfloat16* xg = reinterpret_cast<__nv_bfloat16*>(base);
     const int64_t slots = rows * pl.kp;
-    gather_expand_kernel<<<(unsigned)((slots + 7) / 8), 256, 0, st>>>(p, rows, a.idx ? 0 : 1, xg);
+    launch_pdl(gather_expand_kernel, dim3((unsigned)((slots + 7) / 8)), dim3(256), 0, st, p, rows, a.idx ? 0 : 1, xg);
     p.xg = xg;
     if (!make_row_map(&tm_rows, xg, kD, (uint64_t)slots, 64)) return cudaErrorInvalidValue;
   } else if (pl.expand) {
     const int64_t nc = (int64_t)a.B * a.N, nw = (a.W > 0) ? (int64_t)a.B * a.Ts : 0;
     __nv_bfloat16* xc = reinterpret_cast<__nv_bfloat16*>(base);
-    if (nc > 0) expand_rows_kernel<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(p.cache, nc, xc);
-    if (nw > 0) expand_rows_kernel<<<(unsigned)((nw + 7) / 8), 256, 0, st>>>(p.swa, nw, xc + nc * kD);
+    if (nc > 0) launch_pdl(expand_rows_kernel, dim3((unsigned)((nc + 7) / 8)), dim3(256), 0, st, p.cache, nc, xc);
+    if (nw > 0) launch_pdl(expand_rows_kernel, dim3((unsigned)((nw + 7) / 8)), dim3(256), 0, st, p.swa, nw, xc + nc * kD);
     p.xcache = xc;
     p.xrows = nc + nw;
     p.xwin0 = nc;
@@ -1249,14 +1254,14 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
   static PerDevice attr_sparse, attr_dense;
   if (a.idx) {
     smem_limit_once(attr_sparse, reinterpret_cast<const void*>(attn_tc_kernel<false>), (int)kSmemBytes);
-    attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q, tm_qr);
+    launch_pdl(attn_tc_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, st, p, tm_rows, tm_q, tm_qr);
   } else {
     smem_limit_once(attr_dense, reinterpret_cast<const void*>(attn_tc_kernel<true>), (int)kSmemBytes);
-    attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p, tm_rows, tm_q, tm_qr);
+    launch_pdl(attn_tc_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, st, p, tm_rows, tm_q, tm_qr);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  attn_combine_kernel<<<dim3((unsigned)rows, kH), 256, 0, st>>>(p);
+  launch_pdl(attn_combine_kernel, dim3(dim3((unsigned)rows, kH)), dim3(256), 0, st, p);
   return cudaGetLastError();
 }
 

@@ -133,6 +133,18 @@ __device__ __forceinline__ void entry_finish(float2 (&v)[kMaxPairs], const float
     }
   } else if (FMT == CSA_FMT_MIXED592) {
     pack_mixed_row(v, lane, reinterpret_cast<uint8_t*>(out));
+  } else if (FMT == CSA_FMT_FP8B32) {   // FP8 keys, C in {32, 64}: block of lane's pair = lane / 16
+    float amax = (lane < npairs) ? fmaxf(fabsf(v[0].x), fabsf(v[0].y)) : 0.0f;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int e = fp8_group_exp(amax);
+    if (lane < npairs) {
+      const float inv = pow2i(-e);
+      const uint32_t c0 = e4m3_encode(__fmul_rn(v[0].x, inv));
+      const uint32_t c1 = e4m3_encode(__fmul_rn(v[0].y, inv));
+      reinterpret_cast<uint16_t*>(out)[lane] = (uint16_t)(c0 | (c1 << 8));
+      if ((lane & 15) == 0) out_scales[lane >> 4] = (uint8_t)(e + 127);
+    }
   } else {  // MXFP4, C in {32, 64}: block of lane's pair = p / 16 = lane / 16
     float amax = (lane < npairs) ? fmaxf(fabsf(v[0].x), fabsf(v[0].y)) : 0.0f;
 #pragma unroll
@@ -232,6 +244,7 @@ compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
                 const float* __restrict__ s, const float* __restrict__ rcos,
                 const float* __restrict__ rsin, int64_t pos0, int B, int64_t T, int C, int R,
                 int m, int64_t N, void* __restrict__ out, uint8_t* __restrict__ out_scales) {
+  pdl_begin();
   __shared__ float alpha_s[kWarpsPerBlock][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t ent = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
@@ -242,15 +255,16 @@ compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
   const size_t esz = BF16 ? 2 : 4;
   void* o = FMT == CSA_FMT_F32 ? (void*)(reinterpret_cast<float*>(out) + ent * C)
             : FMT == CSA_FMT_MIXED592 ? (void*)(reinterpret_cast<uint8_t*>(out) + ent * kMixRow)
+            : FMT == CSA_FMT_FP8B32   ? (void*)(reinterpret_cast<uint8_t*>(out) + ent * C)
                                       : (void*)(reinterpret_cast<uint8_t*>(out) + ent * (C / 2));
+  constexpr bool kScales = FMT == CSA_FMT_MXFP4 || FMT == CSA_FMT_FP8B32;
   if (ZC)
     compress_entry_channel_logits<FMT, BF16>(reinterpret_cast<const uint8_t*>(x) + tok0 * C * esz, z + tok0 * C, s,
-                                             rcos, rsin, P, C, R, m, o,
-                                             FMT == CSA_FMT_MXFP4 ? out_scales + ent * (C / 32) : nullptr, lane);
+                                             rcos, rsin, P, C, R, m, o, kScales ? out_scales + ent * (C / 32) : nullptr,
+                                             lane);
   else
     compress_entry<FMT, BF16>(reinterpret_cast<const uint8_t*>(x) + tok0 * C * esz, z + tok0, s, rcos, rsin, P, C,
-                              R, m, o, FMT == CSA_FMT_MXFP4 ? out_scales + ent * (C / 32) : nullptr, alpha_s[warp],
-                              lane);
+                              R, m, o, kScales ? out_scales + ent * (C / 32) : nullptr, alpha_s[warp], lane);
 }
 
 // Decode-time cache maintenance, one CTA per sequence: the new token at
@@ -273,6 +287,7 @@ decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restri
                      uint8_t* __restrict__ cache, int64_t nmax, uint8_t* __restrict__ kI_codes,
                      uint8_t* __restrict__ kI_scales, uint8_t* __restrict__ swa, int64_t Ts, int W,
                      int64_t* __restrict__ swa_pos0) {
+  pdl_begin();
   __shared__ float alpha_s[3][128];
   __shared__ float z_s[2][128];              // the closing block's logits (cache, key)
   __shared__ float2 acc_s[(512 + 64) / 2];   // the closing block's pair sums: C/2 of the cache, CI/2 of the key
@@ -404,6 +419,7 @@ decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restri
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 pack_mixed_kernel(const float* __restrict__ v, int64_t n, uint8_t* __restrict__ out) {
+  pdl_begin();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
   if (row >= n) return;
@@ -425,16 +441,18 @@ cudaError_t launch_compress(const void* x, bool x_bf16, const float* z, bool z_p
 #define CSA_CK(F, BF)                                                                                 \
   do {                                                                                                \
     if (z_per_channel)                                                                                \
-      compress_kernel<F, BF, true><<<grid, block, 0, st>>>(x, z, s, rcos, rsin, pos0, B, T, C, R, m, N, out, \
+      launch_pdl(compress_kernel<F, BF, true>, dim3(grid), dim3(block), 0, st, x, z, s, rcos, rsin, pos0, B, T, C, R, m, N, out, \
                                                            out_scales);                               \
     else                                                                                              \
-      compress_kernel<F, BF, false><<<grid, block, 0, st>>>(x, z, s, rcos, rsin, pos0, B, T, C, R, m, N, out, \
+      launch_pdl(compress_kernel<F, BF, false>, dim3(grid), dim3(block), 0, st, x, z, s, rcos, rsin, pos0, B, T, C, R, m, N, out, \
                                                             out_scales);                              \
   } while (0)
   if (fmt == CSA_FMT_F32) {
     if (x_bf16) CSA_CK(CSA_FMT_F32, true); else CSA_CK(CSA_FMT_F32, false);
   } else if (fmt == CSA_FMT_MIXED592) {
     if (x_bf16) CSA_CK(CSA_FMT_MIXED592, true); else CSA_CK(CSA_FMT_MIXED592, false);
+  } else if (fmt == CSA_FMT_FP8B32) {
+    if (x_bf16) CSA_CK(CSA_FMT_FP8B32, true); else CSA_CK(CSA_FMT_FP8B32, false);
   } else {
     if (x_bf16) CSA_CK(CSA_FMT_MXFP4, true); else CSA_CK(CSA_FMT_MXFP4, false);
   }
@@ -453,7 +471,7 @@ cudaError_t launch_decode_append(const void* kv, const float* z, const void* kI,
   const size_t ring = (size_t)m * (C + CI) * 2;   // staged rows of a closing block
   static PerDevice attr;
   smem_limit_once(attr, reinterpret_cast<const void*>(decode_append_kernel), 128 * (512 + 64) * 2);
-  decode_append_kernel<<<(unsigned)B, kWarpsPerBlock * 32, ring, st>>>(
+  launch_pdl(decode_append_kernel, dim3((unsigned)B), dim3(kWarpsPerBlock * 32), ring, st, 
       reinterpret_cast<const __nv_bfloat16*>(kv), z, reinterpret_cast<const __nv_bfloat16*>(kI), zI, s, sI, rcos,
       rsin, rope_rows, t_pos, C, R, CI, m, reinterpret_cast<__nv_bfloat16*>(kv_tail), z_tail,
       reinterpret_cast<__nv_bfloat16*>(kI_tail), zI_tail, cache, nmax, kI_codes, kI_scales, swa, Ts, W, swa_pos0);
@@ -462,8 +480,7 @@ cudaError_t launch_decode_append(const void* kv, const float* z, const void* kI,
 
 cudaError_t launch_pack_mixed(const float* v, int64_t n, uint8_t* out, cudaStream_t st) {
   if (n == 0) return cudaSuccess;
-  pack_mixed_kernel<<<(unsigned)((n + kWarpsPerBlock - 1) / kWarpsPerBlock), kWarpsPerBlock * 32, 0,
-                      st>>>(v, n, out);
+  launch_pdl(pack_mixed_kernel, dim3((unsigned)((n + kWarpsPerBlock - 1) / kWarpsPerBlock)), dim3(kWarpsPerBlock * 32), 0, st, v, n, out);
   return cudaGetLastError();
 }
 

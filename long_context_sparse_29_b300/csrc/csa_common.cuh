@@ -39,6 +39,17 @@ __device__ __forceinline__ void flag_timeout(void* ws) {
   if (ws) atomicOr(&reinterpret_cast<Status*>(ws)->flags, CSA_FLAG_TIMEOUT);
 }
 
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the kernel before it on the stream finishes
+// (launch_pdl in launch.h).  It first lets its own dependents launch, then
+// waits until the grids it depends on have completed and their writes are
+// visible -- before it reads or writes any global memory -- so the order of
+// results is the stream order; only the launch latency overlaps.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // 2^n as fp32 for n in [-126, 127]
 __device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
 

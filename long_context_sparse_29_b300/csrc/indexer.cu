@@ -45,33 +45,15 @@ __device__ __forceinline__ float combine_blocks(int P0, int e0, int P1, int e1) 
   return __fadd_rn(scale_pow2((float)P0, e0), scale_pow2((float)P1, e1));
 }
 
-// ---------------------------------------------------------------------------
-// FP4 scores: grid (entry chunks, query tiles, B); one thread per entry.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kScoreThreads)
-scores_fp4_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
-                  const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
-                  const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
-                  float* __restrict__ scores) {
-  // int8 (2 * E2M1) query values, 64 per head; block exponents; weights
-  __shared__ __align__(16) int32_t qv_s[kScoreQT][kMaxHI][16];
-  __shared__ int8_t qe_s[kScoreQT][kMaxHI][2];
-  __shared__ float w_s[kScoreQT][kMaxHI];
-  __shared__ int64_t nv_s[kScoreQT];
-  const int b = blockIdx.z;
-  const int64_t q0 = (int64_t)blockIdx.y * kScoreQT;
-  const int nq = (int)(Tq - q0 < kScoreQT ? Tq - q0 : kScoreQT);
-  const int64_t j0 = (int64_t)blockIdx.x * kScoreThreads;
-  const int tid = threadIdx.x;
-
-  if (tid < kScoreQT) nv_s[tid] = tid < nq ? visible_entries(q_pos[b * Tq + q0 + tid], m, N) : 0;
-  __syncthreads();
-  int64_t nv_max = 0;
-  for (int q = 0; q < nq; ++q) nv_max = nv_max > nv_s[q] ? nv_max : nv_s[q];
-  if (j0 >= nv_max) return;   // no query of the tile sees this chunk
-
-  // quantise the tile's queries: one (query, head, block) of 32 elements per step
-  for (int u = tid; u < nq * HI * 2; u += kScoreThreads) {
+// The MXFP4 queries of a tile of nq rows (q0 ..) of sequence b into shared
+// memory: per (query, head) 64 doubled E2M1 values as int8 (four per word),
+// the two block exponents, and the head weights.  One (query, head, block)
+// of 32 elements per thread and step.
+__device__ __forceinline__ void quantise_query_tile(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
+                                                    int b, int64_t Tq, int64_t q0, int nq, int HI,
+                                                    int32_t (*qv_s)[kMaxHI][16], int8_t (*qe_s)[kMaxHI][2],
+                                                    float (*w_s)[kMaxHI]) {
+  for (int u = threadIdx.x; u < nq * HI * 2; u += blockDim.x) {
     const int q = u / (HI * 2), h = (u / 2) % HI, blk = u & 1;
     const __nv_bfloat16* src = qI + (((b * Tq + q0 + q) * HI + h) * 64 + 32 * blk);
     float v[32];
@@ -95,8 +77,36 @@ scores_fp4_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict_
     }
     qe_s[q][h][blk] = (int8_t)sx;
   }
-  for (int u = tid; u < nq * HI; u += kScoreThreads)
-    w_s[u / HI][u % HI] = w[(b * Tq + q0) * HI + u];
+  for (int u = threadIdx.x; u < nq * HI; u += blockDim.x) w_s[u / HI][u % HI] = w[(b * Tq + q0) * HI + u];
+}
+
+// ---------------------------------------------------------------------------
+// FP4 scores: grid (entry chunks, query tiles, B); one thread per entry.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScoreThreads)
+scores_fp4_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
+                  const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
+                  const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
+                  float* __restrict__ scores) {
+  pdl_begin();
+  // int8 (2 * E2M1) query values, 64 per head; block exponents; weights
+  __shared__ __align__(16) int32_t qv_s[kScoreQT][kMaxHI][16];
+  __shared__ int8_t qe_s[kScoreQT][kMaxHI][2];
+  __shared__ float w_s[kScoreQT][kMaxHI];
+  __shared__ int64_t nv_s[kScoreQT];
+  const int b = blockIdx.z;
+  const int64_t q0 = (int64_t)blockIdx.y * kScoreQT;
+  const int nq = (int)(Tq - q0 < kScoreQT ? Tq - q0 : kScoreQT);
+  const int64_t j0 = (int64_t)blockIdx.x * kScoreThreads;
+  const int tid = threadIdx.x;
+
+  if (tid < kScoreQT) nv_s[tid] = tid < nq ? visible_entries(q_pos[b * Tq + q0 + tid], m, N) : 0;
+  __syncthreads();
+  int64_t nv_max = 0;
+  for (int q = 0; q < nq; ++q) nv_max = nv_max > nv_s[q] ? nv_max : nv_s[q];
+  if (j0 >= nv_max) return;   // no query of the tile sees this chunk
+
+  quantise_query_tile(qI, w, b, Tq, q0, nq, HI, qv_s, qe_s, w_s);
   __syncthreads();
 
   const int64_t j = j0 + tid;
@@ -150,6 +160,143 @@ scores_fp4_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict_
 }
 
 // ---------------------------------------------------------------------------
+// FP4-query x FP8-key scores (keys: E4M3 codes with a power-of-two scale per
+// 32 channels).  xmsumi.com DeepSeek-V4 article, section "算力与内存效率":
+// an FP4 x FP8 product runs at the FP8 rate; zcldvi.com article: FP4 -> FP8
+// dequantisation is lossless.
+//
+// Exact integer form: twice an E2M1 value is an integer in [-12, 12] and 512
+// times an E4M3 value an integer below 2^18, so a 32-element block dot is an
+// integer P with |P| <= 32 * 12 * 229376 < 2^27, worth P 2^(e_q + e_k - 10).
+// The head's dot is the exact sum of its two blocks rounded once to fp32:
+// both are put on one integer scale in 64 bits (when their exponents are more
+// than 35 apart the smaller is folded in as a sticky bit, round to odd), then
+// converted with one rounding.
+// ---------------------------------------------------------------------------
+
+// 512 x the value of an E4M3 code, as a signed integer (exact; NaN codes
+// are never stored)
+__device__ __forceinline__ int e4m3_x512(uint32_t c) {
+  const int E = (int)((c >> 3) & 15u), M = (int)(c & 7u);
+  const int mag = E == 0 ? M : (8 + M) << (E - 1);
+  return (c & 0x80u) ? -mag : mag;
+}
+
+// RN(S 2^es) as fp32 with one rounding, subnormal results included.
+__device__ __forceinline__ float ll_scaled_rn(long long S, int es) {
+  if (S == 0) return 0.0f;
+  const unsigned long long a = S < 0 ? 0ull - (unsigned long long)S : (unsigned long long)S;
+  const int E = es + (63 - __clzll((long long)a));   // the value lies in [2^E, 2^(E+1))
+  if (E >= -126) return scale_pow2(__ll2float_rn(S), es);   // rounded integer, scaled exactly
+  // subnormal: nearest multiple of 2^-149, ties to even
+  const int t = es + 149;
+  long long q;
+  if (t >= 0) {
+    q = S << t;   // below 2^23 here
+  } else if (-t >= 64) {
+    q = 0;        // below half of 2^-149
+  } else {
+    const int sh = -t;
+    q = S >> sh;
+    const unsigned long long r = (unsigned long long)(S - (q << sh));
+    const unsigned long long half = 1ull << (sh - 1);
+    if (r > half || (r == half && (q & 1))) q += 1;
+  }
+  if (q == 0) return S < 0 ? -0.0f : 0.0f;
+  return __fmul_rn(__fmul_rn((float)q, 0x1p-23f), 0x1p-126f);
+}
+
+// RN(P0 2^e0 + P1 2^e1) for integer block dots |P| < 2^27, one rounding.
+__device__ __forceinline__ float fp8k_combine(int P0, int e0, int P1, int e1) {
+  int Ph = P0, eh = e0, Pl = P1, el = e1;
+  if (P0 == 0 || (P1 != 0 && e1 > e0)) {
+    Ph = P1;
+    eh = e1;
+    Pl = P0;
+    el = e0;
+  }
+  if (Ph == 0) return 0.0f;
+  if (Pl == 0) return ll_scaled_rn(Ph, eh);
+  const int d = eh - el;
+  if (d <= 35) return ll_scaled_rn(((long long)Ph << d) + Pl, el);   // |sum| < 2^62: exact
+  // Pl lies below bit 0 of Ph 2^35 (Ph != 0 has at least 36 bits there, so
+  // the rounding position is bit 12 or higher): floor it onto that grid and
+  // keep whether anything was dropped in bit 0 (round to odd) -- the odd
+  // integer and the exact value round alike
+  const int sh = d - 35;
+  long long u;
+  bool rem;
+  if (sh >= 40) {
+    u = Pl < 0 ? -1 : 0;
+    rem = true;
+  } else {
+    u = (long long)Pl >> sh;
+    rem = ((long long)Pl - (u << sh)) != 0;
+  }
+  long long S = ((long long)Ph << 35) + u;
+  if (rem) S |= 1;
+  return ll_scaled_rn(S, eh - 35);
+}
+
+__global__ void __launch_bounds__(kScoreThreads)
+scores_fp8k_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
+                   const uint8_t* __restrict__ kc8, const uint8_t* __restrict__ ks8,
+                   const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
+                   float* __restrict__ scores) {
+  pdl_begin();
+  __shared__ __align__(16) int32_t qv_s[kScoreQT][kMaxHI][16];
+  __shared__ int8_t qe_s[kScoreQT][kMaxHI][2];
+  __shared__ float w_s[kScoreQT][kMaxHI];
+  __shared__ int64_t nv_s[kScoreQT];
+  const int b = blockIdx.z;
+  const int64_t q0 = (int64_t)blockIdx.y * kScoreQT;
+  const int nq = (int)(Tq - q0 < kScoreQT ? Tq - q0 : kScoreQT);
+  const int64_t j0 = (int64_t)blockIdx.x * kScoreThreads;
+  const int tid = threadIdx.x;
+  if (tid < kScoreQT) nv_s[tid] = tid < nq ? visible_entries(q_pos[b * Tq + q0 + tid], m, N) : 0;
+  __syncthreads();
+  int64_t nv_max = 0;
+  for (int q = 0; q < nq; ++q) nv_max = nv_max > nv_s[q] ? nv_max : nv_s[q];
+  if (j0 >= nv_max) return;   // no query of the tile sees this chunk
+  quantise_query_tile(qI, w, b, Tq, q0, nq, HI, qv_s, qe_s, w_s);
+  __syncthreads();
+  const int64_t j = j0 + tid;
+  if (j >= nv_max) return;
+  // the key: 64 E4M3 codes as integers (512 x value) and its two block exponents
+  int kv[64];
+  const uint4* src = reinterpret_cast<const uint4*>(kc8 + (b * N + j) * 64);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 c = src[i];
+    const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int e = 0; e < 16; ++e) kv[16 * i + e] = e4m3_x512((wd[e >> 2] >> (8 * (e & 3))) & 0xffu);
+  }
+  const int ke0 = (int)ks8[(b * N + j) * 2] - 127, ke1 = (int)ks8[(b * N + j) * 2 + 1] - 127;
+  for (int q = 0; q < nq; ++q) {
+    if (j >= nv_s[q]) continue;
+    float s = 0.0f;
+    for (int h = 0; h < HI; ++h) {
+      const int4* qv4 = reinterpret_cast<const int4*>(qv_s[q][h]);
+      int P[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int4 a = qv4[i];
+        const int aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int qv = (aw[e >> 2] << (24 - 8 * (e & 3))) >> 24;   // signed byte e & 3
+          P[i >> 1] += qv * kv[16 * i + e];
+        }
+      }
+      const float d = fp8k_combine(P[0], qe_s[q][h][0] + ke0 - 10, P[1], qe_s[q][h][1] + ke1 - 10);
+      s = __fmaf_rn(w_s[q][h], d > 0.0f ? d : 0.0f, s);
+    }
+    scores[(b * Tq + q0 + q) * N + j] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // FP4 scores for few query rows against long entry lists (decode): grid
 // (entry chunks, rows), the chunk length chosen by the host so that the grid
 // fills the resident CTA slots of the GPU about once; the row's query is
@@ -190,6 +337,7 @@ scores_fp4_decode_kernel(const __nv_bfloat16* __restrict__ qI, const float* __re
                          const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
                          const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
                          int64_t chunk, float* __restrict__ scores) {
+  pdl_begin();
   // doubled query values: head h, block b, group i (8 elements): word [h][b][0][i] even
   // elements, [h][b][1][i] odd elements of the group
   __shared__ __align__(16) int32_t qv_s[kMaxHI][2][2][4];
@@ -310,6 +458,7 @@ __global__ void __launch_bounds__(kScoreThreads)
 scores_f32_kernel(const float* __restrict__ qI, const float* __restrict__ w,
                   const float* __restrict__ kI, const int64_t* __restrict__ q_pos, int64_t Tq,
                   int HI, int dI, int64_t N, int m, float* __restrict__ scores) {
+  pdl_begin();
   __shared__ float q_s[kScoreQT][512];   // HI * dI <= 512
   __shared__ float w_s[kScoreQT][kMaxHI];
   __shared__ int64_t nv_s[kScoreQT];
@@ -599,6 +748,7 @@ __device__ __forceinline__ void emit_topk(const unsigned long long* sorted, int 
 __global__ void __launch_bounds__(kTopkRowThreads)
 topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int P,
             int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
+  pdl_begin();
   constexpr int NT = kTopkRowThreads;
   extern __shared__ unsigned long long keys_s[];   // 2 P composite keys
   __shared__ TkShared<NT> sh;
@@ -622,6 +772,7 @@ topk_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos,
 __global__ void __launch_bounds__(kTopkThreads)
 topk_stage1_kernel(const float* __restrict__ scores, const int64_t* __restrict__ q_pos, int64_t N, int m, int k,
                    int chunks, int64_t C, bool stage, unsigned long long* __restrict__ cand) {
+  pdl_begin();
   constexpr int NT = kTopkThreads;
   extern __shared__ __align__(16) float chunk_s[];
   __shared__ TkShared<NT> sh;
@@ -652,6 +803,7 @@ __global__ void __launch_bounds__(kTopkThreads)
 topk_stage2_kernel(const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int chunks, int P, bool stage,
                    const unsigned long long* __restrict__ cand, int32_t* __restrict__ idx_out,
                    float* __restrict__ score_out) {
+  pdl_begin();
   constexpr int NT = kTopkThreads;
   // 2 P composite keys, then (stage) the row's chunks x k candidates
   extern __shared__ __align__(16) unsigned long long keys_s[];
@@ -698,15 +850,23 @@ bool topk_two_stage(int B, int64_t Tq, int64_t N) {
   return N > kTkChunk && (int64_t)B * Tq < 4 * 148;
 }
 
-cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
+cudaError_t launch_indexer_topk(const void* qI, int key_fmt, const float* w, const void* kI,
                                 const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
                                 int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
                                 float* score_out, float* scores_ws, void* tc_ws, void* cand_ws, void* flags_ws,
                                 bool tensor_cores, cudaStream_t st) {
   if ((int64_t)B * Tq == 0) return cudaSuccess;
+  const bool fp4 = key_fmt == CSA_FMT_MXFP4;
   if (N > 0) {
     cudaError_t e;
-    if (fp4 && tc_ws && indexer_tc_applies(B, Tq, HI, dI, N)) {
+    if (key_fmt == CSA_FMT_FP8B32) {
+      const dim3 grid((unsigned)((N + kScoreThreads - 1) / kScoreThreads),
+                      (unsigned)((Tq + kScoreQT - 1) / kScoreQT), (unsigned)B);
+      launch_pdl(scores_fp8k_kernel, dim3(grid), dim3(kScoreThreads), 0, st, reinterpret_cast<const __nv_bfloat16*>(qI), w,
+                                                         reinterpret_cast<const uint8_t*>(kI), kI_scales, q_pos, Tq,
+                                                         HI, N, m, scores_ws);
+      e = cudaGetLastError();
+    } else if (fp4 && tc_ws && indexer_tc_applies(B, Tq, HI, dI, N)) {
       e = launch_indexer_scores_tc(qI, w, reinterpret_cast<const uint8_t*>(kI), kI_scales, q_pos, B, Tq, HI, N,
                                    m, scores_ws, tc_ws, flags_ws, st);
     } else if (fp4 && tensor_cores && decode_tc_applies(Tq, HI, dI, N)) {
@@ -715,7 +875,7 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
     } else if (fp4 && dI == 64 && Tq <= 4 && HI <= kMaxHI && N >= 8 * kDecRound) {
       const int64_t chunk = decode_chunk(N, (int64_t)B * Tq);
       const dim3 grid((unsigned)((N + chunk - 1) / chunk), (unsigned)(B * Tq));
-      scores_fp4_decode_kernel<<<grid, kScoreThreads, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(qI), w,
+      launch_pdl(scores_fp4_decode_kernel, dim3(grid), dim3(kScoreThreads), 0, st, reinterpret_cast<const __nv_bfloat16*>(qI), w,
                                                                reinterpret_cast<const uint8_t*>(kI), kI_scales,
                                                                q_pos, Tq, HI, N, m, chunk, scores_ws);
       e = cudaGetLastError();
@@ -723,11 +883,11 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
       const dim3 grid((unsigned)((N + kScoreThreads - 1) / kScoreThreads),
                       (unsigned)((Tq + kScoreQT - 1) / kScoreQT), (unsigned)B);
       if (fp4)
-        scores_fp4_kernel<<<grid, kScoreThreads, 0, st>>>(
+        launch_pdl(scores_fp4_kernel, dim3(grid), dim3(kScoreThreads), 0, st, 
             reinterpret_cast<const __nv_bfloat16*>(qI), w, reinterpret_cast<const uint8_t*>(kI),
             kI_scales, q_pos, Tq, HI, N, m, scores_ws);
       else
-        scores_f32_kernel<<<grid, kScoreThreads, 0, st>>>(reinterpret_cast<const float*>(qI), w,
+        launch_pdl(scores_f32_kernel, dim3(grid), dim3(kScoreThreads), 0, st, reinterpret_cast<const float*>(qI), w,
                                                           reinterpret_cast<const float*>(kI), q_pos,
                                                           Tq, HI, dI, N, m, scores_ws);
       e = cudaGetLastError();
@@ -747,12 +907,12 @@ cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const 
     // stage a chunk's scores / a row's candidates in shared memory when they fit
     const int64_t C = topk_chunk_size(N, k);
     const bool st1 = (size_t)C * 4 <= kTkStageMax, st2 = smem + (size_t)ch * k * 8 <= kTkStageMax;
-    topk_stage1_kernel<<<dim3((unsigned)rows, (unsigned)ch), kTopkThreads, st1 ? (size_t)C * 4 : 0, st>>>(
+    launch_pdl(topk_stage1_kernel, dim3(dim3((unsigned)rows, (unsigned)ch)), dim3(kTopkThreads), st1 ? (size_t)C * 4 : 0, st, 
         scores_ws, q_pos, N, m, k, ch, C, st1, cand);
-    topk_stage2_kernel<<<(unsigned)rows, kTopkThreads, st2 ? smem + (size_t)ch * k * 8 : smem, st>>>(
+    launch_pdl(topk_stage2_kernel, dim3((unsigned)rows), dim3(kTopkThreads), st2 ? smem + (size_t)ch * k * 8 : smem, st, 
         q_pos, N, m, k, ch, P, st2, cand, idx_out, score_out);
   } else {
-    topk_kernel<<<(unsigned)rows, kTopkRowThreads, smem, st>>>(scores_ws, q_pos, N, m, k, P, idx_out, score_out);
+    launch_pdl(topk_kernel, dim3((unsigned)rows), dim3(kTopkRowThreads), smem, st, scores_ws, q_pos, N, m, k, P, idx_out, score_out);
   }
   return cudaGetLastError();
 }

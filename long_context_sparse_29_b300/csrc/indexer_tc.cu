@@ -92,6 +92,7 @@ __device__ __forceinline__ int64_t visible(int64_t t, int m, int64_t N) {
 __global__ void __launch_bounds__(256)
 ix_quant_q_kernel(const __nv_bfloat16* __restrict__ qI, int64_t rows, int HI, uint8_t* __restrict__ qx,
                   int8_t* __restrict__ qe) {
+  pdl_begin();
   const int64_t u = (int64_t)blockIdx.x * 256 + threadIdx.x;
   if (u >= rows * HI * 2) return;
   const int64_t rh = u >> 1;        // row * HI + h
@@ -132,6 +133,7 @@ ix_quant_q_kernel(const __nv_bfloat16* __restrict__ qI, int64_t rows, int HI, ui
 // swizzled TMA layout).  One thread per (entry, 16-byte output unit).
 __global__ void __launch_bounds__(256)
 ix_expand_k_kernel(const uint8_t* __restrict__ kc, int64_t n, uint8_t* __restrict__ kx) {
+  pdl_begin();
   const int64_t u = (int64_t)blockIdx.x * 256 + threadIdx.x;
   if (u >= n * 8) return;
   const int64_t key = u >> 3;
@@ -167,6 +169,7 @@ struct IxParams {
 
 __global__ void __launch_bounds__(kIxThreads, 1)
 ix_scores_tc_kernel(const IxParams p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k) {
+  pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   IxMisc* ms = reinterpret_cast<IxMisc*>(sm + kIxMiscOff);
@@ -456,6 +459,7 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
                             const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
                             const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
                             int64_t chunk, float* __restrict__ scores, void* ws) {
+  pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DtMisc* ms = reinterpret_cast<DtMisc*>(sm + kDtMiscOff);
@@ -687,9 +691,9 @@ cudaError_t launch_indexer_scores_tc(const void* qI, const float* w, const uint8
   int8_t* qe = reinterpret_cast<int8_t*>(base + al256((size_t)rows * HI * 64));
   uint8_t* kx = base + al256((size_t)rows * HI * 64) + al256((size_t)rows * HI * 2);
   const int64_t nq = rows * HI * 2, nk = (int64_t)B * N * 8;
-  ix_quant_q_kernel<<<(unsigned)((nq + 255) / 256), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(qI), rows,
+  launch_pdl(ix_quant_q_kernel, dim3((unsigned)((nq + 255) / 256)), dim3(256), 0, st, reinterpret_cast<const __nv_bfloat16*>(qI), rows,
                                                                  HI, qx, qe);
-  ix_expand_k_kernel<<<(unsigned)((nk + 255) / 256), 256, 0, st>>>(kc, (int64_t)B * N, kx);
+  launch_pdl(ix_expand_k_kernel, dim3((unsigned)((nk + 255) / 256)), dim3(256), 0, st, kc, (int64_t)B * N, kx);
   CUtensorMap tm_q, tm_k;
   if (!ix_byte_map(&tm_q, qx, (uint64_t)HI * 64, (uint64_t)rows, kIxRows)) return cudaErrorInvalidValue;
   if (!ix_byte_map(&tm_k, kx, 128, (uint64_t)B * N, kIxKeys)) return cudaErrorInvalidValue;
@@ -707,7 +711,7 @@ cudaError_t launch_indexer_scores_tc(const void* qI, const float* w, const uint8
   static PerDevice attr;
   smem_limit_once(attr, reinterpret_cast<const void*>(ix_scores_tc_kernel), (int)kIxSmem);
   const dim3 grid((unsigned)((N + kIxChunk - 1) / kIxChunk), (unsigned)((Tq + kIxRows - 1) / kIxRows), (unsigned)B);
-  ix_scores_tc_kernel<<<grid, kIxThreads, kIxSmem, st>>>(p, tm_q, tm_k);
+  launch_pdl(ix_scores_tc_kernel, dim3(grid), dim3(kIxThreads), kIxSmem, st, p, tm_q, tm_k);
   return cudaGetLastError();
 }
 
@@ -715,6 +719,7 @@ cudaError_t launch_indexer_scores_tc(const void* qI, const float* w, const uint8
 // nothing completes, with the same bounded wait every kernel here uses, and
 // records the expiry in the workspace's status flags.
 __global__ void wait_selftest_kernel(void* ws, uint32_t polls) {
+  pdl_begin();
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -725,7 +730,7 @@ __global__ void wait_selftest_kernel(void* ws, uint32_t polls) {
 }
 
 cudaError_t launch_wait_selftest(void* ws, uint32_t polls, cudaStream_t st) {
-  wait_selftest_kernel<<<1, 32, 0, st>>>(ws, polls);
+  launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, st, ws, polls);
   return cudaGetLastError();
 }
 
@@ -751,7 +756,7 @@ cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const ui
   chunk = (chunk + kDtThreads - 1) / kDtThreads * kDtThreads;
   if (chunk < 2 * kDtThreads) chunk = 2 * kDtThreads;
   const dim3 grid((unsigned)((N + chunk - 1) / chunk), (unsigned)rows);
-  scores_fp4_decode_tc_kernel<<<grid, kDtThreads, kDtSmem, st>>>(reinterpret_cast<const __nv_bfloat16*>(qI), w, kc,
+  launch_pdl(scores_fp4_decode_tc_kernel, dim3(grid), dim3(kDtThreads), kDtSmem, st, reinterpret_cast<const __nv_bfloat16*>(qI), w, kc,
                                                                  ks, q_pos, Tq, HI, N, m, chunk, scores, flags_ws);
   return cudaGetLastError();
 }

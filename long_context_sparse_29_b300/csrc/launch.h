@@ -30,6 +30,25 @@ class PerDevice {
   std::atomic<int> v_[kMaxDevices]{};
 };
 
+// Launches `kernel` on `st` with programmatic stream serialisation allowed:
+// the kernel may be scheduled while the previous kernel on the stream is
+// still running; it waits for it (pdl_begin) before touching memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
 // device, once per device and call site (`once`).
 inline void smem_limit_once(PerDevice& once, const void* kernel, int bytes) {
@@ -91,7 +110,9 @@ cudaError_t launch_decode_append(const void* kv, const float* z, const void* kI,
                                  float* zI_tail, uint8_t* cache, int64_t nmax, uint8_t* kI_codes,
                                  uint8_t* kI_scales, uint8_t* swa, int64_t Ts, int W, int64_t* swa_pos0,
                                  cudaStream_t st);
-cudaError_t launch_indexer_topk(const void* qI, bool fp4, const float* w, const void* kI,
+// key_fmt: CSA_FMT_MXFP4 or CSA_FMT_FP8B32 (bf16 queries, quantised to MXFP4
+// inside) or CSA_FMT_F32 (fp32 queries)
+cudaError_t launch_indexer_topk(const void* qI, int key_fmt, const float* w, const void* kI,
                                 const uint8_t* kI_scales, const int64_t* q_pos, int B, int64_t Tq,
                                 int HI, int dI, int64_t N, int m, int k, int32_t* idx_out,
                                 float* score_out, float* scores_ws, void* tc_ws, void* cand_ws, void* flags_ws,

@@ -82,11 +82,12 @@ extern "C" int csa_indexer_topk_noalloc(const void* qI, int qI_dtype, const floa
   if (k < 1 || k > 4096)
     return csa::report_error(CSA_ERR_UNSUPPORTED, "csa_indexer_topk_noalloc: k must be in [1, 4096]");
   const bool fp4 = qI_dtype == CSA_DTYPE_BF16 && kI_fmt == CSA_FMT_MXFP4;
+  const bool fp8k = qI_dtype == CSA_DTYPE_BF16 && kI_fmt == CSA_FMT_FP8B32;
   const bool f32 = qI_dtype == CSA_DTYPE_F32 && kI_fmt == CSA_FMT_F32;
-  if (!fp4 && !f32)
+  if (!fp4 && !fp8k && !f32)
     return csa::report_error(CSA_ERR_UNSUPPORTED, "csa_indexer_topk_noalloc: dtype/format pair not supported");
-  if (fp4 && (dI != 64 || HI > 32))
-    return csa::report_error(CSA_ERR_UNSUPPORTED, "csa_indexer_topk_noalloc: FP4 path needs dI=64, HI<=32");
+  if ((fp4 || fp8k) && (dI != 64 || HI > 32))
+    return csa::report_error(CSA_ERR_UNSUPPORTED, "csa_indexer_topk_noalloc: FP4 / FP8 keys need dI=64, HI<=32");
   if (f32 && (dI > 64 || HI > 32 || HI * dI > 512))
     return csa::report_error(CSA_ERR_UNSUPPORTED,
                              "csa_indexer_topk_noalloc: fp32 path needs dI<=64, HI<=32, HI*dI<=512");
@@ -96,12 +97,12 @@ extern "C" int csa_indexer_topk_noalloc(const void* qI, int qI_dtype, const floa
                              "csa_indexer_topk_noalloc: B*Tq*N scores exceed the built-in 16 MiB scratch "
                              "(4194304 scores); use csa_indexer_topk with a workspace");
   if ((int64_t)B * Tq == 0) return CSA_OK;
-  if (!qI || !w || !q_pos || !idx_out || (N > 0 && !kI) || (fp4 && N > 0 && !kI_scales))
+  if (!qI || !w || !q_pos || !idx_out || (N > 0 && !kI) || ((fp4 || fp8k) && N > 0 && !kI_scales))
     return csa::report_error(CSA_ERR_INVALID_ARG, "csa_indexer_topk_noalloc: NULL pointer");
   void* scratch = nullptr;
   const int r = scratch_address(&scratch);
   if (r != CSA_OK) return r;
-  const cudaError_t e = csa::launch_indexer_topk(qI, fp4, w, kI, kI_scales, q_pos, B, Tq, HI, dI, N, m,
+  const cudaError_t e = csa::launch_indexer_topk(qI, kI_fmt, w, kI, kI_scales, q_pos, B, Tq, HI, dI, N, m,
                                                  k, idx_out, score_out, reinterpret_cast<float*>(scratch),
                                                  nullptr, nullptr, nullptr, /*tensor_cores=*/false,
                                                  reinterpret_cast<cudaStream_t>(stream));
