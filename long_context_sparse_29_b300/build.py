@@ -13,8 +13,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 SO = os.path.join(HERE, "libcsa_b300.so")
 OBJ = os.path.join(os.path.dirname(HERE), "_build", "csa_b300")
-SOURCES = ["abi.cu", "compress.cu", "indexer.cu", "indexer_tc.cu", "attn_simt.cu", "attn_tc.cu", "noalloc.cu"]
-HEADERS = ["csa_common.cuh", "launch.h", "tc_ptx.cuh"]
+SOURCES = ["abi.cu", "compress.cu", "indexer.cu", "indexer_tc.cu", "attn_simt.cu", "attn_tc.cu", "attn_decode.cu",
+           "noalloc.cu"]
+HEADERS = ["csa_common.cuh", "launch.h", "tc_ptx.cuh", "attn_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

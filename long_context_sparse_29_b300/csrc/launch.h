@@ -153,6 +153,10 @@ cudaError_t launch_indexer_scores_tc(const void* qI, const float* w, const uint8
                                      const int64_t* q_pos, int B, int64_t Tq, int HI, int64_t N, int m,
                                      float* scores, void* tc_ws, void* flags_ws, cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t st);
+// decode attention (attn_decode.cu): few rows, every step in one launch
+bool attn_decode_applies(int H, int D, int R, int64_t rows, int k, bool sparse);
+size_t attn_decode_workspace(int64_t rows, int64_t max_keys);
+cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t st);
 size_t attn_tc_workspace(int B, int64_t Tq, int H, int D, int64_t max_keys, int64_t N, int64_t Ts, int k);
 

@@ -1,0 +1,116 @@
+"""The one-launch decode attention (few query rows) against the oracle and
+against the long-row path (CSA_ATTN_DECODE=0), through the C ABI.
+
+Decode rows split their keys over many CTAs that merge their partial
+softmax states in-kernel; these cases cover one row spread over the most
+splits, rows whose splits are partly empty, rows without keys, sparse and
+dense key lists, and an invalid index.  Outputs must match the oracle within
+max|err| <= 1e-2 max|ref| (bf16 outputs, fp32 accumulation).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_common import dev, dev_bf16, max_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csa():
+    from long_context_sparse_29_b300 import build
+    build.build()
+    import long_context_sparse_29_b300 as m
+    return m
+
+
+def _caches(oracle_mod, rng, B, N, Ts):
+    cache = np.stack([oracle_mod.pack_mixed(rng.standard_normal((N, 512)).astype(np.float32)) for _ in range(B)])
+    swa = np.stack([oracle_mod.pack_mixed(rng.standard_normal((Ts, 512)).astype(np.float32)) for _ in range(B)])
+    return cache, swa
+
+
+@pytest.mark.parametrize("B,N,m,k,W", [
+    (1, 8192, 128, 0, 128),      # one row over ~130 splits (dense HCA)
+    (4, 8192, 128, 0, 128),      # the 1M HCA decode shape
+    (32, 8192, 4, 1024, 128),    # the CSA decode shape: 32 rows, k = 1024
+    (3, 4096, 4, 300, 37),       # ragged tiles, few splits each
+    (7, 2048, 4, 64, 0),         # one tile per row: most splits empty
+])
+def test_decode_attention_matches_oracle_and_long_row_path(csa, oracle_mod, monkeypatch, B, N, m, k, W):
+    rng = np.random.default_rng(1000 + B + k)
+    T = N * m
+    Ts = 256
+    rope_np, rope_dev = oracle_mod.rope_table(T + 1, 64), csa.rope_table(T + 1, 64)
+    cache, swa = _caches(oracle_mod, rng, B, N, Ts)
+    q = wl.f32_to_bf16_bits(rng.standard_normal((B, 1, 64, 512)).astype(np.float32))
+    q_pos = (T - 1 - rng.integers(0, 64, size=(B, 1))).astype(np.int64)
+    pos0 = (q_pos[:, 0] - Ts + 1 + rng.integers(0, 32, size=B)).astype(np.int64)   # windows inside the buffer
+    idx = None
+    if k:
+        idx = np.full((B, 1, k), -1, np.int32)
+        for b in range(B):
+            nv = min(N, (q_pos[b, 0] + 1) // m)
+            sel = rng.permutation(nv)[:k - 3]
+            idx[b, 0, :len(sel)] = sel                     # a few -1 pads at the end
+    scale = 1 / math.sqrt(512)
+    args = (dev_bf16(q), dev(q_pos), dev(cache), m)
+    rest = (dev(swa), dev(pos0), W, scale, rope_dev)
+
+    def run():
+        ws = csa.Workspace()
+        if k:
+            o, l = csa.sparse_mqa(*args, dev(idx), *rest, lse=True, ws=ws)
+        else:
+            o, l = csa.hca_dense_attn(*args, *rest, lse=True, ws=ws)
+        torch.cuda.synchronize()
+        assert ws.flags() == 0
+        return o.float().cpu().numpy(), l.cpu().numpy()
+
+    got, glse = run()
+    again, _ = run()
+    np.testing.assert_array_equal(got, again)            # deterministic
+    monkeypatch.setenv("CSA_ATTN_DECODE", "0")
+    alt, _ = run()
+    monkeypatch.delenv("CSA_ATTN_DECODE")
+    ref, rlse, bad = oracle_mod.attention(wl.bf16_bits_to_f32(q), q_pos, cache, N, m, idx, swa, pos0, W, scale,
+                                          rope_np, 64)
+    assert bad == 0
+    assert max_rel_err(got, ref) <= 1e-2, max_rel_err(got, ref)
+    assert max_rel_err(alt, ref) <= 1e-2
+    np.testing.assert_allclose(glse, rlse, rtol=0, atol=2e-2)
+
+
+def test_decode_rows_without_keys_and_invalid_positions(csa, oracle_mod):
+    """A batch where one row has no keys (position 0, no window) and one row's
+    position has no RoPE row: zeros and -inf for them, the device-check flag
+    for the bad position, the other rows unaffected."""
+    rng = np.random.default_rng(2000)
+    B, N, m, W, Ts = 4, 1024, 4, 16, 64
+    T = N * m
+    rope_np, rope_dev = oracle_mod.rope_table(T + 1, 64), csa.rope_table(T + 1, 64)
+    cache, swa = _caches(oracle_mod, rng, B, N, Ts)
+    q = wl.f32_to_bf16_bits(rng.standard_normal((B, 1, 64, 512)).astype(np.float32))
+    q_pos = np.array([[T - 1], [2], [T + 50], [T - 7]], np.int64)   # row 2: no RoPE row for it
+    pos0 = np.array([T - Ts, 0, T - Ts, T - Ts], np.int64)
+    idx = np.full((B, 1, 40), -1, np.int32)
+    for b in (0, 3):
+        idx[b, 0] = rng.permutation(N)[:40]
+    ws = csa.Workspace()
+    out, lse = csa.sparse_mqa(dev_bf16(q), dev(q_pos), dev(cache), m, dev(idx), dev(swa), dev(pos0), W,
+                              1 / math.sqrt(512), rope_dev, lse=True, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.flags() & csa.FLAG_DEVICE_CHECK
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
+    good = [0, 3]
+    ref, _, _ = oracle_mod.attention(wl.bf16_bits_to_f32(q[good]), q_pos[good], cache[good], N, m, idx[good],
+                                     swa[good], pos0[good], W, 1 / math.sqrt(512), rope_np, 64)
+    assert max_rel_err(out[good], ref) <= 1e-2
+    # row 1 (t = 2): entries need 4 tokens, so only the window (tokens 0..2)
+    ref1, _, _ = oracle_mod.attention(wl.bf16_bits_to_f32(q[1:2]), q_pos[1:2], cache[1:2], N, m, idx[1:2],
+                                      swa[1:2], pos0[1:2], W, 1 / math.sqrt(512), rope_np, 64)
+    assert max_rel_err(out[1:2], ref1) <= 1e-2
