@@ -72,7 +72,7 @@ constexpr float kLazy = 8.0f;
 
 struct Misc {
   uint64_t raw_full[2], kv_full[2], kv_empty[2], s_full[2], p_full[2];
-  uint64_t q_full, q_ready, o_full, drain[2];
+  uint64_t q_full, q_ready, o_full, drain[2], merge_in;
   uint32_t tmem;
   int abort;
   int cnt[4];                       // valid selected entries per producer warp's share of idx
@@ -149,6 +149,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->drain[0], 1);
     mbar_init(&ms->drain[1], 1);
+    mbar_init(&ms->merge_in, 1);
     mbar_fence_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&ms->tmem, kTmemCols);
@@ -565,7 +566,10 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
       for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
     }
     if (bad) fail = true;
-    __threadfence();   // the partial is visible to the row's other items before the arrival below
+    // the partial is visible to the row's other items (read there by bulk
+    // copies: the async proxy) before the arrival below
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
   }
   if (fail) {
     ms->abort = 1;
@@ -594,43 +598,60 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
   __syncthreads();
   if (!ms->go) return;
   // ---- merge this item's slice of the row's dims over the splits ----
+  // dims of this slice: [d0, d1), even bounds (RoPE pairs stay together)
   const int ns = p.nsplit;
-  float* wgt = reinterpret_cast<float*>(sKV);              // [ns][64] weights, then [64] 1 / L
-  float* Ms = wgt + (size_t)ns * kH;                        // [64] max over splits
-  float* Ls = Ms + kH;                                      // [64] 1 / L
-  const float* mlr = p.part_ml + row * (int64_t)ns * kH * 2;
+  const int dp = ((kD + ns - 1) / ns + 1) & ~1;
+  const int d0 = min(kD, split * dp), d1 = min(kD, d0 + dp);
+  const int nd = d1 - d0;
+  // shared memory is free now: the row's statistics [ns][64] (m, l) at 0,
+  // this slice's partial rows [ns][nd][64 heads] bf16 after them, staged by
+  // bulk copies (all in flight together)
+  const uint32_t ml_bytes = (uint32_t)ns * kH * 8;
+  const uint32_t sl_off = (ml_bytes + 1023) & ~1023u;
+  const float2* ml_s = reinterpret_cast<const float2*>(sm);
+  const __nv_bfloat16* sl_s = reinterpret_cast<const __nv_bfloat16*>(sm + sl_off);
+  if (tid == 0) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    mbar_arrive_expect_tx(&ms->merge_in, ml_bytes + (uint32_t)ns * nd * kH * 2);
+    bulk_copy_g2s(smem_u32(sm), p.part_ml + row * (int64_t)ns * kH * 2, ml_bytes, &ms->merge_in);
+    if (nd > 0)
+      for (int s = 0; s < ns; ++s)
+        bulk_copy_g2s(smem_u32(sm + sl_off + (uint32_t)s * nd * kH * 2),
+                      p.part_o + (row * (int64_t)ns + s) * (kH * kD) + (int64_t)d0 * kH, (uint32_t)nd * kH * 2,
+                      &ms->merge_in);
+  }
+  if (!mbar_wait(&ms->merge_in, 0, kWaitLimit)) {
+    if (tid == 0) flag_timeout(p.ws);
+    return;   // (a copy still in flight lands in memory nobody reads again)
+  }
+  // per head: the splits' weights 2^(m_s - M) l_s, then 1 / L
+  float* wgt = reinterpret_cast<float*>(sm + sl_off + (((uint32_t)ns * nd * kH * 2 + 1023) & ~1023u));
+  float* Ls = wgt + (size_t)ns * kH;
   if (tid < kH) {
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(mlr + (s * kH + tid) * 2));
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml_s[s * kH + tid].x);
     float L = 0.0f;
     for (int s = 0; s < ns; ++s) {
-      const float mi = __ldcg(mlr + (s * kH + tid) * 2);
-      const float w = mi == -INFINITY ? 0.0f : exp2f(mi - M) * __ldcg(mlr + (s * kH + tid) * 2 + 1);
+      const float2 v = ml_s[s * kH + tid];
+      const float w = v.x == -INFINITY ? 0.0f : exp2f(v.x - M) * v.y;
       wgt[s * kH + tid] = w;
       L += w;
     }
-    Ms[tid] = M;
     Ls[tid] = L > 0.0f ? 1.0f / L : 0.0f;
     if (split == 0 && p.lse) p.lse[row * kH + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();
-  // dims of this slice: [d0, d1), even bounds (RoPE pairs stay together)
-  const int dp = ((kD + ns - 1) / ns + 1) & ~1;
-  const int d0 = min(kD, split * dp), d1 = min(kD, d0 + dp);
   const float* cs = p.rcos + (t_ok ? t : 0) * 32;
   const float* sn = p.rsin + (t_ok ? t : 0) * 32;
-  const __nv_bfloat16* prow = p.part_o + row * (int64_t)ns * kH * kD;
   // thread: a pair of dims (d, d + 1) of one head, weighted sum in split order
-  for (int u = tid; u < ((d1 - d0) >> 1) * kH; u += kThreads) {
-    const int h = u % kH, d = d0 + 2 * (u / kH);
+  for (int u = tid; u < (nd >> 1) * kH; u += kThreads) {
+    const int h = u % kH, dl = 2 * (u / kH), d = d0 + dl;
     float o0 = 0.0f, o1 = 0.0f;
     for (int s = 0; s < ns; ++s) {
       const float w = wgt[s * kH + h];
-      const __nv_bfloat16* src = prow + (int64_t)s * kH * kD;
-      const float a0 = __bfloat162float(__ldcg(src + (int64_t)d * kH + h));
-      const float a1 = __bfloat162float(__ldcg(src + (int64_t)(d + 1) * kH + h));
-      o0 = __fmaf_rn(w, a0, o0);
-      o1 = __fmaf_rn(w, a1, o1);
+      const __nv_bfloat16* src = sl_s + ((size_t)s * nd + dl) * kH + h;
+      o0 = __fmaf_rn(w, __bfloat162float(src[0]), o0);
+      o1 = __fmaf_rn(w, __bfloat162float(src[kH]), o1);
     }
     o0 *= Ls[h];
     o1 *= Ls[h];

@@ -823,6 +823,168 @@ topk_stage2_kernel(const int64_t* __restrict__ q_pos, int64_t N, int m, int k, i
   emit_topk<NT>(sorted, kk, k, row, idx_out, score_out);
 }
 
+// ---------------------------------------------------------------------------
+// Top-k of few long rows from a score histogram (decode).  The tensor-core
+// decode scorer counts every visible score of a row into kHistBins bins by
+// the top kHistBits bits of its order key.  From that histogram every CTA
+// of the row finds the bin b* that holds the k-th largest key: every score
+// in a bin above b* is among the top k ("sure": fewer than k of them) and
+// the rest of the top k are the best of bin b* ("ties").  Chunk CTAs append
+// the row's sure and tie candidates, as 64-bit composite keys, to workspace
+// lists (warp-aggregated); the last chunk CTA of the row to finish selects
+// the needed ties exactly (radix threshold on the order key, equal keys by
+// ascending index), sorts the k winners (score descending, index ascending)
+// and writes them.  When bin b* holds more than kTieCap candidates the last
+// CTA selects over the row's whole score array instead (same result).
+// ---------------------------------------------------------------------------
+constexpr int kHistBits = 11;
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kTieCap = 8192;
+constexpr int kSelThreads = 1024;
+constexpr int kSelChunk = 8192;       // scores scanned per chunk CTA
+
+__global__ void __launch_bounds__(kSelThreads)
+topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __restrict__ hist,
+                        const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int nchunk, int P,
+                        unsigned long long* __restrict__ cand, int* __restrict__ ctr, int32_t* __restrict__ idx_out,
+                        float* __restrict__ score_out) {
+  pdl_begin();
+  constexpr int NT = kSelThreads;
+  // final stage: 2 P sort keys, then the staged ties
+  extern __shared__ __align__(16) unsigned long long dyn_s[];
+  __shared__ unsigned int warp_sum[NT / 32];
+  __shared__ int bstar_s, last_s;
+  __shared__ unsigned int above_s, neq_s, take_s;
+  __shared__ TkShared<NT> sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.y;
+  const int c = blockIdx.x;
+  const int64_t nv = visible_entries(q_pos[row], m, N);
+  const int kk = (int)((int64_t)k < nv ? (int64_t)k : nv);
+  unsigned long long* sure = cand + row * (int64_t)(P + kTieCap);
+  unsigned long long* tie = sure + P;
+  int* rc = ctr + row * 4;   // [0] sure appended, [1] ties appended, [2] chunk CTAs done
+
+  // ---- b*: the largest bin whose suffix count (bins >= it) reaches kk ----
+  {
+    const unsigned int* hr = hist + row * (int64_t)kHistBins;
+    // thread t owns bins kHistBins-1-2t and kHistBins-2-2t (descending order)
+    const unsigned int h0 = hr[kHistBins - 1 - 2 * tid], h1 = hr[kHistBins - 2 - 2 * tid];
+    const unsigned int own = h0 + h1;
+    unsigned int incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    if (tid == 0) {
+      bstar_s = -1;
+      above_s = 0;
+    }
+    __syncthreads();
+    unsigned int before = 0;
+    for (int w2 = 0; w2 < warp; ++w2) before += warp_sum[w2];
+    const unsigned int excl = before + incl - own;   // keys in bins above this thread's two
+    if (kk > 0 && kk < nv) {
+      if (excl < (unsigned)kk && excl + h0 >= (unsigned)kk) {
+        bstar_s = kHistBins - 1 - 2 * tid;
+        above_s = excl;
+      } else if (excl + h0 < (unsigned)kk && excl + own >= (unsigned)kk) {
+        bstar_s = kHistBins - 2 - 2 * tid;
+        above_s = excl + h0;
+      }
+    }
+    __syncthreads();
+  }
+  const int bstar = bstar_s;   // -1: every visible key is taken
+  // ---- this chunk's candidates ----
+  const int64_t j0 = (int64_t)c * kSelChunk, j1 = j0 + kSelChunk < nv ? j0 + kSelChunk : nv;
+  for (int64_t jb = j0; jb < j1; jb += NT) {
+    const int64_t j = jb + tid;
+    uint32_t key = 0, bin = 0;
+    if (j < j1) {
+      key = order_key(scores[row * N + j]);
+      bin = key >> (32 - kHistBits);
+    }
+    const bool is_sure = j < j1 && (int)bin > bstar;
+    const bool is_tie = j < j1 && (int)bin == bstar;
+    const unsigned bs = __ballot_sync(0xffffffffu, is_sure), bt = __ballot_sync(0xffffffffu, is_tie);
+    const unsigned lt = (1u << lane) - 1u;
+    int base_s = 0, base_t = 0;
+    if (lane == 0 && bs) base_s = atomicAdd(rc + 0, __popc(bs));
+    if (lane == 0 && bt) base_t = atomicAdd(rc + 1, __popc(bt));
+    base_s = __shfl_sync(0xffffffffu, base_s, 0);
+    base_t = __shfl_sync(0xffffffffu, base_t, 0);
+    if (is_sure) {
+      const int pos = base_s + __popc(bs & lt);
+      if (pos < P) sure[pos] = composite(key, (uint32_t)j);
+    }
+    if (is_tie) {
+      const int pos = base_t + __popc(bt & lt);
+      if (pos < kTieCap) tie[pos] = composite(key, (uint32_t)j);
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last_s = atomicAdd(rc + 2, 1) == nchunk - 1;
+  __syncthreads();
+  if (!last_s) return;
+  // ================= the row's last chunk CTA: select and sort =================
+  __threadfence();
+  const int nsure = min(*reinterpret_cast<volatile int*>(rc + 0), P);
+  const int ntie = *reinterpret_cast<volatile int*>(rc + 1);
+  unsigned long long* keys_s = dyn_s;          // 2 P
+  unsigned long long* tie_s = dyn_s + 2 * P;   // kTieCap
+  if (kk > 0) {
+    if (bstar >= 0 && ntie > kTieCap) {
+      // bin b* too full for the tie list: select over the whole row
+      const DenseRow src{scores + row * N, 0};
+      const uint32_t thr = radix_threshold<NT>(src, nv, kk, sh);
+      ordered_collect<NT>(src, nv, thr, sh.remaining, keys_s, sh);
+    } else {
+      for (int i = tid; i < nsure; i += NT) keys_s[i] = __ldcg(sure + i);
+      const int need = kk - nsure;   // ties to take (0 when every key is taken)
+      if (need > 0) {
+        for (int i = tid; i < ntie; i += NT) tie_s[i] = __ldcg(tie + i);
+        __syncthreads();
+        const CandList src{tie_s};
+        const uint32_t thr = radix_threshold<NT>(src, ntie, need, sh);
+        const unsigned int rem = sh.remaining;   // keys equal to thr to take, lowest indices first
+        if (tid == 0) {
+          neq_s = 0;
+          take_s = nsure;
+        }
+        __syncthreads();
+        for (int i = tid; i < ntie; i += NT) {
+          const unsigned long long v = tie_s[i];
+          const uint32_t key = (uint32_t)(v >> 32);
+          if (key > thr) {
+            keys_s[atomicAdd(&take_s, 1u)] = v;
+          } else if (key == thr) {
+            // its rank among the equal keys: how many of them have a lower index
+            const uint32_t idx = 0xffffffffu - (uint32_t)(v & 0xffffffffull);
+            unsigned int r = 0;
+            for (int i2 = 0; i2 < ntie; ++i2) {
+              const unsigned long long v2 = tie_s[i2];
+              r += ((uint32_t)(v2 >> 32) == thr && 0xffffffffu - (uint32_t)(v2 & 0xffffffffull) < idx) ? 1u : 0u;
+            }
+            if (r < rem) keys_s[atomicAdd(&take_s, 1u)] = v;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  const unsigned long long* sorted = merge_sort_desc<NT>(keys_s, kk, P);
+  emit_topk<NT>(sorted, kk, k, row, idx_out, score_out);
+  if (tid == 0) {   // the workspace counters for the next call
+    rc[0] = 0;
+    rc[1] = 0;
+    rc[2] = 0;
+  }
+}
+
 int topk_pad(int k) {
   int p = 32;
   while (p < k) p <<= 1;
@@ -841,9 +1003,18 @@ int topk_chunks(int64_t N, int k) {
   return (int)((N + c - 1) / c);
 }
 
+// scratch of the histogram path: [rows][kHistBins] counts, [rows][4] counters,
+// [rows][P + kTieCap] candidate keys
+size_t topk_hist_bytes(int64_t rows, int k) {
+  const size_t P = (size_t)topk_pad(k);
+  return ((size_t)rows * kHistBins * 4 + (size_t)rows * 16 + 255) / 256 * 256 + (size_t)rows * (P + kTieCap) * 8;
+}
+
 size_t topk_cand_bytes(int B, int64_t Tq, int64_t N, int k) {
   const int ch = topk_chunks(N, k);
-  return ch ? (size_t)B * (size_t)Tq * (size_t)ch * (size_t)k * 8 : 0;
+  const size_t two = ch ? (size_t)B * (size_t)Tq * (size_t)ch * (size_t)k * 8 : 0;
+  const size_t hh = topk_hist_bytes((int64_t)B * Tq, k);
+  return ch ? (two > hh ? two : hh) : 0;
 }
 
 bool topk_two_stage(int B, int64_t Tq, int64_t N) {
@@ -857,6 +1028,7 @@ cudaError_t launch_indexer_topk(const void* qI, int key_fmt, const float* w, con
                                 bool tensor_cores, cudaStream_t st) {
   if ((int64_t)B * Tq == 0) return cudaSuccess;
   const bool fp4 = key_fmt == CSA_FMT_MXFP4;
+  unsigned int* hist = nullptr;   // set when the scorer also counts the scores into bins
   if (N > 0) {
     cudaError_t e;
     if (key_fmt == CSA_FMT_FP8B32) {
@@ -870,8 +1042,14 @@ cudaError_t launch_indexer_topk(const void* qI, int key_fmt, const float* w, con
       e = launch_indexer_scores_tc(qI, w, reinterpret_cast<const uint8_t*>(kI), kI_scales, q_pos, B, Tq, HI, N,
                                    m, scores_ws, tc_ws, flags_ws, st);
     } else if (fp4 && tensor_cores && decode_tc_applies(Tq, HI, dI, N)) {
+      // with the two-stage scratch given: the scores' histogram for the top-k
+      if (cand_ws && topk_two_stage(B, Tq, N)) {
+        hist = reinterpret_cast<unsigned int*>(cand_ws);
+        e = cudaMemsetAsync(cand_ws, 0, (size_t)B * Tq * (kHistBins * 4 + 16), st);
+        if (e != cudaSuccess) return e;
+      }
       e = launch_scores_fp4_decode_tc(qI, w, reinterpret_cast<const uint8_t*>(kI), kI_scales, q_pos, B, Tq, HI, N,
-                                      m, scores_ws, flags_ws, st);
+                                      m, scores_ws, hist, flags_ws, st);
     } else if (fp4 && dI == 64 && Tq <= 4 && HI <= kMaxHI && N >= 8 * kDecRound) {
       const int64_t chunk = decode_chunk(N, (int64_t)B * Tq);
       const dim3 grid((unsigned)((N + chunk - 1) / chunk), (unsigned)(B * Tq));
@@ -901,7 +1079,18 @@ cudaError_t launch_indexer_topk(const void* qI, int key_fmt, const float* w, con
   smem_limit_once(attr_s1, reinterpret_cast<const void*>(topk_stage1_kernel), (int)kTkStageMax);
   smem_limit_once(attr_s2, reinterpret_cast<const void*>(topk_stage2_kernel), (int)kTkStageMax);
   const int64_t rows = (int64_t)B * Tq;
-  if (cand_ws && topk_two_stage(B, Tq, N)) {
+  if (hist) {
+    static PerDevice attr_h;
+    const size_t hsmem = sizeof(unsigned long long) * (2 * (size_t)P + kTieCap);
+    smem_limit_once(attr_h, reinterpret_cast<const void*>(topk_hist_select_kernel), (int)hsmem);
+    const size_t hoff = ((size_t)rows * kHistBins * 4 + (size_t)rows * 16 + 255) / 256 * 256;
+    int* ctr = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(cand_ws) + (size_t)rows * kHistBins * 4);
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(cand_ws) + hoff);
+    const int nchunk = (int)((N + kSelChunk - 1) / kSelChunk);
+    launch_pdl(topk_hist_select_kernel, dim3((unsigned)nchunk, (unsigned)rows), dim3(kSelThreads), hsmem, st,
+               (const float*)scores_ws, (const unsigned int*)hist, q_pos, N, m, k, nchunk, P, cand, ctr, idx_out,
+               score_out);
+  } else if (cand_ws && topk_two_stage(B, Tq, N)) {
     const int ch = topk_chunks(N, k);
     unsigned long long* cand = reinterpret_cast<unsigned long long*>(cand_ws);
     // stage a chunk's scores / a row's candidates in shared memory when they fit

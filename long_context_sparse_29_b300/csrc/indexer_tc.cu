@@ -407,33 +407,43 @@ ix_scores_tc_kernel(const IxParams p, const __grid_constant__ CUtensorMap tm_q, 
 // row's quantised query the N side (B, one row per head, 16 rows), and
 // kind::f8f6f4 takes the E2M1 codes as they are stored: a 16-element run of
 // K is 8 bytes of packed codes followed by 8 bytes of padding in shared
-// memory, so an entry's 32 code bytes become its 64-byte operand row without
-// any conversion.  Products of E2M1 values are multiples of 1/4 and a block
-// dot is below 2^11 in magnitude: exact in the fp32 accumulator.  Block b of
-// all heads lands in TMEM columns 16 b .. 16 b + 15 of the tile's buffer.
+// memory, so an entry's 32 code bytes become its operand row by four 8-byte
+// asynchronous copies straight from global memory.  Products of E2M1 values
+// are multiples of 1/4 and a block dot is below 2^11 in magnitude: exact in
+// the fp32 accumulator.  Block b of all heads lands in TMEM columns
+// 16 b .. 16 b + 15 of the tile's buffer.
 //
-// One CTA of 4 warps walks a chunk of entries in 128-entry tiles: every
-// thread loads one entry's codes and scales, writes the operand row, one
-// elected lane issues the two block MMAs; while tile u + 1 is multiplied
-// the threads combine tile u from the other TMEM buffer (lane = entry) and
-// store its scores.  All waits have iteration limits and their outcome is
-// made uniform by the CTA barrier before the next step.
+// One CTA of 4 warps streams a chunk of entries through a ring of kDtStages
+// operand tiles: every thread copies its entry of tile u + kDtStages - 1
+// (codes and scale bytes) while warp 0 issues the two block MMAs of tile u
+// into one of four TMEM buffers and all threads combine tile u - 1 (thread =
+// entry): loads, MMAs and the epilogue of different tiles overlap.  All
+// waits have iteration limits; a thread whose wait expires records the
+// timeout and stops, and the CTA waits (bounded) for its copies and MMAs
+// before freeing TMEM.
 // ---------------------------------------------------------------------------
 namespace {
 
 constexpr int kDtThreads = 128;             // entries per tile (MMA M) = threads
 constexpr int kDtHeads = 16;                // MMA N
+constexpr int kDtStages = 4;                // operand ring
+constexpr int kDtTbufs = 4;                 // TMEM buffers of 32 columns
 constexpr uint32_t kDtBOff = 0;             // query operand, 16 rows x 128 B
-constexpr uint32_t kDtAOff = 2048;          // entry operand, 128 rows x 128 B
-constexpr uint32_t kDtMiscOff = kDtAOff + 128 * 128;
+constexpr uint32_t kDtAOff = 2048;          // entry operand ring: kDtStages x [128 rows x 128 B]
+constexpr int kDtMaxChunk = 4096;           // entries per CTA at most (their scale bytes are staged)
+constexpr uint32_t kDtSOff = kDtAOff + kDtStages * 128 * 128;   // the chunk's scale bytes: kDtMaxChunk x 2 B
+constexpr uint32_t kDtHOff = kDtSOff + kDtMaxChunk * 2;      // score histogram of the chunk: 2048 bins
+constexpr int kDtHistBits = 11;
+constexpr uint32_t kDtMiscOff = kDtHOff + (1u << kDtHistBits) * 4;
 constexpr uint32_t kDtSmem = kDtMiscOff + 512 + 1024;   // + alignment slack
 
 struct DtMisc {
-  uint64_t mma_done;
+  uint64_t full[kDtStages], empty[kDtStages], tfull[kDtTbufs], tempty[kDtTbufs];
   uint32_t tmem;
   int qlo0, qhi0, qlo1, qhi1;   // range of the query's block exponents over the heads
   int4 hx[kDtHeads];            // per head: {eq0 << 23, eq1 << 23, w bits, 0}
 };
+static_assert(sizeof(DtMisc) <= 512, "DtMisc overflows its smem slot");
 
 // kind::f8f6f4 with E2M1 A and B (format 5), fp32 D, both K-major
 __host__ __device__ constexpr uint32_t idesc_e2m1(int M, int N) {
@@ -452,18 +462,26 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
   return (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4);
 }
 
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+// arrive on `bar` once this thread's copies so far have landed (counted arrival)
+__device__ __forceinline__ void cp_async_arrive(void* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 }  // namespace
 
-__global__ void __launch_bounds__(kDtThreads, 6)
+__global__ void __launch_bounds__(kDtThreads, 3)
 scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
                             const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
                             const int64_t* __restrict__ q_pos, int64_t Tq, int HI, int64_t N, int m,
-                            int64_t chunk, float* __restrict__ scores, void* ws) {
+                            int64_t chunk, float* __restrict__ scores, unsigned int* __restrict__ hist, void* ws) {
   pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DtMisc* ms = reinterpret_cast<DtMisc*>(sm + kDtMiscOff);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t row = blockIdx.y;
   const int64_t b = row / Tq;
   const int64_t nv = visible(q_pos[row], m, N);
@@ -472,32 +490,51 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
   const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
   const int ntiles = (int)((c1 - c0 + kDtThreads - 1) / kDtThreads);
 
-  // the first tile's entry (codes and scales) in flight during the set-up
-  auto load_entry = [&](int u, uint4& lo, uint4& hi, uint32_t& sc) {
-    int64_t j = c0 + (int64_t)u * kDtThreads + tid;
-    j = j < c1 ? j : c0;
-    const uint4* src = reinterpret_cast<const uint4*>(kc + (b * N + j) * 32);
-    lo = __ldg(src);
-    hi = __ldg(src + 1);
-    sc = __ldg(reinterpret_cast<const uint16_t*>(ks + (b * N + j) * 2));
-  };
-  uint4 klo, khi;
-  uint32_t ksc;
-  load_entry(0, klo, khi, ksc);
-
-  // ---- set-up: TMEM, barrier, zeroed query operand ----
-  for (int i = tid; i < 2048 / 16; i += kDtThreads) reinterpret_cast<uint4*>(sm + kDtBOff)[i] = make_uint4(0, 0, 0, 0);
+  // ---- set-up: zeroed operands (the padding bytes stay zero), barriers, TMEM ----
+  for (int i = tid; i < (int)(kDtSOff / 16); i += kDtThreads) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
+  unsigned int* hist_s = reinterpret_cast<unsigned int*>(sm + kDtHOff);
+  if (hist)
+    for (int i = tid; i < (1 << kDtHistBits); i += kDtThreads) hist_s[i] = 0u;
   if (tid == 0) {
-    mbar_init(&ms->mma_done, 1);
+    for (int s = 0; s < kDtStages; ++s) {
+      mbar_init(&ms->full[s], kDtThreads);   // every thread's copies of the stage
+      mbar_init(&ms->empty[s], 1);           // the stage's MMAs completed
+    }
+    for (int i = 0; i < kDtTbufs; ++i) {
+      mbar_init(&ms->tfull[i], 1);
+      mbar_init(&ms->tempty[i], 4);          // one arrival per warp once it has read the buffer
+    }
     mbar_fence_init();
     ms->qlo0 = ms->qlo1 = 1 << 30;
     ms->qhi0 = ms->qhi1 = -(1 << 30);
   }
-  if (warp == 0) tmem_alloc(&ms->tmem, 64);
+  if (warp == 0) tmem_alloc(&ms->tmem, kDtTbufs * 32);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = ms->tmem;
+
+  // this thread's entry of tile u into stage u % kDtStages: its 32 code bytes
+  // as four 8-byte copies into the padded operand row; then its counted
+  // arrival on the stage
+  auto load_tile = [&](int u) {
+    const int s = u % kDtStages;
+    int64_t j = c0 + (int64_t)u * kDtThreads + tid;
+    j = j < c1 ? j : c0;   // past the chunk: any valid entry (its score is not stored)
+    const uint8_t* src = kc + (b * N + j) * 32;
+    const uint32_t a = smem_u32(sm + kDtAOff + s * 16384);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cp_async8(a + sw128_off(tid, i), src + 8 * i);
+    cp_async_arrive(&ms->full[s]);
+  };
+  bool ok = true;
+  for (int u = 0; u < kDtStages - 1 && u < ntiles; ++u) load_tile(u);
+  // the chunk's scale bytes (two per entry), staged once
+  {
+    uint16_t* sc_s = reinterpret_cast<uint16_t*>(sm + kDtSOff);
+    const uint16_t* ks16 = reinterpret_cast<const uint16_t*>(ks) + b * N + c0;
+    for (int i = tid; i < (int)(c1 - c0); i += kDtThreads) sc_s[i] = __ldg(ks16 + i);
+  }
 
   // ---- the query: MXFP4 codes into the B operand, block exponents ----
   // thread t: elements 4u .. 4u + 3 (u = t mod 8) of blocks t / 8 + 16 r
@@ -535,63 +572,29 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
       }
     }
   }
+  fence_proxy_async();   // the query operand, written through the generic proxy
+  fence_before_sync();
+  __syncthreads();
+  const int qlo0 = ms->qlo0, qhi0 = ms->qhi0, qlo1 = ms->qlo1, qhi1 = ms->qhi1;
   const uint32_t aA = smem_u32(sm + kDtAOff), aB = smem_u32(sm + kDtBOff);
   constexpr uint32_t id = idesc_e2m1(kDtThreads, kDtHeads);
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-  bool ok = true;
-  int issued = 0, waited = 0;   // MMA tile pairs issued / seen complete
-  uint32_t sc_cur = 0;   // scales of the tile in the TMEM buffer being combined
-  // tile u: operand row written from the registers, then multiplied
-  auto put_tile = [&]() {
-    uint8_t* a = sm + kDtAOff;
-    *reinterpret_cast<uint4*>(a + sw128_off(tid, 0)) = make_uint4(klo.x, klo.y, 0, 0);
-    *reinterpret_cast<uint4*>(a + sw128_off(tid, 1)) = make_uint4(klo.z, klo.w, 0, 0);
-    *reinterpret_cast<uint4*>(a + sw128_off(tid, 2)) = make_uint4(khi.x, khi.y, 0, 0);
-    *reinterpret_cast<uint4*>(a + sw128_off(tid, 3)) = make_uint4(khi.z, khi.w, 0, 0);
-    fence_proxy_async();
-  };
-  auto issue = [&](int u) {
-    if (warp == 0) {
-      fence_after_sync();
-      const uint64_t ad = sdesc_sw128(aA, 16, 1024), bd = sdesc_sw128(aB, 16, 1024);
-      const uint32_t d = tmem + 32u * (u & 1);
-      mma_f8f6f4_elect(d, ad, bd, id);
-      mma_f8f6f4_elect(d + 16u, ad + 2, bd + 2, id);
-      mma_commit_elect(&ms->mma_done);
-      __syncwarp();
-    }
-  };
-  put_tile();
-  sc_cur = ksc;
-  fence_before_sync();
-  __syncthreads();   // query operand, exponent ranges, tile 0 written
-  const int qlo0 = ms->qlo0, qhi0 = ms->qhi0, qlo1 = ms->qlo1, qhi1 = ms->qhi1;
-  issue(0);
-  issued = 1;
-  if (ntiles > 1) load_entry(1, klo, khi, ksc);
+  int issued = 0;   // tiles whose MMAs warp 0 has issued
 
-  for (int u = 0; u < ntiles; ++u) {
-    const bool done = mbar_wait(&ms->mma_done, (uint32_t)(u & 1), kIxWait);
-    waited += done ? 1 : 0;
+  // the epilogue of tile u: lane = entry, 16 heads x 2 blocks from TMEM
+  auto combine = [&](int u) {
+    const int tb = u % kDtTbufs;
+    if (ok && !mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDtTbufs) & 1, kIxWait)) ok = false;
     fence_after_sync();
-    const uint32_t sc_this = sc_cur;
-    if (u + 1 < ntiles) {   // the operand is free: write tile u + 1
-      put_tile();
-      sc_cur = ksc;
-    }
-    fence_before_sync();
-    ok = __syncthreads_and(ok && done) != 0;
-    if (!ok) break;
-    if (u + 1 < ntiles) {
-      issue(u + 1);
-      ++issued;
-      if (u + 2 < ntiles) load_entry(u + 2, klo, khi, ksc);
-    }
-    // ---- combine tile u: lane = entry, 16 heads x 2 blocks from TMEM ----
     uint32_t P[32];
-    tmem_ld32(tmem + lane_base + 32u * (u & 1), P);
+    tmem_ld32(tmem + lane_base + 32u * tb, P);
     tmem_wait_ld();
-    const int x0 = (int)(sc_this & 0xffu), x1 = (int)(sc_this >> 8);
+    fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ms->tempty[tb]);
+    const int64_t jj = (int64_t)u * kDtThreads + tid;
+    const uint32_t sc = jj < c1 - c0 ? reinterpret_cast<const uint16_t*>(sm + kDtSOff)[jj] : 0x7f7fu;
+    const int x0 = (int)(sc & 0xffu), x1 = (int)(sc >> 8);
     const int X0 = x0 << 23, X1 = x1 << 23;
     // block b of head h is scaled by 2^(eq_bh + x_b - 127): one exact multiply
     // when every such power of the entry lies in [2^-100, 2^100]
@@ -619,18 +622,70 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
       }
     }
     const int64_t j = c0 + (int64_t)u * kDtThreads + tid;
-    if (j < c1) scores[row * N + j] = s;
+    if (ok && j < c1) {
+      scores[row * N + j] = s;
+      if (hist) {   // the bin of its order key (top bits; -0 ranks as +0)
+        uint32_t key = __float_as_uint(s);
+        if (key == 0x80000000u) key = 0u;
+        key = (key & 0x80000000u) ? ~key : (key | 0x80000000u);
+        atomicAdd(hist_s + (key >> (32 - kDtHistBits)), 1u);
+      }
+    }
+  };
+
+  for (int u = 0; u < ntiles && ok; ++u) {
+    // the copies of tile u + kDtStages - 1, once the MMAs of its stage's last tile (u - 1) are done
+    const int ul = u + kDtStages - 1;
+    if (ul < ntiles) {
+      if (ul >= kDtStages && !mbar_wait(&ms->empty[ul % kDtStages], (uint32_t)(ul / kDtStages - 1) & 1, kIxWait))
+        ok = false;
+      if (ok) load_tile(ul);
+    }
+    // warp 0: the two block MMAs of tile u into TMEM buffer u % kDtTbufs
+    if (warp == 0 && ok) {
+      const int s = u % kDtStages, tb = u % kDtTbufs;
+      bool got = mbar_wait(&ms->full[s], (uint32_t)(u / kDtStages) & 1, kIxWait);
+      if (got && u >= kDtTbufs) got = mbar_wait(&ms->tempty[tb], (uint32_t)(u / kDtTbufs - 1) & 1, kIxWait);
+      if (got) {
+        fence_after_sync();
+        fence_proxy_async();   // the operand rows came through the generic proxy (cp.async)
+        const uint64_t ad = sdesc_sw128(aA + s * 16384, 16, 1024), bd = sdesc_sw128(aB, 16, 1024);
+        const uint32_t d = tmem + 32u * tb;
+        mma_f8f6f4_elect(d, ad, bd, id);
+        mma_f8f6f4_elect(d + 16u, ad + 2, bd + 2, id);
+        mma_commit_elect(&ms->tfull[tb]);
+        mma_commit_elect(&ms->empty[s]);
+        ++issued;
+      } else {
+        ok = false;
+      }
+      __syncwarp();
+    }
+    if (u >= 1) combine(u - 1);
   }
+  if (ok && ntiles > 0) combine(ntiles - 1);
   if (!ok) {
-    if (tid == 0) flag_timeout(ws);
-    // an MMA still in flight finishes (bounded wait) before its TMEM is freed
-    if (issued > waited) mbar_wait(&ms->mma_done, (uint32_t)((issued - 1) & 1), kIxWait);
+    if (lane == 0) flag_timeout(ws);
+  }
+  // this chunk's histogram into the row's
+  if (hist) {
+    __syncthreads();
+    for (int i = tid; i < (1 << kDtHistBits); i += kDtThreads) {
+      const unsigned int v = hist_s[i];
+      if (v) atomicAdd(hist + row * (int64_t)(1 << kDtHistBits) + i, v);
+    }
+  }
+  // copies and MMAs of this CTA land before its TMEM and shared memory go
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (warp == 0 && issued > 0) {
+    const int u = issued - 1;
+    mbar_wait(&ms->tfull[u % kDtTbufs], (uint32_t)(u / kDtTbufs) & 1, kIxWait);
   }
   fence_before_sync();
   __syncthreads();
   if (warp == 0) {
     fence_after_sync();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, kDtTbufs * 32);
   }
 }
 
@@ -740,24 +795,26 @@ bool decode_tc_applies(int64_t Tq, int HI, int dI, int64_t N) {
 
 cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const uint8_t* kc, const uint8_t* ks,
                                         const int64_t* q_pos, int B, int64_t Tq, int HI, int64_t N, int m,
-                                        float* scores, void* flags_ws, cudaStream_t st) {
+                                        float* scores, unsigned int* hist, void* flags_ws, cudaStream_t st) {
   static PerDevice attr, slots_dev;
   smem_limit_once(attr, reinterpret_cast<const void*>(scores_fp4_decode_tc_kernel), (int)kDtSmem);
   const int slots = slots_dev.get([] {
     int per = resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_tc_kernel), kDtThreads, kDtSmem);
-    per = per > 8 ? 8 : per;   // 64 TMEM columns each: at most 8 per SM
+    per = per > 4 ? 4 : per;   // 128 TMEM columns each: at most 4 per SM
     return device_sms() * per;
   });
   const int64_t rows = (int64_t)B * Tq;
-  // chunks of whole tiles, about one CTA per resident slot, at least 2 tiles each
+  // chunks of whole tiles, about one CTA per resident slot, at least 2 tiles
+  // and at most kDtMaxChunk entries each
   int64_t per_row = slots / rows;
   if (per_row < 1) per_row = 1;
   int64_t chunk = (N + per_row - 1) / per_row;
   chunk = (chunk + kDtThreads - 1) / kDtThreads * kDtThreads;
   if (chunk < 2 * kDtThreads) chunk = 2 * kDtThreads;
+  if (chunk > kDtMaxChunk) chunk = kDtMaxChunk;
   const dim3 grid((unsigned)((N + chunk - 1) / chunk), (unsigned)rows);
   launch_pdl(scores_fp4_decode_tc_kernel, dim3(grid), dim3(kDtThreads), kDtSmem, st, reinterpret_cast<const __nv_bfloat16*>(qI), w, kc,
-                                                                 ks, q_pos, Tq, HI, N, m, chunk, scores, flags_ws);
+                                                                 ks, q_pos, Tq, HI, N, m, chunk, scores, hist, flags_ws);
   return cudaGetLastError();
 }
 

@@ -141,7 +141,7 @@ cudaError_t launch_wait_selftest(void* ws, uint32_t polls, cudaStream_t st);
 bool decode_tc_applies(int64_t Tq, int HI, int dI, int64_t N);
 cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const uint8_t* kc, const uint8_t* ks,
                                         const int64_t* q_pos, int B, int64_t Tq, int HI, int64_t N, int m,
-                                        float* scores, void* flags_ws, cudaStream_t st);
+                                        float* scores, unsigned int* hist, void* flags_ws, cudaStream_t st);
 // two-stage top-k for long rows when there are few of them, and its scratch
 bool topk_two_stage(int B, int64_t Tq, int64_t N);
 size_t topk_cand_bytes(int B, int64_t Tq, int64_t N, int k);

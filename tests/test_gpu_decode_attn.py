@@ -98,7 +98,7 @@ def test_decode_rows_without_keys_and_invalid_positions(csa, oracle_mod):
     pos0 = np.array([T - Ts, 0, T - Ts, T - Ts], np.int64)
     idx = np.full((B, 1, 40), -1, np.int32)
     for b in (0, 3):
-        idx[b, 0] = rng.permutation(N)[:40]
+        idx[b, 0] = rng.permutation(N - 2)[:40]          # entries visible at both positions
     ws = csa.Workspace()
     out, lse = csa.sparse_mqa(dev_bf16(q), dev(q_pos), dev(cache), m, dev(idx), dev(swa), dev(pos0), W,
                               1 / math.sqrt(512), rope_dev, lse=True, ws=ws)
@@ -114,3 +114,31 @@ def test_decode_rows_without_keys_and_invalid_positions(csa, oracle_mod):
     ref1, _, _ = oracle_mod.attention(wl.bf16_bits_to_f32(q[1:2]), q_pos[1:2], cache[1:2], N, m, idx[1:2],
                                       swa[1:2], pos0[1:2], W, 1 / math.sqrt(512), rope_np, 64)
     assert max_rel_err(out[1:2], ref1) <= 1e-2
+
+
+def test_decode_in_item_rescale(csa, oracle_mod):
+    """100 rows (one split each: every tile of a row in one item) whose later
+    key tiles carry much larger logits, so the running maxima grow tile by
+    tile and O is rescaled in TMEM inside the item."""
+    rng = np.random.default_rng(3000)
+    B, N, m, k, W = 100, 1024, 4, 640, 0
+    T = N * m
+    rope_np, rope_dev = oracle_mod.rope_table(T + 1, 64), csa.rope_table(T + 1, 64)
+    q32 = rng.standard_normal((1, 1, 64, 512)).astype(np.float32)
+    dirn = q32[0, 0].mean(0)
+    grow = np.linspace(0, 6, N).astype(np.float32)[:, None]
+    ent = rng.standard_normal((N, 512)).astype(np.float32) + grow * dirn[None, :] / np.linalg.norm(dirn) * 8
+    cache = np.broadcast_to(oracle_mod.pack_mixed(ent.astype(np.float32)), (B, N, 592)).copy()
+    swa = np.zeros((B, 8, 592), np.uint8)
+    q = np.broadcast_to(wl.f32_to_bf16_bits(q32), (B, 1, 64, 512)).copy()
+    q_pos = np.full((B, 1), T - 1, np.int64)
+    idx = np.broadcast_to(np.arange(N - k, N, dtype=np.int32), (B, 1, k)).copy()   # increasing logits
+    pos0 = np.full(B, T - 8, np.int64)
+    scale = 1 / math.sqrt(512)
+    got = csa.sparse_mqa(dev_bf16(q), dev(q_pos), dev(cache), m, dev(idx), dev(swa), dev(pos0), W, scale,
+                         rope_dev).float().cpu().numpy()
+    ref, _, bad = oracle_mod.attention(wl.bf16_bits_to_f32(q[:1]), q_pos[:1], cache[:1], N, m, idx[:1], swa[:1],
+                                       pos0[:1], W, scale, rope_np, 64)
+    assert bad == 0
+    for b in (0, 57, 99):
+        assert max_rel_err(got[b:b + 1], ref) <= 1e-2
