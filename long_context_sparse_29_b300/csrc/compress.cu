@@ -267,15 +267,23 @@ compress_kernel(const void* __restrict__ x, const float* __restrict__ z,
                               R, m, o, kScales ? out_scales + ent * (C / 32) : nullptr, alpha_s[warp], lane);
 }
 
-// Decode-time cache maintenance, one CTA per sequence: the new token at
-// position t (t_pos[b]) enters the ring of the sequence's last m raw tokens
-// (slot t mod m), is packed into the window cache at row t - swa_pos0[b]
-// (when that row is past the buffer, the last W - 1 rows first move to the
-// front and swa_pos0[b] becomes t - W + 1), and when t closes a block
-// ((t + 1) mod m == 0) the block is compressed into entry (t + 1) / m - 1 of
-// the cache and, with its own ring, of the indexer keys: one thread per
-// channel pair sums the m ring rows (the same fma order as compress_entry, so
-// the same bytes), then one warp scales, rotates and packs.
+// Decode-time cache maintenance: the new token at position t (t_pos[b])
+// enters the ring of the sequence's last m raw tokens (slot t mod m), is
+// packed into the window cache at row t - swa_pos0[b] (when that row is past
+// the buffer, the last W - 1 rows first move to the front and swa_pos0[b]
+// becomes t - W + 1), and when t closes a block ((t + 1) mod m == 0) the
+// block is compressed into entry (t + 1) / m - 1 of the cache and, with its
+// own ring, of the indexer keys.  The work of a sequence is split over
+// kAppendParts CTAs with disjoint outputs, so their latency chains run side
+// by side: part 0 the ring slot and the window row; parts 1-4 one 128-channel
+// quarter of the closing entry each (FP8 groups 0, 1, 2, and group 3 with the
+// bf16 RoPE channels); part 5 the closing indexer key.  The parts read the
+// new token from kv / kI and the block's older tokens from the ring slots
+// 0 .. m - 2 (part 0 writes only slot t mod m = m - 1 then), and every
+// channel is summed over the m tokens in token order and packed by the same
+// operations as compress_entry / pack_mixed_row: the same bytes.
+constexpr int kAppendParts = 6;
+
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restrict__ z,
                      const __nv_bfloat16* __restrict__ kI, const float* __restrict__ zI,
@@ -288,133 +296,165 @@ decode_append_kernel(const __nv_bfloat16* __restrict__ kv, const float* __restri
                      uint8_t* __restrict__ kI_scales, uint8_t* __restrict__ swa, int64_t Ts, int W,
                      int64_t* __restrict__ swa_pos0) {
   pdl_begin();
-  __shared__ float alpha_s[3][128];
-  __shared__ float z_s[2][128];              // the closing block's logits (cache, key)
-  __shared__ float2 acc_s[(512 + 64) / 2];   // the closing block's pair sums: C/2 of the cache, CI/2 of the key
-  extern __shared__ __align__(16) uint8_t ring_s[];   // closing block: m rows of C, then m rows of CI (bf16)
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ float alpha_s[128];             // the block's weights
+  __shared__ float z_s[128];                 // the block's logits
   __shared__ float rope_s[2][32];            // cos, sin of position t (R = 64)
-  __shared__ float s_s[512], sI_s[64];       // the channel scales
+  __shared__ float2 acc_s[64];               // this part's pair sums
+  __shared__ float amax_s[2];
+  extern __shared__ __align__(16) uint8_t ring_s[];   // closing block: m rows of this part's channels (bf16)
+  const int b = blockIdx.x, part = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t t = t_pos[b];
-  const int64_t old0 = W > 0 ? swa_pos0[b] : 0;   // read with t, before anything waits on either
   if (t < 0 || t >= rope_rows) return;   // no RoPE row for it: nothing is stored
-  // the RoPE row of t and the channel scales, read into shared memory now:
-  // the window row and the entry use them only at the ends of their chains
-  for (int i = tid; i < (R >> 1); i += blockDim.x) {
-    rope_s[0][i] = rcos[t * (R >> 1) + i];
-    rope_s[1][i] = rsin[t * (R >> 1) + i];
-  }
-  if (s)
-    for (int i = tid; i < C; i += blockDim.x) s_s[i] = s[i];
-  if (kI && sI)
-    for (int i = tid; i < CI; i += blockDim.x) sI_s[i] = sI[i];
-  const int slot = (int)(t % m);
   const bool closes = (t + 1) % m == 0 && (t + 1) / m - 1 < nmax;
-  if (closes) {
-    // stage the block's rows: slots 0 .. m-2 from the ring, slot m-1 is this
-    // token; 16-byte asynchronous copies, all in flight together
-    const int rk = C * 2 / 16, ri = CI * 2 / 16;   // 16-byte pieces per row
-    for (int q = tid; q < m * (rk + ri); q += blockDim.x) {
-      const bool key = q >= m * rk;
-      const int qq = key ? q - m * rk : q, per = key ? ri : rk;
-      const int i = qq / per, c = qq - i * per;
-      const uint8_t* src = key ? (i == m - 1 ? reinterpret_cast<const uint8_t*>(kI + (int64_t)b * CI)
-                                             : reinterpret_cast<const uint8_t*>(kI_tail + ((int64_t)b * m + i) * CI))
-                               : (i == m - 1 ? reinterpret_cast<const uint8_t*>(kv + (int64_t)b * C)
-                                             : reinterpret_cast<const uint8_t*>(kv_tail + ((int64_t)b * m + i) * C));
-      uint8_t* dst = ring_s + (key ? (size_t)m * C * 2 : 0) + ((size_t)i * per + c) * 16;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
-                   "l"(src + c * 16)
+  if (part == 0) {
+    // ---- the raw token into its ring slot; the window row ----
+    const int64_t old0 = W > 0 ? swa_pos0[b] : 0;
+    const int slot = (int)(t % m);
+    for (int i = tid; i < (R >> 1); i += blockDim.x) {
+      rope_s[0][i] = rcos[t * (R >> 1) + i];
+      rope_s[1][i] = rsin[t * (R >> 1) + i];
+    }
+    for (int c = tid; c < C / 8; c += blockDim.x)
+      reinterpret_cast<uint4*>(kv_tail + ((int64_t)b * m + slot) * C)[c] = reinterpret_cast<const uint4*>(kv + (int64_t)b * C)[c];
+    if (kI)
+      for (int c = tid; c < CI / 8; c += blockDim.x)
+        reinterpret_cast<uint4*>(kI_tail + ((int64_t)b * m + slot) * CI)[c] =
+            reinterpret_cast<const uint4*>(kI + (int64_t)b * CI)[c];
+    if (tid == 0) {
+      z_tail[(int64_t)b * m + slot] = z[b];
+      if (kI) zI_tail[(int64_t)b * m + slot] = zI[b];
+    }
+    if (W > 0) {
+      const bool slide = t - old0 >= Ts;
+      __syncthreads();   // every thread has read swa_pos0[b]; the RoPE row is in
+      if (slide) {
+        // rows of tokens t - W + 1 .. t - 1 move to rows 0 .. W - 2; source rows
+        // are >= Ts - W + 1 >= W + 1 (Ts >= 2 W): no overlap.  Rows past the
+        // buffer (appends out of order) are not read.
+        const int64_t keep0 = t - W + 1, src0 = keep0 - old0;
+        const int per = kMixRow / 16;
+        const uint4* srcp = reinterpret_cast<const uint4*>(swa + (int64_t)b * Ts * kMixRow);
+        uint4* dst = reinterpret_cast<uint4*>(swa + (int64_t)b * Ts * kMixRow);
+        for (int i = tid; i < (W - 1) * per; i += blockDim.x) {
+          const int64_t sr = src0 + i / per;
+          if (sr >= 0 && sr < Ts) dst[i] = srcp[sr * per + i % per];
+        }
+        __syncthreads();
+        if (tid == 0) swa_pos0[b] = keep0;
+      }
+      const int64_t row = slide ? (int64_t)W - 1 : t - old0;
+      if (warp == 0 && row >= 0 && row < Ts) {   // the token itself: m = 1, no channel scale, RoPE at t
+        const float zz = 0.0f;
+        compress_entry<CSA_FMT_MIXED592, true>(kv + (int64_t)b * C, &zz, nullptr, rope_s[0], rope_s[1], 0, C, R, 1,
+                                               swa + ((int64_t)b * Ts + row) * kMixRow, nullptr, alpha_s, lane);
+      }
+    }
+    return;
+  }
+  const bool key = part == kAppendParts - 1;
+  if (!closes || (key && !kI)) return;
+  // ---- a closing block: this part's channels [c0, c0 + nc) of the m rows ----
+  const int64_t j = (t + 1) / m - 1;
+  const int cc = key ? CI : C;                       // row width of the source
+  const int c0 = key ? 0 : 128 * (part - 1), nc = key ? CI : 128;
+  const __nv_bfloat16* x_new = key ? kI + (int64_t)b * CI : kv + (int64_t)b * C;
+  const __nv_bfloat16* x_ring = key ? kI_tail + (int64_t)b * m * CI : kv_tail + (int64_t)b * m * C;
+  {
+    const int per = nc * 2 / 16;   // 16-byte pieces of a row's part
+    for (int q = tid; q < m * per; q += blockDim.x) {
+      const int i = q / per, c = q - i * per;
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(i == m - 1 ? x_new : x_ring + (int64_t)i * cc) + c0 * 2 +
+                           c * 16;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(
+                       ring_s + ((size_t)i * per + c) * 16)),
+                   "l"(src)
                    : "memory");
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
   }
-  // ---- the raw token into its ring slot ----
-  for (int c = tid; c < C; c += blockDim.x) kv_tail[((int64_t)b * m + slot) * C + c] = kv[(int64_t)b * C + c];
-  if (kI)
-    for (int c = tid; c < CI; c += blockDim.x) kI_tail[((int64_t)b * m + slot) * CI + c] = kI[(int64_t)b * CI + c];
-  if (tid == 0) {
-    z_tail[(int64_t)b * m + slot] = z[b];
-    if (kI) zI_tail[(int64_t)b * m + slot] = zI[b];
+  if (!key)
+    for (int i = tid; i < (R >> 1); i += blockDim.x) {
+      rope_s[0][i] = rcos[t * (R >> 1) + i];
+      rope_s[1][i] = rsin[t * (R >> 1) + i];
+    }
+  if (warp == 0) {   // the logits: slots 0 .. m-2 from the ring, slot m-1 this token's; then the weights
+    const float* zt = key ? zI_tail : z_tail;
+    const float zn = key ? zI[b] : z[b];
+    for (int i = lane; i < m; i += 32) z_s[i] = i == m - 1 ? zn : zt[(int64_t)b * m + i];
+    __syncwarp();
+    entry_weights(z_s, m, alpha_s, lane);
   }
-  // ---- window: slide when the row is past the buffer ----
-  if (W > 0) {
-    const bool slide = t - old0 >= Ts;
-    __syncthreads();   // every thread has read swa_pos0[b]; the RoPE row and scales are in
-    if (slide) {
-      // rows of tokens t - W + 1 .. t - 1 move to rows 0 .. W - 2; source rows
-      // are >= Ts - W + 1 >= W + 1 (Ts >= 2 W): no overlap.  Rows past the
-      // buffer (appends out of order) are not read.
-      const int64_t keep0 = t - W + 1, src0 = keep0 - old0;
-      const int per = kMixRow / 16;
-      const uint4* src = reinterpret_cast<const uint4*>(swa + (int64_t)b * Ts * kMixRow);
-      uint4* dst = reinterpret_cast<uint4*>(swa + (int64_t)b * Ts * kMixRow);
-      for (int i = tid; i < (W - 1) * per; i += blockDim.x) {
-        const int64_t sr = src0 + i / per;
-        if (sr >= 0 && sr < Ts) dst[i] = src[sr * per + i % per];
-      }
-      __syncthreads();
-      if (tid == 0) swa_pos0[b] = keep0;
-    }
-    const int64_t row = slide ? (int64_t)W - 1 : t - old0;
-    if (warp == 0 && row >= 0 && row < Ts) {   // the token itself: m = 1, no channel scale, RoPE at t
-      const float zz = 0.0f;
-      compress_entry<CSA_FMT_MIXED592, true>(kv + (int64_t)b * C, &zz, nullptr, rope_s[0], rope_s[1], 0, C, R, 1,
-                                             swa + ((int64_t)b * Ts + row) * kMixRow, nullptr, alpha_s[0], lane);
-    }
-  }
-  if (closes) {   // CTA-wide, the same fma order per channel as compress_entry
-    const int64_t j = (t + 1) / m - 1;
-    // the logits: slots 0 .. m-2 from the ring, slot m-1 this token's
-    if (warp == 1) {
-      for (int i = lane; i < m; i += 32) z_s[0][i] = i == m - 1 ? z[b] : z_tail[(int64_t)b * m + i];
-      __syncwarp();
-      entry_weights(z_s[0], m, alpha_s[1], lane);
-    }
-    if (warp == 2 && kI) {
-      for (int i = lane; i < m; i += 32) z_s[1][i] = i == m - 1 ? zI[b] : zI_tail[(int64_t)b * m + i];
-      __syncwarp();
-      entry_weights(z_s[1], m, alpha_s[2], lane);
-    }
-    asm volatile("cp.async.wait_all;\n" ::: "memory");
-    __syncthreads();
-    const void* xk = ring_s;
-    const void* xi = ring_s + (size_t)m * C * 2;
-    for (int p = tid; p < (C >> 1) + (CI >> 1); p += blockDim.x) {
-      const bool key = p >= (C >> 1);
-      const int q = key ? p - (C >> 1) : p;
-      const float* a = alpha_s[key ? 2 : 1];
-      const void* x = key ? xi : xk;
-      const int cc = key ? CI : C;
-      float2 acc = make_float2(0.0f, 0.0f);
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
+  __syncthreads();
+  // the pair sums, in token order (the fma sequence of compress_entry)
+  const float* sc = key ? sI : s;
+  if (tid < nc / 2) {
+    const int pp = tid;   // pair (c0 / 2 + pp) of the row
+    float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll 8
-      for (int i = 0; i < m; ++i) {
-        const float2 w = load_pair<true>(x, (int64_t)i * cc, q);
-        acc.x = __fmaf_rn(a[i], w.x, acc.x);
-        acc.y = __fmaf_rn(a[i], w.y, acc.y);
-      }
-      acc_s[p] = acc;
+    for (int i = 0; i < m; ++i) {
+      const float2 w2 = load_pair<true>(ring_s, (int64_t)i * nc, pp);
+      acc.x = __fmaf_rn(alpha_s[i], w2.x, acc.x);
+      acc.y = __fmaf_rn(alpha_s[i], w2.y, acc.y);
     }
-    __syncthreads();
-    if (warp == 1 || (warp == 2 && kI)) {
-      const bool key = warp == 2;
-      const int off = key ? (C >> 1) : 0, np = key ? (CI >> 1) : (C >> 1);
+    const int c = c0 + 2 * pp;   // channel of acc.x
+    if (sc) {
+      acc.x = __fmul_rn(acc.x, sc[c]);
+      acc.y = __fmul_rn(acc.y, sc[c + 1]);
+    }
+    if (!key && c >= C - R) {   // RoPE at the block's last token t
+      const int i = (c - (C - R)) >> 1;
+      const float cs = rope_s[0][i], sn = rope_s[1][i];
+      const float x0 = acc.x, x1 = acc.y;
+      acc.x = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+      acc.y = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs));
+    }
+    acc_s[pp] = acc;
+  }
+  __syncthreads();
+  if (key) {   // the MXFP4 key, by one warp: lane holds pair lane (C <= 64)
+    if (warp == 0) {
       float2 v[kMaxPairs];
 #pragma unroll
-      for (int r = 0; r < kMaxPairs; ++r) {
-        const int p = lane + 32 * r;
-        v[r] = p < np ? acc_s[off + p] : make_float2(0.0f, 0.0f);
-      }
-      if (key)
-        entry_finish<CSA_FMT_MXFP4>(v, sI ? sI_s : nullptr, rope_s[0], rope_s[1], 0, CI, 0,
-                                    kI_codes + ((int64_t)b * nmax + j) * (CI / 2),
-                                    kI_scales + ((int64_t)b * nmax + j) * (CI / 32), lane);
-      else
-        entry_finish<CSA_FMT_MIXED592>(v, s ? s_s : nullptr, rope_s[0], rope_s[1], 0, C, R,
-                                       cache + ((int64_t)b * nmax + j) * kMixRow, nullptr, lane);
+      for (int r = 0; r < kMaxPairs; ++r) v[r] = make_float2(0.0f, 0.0f);
+      if (lane < nc / 2) v[0] = acc_s[lane];
+      entry_finish<CSA_FMT_MXFP4>(v, nullptr, rope_s[0], rope_s[1], 0, CI, 0,
+                                  kI_codes + ((int64_t)b * nmax + j) * (CI / 2),
+                                  kI_scales + ((int64_t)b * nmax + j) * (CI / 32), lane);
     }
+    return;
   }
+  // the mixed row's part: FP8 codes of this quarter's group (quarter 4: channels
+  // 384..447 only), its scale, and (quarter 4) the bf16 RoPE channels
+  uint8_t* row = cache + ((int64_t)b * nmax + j) * kMixRow;
+  const int g = part - 1;
+  const int nfp8 = g < 3 ? 64 : 32;   // pairs of FP8 channels in this part
+  if (warp < 2) {
+    const int pp = tid;   // pairs 0 .. 63 over warps 0 and 1
+    float a = 0.0f;
+    if (pp < nfp8) {
+      const float2 v = acc_s[pp];
+      a = fmaxf(fabsf(v.x), fabsf(v.y));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) amax_s[warp] = a;
+  }
+  __syncthreads();
+  const int e = fp8_group_exp(fmaxf(amax_s[0], amax_s[1]));
+  if (tid < nfp8) {
+    const float inv = pow2i(-e);
+    const float2 v = acc_s[tid];
+    const uint16_t c0v = e4m3_encode(__fmul_rn(v.x, inv));
+    const uint16_t c1v = e4m3_encode(__fmul_rn(v.y, inv));
+    *reinterpret_cast<uint16_t*>(row + c0 + 2 * tid) = (uint16_t)(c0v | (c1v << 8));
+  } else if (g == 3 && tid < 64) {   // RoPE pairs: bf16
+    const float2 v = acc_s[tid];
+    const uint32_t b0 = f32_to_bf16_bits(v.x), b1 = f32_to_bf16_bits(v.y);
+    *reinterpret_cast<uint32_t*>(row + kMixRopeOff + 4 * (tid - 32)) = b0 | (b1 << 16);
+  }
+  if (tid == 0) *reinterpret_cast<float*>(row + kMixScaleOff + 4 * g) = pow2i(e);
 }
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
@@ -468,10 +508,8 @@ cudaError_t launch_decode_append(const void* kv, const float* z, const void* kI,
                                  uint8_t* kI_scales, uint8_t* swa, int64_t Ts, int W, int64_t* swa_pos0,
                                  cudaStream_t st) {
   if (B == 0) return cudaSuccess;
-  const size_t ring = (size_t)m * (C + CI) * 2;   // staged rows of a closing block
-  static PerDevice attr;
-  smem_limit_once(attr, reinterpret_cast<const void*>(decode_append_kernel), 128 * (512 + 64) * 2);
-  launch_pdl(decode_append_kernel, dim3((unsigned)B), dim3(kWarpsPerBlock * 32), ring, st, 
+  const size_t ring = (size_t)m * 128 * 2;   // staged rows of a closing block: one part's channels
+  launch_pdl(decode_append_kernel, dim3((unsigned)B, kAppendParts), dim3(kWarpsPerBlock * 32), ring, st, 
       reinterpret_cast<const __nv_bfloat16*>(kv), z, reinterpret_cast<const __nv_bfloat16*>(kI), zI, s, sI, rcos,
       rsin, rope_rows, t_pos, C, R, CI, m, reinterpret_cast<__nv_bfloat16*>(kv_tail), z_tail,
       reinterpret_cast<__nv_bfloat16*>(kI_tail), zI_tail, cache, nmax, kI_codes, kI_scales, swa, Ts, W, swa_pos0);

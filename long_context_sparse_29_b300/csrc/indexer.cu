@@ -1082,7 +1082,9 @@ cudaError_t launch_indexer_topk(const void* qI, int key_fmt, const float* w, con
   if (hist) {
     static PerDevice attr_h;
     const size_t hsmem = sizeof(unsigned long long) * (2 * (size_t)P + kTieCap);
-    smem_limit_once(attr_h, reinterpret_cast<const void*>(topk_hist_select_kernel), (int)hsmem);
+    // the largest request (k = 4096), set once per device
+    smem_limit_once(attr_h, reinterpret_cast<const void*>(topk_hist_select_kernel),
+                    (int)(sizeof(unsigned long long) * (2 * 4096 + kTieCap)));
     const size_t hoff = ((size_t)rows * kHistBins * 4 + (size_t)rows * 16 + 255) / 256 * 256;
     int* ctr = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(cand_ws) + (size_t)rows * kHistBins * 4);
     unsigned long long* cand = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(cand_ws) + hoff);
