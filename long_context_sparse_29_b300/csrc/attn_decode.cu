@@ -171,24 +171,32 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
     const int seg = ((p.k + 3) / 4 + 31) / 32 * 32;
     const int lo = pw * seg, hi = min(p.k, lo + seg);
     const int32_t* ir = p.idx + row * (int64_t)p.k;
+    // the warp's share of idx: at most 32 per lane (k <= 4096), all loads in flight together
+    int32_t js[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int i = lo + 32 * r + lane;
+      js[r] = i < hi ? __ldg(ir + i) : -1;
+    }
+    uint32_t okbits = 0;
     int cnt = 0;
-    for (int base = lo; base < hi; base += 32) {
-      const int r = base + lane;
-      const int32_t j = r < hi ? __ldg(ir + r) : -1;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int32_t j = js[r];
       const bool ok = t_ok && j >= 0 && (int64_t)j < p.N && (int64_t)(j + 1) * p.m - 1 <= t;
       if (split == 0 && t_ok && j >= 0 && !ok) flag_device_check(p.ws, (unsigned)j);
+      okbits |= ok ? 1u << r : 0u;
       cnt += __popc(__ballot_sync(0xffffffffu, ok));
     }
     if (lane == 0) ms->cnt[pw] = cnt;
     producer_sync();
     int out = 0;
     for (int w2 = 0; w2 < pw; ++w2) out += ms->cnt[w2];
-    for (int base = lo; base < hi; base += 32) {
-      const int r = base + lane;
-      const int32_t j = r < hi ? __ldg(ir + r) : -1;
-      const bool ok = t_ok && j >= 0 && (int64_t)j < p.N && (int64_t)(j + 1) * p.m - 1 <= t;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const bool ok = (okbits >> r) & 1u;
       const unsigned bal = __ballot_sync(0xffffffffu, ok);
-      if (ok) list[out + __popc(bal & ((1u << lane) - 1u))] = j;
+      if (ok) list[out + __popc(bal & ((1u << lane) - 1u))] = js[r];
       out += __popc(bal);
     }
   }
@@ -399,10 +407,18 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
     const uint32_t tq_lane = (uint32_t)(32 * qd) << 16;
     // the query's RoPE dims (chunk 7) rotated to position t, in place:
     // thread tid takes head tid / 2, pairs 16 (tid & 1) .. + 15
+    float csr[16], snr[16];   // cos / sin of this thread's 16 pairs, loaded while the query is in flight
+    {
+      const float* cs = p.rcos + (t_ok ? t : 0) * 32 + 16 * (tid & 1);
+      const float* sn = p.rsin + (t_ok ? t : 0) * 32 + 16 * (tid & 1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        csr[i] = __ldg(cs + i);
+        snr[i] = __ldg(sn + i);
+      }
+    }
     if (mbar_wait(&ms->q_full, 0, kWaitLimit)) {
       const int h = tid >> 1;
-      const float* cs = p.rcos + (t_ok ? t : 0) * 32;
-      const float* sn = p.rsin + (t_ok ? t : 0) * 32;
 #pragma unroll
       for (int uu = 0; uu < 4; ++uu) {
         const int u = 4 * (tid & 1) + uu;      // 16-byte unit: pairs 4u .. 4u + 3
@@ -411,9 +427,8 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int i = 4 * u + e;
           const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-          const float c = cs[i], s = sn[i];
+          const float c = csr[4 * uu + e], s = snr[4 * uu + e];
           const float y0 = __fsub_rn(__fmul_rn(f.x, c), __fmul_rn(f.y, s));
           const float y1 = __fadd_rn(__fmul_rn(f.x, s), __fmul_rn(f.y, c));
           const __nv_bfloat162 r2 = __floats2bfloat162_rn(y0, y1);
@@ -641,8 +656,13 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
     if (split == 0 && p.lse) p.lse[row * kH + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();
-  const float* cs = p.rcos + (t_ok ? t : 0) * 32;
-  const float* sn = p.rsin + (t_ok ? t : 0) * 32;
+  float* cs = Ls + kH;   // the RoPE row of t: 32 cos, 32 sin
+  float* sn = cs + 32;
+  if (tid >= 64 && tid < 96) {
+    cs[tid - 64] = p.rcos[(t_ok ? t : 0) * 32 + tid - 64];
+    sn[tid - 64] = p.rsin[(t_ok ? t : 0) * 32 + tid - 64];
+  }
+  __syncthreads();
   // thread: a pair of dims (d, d + 1) of one head, weighted sum in split order
   for (int u = tid; u < (nd >> 1) * kH; u += kThreads) {
     const int h = u % kH, dl = 2 * (u / kH), d = d0 + dl;

@@ -841,7 +841,46 @@ constexpr int kHistBits = 11;
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kTieCap = 8192;
 constexpr int kSelThreads = 1024;
-constexpr int kSelChunk = 8192;       // scores scanned per chunk CTA
+constexpr int kSelChunk = 8192;       // scores scanned per chunk CTA (8 per thread)
+
+// Sorts a[0..P) descending by a bitonic network in shared memory (P a power
+// of two; slots past `count` are padded with 0, below every real key).
+template <int NT>
+__device__ void bitonic_desc(unsigned long long* a, int count, int P) {
+  for (int i = threadIdx.x; i < P; i += NT)
+    if (i >= count) a[i] = 0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += NT) {
+        const int lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const unsigned long long x = a[lo], y = a[hi];
+        if ((x < y) == desc) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Candidate stream over staged composite keys whose order key equals `thr`:
+// their low words (the complement of the index) as the key, so the largest
+// of them are the lowest indices.
+struct EqualKeyList {
+  const unsigned long long* c;
+  uint32_t thr;
+  __device__ __forceinline__ bool get(int64_t i, uint32_t& key, uint32_t& idx) const {
+    const unsigned long long v = c[i];
+    key = (uint32_t)(v & 0xffffffffull);
+    idx = 0xffffffffu - key;
+    return (uint32_t)(v >> 32) == thr;
+  }
+};
+
+constexpr int kSelPerThread = kSelChunk / kSelThreads;
 
 __global__ void __launch_bounds__(kSelThreads)
 topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __restrict__ hist,
@@ -850,11 +889,12 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
                         float* __restrict__ score_out) {
   pdl_begin();
   constexpr int NT = kSelThreads;
-  // final stage: 2 P sort keys, then the staged ties
+  // chunk phase: this CTA's sure keys [P] and ties [kTieCap]; final phase:
+  // 2 P sort keys, then the row's staged ties
   extern __shared__ __align__(16) unsigned long long dyn_s[];
   __shared__ unsigned int warp_sum[NT / 32];
-  __shared__ int bstar_s, last_s;
-  __shared__ unsigned int above_s, neq_s, take_s;
+  __shared__ int bstar_s, last_s, base_s, base_t;
+  __shared__ unsigned int above_s, nls_s, nlt_s, take_s;
   __shared__ TkShared<NT> sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.y;
@@ -864,6 +904,14 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
   unsigned long long* sure = cand + row * (int64_t)(P + kTieCap);
   unsigned long long* tie = sure + P;
   int* rc = ctr + row * 4;   // [0] sure appended, [1] ties appended, [2] chunk CTAs done
+  // this chunk's scores, loaded while the histogram is read
+  const int64_t j0 = (int64_t)c * kSelChunk, j1 = j0 + kSelChunk < nv ? j0 + kSelChunk : nv;
+  float sv[kSelPerThread];
+#pragma unroll
+  for (int r = 0; r < kSelPerThread; ++r) {
+    const int64_t j = j0 + r * NT + tid;
+    sv[r] = j < j1 ? scores[row * N + j] : 0.0f;
+  }
 
   // ---- b*: the largest bin whose suffix count (bins >= it) reaches kk ----
   {
@@ -881,6 +929,8 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
     if (tid == 0) {
       bstar_s = -1;
       above_s = 0;
+      nls_s = 0;
+      nlt_s = 0;
     }
     __syncthreads();
     unsigned int before = 0;
@@ -898,33 +948,35 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
     __syncthreads();
   }
   const int bstar = bstar_s;   // -1: every visible key is taken
-  // ---- this chunk's candidates ----
-  const int64_t j0 = (int64_t)c * kSelChunk, j1 = j0 + kSelChunk < nv ? j0 + kSelChunk : nv;
-  for (int64_t jb = j0; jb < j1; jb += NT) {
-    const int64_t j = jb + tid;
-    uint32_t key = 0, bin = 0;
+  // ---- this chunk's candidates: into shared lists, then one reservation per list ----
+  unsigned long long* sure_l = dyn_s;
+  unsigned long long* tie_l = dyn_s + P;
+#pragma unroll
+  for (int r = 0; r < kSelPerThread; ++r) {
+    const int64_t j = j0 + r * NT + tid;
     if (j < j1) {
-      key = order_key(scores[row * N + j]);
-      bin = key >> (32 - kHistBits);
-    }
-    const bool is_sure = j < j1 && (int)bin > bstar;
-    const bool is_tie = j < j1 && (int)bin == bstar;
-    const unsigned bs = __ballot_sync(0xffffffffu, is_sure), bt = __ballot_sync(0xffffffffu, is_tie);
-    const unsigned lt = (1u << lane) - 1u;
-    int base_s = 0, base_t = 0;
-    if (lane == 0 && bs) base_s = atomicAdd(rc + 0, __popc(bs));
-    if (lane == 0 && bt) base_t = atomicAdd(rc + 1, __popc(bt));
-    base_s = __shfl_sync(0xffffffffu, base_s, 0);
-    base_t = __shfl_sync(0xffffffffu, base_t, 0);
-    if (is_sure) {
-      const int pos = base_s + __popc(bs & lt);
-      if (pos < P) sure[pos] = composite(key, (uint32_t)j);
-    }
-    if (is_tie) {
-      const int pos = base_t + __popc(bt & lt);
-      if (pos < kTieCap) tie[pos] = composite(key, (uint32_t)j);
+      const uint32_t key = order_key(sv[r]);
+      const int bin = (int)(key >> (32 - kHistBits));
+      if (bin > bstar) {
+        const unsigned int pos = atomicAdd(&nls_s, 1u);
+        if (pos < (unsigned)P) sure_l[pos] = composite(key, (uint32_t)j);
+      } else if (bin == bstar) {
+        const unsigned int pos = atomicAdd(&nlt_s, 1u);
+        if (pos < (unsigned)kTieCap) tie_l[pos] = composite(key, (uint32_t)j);
+      }
     }
   }
+  __syncthreads();
+  const int nls = min((int)nls_s, P), nlt_all = (int)nlt_s, nlt = min(nlt_all, kTieCap);
+  if (tid == 0) {
+    base_s = nls ? atomicAdd(rc + 0, nls) : 0;
+    base_t = nlt_all ? atomicAdd(rc + 1, nlt_all) : 0;
+  }
+  __syncthreads();
+  for (int i = tid; i < nls; i += NT)
+    if (base_s + i < P) sure[base_s + i] = sure_l[i];
+  for (int i = tid; i < nlt; i += NT)
+    if (base_t + i < kTieCap) tie[base_t + i] = tie_l[i];
   __threadfence();
   __syncthreads();
   if (tid == 0) last_s = atomicAdd(rc + 2, 1) == nchunk - 1;
@@ -947,37 +999,28 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
       const int need = kk - nsure;   // ties to take (0 when every key is taken)
       if (need > 0) {
         for (int i = tid; i < ntie; i += NT) tie_s[i] = __ldcg(tie + i);
+        if (tid == 0) take_s = nsure;
         __syncthreads();
-        const CandList src{tie_s};
-        const uint32_t thr = radix_threshold<NT>(src, ntie, need, sh);
+        const uint32_t thr = radix_threshold<NT>(CandList{tie_s}, ntie, need, sh);
         const unsigned int rem = sh.remaining;   // keys equal to thr to take, lowest indices first
-        if (tid == 0) {
-          neq_s = 0;
-          take_s = nsure;
+        // among the keys equal to thr, the rem lowest indices: a second
+        // threshold on their index words
+        uint32_t ithr = 0;
+        if (rem > 0) {
+          __syncthreads();
+          ithr = radix_threshold<NT>(EqualKeyList{tie_s, thr}, ntie, (int)rem, sh);
         }
-        __syncthreads();
         for (int i = tid; i < ntie; i += NT) {
           const unsigned long long v = tie_s[i];
-          const uint32_t key = (uint32_t)(v >> 32);
-          if (key > thr) {
-            keys_s[atomicAdd(&take_s, 1u)] = v;
-          } else if (key == thr) {
-            // its rank among the equal keys: how many of them have a lower index
-            const uint32_t idx = 0xffffffffu - (uint32_t)(v & 0xffffffffull);
-            unsigned int r = 0;
-            for (int i2 = 0; i2 < ntie; ++i2) {
-              const unsigned long long v2 = tie_s[i2];
-              r += ((uint32_t)(v2 >> 32) == thr && 0xffffffffu - (uint32_t)(v2 & 0xffffffffull) < idx) ? 1u : 0u;
-            }
-            if (r < rem) keys_s[atomicAdd(&take_s, 1u)] = v;
-          }
+          const uint32_t key = (uint32_t)(v >> 32), low = (uint32_t)(v & 0xffffffffull);
+          if (key > thr || (rem > 0 && key == thr && low >= ithr)) keys_s[atomicAdd(&take_s, 1u)] = v;
         }
       }
       __syncthreads();
     }
   }
-  const unsigned long long* sorted = merge_sort_desc<NT>(keys_s, kk, P);
-  emit_topk<NT>(sorted, kk, k, row, idx_out, score_out);
+  bitonic_desc<NT>(keys_s, kk, P);
+  emit_topk<NT>(keys_s, kk, k, row, idx_out, score_out);
   if (tid == 0) {   // the workspace counters for the next call
     rc[0] = 0;
     rc[1] = 0;

@@ -529,11 +529,23 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
   };
   bool ok = true;
   for (int u = 0; u < kDtStages - 1 && u < ntiles; ++u) load_tile(u);
-  // the chunk's scale bytes (two per entry), staged once
+  // the chunk's scale bytes (two per entry), staged once: every load of the
+  // thread in flight before the first store
   {
     uint16_t* sc_s = reinterpret_cast<uint16_t*>(sm + kDtSOff);
     const uint16_t* ks16 = reinterpret_cast<const uint16_t*>(ks) + b * N + c0;
-    for (int i = tid; i < (int)(c1 - c0); i += kDtThreads) sc_s[i] = __ldg(ks16 + i);
+    const int n = (int)(c1 - c0);
+    uint16_t v[kDtMaxChunk / kDtThreads];
+#pragma unroll
+    for (int r = 0; r < kDtMaxChunk / kDtThreads; ++r) {
+      const int i = tid + r * kDtThreads;
+      v[r] = i < n ? __ldg(ks16 + i) : (uint16_t)0;
+    }
+#pragma unroll
+    for (int r = 0; r < kDtMaxChunk / kDtThreads; ++r) {
+      const int i = tid + r * kDtThreads;
+      if (i < n) sc_s[i] = v[r];
+    }
   }
 
   // ---- the query: MXFP4 codes into the B operand, block exponents ----
