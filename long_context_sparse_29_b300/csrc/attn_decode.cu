@@ -138,7 +138,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
     ms->abort = 0;
     ms->go = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms->raw_full[i], 4);   // one arrive (with its byte count) per producer warp
+      mbar_init(&ms->raw_full[i], 4 + 128);   // one arrive per producer warp, one counted per producer lane
       mbar_init(&ms->kv_full[i], 4);    // one arrive per producer warp once its rows are expanded
       mbar_init(&ms->kv_empty[i], 1);
       mbar_init(&ms->s_full[i], 1);
@@ -238,10 +238,15 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
   if (warp >= 4 && warp < 8) {
     // ================================ producers ================================
     const int pw = warp - 4;
-    // the item's key rows into L2 now: every fetch below then hits L2
-    for (int key = tlo * kTile + pw * 32 + lane; key < key_hi; key += 128) {
-      const uint8_t* r = key_row(key);
-      if (r) prefetch_l2(r, kMixRow);
+    // dense keys are runs of consecutive rows (the entries, then the window):
+    // the item's runs into L2 now, in pieces of at most 64 rows
+    if (dense && pw == 0) {
+      const int e_lo = tlo * kTile, e_hi = min(ne, key_hi);
+      for (int r = e_lo + 64 * lane; r < e_hi; r += 64 * 32)
+        prefetch_l2(p.cache + (b * p.N + r) * kMixRow, (uint32_t)min(64, e_hi - r) * kMixRow);
+      const int w_lo2 = max(ne, tlo * kTile), w_hi2 = key_hi;
+      for (int r = w_lo2 + 64 * lane; r < w_hi2; r += 64 * 32)
+        prefetch_l2(p.swa + (b * p.Ts + (w_lo - p0 + (r - ne))) * kMixRow, (uint32_t)min(64, w_hi2 - r) * kMixRow);
     }
     uint32_t g = 0;
     bool ok = true;
@@ -253,13 +258,40 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
       }
       uint8_t* slot = sKV + buf * 65536;
       uint8_t* raw = slot + kRawOff;
-      // this warp's 16 rows of the tile: bulk copies of the 592-byte rows
+      // this warp's 16 rows of the tile (valid ones in vmask); dense: the
+      // tile's runs of consecutive rows as at most two bulk copies (warp 0);
+      // sparse: 16-byte asynchronous copies, 37 per row, spread over the lanes
       const int r0 = 16 * pw;
       const uint8_t* src = lane < 16 ? key_row(tl * kTile + r0 + lane) : nullptr;
       const unsigned vmask = __ballot_sync(0xffffffffu, src != nullptr);
-      if (lane == 0) mbar_arrive_expect_tx(&ms->raw_full[buf], (uint32_t)__popc(vmask) * kMixRow);
+      if (dense) {
+        if (pw == 0 && lane == 0) {
+          const int k0 = tl * kTile, k1 = min(key_hi, k0 + kTile);
+          const int ce = max(k0, min(ne, k1));   // entries [k0, ce), window [ce, k1)
+          mbar_arrive_expect_tx(&ms->raw_full[buf], (uint32_t)(k1 - k0) * kMixRow);
+          if (ce > k0)
+            bulk_copy_g2s(smem_u32(raw), p.cache + (b * p.N + k0) * kMixRow, (uint32_t)(ce - k0) * kMixRow,
+                          &ms->raw_full[buf]);
+          if (k1 > ce)
+            bulk_copy_g2s(smem_u32(raw + (ce - k0) * kMixRow), p.swa + (b * p.Ts + (w_lo - p0 + (ce - ne))) * kMixRow,
+                          (uint32_t)(k1 - ce) * kMixRow, &ms->raw_full[buf]);
+        } else if (lane == 0) {
+          mbar_arrive(&ms->raw_full[buf]);
+        }
+      } else {
+        if (lane == 0) mbar_arrive(&ms->raw_full[buf]);
+        const unsigned long long sp = reinterpret_cast<unsigned long long>(src);
+#pragma unroll 1
+        for (int it = 0; it < (16 * 37 + 31) / 32; ++it) {
+          const int q = lane + 32 * it;
+          const int i = q / 37, u = q - 37 * (q / 37);
+          const unsigned long long rp = __shfl_sync(0xffffffffu, sp, q < 16 * 37 ? i : 0);
+          if (q < 16 * 37 && rp)
+            cp_async16(smem_u32(raw + (r0 + i) * kMixRow + 16 * u), reinterpret_cast<const uint8_t*>(rp) + 16 * u);
+        }
+      }
+      cp_async_mbar_arrive_noinc(&ms->raw_full[buf]);
       __syncwarp();
-      if (src) bulk_copy_g2s(smem_u32(raw + (r0 + lane) * kMixRow), src, kMixRow, &ms->raw_full[buf]);
       if (!mbar_wait(&ms->raw_full[buf], (g >> 1) & 1, kWaitLimit)) {
         ok = false;
         break;
@@ -326,6 +358,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
       if (lane == 0) flag_timeout(p.ws);
       fail = true;
       // a bulk copy of this tile may still be in flight: let it land
+      cp_async_wait_all();
       if (g < (uint32_t)(thi - tlo)) mbar_wait(&ms->raw_full[g & 1], (g >> 1) & 1, kWaitLimit);
     }
   } else if (warp == kMmaWarp) {

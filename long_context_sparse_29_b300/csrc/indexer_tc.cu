@@ -428,6 +428,7 @@ constexpr int kDtThreads = 128;             // entries per tile (MMA M) = thread
 constexpr int kDtHeads = 16;                // MMA N
 constexpr int kDtStages = 4;                // operand ring
 constexpr int kDtTbufs = 4;                 // TMEM buffers of 32 columns
+constexpr int kDtLag = 2;                   // tiles between a tile's MMAs and its epilogue
 constexpr uint32_t kDtBOff = 0;             // query operand, 16 rows x 128 B
 constexpr uint32_t kDtAOff = 2048;          // entry operand ring: kDtStages x [128 rows x 128 B]
 constexpr int kDtMaxChunk = 4096;           // entries per CTA at most (their scale bytes are staged)
@@ -673,9 +674,10 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
       }
       __syncwarp();
     }
-    if (u >= 1) combine(u - 1);
+    // the epilogue runs kDtLag tiles behind the MMAs (kDtLag < kDtTbufs)
+    if (u >= kDtLag) combine(u - kDtLag);
   }
-  if (ok && ntiles > 0) combine(ntiles - 1);
+  for (int u = max(0, ntiles - kDtLag); u < ntiles && ok; ++u) combine(u);
   if (!ok) {
     if (lane == 0) flag_timeout(ws);
   }
