@@ -413,11 +413,13 @@ ix_scores_tc_kernel(const IxParams p, const __grid_constant__ CUtensorMap tm_q, 
 // the fp32 accumulator.  Block b of all heads lands in TMEM columns
 // 16 b .. 16 b + 15 of the tile's buffer.
 //
-// One CTA of 4 warps streams a chunk of entries through a ring of kDtStages
-// operand tiles: every thread copies its entry of tile u + kDtStages - 1
-// (codes and scale bytes) while warp 0 issues the two block MMAs of tile u
-// into one of four TMEM buffers and all threads combine tile u - 1 (thread =
-// entry): loads, MMAs and the epilogue of different tiles overlap.  All
+// One CTA of 4 warps streams a chunk of entries through kDtSlots operand
+// tile slots (two tiles share each 16 KiB stage: one in the first 64 bytes of
+// every 128-byte row, one in the second): every thread copies its entry of
+// tile u + kDtAhead while warp 0 issues the two block MMAs of tile u into one
+// of four TMEM buffers and all threads combine tile u - kDtLag (thread =
+// entry): loads, MMAs and the epilogue of different tiles overlap.  The
+// chunk's scale bytes are staged once.  All
 // waits have iteration limits; a thread whose wait expires records the
 // timeout and stops, and the CTA waits (bounded) for its copies and MMAs
 // before freeing TMEM.
@@ -426,7 +428,9 @@ namespace {
 
 constexpr int kDtThreads = 128;             // entries per tile (MMA M) = threads
 constexpr int kDtHeads = 16;                // MMA N
-constexpr int kDtStages = 4;                // operand ring
+constexpr int kDtStages = 4;                // operand ring: 16 KiB stages of two tiles each
+constexpr int kDtSlots = 2 * kDtStages;     // tile slots: tile u in slot u % kDtSlots
+constexpr int kDtAhead = 5;                 // tiles whose copies are in flight ahead of the MMAs
 constexpr int kDtTbufs = 4;                 // TMEM buffers of 32 columns
 constexpr int kDtLag = 2;                   // tiles between a tile's MMAs and its epilogue
 constexpr uint32_t kDtBOff = 0;             // query operand, 16 rows x 128 B
@@ -439,7 +443,7 @@ constexpr uint32_t kDtMiscOff = kDtHOff + (1u << kDtHistBits) * 4;
 constexpr uint32_t kDtSmem = kDtMiscOff + 512 + 1024;   // + alignment slack
 
 struct DtMisc {
-  uint64_t full[kDtStages], empty[kDtStages], tfull[kDtTbufs], tempty[kDtTbufs];
+  uint64_t full[kDtSlots], empty[kDtSlots], tfull[kDtTbufs], tempty[kDtTbufs];
   uint32_t tmem;
   int qlo0, qhi0, qlo1, qhi1;   // range of the query's block exponents over the heads
   int4 hx[kDtHeads];            // per head: {eq0 << 23, eq1 << 23, w bits, 0}
@@ -497,9 +501,9 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
   if (hist)
     for (int i = tid; i < (1 << kDtHistBits); i += kDtThreads) hist_s[i] = 0u;
   if (tid == 0) {
-    for (int s = 0; s < kDtStages; ++s) {
-      mbar_init(&ms->full[s], kDtThreads);   // every thread's copies of the stage
-      mbar_init(&ms->empty[s], 1);           // the stage's MMAs completed
+    for (int s = 0; s < kDtSlots; ++s) {
+      mbar_init(&ms->full[s], kDtThreads);   // every thread's copies of the slot's tile
+      mbar_init(&ms->empty[s], 1);           // the slot's MMAs completed
     }
     for (int i = 0; i < kDtTbufs; ++i) {
       mbar_init(&ms->tfull[i], 1);
@@ -515,21 +519,22 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
   fence_after_sync();
   const uint32_t tmem = ms->tmem;
 
-  // this thread's entry of tile u into stage u % kDtStages: its 32 code bytes
-  // as four 8-byte copies into the padded operand row; then its counted
-  // arrival on the stage
+  // this thread's entry of tile u into slot u % kDtSlots -- stage slot / 2,
+  // 16-byte units 4 (slot & 1) .. + 3 of its 128-byte operand row (the two
+  // tiles of a stage share its rows): its 32 code bytes as four 8-byte
+  // copies into the padded layout; then its counted arrival on the slot
   auto load_tile = [&](int u) {
-    const int s = u % kDtStages;
+    const int s = u % kDtSlots;
     int64_t j = c0 + (int64_t)u * kDtThreads + tid;
     j = j < c1 ? j : c0;   // past the chunk: any valid entry (its score is not stored)
     const uint8_t* src = kc + (b * N + j) * 32;
-    const uint32_t a = smem_u32(sm + kDtAOff + s * 16384);
+    const uint32_t a = smem_u32(sm + kDtAOff + (s >> 1) * 16384);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) cp_async8(a + sw128_off(tid, i), src + 8 * i);
+    for (int i = 0; i < 4; ++i) cp_async8(a + sw128_off(tid, 4 * (s & 1) + i), src + 8 * i);
     cp_async_arrive(&ms->full[s]);
   };
   bool ok = true;
-  for (int u = 0; u < kDtStages - 1 && u < ntiles; ++u) load_tile(u);
+  for (int u = 0; u < kDtAhead && u < ntiles; ++u) load_tile(u);
   // the chunk's scale bytes (two per entry), staged once: every load of the
   // thread in flight before the first store
   {
@@ -647,22 +652,24 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
   };
 
   for (int u = 0; u < ntiles && ok; ++u) {
-    // the copies of tile u + kDtStages - 1, once the MMAs of its stage's last tile (u - 1) are done
-    const int ul = u + kDtStages - 1;
+    // the copies of tile u + kDtAhead, once the MMAs of its slot's last tile are done
+    const int ul = u + kDtAhead;
     if (ul < ntiles) {
-      if (ul >= kDtStages && !mbar_wait(&ms->empty[ul % kDtStages], (uint32_t)(ul / kDtStages - 1) & 1, kIxWait))
+      if (ul >= kDtSlots && !mbar_wait(&ms->empty[ul % kDtSlots], (uint32_t)(ul / kDtSlots - 1) & 1, kIxWait))
         ok = false;
       if (ok) load_tile(ul);
     }
     // warp 0: the two block MMAs of tile u into TMEM buffer u % kDtTbufs
     if (warp == 0 && ok) {
-      const int s = u % kDtStages, tb = u % kDtTbufs;
-      bool got = mbar_wait(&ms->full[s], (uint32_t)(u / kDtStages) & 1, kIxWait);
+      const int s = u % kDtSlots, tb = u % kDtTbufs;
+      bool got = mbar_wait(&ms->full[s], (uint32_t)(u / kDtSlots) & 1, kIxWait);
       if (got && u >= kDtTbufs) got = mbar_wait(&ms->tempty[tb], (uint32_t)(u / kDtTbufs - 1) & 1, kIxWait);
       if (got) {
         fence_after_sync();
         fence_proxy_async();   // the operand rows came through the generic proxy (cp.async)
-        const uint64_t ad = sdesc_sw128(aA + s * 16384, 16, 1024), bd = sdesc_sw128(aB, 16, 1024);
+        // the slot's tile starts 64 bytes into the rows for odd slots (K offset within the swizzle atom)
+        const uint64_t ad = sdesc_sw128(aA + (s >> 1) * 16384, 16, 1024) + (uint64_t)(4 * (s & 1)),
+                       bd = sdesc_sw128(aB, 16, 1024);
         const uint32_t d = tmem + 32u * tb;
         mma_f8f6f4_elect(d, ad, bd, id);
         mma_f8f6f4_elect(d + 16u, ad + 2, bd + 2, id);
