@@ -11,23 +11,20 @@
 // bf16 operands, fp32 accumulation in TMEM, online softmax in the exp2
 // domain with a lazy rescale), organised for a handful of rows: a row's
 // keys are split over many CTAs (one work item = one row and one split, at
-// most one item per SM, every item resident at once: cooperative launch),
-// and everything the long-row path does in separate launches happens here:
-//  * the query is loaded by TMA and its RoPE dims rotated to its position
-//    in shared memory by the softmax warps;
-//  * the producer warps build the row's ordered list of valid selected
-//    entries from idx (invalid ones set the device-check flag), prefetch the
-//    item's key rows into L2, and fetch each 64-key tile's 592-byte rows
-//    with bulk copies into the end of its ring slot; they then expand the
-//    FP8 codes (times their group scale: exact) and the bf16 RoPE dims into
-//    the slot's bf16 tile in place -- first the dims whose bf16 lines lie
-//    below the raw rows, then, once every producer warp holds the rest in
-//    registers, the others;
-//  * each item writes its normalised partial output (bf16) and its softmax
-//    statistics, the items of a row meet at a bounded grid barrier (a
-//    counter per row), and each item then merges one slice of the row's
-//    dims over all splits in split order, rotates the RoPE dims back and
-//    stores the output.
+// most one item per SM, every item resident at once: cooperative launch).
+// Two launches:
+//  * decode_gather_kernel writes every row's keys -- its valid selected
+//    entries in idx order (invalid ones set the device-check flag), or every
+//    visible entry, then its window tokens -- as contiguous bf16 rows
+//    (exact expansion of the 592-byte rows), with many CTAs per row;
+//  * attn_decode_kernel: the query is loaded by TMA and its RoPE dims
+//    rotated to its position in shared memory by the softmax warps; each
+//    64-key tile of the item's split is one set of TMA boxes from the
+//    gathered rows; each item writes its normalised partial output (bf16)
+//    and its softmax statistics, the items of a row meet at a bounded grid
+//    barrier (a counter per row), and each item then merges one slice of
+//    the row's dims over all splits in split order (inputs staged by bulk
+//    copies), rotates the RoPE dims back and stores the output.
 // Every wait is bounded; on expiry the CTA records the timeout flag in the
 // workspace, waits (bounded) for its own copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -56,11 +53,8 @@ constexpr uint32_t kQOff = 0;                     // 8 chunks x [64 heads x 128 
 constexpr uint32_t kKVOff = 65536;                // 2 slots x 8 chunks x [64 keys x 128 B]
 constexpr uint32_t kPOff = kKVOff + 131072;       // 2 buffers x [64 heads x 64 keys bf16]
 constexpr uint32_t kMiscOff = kPOff + 16384;      // barriers and per-head state
-constexpr uint32_t kListOff = kMiscOff + 2048;    // int32 list of the row's valid selected entries
 constexpr uint32_t kSmemBytes = 232448;           // 227 KiB
-constexpr int kMaxList = (int)((kSmemBytes - 1024 - kListOff) / 4);
-constexpr uint32_t kRawOff = 65536 - 64 * kMixRow;   // a tile's raw rows, at the end of its slot
-static_assert(kRawOff == 27648 && kRawOff > 3 * 8192, "raw rows must lie above bf16 chunks 0-2");
+constexpr int kMaxK = 4096;                       // selected entries per row at most
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O^T: 4 blocks of 64 columns (heads); lanes = dims
@@ -71,11 +65,10 @@ constexpr uint32_t kGridWaitLimit = 1u << 22; // polls of the row barrier (64 ns
 constexpr float kLazy = 8.0f;
 
 struct Misc {
-  uint64_t raw_full[2], kv_full[2], kv_empty[2], s_full[2], p_full[2];
+  uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
   uint64_t q_full, q_ready, o_full, drain[2], merge_in;
   uint32_t tmem;
   int abort;
-  int cnt[4];                       // valid selected entries per producer warp's share of idx
   int go;                           // the row barrier passed
   alignas(16) float alpha[2][kH];   // per-head rescale factors of a tile, double-buffered
 };
@@ -86,8 +79,6 @@ __device__ __forceinline__ bool vabort(const Misc* ms) {
   return *reinterpret_cast<const volatile int*>(&ms->abort) != 0;
 }
 
-// Barrier of the four producer warps (named barrier 2, 128 threads).
-__device__ __forceinline__ void producer_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 struct DParams {
   const __nv_bfloat16* q;   // [rows, 64, 512]
@@ -113,10 +104,139 @@ struct DParams {
   __nv_bfloat16* part_o;    // [items, 512 dims, 64 heads] normalised partial outputs
   float* part_ml;           // [items, 64, 2]: running max (log2 units), sum
   int* arrive;              // [rows] items that finished their partial (zero at launch)
+  __nv_bfloat16* xg;        // [rows, kp, 512] every row's keys in bf16, in order, zero past them
+  int64_t kp;               // key slots per row of xg (a multiple of the tile)
+  int* ecount;              // [rows] valid selected entries of each row (sparse)
 };
 
+// ---------------------------------------------------------------------------
+// Per row, ahead of the attention: the row's keys -- its valid selected
+// entries in idx order (or every visible entry), then its window tokens --
+// expanded exactly from the 592-byte rows to bf16 rows of xg, 64 per CTA
+// (grid: the row's key tiles x rows), with zeros past the row's keys in its
+// last tile.  A sparse row's CTAs each find the valid entries of their tile
+// from idx (a block-wide count of the valid ones before each position);
+// invalid indices set the device-check flag (tile 0's CTA) and are skipped.
+// ---------------------------------------------------------------------------
+constexpr int kGatherThreads = 256;
+
+__global__ void __launch_bounds__(kGatherThreads)
+decode_gather_kernel(const DParams p) {
+  pdl_begin();
+  __shared__ int32_t src_s[kTile];            // this tile's selected entries
+  __shared__ unsigned int wcnt_s[kGatherThreads / 32];
+  __shared__ int ne_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = blockIdx.x;
+  const int64_t row = blockIdx.y;
+  const int64_t b = row / p.Tq;
+  const int64_t t = p.q_pos[row];
+  const bool t_ok = t >= 0 && t < p.rope_rows;
+  const bool dense = p.idx == nullptr;
+  int ne = 0;
+  if (t_ok && dense) {
+    const int64_t nv = (t + 1) / p.m;
+    ne = (int)(nv < p.N ? nv : p.N);
+  } else if (t_ok) {
+    // thread tid owns idx entries [16 tid, 16 tid + 16): valid ones counted,
+    // their ranks found by a block-wide exclusive scan of the counts
+    constexpr int kPer = 16;   // k <= 4096 = 256 x 16
+    const int32_t* ir = p.idx + row * (int64_t)p.k;
+    int32_t js[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int i = kPer * tid + r;
+      js[r] = i < p.k ? __ldg(ir + i) : -1;
+    }
+    uint32_t okbits = 0;
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int32_t j = js[r];
+      const bool ok = j >= 0 && (int64_t)j < p.N && (int64_t)(j + 1) * p.m - 1 <= t;
+      if (tile == 0 && j >= 0 && !ok) flag_device_check(p.ws, (unsigned)j);
+      okbits |= ok ? 1u << r : 0u;
+    }
+    const unsigned int own = __popc(okbits);
+    unsigned int incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wcnt_s[warp] = incl;
+    __syncthreads();
+    unsigned int before = 0, total = 0;
+    for (int w2 = 0; w2 < kGatherThreads / 32; ++w2) {
+      if (w2 < warp) before += wcnt_s[w2];
+      total += wcnt_s[w2];
+    }
+    unsigned int pos = before + incl - own;
+    const int lo = tile * kTile;
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      if ((okbits >> r) & 1u) {
+        if ((int)pos >= lo && (int)pos < lo + kTile) src_s[pos - lo] = js[r];
+        ++pos;
+      }
+    }
+    ne = (int)total;
+    if (tile == 0 && tid == 0) p.ecount[row] = ne;
+  }
+  if (dense && tile == 0 && tid == 0) p.ecount[row] = ne;
+  if (tid == 0) ne_s = ne;
+  __syncthreads();
+  ne = ne_s;
+  const int64_t u_lo = t - p.W + 1 < 0 ? 0 : t - p.W + 1;
+  const int64_t p0 = p.W > 0 ? p.swa_pos0[b] : 0;
+  const int64_t w_lo = u_lo < p0 ? p0 : u_lo;
+  const int64_t w_hi = t < p0 + p.Ts - 1 ? t : p0 + p.Ts - 1;
+  const int nwin = (t_ok && p.W > 0 && w_hi >= w_lo) ? (int)(w_hi - w_lo + 1) : 0;
+  const int nkeys = ne + nwin;
+  if (tile * kTile >= nkeys) return;   // past the row's keys (uniform)
+  // warp w: slots 8 w .. 8 w + 7 of the tile; all eight rows' loads in flight together
+  uint4 c[8];
+  float sc[8];
+  uint4 rp[8][2];
+  bool have[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int key = tile * kTile + 8 * warp + i;
+    const uint8_t* rowp = nullptr;
+    if (key < ne) rowp = p.cache + (b * p.N + (dense ? (int64_t)key : (int64_t)src_s[key - tile * kTile])) * kMixRow;
+    else if (key < nkeys) rowp = p.swa + (b * p.Ts + (w_lo - p0 + (key - ne))) * kMixRow;
+    have[i] = rowp != nullptr;
+    c[i] = make_uint4(0, 0, 0, 0);
+    sc[i] = 0.0f;
+    rp[i][0] = rp[i][1] = make_uint4(0, 0, 0, 0);
+    if (rowp) {
+      if (lane < 28) {
+        c[i] = __ldg(reinterpret_cast<const uint4*>(rowp) + lane);
+        sc[i] = __ldg(reinterpret_cast<const float*>(rowp + kMixScaleOff) + (lane >> 3));
+      } else {
+        rp[i][0] = __ldg(reinterpret_cast<const uint4*>(rowp + kMixRopeOff) + 2 * (lane - 28));
+        rp[i][1] = __ldg(reinterpret_cast<const uint4*>(rowp + kMixRopeOff) + 2 * (lane - 28) + 1);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int key = tile * kTile + 8 * warp + i;
+    uint4* dst = reinterpret_cast<uint4*>(p.xg + (row * p.kp + key) * kD);
+    if (lane < 28) {
+      uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+      if (have[i]) dequant16(c[i], sc[i], o0, o1);
+      dst[2 * lane] = o0;
+      dst[2 * lane + 1] = o1;
+    } else {
+      dst[56 + 2 * (lane - 28)] = rp[i][0];
+      dst[56 + 2 * (lane - 28) + 1] = rp[i][1];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
+attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_xg) {
   pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -124,7 +244,6 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
   uint8_t* sKV = sm + kKVOff;
   uint8_t* sP = sm + kPOff;
   Misc* ms = reinterpret_cast<Misc*>(sm + kMiscOff);
-  int32_t* list = reinterpret_cast<int32_t*>(sm + kListOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t item = blockIdx.x;
   const int64_t row = item / p.nsplit;
@@ -138,8 +257,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
     ms->abort = 0;
     ms->go = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms->raw_full[i], 4 + 128);   // one arrive per producer warp, one counted per producer lane
-      mbar_init(&ms->kv_full[i], 4);    // one arrive per producer warp once its rows are expanded
+      mbar_init(&ms->kv_full[i], 1);    // the tile's TMA boxes (one arrive with their byte count)
       mbar_init(&ms->kv_empty[i], 1);
       mbar_init(&ms->s_full[i], 1);
       mbar_init(&ms->p_full[i], 4);
@@ -158,50 +276,13 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
   fence_after_sync();
   const uint32_t tmem = ms->tmem;
 
-  // ---- the query: 8 TMA boxes, in flight while the entry list is built ----
+  // ---- the query: 8 TMA boxes ----
   if (warp == kMmaWarp) {
     if (lane == 0) mbar_arrive_expect_tx(&ms->q_full, kH * kD * 2);
     __syncwarp();
     if (lane < 8) tma_load_2d(smem_u32(sQ) + lane * 8192, &tm_q, 64 * lane, (int)(row * kH), &ms->q_full);
     __syncwarp();
   }
-  // ---- sparse: the row's valid selected entries, in idx order ----
-  if (!dense && warp >= 4 && warp < 8) {
-    const int pw = warp - 4;
-    const int seg = ((p.k + 3) / 4 + 31) / 32 * 32;
-    const int lo = pw * seg, hi = min(p.k, lo + seg);
-    const int32_t* ir = p.idx + row * (int64_t)p.k;
-    // the warp's share of idx: at most 32 per lane (k <= 4096), all loads in flight together
-    int32_t js[32];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int i = lo + 32 * r + lane;
-      js[r] = i < hi ? __ldg(ir + i) : -1;
-    }
-    uint32_t okbits = 0;
-    int cnt = 0;
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int32_t j = js[r];
-      const bool ok = t_ok && j >= 0 && (int64_t)j < p.N && (int64_t)(j + 1) * p.m - 1 <= t;
-      if (split == 0 && t_ok && j >= 0 && !ok) flag_device_check(p.ws, (unsigned)j);
-      okbits |= ok ? 1u << r : 0u;
-      cnt += __popc(__ballot_sync(0xffffffffu, ok));
-    }
-    if (lane == 0) ms->cnt[pw] = cnt;
-    producer_sync();
-    int out = 0;
-    for (int w2 = 0; w2 < pw; ++w2) out += ms->cnt[w2];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const bool ok = (okbits >> r) & 1u;
-      const unsigned bal = __ballot_sync(0xffffffffu, ok);
-      if (ok) list[out + __popc(bal & ((1u << lane) - 1u))] = js[r];
-      out += __popc(bal);
-    }
-  }
-  __syncthreads();
-
   // ---- this item's keys: entries first, then the window tokens ----
   int ne = 0;
   if (t_ok) {
@@ -209,7 +290,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
       const int64_t nv = (t + 1) / p.m;
       ne = (int)(nv < p.N ? nv : p.N);
     } else {
-      ne = min(ms->cnt[0] + ms->cnt[1] + ms->cnt[2] + ms->cnt[3], kMaxList);
+      ne = p.ecount[row];
     }
   }
   const int64_t u_lo = t - p.W + 1 < 0 ? 0 : t - p.W + 1;
@@ -227,139 +308,36 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q) {
   const int tlo = min(ntiles, split * per);
   const int thi = min(ntiles, tlo + per);
   const int key_hi = min(nkeys, thi * kTile);
-  // the key row of key number `key` of this row, or NULL past its keys
-  auto key_row = [&](int key) -> const uint8_t* {
-    if (key >= key_hi) return nullptr;
-    if (key < ne) return p.cache + (b * p.N + (dense ? (int64_t)key : (int64_t)list[key])) * kMixRow;
-    return p.swa + (b * p.Ts + (w_lo - p0 + (key - ne))) * kMixRow;
-  };
   bool fail = false;
 
   if (warp >= 4 && warp < 8) {
     // ================================ producers ================================
+    // the row's keys are contiguous bf16 rows of xg: 8 TMA boxes of 64 rows x
+    // 64 columns per tile, from producer warp 0 (the tile's other warps idle)
     const int pw = warp - 4;
-    // dense keys are runs of consecutive rows (the entries, then the window):
-    // the item's runs into L2 now, in pieces of at most 64 rows
-    if (dense && pw == 0) {
-      const int e_lo = tlo * kTile, e_hi = min(ne, key_hi);
-      for (int r = e_lo + 64 * lane; r < e_hi; r += 64 * 32)
-        prefetch_l2(p.cache + (b * p.N + r) * kMixRow, (uint32_t)min(64, e_hi - r) * kMixRow);
-      const int w_lo2 = max(ne, tlo * kTile), w_hi2 = key_hi;
-      for (int r = w_lo2 + 64 * lane; r < w_hi2; r += 64 * 32)
-        prefetch_l2(p.swa + (b * p.Ts + (w_lo - p0 + (r - ne))) * kMixRow, (uint32_t)min(64, w_hi2 - r) * kMixRow);
-    }
     uint32_t g = 0;
     bool ok = true;
-    for (int tl = tlo; tl < thi && ok && !vabort(ms); ++tl, ++g) {
-      const int buf = g & 1;
-      if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
-        ok = false;
-        break;
-      }
-      uint8_t* slot = sKV + buf * 65536;
-      uint8_t* raw = slot + kRawOff;
-      // this warp's 16 rows of the tile (valid ones in vmask); dense: the
-      // tile's runs of consecutive rows as at most two bulk copies (warp 0);
-      // sparse: 16-byte asynchronous copies, 37 per row, spread over the lanes
-      const int r0 = 16 * pw;
-      const uint8_t* src = lane < 16 ? key_row(tl * kTile + r0 + lane) : nullptr;
-      const unsigned vmask = __ballot_sync(0xffffffffu, src != nullptr);
-      if (dense) {
-        if (pw == 0 && lane == 0) {
-          const int k0 = tl * kTile, k1 = min(key_hi, k0 + kTile);
-          const int ce = max(k0, min(ne, k1));   // entries [k0, ce), window [ce, k1)
-          mbar_arrive_expect_tx(&ms->raw_full[buf], (uint32_t)(k1 - k0) * kMixRow);
-          if (ce > k0)
-            bulk_copy_g2s(smem_u32(raw), p.cache + (b * p.N + k0) * kMixRow, (uint32_t)(ce - k0) * kMixRow,
-                          &ms->raw_full[buf]);
-          if (k1 > ce)
-            bulk_copy_g2s(smem_u32(raw + (ce - k0) * kMixRow), p.swa + (b * p.Ts + (w_lo - p0 + (ce - ne))) * kMixRow,
-                          (uint32_t)(k1 - ce) * kMixRow, &ms->raw_full[buf]);
-        } else if (lane == 0) {
-          mbar_arrive(&ms->raw_full[buf]);
+    if (pw == 0) {
+      for (int tl = tlo; tl < thi && ok && !vabort(ms); ++tl, ++g) {
+        const int buf = g & 1;
+        if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          break;
         }
-      } else {
-        if (lane == 0) mbar_arrive(&ms->raw_full[buf]);
-        const unsigned long long sp = reinterpret_cast<unsigned long long>(src);
-#pragma unroll 1
-        for (int it = 0; it < (16 * 37 + 31) / 32; ++it) {
-          const int q = lane + 32 * it;
-          const int i = q / 37, u = q - 37 * (q / 37);
-          const unsigned long long rp = __shfl_sync(0xffffffffu, sp, q < 16 * 37 ? i : 0);
-          if (q < 16 * 37 && rp)
-            cp_async16(smem_u32(raw + (r0 + i) * kMixRow + 16 * u), reinterpret_cast<const uint8_t*>(rp) + 16 * u);
-        }
+        const uint32_t tb = smem_u32(sKV + buf * 65536);
+        if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], kTile * kD * 2);
+        __syncwarp();
+        if (lane < 8)
+          tma_load_2d(tb + lane * 8192, &tm_xg, 64 * lane, (int)(row * p.kp + (int64_t)tl * kTile), &ms->kv_full[buf]);
+        __syncwarp();
       }
-      cp_async_mbar_arrive_noinc(&ms->raw_full[buf]);
-      __syncwarp();
-      if (!mbar_wait(&ms->raw_full[buf], (g >> 1) & 1, kWaitLimit)) {
-        ok = false;
-        break;
+      if (!ok) {
+        ms->abort = 1;
+        if (lane == 0) flag_timeout(p.ws);
+        fail = true;
       }
-      // phase 1: bf16 chunks 0-2 (dims 0..191, below the raw rows), and the
-      // rest of this warp's rows into registers
-#pragma unroll 4
-      for (int v = 0; v < 12; ++v) {
-        const int U = lane + 32 * v;                // 16 rows x 24 units of 8 dims
-        const int i = U / 24, u = U - 24 * (U / 24);
-        const int r = r0 + i;
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if ((vmask >> i) & 1u) {
-          const uint8_t* rr = raw + r * kMixRow;
-          const uint2 c = *reinterpret_cast<const uint2*>(rr + 8 * u);
-          const float sc = *reinterpret_cast<const float*>(rr + kMixScaleOff + 4 * (u >> 4));
-          o = dequant8(c, sc);
-        }
-        *reinterpret_cast<uint4*>(slot + (u >> 3) * 8192 + sw128((uint32_t)r, (uint32_t)(u & 7))) = o;
-      }
-      // dims 192..447: unit 24 + lane of each row (group 1, 2 or 3 by lane)
-      // (the group scales are powers of two: their exponent bytes, four per word)
-      const int gsc = lane < 8 ? 1 : (lane < 24 ? 2 : 3);
-      uint2 hc[16];
-      uint32_t hs[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        hc[i] = make_uint2(0, 0);
-        if ((vmask >> i) & 1u) {
-          const uint8_t* rr = raw + (r0 + i) * kMixRow;
-          hc[i] = *reinterpret_cast<const uint2*>(rr + 8 * (24 + lane));
-          const uint32_t sb = *reinterpret_cast<const uint32_t*>(rr + kMixScaleOff + 4 * gsc);
-          hs[i >> 2] |= ((sb >> 23) & 0xffu) << (8 * (i & 3));
-        }
-      }
-      // RoPE dims: 16 rows x 8 units of 16 bytes, four per lane
-      uint4 hr[4];
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int U = lane + 32 * v, i = U >> 3, u = U & 7;
-        hr[v] = make_uint4(0, 0, 0, 0);
-        if ((vmask >> i) & 1u) hr[v] = *reinterpret_cast<const uint4*>(raw + (r0 + i) * kMixRow + kMixRopeOff + 16 * u);
-      }
-      producer_sync();   // every producer warp holds what it still needs of the raw rows
-      // phase 2: chunks 3-6 (FP8) and 7 (RoPE) over the raw rows
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int u = 24 + lane, r = r0 + i;
-        const float sc = __uint_as_float(((hs[i >> 2] >> (8 * (i & 3))) & 0xffu) << 23);
-        const uint4 o = ((vmask >> i) & 1u) ? dequant8(hc[i], sc) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(slot + (u >> 3) * 8192 + sw128((uint32_t)r, (uint32_t)(u & 7))) = o;
-      }
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int U = lane + 32 * v, i = U >> 3, u = U & 7, r = r0 + i;
-        *reinterpret_cast<uint4*>(slot + 7 * 8192 + sw128((uint32_t)r, (uint32_t)u)) = hr[v];
-      }
-      fence_proxy_async();   // generic-proxy writes, read next by the tensor cores
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ms->kv_full[buf]);
-    }
-    if (!ok) {
-      ms->abort = 1;
-      if (lane == 0) flag_timeout(p.ws);
-      fail = true;
-      // a bulk copy of this tile may still be in flight: let it land
-      cp_async_wait_all();
-      if (g < (uint32_t)(thi - tlo)) mbar_wait(&ms->raw_full[g & 1], (g >> 1) & 1, kWaitLimit);
+      // the copies of this warp land before the CTA can exit
+      if (g > 0) mbar_wait(&ms->kv_full[(g - 1) & 1], ((g - 1) >> 1) & 1, kWaitLimit);
     }
   } else if (warp == kMmaWarp) {
     // ============================== QK^T issue ==============================
@@ -755,12 +733,15 @@ int attn_decode_splits(int64_t rows, int64_t max_keys) {
 
 bool attn_decode_applies(int H, int D, int R, int64_t rows, int k, bool sparse) {
   const int sms = device_sms() > 0 ? device_sms() : 148;
-  return H == kH && D == kD && R == 64 && rows > 0 && rows < sms && (!sparse || k <= kMaxList);
+  return H == kH && D == kD && R == 64 && rows > 0 && rows < sms && (!sparse || k <= kMaxK);
 }
+
+int64_t attn_decode_kp(int64_t max_keys) { return (max_keys + kTile - 1) / kTile * kTile; }
 
 size_t attn_decode_workspace(int64_t rows, int64_t max_keys) {
   const int64_t items = rows * attn_decode_splits(rows, max_keys);
-  return al256((size_t)items * kH * kD * 2) + al256((size_t)items * kH * 2 * 4) + al256((size_t)rows * 4);
+  return al256((size_t)items * kH * kD * 2) + al256((size_t)items * kH * 2 * 4) + al256((size_t)rows * 4) +
+         al256((size_t)rows * 4) + al256((size_t)rows * attn_decode_kp(max_keys) * kD * 2);
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
@@ -793,7 +774,12 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   p.part_ml = reinterpret_cast<float*>(base);
   base += al256((size_t)items * kH * 2 * 4);
   p.arrive = reinterpret_cast<int*>(base);
-  CUtensorMap tm_q;
+  base += al256((size_t)rows * 4);
+  p.ecount = reinterpret_cast<int*>(base);
+  base += al256((size_t)rows * 4);
+  p.kp = attn_decode_kp(a.max_keys);
+  p.xg = reinterpret_cast<__nv_bfloat16*>(base);
+  CUtensorMap tm_q, tm_xg;
   {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorInvalidValue;
@@ -805,8 +791,15 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+    const cuuint64_t gdims[2] = {(cuuint64_t)kD, (cuuint64_t)(rows * p.kp)};
+    if (fn(&tm_xg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.xg, gdims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaMemsetAsync(p.arrive, 0, (size_t)rows * 4, st);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(decode_gather_kernel, dim3((unsigned)(p.kp / kTile), (unsigned)rows), dim3(kGatherThreads), 0, st, p);
   if (e != cudaSuccess) return e;
   static PerDevice attr;
   smem_limit_once(attr, reinterpret_cast<const void*>(attn_decode_kernel), (int)kSmemBytes);
@@ -821,7 +814,7 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   attrs[0].val.cooperative = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, p, tm_q);
+  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, p, tm_q, tm_xg);
   return e;
 }
 

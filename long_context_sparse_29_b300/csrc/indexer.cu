@@ -894,7 +894,7 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
   extern __shared__ __align__(16) unsigned long long dyn_s[];
   __shared__ unsigned int warp_sum[NT / 32];
   __shared__ int bstar_s, last_s, base_s, base_t;
-  __shared__ unsigned int above_s, nls_s, nlt_s, take_s;
+  __shared__ unsigned int nls_s, nlt_s, take_s;
   __shared__ TkShared<NT> sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.y;
@@ -928,7 +928,6 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
     if (lane == 31) warp_sum[warp] = incl;
     if (tid == 0) {
       bstar_s = -1;
-      above_s = 0;
       nls_s = 0;
       nlt_s = 0;
     }
@@ -939,10 +938,8 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
     if (kk > 0 && kk < nv) {
       if (excl < (unsigned)kk && excl + h0 >= (unsigned)kk) {
         bstar_s = kHistBins - 1 - 2 * tid;
-        above_s = excl;
       } else if (excl + h0 < (unsigned)kk && excl + own >= (unsigned)kk) {
         bstar_s = kHistBins - 2 - 2 * tid;
-        above_s = excl + h0;
       }
     }
     __syncthreads();
