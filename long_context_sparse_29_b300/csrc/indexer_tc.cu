@@ -710,6 +710,279 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
   }
 }
 
+// ---------------------------------------------------------------------------
+// The same decode scoring with the operand tiles brought in by TMA: the key
+// codes viewed as rows of two entries (128 E2M1 values, 64 bytes), loaded
+// with the tensor-map element type that writes every 16 packed values as 8
+// bytes followed by an 8-byte gap -- the padded operand form above -- so one
+// box of 128 rows is 256 entries: entry 2r in bytes 0..63 of row r, entry
+// 2r + 1 in bytes 64..127.  Four MMAs per tile (two entry parities x two
+// blocks) into 64 TMEM columns; thread r of the epilogue combines entries 2r
+// and 2r + 1 (two independent head chains).  Needs an even N (a row of the
+// view never straddles two sequences).
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kDmEntries = 256;             // entries per tile
+constexpr int kDmStages = 4;                // 16 KiB TMA boxes
+constexpr int kDmTbufs = 4;                 // TMEM buffers of 64 columns
+constexpr int kDmLag = 2;                   // tiles between a tile's MMAs and its epilogue
+constexpr int kDmMaxChunk = 4096;           // entries per CTA at most (their scale bytes are staged)
+constexpr uint32_t kDmBOff = 0;             // query operand, 16 rows x 128 B
+constexpr uint32_t kDmAOff = 2048;          // kDmStages x [128 rows x 128 B]
+constexpr uint32_t kDmSOff = kDmAOff + kDmStages * 16384;
+constexpr uint32_t kDmHOff = kDmSOff + kDmMaxChunk * 2;
+constexpr uint32_t kDmMiscOff = kDmHOff + (1u << kDtHistBits) * 4;
+constexpr uint32_t kDmSmem = kDmMiscOff + 512 + 1024;
+
+struct DmMisc {
+  uint64_t full[kDmStages], empty[kDmStages], tfull[kDmTbufs], tempty[kDmTbufs];
+  uint32_t tmem;
+  int qlo0, qhi0, qlo1, qhi1;
+  int4 hx[kDtHeads];
+};
+static_assert(sizeof(DmMisc) <= 512, "DmMisc overflows its smem slot");
+
+}  // namespace
+
+__global__ void __launch_bounds__(kDtThreads, 2)
+scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
+                             const uint8_t* __restrict__ ks, const int64_t* __restrict__ q_pos, int64_t Tq,
+                             int HI, int64_t N, int m, int64_t chunk, float* __restrict__ scores,
+                             unsigned int* __restrict__ hist, void* ws, const __grid_constant__ CUtensorMap tm_k) {
+  pdl_begin();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DmMisc* ms = reinterpret_cast<DmMisc*>(sm + kDmMiscOff);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t row = blockIdx.y;
+  const int64_t b = row / Tq;
+  const int64_t nv = visible(q_pos[row], m, N);
+  const int64_t c0 = (int64_t)blockIdx.x * chunk;
+  if (c0 >= nv) return;   // uniform
+  const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
+  const int ntiles = (int)((c1 - c0 + kDmEntries - 1) / kDmEntries);
+  const int64_t vrow0 = (b * N + c0) / 2;   // first row of the two-entry view
+
+  for (int i = tid; i < 2048 / 16; i += kDtThreads) reinterpret_cast<uint4*>(sm + kDmBOff)[i] = make_uint4(0, 0, 0, 0);
+  unsigned int* hist_s = reinterpret_cast<unsigned int*>(sm + kDmHOff);
+  if (hist)
+    for (int i = tid; i < (1 << kDtHistBits); i += kDtThreads) hist_s[i] = 0u;
+  if (tid == 0) {
+    for (int s = 0; s < kDmStages; ++s) {
+      mbar_init(&ms->full[s], 1);
+      mbar_init(&ms->empty[s], 1);
+    }
+    for (int i = 0; i < kDmTbufs; ++i) {
+      mbar_init(&ms->tfull[i], 1);
+      mbar_init(&ms->tempty[i], 4);
+    }
+    mbar_fence_init();
+    ms->qlo0 = ms->qlo1 = 1 << 30;
+    ms->qhi0 = ms->qhi1 = -(1 << 30);
+  }
+  if (warp == 0) tmem_alloc(&ms->tmem, kDmTbufs * 64);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = ms->tmem;
+  const uint32_t aA = smem_u32(sm + kDmAOff), aB = smem_u32(sm + kDmBOff);
+  // tile u: one box of 128 view rows into stage u % kDmStages (thread 0)
+  auto load_tile = [&](int u) {
+    const int s = u % kDmStages;
+    mbar_arrive_expect_tx(&ms->full[s], 16384);
+    tma_load_2d(aA + s * 16384, &tm_k, 0, (int)(vrow0 + (int64_t)u * (kDmEntries / 2)), &ms->full[s]);
+  };
+  bool ok = true;
+  if (tid == 0)
+    for (int u = 0; u < kDmStages && u < ntiles; ++u) load_tile(u);
+  // the chunk's scale bytes, staged once: every load of the thread in flight together
+  {
+    uint16_t* sc_s = reinterpret_cast<uint16_t*>(sm + kDmSOff);
+    const uint16_t* ks16 = reinterpret_cast<const uint16_t*>(ks) + b * N + c0;
+    const int n = (int)(c1 - c0);
+    uint16_t v[kDmMaxChunk / kDtThreads];
+#pragma unroll
+    for (int r = 0; r < kDmMaxChunk / kDtThreads; ++r) {
+      const int i = tid + r * kDtThreads;
+      v[r] = i < n ? __ldg(ks16 + i) : (uint16_t)0;
+    }
+#pragma unroll
+    for (int r = 0; r < kDmMaxChunk / kDtThreads; ++r) {
+      const int i = tid + r * kDtThreads;
+      if (i < n) sc_s[i] = v[r];
+    }
+  }
+  // ---- the query: MXFP4 codes into the B operand, block exponents ----
+  for (int blkid = tid >> 3; blkid < 2 * kDtHeads; blkid += kDtThreads / 8) {
+    const int u = tid & 7, h = blkid >> 1, blk = blkid & 1;
+    const bool act = h < HI;
+    float v[4];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] = act ? __bfloat162float(qI[(row * HI + h) * 64 + 32 * blk + 4 * u + i]) : 0.0f;
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int sx = mx_block_exp(amax);
+    const float inv = pow2i(-sx);
+    if (act) {
+      uint32_t cd = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cd |= e2m1_encode(__fmul_rn(v[i], inv)) << (4 * i);
+      *reinterpret_cast<uint16_t*>(sm + kDmBOff + sw128_off(h, 2 * blk + (u >> 2)) + 2 * (u & 3)) = (uint16_t)cd;
+      if (u == 0) {
+        if (blk == 0) {
+          atomicMin(&ms->qlo0, sx);
+          atomicMax(&ms->qhi0, sx);
+          ms->hx[h].x = sx << 23;
+          ms->hx[h].z = __float_as_int(w[row * HI + h]);
+        } else {
+          atomicMin(&ms->qlo1, sx);
+          atomicMax(&ms->qhi1, sx);
+          ms->hx[h].y = sx << 23;
+        }
+      }
+    }
+  }
+  fence_proxy_async();
+  fence_before_sync();
+  __syncthreads();
+  const int qlo0 = ms->qlo0, qhi0 = ms->qhi0, qlo1 = ms->qlo1, qhi1 = ms->qhi1;
+  constexpr uint32_t id = idesc_e2m1(kDtThreads, kDtHeads);
+  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  int issued = 0;
+
+  // one entry's score from its 32 block dots (P[0..15] block 0, P[16..31] block 1)
+  auto score_of = [&](const uint32_t* P, uint32_t sc) -> float {
+    const int x0 = (int)(sc & 0xffu), x1 = (int)((sc >> 8) & 0xffu);
+    const int X0 = x0 << 23, X1 = x1 << 23;
+    const bool fast = qlo0 + x0 >= 27 && qhi0 + x0 <= 227 && qlo1 + x1 >= 27 && qhi1 + x1 <= 227;
+    float s = 0.0f;
+    if (fast) {
+#pragma unroll
+      for (int h = 0; h < kDtHeads; ++h) {
+        if (h < HI) {
+          const int4 hx = ms->hx[h];
+          const float d = __fmaf_rn(__uint_as_float(P[h]), __int_as_float(hx.x + X0),
+                                    __fmul_rn(__uint_as_float(P[16 + h]), __int_as_float(hx.y + X1)));
+          s = __fmaf_rn(__int_as_float(hx.z), fmaxf(d, 0.0f), s);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < kDtHeads; ++h) {
+        if (h < HI) {
+          const int4 hx = ms->hx[h];
+          const float d = __fadd_rn(scale_pow2(__uint_as_float(P[h]), (hx.x >> 23) + x0 - 127),
+                                    scale_pow2(__uint_as_float(P[16 + h]), (hx.y >> 23) + x1 - 127));
+          s = __fmaf_rn(__int_as_float(hx.z), d > 0.0f ? d : 0.0f, s);
+        }
+      }
+    }
+    return s;
+  };
+  auto to_key_bin = [&](float s) -> uint32_t {
+    uint32_t key = __float_as_uint(s);
+    if (key == 0x80000000u) key = 0u;
+    key = (key & 0x80000000u) ? ~key : (key | 0x80000000u);
+    return key >> (32 - kDtHistBits);
+  };
+  // the epilogue of tile u: thread r = view row r = entries 2r and 2r + 1
+  auto combine = [&](int u) {
+    const int tb = u % kDmTbufs;
+    if (ok && !mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDmTbufs) & 1, kIxWait)) ok = false;
+    fence_after_sync();
+    uint32_t P0[32], P1[32];
+    tmem_ld32(tmem + lane_base + 64u * tb, P0);
+    tmem_ld32(tmem + lane_base + 64u * tb + 32u, P1);
+    tmem_wait_ld();
+    fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ms->tempty[tb]);
+    const int64_t jl = (int64_t)u * kDmEntries + 2 * tid;   // chunk-relative index of entry 2r
+    uint32_t sc2 = 0x7f7f7f7fu;
+    if (jl + 1 < c1 - c0) sc2 = *reinterpret_cast<const uint32_t*>(sm + kDmSOff + 2 * jl);
+    else if (jl < c1 - c0) sc2 = 0x7f7f0000u | reinterpret_cast<const uint16_t*>(sm + kDmSOff)[jl];
+    const float s0 = score_of(P0, sc2 & 0xffffu), s1 = score_of(P1, sc2 >> 16);
+    if (ok) {
+      const int64_t j = c0 + jl;
+      if (jl + 1 < c1 - c0) {
+        *reinterpret_cast<float2*>(scores + row * N + j) = make_float2(s0, s1);
+        if (hist) {
+          atomicAdd(hist_s + to_key_bin(s0), 1u);
+          atomicAdd(hist_s + to_key_bin(s1), 1u);
+        }
+      } else if (jl < c1 - c0) {
+        scores[row * N + j] = s0;
+        if (hist) atomicAdd(hist_s + to_key_bin(s0), 1u);
+      }
+    }
+  };
+
+  int loaded = min(ntiles, kDmStages);   // tiles whose boxes were issued
+  for (int u = 0; u < ntiles && ok; ++u) {
+    if (warp == 0) {
+      bool got = true;
+      // the stage of tile u - 1 takes tile u - 1 + kDmStages once tile u - 1's MMAs are done
+      if (u >= 1 && u - 1 + kDmStages < ntiles) {
+        const int sp = (u - 1) % kDmStages;
+        if (lane == 0) {
+          if (mbar_wait(&ms->empty[sp], (uint32_t)((u - 1) / kDmStages) & 1, kIxWait)) load_tile(u - 1 + kDmStages);
+          else got = false;
+        }
+        got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+        if (got) loaded = u - 1 + kDmStages + 1;
+      }
+      const int s = u % kDmStages, tb = u % kDmTbufs;
+      if (got) got = mbar_wait(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxWait);
+      if (got && u >= kDmTbufs) got = mbar_wait(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxWait);
+      if (got) {
+        fence_after_sync();
+        const uint64_t ad = sdesc_sw128(aA + s * 16384, 16, 1024), bd = sdesc_sw128(aB, 16, 1024);
+        const uint32_t d = tmem + 64u * tb;
+#pragma unroll
+        for (int par = 0; par < 2; ++par) {
+          mma_f8f6f4_elect(d + 32u * par, ad + (uint64_t)(4 * par), bd, id);
+          mma_f8f6f4_elect(d + 32u * par + 16u, ad + (uint64_t)(4 * par + 2), bd + 2, id);
+        }
+        mma_commit_elect(&ms->tfull[tb]);
+        mma_commit_elect(&ms->empty[s]);
+        ++issued;
+      }
+      if (!got) ok = false;
+      __syncwarp();
+    }
+    if (u >= kDmLag) combine(u - kDmLag);
+  }
+  for (int u = max(0, ntiles - kDmLag); u < ntiles && ok; ++u) combine(u);
+  if (!ok && lane == 0) flag_timeout(ws);
+  if (hist) {
+    __syncthreads();
+    for (int i = tid; i < (1 << kDtHistBits); i += kDtThreads) {
+      const unsigned int v = hist_s[i];
+      if (v) atomicAdd(hist + row * (int64_t)(1 << kDtHistBits) + i, v);
+    }
+  }
+  // boxes and MMAs of this CTA land before its TMEM and shared memory go
+  if (warp == 0 && issued > 0) {
+    const int u = issued - 1;
+    mbar_wait(&ms->tfull[u % kDmTbufs], (uint32_t)(u / kDmTbufs) & 1, kIxWait);
+  }
+  if (tid == 0 && !ok) {
+    // boxes issued for tiles whose MMAs never ran: let them land
+    for (int u = issued; u < loaded; ++u) mbar_wait(&ms->full[u % kDmStages], (uint32_t)(u / kDmStages) & 1, kIxWait);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, kDmTbufs * 64);
+  }
+}
+
 namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -833,6 +1106,36 @@ cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const ui
   chunk = (chunk + kDtThreads - 1) / kDtThreads * kDtThreads;
   if (chunk < 2 * kDtThreads) chunk = 2 * kDtThreads;
   if (chunk > kDtMaxChunk) chunk = kDtMaxChunk;
+  // even N: the TMA-fed kernel (the two-entry view of the codes never
+  // straddles two sequences); otherwise the copy-fed one
+  CUtensorMap tm;
+  if ((N & 1) == 0 && (reinterpret_cast<uintptr_t>(kc) & 31) == 0 && ix_encode_fn()) {
+    const cuuint64_t dims[2] = {128, (cuuint64_t)((int64_t)B * N / 2)};
+    const cuuint64_t strides[1] = {64};
+    const cuuint32_t box[2] = {128u, 128u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    if (ix_encode_fn()(&tm, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(kc), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+      static PerDevice attr_m, slots_m;
+      smem_limit_once(attr_m, reinterpret_cast<const void*>(scores_fp4_decode_tma_kernel), (int)kDmSmem);
+      const int sl = slots_m.get([] {
+        int per = resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_tma_kernel), kDtThreads, kDmSmem);
+        per = per > 2 ? 2 : per;   // 256 TMEM columns each: at most 2 per SM
+        return device_sms() * per;
+      });
+      int64_t pr = sl / rows;
+      if (pr < 1) pr = 1;
+      int64_t ch = (N + pr - 1) / pr;
+      ch = (ch + kDmEntries - 1) / kDmEntries * kDmEntries;
+      if (ch < 2 * kDmEntries) ch = 2 * kDmEntries;
+      if (ch > kDmMaxChunk) ch = kDmMaxChunk;
+      const dim3 g2((unsigned)((N + ch - 1) / ch), (unsigned)rows);
+      launch_pdl(scores_fp4_decode_tma_kernel, g2, dim3(kDtThreads), kDmSmem, st,
+                 reinterpret_cast<const __nv_bfloat16*>(qI), w, ks, q_pos, Tq, HI, N, m, ch, scores, hist, flags_ws, tm);
+      return cudaGetLastError();
+    }
+  }
   const dim3 grid((unsigned)((N + chunk - 1) / chunk), (unsigned)rows);
   launch_pdl(scores_fp4_decode_tc_kernel, dim3(grid), dim3(kDtThreads), kDtSmem, st, reinterpret_cast<const __nv_bfloat16*>(qI), w, kc,
                                                                  ks, q_pos, Tq, HI, N, m, chunk, scores, hist, flags_ws);
