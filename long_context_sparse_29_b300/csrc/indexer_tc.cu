@@ -714,7 +714,8 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
 // The same decode scoring with the operand tiles brought in by TMA: the key
 // codes viewed as rows of two entries (128 E2M1 values, 64 bytes), loaded
 // with the tensor-map element type that writes every 16 packed values as 8
-// bytes followed by an 8-byte gap -- the padded operand form above -- so one
+// bytes followed by an 8-byte gap -- the padded operand form above; the gaps
+// are not written, and a box's transaction count is its global bytes -- so one
 // box of 128 rows is 256 entries: entry 2r in bytes 0..63 of row r, entry
 // 2r + 1 in bytes 64..127.  Four MMAs per tile (two entry parities x two
 // blocks) into 64 TMEM columns; thread r of the epilogue combines entries 2r
@@ -764,7 +765,9 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   const int ntiles = (int)((c1 - c0 + kDmEntries - 1) / kDmEntries);
   const int64_t vrow0 = (b * N + c0) / 2;   // first row of the two-entry view
 
-  for (int i = tid; i < 2048 / 16; i += kDtThreads) reinterpret_cast<uint4*>(sm + kDmBOff)[i] = make_uint4(0, 0, 0, 0);
+  // the query operand and the key stages zeroed: TMA leaves the gaps of the padded form untouched
+  for (int i = tid; i < (int)(kDmSOff / 16); i += kDtThreads) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async();
   unsigned int* hist_s = reinterpret_cast<unsigned int*>(sm + kDmHOff);
   if (hist)
     for (int i = tid; i < (1 << kDtHistBits); i += kDtThreads) hist_s[i] = 0u;
@@ -790,7 +793,7 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   // tile u: one box of 128 view rows into stage u % kDmStages (thread 0)
   auto load_tile = [&](int u) {
     const int s = u % kDmStages;
-    mbar_arrive_expect_tx(&ms->full[s], 16384);
+    mbar_arrive_expect_tx(&ms->full[s], 8192);   // the box's global bytes: the gaps are neither written nor counted
     tma_load_2d(aA + s * 16384, &tm_k, 0, (int)(vrow0 + (int64_t)u * (kDmEntries / 2)), &ms->full[s]);
   };
   bool ok = true;
