@@ -512,10 +512,10 @@ def run_config(args, name):
         l2 = "caches resident; each step reads them once (larger than L2 except the HCA-only step)"
         step_desc = "decode_append + indexer_topk + sparse_mqa (CSA) / decode_append + hca_dense_attn (HCA), " \
                     "one CUDA graph per step"
-        # kernels per step: CSA layer 8 (append; scores, top-k stages 1 and 2;
-        # row prep, row gather, attention, split merge), HCA layer 5 (append;
-        # row prep, row gather, attention, split merge)
-        launches = sum(8 if c.k else 5 for c in layers)
+        # kernels per step: CSA layer 5 (append; scores with the score
+        # histogram, histogram top-k; row gather, attention with the split
+        # merge), HCA layer 3 (append; row gather, attention)
+        launches = sum(5 if c.k else 3 for c in layers)
     elif name == "c2_csa_prefill_128k":
         cfg = wl.CONFIGS[name]
         T, W, m, Tc = cfg.T, cfg.W, cfg.m, 8192

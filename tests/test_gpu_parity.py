@@ -550,6 +550,51 @@ def test_indexer_decode_tc_matches_dp4a(csa, monkeypatch, B, N, HI, key_exps, q_
     np.testing.assert_array_equal(sc_tc.cpu().numpy().view(np.uint32), sc_dp.cpu().numpy().view(np.uint32))
 
 
+def _pattern_with_positive_score(oracle_mod, rng, qbits, w):
+    """32 random code bytes whose score at block scales 2^0 is positive."""
+    q = wl.bf16_bits_to_f32(qbits)
+    for _ in range(64):
+        pat = rng.integers(0, 256, size=32, dtype=np.uint8)
+        _, sc = oracle_mod.indexer_topk(q, w, (pat[None, None], np.full((1, 1, 2), 127, np.uint8)),
+                                        np.zeros((1, 1), np.int64), 1, 1, 1)
+        if sc[0, 0, 0] > 0:
+            return pat
+    raise AssertionError("no pattern with a positive score")
+
+
+@pytest.mark.parametrize("N", [20000, 20001])   # even N: TMA-fed scorer; odd: copy-fed
+def test_indexer_decode_topk_equal_scores(csa, oracle_mod, N):
+    """Decode rows (histogram top-k) whose scores repeat exactly, against the
+    oracle bit for bit (equal scores by ascending index):
+    row 0: 50 distinct entries repeated at random -- the sure and tie keys
+    sorted together; row 1: one entry everywhere -- the threshold bin holds
+    more than the tie list, selection over the whole row; row 2: 500 entries
+    4x above 6000 equal ones above the rest -- too many sure and tie keys
+    to sort at once, the ties selected first; row 3: fewer visible entries
+    than k -- every one taken."""
+    rng = np.random.default_rng(31337 + N)
+    B, HI, k = 4, 16, 1024
+    qI = rng.standard_normal((1, 1, HI, 64)).astype(np.float32)
+    qbits = np.repeat(wl.f32_to_bf16_bits(qI), B, axis=0)
+    w = np.repeat(rng.uniform(0.1, 1.0, (1, 1, HI)).astype(np.float32), B, axis=0)
+    pat = _pattern_with_positive_score(oracle_mod, rng, qbits[:1], w[:1])
+    codes = np.empty((B, N, 32), np.uint8)
+    scales = np.empty((B, N, 2), np.uint8)
+    pats, pscl = rng.integers(0, 256, size=(50, 32), dtype=np.uint8), rng.integers(124, 131, size=(50, 2))
+    pick = rng.integers(0, 50, size=N)
+    codes[0], scales[0] = pats[pick], pscl[pick]
+    codes[1], scales[1] = pat, 127
+    grp = rng.permutation(np.concatenate([np.full(500, 129), np.full(6000, 127), np.full(N - 6500, 124)]))
+    codes[2], scales[2] = pat, grp[:, None]
+    codes[3], scales[3] = _mxfp4_keys_random(rng, N, list(range(120, 135)))
+    q_pos = np.array([[N - 1], [N - 1], [N - 1], [700]], np.int64)
+    idx, sc = csa.indexer_topk(dev_bf16(qbits), dev(w), dev(codes), dev(scales), dev(q_pos), N, 1, k)
+    oidx, osc = oracle_mod.indexer_topk(wl.bf16_bits_to_f32(qbits), w, (codes, scales), q_pos, N, 1, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), osc.view(np.uint32))
+    assert len(set(osc[1, 0].tolist())) == 1 and list(oidx[1, 0]) == list(range(k))
+
+
 # --------------------------------------------------------------------------
 # per-channel compression logits: bit-exact bytes against the oracle
 # --------------------------------------------------------------------------
