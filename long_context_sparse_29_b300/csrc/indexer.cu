@@ -831,18 +831,40 @@ topk_stage2_kernel(const int64_t* __restrict__ q_pos, int64_t N, int m, int k, i
 // in a bin above b* is among the top k ("sure": fewer than k of them) and
 // the rest of the top k are the best of bin b* ("ties").  Chunk CTAs append
 // the row's sure and tie candidates, as 64-bit composite keys, to workspace
-// lists (one reservation per list and CTA); the last chunk CTA of the row
-// to finish sorts the sure and tie keys together (score descending, index
-// ascending) and writes the first k.  When they do not fit its shared
-// memory it selects the needed ties first (radix threshold on the order
-// key, equal keys by ascending index); when bin b* holds more than kTieCap
-// candidates it selects over the row's whole score array (same result).
+// lists (warp-aggregated); the last chunk CTA of the row to finish selects
+// the needed ties exactly (radix threshold on the order key, equal keys by
+// ascending index), sorts the k winners (score descending, index ascending)
+// and writes them.  When bin b* holds more than kTieCap candidates the last
+// CTA selects over the row's whole score array instead (same result).
 // ---------------------------------------------------------------------------
 constexpr int kHistBits = 11;
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kTieCap = 8192;
 constexpr int kSelThreads = 1024;
 constexpr int kSelChunk = 8192;       // scores scanned per chunk CTA (8 per thread)
+
+// Sorts a[0..P) descending by a bitonic network in shared memory (P a power
+// of two; slots past `count` are padded with 0, below every real key).
+template <int NT>
+__device__ void bitonic_desc(unsigned long long* a, int count, int P) {
+  for (int i = threadIdx.x; i < P; i += NT)
+    if (i >= count) a[i] = 0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += NT) {
+        const int lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const unsigned long long x = a[lo], y = a[hi];
+        if ((x < y) == desc) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
 
 // Candidate stream over staged composite keys whose order key equals `thr`:
 // their low words (the complement of the index) as the key, so the largest
@@ -963,23 +985,6 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
   const int ntie = *reinterpret_cast<volatile int*>(rc + 1);
   unsigned long long* keys_s = dyn_s;          // 2 P
   unsigned long long* tie_s = dyn_s + 2 * P;   // kTieCap
-  // sure and tie keys together few enough to sort in the shared space: the
-  // first kk of them in composite order (score descending, index ascending)
-  // are the top kk, with no selection among the ties
-  int P2 = P;
-  while (P2 < nsure + ntie) P2 <<= 1;
-  if (kk > 0 && bstar >= 0 && ntie <= kTieCap && 2 * P2 <= 2 * P + kTieCap) {
-    for (int i = tid; i < nsure; i += NT) keys_s[i] = __ldcg(sure + i);
-    for (int i = tid; i < ntie; i += NT) keys_s[nsure + i] = __ldcg(tie + i);
-    __syncthreads();
-    emit_topk<NT>(merge_sort_desc<NT>(keys_s, nsure + ntie, P2), kk, k, row, idx_out, score_out);
-    if (tid == 0) {
-      rc[0] = 0;
-      rc[1] = 0;
-      rc[2] = 0;
-    }
-    return;
-  }
   if (kk > 0) {
     if (bstar >= 0 && ntie > kTieCap) {
       // bin b* too full for the tie list: select over the whole row
@@ -1011,7 +1016,8 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
       __syncthreads();
     }
   }
-  emit_topk<NT>(merge_sort_desc<NT>(keys_s, kk, P), kk, k, row, idx_out, score_out);
+  bitonic_desc<NT>(keys_s, kk, P);
+  emit_topk<NT>(keys_s, kk, k, row, idx_out, score_out);
   if (tid == 0) {   // the workspace counters for the next call
     rc[0] = 0;
     rc[1] = 0;

@@ -470,13 +470,6 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
-// adds 1 to bin `bin` of a shared histogram for every lane of the warp
-// (0xffffffff: nothing); every lane of the warp takes part
-__device__ __forceinline__ void hist_add_warp(unsigned int* h, uint32_t bin, int lane) {
-  const unsigned int same = __match_any_sync(0xffffffffu, bin);
-  if (bin != 0xffffffffu && lane == __ffs(same) - 1) atomicAdd(h + bin, (unsigned int)__popc(same));
-}
-
 // arrive on `bar` once this thread's copies so far have landed (counted arrival)
 __device__ __forceinline__ void cp_async_arrive(void* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -610,7 +603,6 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
   auto combine = [&](int u) {
     const int tb = u % kDtTbufs;
     if (ok && !mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDtTbufs) & 1, kIxWait)) ok = false;
-    ok = __all_sync(0xffffffffu, ok);   // warp-uniform: the histogram adds take every lane
     fence_after_sync();
     uint32_t P[32];
     tmem_ld32(tmem + lane_base + 32u * tb, P);
@@ -648,13 +640,14 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
       }
     }
     const int64_t j = c0 + (int64_t)u * kDtThreads + tid;
-    const bool valid = ok && j < c1;
-    if (valid) scores[row * N + j] = s;
-    if (hist) {   // the bin of its order key (top bits; -0 ranks as +0), one add per bin and warp
-      uint32_t key = __float_as_uint(s);
-      if (key == 0x80000000u) key = 0u;
-      key = (key & 0x80000000u) ? ~key : (key | 0x80000000u);
-      hist_add_warp(hist_s, valid ? key >> (32 - kDtHistBits) : 0xffffffffu, lane);
+    if (ok && j < c1) {
+      scores[row * N + j] = s;
+      if (hist) {   // the bin of its order key (top bits; -0 ranks as +0)
+        uint32_t key = __float_as_uint(s);
+        if (key == 0x80000000u) key = 0u;
+        key = (key & 0x80000000u) ? ~key : (key | 0x80000000u);
+        atomicAdd(hist_s + (key >> (32 - kDtHistBits)), 1u);
+      }
     }
   };
 
@@ -664,7 +657,6 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
     if (ul < ntiles) {
       if (ul >= kDtSlots && !mbar_wait(&ms->empty[ul % kDtSlots], (uint32_t)(ul / kDtSlots - 1) & 1, kIxWait))
         ok = false;
-      ok = __all_sync(0xffffffffu, ok);
       if (ok) load_tile(ul);
     }
     // warp 0: the two block MMAs of tile u into TMEM buffer u % kDtTbufs
@@ -672,7 +664,6 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
       const int s = u % kDtSlots, tb = u % kDtTbufs;
       bool got = mbar_wait(&ms->full[s], (uint32_t)(u / kDtSlots) & 1, kIxWait);
       if (got && u >= kDtTbufs) got = mbar_wait(&ms->tempty[tb], (uint32_t)(u / kDtTbufs - 1) & 1, kIxWait);
-      got = __all_sync(0xffffffffu, got);
       if (got) {
         fence_after_sync();
         fence_proxy_async();   // the operand rows came through the generic proxy (cp.async)
@@ -906,7 +897,6 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   auto combine = [&](int u) {
     const int tb = u % kDmTbufs;
     if (ok && !mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDmTbufs) & 1, kIxWait)) ok = false;
-    ok = __all_sync(0xffffffffu, ok);   // warp-uniform: the histogram adds take every lane
     fence_after_sync();
     uint32_t P0[32], P1[32];
     tmem_ld32(tmem + lane_base + 64u * tb, P0);
@@ -920,14 +910,18 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
     if (jl + 1 < c1 - c0) sc2 = *reinterpret_cast<const uint32_t*>(sm + kDmSOff + 2 * jl);
     else if (jl < c1 - c0) sc2 = 0x7f7f0000u | reinterpret_cast<const uint16_t*>(sm + kDmSOff)[jl];
     const float s0 = score_of(P0, sc2 & 0xffffu), s1 = score_of(P1, sc2 >> 16);
-    const bool v0 = ok && jl < c1 - c0, v1 = ok && jl + 1 < c1 - c0;
-    if (v1) *reinterpret_cast<float2*>(scores + row * N + c0 + jl) = make_float2(s0, s1);
-    else if (v0) scores[row * N + c0 + jl] = s0;
-    if (hist) {
-      // one shared add per distinct bin and warp: the scores of a tile fall in
-      // few bins, and same-address adds within a warp are serialised
-      hist_add_warp(hist_s, v0 ? to_key_bin(s0) : 0xffffffffu, lane);
-      hist_add_warp(hist_s, v1 ? to_key_bin(s1) : 0xffffffffu, lane);
+    if (ok) {
+      const int64_t j = c0 + jl;
+      if (jl + 1 < c1 - c0) {
+        *reinterpret_cast<float2*>(scores + row * N + j) = make_float2(s0, s1);
+        if (hist) {
+          atomicAdd(hist_s + to_key_bin(s0), 1u);
+          atomicAdd(hist_s + to_key_bin(s1), 1u);
+        }
+      } else if (jl < c1 - c0) {
+        scores[row * N + j] = s0;
+        if (hist) atomicAdd(hist_s + to_key_bin(s0), 1u);
+      }
     }
   };
 
@@ -948,7 +942,6 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       const int s = u % kDmStages, tb = u % kDmTbufs;
       if (got) got = mbar_wait(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxWait);
       if (got && u >= kDmTbufs) got = mbar_wait(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxWait);
-      got = __all_sync(0xffffffffu, got);
       if (got) {
         fence_after_sync();
         const uint64_t ad = sdesc_sw128(aA + s * 16384, 16, 1024), bd = sdesc_sw128(aB, 16, 1024);
