@@ -528,7 +528,7 @@ template <int NT>
 struct TkShared {
   unsigned int hist[256];
   unsigned int cnt_gt[NT / 32], cnt_eq[NT / 32];
-  unsigned int prefix, remaining;
+  unsigned int prefix, remaining, equal;
 };
 
 // Candidate streams: get(i, key, idx) for i in [0, n), false when slot i holds
@@ -581,16 +581,18 @@ __device__ __forceinline__ void stage_to_smem(void* dst, const void* src, int64_
 
 // The kk-th largest key of the stream (kk >= 1 and at most the number of
 // candidates): returns its value; sh.remaining = how many keys equal to it
-// are taken.
+// are taken, sh.equal = how many there are.  Keys known to share their top
+// 8 (32 - first_shift) bits `top` start the search at first_shift.
 template <int NT, class Src>
-__device__ uint32_t radix_threshold(const Src& src, int64_t n, int kk, TkShared<NT>& sh) {
+__device__ uint32_t radix_threshold(const Src& src, int64_t n, int kk, TkShared<NT>& sh, int first_shift = 24,
+                                   uint32_t top = 0) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    sh.prefix = 0;
+    sh.prefix = top;
     sh.remaining = (unsigned)kk;
   }
-  uint32_t mask = 0;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  uint32_t mask = first_shift == 24 ? 0u : ~0u << (first_shift + 8);
+  for (int shift = first_shift; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += NT) sh.hist[i] = 0;
     __syncthreads();
     const uint32_t prefix = sh.prefix;
@@ -619,17 +621,19 @@ __device__ uint32_t radix_threshold(const Src& src, int64_t n, int kk, TkShared<
       const bool here = excl < rem && incl >= rem;
       const unsigned int who = __ballot_sync(0xffffffffu, here);
       if (lane == __ffs(who) - 1) {
-        unsigned int acc = excl;
+        unsigned int acc = excl, eqc = 0;
         int d = 255 - 8 * lane;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (acc + c[i] >= rem) {
             d = 255 - 8 * lane - i;
+            eqc = c[i];
             break;
           }
           acc += c[i];
         }
         sh.remaining = rem - acc;
+        sh.equal = eqc;
         sh.prefix = prefix | ((uint32_t)d << shift);
       }
     }
@@ -843,29 +847,6 @@ constexpr int kTieCap = 8192;
 constexpr int kSelThreads = 1024;
 constexpr int kSelChunk = 8192;       // scores scanned per chunk CTA (8 per thread)
 
-// Sorts a[0..P) descending by a bitonic network in shared memory (P a power
-// of two; slots past `count` are padded with 0, below every real key).
-template <int NT>
-__device__ void bitonic_desc(unsigned long long* a, int count, int P) {
-  for (int i = threadIdx.x; i < P; i += NT)
-    if (i >= count) a[i] = 0ull;
-  __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < P / 2; i += NT) {
-        const int lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const unsigned long long x = a[lo], y = a[hi];
-        if ((x < y) == desc) {
-          a[lo] = y;
-          a[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
 // Candidate stream over staged composite keys whose order key equals `thr`:
 // their low words (the complement of the index) as the key, so the largest
 // of them are the lowest indices.
@@ -998,26 +979,28 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
         for (int i = tid; i < ntie; i += NT) tie_s[i] = __ldcg(tie + i);
         if (tid == 0) take_s = nsure;
         __syncthreads();
-        const uint32_t thr = radix_threshold<NT>(CandList{tie_s}, ntie, need, sh);
-        const unsigned int rem = sh.remaining;   // keys equal to thr to take, lowest indices first
-        // among the keys equal to thr, the rem lowest indices: a second
-        // threshold on their index words
+        // every tie shares the top kHistBits bits (bin b*): the search starts
+        // below the top byte
+        const uint32_t thr = radix_threshold<NT>(CandList{tie_s}, ntie, need, sh, 16,
+                                                 (uint32_t)(bstar >> (kHistBits - 8)) << 24);
+        // keys equal to thr to take, lowest indices first; when all of them
+        // are taken no index threshold is needed
+        const unsigned int rem = sh.remaining, neq = sh.equal;
         uint32_t ithr = 0;
-        if (rem > 0) {
+        if (rem < neq) {
           __syncthreads();
           ithr = radix_threshold<NT>(EqualKeyList{tie_s, thr}, ntie, (int)rem, sh);
         }
         for (int i = tid; i < ntie; i += NT) {
           const unsigned long long v = tie_s[i];
           const uint32_t key = (uint32_t)(v >> 32), low = (uint32_t)(v & 0xffffffffull);
-          if (key > thr || (rem > 0 && key == thr && low >= ithr)) keys_s[atomicAdd(&take_s, 1u)] = v;
+          if (key > thr || (key == thr && low >= ithr)) keys_s[atomicAdd(&take_s, 1u)] = v;
         }
       }
       __syncthreads();
     }
   }
-  bitonic_desc<NT>(keys_s, kk, P);
-  emit_topk<NT>(keys_s, kk, k, row, idx_out, score_out);
+  emit_topk<NT>(merge_sort_desc<NT>(keys_s, kk, P), kk, k, row, idx_out, score_out);
   if (tid == 0) {   // the workspace counters for the next call
     rc[0] = 0;
     rc[1] = 0;

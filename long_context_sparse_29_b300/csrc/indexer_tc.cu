@@ -725,9 +725,9 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
 namespace {
 
 constexpr int kDmEntries = 256;             // entries per tile
+constexpr int kDmThreads = 160;             // warps 0-3 epilogue (thread = TMEM lane), warp 4 TMA + MMA
 constexpr int kDmStages = 4;                // 16 KiB TMA boxes
 constexpr int kDmTbufs = 4;                 // TMEM buffers of 64 columns
-constexpr int kDmLag = 2;                   // tiles between a tile's MMAs and its epilogue
 constexpr int kDmMaxChunk = 4096;           // entries per CTA at most (their scale bytes are staged)
 constexpr uint32_t kDmBOff = 0;             // query operand, 16 rows x 128 B
 constexpr uint32_t kDmAOff = 2048;          // kDmStages x [128 rows x 128 B]
@@ -737,16 +737,19 @@ constexpr uint32_t kDmMiscOff = kDmHOff + (1u << kDtHistBits) * 4;
 constexpr uint32_t kDmSmem = kDmMiscOff + 512 + 1024;
 
 struct DmMisc {
-  uint64_t full[kDmStages], empty[kDmStages], tfull[kDmTbufs], tempty[kDmTbufs];
+  uint64_t full[kDmStages], empty[kDmStages], tfull[kDmTbufs], tempty[kDmTbufs], qready;
   uint32_t tmem;
   int qlo0, qhi0, qlo1, qhi1;
   int4 hx[kDtHeads];
 };
 static_assert(sizeof(DmMisc) <= 512, "DmMisc overflows its smem slot");
 
+// the 128 epilogue threads only
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 }  // namespace
 
-__global__ void __launch_bounds__(kDtThreads, 2)
+__global__ void __launch_bounds__(kDmThreads, 2)
 scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
                              const uint8_t* __restrict__ ks, const int64_t* __restrict__ q_pos, int64_t Tq,
                              int HI, int64_t N, int m, int64_t chunk, float* __restrict__ scores,
@@ -766,11 +769,11 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   const int64_t vrow0 = (b * N + c0) / 2;   // first row of the two-entry view
 
   // the query operand and the key stages zeroed: TMA leaves the gaps of the padded form untouched
-  for (int i = tid; i < (int)(kDmSOff / 16); i += kDtThreads) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < (int)(kDmSOff / 16); i += kDmThreads) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async();
   unsigned int* hist_s = reinterpret_cast<unsigned int*>(sm + kDmHOff);
   if (hist)
-    for (int i = tid; i < (1 << kDtHistBits); i += kDtThreads) hist_s[i] = 0u;
+    for (int i = tid; i < (1 << kDtHistBits); i += kDmThreads) hist_s[i] = 0u;
   if (tid == 0) {
     for (int s = 0; s < kDmStages; ++s) {
       mbar_init(&ms->full[s], 1);
@@ -780,6 +783,7 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       mbar_init(&ms->tfull[i], 1);
       mbar_init(&ms->tempty[i], 4);
     }
+    mbar_init(&ms->qready, 128);
     mbar_fence_init();
     ms->qlo0 = ms->qlo1 = 1 << 30;
     ms->qhi0 = ms->qhi1 = -(1 << 30);
@@ -789,92 +793,123 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = ms->tmem;
-  const uint32_t aA = smem_u32(sm + kDmAOff), aB = smem_u32(sm + kDmBOff);
-  // tile u: one box of 128 view rows into stage u % kDmStages (thread 0)
-  auto load_tile = [&](int u) {
-    const int s = u % kDmStages;
-    mbar_arrive_expect_tx(&ms->full[s], 8192);   // the box's global bytes: the gaps are neither written nor counted
-    tma_load_2d(aA + s * 16384, &tm_k, 0, (int)(vrow0 + (int64_t)u * (kDmEntries / 2)), &ms->full[s]);
-  };
   bool ok = true;
-  if (tid == 0)
-    for (int u = 0; u < kDmStages && u < ntiles; ++u) load_tile(u);
-  // the chunk's scale bytes, staged once: every load of the thread in flight together
-  {
+
+  if (warp == 4) {
+    // ---- TMA and MMA issue: tile u = one box of 128 view rows into stage u % kDmStages ----
+    const uint32_t aA = smem_u32(sm + kDmAOff), aB = smem_u32(sm + kDmBOff);
+    auto load_tile = [&](int u) {
+      const int s = u % kDmStages;
+      mbar_arrive_expect_tx(&ms->full[s], 8192);   // the box's global bytes: the gaps are neither written nor counted
+      tma_load_2d(aA + s * 16384, &tm_k, 0, (int)(vrow0 + (int64_t)u * (kDmEntries / 2)), &ms->full[s]);
+    };
+    if (lane == 0)
+      for (int u = 0; u < kDmStages && u < ntiles; ++u) load_tile(u);
+    int loaded = min(ntiles, kDmStages), issued = 0;
+    bool got = __all_sync(0xffffffffu, mbar_wait(&ms->qready, 0, kIxWait));
+    constexpr uint32_t id = idesc_e2m1(kDtThreads, kDtHeads);
+    for (int u = 0; u < ntiles && got; ++u) {
+      const int s = u % kDmStages, tb = u % kDmTbufs;
+      got = mbar_wait(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxWait);
+      if (got && u >= kDmTbufs) got = mbar_wait(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxWait);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) break;
+      fence_after_sync();
+      const uint64_t ad = sdesc_sw128(aA + s * 16384, 16, 1024), bd = sdesc_sw128(aB, 16, 1024);
+      const uint32_t d = tmem + 64u * tb;
+#pragma unroll
+      for (int par = 0; par < 2; ++par) {
+        mma_f8f6f4_elect(d + 32u * par, ad + (uint64_t)(4 * par), bd, id);
+        mma_f8f6f4_elect(d + 32u * par + 16u, ad + (uint64_t)(4 * par + 2), bd + 2, id);
+      }
+      mma_commit_elect(&ms->tfull[tb]);
+      mma_commit_elect(&ms->empty[s]);
+      ++issued;
+      __syncwarp();
+      // the stage of tile u - 1 takes tile u - 1 + kDmStages once tile u - 1's MMAs are done
+      if (u >= 1 && u - 1 + kDmStages < ntiles) {
+        const int sp = (u - 1) % kDmStages;
+        bool fine = true;
+        if (lane == 0) {
+          if (mbar_wait(&ms->empty[sp], (uint32_t)((u - 1) / kDmStages) & 1, kIxWait)) load_tile(u - 1 + kDmStages);
+          else fine = false;
+        }
+        got = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
+        if (got) loaded = u - 1 + kDmStages + 1;
+      }
+    }
+    if (!got) {
+      ok = false;
+      if (lane == 0) flag_timeout(ws);
+    }
+    // the MMAs issued complete and the boxes issued land before TMEM and shared memory go
+    if (issued > 0) mbar_wait(&ms->tfull[(issued - 1) % kDmTbufs], (uint32_t)((issued - 1) / kDmTbufs) & 1, kIxWait);
+    if (lane == 0)
+      for (int u = issued; u < loaded; ++u) mbar_wait(&ms->full[u % kDmStages], (uint32_t)(u / kDmStages) & 1, kIxWait);
+  } else {
+    // ---- warps 0-3: the chunk's scale bytes (loads in flight while the query is quantised) ----
     uint16_t* sc_s = reinterpret_cast<uint16_t*>(sm + kDmSOff);
     const uint16_t* ks16 = reinterpret_cast<const uint16_t*>(ks) + b * N + c0;
     const int n = (int)(c1 - c0);
-    uint16_t v[kDmMaxChunk / kDtThreads];
+    uint16_t v[kDmMaxChunk / 128];
 #pragma unroll
-    for (int r = 0; r < kDmMaxChunk / kDtThreads; ++r) {
-      const int i = tid + r * kDtThreads;
+    for (int r = 0; r < kDmMaxChunk / 128; ++r) {
+      const int i = tid + r * 128;
       v[r] = i < n ? __ldg(ks16 + i) : (uint16_t)0;
     }
+    // ---- the query: MXFP4 codes into the B operand, block exponents ----
+    for (int blkid = tid >> 3; blkid < 2 * kDtHeads; blkid += 128 / 8) {
+      const int u = tid & 7, h = blkid >> 1, blk = blkid & 1;
+      const bool act = h < HI;
+      float qv[4];
+      float amax = 0.0f;
 #pragma unroll
-    for (int r = 0; r < kDmMaxChunk / kDtThreads; ++r) {
-      const int i = tid + r * kDtThreads;
+      for (int i = 0; i < 4; ++i) {
+        qv[i] = act ? __bfloat162float(qI[(row * HI + h) * 64 + 32 * blk + 4 * u + i]) : 0.0f;
+        amax = fmaxf(amax, fabsf(qv[i]));
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const int sx = mx_block_exp(amax);
+      const float inv = pow2i(-sx);
+      if (act) {
+        uint32_t cd = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cd |= e2m1_encode(__fmul_rn(qv[i], inv)) << (4 * i);
+        *reinterpret_cast<uint16_t*>(sm + kDmBOff + sw128_off(h, 2 * blk + (u >> 2)) + 2 * (u & 3)) = (uint16_t)cd;
+        if (u == 0) {
+          if (blk == 0) {
+            atomicMin(&ms->qlo0, sx);
+            atomicMax(&ms->qhi0, sx);
+            ms->hx[h].x = sx << 23;
+            ms->hx[h].z = __float_as_int(w[row * HI + h]);
+          } else {
+            atomicMin(&ms->qlo1, sx);
+            atomicMax(&ms->qhi1, sx);
+            ms->hx[h].y = sx << 23;
+          }
+        }
+      }
+    }
+    fence_proxy_async();
+    mbar_arrive(&ms->qready);
+#pragma unroll
+    for (int r = 0; r < kDmMaxChunk / 128; ++r) {
+      const int i = tid + r * 128;
       if (i < n) sc_s[i] = v[r];
     }
-  }
-  // ---- the query: MXFP4 codes into the B operand, block exponents ----
-  for (int blkid = tid >> 3; blkid < 2 * kDtHeads; blkid += kDtThreads / 8) {
-    const int u = tid & 7, h = blkid >> 1, blk = blkid & 1;
-    const bool act = h < HI;
-    float v[4];
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[i] = act ? __bfloat162float(qI[(row * HI + h) * 64 + 32 * blk + 4 * u + i]) : 0.0f;
-      amax = fmaxf(amax, fabsf(v[i]));
-    }
-#pragma unroll
-    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const int sx = mx_block_exp(amax);
-    const float inv = pow2i(-sx);
-    if (act) {
-      uint32_t cd = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) cd |= e2m1_encode(__fmul_rn(v[i], inv)) << (4 * i);
-      *reinterpret_cast<uint16_t*>(sm + kDmBOff + sw128_off(h, 2 * blk + (u >> 2)) + 2 * (u & 3)) = (uint16_t)cd;
-      if (u == 0) {
-        if (blk == 0) {
-          atomicMin(&ms->qlo0, sx);
-          atomicMax(&ms->qhi0, sx);
-          ms->hx[h].x = sx << 23;
-          ms->hx[h].z = __float_as_int(w[row * HI + h]);
-        } else {
-          atomicMin(&ms->qlo1, sx);
-          atomicMax(&ms->qhi1, sx);
-          ms->hx[h].y = sx << 23;
-        }
-      }
-    }
-  }
-  fence_proxy_async();
-  fence_before_sync();
-  __syncthreads();
-  const int qlo0 = ms->qlo0, qhi0 = ms->qhi0, qlo1 = ms->qlo1, qhi1 = ms->qhi1;
-  constexpr uint32_t id = idesc_e2m1(kDtThreads, kDtHeads);
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-  int issued = 0;
+    epi_sync();
+    const int qlo0 = ms->qlo0, qhi0 = ms->qhi0, qlo1 = ms->qlo1, qhi1 = ms->qhi1;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
 
-  // one entry's score from its 32 block dots (P[0..15] block 0, P[16..31] block 1)
-  auto score_of = [&](const uint32_t* P, uint32_t sc) -> float {
-    const int x0 = (int)(sc & 0xffu), x1 = (int)((sc >> 8) & 0xffu);
-    const int X0 = x0 << 23, X1 = x1 << 23;
-    const bool fast = qlo0 + x0 >= 27 && qhi0 + x0 <= 227 && qlo1 + x1 >= 27 && qhi1 + x1 <= 227;
-    float s = 0.0f;
-    if (fast) {
-#pragma unroll
-      for (int h = 0; h < kDtHeads; ++h) {
-        if (h < HI) {
-          const int4 hx = ms->hx[h];
-          const float d = __fmaf_rn(__uint_as_float(P[h]), __int_as_float(hx.x + X0),
-                                    __fmul_rn(__uint_as_float(P[16 + h]), __int_as_float(hx.y + X1)));
-          s = __fmaf_rn(__int_as_float(hx.z), fmaxf(d, 0.0f), s);
-        }
-      }
-    } else {
+    // one entry's score from its 32 block dots (P[0..15] block 0, P[16..31] block 1)
+    auto fast_of = [&](uint32_t sc) -> bool {
+      const int x0 = (int)(sc & 0xffu), x1 = (int)((sc >> 8) & 0xffu);
+      return qlo0 + x0 >= 27 && qhi0 + x0 <= 227 && qlo1 + x1 >= 27 && qhi1 + x1 <= 227;
+    };
+    auto score_slow = [&](const uint32_t* P, uint32_t sc) -> float {
+      const int x0 = (int)(sc & 0xffu), x1 = (int)((sc >> 8) & 0xffu);
+      float s = 0.0f;
 #pragma unroll
       for (int h = 0; h < kDtHeads; ++h) {
         if (h < HI) {
@@ -884,33 +919,54 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
           s = __fmaf_rn(__int_as_float(hx.z), d > 0.0f ? d : 0.0f, s);
         }
       }
-    }
-    return s;
-  };
-  auto to_key_bin = [&](float s) -> uint32_t {
-    uint32_t key = __float_as_uint(s);
-    if (key == 0x80000000u) key = 0u;
-    key = (key & 0x80000000u) ? ~key : (key | 0x80000000u);
-    return key >> (32 - kDtHistBits);
-  };
-  // the epilogue of tile u: thread r = view row r = entries 2r and 2r + 1
-  auto combine = [&](int u) {
-    const int tb = u % kDmTbufs;
-    if (ok && !mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDmTbufs) & 1, kIxWait)) ok = false;
-    fence_after_sync();
-    uint32_t P0[32], P1[32];
-    tmem_ld32(tmem + lane_base + 64u * tb, P0);
-    tmem_ld32(tmem + lane_base + 64u * tb + 32u, P1);
-    tmem_wait_ld();
-    fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ms->tempty[tb]);
-    const int64_t jl = (int64_t)u * kDmEntries + 2 * tid;   // chunk-relative index of entry 2r
-    uint32_t sc2 = 0x7f7f7f7fu;
-    if (jl + 1 < c1 - c0) sc2 = *reinterpret_cast<const uint32_t*>(sm + kDmSOff + 2 * jl);
-    else if (jl < c1 - c0) sc2 = 0x7f7f0000u | reinterpret_cast<const uint16_t*>(sm + kDmSOff)[jl];
-    const float s0 = score_of(P0, sc2 & 0xffffu), s1 = score_of(P1, sc2 >> 16);
-    if (ok) {
+      return s;
+    };
+    auto to_key_bin = [&](float s) -> uint32_t {
+      uint32_t key = __float_as_uint(s);
+      if (key == 0x80000000u) key = 0u;
+      key = (key & 0x80000000u) ? ~key : (key | 0x80000000u);
+      return key >> (32 - kDtHistBits);
+    };
+    // ---- the epilogue of every tile: thread r = view row r = entries 2r and 2r + 1 ----
+    for (int u = 0; u < ntiles && ok; ++u) {
+      const int tb = u % kDmTbufs;
+      ok = __all_sync(0xffffffffu, mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDmTbufs) & 1, kIxWait));
+      if (!ok) break;
+      fence_after_sync();
+      uint32_t P0[32], P1[32];
+      tmem_ld32(tmem + lane_base + 64u * tb, P0);
+      tmem_ld32(tmem + lane_base + 64u * tb + 32u, P1);
+      tmem_wait_ld();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms->tempty[tb]);
+      const int64_t jl = (int64_t)u * kDmEntries + 2 * tid;   // chunk-relative index of entry 2r
+      uint32_t sc2 = 0x7f7f7f7fu;
+      if (jl + 1 < c1 - c0) sc2 = *reinterpret_cast<const uint32_t*>(sm + kDmSOff + 2 * jl);
+      else if (jl < c1 - c0) sc2 = 0x7f7f0000u | reinterpret_cast<const uint16_t*>(sm + kDmSOff)[jl];
+      const uint32_t sa = sc2 & 0xffffu, sb = sc2 >> 16;
+      float s0 = 0.0f, s1 = 0.0f;
+      if (fast_of(sa) && fast_of(sb)) {
+        // both entries in one pass over the heads: the head's factors read once,
+        // two independent chains (each entry's arithmetic as in every other indexer kernel)
+        const int X00 = (int)(sa & 0xffu) << 23, X01 = (int)((sa >> 8) & 0xffu) << 23;
+        const int X10 = (int)(sb & 0xffu) << 23, X11 = (int)((sb >> 8) & 0xffu) << 23;
+#pragma unroll
+        for (int h = 0; h < kDtHeads; ++h) {
+          if (h < HI) {
+            const int4 hx = ms->hx[h];
+            const float d0 = __fmaf_rn(__uint_as_float(P0[h]), __int_as_float(hx.x + X00),
+                                       __fmul_rn(__uint_as_float(P0[16 + h]), __int_as_float(hx.y + X01)));
+            const float d1 = __fmaf_rn(__uint_as_float(P1[h]), __int_as_float(hx.x + X10),
+                                       __fmul_rn(__uint_as_float(P1[16 + h]), __int_as_float(hx.y + X11)));
+            s0 = __fmaf_rn(__int_as_float(hx.z), fmaxf(d0, 0.0f), s0);
+            s1 = __fmaf_rn(__int_as_float(hx.z), fmaxf(d1, 0.0f), s1);
+          }
+        }
+      } else {
+        s0 = score_slow(P0, sa);
+        s1 = score_slow(P1, sb);
+      }
       const int64_t j = c0 + jl;
       if (jl + 1 < c1 - c0) {
         *reinterpret_cast<float2*>(scores + row * N + j) = make_float2(s0, s1);
@@ -923,60 +979,14 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
         if (hist) atomicAdd(hist_s + to_key_bin(s0), 1u);
       }
     }
-  };
-
-  int loaded = min(ntiles, kDmStages);   // tiles whose boxes were issued
-  for (int u = 0; u < ntiles && ok; ++u) {
-    if (warp == 0) {
-      bool got = true;
-      // the stage of tile u - 1 takes tile u - 1 + kDmStages once tile u - 1's MMAs are done
-      if (u >= 1 && u - 1 + kDmStages < ntiles) {
-        const int sp = (u - 1) % kDmStages;
-        if (lane == 0) {
-          if (mbar_wait(&ms->empty[sp], (uint32_t)((u - 1) / kDmStages) & 1, kIxWait)) load_tile(u - 1 + kDmStages);
-          else got = false;
-        }
-        got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-        if (got) loaded = u - 1 + kDmStages + 1;
-      }
-      const int s = u % kDmStages, tb = u % kDmTbufs;
-      if (got) got = mbar_wait(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxWait);
-      if (got && u >= kDmTbufs) got = mbar_wait(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxWait);
-      if (got) {
-        fence_after_sync();
-        const uint64_t ad = sdesc_sw128(aA + s * 16384, 16, 1024), bd = sdesc_sw128(aB, 16, 1024);
-        const uint32_t d = tmem + 64u * tb;
-#pragma unroll
-        for (int par = 0; par < 2; ++par) {
-          mma_f8f6f4_elect(d + 32u * par, ad + (uint64_t)(4 * par), bd, id);
-          mma_f8f6f4_elect(d + 32u * par + 16u, ad + (uint64_t)(4 * par + 2), bd + 2, id);
-        }
-        mma_commit_elect(&ms->tfull[tb]);
-        mma_commit_elect(&ms->empty[s]);
-        ++issued;
-      }
-      if (!got) ok = false;
-      __syncwarp();
-    }
-    if (u >= kDmLag) combine(u - kDmLag);
+    if (!ok && lane == 0) flag_timeout(ws);
   }
-  for (int u = max(0, ntiles - kDmLag); u < ntiles && ok; ++u) combine(u);
-  if (!ok && lane == 0) flag_timeout(ws);
+  __syncthreads();
   if (hist) {
-    __syncthreads();
-    for (int i = tid; i < (1 << kDtHistBits); i += kDtThreads) {
-      const unsigned int v = hist_s[i];
-      if (v) atomicAdd(hist + row * (int64_t)(1 << kDtHistBits) + i, v);
+    for (int i = tid; i < (1 << kDtHistBits); i += kDmThreads) {
+      const unsigned int hv = hist_s[i];
+      if (hv) atomicAdd(hist + row * (int64_t)(1 << kDtHistBits) + i, hv);
     }
-  }
-  // boxes and MMAs of this CTA land before its TMEM and shared memory go
-  if (warp == 0 && issued > 0) {
-    const int u = issued - 1;
-    mbar_wait(&ms->tfull[u % kDmTbufs], (uint32_t)(u / kDmTbufs) & 1, kIxWait);
-  }
-  if (tid == 0 && !ok) {
-    // boxes issued for tiles whose MMAs never ran: let them land
-    for (int u = issued; u < loaded; ++u) mbar_wait(&ms->full[u % kDmStages], (uint32_t)(u / kDmStages) & 1, kIxWait);
   }
   fence_before_sync();
   __syncthreads();
@@ -1123,7 +1133,7 @@ cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const ui
       static PerDevice attr_m, slots_m;
       smem_limit_once(attr_m, reinterpret_cast<const void*>(scores_fp4_decode_tma_kernel), (int)kDmSmem);
       const int sl = slots_m.get([] {
-        int per = resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_tma_kernel), kDtThreads, kDmSmem);
+        int per = resident_ctas(reinterpret_cast<const void*>(scores_fp4_decode_tma_kernel), kDmThreads, kDmSmem);
         per = per > 2 ? 2 : per;   // 256 TMEM columns each: at most 2 per SM
         return device_sms() * per;
       });
@@ -1134,7 +1144,7 @@ cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const ui
       if (ch < 2 * kDmEntries) ch = 2 * kDmEntries;
       if (ch > kDmMaxChunk) ch = kDmMaxChunk;
       const dim3 g2((unsigned)((N + ch - 1) / ch), (unsigned)rows);
-      launch_pdl(scores_fp4_decode_tma_kernel, g2, dim3(kDtThreads), kDmSmem, st,
+      launch_pdl(scores_fp4_decode_tma_kernel, g2, dim3(kDmThreads), kDmSmem, st,
                  reinterpret_cast<const __nv_bfloat16*>(qI), w, ks, q_pos, Tq, HI, N, m, ch, scores, hist, flags_ws, tm);
       return cudaGetLastError();
     }
