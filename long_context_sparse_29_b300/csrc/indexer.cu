@@ -863,6 +863,141 @@ struct EqualKeyList {
 
 constexpr int kSelPerThread = kSelChunk / kSelThreads;
 
+// Sorts a[0..P) descending (P a power of two, 32 <= P <= E * NT); slots past
+// `count` are padded with 0, below every real key.  Thread t holds elements
+// E t .. E t + E - 1 in registers: compare-exchanges within a thread, across
+// lanes by shuffles, across warps through shared memory (a[0..P) and
+// a[P..2P) in turn, one barrier per such stage).
+template <int NT, int E>
+__device__ void bitonic_sort_desc(unsigned long long* a, int count, int P) {
+  const int tid = threadIdx.x;
+  const bool act = E * tid < P;   // whole warps: P >= 32 E
+  unsigned long long v[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const int e = E * tid + j;
+    v[j] = act && e < count ? a[e] : 0ull;
+  }
+  int buf = 0;
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride < E) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          if ((j & stride) == 0 && j + stride < E) {
+            const bool desc = ((E * tid + j) & size) == 0;
+            const unsigned long long x = v[j], y = v[j + stride];
+            if ((x < y) == desc) {
+              v[j] = y;
+              v[j + stride] = x;
+            }
+          }
+        }
+      } else if (stride < 32 * E) {
+        if (act) {
+          const int ts = stride / E;
+#pragma unroll
+          for (int j = 0; j < E; ++j) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[j], ts);
+            const int e = E * tid + j;
+            const bool desc = (e & size) == 0, lower = (e & stride) == 0;
+            v[j] = (desc == lower) ? (v[j] > o ? v[j] : o) : (v[j] < o ? v[j] : o);
+          }
+        }
+      } else {
+        unsigned long long* x = a + buf * P;
+        if (act) {
+#pragma unroll
+          for (int j = 0; j < E; ++j) x[E * tid + j] = v[j];
+        }
+        __syncthreads();
+        if (act) {
+#pragma unroll
+          for (int j = 0; j < E; ++j) {
+            const int e = E * tid + j;
+            const unsigned long long o = x[e ^ stride];
+            const bool desc = (e & size) == 0, lower = (e & stride) == 0;
+            v[j] = (desc == lower) ? (v[j] > o ? v[j] : o) : (v[j] < o ? v[j] : o);
+          }
+        }
+        buf ^= 1;
+      }
+    }
+  }
+  __syncthreads();   // every exchange read before the result overwrites a[0..P)
+  if (act) {
+#pragma unroll
+    for (int j = 0; j < E; ++j) a[E * tid + j] = v[j];
+  }
+  __syncthreads();
+}
+
+template <int NT>
+__device__ void sort_desc(unsigned long long* a, int count, int P) {
+  if (P <= NT) bitonic_sort_desc<NT, 1>(a, count, P);
+  else if (P <= 2 * NT) bitonic_sort_desc<NT, 2>(a, count, P);
+  else bitonic_sort_desc<NT, 4>(a, count, P);
+}
+
+// The need-th largest order key among composite keys c[0..n) that all share
+// their top kHistBits bits `top` (the bin b*): two passes of 11 and 10 bits,
+// histograms of up to 2048 bins (the ties differ only below the bin, so
+// 8-bit digits would crowd few bins).  sh.remaining = how many keys equal to
+// it are taken, sh.equal = how many there are.
+template <int NT>
+__device__ uint32_t tie_threshold(const unsigned long long* c, int n, int need, uint32_t top, unsigned int* hist,
+                                  unsigned int* warp_sum, TkShared<NT>& sh) {
+  static_assert(kHistBits == 11 && NT >= 1024, "two passes of 11 and 10 bits, two bins per thread");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = top << 21, mask = 0xffe00000u;
+  unsigned int rem = (unsigned)need;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0, nb = pass == 0 ? 2048 : 1024;
+    for (int i = tid; i < nb; i += NT) hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += NT) {
+      const uint32_t key = (uint32_t)(c[i] >> 32);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (uint32_t)(nb - 1)], 1u);
+    }
+    __syncthreads();
+    // thread t owns bins nb-1-2t and nb-2-2t (descending)
+    unsigned int h0 = 0, h1 = 0;
+    if (2 * tid < nb) {
+      h0 = hist[nb - 1 - 2 * tid];
+      h1 = hist[nb - 2 - 2 * tid];
+    }
+    const unsigned int own = h0 + h1;
+    unsigned int incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    unsigned int before = 0;
+    for (int w2 = 0; w2 < warp; ++w2) before += warp_sum[w2];
+    const unsigned int excl = before + incl - own;
+    if (2 * tid < nb) {
+      if (excl < rem && excl + h0 >= rem) {
+        sh.prefix = prefix | ((uint32_t)(nb - 1 - 2 * tid) << shift);
+        sh.remaining = rem - excl;
+        sh.equal = h0;
+      } else if (excl + h0 < rem && excl + own >= rem) {
+        sh.prefix = prefix | ((uint32_t)(nb - 2 - 2 * tid) << shift);
+        sh.remaining = rem - excl - h0;
+        sh.equal = h1;
+      }
+    }
+    __syncthreads();
+    prefix = sh.prefix;
+    rem = sh.remaining;
+    mask |= (uint32_t)(nb - 1) << shift;
+  }
+  return prefix;
+}
+
 __global__ void __launch_bounds__(kSelThreads)
 topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __restrict__ hist,
                         const int64_t* __restrict__ q_pos, int64_t N, int m, int k, int nchunk, int P,
@@ -874,6 +1009,7 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
   // 2 P sort keys, then the row's staged ties
   extern __shared__ __align__(16) unsigned long long dyn_s[];
   __shared__ unsigned int warp_sum[NT / 32];
+  __shared__ unsigned int hist2_s[2048];
   __shared__ int bstar_s, last_s, base_s, base_t;
   __shared__ unsigned int nls_s, nlt_s, take_s;
   __shared__ TkShared<NT> sh;
@@ -973,16 +1109,26 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
       const uint32_t thr = radix_threshold<NT>(src, nv, kk, sh);
       ordered_collect<NT>(src, nv, thr, sh.remaining, keys_s, sh);
     } else {
-      for (int i = tid; i < nsure; i += NT) keys_s[i] = __ldcg(sure + i);
+      // the row's sure and tie keys into shared memory, every load in flight together
+      {
+        unsigned long long t[kTieCap / NT];
+#pragma unroll
+        for (int r = 0; r < kTieCap / NT; ++r) {
+          const int i = tid + r * NT;
+          t[r] = i < ntie ? __ldcg(tie + i) : 0ull;
+        }
+        for (int i = tid; i < nsure; i += NT) keys_s[i] = __ldcg(sure + i);
+#pragma unroll
+        for (int r = 0; r < kTieCap / NT; ++r) {
+          const int i = tid + r * NT;
+          if (i < ntie) tie_s[i] = t[r];
+        }
+      }
       const int need = kk - nsure;   // ties to take (0 when every key is taken)
       if (need > 0) {
-        for (int i = tid; i < ntie; i += NT) tie_s[i] = __ldcg(tie + i);
         if (tid == 0) take_s = nsure;
         __syncthreads();
-        // every tie shares the top kHistBits bits (bin b*): the search starts
-        // below the top byte
-        const uint32_t thr = radix_threshold<NT>(CandList{tie_s}, ntie, need, sh, 16,
-                                                 (uint32_t)(bstar >> (kHistBits - 8)) << 24);
+        const uint32_t thr = tie_threshold<NT>(tie_s, ntie, need, (uint32_t)bstar, hist2_s, warp_sum, sh);
         // keys equal to thr to take, lowest indices first; when all of them
         // are taken no index threshold is needed
         const unsigned int rem = sh.remaining, neq = sh.equal;
@@ -991,16 +1137,28 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
           __syncthreads();
           ithr = radix_threshold<NT>(EqualKeyList{tie_s, thr}, ntie, (int)rem, sh);
         }
-        for (int i = tid; i < ntie; i += NT) {
-          const unsigned long long v = tie_s[i];
-          const uint32_t key = (uint32_t)(v >> 32), low = (uint32_t)(v & 0xffffffffull);
-          if (key > thr || (key == thr && low >= ithr)) keys_s[atomicAdd(&take_s, 1u)] = v;
+        // the chosen ties appended after the sure keys, one reservation per warp
+        for (int i0 = 0; i0 < ntie; i0 += NT) {
+          const int i = i0 + tid;
+          unsigned long long v = 0;
+          bool take = false;
+          if (i < ntie) {
+            v = tie_s[i];
+            const uint32_t key = (uint32_t)(v >> 32), low = (uint32_t)(v & 0xffffffffull);
+            take = key > thr || (key == thr && low >= ithr);
+          }
+          const unsigned int bt = __ballot_sync(0xffffffffu, take);
+          unsigned int base = 0;
+          if (lane == 0 && bt) base = atomicAdd(&take_s, (unsigned)__popc(bt));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          if (take) keys_s[base + __popc(bt & ((1u << lane) - 1u))] = v;
         }
       }
       __syncthreads();
     }
   }
-  emit_topk<NT>(merge_sort_desc<NT>(keys_s, kk, P), kk, k, row, idx_out, score_out);
+  sort_desc<NT>(keys_s, kk, P);
+  emit_topk<NT>(keys_s, kk, k, row, idx_out, score_out);
   if (tid == 0) {   // the workspace counters for the next call
     rc[0] = 0;
     rc[1] = 0;

@@ -562,8 +562,8 @@ def _pattern_with_positive_score(oracle_mod, rng, qbits, w):
     raise AssertionError("no pattern with a positive score")
 
 
-@pytest.mark.parametrize("N", [20000, 20001])   # even N: TMA-fed scorer; odd: copy-fed
-def test_indexer_decode_topk_equal_scores(csa, oracle_mod, N):
+@pytest.mark.parametrize("N,k", [(20000, 1024), (20001, 1024), (20000, 2000)])   # odd N: copy-fed scorer
+def test_indexer_decode_topk_equal_scores(csa, oracle_mod, N, k):
     """Decode rows (histogram top-k) whose scores repeat exactly, against the
     oracle bit for bit (equal scores by ascending index):
     row 0: 50 distinct entries repeated at random -- the sure and tie keys
@@ -573,7 +573,7 @@ def test_indexer_decode_topk_equal_scores(csa, oracle_mod, N):
     to sort at once, the ties selected first; row 3: fewer visible entries
     than k -- every one taken."""
     rng = np.random.default_rng(31337 + N)
-    B, HI, k = 4, 16, 1024
+    B, HI = 4, 16
     qI = rng.standard_normal((1, 1, HI, 64)).astype(np.float32)
     qbits = np.repeat(wl.f32_to_bf16_bits(qI), B, axis=0)
     w = np.repeat(rng.uniform(0.1, 1.0, (1, 1, HI)).astype(np.float32), B, axis=0)
