@@ -41,9 +41,6 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
 
 // cp.async of 16 bytes, of which the first `src_bytes` (0 or 16) are read
 // and the rest zero-filled.

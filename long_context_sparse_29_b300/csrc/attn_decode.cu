@@ -252,6 +252,12 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   const int64_t t = p.q_pos[row];
   const bool t_ok = t >= 0 && t < p.rope_rows;
   const bool dense = p.idx == nullptr;
+  // the RoPE row of t for the merge's inverse rotation, loaded now (threads 64..95)
+  float rope_c = 0.0f, rope_s = 0.0f;
+  if (tid >= 64 && tid < 96) {
+    rope_c = p.rcos[(t_ok ? t : 0) * 32 + tid - 64];
+    rope_s = p.rsin[(t_ok ? t : 0) * 32 + tid - 64];
+  }
 
   if (tid == 0) {
     ms->abort = 0;
@@ -570,26 +576,30 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     // heads 64 mt .. ; stored as [dim][head] bf16 rows of 128 bytes
     __nv_bfloat16* po = p.part_o + item * (int64_t)(kH * kD);
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      const int mt = c >> 1, hh = c & 1;
-      uint32_t o[32];
+    for (int mt = 0; mt < 4; ++mt) {
+      // both head halves of dim block mt: two TMEM loads in flight per wait
+      uint32_t o[2][32];
       if (any_keys && !bad) {
-        tmem_ld32(tmem + tq_lane + kTmemO + 64u * mt + 32u * hh, o);
+        tmem_ld32(tmem + tq_lane + kTmemO + 64u * mt, o[0]);
+        tmem_ld32(tmem + tq_lane + kTmemO + 64u * mt + 32u, o[1]);
         tmem_wait_ld();
       }
       const int d = 128 * mt + 32 * qd + lane;
-      uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int h0 = 32 * hh + 2 * j;
-        const float f0 = (any_keys && !bad) ? __uint_as_float(o[2 * j]) * inv_s[h0] : 0.0f;
-        const float f1 = (any_keys && !bad) ? __uint_as_float(o[2 * j + 1]) * inv_s[h0 + 1] : 0.0f;
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(f0, f1);
-        pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int h0 = 32 * hh + 2 * j;
+          const float f0 = (any_keys && !bad) ? __uint_as_float(o[hh][2 * j]) * inv_s[h0] : 0.0f;
+          const float f1 = (any_keys && !bad) ? __uint_as_float(o[hh][2 * j + 1]) * inv_s[h0 + 1] : 0.0f;
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(f0, f1);
+          pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(po + (int64_t)d * kH + 32 * hh);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
       }
-      uint4* dst = reinterpret_cast<uint4*>(po + (int64_t)d * kH + 32 * hh);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
     }
     if (bad) fail = true;
     // the partial is visible to the row's other items (read there by bulk
@@ -655,8 +665,10 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   float* Ls = wgt + (size_t)ns * kH;
   if (tid < kH) {
     float M = -INFINITY;
+#pragma unroll 4
     for (int s = 0; s < ns; ++s) M = fmaxf(M, ml_s[s * kH + tid].x);
     float L = 0.0f;
+#pragma unroll 4
     for (int s = 0; s < ns; ++s) {
       const float2 v = ml_s[s * kH + tid];
       const float w = v.x == -INFINITY ? 0.0f : exp2f(v.x - M) * v.y;
@@ -670,14 +682,15 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   float* cs = Ls + kH;   // the RoPE row of t: 32 cos, 32 sin
   float* sn = cs + 32;
   if (tid >= 64 && tid < 96) {
-    cs[tid - 64] = p.rcos[(t_ok ? t : 0) * 32 + tid - 64];
-    sn[tid - 64] = p.rsin[(t_ok ? t : 0) * 32 + tid - 64];
+    cs[tid - 64] = rope_c;
+    sn[tid - 64] = rope_s;
   }
   __syncthreads();
   // thread: a pair of dims (d, d + 1) of one head, weighted sum in split order
   for (int u = tid; u < (nd >> 1) * kH; u += kThreads) {
     const int h = u % kH, dl = 2 * (u / kH), d = d0 + dl;
     float o0 = 0.0f, o1 = 0.0f;
+#pragma unroll 4
     for (int s = 0; s < ns; ++s) {
       const float w = wgt[s * kH + h];
       const __nv_bfloat16* src = sl_s + ((size_t)s * nd + dl) * kH + h;

@@ -867,16 +867,18 @@ constexpr int kSelPerThread = kSelChunk / kSelThreads;
 // `count` are padded with 0, below every real key.  Thread t holds elements
 // E t .. E t + E - 1 in registers: compare-exchanges within a thread, across
 // lanes by shuffles, across warps through shared memory (a[0..P) and
-// a[P..2P) in turn, one barrier per such stage).
+// a[P..2P) in turn, one barrier per such stage).  The warps that hold
+// elements take part whole; below P = 32 E the lanes past P / E carry
+// padding among themselves (no stage reaches across warps there).
 template <int NT, int E>
 __device__ void bitonic_sort_desc(unsigned long long* a, int count, int P) {
   const int tid = threadIdx.x;
-  const bool act = E * tid < P;   // whole warps: P >= 32 E
+  const bool act = (tid >> 5) < (P / E + 31) / 32;
   unsigned long long v[E];
 #pragma unroll
   for (int j = 0; j < E; ++j) {
     const int e = E * tid + j;
-    v[j] = act && e < count ? a[e] : 0ull;
+    v[j] = act && e < count && e < P ? a[e] : 0ull;
   }
   int buf = 0;
   for (int size = 2; size <= P; size <<= 1) {
@@ -927,16 +929,17 @@ __device__ void bitonic_sort_desc(unsigned long long* a, int count, int P) {
   __syncthreads();   // every exchange read before the result overwrites a[0..P)
   if (act) {
 #pragma unroll
-    for (int j = 0; j < E; ++j) a[E * tid + j] = v[j];
+    for (int j = 0; j < E; ++j)
+      if (E * tid + j < P) a[E * tid + j] = v[j];
   }
   __syncthreads();
 }
 
+// four keys per thread (P / 4 threads take part): most compare-exchanges stay
+// in registers or within a warp, and fewer warps issue the network
 template <int NT>
 __device__ void sort_desc(unsigned long long* a, int count, int P) {
-  if (P <= NT) bitonic_sort_desc<NT, 1>(a, count, P);
-  else if (P <= 2 * NT) bitonic_sort_desc<NT, 2>(a, count, P);
-  else bitonic_sort_desc<NT, 4>(a, count, P);
+  bitonic_sort_desc<NT, 4>(a, count, P);
 }
 
 // The need-th largest order key among composite keys c[0..n) that all share

@@ -751,7 +751,8 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 
 __global__ void __launch_bounds__(kDmThreads, 2)
 scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
-                             const uint8_t* __restrict__ ks, const int64_t* __restrict__ q_pos, int64_t Tq,
+                             const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
+                             const int64_t* __restrict__ q_pos, int64_t Tq,
                              int HI, int64_t N, int m, int64_t chunk, float* __restrict__ scores,
                              unsigned int* __restrict__ hist, void* ws, const __grid_constant__ CUtensorMap tm_k) {
   pdl_begin();
@@ -767,6 +768,27 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
   const int ntiles = (int)((c1 - c0 + kDmEntries - 1) / kDmEntries);
   const int64_t vrow0 = (b * N + c0) / 2;   // first row of the two-entry view
+  const int n = (int)(c1 - c0);
+
+  // warps 0-3: the chunk's scale bytes and this thread's query values, the
+  // loads in flight during the set-up
+  uint16_t v[kDmMaxChunk / 128];
+  float qv[2][4];
+  if (warp < 4) {
+    const uint16_t* ks16 = reinterpret_cast<const uint16_t*>(ks) + b * N + c0;
+#pragma unroll
+    for (int r = 0; r < kDmMaxChunk / 128; ++r) {
+      const int i = tid + r * 128;
+      v[r] = i < n ? __ldg(ks16 + i) : (uint16_t)0;
+    }
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int blkid = (tid >> 3) + 16 * it, u = tid & 7, h = blkid >> 1, blk = blkid & 1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        qv[it][i] = h < HI ? __bfloat162float(qI[(row * HI + h) * 64 + 32 * blk + 4 * u + i]) : 0.0f;
+    }
+  }
 
   // the query operand and the key stages zeroed: TMA leaves the gaps of the padded form untouched
   for (int i = tid; i < (int)(kDmSOff / 16); i += kDmThreads) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
@@ -803,8 +825,16 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       mbar_arrive_expect_tx(&ms->full[s], 8192);   // the box's global bytes: the gaps are neither written nor counted
       tma_load_2d(aA + s * 16384, &tm_k, 0, (int)(vrow0 + (int64_t)u * (kDmEntries / 2)), &ms->full[s]);
     };
-    if (lane == 0)
+    // tile u's codes into L2 ahead of its box (no shared memory held meanwhile)
+    auto prefetch_tile = [&](int u) {
+      const int64_t e0 = (int64_t)u * kDmEntries;
+      const int64_t ne = n - e0 < kDmEntries ? n - e0 : kDmEntries;
+      prefetch_l2(kc + (b * N + c0 + e0) * 32, (uint32_t)ne * 32);
+    };
+    if (lane == 0) {
       for (int u = 0; u < kDmStages && u < ntiles; ++u) load_tile(u);
+      for (int u = kDmStages; u < 2 * kDmStages && u < ntiles; ++u) prefetch_tile(u);
+    }
     int loaded = min(ntiles, kDmStages), issued = 0;
     bool got = __all_sync(0xffffffffu, mbar_wait(&ms->qready, 0, kIxWait));
     constexpr uint32_t id = idesc_e2m1(kDtThreads, kDtHeads);
@@ -831,8 +861,12 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
         const int sp = (u - 1) % kDmStages;
         bool fine = true;
         if (lane == 0) {
-          if (mbar_wait(&ms->empty[sp], (uint32_t)((u - 1) / kDmStages) & 1, kIxWait)) load_tile(u - 1 + kDmStages);
-          else fine = false;
+          if (mbar_wait(&ms->empty[sp], (uint32_t)((u - 1) / kDmStages) & 1, kIxWait)) {
+            load_tile(u - 1 + kDmStages);
+            if (u - 1 + 2 * kDmStages < ntiles) prefetch_tile(u - 1 + 2 * kDmStages);
+          } else {
+            fine = false;
+          }
         }
         got = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
         if (got) loaded = u - 1 + kDmStages + 1;
@@ -847,27 +881,15 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
     if (lane == 0)
       for (int u = issued; u < loaded; ++u) mbar_wait(&ms->full[u % kDmStages], (uint32_t)(u / kDmStages) & 1, kIxWait);
   } else {
-    // ---- warps 0-3: the chunk's scale bytes (loads in flight while the query is quantised) ----
+    // ---- warps 0-3: the query's MXFP4 codes into the B operand, block exponents ----
     uint16_t* sc_s = reinterpret_cast<uint16_t*>(sm + kDmSOff);
-    const uint16_t* ks16 = reinterpret_cast<const uint16_t*>(ks) + b * N + c0;
-    const int n = (int)(c1 - c0);
-    uint16_t v[kDmMaxChunk / 128];
 #pragma unroll
-    for (int r = 0; r < kDmMaxChunk / 128; ++r) {
-      const int i = tid + r * 128;
-      v[r] = i < n ? __ldg(ks16 + i) : (uint16_t)0;
-    }
-    // ---- the query: MXFP4 codes into the B operand, block exponents ----
-    for (int blkid = tid >> 3; blkid < 2 * kDtHeads; blkid += 128 / 8) {
-      const int u = tid & 7, h = blkid >> 1, blk = blkid & 1;
+    for (int it = 0; it < 2; ++it) {
+      const int blkid = (tid >> 3) + 16 * it, u = tid & 7, h = blkid >> 1, blk = blkid & 1;
       const bool act = h < HI;
-      float qv[4];
       float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        qv[i] = act ? __bfloat162float(qI[(row * HI + h) * 64 + 32 * blk + 4 * u + i]) : 0.0f;
-        amax = fmaxf(amax, fabsf(qv[i]));
-      }
+      for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(qv[it][i]));
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       const int sx = mx_block_exp(amax);
@@ -875,7 +897,7 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       if (act) {
         uint32_t cd = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cd |= e2m1_encode(__fmul_rn(qv[i], inv)) << (4 * i);
+        for (int i = 0; i < 4; ++i) cd |= e2m1_encode(__fmul_rn(qv[it][i], inv)) << (4 * i);
         *reinterpret_cast<uint16_t*>(sm + kDmBOff + sw128_off(h, 2 * blk + (u >> 2)) + 2 * (u & 3)) = (uint16_t)cd;
         if (u == 0) {
           if (blk == 0) {
@@ -1145,7 +1167,8 @@ cudaError_t launch_scores_fp4_decode_tc(const void* qI, const float* w, const ui
       if (ch > kDmMaxChunk) ch = kDmMaxChunk;
       const dim3 g2((unsigned)((N + ch - 1) / ch), (unsigned)rows);
       launch_pdl(scores_fp4_decode_tma_kernel, g2, dim3(kDmThreads), kDmSmem, st,
-                 reinterpret_cast<const __nv_bfloat16*>(qI), w, ks, q_pos, Tq, HI, N, m, ch, scores, hist, flags_ws, tm);
+                 reinterpret_cast<const __nv_bfloat16*>(qI), w, kc, ks, q_pos, Tq, HI, N, m, ch, scores, hist, flags_ws,
+                 tm);
       return cudaGetLastError();
     }
   }

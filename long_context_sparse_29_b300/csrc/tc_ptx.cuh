@@ -229,6 +229,11 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
                : "memory");
 }
 
+// Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 // Wait for the phase with the given parity to complete; gives up after
 // `limit` polls and returns false (the caller records a timeout).
 __device__ __forceinline__ bool mbar_wait(void* bar, uint32_t parity, uint32_t limit) {
