@@ -884,14 +884,20 @@ __device__ void bitonic_sort_desc(unsigned long long* a, int count, int P) {
   for (int size = 2; size <= P; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       if (stride < E) {
+        // register indices fixed at compile time (one branch per stride)
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-          if ((j & stride) == 0 && j + stride < E) {
-            const bool desc = ((E * tid + j) & size) == 0;
-            const unsigned long long x = v[j], y = v[j + stride];
-            if ((x < y) == desc) {
-              v[j] = y;
-              v[j + stride] = x;
+        for (int st = 1; st < E; st <<= 1) {
+          if (stride == st) {
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+              if ((j & st) == 0) {
+                const bool desc = ((E * tid + j) & size) == 0;
+                const unsigned long long x = v[j], y = v[j + st];
+                if ((x < y) == desc) {
+                  v[j] = y;
+                  v[j + st] = x;
+                }
+              }
             }
           }
         }
