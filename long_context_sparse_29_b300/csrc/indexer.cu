@@ -863,91 +863,6 @@ struct EqualKeyList {
 
 constexpr int kSelPerThread = kSelChunk / kSelThreads;
 
-// Sorts a[0..P) descending (P a power of two, 32 <= P <= E * NT); slots past
-// `count` are padded with 0, below every real key.  Thread t holds elements
-// E t .. E t + E - 1 in registers: compare-exchanges within a thread, across
-// lanes by shuffles, across warps through shared memory (a[0..P) and
-// a[P..2P) in turn, one barrier per such stage).  The warps that hold
-// elements take part whole; below P = 32 E the lanes past P / E carry
-// padding among themselves (no stage reaches across warps there).
-template <int NT, int E>
-__device__ void bitonic_sort_desc(unsigned long long* a, int count, int P) {
-  const int tid = threadIdx.x;
-  const bool act = (tid >> 5) < (P / E + 31) / 32;
-  unsigned long long v[E];
-#pragma unroll
-  for (int j = 0; j < E; ++j) {
-    const int e = E * tid + j;
-    v[j] = act && e < count && e < P ? a[e] : 0ull;
-  }
-  int buf = 0;
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride < E) {
-        // register indices fixed at compile time (one branch per stride)
-#pragma unroll
-        for (int st = 1; st < E; st <<= 1) {
-          if (stride == st) {
-#pragma unroll
-            for (int j = 0; j < E; ++j) {
-              if ((j & st) == 0) {
-                const bool desc = ((E * tid + j) & size) == 0;
-                const unsigned long long x = v[j], y = v[j + st];
-                if ((x < y) == desc) {
-                  v[j] = y;
-                  v[j + st] = x;
-                }
-              }
-            }
-          }
-        }
-      } else if (stride < 32 * E) {
-        if (act) {
-          const int ts = stride / E;
-#pragma unroll
-          for (int j = 0; j < E; ++j) {
-            const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[j], ts);
-            const int e = E * tid + j;
-            const bool desc = (e & size) == 0, lower = (e & stride) == 0;
-            v[j] = (desc == lower) ? (v[j] > o ? v[j] : o) : (v[j] < o ? v[j] : o);
-          }
-        }
-      } else {
-        unsigned long long* x = a + buf * P;
-        if (act) {
-#pragma unroll
-          for (int j = 0; j < E; ++j) x[E * tid + j] = v[j];
-        }
-        __syncthreads();
-        if (act) {
-#pragma unroll
-          for (int j = 0; j < E; ++j) {
-            const int e = E * tid + j;
-            const unsigned long long o = x[e ^ stride];
-            const bool desc = (e & size) == 0, lower = (e & stride) == 0;
-            v[j] = (desc == lower) ? (v[j] > o ? v[j] : o) : (v[j] < o ? v[j] : o);
-          }
-        }
-        buf ^= 1;
-      }
-    }
-  }
-  __syncthreads();   // every exchange read before the result overwrites a[0..P)
-  if (act) {
-#pragma unroll
-    for (int j = 0; j < E; ++j)
-      if (E * tid + j < P) a[E * tid + j] = v[j];
-  }
-  __syncthreads();
-}
-
-// four keys per thread (P / 4 threads take part): most compare-exchanges stay
-// in registers or within a warp, and fewer warps issue the network
-template <int NT>
-__device__ void sort_desc(unsigned long long* a, int count, int P) {
-  bitonic_sort_desc<NT, 4>(a, count, P);
-}
-
 // The need-th largest order key among composite keys c[0..n) that all share
 // their top kHistBits bits `top` (the bin b*): two passes of 11 and 10 bits,
 // histograms of up to 2048 bins (the ties differ only below the bin, so
@@ -1166,8 +1081,7 @@ topk_hist_select_kernel(const float* __restrict__ scores, const unsigned int* __
       __syncthreads();
     }
   }
-  sort_desc<NT>(keys_s, kk, P);
-  emit_topk<NT>(keys_s, kk, k, row, idx_out, score_out);
+  emit_topk<NT>(merge_sort_desc<NT>(keys_s, kk, P), kk, k, row, idx_out, score_out);
   if (tid == 0) {   // the workspace counters for the next call
     rc[0] = 0;
     rc[1] = 0;
