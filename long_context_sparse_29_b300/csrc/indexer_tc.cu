@@ -725,7 +725,11 @@ scores_fp4_decode_tc_kernel(const __nv_bfloat16* __restrict__ qI, const float* _
 namespace {
 
 constexpr int kDmEntries = 256;             // entries per tile
-constexpr int kDmThreads = 160;             // warps 0-3 epilogue (thread = TMEM lane), warp 4 TMA + MMA
+constexpr int kDmEpiWarps = 8;              // epilogue: warp w reads TMEM lanes 32 (w % 4) .., entry parity w / 4
+constexpr int kDmMmaWarp = 8;               // MMA issue
+constexpr int kDmTmaWarp = 9;               // TMA boxes and L2 prefetches
+constexpr int kDmThreads = 320;
+constexpr int kDmEpi = 32 * kDmEpiWarps;    // epilogue threads
 constexpr int kDmStages = 4;                // 16 KiB TMA boxes
 constexpr int kDmTbufs = 4;                 // TMEM buffers of 64 columns
 constexpr int kDmMaxChunk = 4096;           // entries per CTA at most (their scale bytes are staged)
@@ -744,8 +748,8 @@ struct DmMisc {
 };
 static_assert(sizeof(DmMisc) <= 512, "DmMisc overflows its smem slot");
 
-// the 128 epilogue threads only
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// the epilogue threads only
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kDmEpi) : "memory"); }
 
 }  // namespace
 
@@ -770,23 +774,25 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   const int64_t vrow0 = (b * N + c0) / 2;   // first row of the two-entry view
   const int n = (int)(c1 - c0);
 
-  // warps 0-3: the chunk's scale bytes and this thread's query values, the
-  // loads in flight during the set-up
-  uint16_t v[kDmMaxChunk / 128];
+  // epilogue threads: the chunk's scale bytes and, threads 0..127, this
+  // thread's query values -- the loads in flight during the set-up
+  uint16_t v[kDmMaxChunk / kDmEpi];
   float qv[2][4];
-  if (warp < 4) {
+  if (warp < kDmEpiWarps) {
     const uint16_t* ks16 = reinterpret_cast<const uint16_t*>(ks) + b * N + c0;
 #pragma unroll
-    for (int r = 0; r < kDmMaxChunk / 128; ++r) {
-      const int i = tid + r * 128;
+    for (int r = 0; r < kDmMaxChunk / kDmEpi; ++r) {
+      const int i = tid + r * kDmEpi;
       v[r] = i < n ? __ldg(ks16 + i) : (uint16_t)0;
     }
+    if (tid < 128) {
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      const int blkid = (tid >> 3) + 16 * it, u = tid & 7, h = blkid >> 1, blk = blkid & 1;
+      for (int it = 0; it < 2; ++it) {
+        const int blkid = (tid >> 3) + 16 * it, u = tid & 7, h = blkid >> 1, blk = blkid & 1;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        qv[it][i] = h < HI ? __bfloat162float(qI[(row * HI + h) * 64 + 32 * blk + 4 * u + i]) : 0.0f;
+        for (int i = 0; i < 4; ++i)
+          qv[it][i] = h < HI ? __bfloat162float(qI[(row * HI + h) * 64 + 32 * blk + 4 * u + i]) : 0.0f;
+      }
     }
   }
 
@@ -803,7 +809,7 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
     }
     for (int i = 0; i < kDmTbufs; ++i) {
       mbar_init(&ms->tfull[i], 1);
-      mbar_init(&ms->tempty[i], 4);
+      mbar_init(&ms->tempty[i], kDmEpiWarps);
     }
     mbar_init(&ms->qready, 128);
     mbar_fence_init();
@@ -817,27 +823,41 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   const uint32_t tmem = ms->tmem;
   bool ok = true;
 
-  if (warp == 4) {
-    // ---- TMA and MMA issue: tile u = one box of 128 view rows into stage u % kDmStages ----
-    const uint32_t aA = smem_u32(sm + kDmAOff), aB = smem_u32(sm + kDmBOff);
-    auto load_tile = [&](int u) {
-      const int s = u % kDmStages;
-      mbar_arrive_expect_tx(&ms->full[s], 8192);   // the box's global bytes: the gaps are neither written nor counted
-      tma_load_2d(aA + s * 16384, &tm_k, 0, (int)(vrow0 + (int64_t)u * (kDmEntries / 2)), &ms->full[s]);
-    };
-    // tile u's codes into L2 ahead of its box (no shared memory held meanwhile)
+  if (warp == kDmTmaWarp) {
+    // ---- TMA: tile u = one box of 128 view rows into stage u % kDmStages, once
+    // the MMAs of the stage's previous tile are done; codes prefetched into L2
+    // a stage set ahead (no shared memory held meanwhile) ----
+    const uint32_t aA = smem_u32(sm + kDmAOff);
     auto prefetch_tile = [&](int u) {
       const int64_t e0 = (int64_t)u * kDmEntries;
       const int64_t ne = n - e0 < kDmEntries ? n - e0 : kDmEntries;
       prefetch_l2(kc + (b * N + c0 + e0) * 32, (uint32_t)ne * 32);
     };
     if (lane == 0) {
-      for (int u = 0; u < kDmStages && u < ntiles; ++u) load_tile(u);
       for (int u = kDmStages; u < 2 * kDmStages && u < ntiles; ++u) prefetch_tile(u);
+      int u = 0;
+      for (; u < ntiles; ++u) {
+        const int s = u % kDmStages;
+        if (u >= kDmStages && !mbar_wait(&ms->empty[s], (uint32_t)(u / kDmStages - 1) & 1, kIxWait)) break;
+        mbar_arrive_expect_tx(&ms->full[s], 8192);   // the box's global bytes: the gaps are neither written nor counted
+        tma_load_2d(aA + s * 16384, &tm_k, 0, (int)(vrow0 + (int64_t)u * (kDmEntries / 2)), &ms->full[s]);
+        if (u >= kDmStages && u + kDmStages < ntiles) prefetch_tile(u + kDmStages);
+      }
+      if (u < ntiles) {
+        ok = false;
+        flag_timeout(ws);
+      }
+      // boxes issued land before shared memory goes (those the MMA warp consumed are done)
+      for (int v2 = max(0, u - kDmStages); v2 < u; ++v2)
+        mbar_wait(&ms->full[v2 % kDmStages], (uint32_t)(v2 / kDmStages) & 1, kIxWait);
     }
-    int loaded = min(ntiles, kDmStages), issued = 0;
-    bool got = __all_sync(0xffffffffu, mbar_wait(&ms->qready, 0, kIxWait));
+    __syncwarp();
+  } else if (warp == kDmMmaWarp) {
+    // ---- MMA issue: four per tile (two entry parities x two blocks) into TMEM buffer u % kDmTbufs ----
+    const uint32_t aA = smem_u32(sm + kDmAOff), aB = smem_u32(sm + kDmBOff);
     constexpr uint32_t id = idesc_e2m1(kDtThreads, kDtHeads);
+    int issued = 0;
+    bool got = __all_sync(0xffffffffu, mbar_wait(&ms->qready, 0, kIxWait));
     for (int u = 0; u < ntiles && got; ++u) {
       const int s = u % kDmStages, tb = u % kDmTbufs;
       got = mbar_wait(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxWait);
@@ -856,149 +876,109 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       mma_commit_elect(&ms->empty[s]);
       ++issued;
       __syncwarp();
-      // the stage of tile u - 1 takes tile u - 1 + kDmStages once tile u - 1's MMAs are done
-      if (u >= 1 && u - 1 + kDmStages < ntiles) {
-        const int sp = (u - 1) % kDmStages;
-        bool fine = true;
-        if (lane == 0) {
-          if (mbar_wait(&ms->empty[sp], (uint32_t)((u - 1) / kDmStages) & 1, kIxWait)) {
-            load_tile(u - 1 + kDmStages);
-            if (u - 1 + 2 * kDmStages < ntiles) prefetch_tile(u - 1 + 2 * kDmStages);
-          } else {
-            fine = false;
-          }
-        }
-        got = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
-        if (got) loaded = u - 1 + kDmStages + 1;
-      }
     }
     if (!got) {
       ok = false;
       if (lane == 0) flag_timeout(ws);
     }
-    // the MMAs issued complete and the boxes issued land before TMEM and shared memory go
+    // the MMAs issued complete before TMEM and shared memory go
     if (issued > 0) mbar_wait(&ms->tfull[(issued - 1) % kDmTbufs], (uint32_t)((issued - 1) / kDmTbufs) & 1, kIxWait);
-    if (lane == 0)
-      for (int u = issued; u < loaded; ++u) mbar_wait(&ms->full[u % kDmStages], (uint32_t)(u / kDmStages) & 1, kIxWait);
   } else {
-    // ---- warps 0-3: the query's MXFP4 codes into the B operand, block exponents ----
+    // ---- threads 0..127: the query's MXFP4 codes into the B operand, block exponents ----
     uint16_t* sc_s = reinterpret_cast<uint16_t*>(sm + kDmSOff);
+    if (tid < 128) {
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      const int blkid = (tid >> 3) + 16 * it, u = tid & 7, h = blkid >> 1, blk = blkid & 1;
-      const bool act = h < HI;
-      float amax = 0.0f;
+      for (int it = 0; it < 2; ++it) {
+        const int blkid = (tid >> 3) + 16 * it, u = tid & 7, h = blkid >> 1, blk = blkid & 1;
+        const bool act = h < HI;
+        float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(qv[it][i]));
+        for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(qv[it][i]));
 #pragma unroll
-      for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const int sx = mx_block_exp(amax);
-      const float inv = pow2i(-sx);
-      if (act) {
-        uint32_t cd = 0;
+        for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const int sx = mx_block_exp(amax);
+        const float inv = pow2i(-sx);
+        if (act) {
+          uint32_t cd = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cd |= e2m1_encode(__fmul_rn(qv[it][i], inv)) << (4 * i);
-        *reinterpret_cast<uint16_t*>(sm + kDmBOff + sw128_off(h, 2 * blk + (u >> 2)) + 2 * (u & 3)) = (uint16_t)cd;
-        if (u == 0) {
-          if (blk == 0) {
-            atomicMin(&ms->qlo0, sx);
-            atomicMax(&ms->qhi0, sx);
-            ms->hx[h].x = sx << 23;
-            ms->hx[h].z = __float_as_int(w[row * HI + h]);
-          } else {
-            atomicMin(&ms->qlo1, sx);
-            atomicMax(&ms->qhi1, sx);
-            ms->hx[h].y = sx << 23;
+          for (int i = 0; i < 4; ++i) cd |= e2m1_encode(__fmul_rn(qv[it][i], inv)) << (4 * i);
+          *reinterpret_cast<uint16_t*>(sm + kDmBOff + sw128_off(h, 2 * blk + (u >> 2)) + 2 * (u & 3)) = (uint16_t)cd;
+          if (u == 0) {
+            if (blk == 0) {
+              atomicMin(&ms->qlo0, sx);
+              atomicMax(&ms->qhi0, sx);
+              ms->hx[h].x = sx << 23;
+              ms->hx[h].z = __float_as_int(w[row * HI + h]);
+            } else {
+              atomicMin(&ms->qlo1, sx);
+              atomicMax(&ms->qhi1, sx);
+              ms->hx[h].y = sx << 23;
+            }
           }
         }
       }
+      fence_proxy_async();
+      mbar_arrive(&ms->qready);
     }
-    fence_proxy_async();
-    mbar_arrive(&ms->qready);
 #pragma unroll
-    for (int r = 0; r < kDmMaxChunk / 128; ++r) {
-      const int i = tid + r * 128;
+    for (int r = 0; r < kDmMaxChunk / kDmEpi; ++r) {
+      const int i = tid + r * kDmEpi;
       if (i < n) sc_s[i] = v[r];
     }
     epi_sync();
     const int qlo0 = ms->qlo0, qhi0 = ms->qhi0, qlo1 = ms->qlo1, qhi1 = ms->qhi1;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const int q4 = warp & 3, par = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int r = 32 * q4 + lane;   // view row of this thread: entry 2r + par
 
-    // one entry's score from its 32 block dots (P[0..15] block 0, P[16..31] block 1)
-    auto fast_of = [&](uint32_t sc) -> bool {
-      const int x0 = (int)(sc & 0xffu), x1 = (int)((sc >> 8) & 0xffu);
-      return qlo0 + x0 >= 27 && qhi0 + x0 <= 227 && qlo1 + x1 >= 27 && qhi1 + x1 <= 227;
-    };
-    auto score_slow = [&](const uint32_t* P, uint32_t sc) -> float {
-      const int x0 = (int)(sc & 0xffu), x1 = (int)((sc >> 8) & 0xffu);
-      float s = 0.0f;
-#pragma unroll
-      for (int h = 0; h < kDtHeads; ++h) {
-        if (h < HI) {
-          const int4 hx = ms->hx[h];
-          const float d = __fadd_rn(scale_pow2(__uint_as_float(P[h]), (hx.x >> 23) + x0 - 127),
-                                    scale_pow2(__uint_as_float(P[16 + h]), (hx.y >> 23) + x1 - 127));
-          s = __fmaf_rn(__int_as_float(hx.z), d > 0.0f ? d : 0.0f, s);
-        }
-      }
-      return s;
-    };
-    auto to_key_bin = [&](float s) -> uint32_t {
-      uint32_t key = __float_as_uint(s);
+    auto to_key_bin = [&](float sv) -> uint32_t {
+      uint32_t key = __float_as_uint(sv);
       if (key == 0x80000000u) key = 0u;
       key = (key & 0x80000000u) ? ~key : (key | 0x80000000u);
       return key >> (32 - kDtHistBits);
     };
-    // ---- the epilogue of every tile: thread r = view row r = entries 2r and 2r + 1 ----
+    // ---- the epilogue of every tile: this thread's entry from its 32 block dots ----
     for (int u = 0; u < ntiles && ok; ++u) {
       const int tb = u % kDmTbufs;
       ok = __all_sync(0xffffffffu, mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDmTbufs) & 1, kIxWait));
       if (!ok) break;
       fence_after_sync();
-      uint32_t P0[32], P1[32];
-      tmem_ld32(tmem + lane_base + 64u * tb, P0);
-      tmem_ld32(tmem + lane_base + 64u * tb + 32u, P1);
+      uint32_t P[32];
+      tmem_ld32(tmem + lane_base + 64u * tb + 32u * par, P);
       tmem_wait_ld();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms->tempty[tb]);
-      const int64_t jl = (int64_t)u * kDmEntries + 2 * tid;   // chunk-relative index of entry 2r
-      uint32_t sc2 = 0x7f7f7f7fu;
-      if (jl + 1 < c1 - c0) sc2 = *reinterpret_cast<const uint32_t*>(sm + kDmSOff + 2 * jl);
-      else if (jl < c1 - c0) sc2 = 0x7f7f0000u | reinterpret_cast<const uint16_t*>(sm + kDmSOff)[jl];
-      const uint32_t sa = sc2 & 0xffffu, sb = sc2 >> 16;
-      float s0 = 0.0f, s1 = 0.0f;
-      if (fast_of(sa) && fast_of(sb)) {
-        // both entries in one pass over the heads: the head's factors read once,
-        // two independent chains (each entry's arithmetic as in every other indexer kernel)
-        const int X00 = (int)(sa & 0xffu) << 23, X01 = (int)((sa >> 8) & 0xffu) << 23;
-        const int X10 = (int)(sb & 0xffu) << 23, X11 = (int)((sb >> 8) & 0xffu) << 23;
+      const int64_t jl = (int64_t)u * kDmEntries + 2 * r + par;   // chunk-relative index of the entry
+      const bool valid = jl < n;
+      const uint32_t sc = valid ? (uint32_t)reinterpret_cast<const uint16_t*>(sm + kDmSOff)[jl] : 0x7f7fu;
+      const int x0 = (int)(sc & 0xffu), x1 = (int)((sc >> 8) & 0xffu);
+      float sv = 0.0f;
+      if (qlo0 + x0 >= 27 && qhi0 + x0 <= 227 && qlo1 + x1 >= 27 && qhi1 + x1 <= 227) {
+        const int X0 = x0 << 23, X1 = x1 << 23;
 #pragma unroll
         for (int h = 0; h < kDtHeads; ++h) {
           if (h < HI) {
             const int4 hx = ms->hx[h];
-            const float d0 = __fmaf_rn(__uint_as_float(P0[h]), __int_as_float(hx.x + X00),
-                                       __fmul_rn(__uint_as_float(P0[16 + h]), __int_as_float(hx.y + X01)));
-            const float d1 = __fmaf_rn(__uint_as_float(P1[h]), __int_as_float(hx.x + X10),
-                                       __fmul_rn(__uint_as_float(P1[16 + h]), __int_as_float(hx.y + X11)));
-            s0 = __fmaf_rn(__int_as_float(hx.z), fmaxf(d0, 0.0f), s0);
-            s1 = __fmaf_rn(__int_as_float(hx.z), fmaxf(d1, 0.0f), s1);
+            const float d = __fmaf_rn(__uint_as_float(P[h]), __int_as_float(hx.x + X0),
+                                      __fmul_rn(__uint_as_float(P[16 + h]), __int_as_float(hx.y + X1)));
+            sv = __fmaf_rn(__int_as_float(hx.z), fmaxf(d, 0.0f), sv);
           }
         }
       } else {
-        s0 = score_slow(P0, sa);
-        s1 = score_slow(P1, sb);
-      }
-      const int64_t j = c0 + jl;
-      if (jl + 1 < c1 - c0) {
-        *reinterpret_cast<float2*>(scores + row * N + j) = make_float2(s0, s1);
-        if (hist) {
-          atomicAdd(hist_s + to_key_bin(s0), 1u);
-          atomicAdd(hist_s + to_key_bin(s1), 1u);
+#pragma unroll
+        for (int h = 0; h < kDtHeads; ++h) {
+          if (h < HI) {
+            const int4 hx = ms->hx[h];
+            const float d = __fadd_rn(scale_pow2(__uint_as_float(P[h]), (hx.x >> 23) + x0 - 127),
+                                      scale_pow2(__uint_as_float(P[16 + h]), (hx.y >> 23) + x1 - 127));
+            sv = __fmaf_rn(__int_as_float(hx.z), d > 0.0f ? d : 0.0f, sv);
+          }
         }
-      } else if (jl < c1 - c0) {
-        scores[row * N + j] = s0;
-        if (hist) atomicAdd(hist_s + to_key_bin(s0), 1u);
+      }
+      if (valid) {
+        scores[row * N + c0 + jl] = sv;
+        if (hist) atomicAdd(hist_s + to_key_bin(sv), 1u);
       }
     }
     if (!ok && lane == 0) flag_timeout(ws);
