@@ -976,19 +976,9 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
           }
         }
       }
-      if (valid) scores[row * N + c0 + jl] = sv;
-      if (hist) {
-        // one shared add per distinct bin of the warp: a tile's scores fall in
-        // few bins, and same-address adds of a warp are serialised
-        const uint32_t bin = to_key_bin(sv);
-        unsigned int pending = __ballot_sync(0xffffffffu, valid);
-        while (pending) {
-          const int leader = __ffs(pending) - 1;
-          const uint32_t lb = __shfl_sync(0xffffffffu, bin, leader);
-          const unsigned int same = __ballot_sync(0xffffffffu, valid && bin == lb);
-          if (lane == leader) atomicAdd(hist_s + lb, (unsigned int)__popc(same));
-          pending &= ~same;
-        }
+      if (valid) {
+        scores[row * N + c0 + jl] = sv;
+        if (hist) atomicAdd(hist_s + to_key_bin(sv), 1u);
       }
     }
     if (!ok && lane == 0) flag_timeout(ws);
