@@ -51,6 +51,7 @@ constexpr uint32_t kIxMiscOff = kIxKOff + kIxStages * kIxKTile;
 constexpr uint32_t kIxSmem = kIxMiscOff + 1024 + 1024;        // + slack for 1 KiB alignment
 
 constexpr uint32_t kIxWait = 1u << 20;
+constexpr uint32_t kIxSleepWait = 1u << 16;   // polls of up to 1 us each
 
 struct IxMisc {
   uint64_t q_full, k_full[kIxStages], k_empty[kIxStages], t_full[kIxBufs], t_empty[kIxBufs], drain;
@@ -838,7 +839,7 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       int u = 0;
       for (; u < ntiles; ++u) {
         const int s = u % kDmStages;
-        if (u >= kDmStages && !mbar_wait(&ms->empty[s], (uint32_t)(u / kDmStages - 1) & 1, kIxWait)) break;
+        if (u >= kDmStages && !mbar_wait_sleep(&ms->empty[s], (uint32_t)(u / kDmStages - 1) & 1, kIxSleepWait, 1000)) break;
         mbar_arrive_expect_tx(&ms->full[s], 8192);   // the box's global bytes: the gaps are neither written nor counted
         tma_load_2d(aA + s * 16384, &tm_k, 0, (int)(vrow0 + (int64_t)u * (kDmEntries / 2)), &ms->full[s]);
         if (u >= kDmStages && u + kDmStages < ntiles) prefetch_tile(u + kDmStages);
@@ -860,8 +861,8 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
     bool got = __all_sync(0xffffffffu, mbar_wait(&ms->qready, 0, kIxWait));
     for (int u = 0; u < ntiles && got; ++u) {
       const int s = u % kDmStages, tb = u % kDmTbufs;
-      got = mbar_wait(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxWait);
-      if (got && u >= kDmTbufs) got = mbar_wait(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxWait);
+      got = mbar_wait_sleep(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxSleepWait, 1000);
+      if (got && u >= kDmTbufs) got = mbar_wait_sleep(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxSleepWait, 1000);
       got = __all_sync(0xffffffffu, got);
       if (!got) break;
       fence_after_sync();
@@ -930,6 +931,16 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
     const int q4 = warp & 3, par = warp >> 2;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int r = 32 * q4 + lane;   // view row of this thread: entry 2r + par
+    // the heads' block exponents and weights, in registers for every tile
+    int hx0[kDtHeads], hx1[kDtHeads];
+    float hw[kDtHeads];
+#pragma unroll
+    for (int h = 0; h < kDtHeads; ++h) {
+      const int4 hx = h < HI ? ms->hx[h] : make_int4(0, 0, 0, 0);
+      hx0[h] = hx.x;
+      hx1[h] = hx.y;
+      hw[h] = __int_as_float(hx.z);
+    }
 
     auto to_key_bin = [&](float sv) -> uint32_t {
       uint32_t key = __float_as_uint(sv);
@@ -959,20 +970,18 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
 #pragma unroll
         for (int h = 0; h < kDtHeads; ++h) {
           if (h < HI) {
-            const int4 hx = ms->hx[h];
-            const float d = __fmaf_rn(__uint_as_float(P[h]), __int_as_float(hx.x + X0),
-                                      __fmul_rn(__uint_as_float(P[16 + h]), __int_as_float(hx.y + X1)));
-            sv = __fmaf_rn(__int_as_float(hx.z), fmaxf(d, 0.0f), sv);
+            const float d = __fmaf_rn(__uint_as_float(P[h]), __int_as_float(hx0[h] + X0),
+                                      __fmul_rn(__uint_as_float(P[16 + h]), __int_as_float(hx1[h] + X1)));
+            sv = __fmaf_rn(hw[h], fmaxf(d, 0.0f), sv);
           }
         }
       } else {
 #pragma unroll
         for (int h = 0; h < kDtHeads; ++h) {
           if (h < HI) {
-            const int4 hx = ms->hx[h];
-            const float d = __fadd_rn(scale_pow2(__uint_as_float(P[h]), (hx.x >> 23) + x0 - 127),
-                                      scale_pow2(__uint_as_float(P[16 + h]), (hx.y >> 23) + x1 - 127));
-            sv = __fmaf_rn(__int_as_float(hx.z), d > 0.0f ? d : 0.0f, sv);
+            const float d = __fadd_rn(scale_pow2(__uint_as_float(P[h]), (hx0[h] >> 23) + x0 - 127),
+                                      scale_pow2(__uint_as_float(P[16 + h]), (hx1[h] >> 23) + x1 - 127));
+            sv = __fmaf_rn(hw[h], d > 0.0f ? d : 0.0f, sv);
           }
         }
       }
