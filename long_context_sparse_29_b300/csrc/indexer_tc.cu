@@ -949,6 +949,13 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       return key >> (32 - kDtHistBits);
     };
     // ---- the epilogue of every tile: this thread's entry from its 32 block dots ----
+    // histogram bins of this thread's entries (two per register), added to the
+    // shared histogram after the last tile: shared atomics in the tile loop
+    // held up the next tile's shared-memory operations
+    constexpr int kBinRegs = kDmMaxChunk / kDmEntries / 2;
+    uint32_t bins[kBinRegs];
+#pragma unroll
+    for (int i = 0; i < kBinRegs; ++i) bins[i] = 0xffffffffu;   // 0xffff: no entry
     for (int u = 0; u < ntiles && ok; ++u) {
       const int tb = u % kDmTbufs;
       ok = __all_sync(0xffffffffu, mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDmTbufs) & 1, kIxWait));
@@ -987,7 +994,19 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       }
       if (valid) {
         scores[row * N + c0 + jl] = sv;
-        if (hist) atomicAdd(hist_s + to_key_bin(sv), 1u);
+        const uint32_t bn = to_key_bin(sv);
+#pragma unroll
+        for (int i = 0; i < kBinRegs; ++i) {   // register index fixed at compile time
+          if ((u >> 1) == i) bins[i] = (u & 1) ? ((bins[i] & 0xffffu) | (bn << 16)) : ((bins[i] & 0xffff0000u) | bn);
+        }
+      }
+    }
+    if (hist) {
+#pragma unroll
+      for (int i = 0; i < kBinRegs; ++i) {
+        const uint32_t lo = bins[i] & 0xffffu, hi = bins[i] >> 16;
+        if (lo != 0xffffu) atomicAdd(hist_s + lo, 1u);
+        if (hi != 0xffffu) atomicAdd(hist_s + hi, 1u);
       }
     }
     if (!ok && lane == 0) flag_timeout(ws);
