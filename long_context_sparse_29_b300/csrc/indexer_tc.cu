@@ -936,7 +936,7 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
     float hw[kDtHeads];
 #pragma unroll
     for (int h = 0; h < kDtHeads; ++h) {
-      const int4 hx = h < HI ? ms->hx[h] : make_int4(0, 0, 0, 0);
+      const int4 hx = h < HI ? ms->hx[h] : make_int4(0, 0, 0, 0);   // past HI: exponent 0, weight +0
       hx0[h] = hx.x;
       hx1[h] = hx.y;
       hw[h] = __int_as_float(hx.z);
@@ -949,13 +949,6 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       return key >> (32 - kDtHistBits);
     };
     // ---- the epilogue of every tile: this thread's entry from its 32 block dots ----
-    // histogram bins of this thread's entries (two per register), added to the
-    // shared histogram after the last tile: shared atomics in the tile loop
-    // held up the next tile's shared-memory operations
-    constexpr int kBinRegs = kDmMaxChunk / kDmEntries / 2;
-    uint32_t bins[kBinRegs];
-#pragma unroll
-    for (int i = 0; i < kBinRegs; ++i) bins[i] = 0xffffffffu;   // 0xffff: no entry
     for (int u = 0; u < ntiles && ok; ++u) {
       const int tb = u % kDmTbufs;
       ok = __all_sync(0xffffffffu, mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDmTbufs) & 1, kIxWait));
@@ -974,39 +967,25 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       float sv = 0.0f;
       if (qlo0 + x0 >= 27 && qhi0 + x0 <= 227 && qlo1 + x1 >= 27 && qhi1 + x1 <= 227) {
         const int X0 = x0 << 23, X1 = x1 << 23;
+        // heads past HI: zero query codes (block dots 0) and weight 0, so
+        // their terms add +0 to the non-negative sum -- no per-head branch
 #pragma unroll
         for (int h = 0; h < kDtHeads; ++h) {
-          if (h < HI) {
-            const float d = __fmaf_rn(__uint_as_float(P[h]), __int_as_float(hx0[h] + X0),
-                                      __fmul_rn(__uint_as_float(P[16 + h]), __int_as_float(hx1[h] + X1)));
-            sv = __fmaf_rn(hw[h], fmaxf(d, 0.0f), sv);
-          }
+          const float d = __fmaf_rn(__uint_as_float(P[h]), __int_as_float(hx0[h] + X0),
+                                    __fmul_rn(__uint_as_float(P[16 + h]), __int_as_float(hx1[h] + X1)));
+          sv = __fmaf_rn(hw[h], fmaxf(d, 0.0f), sv);
         }
       } else {
 #pragma unroll
         for (int h = 0; h < kDtHeads; ++h) {
-          if (h < HI) {
-            const float d = __fadd_rn(scale_pow2(__uint_as_float(P[h]), (hx0[h] >> 23) + x0 - 127),
-                                      scale_pow2(__uint_as_float(P[16 + h]), (hx1[h] >> 23) + x1 - 127));
-            sv = __fmaf_rn(hw[h], d > 0.0f ? d : 0.0f, sv);
-          }
+          const float d = __fadd_rn(scale_pow2(__uint_as_float(P[h]), (hx0[h] >> 23) + x0 - 127),
+                                    scale_pow2(__uint_as_float(P[16 + h]), (hx1[h] >> 23) + x1 - 127));
+          sv = __fmaf_rn(hw[h], d > 0.0f ? d : 0.0f, sv);
         }
       }
       if (valid) {
         scores[row * N + c0 + jl] = sv;
-        const uint32_t bn = to_key_bin(sv);
-#pragma unroll
-        for (int i = 0; i < kBinRegs; ++i) {   // register index fixed at compile time
-          if ((u >> 1) == i) bins[i] = (u & 1) ? ((bins[i] & 0xffffu) | (bn << 16)) : ((bins[i] & 0xffff0000u) | bn);
-        }
-      }
-    }
-    if (hist) {
-#pragma unroll
-      for (int i = 0; i < kBinRegs; ++i) {
-        const uint32_t lo = bins[i] & 0xffffu, hi = bins[i] >> 16;
-        if (lo != 0xffffu) atomicAdd(hist_s + lo, 1u);
-        if (hi != 0xffffu) atomicAdd(hist_s + hi, 1u);
+        if (hist) atomicAdd(hist_s + to_key_bin(sv), 1u);
       }
     }
     if (!ok && lane == 0) flag_timeout(ws);
