@@ -858,12 +858,12 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
     const uint32_t aA = smem_u32(sm + kDmAOff), aB = smem_u32(sm + kDmBOff);
     constexpr uint32_t id = idesc_e2m1(kDtThreads, kDtHeads);
     int issued = 0;
-    bool got = mbar_wait_warp(&ms->qready, 0, kIxWait);
+    bool got = __all_sync(0xffffffffu, mbar_wait(&ms->qready, 0, kIxWait));
     for (int u = 0; u < ntiles && got; ++u) {
       const int s = u % kDmStages, tb = u % kDmTbufs;
-      got = mbar_wait_warp_sleep(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxSleepWait, 1000);
-      if (got && u >= kDmTbufs)
-        got = mbar_wait_warp_sleep(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxSleepWait, 1000);
+      got = mbar_wait_sleep(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxSleepWait, 1000);
+      if (got && u >= kDmTbufs) got = mbar_wait_sleep(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxSleepWait, 1000);
+      got = __all_sync(0xffffffffu, got);
       if (!got) break;
       fence_after_sync();
       const uint64_t ad = sdesc_sw128(aA + s * 16384, 16, 1024), bd = sdesc_sw128(aB, 16, 1024);
@@ -951,7 +951,7 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
     // ---- the epilogue of every tile: this thread's entry from its 32 block dots ----
     for (int u = 0; u < ntiles && ok; ++u) {
       const int tb = u % kDmTbufs;
-      ok = mbar_wait_warp(&ms->tfull[tb], (uint32_t)(u / kDmTbufs) & 1, kIxWait);
+      ok = __all_sync(0xffffffffu, mbar_wait(&ms->tfull[tb], (uint32_t)(u / kDmTbufs) & 1, kIxWait));
       if (!ok) break;
       fence_after_sync();
       uint32_t P[32];

@@ -270,18 +270,5 @@ __device__ __forceinline__ bool mbar_wait_sleep(void* bar, uint32_t parity, uint
   return false;
 }
 
-// mbar_wait for a whole warp: lane 0 polls (the other lanes do not hit the
-// barrier word), the outcome is broadcast and the warp reconverges.
-__device__ __forceinline__ bool mbar_wait_warp(void* bar, uint32_t parity, uint32_t limit) {
-  bool ok = false;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, limit);
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-}
-__device__ __forceinline__ bool mbar_wait_warp_sleep(void* bar, uint32_t parity, uint32_t limit, uint32_t hint_ns) {
-  bool ok = false;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_sleep(bar, parity, limit, hint_ns);
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-}
-
 }  // namespace tc
 }  // namespace csa
