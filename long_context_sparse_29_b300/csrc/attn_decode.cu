@@ -236,7 +236,7 @@ decode_gather_kernel(const DParams p) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_xg) {
+                   const __grid_constant__ CUtensorMap tm_xg, const __grid_constant__ CUtensorMap tm_po) {
   pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -573,10 +573,11 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     group_vote(false);
     const bool bad = group_vote(__any_sync(0xffffffffu, fail || stop || vabort(ms))) != 0;
     // O^T lanes are dims: thread (qd, lane) holds dim 128 mt + 32 qd + lane of
-    // heads 64 mt .. ; stored as [dim][head] bf16 rows of 128 bytes
-    __nv_bfloat16* po = p.part_o + item * (int64_t)(kH * kD);
+    // every head; the partial is [dim][head] bf16 rows of 128 bytes, staged in
+    // the query's shared memory (free once o_full has passed) with the
+    // 128-byte swizzle and written by four TMA boxes of 128 dims
 #pragma unroll 1
-    for (int mt = 0; mt < 4; ++mt) {
+    for (int mt = 0; mt < 4 && !bad; ++mt) {   // (a failed item leaves its partial alone: MMAs may still read sQ)
       // both head halves of dim block mt: two TMEM loads in flight per wait
       uint32_t o[2][32];
       if (any_keys && !bad) {
@@ -596,16 +597,24 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(f0, f1);
           pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
         }
-        uint4* dst = reinterpret_cast<uint4*>(po + (int64_t)d * kH + 32 * hh);
+        const uint32_t r = (uint32_t)(d & 127);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(sQ + mt * 16384 + sw128(r, (uint32_t)(4 * hh + j))) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
       }
     }
     if (bad) fail = true;
-    // the partial is visible to the row's other items (read there by bulk
-    // copies: the async proxy) before the arrival below
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    __threadfence();
+    fence_proxy_async();
+    group_vote(false);   // the whole partial is staged
+    if (tid == 0 && !bad) {
+      for (int mt = 0; mt < 4; ++mt) tma_store_2d(&tm_po, smem_u32(sQ) + mt * 16384, 0, (int)(item * kD + 128 * mt));
+      bulk_commit_wait_all();
+      // the partial is visible to the row's other items (read there by bulk
+      // copies: the async proxy) before the arrival below
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __threadfence();
+    }
   }
   if (fail) {
     ms->abort = 1;
@@ -660,45 +669,49 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     if (tid == 0) flag_timeout(p.ws);
     return;   // (a copy still in flight lands in memory nobody reads again)
   }
-  // per head: the splits' weights 2^(m_s - M) l_s, then 1 / L
+  // per head: the splits' weights 2^(m_s - M) l_s (M the maximum over the
+  // splits: five partial maxima per head, then every weight in parallel)
   float* wgt = reinterpret_cast<float*>(sm + sl_off + (((uint32_t)ns * nd * kH * 2 + 1023) & ~1023u));
-  float* Ls = wgt + (size_t)ns * kH;
-  if (tid < kH) {
-    float M = -INFINITY;
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml_s[s * kH + tid].x);
-    float L = 0.0f;
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) {
-      const float2 v = ml_s[s * kH + tid];
-      const float w = v.x == -INFINITY ? 0.0f : exp2f(v.x - M) * v.y;
-      wgt[s * kH + tid] = w;
-      L += w;
-    }
-    Ls[tid] = L > 0.0f ? 1.0f / L : 0.0f;
-    if (split == 0 && p.lse) p.lse[row * kH + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-  }
-  __syncthreads();
-  float* cs = Ls + kH;   // the RoPE row of t: 32 cos, 32 sin
+  float* red = wgt + (size_t)ns * kH;   // [5][64] partial maxima
+  float* cs = red + 5 * kH;             // the RoPE row of t: 32 cos, 32 sin
   float* sn = cs + 32;
+  {
+    const int g = tid >> 6, h = tid & (kH - 1);   // kThreads = 5 x 64
+    float M = -INFINITY;
+    for (int s = g; s < ns; s += 5) M = fmaxf(M, ml_s[s * kH + h].x);
+    red[g * kH + h] = M;
+  }
   if (tid >= 64 && tid < 96) {
     cs[tid - 64] = rope_c;
     sn[tid - 64] = rope_s;
   }
   __syncthreads();
+  for (int i = tid; i < ns * kH; i += kThreads) {
+    const int h = i & (kH - 1);
+    const float M = fmaxf(fmaxf(fmaxf(red[h], red[kH + h]), fmaxf(red[2 * kH + h], red[3 * kH + h])), red[4 * kH + h]);
+    const float2 v = ml_s[i];
+    wgt[i] = v.x == -INFINITY ? 0.0f : exp2f(v.x - M) * v.y;
+  }
+  __syncthreads();
   // thread: a pair of dims (d, d + 1) of one head, weighted sum in split order
   for (int u = tid; u < (nd >> 1) * kH; u += kThreads) {
     const int h = u % kH, dl = 2 * (u / kH), d = d0 + dl;
-    float o0 = 0.0f, o1 = 0.0f;
+    float o0 = 0.0f, o1 = 0.0f, L = 0.0f;
 #pragma unroll 4
     for (int s = 0; s < ns; ++s) {
       const float w = wgt[s * kH + h];
       const __nv_bfloat16* src = sl_s + ((size_t)s * nd + dl) * kH + h;
       o0 = __fmaf_rn(w, __bfloat162float(src[0]), o0);
       o1 = __fmaf_rn(w, __bfloat162float(src[kH]), o1);
+      L += w;   // split order, as every thread of head h
     }
-    o0 *= Ls[h];
-    o1 *= Ls[h];
+    if (split == 0 && dl == 0 && p.lse) {
+      const float M = fmaxf(fmaxf(fmaxf(red[h], red[kH + h]), fmaxf(red[2 * kH + h], red[3 * kH + h])), red[4 * kH + h]);
+      p.lse[row * kH + h] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    o0 *= inv;
+    o1 *= inv;
     if (d >= kMixDn) {
       const int pi = (d - kMixDn) >> 1;
       const float y0 = o0 * cs[pi] + o1 * sn[pi];
@@ -792,7 +805,7 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   base += al256((size_t)rows * 4);
   p.kp = attn_decode_kp(a.max_keys);
   p.xg = reinterpret_cast<__nv_bfloat16*>(base);
-  CUtensorMap tm_q, tm_xg;
+  CUtensorMap tm_q, tm_xg, tm_po;
   {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorInvalidValue;
@@ -801,6 +814,13 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
     const cuuint32_t box[2] = {64u, 64u};
     const cuuint32_t estr[2] = {1u, 1u};
     if (fn(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    const cuuint64_t pdims[2] = {(cuuint64_t)kH, (cuuint64_t)(items * kD)};
+    const cuuint64_t pstrides[1] = {(cuuint64_t)kH * 2};
+    const cuuint32_t pbox[2] = {(cuuint32_t)kH, 128u};
+    if (fn(&tm_po, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.part_o, pdims, pstrides, pbox, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -827,7 +847,7 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   attrs[0].val.cooperative = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, p, tm_q, tm_xg);
+  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, p, tm_q, tm_xg, tm_po);
   return e;
 }
 
