@@ -61,15 +61,14 @@ constexpr uint32_t kTmemO = 0;       // O^T: 4 blocks of 64 columns (heads); lan
 constexpr uint32_t kTmemS = 256;     // S: 2 buffers of 64 columns (keys); M = 64 layout
 
 constexpr uint32_t kWaitLimit = 1u << 20;     // suspending polls of one mbarrier wait
-constexpr uint32_t kGridWaitLimit = 1u << 22; // polls of the row barrier (64 ns naps)
+constexpr int kMaxSplits = 16;                // splits of a row = CTAs of one cluster
 constexpr float kLazy = 8.0f;
 
 struct Misc {
   uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
-  uint64_t q_full, q_ready, o_full, drain[2], merge_in;
+  uint64_t q_full, q_ready, o_full, drain[2];
   uint32_t tmem;
   int abort;
-  int go;                           // the row barrier passed
   alignas(16) float alpha[2][kH];   // per-head rescale factors of a tile, double-buffered
 };
 static_assert(sizeof(Misc) <= 2048, "Misc overflows its smem slot");
@@ -100,10 +99,7 @@ struct DParams {
   __nv_bfloat16* out;       // [rows, 64, 512]
   float* lse;               // [rows, 64] or NULL
   void* ws;                 // status flags
-  int nsplit;
-  __nv_bfloat16* part_o;    // [items, 512 dims, 64 heads] normalised partial outputs
-  float* part_ml;           // [items, 64, 2]: running max (log2 units), sum
-  int* arrive;              // [rows] items that finished their partial (zero at launch)
+  int nsplit;               // items per row = the cluster size
   __nv_bfloat16* xg;        // [rows, kp, 512] every row's keys in bf16, in order, zero past them
   int64_t kp;               // key slots per row of xg (a multiple of the tile)
   int* ecount;              // [rows] valid selected entries of each row (sparse)
@@ -236,7 +232,7 @@ decode_gather_kernel(const DParams p) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_xg, const __grid_constant__ CUtensorMap tm_po) {
+                   const __grid_constant__ CUtensorMap tm_xg) {
   pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -261,7 +257,6 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
 
   if (tid == 0) {
     ms->abort = 0;
-    ms->go = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->kv_full[i], 1);    // the tile's TMA boxes (one arrive with their byte count)
       mbar_init(&ms->kv_empty[i], 1);
@@ -273,7 +268,6 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->drain[0], 1);
     mbar_init(&ms->drain[1], 1);
-    mbar_init(&ms->merge_in, 1);
     mbar_fence_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&ms->tmem, kTmemCols);
@@ -556,16 +550,16 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     const bool any_keys = thi > tlo;
     if (any_keys && !stop && !fail && !mbar_wait(&ms->o_full, 0, kWaitLimit)) fail = true;
     fence_after_sync();
+    // this item's statistics per head, (m, l), in P buffer 1 (free now): the
+    // row's other items read them there
+    float2* ml_own = reinterpret_cast<float2*>(sP + 8192);
     if (leader) {
-      float* ml = p.part_ml + item * (kH * 2);
-      ml[2 * ha] = any_keys ? ma : -INFINITY;
-      ml[2 * ha + 1] = any_keys ? la : 0.0f;
-      ml[2 * hb] = any_keys ? mb : -INFINITY;
-      ml[2 * hb + 1] = any_keys ? lb : 0.0f;
+      ml_own[ha] = make_float2(any_keys ? ma : -INFINITY, any_keys ? la : 0.0f);
+      ml_own[hb] = make_float2(any_keys ? mb : -INFINITY, any_keys ? lb : 0.0f);
     }
-    // 1 / l per head through shared memory (the P buffers are free now)
+    // 1 / l per head through shared memory (P buffer 0)
     float* inv_s = reinterpret_cast<float*>(sP);
-    group_vote(false);   // every softmax warp is past its last P (its PV may still read P? no: o_full)
+    group_vote(false);   // every softmax warp is past its last P
     if (leader) {
       inv_s[ha] = la > 0.0f ? 1.0f / la : 0.0f;
       inv_s[hb] = lb > 0.0f ? 1.0f / lb : 0.0f;
@@ -573,14 +567,15 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     group_vote(false);
     const bool bad = group_vote(__any_sync(0xffffffffu, fail || stop || vabort(ms))) != 0;
     // O^T lanes are dims: thread (qd, lane) holds dim 128 mt + 32 qd + lane of
-    // every head; the partial is [dim][head] bf16 rows of 128 bytes, staged in
-    // the query's shared memory (free once o_full has passed) with the
-    // 128-byte swizzle and written by four TMA boxes of 128 dims
+    // every head; the normalised partial stays in the query's shared memory
+    // (free once o_full has passed) as [dim][head] bf16 rows of 128 bytes,
+    // 16-byte chunk c of row d at chunk c ^ (d mod 8), where the row's other
+    // items read it
 #pragma unroll 1
-    for (int mt = 0; mt < 4 && !bad; ++mt) {   // (a failed item leaves its partial alone: MMAs may still read sQ)
+    for (int mt = 0; mt < 4 && !bad; ++mt) {   // (a failed item leaves sQ alone: MMAs may still read it)
       // both head halves of dim block mt: two TMEM loads in flight per wait
       uint32_t o[2][32];
-      if (any_keys && !bad) {
+      if (any_keys) {
         tmem_ld32(tmem + tq_lane + kTmemO + 64u * mt, o[0]);
         tmem_ld32(tmem + tq_lane + kTmemO + 64u * mt + 32u, o[1]);
         tmem_wait_ld();
@@ -592,29 +587,18 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int h0 = 32 * hh + 2 * j;
-          const float f0 = (any_keys && !bad) ? __uint_as_float(o[hh][2 * j]) * inv_s[h0] : 0.0f;
-          const float f1 = (any_keys && !bad) ? __uint_as_float(o[hh][2 * j + 1]) * inv_s[h0 + 1] : 0.0f;
+          const float f0 = any_keys ? __uint_as_float(o[hh][2 * j]) * inv_s[h0] : 0.0f;
+          const float f1 = any_keys ? __uint_as_float(o[hh][2 * j + 1]) * inv_s[h0 + 1] : 0.0f;
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(f0, f1);
           pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
         }
-        const uint32_t r = (uint32_t)(d & 127);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(sQ + mt * 16384 + sw128(r, (uint32_t)(4 * hh + j))) =
+          *reinterpret_cast<uint4*>(sQ + (uint32_t)d * 128u + ((((uint32_t)(4 * hh + j)) ^ ((uint32_t)d & 7u)) << 4)) =
               make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
       }
     }
     if (bad) fail = true;
-    fence_proxy_async();
-    group_vote(false);   // the whole partial is staged
-    if (tid == 0 && !bad) {
-      for (int mt = 0; mt < 4; ++mt) tma_store_2d(&tm_po, smem_u32(sQ) + mt * 16384, 0, (int)(item * kD + 128 * mt));
-      bulk_commit_wait_all();
-      // the partial is visible to the row's other items (read there by bulk
-      // copies: the async proxy) before the arrival below
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      __threadfence();
-    }
   }
   if (fail) {
     ms->abort = 1;
@@ -625,102 +609,84 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // ---- the row's items meet: every partial of the row is written ----
-  if (tid == 0) {
-    atomicAdd(p.arrive + row, 1);
-    bool ok = false;
-    for (uint32_t it = 0; it < kGridWaitLimit; ++it) {
-      if (*reinterpret_cast<volatile int*>(p.arrive + row) >= p.nsplit) {
-        ok = true;
-        break;
-      }
-      __nanosleep(64);
-    }
-    __threadfence();
-    if (!ok) flag_timeout(p.ws);
-    ms->go = ok ? 1 : 0;
-  }
-  __syncthreads();
-  if (!ms->go) return;
-  // ---- merge this item's slice of the row's dims over the splits ----
+  // ---- the row's items meet: every partial of the row is staged (cluster barrier) ----
+  cluster_sync_all();
+  // ---- merge this item's slice of the row's dims over the splits, reading
+  // the other items' shared memory ----
   // dims of this slice: [d0, d1), even bounds (RoPE pairs stay together)
   const int ns = p.nsplit;
   const int dp = ((kD + ns - 1) / ns + 1) & ~1;
   const int d0 = min(kD, split * dp), d1 = min(kD, d0 + dp);
   const int nd = d1 - d0;
-  // shared memory is free now: the row's statistics [ns][64] (m, l) at 0,
-  // this slice's partial rows [ns][nd][64 heads] bf16 after them, staged by
-  // bulk copies (all in flight together)
-  const uint32_t ml_bytes = (uint32_t)ns * kH * 8;
-  const uint32_t sl_off = (ml_bytes + 1023) & ~1023u;
-  const float2* ml_s = reinterpret_cast<const float2*>(sm);
-  const __nv_bfloat16* sl_s = reinterpret_cast<const __nv_bfloat16*>(sm + sl_off);
-  if (tid == 0) {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    mbar_arrive_expect_tx(&ms->merge_in, ml_bytes + (uint32_t)ns * nd * kH * 2);
-    bulk_copy_g2s(smem_u32(sm), p.part_ml + row * (int64_t)ns * kH * 2, ml_bytes, &ms->merge_in);
-    if (nd > 0)
-      for (int s = 0; s < ns; ++s)
-        bulk_copy_g2s(smem_u32(sm + sl_off + (uint32_t)s * nd * kH * 2),
-                      p.part_o + (row * (int64_t)ns + s) * (kH * kD) + (int64_t)d0 * kH, (uint32_t)nd * kH * 2,
-                      &ms->merge_in);
-  }
-  if (!mbar_wait(&ms->merge_in, 0, kWaitLimit)) {
-    if (tid == 0) flag_timeout(p.ws);
-    return;   // (a copy still in flight lands in memory nobody reads again)
-  }
-  // per head: the splits' weights 2^(m_s - M) l_s (M the maximum over the
-  // splits: five partial maxima per head, then every weight in parallel)
-  float* wgt = reinterpret_cast<float*>(sm + sl_off + (((uint32_t)ns * nd * kH * 2 + 1023) & ~1023u));
-  float* red = wgt + (size_t)ns * kH;   // [5][64] partial maxima
-  float* cs = red + 5 * kH;             // the RoPE row of t: 32 cos, 32 sin
+  // scratch in the KV slots (only sQ and sP are read by the other items)
+  float2* mls = reinterpret_cast<float2*>(sKV);                  // [ns][64] (m, l)
+  float* wgt = reinterpret_cast<float*>(sKV + kMaxSplits * kH * 8);   // [ns][64]
+  float* Linv = wgt + kMaxSplits * kH;                           // [64]
+  float* cs = Linv + kH;                                         // the RoPE row of t: 32 cos, 32 sin
   float* sn = cs + 32;
-  {
-    const int g = tid >> 6, h = tid & (kH - 1);   // kThreads = 5 x 64
-    float M = -INFINITY;
-    for (int s = g; s < ns; s += 5) M = fmaxf(M, ml_s[s * kH + h].x);
-    red[g * kH + h] = M;
-  }
+  for (int i = tid; i < ns * kH; i += kThreads)
+    mls[i] = ld_cluster_f2(map_cluster(sP + 8192 + (i & (kH - 1)) * 8, (uint32_t)(i / kH)));
   if (tid >= 64 && tid < 96) {
     cs[tid - 64] = rope_c;
     sn[tid - 64] = rope_s;
   }
   __syncthreads();
-  for (int i = tid; i < ns * kH; i += kThreads) {
-    const int h = i & (kH - 1);
-    const float M = fmaxf(fmaxf(fmaxf(red[h], red[kH + h]), fmaxf(red[2 * kH + h], red[3 * kH + h])), red[4 * kH + h]);
-    const float2 v = ml_s[i];
-    wgt[i] = v.x == -INFINITY ? 0.0f : exp2f(v.x - M) * v.y;
+  // per head: the splits' weights 2^(m_s - M) l_s and their sum L in split order
+  if (tid < kH) {
+    float M = -INFINITY;
+    for (int c = 0; c < ns; ++c) M = fmaxf(M, mls[c * kH + tid].x);
+    float L = 0.0f;
+    for (int c = 0; c < ns; ++c) {
+      const float2 v = mls[c * kH + tid];
+      const float w = v.x == -INFINITY ? 0.0f : exp2f(v.x - M) * v.y;
+      wgt[c * kH + tid] = w;
+      L += w;
+    }
+    Linv[tid] = L > 0.0f ? 1.0f / L : 0.0f;
+    if (split == 0 && p.lse) p.lse[row * kH + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();
-  // thread: a pair of dims (d, d + 1) of one head, weighted sum in split order
-  for (int u = tid; u < (nd >> 1) * kH; u += kThreads) {
-    const int h = u % kH, dl = 2 * (u / kH), d = d0 + dl;
-    float o0 = 0.0f, o1 = 0.0f, L = 0.0f;
+  // thread: a pair of dims (d, d + 1) of eight heads (one 16-byte chunk of
+  // each of the two rows in every split), weighted sum in split order
+  for (int u = tid; u < (nd >> 1) * 8; u += kThreads) {
+    const int hg = u & 7, d = d0 + 2 * (u >> 3);
+    const uint32_t r0 = smem_u32(sQ) + (uint32_t)d * 128u + ((((uint32_t)hg) ^ ((uint32_t)d & 7u)) << 4);
+    const uint32_t r1 = smem_u32(sQ) + (uint32_t)(d + 1) * 128u + ((((uint32_t)hg) ^ ((uint32_t)(d + 1) & 7u)) << 4);
+    float o0[8], o1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o0[j] = o1[j] = 0.0f;
 #pragma unroll 4
-    for (int s = 0; s < ns; ++s) {
-      const float w = wgt[s * kH + h];
-      const __nv_bfloat16* src = sl_s + ((size_t)s * nd + dl) * kH + h;
-      o0 = __fmaf_rn(w, __bfloat162float(src[0]), o0);
-      o1 = __fmaf_rn(w, __bfloat162float(src[kH]), o1);
-      L += w;   // split order, as every thread of head h
+    for (int c = 0; c < ns; ++c) {
+      const uint4 x0 = ld_cluster_v4(map_cluster_u32(r0, (uint32_t)c));
+      const uint4 x1 = ld_cluster_v4(map_cluster_u32(r1, (uint32_t)c));
+      const uint32_t a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a0[j]));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a1[j]));
+        const float w0 = wgt[c * kH + 8 * hg + 2 * j], w1 = wgt[c * kH + 8 * hg + 2 * j + 1];
+        o0[2 * j] = __fmaf_rn(w0, f0.x, o0[2 * j]);
+        o0[2 * j + 1] = __fmaf_rn(w1, f0.y, o0[2 * j + 1]);
+        o1[2 * j] = __fmaf_rn(w0, f1.x, o1[2 * j]);
+        o1[2 * j + 1] = __fmaf_rn(w1, f1.y, o1[2 * j + 1]);
+      }
     }
-    if (split == 0 && dl == 0 && p.lse) {
-      const float M = fmaxf(fmaxf(fmaxf(red[h], red[kH + h]), fmaxf(red[2 * kH + h], red[3 * kH + h])), red[4 * kH + h]);
-      p.lse[row * kH + h] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int h = 8 * hg + j;
+      float y0 = o0[j] * Linv[h], y1 = o1[j] * Linv[h];
+      if (d >= kMixDn) {
+        const int pi = (d - kMixDn) >> 1;
+        const float z0 = y0 * cs[pi] + y1 * sn[pi];
+        const float z1 = -y0 * sn[pi] + y1 * cs[pi];
+        y0 = z0;
+        y1 = z1;
+      }
+      *reinterpret_cast<__nv_bfloat162*>(p.out + (row * kH + h) * (int64_t)kD + d) = __floats2bfloat162_rn(y0, y1);
     }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    o0 *= inv;
-    o1 *= inv;
-    if (d >= kMixDn) {
-      const int pi = (d - kMixDn) >> 1;
-      const float y0 = o0 * cs[pi] + o1 * sn[pi];
-      const float y1 = -o0 * sn[pi] + o1 * cs[pi];
-      o0 = y0;
-      o1 = y1;
-    }
-    *reinterpret_cast<__nv_bfloat162*>(p.out + (row * kH + h) * (int64_t)kD + d) = __floats2bfloat162_rn(o0, o1);
   }
+  // every item of the row has read this one's shared memory before it exits
+  cluster_sync_all();
 }
 
 // cuTensorMapEncodeTiled, fetched from the driver once
@@ -748,12 +714,50 @@ size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
-// Splits per row: as many as fill the SMs once, at most one per key tile.
+namespace {
+
+// The largest cluster of attention CTAs (one per SM: 227 KiB of shared
+// memory each) the device can schedule: 16 when it reports room for at
+// least one, else the portable 8.
+int decode_cluster_cap() {
+  static PerDevice cap;
+  return cap.get([] {
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel),
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kMaxSplits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kMaxSplits;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(attn_decode_kernel), &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 8;
+    }
+    return n >= 1 ? kMaxSplits : 8;
+  });
+}
+
+}  // namespace
+
+// Splits per row (the CTAs of one cluster): as many as fill the SMs once, at
+// most one per key tile and at most the schedulable cluster size.
 int attn_decode_splits(int64_t rows, int64_t max_keys) {
   const int sms = device_sms() > 0 ? device_sms() : 148;
   const int64_t tiles = (max_keys + kTile - 1) / kTile;
   int64_t s = sms / (rows > 0 ? rows : 1);
   if (s > tiles) s = tiles;
+  const int cap = decode_cluster_cap();
+  if (s > cap) s = cap;
   return (int)(s < 1 ? 1 : s);
 }
 
@@ -765,9 +769,7 @@ bool attn_decode_applies(int H, int D, int R, int64_t rows, int k, bool sparse) 
 int64_t attn_decode_kp(int64_t max_keys) { return (max_keys + kTile - 1) / kTile * kTile; }
 
 size_t attn_decode_workspace(int64_t rows, int64_t max_keys) {
-  const int64_t items = rows * attn_decode_splits(rows, max_keys);
-  return al256((size_t)items * kH * kD * 2) + al256((size_t)items * kH * 2 * 4) + al256((size_t)rows * 4) +
-         al256((size_t)rows * 4) + al256((size_t)rows * attn_decode_kp(max_keys) * kD * 2);
+  return al256((size_t)rows * 4) + al256((size_t)rows * attn_decode_kp(max_keys) * kD * 2);
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
@@ -795,17 +797,11 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   p.nsplit = attn_decode_splits(rows, a.max_keys);
   const int64_t items = rows * p.nsplit;
   uint8_t* base = reinterpret_cast<uint8_t*>(a.ws) + kWsHeader;
-  p.part_o = reinterpret_cast<__nv_bfloat16*>(base);
-  base += al256((size_t)items * kH * kD * 2);
-  p.part_ml = reinterpret_cast<float*>(base);
-  base += al256((size_t)items * kH * 2 * 4);
-  p.arrive = reinterpret_cast<int*>(base);
-  base += al256((size_t)rows * 4);
   p.ecount = reinterpret_cast<int*>(base);
   base += al256((size_t)rows * 4);
   p.kp = attn_decode_kp(a.max_keys);
   p.xg = reinterpret_cast<__nv_bfloat16*>(base);
-  CUtensorMap tm_q, tm_xg, tm_po;
+  CUtensorMap tm_q, tm_xg;
   {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorInvalidValue;
@@ -817,37 +813,33 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    const cuuint64_t pdims[2] = {(cuuint64_t)kH, (cuuint64_t)(items * kD)};
-    const cuuint64_t pstrides[1] = {(cuuint64_t)kH * 2};
-    const cuuint32_t pbox[2] = {(cuuint32_t)kH, 128u};
-    if (fn(&tm_po, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.part_o, pdims, pstrides, pbox, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
     const cuuint64_t gdims[2] = {(cuuint64_t)kD, (cuuint64_t)(rows * p.kp)};
     if (fn(&tm_xg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.xg, gdims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
         CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaMemsetAsync(p.arrive, 0, (size_t)rows * 4, st);
+  cudaError_t e =
+      launch_pdl(decode_gather_kernel, dim3((unsigned)(p.kp / kTile), (unsigned)rows), dim3(kGatherThreads), 0, st, p);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_gather_kernel, dim3((unsigned)(p.kp / kTile), (unsigned)rows), dim3(kGatherThreads), 0, st, p);
-  if (e != cudaSuccess) return e;
-  static PerDevice attr;
-  smem_limit_once(attr, reinterpret_cast<const void*>(attn_decode_kernel), (int)kSmemBytes);
-  // every item resident at once (the row barrier waits on its siblings)
+  decode_cluster_cap();   // the kernel's shared-memory and cluster-size attributes, set once per device
+  // one cluster per row: its items meet at cluster barriers and merge through
+  // each other's shared memory
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)items);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeCooperative;
-  attrs[0].val.cooperative = 1;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = (unsigned)p.nsplit;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, p, tm_q, tm_xg, tm_po);
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, p, tm_q, tm_xg);
   return e;
 }
 
