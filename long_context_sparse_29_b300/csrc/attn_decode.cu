@@ -66,7 +66,7 @@ constexpr float kLazy = 8.0f;
 
 struct Misc {
   uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
-  uint64_t q_full, q_ready, o_full, drain[2];
+  uint64_t q_full, q_ready, o_full, drain[2], recv;
   uint32_t tmem;
   int abort;
   alignas(16) float alpha[2][kH];   // per-head rescale factors of a tile, double-buffered
@@ -268,6 +268,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->drain[0], 1);
     mbar_init(&ms->drain[1], 1);
+    mbar_init(&ms->recv, 1);          // the row's partial slices and statistics pushed by its items
     mbar_fence_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&ms->tmem, kTmemCols);
@@ -609,56 +610,68 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // ---- the row's items meet: every partial of the row is staged (cluster barrier) ----
+  // ---- the row's items meet: every partial of the row is staged, every
+  // item's KV slots are free and its barriers initialised (cluster barrier) ----
   cluster_sync_all();
-  // ---- merge this item's slice of the row's dims over the splits, reading
-  // the other items' shared memory ----
-  // dims of this slice: [d0, d1), even bounds (RoPE pairs stay together)
+  // ---- each item pushes to item c the rows of item c's dim slice and its
+  // statistics; then merges its own slice over the splits ----
+  // dims of a slice: [d0, d1), even bounds (RoPE pairs stay together)
   const int ns = p.nsplit;
   const int dp = ((kD + ns - 1) / ns + 1) & ~1;
   const int d0 = min(kD, split * dp), d1 = min(kD, d0 + dp);
   const int nd = d1 - d0;
-  // scratch in the KV slots (only sQ and sP are read by the other items)
-  float2* mls = reinterpret_cast<float2*>(sKV);                  // [ns][64] (m, l)
-  float* wgt = reinterpret_cast<float*>(sKV + kMaxSplits * kH * 8);   // [ns][64]
-  float* Linv = wgt + kMaxSplits * kH;                           // [64]
-  float* cs = Linv + kH;                                         // the RoPE row of t: 32 cos, 32 sin
+  // receive area in the KV slots: [ns][dp] partial rows of 128 bytes, then
+  // [ns][64] (m, l); scratch after it
+  uint8_t* rcv = sKV;
+  float2* mls = reinterpret_cast<float2*>(sKV + 73728);
+  float* Ms = reinterpret_cast<float*>(sKV + 73728 + kMaxSplits * kH * 8);   // [64]
+  float* wgt = Ms + kH;                                                       // [ns][64]
+  float* cs = wgt + kMaxSplits * kH;   // the RoPE row of t: 32 cos, 32 sin
   float* sn = cs + 32;
-  for (int i = tid; i < ns * kH; i += kThreads)
-    mls[i] = ld_cluster_f2(map_cluster(sP + 8192 + (i & (kH - 1)) * 8, (uint32_t)(i / kH)));
+  static_assert((kMaxSplits * ((kD + kMaxSplits - 1) / kMaxSplits + 2)) * 128 <= 73728, "receive rows");
+  static_assert(73728 + kMaxSplits * kH * 8 + (kH + kMaxSplits * kH + 64) * 4 <= 131072, "merge scratch");
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&ms->recv, (uint32_t)ns * ((uint32_t)nd * 128u + kH * 8u));
+    for (int c = 0; c < ns; ++c) {
+      const int c0 = min(kD, c * dp), c1 = min(kD, c0 + dp);
+      const uint32_t bar = map_cluster(&ms->recv, (uint32_t)c);
+      if (c1 > c0)
+        bulk_push_cluster(map_cluster(rcv + (uint32_t)split * dp * 128u, (uint32_t)c), smem_u32(sQ) + (uint32_t)c0 * 128u,
+                          (uint32_t)(c1 - c0) * 128u, bar);
+      bulk_push_cluster(map_cluster(mls + split * kH, (uint32_t)c), smem_u32(sP + 8192), kH * 8u, bar);
+    }
+  }
   if (tid >= 64 && tid < 96) {
     cs[tid - 64] = rope_c;
     sn[tid - 64] = rope_s;
   }
-  __syncthreads();
-  // per head: the splits' weights 2^(m_s - M) l_s and their sum L in split order
+  if (!mbar_wait(&ms->recv, 0, kWaitLimit) && tid == 0) flag_timeout(p.ws);
+  // per head: M, the maximum over the splits, then every weight 2^(m_s - M) l_s
   if (tid < kH) {
     float M = -INFINITY;
     for (int c = 0; c < ns; ++c) M = fmaxf(M, mls[c * kH + tid].x);
-    float L = 0.0f;
-    for (int c = 0; c < ns; ++c) {
-      const float2 v = mls[c * kH + tid];
-      const float w = v.x == -INFINITY ? 0.0f : exp2f(v.x - M) * v.y;
-      wgt[c * kH + tid] = w;
-      L += w;
-    }
-    Linv[tid] = L > 0.0f ? 1.0f / L : 0.0f;
-    if (split == 0 && p.lse) p.lse[row * kH + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    Ms[tid] = M;
+  }
+  __syncthreads();
+  for (int i = tid; i < ns * kH; i += kThreads) {
+    const float2 v = mls[i];
+    wgt[i] = v.x == -INFINITY ? 0.0f : exp2f(v.x - Ms[i & (kH - 1)]) * v.y;
   }
   __syncthreads();
   // thread: a pair of dims (d, d + 1) of eight heads (one 16-byte chunk of
-  // each of the two rows in every split), weighted sum in split order
+  // each of the two rows in every split), weighted sum and weight sum L in
+  // split order
   for (int u = tid; u < (nd >> 1) * 8; u += kThreads) {
-    const int hg = u & 7, d = d0 + 2 * (u >> 3);
-    const uint32_t r0 = smem_u32(sQ) + (uint32_t)d * 128u + ((((uint32_t)hg) ^ ((uint32_t)d & 7u)) << 4);
-    const uint32_t r1 = smem_u32(sQ) + (uint32_t)(d + 1) * 128u + ((((uint32_t)hg) ^ ((uint32_t)(d + 1) & 7u)) << 4);
-    float o0[8], o1[8];
+    const int hg = u & 7, dl = 2 * (u >> 3), d = d0 + dl;
+    const uint32_t k0 = (((uint32_t)hg) ^ ((uint32_t)d & 7u)) << 4, k1 = (((uint32_t)hg) ^ ((uint32_t)(d + 1) & 7u)) << 4;
+    float o0[8], o1[8], L[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) o0[j] = o1[j] = 0.0f;
+    for (int j = 0; j < 8; ++j) o0[j] = o1[j] = L[j] = 0.0f;
 #pragma unroll 4
     for (int c = 0; c < ns; ++c) {
-      const uint4 x0 = ld_cluster_v4(map_cluster_u32(r0, (uint32_t)c));
-      const uint4 x1 = ld_cluster_v4(map_cluster_u32(r1, (uint32_t)c));
+      const uint8_t* rr = rcv + ((uint32_t)c * dp + (uint32_t)dl) * 128u;
+      const uint4 x0 = *reinterpret_cast<const uint4*>(rr + k0);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(rr + 128 + k1);
       const uint32_t a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -669,12 +682,15 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
         o0[2 * j + 1] = __fmaf_rn(w1, f0.y, o0[2 * j + 1]);
         o1[2 * j] = __fmaf_rn(w0, f1.x, o1[2 * j]);
         o1[2 * j + 1] = __fmaf_rn(w1, f1.y, o1[2 * j + 1]);
+        L[2 * j] += w0;
+        L[2 * j + 1] += w1;
       }
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int h = 8 * hg + j;
-      float y0 = o0[j] * Linv[h], y1 = o1[j] * Linv[h];
+      const float inv = L[j] > 0.0f ? 1.0f / L[j] : 0.0f;
+      float y0 = o0[j] * inv, y1 = o1[j] * inv;
       if (d >= kMixDn) {
         const int pi = (d - kMixDn) >> 1;
         const float z0 = y0 * cs[pi] + y1 * sn[pi];
@@ -683,6 +699,8 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
         y1 = z1;
       }
       *reinterpret_cast<__nv_bfloat162*>(p.out + (row * kH + h) * (int64_t)kD + d) = __floats2bfloat162_rn(y0, y1);
+      if (split == 0 && dl == 0 && p.lse)
+        p.lse[row * kH + h] = L[j] > 0.0f ? (Ms[h] + log2f(L[j])) * 0.69314718055994531f : -INFINITY;
     }
   }
   // every item of the row has read this one's shared memory before it exits
@@ -716,49 +734,59 @@ size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 namespace {
 
-// The largest cluster of attention CTAs (one per SM: 227 KiB of shared
-// memory each) the device can schedule: 16 when it reports room for at
-// least one, else the portable 8.
-int decode_cluster_cap() {
-  static PerDevice cap;
-  return cap.get([] {
-    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel),
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return 8;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kMaxSplits);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = kMaxSplits;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(attn_decode_kernel), &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      return 8;
-    }
-    return n >= 1 ? kMaxSplits : 8;
+// How many clusters of `s` attention CTAs (one per SM: 227 KiB of shared
+// memory each) the device can hold at once, asked once per device and size
+// (clusters stay inside a GPC, so this depends on how its SMs are grouped).
+int decode_clusters_resident(int s) {
+  static PerDevice attrs;
+  static PerDevice count[kMaxSplits + 1];
+  attrs.get([] {
+    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kSmemBytes);
+    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel),
+                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaGetLastError();
+    return 1;
   });
+  // stored plus one (a stored zero would be asked again)
+  return count[s].get([s] {
+           cudaLaunchConfig_t cfg = {};
+           cfg.gridDim = dim3((unsigned)s);
+           cfg.blockDim = dim3(kThreads);
+           cfg.dynamicSmemBytes = kSmemBytes;
+           cudaLaunchAttribute at[1];
+           at[0].id = cudaLaunchAttributeClusterDimension;
+           at[0].val.clusterDim.x = (unsigned)s;
+           at[0].val.clusterDim.y = 1;
+           at[0].val.clusterDim.z = 1;
+           cfg.attrs = at;
+           cfg.numAttrs = 1;
+           int n = 0;
+           if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(attn_decode_kernel), &cfg) !=
+               cudaSuccess) {
+             cudaGetLastError();
+             n = 0;
+           }
+           return n + 1;
+         }) -
+         1;
 }
 
 }  // namespace
 
 // Splits per row (the CTAs of one cluster): as many as fill the SMs once, at
-// most one per key tile and at most the schedulable cluster size.
+// most one per key tile and at most 16; then the largest such size whose
+// clusters, one per row, the device holds all at once (a size that leaves
+// rows for a second wave costs more than fewer splits).
 int attn_decode_splits(int64_t rows, int64_t max_keys) {
   const int sms = device_sms() > 0 ? device_sms() : 148;
   const int64_t tiles = (max_keys + kTile - 1) / kTile;
   int64_t s = sms / (rows > 0 ? rows : 1);
   if (s > tiles) s = tiles;
-  const int cap = decode_cluster_cap();
-  if (s > cap) s = cap;
-  return (int)(s < 1 ? 1 : s);
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s < 1) s = 1;
+  while (s > 1 && decode_clusters_resident((int)s) < rows) --s;
+  return (int)s;
 }
 
 bool attn_decode_applies(int H, int D, int R, int64_t rows, int k, bool sparse) {
@@ -822,7 +850,7 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e =
       launch_pdl(decode_gather_kernel, dim3((unsigned)(p.kp / kTile), (unsigned)rows), dim3(kGatherThreads), 0, st, p);
   if (e != cudaSuccess) return e;
-  decode_cluster_cap();   // the kernel's shared-memory and cluster-size attributes, set once per device
+  decode_clusters_resident(1);   // the kernel's shared-memory and cluster-size attributes, set once per device
   // one cluster per row: its items meet at cluster barriers and merge through
   // each other's shared memory
   cudaLaunchConfig_t cfg = {};

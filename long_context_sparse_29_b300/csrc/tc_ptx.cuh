@@ -208,6 +208,14 @@ __device__ __forceinline__ uint32_t map_cluster_u32(uint32_t local, uint32_t ran
 __device__ __forceinline__ uint32_t map_cluster(const void* local, uint32_t rank) {
   return map_cluster_u32(smem_u32(local), rank);
 }
+// Bulk copy of `bytes` from this CTA's shared memory into a cluster peer's
+// (dst and bar mapped with map_cluster), completing on the peer's mbarrier;
+// the source stays untouched until the peer has seen the bytes arrive.
+__device__ __forceinline__ void bulk_push_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
