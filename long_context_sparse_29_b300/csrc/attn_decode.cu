@@ -230,7 +230,7 @@ decode_gather_kernel(const DParams p) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)   // one CTA per SM (shared memory): 10 warps x 192 registers fit
 attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_xg) {
   pdl_begin();
@@ -625,28 +625,29 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   uint8_t* rcv = sKV;
   float2* mls = reinterpret_cast<float2*>(sKV + 73728);
   float* Ms = reinterpret_cast<float*>(sKV + 73728 + kMaxSplits * kH * 8);   // [64]
-  float* wgt = Ms + kH;                                                       // [ns][64]
+  float* Linv = Ms + kH;                                                      // [64]
+  float* wgt = Linv + kH;                                                     // [ns][64]
   float* cs = wgt + kMaxSplits * kH;   // the RoPE row of t: 32 cos, 32 sin
   float* sn = cs + 32;
   static_assert((kMaxSplits * ((kD + kMaxSplits - 1) / kMaxSplits + 2)) * 128 <= 73728, "receive rows");
-  static_assert(73728 + kMaxSplits * kH * 8 + (kH + kMaxSplits * kH + 64) * 4 <= 131072, "merge scratch");
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&ms->recv, (uint32_t)ns * ((uint32_t)nd * 128u + kH * 8u));
-    for (int c = 0; c < ns; ++c) {
-      const int c0 = min(kD, c * dp), c1 = min(kD, c0 + dp);
-      const uint32_t bar = map_cluster(&ms->recv, (uint32_t)c);
-      if (c1 > c0)
-        bulk_push_cluster(map_cluster(rcv + (uint32_t)split * dp * 128u, (uint32_t)c), smem_u32(sQ) + (uint32_t)c0 * 128u,
-                          (uint32_t)(c1 - c0) * 128u, bar);
-      bulk_push_cluster(map_cluster(mls + split * kH, (uint32_t)c), smem_u32(sP + 8192), kH * 8u, bar);
-    }
+  static_assert(73728 + kMaxSplits * kH * 8 + (2 * kH + kMaxSplits * kH + 64) * 4 <= 131072, "merge scratch");
+  if (tid == 0) mbar_arrive_expect_tx(&ms->recv, (uint32_t)ns * ((uint32_t)nd * 128u + kH * 8u));
+  if (tid >= 32 && tid < 32 + ns) {   // thread 32 + c pushes to item c
+    const int c = tid - 32;
+    const int c0 = min(kD, c * dp), c1 = min(kD, c0 + dp);
+    const uint32_t bar = map_cluster(&ms->recv, (uint32_t)c);
+    if (c1 > c0)
+      bulk_push_cluster(map_cluster(rcv + (uint32_t)split * dp * 128u, (uint32_t)c), smem_u32(sQ) + (uint32_t)c0 * 128u,
+                        (uint32_t)(c1 - c0) * 128u, bar);
+    bulk_push_cluster(map_cluster(mls + split * kH, (uint32_t)c), smem_u32(sP + 8192), kH * 8u, bar);
   }
   if (tid >= 64 && tid < 96) {
     cs[tid - 64] = rope_c;
     sn[tid - 64] = rope_s;
   }
   if (!mbar_wait(&ms->recv, 0, kWaitLimit) && tid == 0) flag_timeout(p.ws);
-  // per head: M, the maximum over the splits, then every weight 2^(m_s - M) l_s
+  // per head: M, the maximum over the splits, then every weight 2^(m_s - M) l_s,
+  // then 1 / L, L their sum in split order
   if (tid < kH) {
     float M = -INFINITY;
     for (int c = 0; c < ns; ++c) M = fmaxf(M, mls[c * kH + tid].x);
@@ -658,39 +659,44 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     wgt[i] = v.x == -INFINITY ? 0.0f : exp2f(v.x - Ms[i & (kH - 1)]) * v.y;
   }
   __syncthreads();
+  if (tid < kH) {
+    float L = 0.0f;
+    for (int c = 0; c < ns; ++c) L += wgt[c * kH + tid];
+    Linv[tid] = L > 0.0f ? 1.0f / L : 0.0f;
+    if (split == 0 && p.lse) p.lse[row * kH + tid] = L > 0.0f ? (Ms[tid] + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncthreads();
   // thread: a pair of dims (d, d + 1) of eight heads (one 16-byte chunk of
-  // each of the two rows in every split), weighted sum and weight sum L in
-  // split order
+  // each of the two rows in every split), weighted sum in split order
   for (int u = tid; u < (nd >> 1) * 8; u += kThreads) {
     const int hg = u & 7, dl = 2 * (u >> 3), d = d0 + dl;
     const uint32_t k0 = (((uint32_t)hg) ^ ((uint32_t)d & 7u)) << 4, k1 = (((uint32_t)hg) ^ ((uint32_t)(d + 1) & 7u)) << 4;
-    float o0[8], o1[8], L[8];
+    float o0[8], o1[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) o0[j] = o1[j] = L[j] = 0.0f;
+    for (int j = 0; j < 8; ++j) o0[j] = o1[j] = 0.0f;
 #pragma unroll 4
     for (int c = 0; c < ns; ++c) {
       const uint8_t* rr = rcv + ((uint32_t)c * dp + (uint32_t)dl) * 128u;
       const uint4 x0 = *reinterpret_cast<const uint4*>(rr + k0);
       const uint4 x1 = *reinterpret_cast<const uint4*>(rr + 128 + k1);
+      const float4 wa = *reinterpret_cast<const float4*>(wgt + c * kH + 8 * hg);
+      const float4 wb = *reinterpret_cast<const float4*>(wgt + c * kH + 8 * hg + 4);
+      const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
       const uint32_t a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a0[j]));
         const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a1[j]));
-        const float w0 = wgt[c * kH + 8 * hg + 2 * j], w1 = wgt[c * kH + 8 * hg + 2 * j + 1];
-        o0[2 * j] = __fmaf_rn(w0, f0.x, o0[2 * j]);
-        o0[2 * j + 1] = __fmaf_rn(w1, f0.y, o0[2 * j + 1]);
-        o1[2 * j] = __fmaf_rn(w0, f1.x, o1[2 * j]);
-        o1[2 * j + 1] = __fmaf_rn(w1, f1.y, o1[2 * j + 1]);
-        L[2 * j] += w0;
-        L[2 * j + 1] += w1;
+        o0[2 * j] = __fmaf_rn(w[2 * j], f0.x, o0[2 * j]);
+        o0[2 * j + 1] = __fmaf_rn(w[2 * j + 1], f0.y, o0[2 * j + 1]);
+        o1[2 * j] = __fmaf_rn(w[2 * j], f1.x, o1[2 * j]);
+        o1[2 * j + 1] = __fmaf_rn(w[2 * j + 1], f1.y, o1[2 * j + 1]);
       }
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int h = 8 * hg + j;
-      const float inv = L[j] > 0.0f ? 1.0f / L[j] : 0.0f;
-      float y0 = o0[j] * inv, y1 = o1[j] * inv;
+      float y0 = o0[j] * Linv[h], y1 = o1[j] * Linv[h];
       if (d >= kMixDn) {
         const int pi = (d - kMixDn) >> 1;
         const float z0 = y0 * cs[pi] + y1 * sn[pi];
@@ -699,8 +705,6 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
         y1 = z1;
       }
       *reinterpret_cast<__nv_bfloat162*>(p.out + (row * kH + h) * (int64_t)kD + d) = __floats2bfloat162_rn(y0, y1);
-      if (split == 0 && dl == 0 && p.lse)
-        p.lse[row * kH + h] = L[j] > 0.0f ? (Ms[h] + log2f(L[j])) * 0.69314718055994531f : -INFINITY;
     }
   }
   // every item of the row has read this one's shared memory before it exits
