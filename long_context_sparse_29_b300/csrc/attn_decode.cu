@@ -230,7 +230,7 @@ decode_gather_kernel(const DParams p) {
   }
 }
 
-__global__ void __maxnreg__(200)   // one CTA per SM (shared memory): 10 warps x 192 registers fit
+__global__ void __launch_bounds__(kThreads, 1)
 attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_xg) {
   pdl_begin();
