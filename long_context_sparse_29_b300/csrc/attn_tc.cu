@@ -347,7 +347,7 @@ gather_expand_kernel(const Params p, int64_t rows, int dense, __nv_bfloat16* __r
 }
 
 template <bool DENSE>
-__global__ void __maxnreg__(200)   // one CTA per SM (shared memory): 10 warps x 192 registers fit
+__global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_qr) {
   pdl_begin();
