@@ -29,6 +29,8 @@
 // workspace, waits (bounded) for its own copies and MMAs and frees TMEM.
 #include <cuda.h>
 
+#include <cstring>
+
 #include "attn_common.cuh"
 #include "csa_common.cuh"
 #include "launch.h"
@@ -61,12 +63,15 @@ constexpr uint32_t kTmemO = 0;       // O^T: 4 blocks of 64 columns (heads); lan
 constexpr uint32_t kTmemS = 256;     // S: 2 buffers of 64 columns (keys); M = 64 layout
 
 constexpr uint32_t kWaitLimit = 1u << 20;     // suspending polls of one mbarrier wait
-constexpr int kMaxSplits = 16;                // splits of a row = CTAs of one cluster
+constexpr int kMaxSplits = 16;                // splits of a row = CTAs of one cluster (cluster merge)
+constexpr int kClusterMergeMax = 8;           // rows needing more splits than this merge through global memory
+constexpr uint32_t kGridWaitLimit = 1u << 22; // polls of the row counter (64 ns naps; global merge)
 constexpr float kLazy = 8.0f;
 
 struct Misc {
   uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
-  uint64_t q_full, q_ready, o_full, drain[2], recv;
+  uint64_t q_full, q_ready, o_full, drain[2], recv, merge_in;
+  int go;                           // the row counter reached every split (global merge)
   uint32_t tmem;
   int abort;
   alignas(16) float alpha[2][kH];   // per-head rescale factors of a tile, double-buffered
@@ -99,7 +104,10 @@ struct DParams {
   __nv_bfloat16* out;       // [rows, 64, 512]
   float* lse;               // [rows, 64] or NULL
   void* ws;                 // status flags
-  int nsplit;               // items per row = the cluster size
+  int nsplit;               // items per row (the cluster size when they merge through shared memory)
+  __nv_bfloat16* part_o;    // global merge: [items, 512 dims, 64 heads] normalised partial outputs
+  float* part_ml;           // global merge: [items, 64, 2] running max (log2 units), sum
+  int* arrive;              // global merge: [rows] items that finished their partial (zero at launch)
   __nv_bfloat16* xg;        // [rows, kp, 512] every row's keys in bf16, in order, zero past them
   int64_t kp;               // key slots per row of xg (a multiple of the tile)
   int* ecount;              // [rows] valid selected entries of each row (sparse)
@@ -230,9 +238,63 @@ decode_gather_kernel(const DParams p) {
   }
 }
 
+// The merge of one dim slice [d0, d0 + nd) of a row over its ns splits:
+// rows[(c stride + dl) 128 bytes] holds split c's partial row of dim d0 + dl
+// (64 heads bf16; 16-byte chunk g at g ^ (d mod 8) when `swz`, else at g).
+// Thread: a pair of dims (d, d + 1) of eight heads, weighted sum in split
+// order, times 1 / L, RoPE dims rotated back, stored to out_row [64][512].
+__device__ __forceinline__ void merge_slice(const uint8_t* rows, uint32_t stride, bool swz, int ns, int d0, int nd,
+                                            const float* wgt, const float* Linv, const float* cs, const float* sn,
+                                            __nv_bfloat16* out_row) {
+  for (int u = threadIdx.x; u < (nd >> 1) * 8; u += kThreads) {
+    const int hg = u & 7, dl = 2 * (u >> 3), d = d0 + dl;
+    const uint32_t k0 = (((uint32_t)hg) ^ (swz ? ((uint32_t)d & 7u) : 0u)) << 4;
+    const uint32_t k1 = (((uint32_t)hg) ^ (swz ? ((uint32_t)(d + 1) & 7u) : 0u)) << 4;
+    float o0[8], o1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o0[j] = o1[j] = 0.0f;
+#pragma unroll 4
+    for (int c = 0; c < ns; ++c) {
+      const uint8_t* rr = rows + ((uint32_t)c * stride + (uint32_t)dl) * 128u;
+      const uint4 x0 = *reinterpret_cast<const uint4*>(rr + k0);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(rr + 128 + k1);
+      const float4 wa = *reinterpret_cast<const float4*>(wgt + c * kH + 8 * hg);
+      const float4 wb = *reinterpret_cast<const float4*>(wgt + c * kH + 8 * hg + 4);
+      const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      const uint32_t a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a0[j]));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a1[j]));
+        o0[2 * j] = __fmaf_rn(w[2 * j], f0.x, o0[2 * j]);
+        o0[2 * j + 1] = __fmaf_rn(w[2 * j + 1], f0.y, o0[2 * j + 1]);
+        o1[2 * j] = __fmaf_rn(w[2 * j], f1.x, o1[2 * j]);
+        o1[2 * j + 1] = __fmaf_rn(w[2 * j + 1], f1.y, o1[2 * j + 1]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int h = 8 * hg + j;
+      float y0 = o0[j] * Linv[h], y1 = o1[j] * Linv[h];
+      if (d >= kMixDn) {
+        const int pi = (d - kMixDn) >> 1;
+        const float z0 = y0 * cs[pi] + y1 * sn[pi];
+        const float z1 = -y0 * sn[pi] + y1 * cs[pi];
+        y0 = z0;
+        y1 = z1;
+      }
+      *reinterpret_cast<__nv_bfloat162*>(out_row + h * (int64_t)kD + d) = __floats2bfloat162_rn(y0, y1);
+    }
+  }
+}
+
+// kCluster: the items of a row are one thread-block cluster and merge through
+// each other's shared memory; otherwise they write their partials to global
+// memory, meet at a per-row counter (cooperative launch) and merge from there.
+template <bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_xg) {
+                   const __grid_constant__ CUtensorMap tm_xg, const __grid_constant__ CUtensorMap tm_po) {
   pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -269,6 +331,8 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&ms->drain[0], 1);
     mbar_init(&ms->drain[1], 1);
     mbar_init(&ms->recv, 1);          // the row's partial slices and statistics pushed by its items
+    mbar_init(&ms->merge_in, 1);
+    ms->go = 0;
     mbar_fence_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&ms->tmem, kTmemCols);
@@ -553,7 +617,8 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     fence_after_sync();
     // this item's statistics per head, (m, l), in P buffer 1 (free now): the
     // row's other items read them there
-    float2* ml_own = reinterpret_cast<float2*>(sP + 8192);
+    float2* ml_own = kCluster ? reinterpret_cast<float2*>(sP + 8192)
+                              : reinterpret_cast<float2*>(p.part_ml + item * (kH * 2));
     if (leader) {
       ml_own[ha] = make_float2(any_keys ? ma : -INFINITY, any_keys ? la : 0.0f);
       ml_own[hb] = make_float2(any_keys ? mb : -INFINITY, any_keys ? lb : 0.0f);
@@ -600,6 +665,19 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
       }
     }
     if (bad) fail = true;
+    if constexpr (!kCluster) {
+      // the staged partial to global memory: four TMA boxes of 128 dims
+      fence_proxy_async();
+      group_vote(false);   // the whole partial is staged
+      if (tid == 0 && !bad) {
+        for (int mt = 0; mt < 4; ++mt) tma_store_2d(&tm_po, smem_u32(sQ) + mt * 16384, 0, (int)(item * kD + 128 * mt));
+        bulk_commit_wait_all();
+        // visible to the row's other items (read there by bulk copies: the
+        // async proxy) before the arrival on the row counter
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      __threadfence();
+    }
   }
   if (fail) {
     ms->abort = 1;
@@ -610,6 +688,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if constexpr (kCluster) {
   // ---- the row's items meet: every partial of the row is staged, every
   // item's KV slots are free and its barriers initialised (cluster barrier) ----
   cluster_sync_all();
@@ -666,49 +745,93 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     if (split == 0 && p.lse) p.lse[row * kH + tid] = L > 0.0f ? (Ms[tid] + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();
-  // thread: a pair of dims (d, d + 1) of eight heads (one 16-byte chunk of
-  // each of the two rows in every split), weighted sum in split order
-  for (int u = tid; u < (nd >> 1) * 8; u += kThreads) {
-    const int hg = u & 7, dl = 2 * (u >> 3), d = d0 + dl;
-    const uint32_t k0 = (((uint32_t)hg) ^ ((uint32_t)d & 7u)) << 4, k1 = (((uint32_t)hg) ^ ((uint32_t)(d + 1) & 7u)) << 4;
-    float o0[8], o1[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) o0[j] = o1[j] = 0.0f;
-#pragma unroll 4
-    for (int c = 0; c < ns; ++c) {
-      const uint8_t* rr = rcv + ((uint32_t)c * dp + (uint32_t)dl) * 128u;
-      const uint4 x0 = *reinterpret_cast<const uint4*>(rr + k0);
-      const uint4 x1 = *reinterpret_cast<const uint4*>(rr + 128 + k1);
-      const float4 wa = *reinterpret_cast<const float4*>(wgt + c * kH + 8 * hg);
-      const float4 wb = *reinterpret_cast<const float4*>(wgt + c * kH + 8 * hg + 4);
-      const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-      const uint32_t a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a0[j]));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a1[j]));
-        o0[2 * j] = __fmaf_rn(w[2 * j], f0.x, o0[2 * j]);
-        o0[2 * j + 1] = __fmaf_rn(w[2 * j + 1], f0.y, o0[2 * j + 1]);
-        o1[2 * j] = __fmaf_rn(w[2 * j], f1.x, o1[2 * j]);
-        o1[2 * j + 1] = __fmaf_rn(w[2 * j + 1], f1.y, o1[2 * j + 1]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int h = 8 * hg + j;
-      float y0 = o0[j] * Linv[h], y1 = o1[j] * Linv[h];
-      if (d >= kMixDn) {
-        const int pi = (d - kMixDn) >> 1;
-        const float z0 = y0 * cs[pi] + y1 * sn[pi];
-        const float z1 = -y0 * sn[pi] + y1 * cs[pi];
-        y0 = z0;
-        y1 = z1;
-      }
-      *reinterpret_cast<__nv_bfloat162*>(p.out + (row * kH + h) * (int64_t)kD + d) = __floats2bfloat162_rn(y0, y1);
-    }
-  }
+  merge_slice(rcv, (uint32_t)dp, true, ns, d0, nd, wgt, Linv, cs, sn, p.out + row * (int64_t)(kH * kD));
   // every item of the row has read this one's shared memory before it exits
   cluster_sync_all();
+  } else {
+  // ---- the row's items meet: every partial of the row is written ----
+  if (tid == 0) {
+    atomicAdd(p.arrive + row, 1);
+    bool ok = false;
+    for (uint32_t it = 0; it < kGridWaitLimit; ++it) {
+      if (*reinterpret_cast<volatile int*>(p.arrive + row) >= p.nsplit) {
+        ok = true;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    if (!ok) flag_timeout(p.ws);
+    ms->go = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!ms->go) return;
+  // ---- merge this item's slice of the row's dims over the splits ----
+  // dims of this slice: [d0, d1), even bounds (RoPE pairs stay together)
+  const int ns = p.nsplit;
+  const int dp = ((kD + ns - 1) / ns + 1) & ~1;
+  const int d0 = min(kD, split * dp), d1 = min(kD, d0 + dp);
+  const int nd = d1 - d0;
+  // shared memory is free now: the row's statistics [ns][64] (m, l) at 0,
+  // this slice's partial rows [ns][nd] of 128 bytes after them (16-byte chunk
+  // c of dim d's row at chunk c ^ (d mod 8), as written), staged by bulk
+  // copies (all in flight together)
+  const uint32_t ml_bytes = (uint32_t)ns * kH * 8;
+  const uint32_t sl_off = (ml_bytes + 1023) & ~1023u;
+  const float2* ml_s = reinterpret_cast<const float2*>(sm);
+  const uint8_t* sl_s = sm + sl_off;
+  if (tid == 0) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    mbar_arrive_expect_tx(&ms->merge_in, ml_bytes + (uint32_t)ns * nd * 128u);
+    bulk_copy_g2s(smem_u32(sm), p.part_ml + row * (int64_t)ns * kH * 2, ml_bytes, &ms->merge_in);
+    if (nd > 0)
+      for (int c = 0; c < ns; ++c)
+        bulk_copy_g2s(smem_u32(sm + sl_off + (uint32_t)c * nd * 128u),
+                      p.part_o + (row * (int64_t)ns + c) * (kH * kD) + (int64_t)d0 * kH, (uint32_t)nd * 128u,
+                      &ms->merge_in);
+  }
+  if (!mbar_wait(&ms->merge_in, 0, kWaitLimit)) {
+    if (tid == 0) flag_timeout(p.ws);
+    return;   // (a copy still in flight lands in memory nobody reads again)
+  }
+  // per head: M, the maximum over the splits (five partial maxima each), every
+  // weight 2^(m_s - M) l_s, then 1 / L, L their sum in split order
+  float* wgt = reinterpret_cast<float*>(sm + sl_off + (((uint32_t)ns * nd * 128u + 1023) & ~1023u));
+  float* red = wgt + (size_t)ns * kH;   // [5][64] partial maxima
+  float* Linv = red + 5 * kH;           // [64]
+  float* cs = Linv + kH;                // the RoPE row of t: 32 cos, 32 sin
+  float* sn = cs + 32;
+  {
+    const int g = tid >> 6, h = tid & (kH - 1);   // kThreads = 5 x 64
+    float M = -INFINITY;
+    for (int c = g; c < ns; c += 5) M = fmaxf(M, ml_s[c * kH + h].x);
+    red[g * kH + h] = M;
+  }
+  if (tid >= 64 && tid < 96) {
+    cs[tid - 64] = rope_c;
+    sn[tid - 64] = rope_s;
+  }
+  __syncthreads();
+  for (int i = tid; i < ns * kH; i += kThreads) {
+    const int h = i & (kH - 1);
+    const float M = fmaxf(fmaxf(fmaxf(red[h], red[kH + h]), fmaxf(red[2 * kH + h], red[3 * kH + h])), red[4 * kH + h]);
+    const float2 v = ml_s[i];
+    wgt[i] = v.x == -INFINITY ? 0.0f : exp2f(v.x - M) * v.y;
+  }
+  __syncthreads();
+  if (tid < kH) {
+    float L = 0.0f;
+    for (int c = 0; c < ns; ++c) L += wgt[c * kH + tid];
+    Linv[tid] = L > 0.0f ? 1.0f / L : 0.0f;
+    if (split == 0 && p.lse) {
+      const float M = fmaxf(fmaxf(fmaxf(red[tid], red[kH + tid]), fmaxf(red[2 * kH + tid], red[3 * kH + tid])),
+                            red[4 * kH + tid]);
+      p.lse[row * kH + tid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+  __syncthreads();
+  merge_slice(sl_s, (uint32_t)nd, false, ns, d0, nd, wgt, Linv, cs, sn, p.out + row * (int64_t)(kH * kD));
+  }
 }
 
 // cuTensorMapEncodeTiled, fetched from the driver once
@@ -745,9 +868,11 @@ int decode_clusters_resident(int s) {
   static PerDevice attrs;
   static PerDevice count[kMaxSplits + 1];
   attrs.get([] {
-    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kSmemBytes);
-    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel),
+    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel<true>),
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel<false>),
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel<true>),
                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaGetLastError();
     return 1;
@@ -766,7 +891,7 @@ int decode_clusters_resident(int s) {
            cfg.attrs = at;
            cfg.numAttrs = 1;
            int n = 0;
-           if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(attn_decode_kernel), &cfg) !=
+           if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(attn_decode_kernel<true>), &cfg) !=
                cudaSuccess) {
              cudaGetLastError();
              n = 0;
@@ -778,18 +903,25 @@ int decode_clusters_resident(int s) {
 
 }  // namespace
 
-// Splits per row (the CTAs of one cluster): as many as fill the SMs once, at
-// most one per key tile and at most 16; then the largest such size whose
-// clusters, one per row, the device holds all at once (a size that leaves
-// rows for a second wave costs more than fewer splits).
-int attn_decode_splits(int64_t rows, int64_t max_keys) {
+// Items per row: as many as fill the SMs once, at most one per key tile.
+// When that is at most kClusterMergeMax the items of a row form a cluster
+// (then the largest size whose clusters, one per row, the device holds all
+// at once: a size that leaves rows for a second wave costs more than fewer
+// splits); more, they merge through global memory.
+static int64_t decode_fill_splits(int64_t rows, int64_t max_keys) {
   const int sms = device_sms() > 0 ? device_sms() : 148;
   const int64_t tiles = (max_keys + kTile - 1) / kTile;
   int64_t s = sms / (rows > 0 ? rows : 1);
   if (s > tiles) s = tiles;
-  if (s > kMaxSplits) s = kMaxSplits;
-  if (s < 1) s = 1;
-  while (s > 1 && decode_clusters_resident((int)s) < rows) --s;
+  return s < 1 ? 1 : s;
+}
+static bool decode_cluster_merge(int64_t rows, int64_t max_keys) {
+  return decode_fill_splits(rows, max_keys) <= kClusterMergeMax;
+}
+int attn_decode_splits(int64_t rows, int64_t max_keys) {
+  int64_t s = decode_fill_splits(rows, max_keys);
+  if (s <= kClusterMergeMax)
+    while (s > 1 && decode_clusters_resident((int)s) < rows) --s;
   return (int)s;
 }
 
@@ -801,7 +933,10 @@ bool attn_decode_applies(int H, int D, int R, int64_t rows, int k, bool sparse) 
 int64_t attn_decode_kp(int64_t max_keys) { return (max_keys + kTile - 1) / kTile * kTile; }
 
 size_t attn_decode_workspace(int64_t rows, int64_t max_keys) {
-  return al256((size_t)rows * 4) + al256((size_t)rows * attn_decode_kp(max_keys) * kD * 2);
+  const size_t base = al256((size_t)rows * 4) + al256((size_t)rows * attn_decode_kp(max_keys) * kD * 2);
+  if (decode_cluster_merge(rows, max_keys)) return base;
+  const int64_t items = rows * attn_decode_splits(rows, max_keys);
+  return base + al256((size_t)items * kH * kD * 2) + al256((size_t)items * kH * 2 * 4) + al256((size_t)rows * 4);
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
@@ -828,12 +963,25 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   p.ws = a.ws;
   p.nsplit = attn_decode_splits(rows, a.max_keys);
   const int64_t items = rows * p.nsplit;
+  const bool cl = decode_cluster_merge(rows, a.max_keys);
   uint8_t* base = reinterpret_cast<uint8_t*>(a.ws) + kWsHeader;
   p.ecount = reinterpret_cast<int*>(base);
   base += al256((size_t)rows * 4);
   p.kp = attn_decode_kp(a.max_keys);
   p.xg = reinterpret_cast<__nv_bfloat16*>(base);
-  CUtensorMap tm_q, tm_xg;
+  base += al256((size_t)rows * p.kp * kD * 2);
+  p.part_o = nullptr;
+  p.part_ml = nullptr;
+  p.arrive = nullptr;
+  if (!cl) {
+    p.part_o = reinterpret_cast<__nv_bfloat16*>(base);
+    base += al256((size_t)items * kH * kD * 2);
+    p.part_ml = reinterpret_cast<float*>(base);
+    base += al256((size_t)items * kH * 2 * 4);
+    p.arrive = reinterpret_cast<int*>(base);
+  }
+  CUtensorMap tm_q, tm_xg, tm_po;
+  memset(&tm_po, 0, sizeof(tm_po));
   {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorInvalidValue;
@@ -845,34 +993,54 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+    if (!cl) {
+      const cuuint64_t pdims[2] = {(cuuint64_t)kH, (cuuint64_t)(items * kD)};
+      const cuuint64_t pstrides[1] = {(cuuint64_t)kH * 2};
+      const cuuint32_t pbox[2] = {(cuuint32_t)kH, 128u};
+      if (fn(&tm_po, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.part_o, pdims, pstrides, pbox, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
     const cuuint64_t gdims[2] = {(cuuint64_t)kD, (cuuint64_t)(rows * p.kp)};
     if (fn(&tm_xg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.xg, gdims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
         CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e =
-      launch_pdl(decode_gather_kernel, dim3((unsigned)(p.kp / kTile), (unsigned)rows), dim3(kGatherThreads), 0, st, p);
+  cudaError_t e = cudaSuccess;
+  if (!cl) {
+    e = cudaMemsetAsync(p.arrive, 0, (size_t)rows * 4, st);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_pdl(decode_gather_kernel, dim3((unsigned)(p.kp / kTile), (unsigned)rows), dim3(kGatherThreads), 0, st, p);
   if (e != cudaSuccess) return e;
-  decode_clusters_resident(1);   // the kernel's shared-memory and cluster-size attributes, set once per device
-  // one cluster per row: its items meet at cluster barriers and merge through
-  // each other's shared memory
+  decode_clusters_resident(1);   // the kernels' shared-memory and cluster-size attributes, set once per device
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)items);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = (unsigned)p.nsplit;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
-  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  if (cl) {
+    // one cluster per row: its items meet at cluster barriers and merge
+    // through each other's shared memory
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = (unsigned)p.nsplit;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<true>, p, tm_q, tm_xg, tm_po);
+  }
+  // every item resident at once (an item waits on its row's counter)
+  attrs[0].id = cudaLaunchAttributeCooperative;
+  attrs[0].val.cooperative = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, p, tm_q, tm_xg);
-  return e;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<false>, p, tm_q, tm_xg, tm_po);
 }
 
 }  // namespace csa
