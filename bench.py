@@ -295,7 +295,7 @@ LAUNCHES_PER_STEP = 11
 # DRAM bytes (read + write) of one attn_tc_kernel launch on this workload, from
 # one ncu capture of it (dram__bytes_read.sum + dram__bytes_write.sum); to be
 # set to None when the kernel changes, until it is captured again
-ATTN_TRAFFIC = 631670784 + 493387264
+ATTN_TRAFFIC = 631751936 + 493387520
 
 
 # --------------------------------------------------------------------------
@@ -506,7 +506,8 @@ def run_config(args, name):
         units, unit = float(layers[0].B), "queries/s"
         metric = {"c3_csa_decode_128k": "CSA decode queries/s (32 sequences at 128K context, top-k 1024)",
                   "c4_hca_decode_1m": "HCA decode queries/s (16 sequences at 1M context, m'=128)",
-                  "c5_hybrid_csa_decode_1m": "hybrid CSA+HCA decode layer-pair steps/s (4 sequences at 1M)"}[name]
+                  "c5_hybrid_csa_decode_1m": "hybrid CSA+HCA decode queries/s (4 sequences at 1M, one CSA and one HCA "
+                                              "layer per query)"}[name]
         alg = sum(decode_bytes(c) for c in layers)
         roof = {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s", "algorithmic_bytes_per_step": alg}
         l2 = "caches resident; each step reads them once (larger than L2 except the HCA-only step)"
