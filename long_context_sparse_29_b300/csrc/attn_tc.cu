@@ -474,9 +474,12 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
           // soon as the PV chunk of tile g - 2 that read it has completed:
           // lanes 0..15 gather quarters 0, 1 (column box lane & 3) and copy
           // quarter 2, lanes 16..31 copy quarter 3
+          // Nothing touches kv_full[buf] for tile g before one of the waits
+          // below has passed: a PV chunk of tile g - 2 done implies that tile's
+          // kv_full phase complete (its QK^T ran), so no arrival or byte of
+          // tile g can land in tile g - 2's phase.
           const uint32_t tb = smem_u32(sKV + buf * 65536);
           const uint32_t par = (uint32_t)((g >> 1) - 1) & 1;
-          if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * (kD / 2) * 2);
           bool fine = true;
           {
             const int rg = (lane >> 2) & 3, cb = lane & 3;
@@ -486,9 +489,11 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
             const int y3 = __shfl_sync(0xffffffffu, myrow, 4 * rg + 3);
             if (lane < 16) {
               if (g >= 2 && !mbar_wait(&ms->kv_empty[buf][cb >> 1], par, kWaitLimit)) fine = false;
-              if (fine)
+              if (fine) {
+                if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * (kD / 2) * 2);
                 tma_gather4(tb + cb * 8192 + (uint32_t)(16 * pw + 4 * rg) * 128u, &tm_rows, 64 * cb, y0, y1, y2, y3,
                             &ms->kv_full[buf]);
+              }
             }
           }
           if (g >= 2 && fine && !mbar_wait(&ms->kv_empty[buf][2 + (lane >> 4)], par, kWaitLimit)) fine = false;
