@@ -75,8 +75,7 @@ constexpr uint32_t kWaitLimit = 1u << 20;    // suspending polls of one mbarrier
 constexpr float kLazy = 8.0f;        // log2 growth of a running max that forces a rescale
 
 struct Misc {
-  uint64_t kv_full[2], s_full[2], p_full[2];
-  uint64_t kv_empty[2][4];   // a slot's quarter q (dims 128 q ..) read by its PV chunk: refillable
+  uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
   uint64_t q_full, q_empty, o_full, o_empty, drain[2];
   uint64_t list_full[2], list_empty[2];  // entry list handover, double-buffered
   uint32_t tmem;
@@ -365,7 +364,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
     ms->abort = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->kv_full[i], 4 + 128);   // per producer warp: one arrival, + one per lane
-      for (int q = 0; q < 4; ++q) mbar_init(&ms->kv_empty[i][q], 1);
+      mbar_init(&ms->kv_empty[i], 1);
       mbar_init(&ms->s_full[i], 1);
       mbar_init(&ms->p_full[i], 4);
       mbar_init(&ms->list_full[i], 1);
@@ -415,13 +414,6 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
       if (good) nl = n + 1;
       return good != 0;
     };
-    // every quarter of slot buf free again (tile g - 2's PV complete)
-    auto slot_free = [&](int buf, uint32_t gg) -> bool {
-      const uint32_t par = (uint32_t)((gg >> 1) - 1) & 1;
-      for (int q = 0; q < 4; ++q)
-        if (!mbar_wait(&ms->kv_empty[buf][q], par, kWaitLimit)) return false;
-      return true;
-    };
     if (!DENSE && have && pw == 0) ok = issue_list(I, 0);
     while (have && ok && !vabort(ms)) {
       const int32_t* lst = list + (nq & 1) * kMaxList;
@@ -435,7 +427,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         // 64 columns per tile from producer warp 0; the others only arrive
         for (int tl = I.tlo; tl < I.thi; ++tl, ++g) {
           const int buf = g & 1;
-          if (g >= 2 && !slot_free(buf, g)) {
+          if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
             ok = false;
             break;
           }
@@ -470,37 +462,22 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
               else myrow = (int)(p.xwin0 + (int64_t)I.b * p.Ts + (I.w_lo - I.p0 + (key - I.ne)));
             }
           }
-          // quarter q of the slot (dims 128 q .. 128 q + 127) is refilled as
-          // soon as the PV chunk of tile g - 2 that read it has completed:
-          // lanes 0..15 gather quarters 0, 1 (column box lane & 3) and copy
-          // quarter 2, lanes 16..31 copy quarter 3
-          // Nothing touches kv_full[buf] for tile g before one of the waits
-          // below has passed: a PV chunk of tile g - 2 done implies that tile's
-          // kv_full phase complete (its QK^T ran), so no arrival or byte of
-          // tile g can land in tile g - 2's phase.
+          if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
+            ok = false;
+            break;
+          }
           const uint32_t tb = smem_u32(sKV + buf * 65536);
-          const uint32_t par = (uint32_t)((g >> 1) - 1) & 1;
-          bool fine = true;
+          if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * (kD / 2) * 2);
+          __syncwarp();
           {
             const int rg = (lane >> 2) & 3, cb = lane & 3;
             const int y0 = __shfl_sync(0xffffffffu, myrow, 4 * rg);
             const int y1 = __shfl_sync(0xffffffffu, myrow, 4 * rg + 1);
             const int y2 = __shfl_sync(0xffffffffu, myrow, 4 * rg + 2);
             const int y3 = __shfl_sync(0xffffffffu, myrow, 4 * rg + 3);
-            if (lane < 16) {
-              if (g >= 2 && !mbar_wait(&ms->kv_empty[buf][cb >> 1], par, kWaitLimit)) fine = false;
-              if (fine) {
-                if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], 16 * (kD / 2) * 2);
-                tma_gather4(tb + cb * 8192 + (uint32_t)(16 * pw + 4 * rg) * 128u, &tm_rows, 64 * cb, y0, y1, y2, y3,
-                            &ms->kv_full[buf]);
-              }
-            }
-          }
-          if (g >= 2 && fine && !mbar_wait(&ms->kv_empty[buf][2 + (lane >> 4)], par, kWaitLimit)) fine = false;
-          if (!__all_sync(0xffffffffu, fine)) {
-            // (boxes already issued land on kv_full; the exit drain waits for them)
-            ok = false;
-            break;
+            if (lane < 16)
+              tma_gather4(tb + cb * 8192 + (uint32_t)(16 * pw + 4 * rg) * 128u, &tm_rows, 64 * cb, y0, y1, y2, y3,
+                          &ms->kv_full[buf]);
           }
 #pragma unroll
           for (int rr = 0; rr < 16; ++rr) {
@@ -544,7 +521,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
               sc[rr] = __ldg(reinterpret_cast<const float*>(row + kMixScaleOff) + (lane >> 3));
             }
           }
-          if (g >= 2 && !slot_free(buf, g)) {
+          if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
             ok = false;
             break;
           }
@@ -684,8 +661,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
     // ================================ PV issue ================================
     // O^T += V^T P^T as soon as P of the tile is in smem; the first tile of
     // an item overwrites O^T, so it waits for the previous item's epilogue.
-    // Each dim chunk's completion frees that quarter of the tile's ring slot
-    // (kv_empty[slot][chunk]); the last chunk's commit covers the whole tile.
+    // Its completion frees the tile's ring slot (kv_empty).
     const uint32_t aKV = smem_u32(sKV), aP = smem_u32(sP);
     constexpr uint32_t idPV = idesc_bf16(128, kH, 1, 0);
     Cursor<DENSE> cur(p);
@@ -709,8 +685,8 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
           for (int ks = 0; ks < kTile / 16; ++ks)
             mma_bf16_elect(tmem + kTmemO + 64u * mt, vd0 + (uint64_t)((2 * mt * 8192 + ks * 2048) >> 4),
                            pd0 + (uint64_t)((ks * 32) >> 4), idPV, (!first || ks > 0) ? 1u : 0u);
-          mma_commit_elect(&ms->kv_empty[g & 1][mt]);   // quarter mt of the slot is read: refillable
         }
+        mma_commit_elect(&ms->kv_empty[g & 1]);
         if (last) mma_commit_elect(&ms->o_full);
         __syncwarp();
       }
@@ -807,7 +783,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
           if (votes > 0) {
             // the previous tile's PV must be complete before O^T is touched
             const uint32_t gv = g - 1;
-            if (!fail && !mbar_wait(&ms->kv_empty[gv & 1][3], (gv >> 1) & 1, kWaitLimit)) fail = true;
+            if (!fail && !mbar_wait(&ms->kv_empty[gv & 1], (gv >> 1) & 1, kWaitLimit)) fail = true;
             fence_after_sync();
             if (!fail) {
 #pragma unroll 1
@@ -829,7 +805,7 @@ attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_rows, cons
         mb = nb;
         // P buffer g & 1 was last read by PV of tile g - 2 (another warp's
         // MMAs: S being ready does not imply it), so wait for that PV
-        if (g >= 2 && !fail && !mbar_wait(&ms->kv_empty[g & 1][3], ((g >> 1) - 1) & 1, kWaitLimit)) fail = true;
+        if (g >= 2 && !fail && !mbar_wait(&ms->kv_empty[g & 1], ((g >> 1) - 1) & 1, kWaitLimit)) fail = true;
         float sa = 0.0f, sb2 = 0.0f;
         uint8_t* dst = sP + (g & 1) * 8192;
 #pragma unroll
