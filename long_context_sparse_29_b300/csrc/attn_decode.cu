@@ -522,10 +522,12 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
       if (g >= 2 && !fail && !mbar_wait(&ms->kv_empty[g & 1], ((g >> 1) - 1) & 1, kWaitLimit)) fail = true;
       float sa = 0.0f, sb2 = 0.0f;
       uint8_t* dst = sP + (g & 1) * 8192;
+      // a head whose keys so far are all masked keeps m = -inf: its P is 0
+      const float mea = ma == -INFINITY ? 0.0f : ma, meb = mb == -INFINITY ? 0.0f : mb;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float pa0 = ex2(xa[2 * j] - ma), pa1 = ex2(xa[2 * j + 1] - ma);
-        const float pb0 = ex2(xb[2 * j] - mb), pb1 = ex2(xb[2 * j + 1] - mb);
+        const float pa0 = ex2(xa[2 * j] - mea), pa1 = ex2(xa[2 * j + 1] - mea);
+        const float pb0 = ex2(xb[2 * j] - meb), pb1 = ex2(xb[2 * j + 1] - meb);
         sa += pa0 + pa1;
         sb2 += pb0 + pb1;
         const __nv_bfloat162 qa = __floats2bfloat162_rn(pa0, pa1);
