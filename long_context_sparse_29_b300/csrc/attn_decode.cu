@@ -9,20 +9,22 @@
 //
 // The same arithmetic as attn_tc.cu (QK^T and PV on the tensor cores with
 // bf16 operands, fp32 accumulation in TMEM, online softmax in the exp2
-// domain with a lazy rescale), organised for a handful of rows in one
-// launch: a row's key slots -- its visible entries (dense) or its k selected
-// positions (an invalid index is a masked slot and sets the device-check
-// flag), then its window tokens -- are split over several CTAs (one work
-// item = one row and one split of its 64-key tiles).  Producer warps expand
-// each tile's 592-byte cache rows exactly to bf16 straight into shared
-// memory (the loads issued before the slot is free) with a mask of the valid
-// keys; the query is loaded by TMA and its RoPE dims rotated to its position
-// by the softmax warps.  Each item normalises its partial output (bf16) and
-// keeps its softmax statistics; the items of a row merge -- through one
-// thread-block cluster's shared memory (many rows) or through global memory
-// after a bounded per-row counter (few rows, many splits) -- each item one
-// slice of the row's dims over all splits in split order, with the RoPE
-// dims rotated back.
+// domain with a lazy rescale), organised for a handful of rows: a row's
+// keys are split over many CTAs (one work item = one row and one split, at
+// most one item per SM, every item resident at once: cooperative launch).
+// Two launches:
+//  * decode_gather_kernel writes every row's keys -- its valid selected
+//    entries in idx order (invalid ones set the device-check flag), or every
+//    visible entry, then its window tokens -- as contiguous bf16 rows
+//    (exact expansion of the 592-byte rows), with many CTAs per row;
+//  * attn_decode_kernel: the query is loaded by TMA and its RoPE dims
+//    rotated to its position in shared memory by the softmax warps; each
+//    64-key tile of the item's split is one set of TMA boxes from the
+//    gathered rows; each item writes its normalised partial output (bf16)
+//    and its softmax statistics, the items of a row meet at a bounded grid
+//    barrier (a counter per row), and each item then merges one slice of
+//    the row's dims over all splits in split order (inputs staged by bulk
+//    copies), rotates the RoPE dims back and stores the output.
 // Every wait is bounded; on expiry the CTA records the timeout flag in the
 // workspace, waits (bounded) for its own copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -70,7 +72,6 @@ struct Misc {
   uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
   uint64_t q_full, q_ready, o_full, drain[2], recv, merge_in;
   int go;                           // the row counter reached every split (global merge)
-  uint32_t kmask[2][2];             // per KV slot: which of its 64 keys are valid (bits)
   uint32_t tmem;
   int abort;
   alignas(16) float alpha[2][kH];   // per-head rescale factors of a tile, double-buffered
@@ -107,8 +108,135 @@ struct DParams {
   __nv_bfloat16* part_o;    // global merge: [items, 512 dims, 64 heads] normalised partial outputs
   float* part_ml;           // global merge: [items, 64, 2] running max (log2 units), sum
   int* arrive;              // global merge: [rows] items that finished their partial (zero at launch)
+  __nv_bfloat16* xg;        // [rows, kp, 512] every row's keys in bf16, in order, zero past them
+  int64_t kp;               // key slots per row of xg (a multiple of the tile)
+  int* ecount;              // [rows] valid selected entries of each row (sparse)
 };
 
+// ---------------------------------------------------------------------------
+// Per row, ahead of the attention: the row's keys -- its valid selected
+// entries in idx order (or every visible entry), then its window tokens --
+// expanded exactly from the 592-byte rows to bf16 rows of xg, 64 per CTA
+// (grid: the row's key tiles x rows), with zeros past the row's keys in its
+// last tile.  A sparse row's CTAs each find the valid entries of their tile
+// from idx (a block-wide count of the valid ones before each position);
+// invalid indices set the device-check flag (tile 0's CTA) and are skipped.
+// ---------------------------------------------------------------------------
+constexpr int kGatherThreads = 256;
+
+__global__ void __launch_bounds__(kGatherThreads)
+decode_gather_kernel(const DParams p) {
+  pdl_begin();
+  __shared__ int32_t src_s[kTile];            // this tile's selected entries
+  __shared__ unsigned int wcnt_s[kGatherThreads / 32];
+  __shared__ int ne_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = blockIdx.x;
+  const int64_t row = blockIdx.y;
+  const int64_t b = row / p.Tq;
+  const int64_t t = p.q_pos[row];
+  const bool t_ok = t >= 0 && t < p.rope_rows;
+  const bool dense = p.idx == nullptr;
+  int ne = 0;
+  if (t_ok && dense) {
+    const int64_t nv = (t + 1) / p.m;
+    ne = (int)(nv < p.N ? nv : p.N);
+  } else if (t_ok) {
+    // thread tid owns idx entries [16 tid, 16 tid + 16): valid ones counted,
+    // their ranks found by a block-wide exclusive scan of the counts
+    constexpr int kPer = 16;   // k <= 4096 = 256 x 16
+    const int32_t* ir = p.idx + row * (int64_t)p.k;
+    int32_t js[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int i = kPer * tid + r;
+      js[r] = i < p.k ? __ldg(ir + i) : -1;
+    }
+    uint32_t okbits = 0;
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int32_t j = js[r];
+      const bool ok = j >= 0 && (int64_t)j < p.N && (int64_t)(j + 1) * p.m - 1 <= t;
+      if (tile == 0 && j >= 0 && !ok) flag_device_check(p.ws, (unsigned)j);
+      okbits |= ok ? 1u << r : 0u;
+    }
+    const unsigned int own = __popc(okbits);
+    unsigned int incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wcnt_s[warp] = incl;
+    __syncthreads();
+    unsigned int before = 0, total = 0;
+    for (int w2 = 0; w2 < kGatherThreads / 32; ++w2) {
+      if (w2 < warp) before += wcnt_s[w2];
+      total += wcnt_s[w2];
+    }
+    unsigned int pos = before + incl - own;
+    const int lo = tile * kTile;
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      if ((okbits >> r) & 1u) {
+        if ((int)pos >= lo && (int)pos < lo + kTile) src_s[pos - lo] = js[r];
+        ++pos;
+      }
+    }
+    ne = (int)total;
+    if (tile == 0 && tid == 0) p.ecount[row] = ne;
+  }
+  if (dense && tile == 0 && tid == 0) p.ecount[row] = ne;
+  if (tid == 0) ne_s = ne;
+  __syncthreads();
+  ne = ne_s;
+  const int64_t u_lo = t - p.W + 1 < 0 ? 0 : t - p.W + 1;
+  const int64_t p0 = p.W > 0 ? p.swa_pos0[b] : 0;
+  const int64_t w_lo = u_lo < p0 ? p0 : u_lo;
+  const int64_t w_hi = t < p0 + p.Ts - 1 ? t : p0 + p.Ts - 1;
+  const int nwin = (t_ok && p.W > 0 && w_hi >= w_lo) ? (int)(w_hi - w_lo + 1) : 0;
+  const int nkeys = ne + nwin;
+  if (tile * kTile >= nkeys) return;   // past the row's keys (uniform)
+  // warp w: slots 8 w .. 8 w + 7 of the tile; all eight rows' loads in flight together
+  uint4 c[8];
+  float sc[8];
+  uint4 rp[8][2];
+  bool have[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int key = tile * kTile + 8 * warp + i;
+    const uint8_t* rowp = nullptr;
+    if (key < ne) rowp = p.cache + (b * p.N + (dense ? (int64_t)key : (int64_t)src_s[key - tile * kTile])) * kMixRow;
+    else if (key < nkeys) rowp = p.swa + (b * p.Ts + (w_lo - p0 + (key - ne))) * kMixRow;
+    have[i] = rowp != nullptr;
+    c[i] = make_uint4(0, 0, 0, 0);
+    sc[i] = 0.0f;
+    rp[i][0] = rp[i][1] = make_uint4(0, 0, 0, 0);
+    if (rowp) {
+      if (lane < 28) {
+        c[i] = __ldg(reinterpret_cast<const uint4*>(rowp) + lane);
+        sc[i] = __ldg(reinterpret_cast<const float*>(rowp + kMixScaleOff) + (lane >> 3));
+      } else {
+        rp[i][0] = __ldg(reinterpret_cast<const uint4*>(rowp + kMixRopeOff) + 2 * (lane - 28));
+        rp[i][1] = __ldg(reinterpret_cast<const uint4*>(rowp + kMixRopeOff) + 2 * (lane - 28) + 1);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int key = tile * kTile + 8 * warp + i;
+    uint4* dst = reinterpret_cast<uint4*>(p.xg + (row * p.kp + key) * kD);
+    if (lane < 28) {
+      uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+      if (have[i]) dequant16(c[i], sc[i], o0, o1);
+      dst[2 * lane] = o0;
+      dst[2 * lane + 1] = o1;
+    } else {
+      dst[56 + 2 * (lane - 28)] = rp[i][0];
+      dst[56 + 2 * (lane - 28) + 1] = rp[i][1];
+    }
+  }
+}
 
 // The merge of one dim slice [d0, d0 + nd) of a row over its ns splits:
 // rows[(c stride + dl) 128 bytes] holds split c's partial row of dim d0 + dl
@@ -166,7 +294,7 @@ __device__ __forceinline__ void merge_slice(const uint8_t* rows, uint32_t stride
 template <bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_po) {
+                   const __grid_constant__ CUtensorMap tm_xg, const __grid_constant__ CUtensorMap tm_po) {
   pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -192,7 +320,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   if (tid == 0) {
     ms->abort = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms->kv_full[i], 4);    // one arrival per producer warp once its rows are in
+      mbar_init(&ms->kv_full[i], 1);    // the tile's TMA boxes (one arrive with their byte count)
       mbar_init(&ms->kv_empty[i], 1);
       mbar_init(&ms->s_full[i], 1);
       mbar_init(&ms->p_full[i], 4);
@@ -221,15 +349,13 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     __syncwarp();
   }
   // ---- this item's keys: entries first, then the window tokens ----
-  // key slots: the visible entries (dense) or the k selected positions (an
-  // invalid index is a masked slot), then the window tokens
   int ne = 0;
   if (t_ok) {
     if (dense) {
       const int64_t nv = (t + 1) / p.m;
       ne = (int)(nv < p.N ? nv : p.N);
     } else {
-      ne = p.k;
+      ne = p.ecount[row];
     }
   }
   const int64_t u_lo = t - p.W + 1 < 0 ? 0 : t - p.W + 1;
@@ -251,88 +377,32 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
 
   if (warp >= 4 && warp < 8) {
     // ================================ producers ================================
-    // Warp pw expands rows 16 pw .. 16 pw + 15 of each 64-key tile from the
-    // 592-byte cache rows straight into the tile's shared-memory slot (bf16,
-    // 128-byte swizzle, 8 column boxes of 64 dims): lane l takes the FP8 16-byte
-    // chunks l + 32 m (m < 14) of the warp's 16 x 28 and the bf16 RoPE chunks
-    // l + 32 m (m < 4) of its 16 x 8.  All of a tile's loads are issued into
-    // registers before the slot is free (they fly while earlier tiles compute).
+    // the row's keys are contiguous bf16 rows of xg: 8 TMA boxes of 64 rows x
+    // 64 columns per tile, from producer warp 0 (the tile's other warps idle)
     const int pw = warp - 4;
     uint32_t g = 0;
     bool ok = true;
-    for (int tl = tlo; tl < thi && ok && !vabort(ms); ++tl, ++g) {
-      const int buf = g & 1;
-      // this warp's 16 rows: lane i < 16 resolves key slot 64 tl + 16 pw + i
-      const uint8_t* myrow = nullptr;
-      bool myok = false;
-      if (lane < 16) {
-        const int key = tl * kTile + 16 * pw + lane;
-        if (key < ne) {
-          int64_t j = key;
-          bool v = true;
-          if (!dense) {
-            j = __ldg(p.idx + row * (int64_t)p.k + key);
-            v = j >= 0 && j < p.N && (j + 1) * p.m - 1 <= t;
-            if (!v && j >= 0) flag_device_check(p.ws, (unsigned)j);
-          }
-          if (v) myrow = p.cache + (b * p.N + j) * kMixRow;
-        } else if (key < nkeys) {
-          myrow = p.swa + (b * p.Ts + (w_lo - p0 + (key - ne))) * kMixRow;
+    if (pw == 0) {
+      for (int tl = tlo; tl < thi && ok && !vabort(ms); ++tl, ++g) {
+        const int buf = g & 1;
+        if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          break;
         }
-        myok = myrow != nullptr;
+        const uint32_t tb = smem_u32(sKV + buf * 65536);
+        if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], kTile * kD * 2);
+        __syncwarp();
+        if (lane < 8)
+          tma_load_2d(tb + lane * 8192, &tm_xg, 64 * lane, (int)(row * p.kp + (int64_t)tl * kTile), &ms->kv_full[buf]);
+        __syncwarp();
       }
-      const uint32_t vbits = __ballot_sync(0xffffffffu, myok) & 0xffffu;
-      uint4 c[14];
-      float sc[14];
-      uint4 rp[4];
-#pragma unroll
-      for (int m = 0; m < 14; ++m) {
-        const int f = lane + 32 * m, rr = f / 28, ch = f - 28 * rr;
-        const uint64_t rw = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(myrow), rr);
-        const uint8_t* r = reinterpret_cast<const uint8_t*>(rw);
-        c[m] = make_uint4(0, 0, 0, 0);
-        sc[m] = 0.0f;
-        if (r) {
-          c[m] = __ldg(reinterpret_cast<const uint4*>(r) + ch);
-          sc[m] = __ldg(reinterpret_cast<const float*>(r + kMixScaleOff) + (ch >> 3));
-        }
+      if (!ok) {
+        ms->abort = 1;
+        if (lane == 0) flag_timeout(p.ws);
+        fail = true;
       }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int f = lane + 32 * m, rr = f >> 3, ch = f & 7;
-        const uint64_t rw = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(myrow), rr);
-        const uint8_t* r = reinterpret_cast<const uint8_t*>(rw);
-        rp[m] = r ? __ldg(reinterpret_cast<const uint4*>(r + kMixRopeOff) + ch) : make_uint4(0, 0, 0, 0);
-      }
-      if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
-        ok = false;
-        break;
-      }
-      uint8_t* kv = sKV + buf * 65536;
-#pragma unroll
-      for (int m = 0; m < 14; ++m) {
-        const int f = lane + 32 * m, rr = f / 28, ch = f - 28 * rr;
-        const uint32_t r = (uint32_t)(16 * pw + rr);
-        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-        if ((vbits >> rr) & 1u) dequant16(c[m], sc[m], o0, o1);
-        uint8_t* box = kv + (ch >> 2) * 8192;
-        *reinterpret_cast<uint4*>(box + sw128(r, 2u * (ch & 3))) = o0;
-        *reinterpret_cast<uint4*>(box + sw128(r, 2u * (ch & 3) + 1)) = o1;
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int f = lane + 32 * m, rr = f >> 3, ch = f & 7;
-        *reinterpret_cast<uint4*>(kv + 7 * 8192 + sw128((uint32_t)(16 * pw + rr), (uint32_t)ch)) = rp[m];
-      }
-      if (lane == 0) reinterpret_cast<uint16_t*>(&ms->kmask[buf][0])[pw] = (uint16_t)vbits;
-      fence_proxy_async();   // the rows were written through the generic proxy; the MMAs read them
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ms->kv_full[buf]);
-    }
-    if (!ok) {
-      ms->abort = 1;
-      if (lane == 0) flag_timeout(p.ws);
-      fail = true;
+      // the copies of this warp land before the CTA can exit
+      if (g > 0) mbar_wait(&ms->kv_full[(g - 1) & 1], ((g - 1) >> 1) & 1, kWaitLimit);
     }
   } else if (warp == kMmaWarp) {
     // ============================== QK^T issue ==============================
@@ -453,11 +523,8 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     bool stop = false;
     for (int tl = tlo; tl < thi; ++tl, ++g) {
       if (!fail && !mbar_wait(&ms->s_full[g & 1], (g >> 1) & 1, kWaitLimit)) fail = true;
-      // the producers' mask of this tile's valid keys (published with kv_full;
-      // S being ready implies it)
-      if (!fail && !mbar_wait(&ms->kv_full[g & 1], (g >> 1) & 1, kWaitLimit)) fail = true;
       fence_after_sync();
-      const uint64_t kmask = (uint64_t)ms->kmask[g & 1][0] | ((uint64_t)ms->kmask[g & 1][1] << 32);
+      const int nvalid = min(kTile, key_hi - tl * kTile);
       uint32_t v[32];
       tmem_ld16x256b_x8(tmem + tq_lane + kTmemS + 64u * (g & 1), v);
       tmem_wait_ld();
@@ -467,7 +534,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
       for (int j = 0; j < 8; ++j) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const bool valid = (kmask >> (8 * j + cq + e)) & 1ull;
+          const bool valid = 8 * j + cq + e < nvalid;
           xa[2 * j + e] = valid ? __uint_as_float(v[4 * j + e]) * p.scale_log2 : -INFINITY;
           xb[2 * j + e] = valid ? __uint_as_float(v[4 * j + 2 + e]) * p.scale_log2 : -INFINITY;
           ta = fmaxf(ta, xa[2 * j + e]);
@@ -522,12 +589,10 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
       if (g >= 2 && !fail && !mbar_wait(&ms->kv_empty[g & 1], ((g >> 1) - 1) & 1, kWaitLimit)) fail = true;
       float sa = 0.0f, sb2 = 0.0f;
       uint8_t* dst = sP + (g & 1) * 8192;
-      // a head whose keys so far are all masked keeps m = -inf: its P is 0
-      const float mea = ma == -INFINITY ? 0.0f : ma, meb = mb == -INFINITY ? 0.0f : mb;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float pa0 = ex2(xa[2 * j] - mea), pa1 = ex2(xa[2 * j + 1] - mea);
-        const float pb0 = ex2(xb[2 * j] - meb), pb1 = ex2(xb[2 * j + 1] - meb);
+        const float pa0 = ex2(xa[2 * j] - ma), pa1 = ex2(xa[2 * j + 1] - ma);
+        const float pb0 = ex2(xb[2 * j] - mb), pb1 = ex2(xb[2 * j + 1] - mb);
         sa += pa0 + pa1;
         sb2 += pb0 + pb1;
         const __nv_bfloat162 qa = __floats2bfloat162_rn(pa0, pa1);
@@ -865,10 +930,13 @@ bool attn_decode_applies(int H, int D, int R, int64_t rows, int k, bool sparse) 
   return H == kH && D == kD && R == 64 && rows > 0 && rows < sms && (!sparse || k <= kMaxK);
 }
 
+int64_t attn_decode_kp(int64_t max_keys) { return (max_keys + kTile - 1) / kTile * kTile; }
+
 size_t attn_decode_workspace(int64_t rows, int64_t max_keys) {
-  if (decode_cluster_merge(rows, max_keys)) return 0;
+  const size_t base = al256((size_t)rows * 4) + al256((size_t)rows * attn_decode_kp(max_keys) * kD * 2);
+  if (decode_cluster_merge(rows, max_keys)) return base;
   const int64_t items = rows * attn_decode_splits(rows, max_keys);
-  return al256((size_t)items * kH * kD * 2) + al256((size_t)items * kH * 2 * 4) + al256((size_t)rows * 4);
+  return base + al256((size_t)items * kH * kD * 2) + al256((size_t)items * kH * 2 * 4) + al256((size_t)rows * 4);
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
@@ -897,6 +965,11 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   const int64_t items = rows * p.nsplit;
   const bool cl = decode_cluster_merge(rows, a.max_keys);
   uint8_t* base = reinterpret_cast<uint8_t*>(a.ws) + kWsHeader;
+  p.ecount = reinterpret_cast<int*>(base);
+  base += al256((size_t)rows * 4);
+  p.kp = attn_decode_kp(a.max_keys);
+  p.xg = reinterpret_cast<__nv_bfloat16*>(base);
+  base += al256((size_t)rows * p.kp * kD * 2);
   p.part_o = nullptr;
   p.part_ml = nullptr;
   p.arrive = nullptr;
@@ -907,7 +980,7 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
     base += al256((size_t)items * kH * 2 * 4);
     p.arrive = reinterpret_cast<int*>(base);
   }
-  CUtensorMap tm_q, tm_po;
+  CUtensorMap tm_q, tm_xg, tm_po;
   memset(&tm_po, 0, sizeof(tm_po));
   {
     EncodeTiledFn fn = encode_fn();
@@ -929,12 +1002,19 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     }
+    const cuuint64_t gdims[2] = {(cuuint64_t)kD, (cuuint64_t)(rows * p.kp)};
+    if (fn(&tm_xg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.xg, gdims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaSuccess;
   if (!cl) {
     e = cudaMemsetAsync(p.arrive, 0, (size_t)rows * 4, st);
     if (e != cudaSuccess) return e;
   }
+  e = launch_pdl(decode_gather_kernel, dim3((unsigned)(p.kp / kTile), (unsigned)rows), dim3(kGatherThreads), 0, st, p);
+  if (e != cudaSuccess) return e;
   decode_clusters_resident(1);   // the kernels' shared-memory and cluster-size attributes, set once per device
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)items);
@@ -953,14 +1033,14 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
     attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<true>, p, tm_q, tm_po);
+    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<true>, p, tm_q, tm_xg, tm_po);
   }
   // every item resident at once (an item waits on its row's counter)
   attrs[0].id = cudaLaunchAttributeCooperative;
   attrs[0].val.cooperative = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<false>, p, tm_q, tm_po);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<false>, p, tm_q, tm_xg, tm_po);
 }
 
 }  // namespace csa
