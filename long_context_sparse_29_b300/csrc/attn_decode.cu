@@ -295,7 +295,7 @@ template <bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_xg, const __grid_constant__ CUtensorMap tm_po) {
-  pdl_begin();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm + kQOff;
@@ -341,13 +341,16 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   fence_after_sync();
   const uint32_t tmem = ms->tmem;
 
-  // ---- the query: 8 TMA boxes ----
+  // ---- the query: 8 TMA boxes (a caller input: issued before the wait) ----
   if (warp == kMmaWarp) {
     if (lane == 0) mbar_arrive_expect_tx(&ms->q_full, kH * kD * 2);
     __syncwarp();
     if (lane < 8) tma_load_2d(smem_u32(sQ) + lane * 8192, &tm_q, 64 * lane, (int)(row * kH), &ms->q_full);
     __syncwarp();
   }
+  // the gathered rows, their counts and the row counters come from the
+  // preceding launches
+  pdl_wait();
   // ---- this item's keys: entries first, then the window tokens ----
   int ne = 0;
   if (t_ok) {

@@ -49,6 +49,13 @@ __device__ __forceinline__ void pdl_begin() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+// The same in two halves, for kernels that first set up what touches no
+// memory another kernel of the library writes (shared memory, barriers,
+// TMEM, reads of the caller's inputs and constant tables): pdl_trigger at
+// the top, pdl_wait before the first access to data a preceding kernel of
+// the library may write (or that one may still read, before writing it).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // 2^n as fp32 for n in [-126, 127]
 __device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }

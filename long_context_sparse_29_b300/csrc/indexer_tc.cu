@@ -760,7 +760,7 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
                              const int64_t* __restrict__ q_pos, int64_t Tq,
                              int HI, int64_t N, int m, int64_t chunk, float* __restrict__ scores,
                              unsigned int* __restrict__ hist, void* ws, const __grid_constant__ CUtensorMap tm_k) {
-  pdl_begin();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DmMisc* ms = reinterpret_cast<DmMisc*>(sm + kDmMiscOff);
@@ -775,17 +775,11 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   const int64_t vrow0 = (b * N + c0) / 2;   // first row of the two-entry view
   const int n = (int)(c1 - c0);
 
-  // epilogue threads: the chunk's scale bytes and, threads 0..127, this
-  // thread's query values -- the loads in flight during the set-up
+  // threads 0..127: this thread's query values (a caller input), loaded
+  // before the wait on the preceding kernel, in flight during the set-up
   uint16_t v[kDmMaxChunk / kDmEpi];
   float qv[2][4];
   if (warp < kDmEpiWarps) {
-    const uint16_t* ks16 = reinterpret_cast<const uint16_t*>(ks) + b * N + c0;
-#pragma unroll
-    for (int r = 0; r < kDmMaxChunk / kDmEpi; ++r) {
-      const int i = tid + r * kDmEpi;
-      v[r] = i < n ? __ldg(ks16 + i) : (uint16_t)0;
-    }
     if (tid < 128) {
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
@@ -823,6 +817,16 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
   fence_after_sync();
   const uint32_t tmem = ms->tmem;
   bool ok = true;
+  // the keys (codes and scales) may come from the preceding kernel
+  pdl_wait();
+  if (warp < kDmEpiWarps) {
+    const uint16_t* ks16 = reinterpret_cast<const uint16_t*>(ks) + b * N + c0;
+#pragma unroll
+    for (int r = 0; r < kDmMaxChunk / kDmEpi; ++r) {
+      const int i = tid + r * kDmEpi;
+      v[r] = i < n ? __ldg(ks16 + i) : (uint16_t)0;
+    }
+  }
 
   if (warp == kDmTmaWarp) {
     // ---- TMA: tile u = one box of 128 view rows into stage u % kDmStages, once
