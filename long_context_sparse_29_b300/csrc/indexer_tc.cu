@@ -51,7 +51,7 @@ constexpr uint32_t kIxMiscOff = kIxKOff + kIxStages * kIxKTile;
 constexpr uint32_t kIxSmem = kIxMiscOff + 1024 + 1024;        // + slack for 1 KiB alignment
 
 constexpr uint32_t kIxWait = 1u << 20;
-constexpr uint32_t kIxSleepWait = 1u << 16;   // polls of up to 1 us each
+constexpr uint32_t kIxNapWait = 1u << 22;     // polls with ~64 ns naps between them (~0.3 s)
 
 struct IxMisc {
   uint64_t q_full, k_full[kIxStages], k_empty[kIxStages], t_full[kIxBufs], t_empty[kIxBufs], drain;
@@ -843,7 +843,7 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
       int u = 0;
       for (; u < ntiles; ++u) {
         const int s = u % kDmStages;
-        if (u >= kDmStages && !mbar_wait_sleep(&ms->empty[s], (uint32_t)(u / kDmStages - 1) & 1, kIxSleepWait, 1000)) break;
+        if (u >= kDmStages && !mbar_wait_backoff(&ms->empty[s], (uint32_t)(u / kDmStages - 1) & 1, kIxNapWait, 64)) break;
         mbar_arrive_expect_tx(&ms->full[s], 8192);   // the box's global bytes: the gaps are neither written nor counted
         tma_load_2d(aA + s * 16384, &tm_k, 0, (int)(vrow0 + (int64_t)u * (kDmEntries / 2)), &ms->full[s]);
         if (u >= kDmStages && u + kDmStages < ntiles) prefetch_tile(u + kDmStages);
@@ -865,8 +865,8 @@ scores_fp4_decode_tma_kernel(const __nv_bfloat16* __restrict__ qI, const float* 
     bool got = __all_sync(0xffffffffu, mbar_wait(&ms->qready, 0, kIxWait));
     for (int u = 0; u < ntiles && got; ++u) {
       const int s = u % kDmStages, tb = u % kDmTbufs;
-      got = mbar_wait_sleep(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxSleepWait, 1000);
-      if (got && u >= kDmTbufs) got = mbar_wait_sleep(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxSleepWait, 1000);
+      got = mbar_wait_backoff(&ms->full[s], (uint32_t)(u / kDmStages) & 1, kIxNapWait, 64);
+      if (got && u >= kDmTbufs) got = mbar_wait_backoff(&ms->tempty[tb], (uint32_t)(u / kDmTbufs - 1) & 1, kIxNapWait, 64);
       got = __all_sync(0xffffffffu, got);
       if (!got) break;
       fence_after_sync();

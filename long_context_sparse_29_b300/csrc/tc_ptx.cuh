@@ -301,21 +301,22 @@ __device__ __forceinline__ bool mbar_wait(void* bar, uint32_t parity, uint32_t l
   return false;
 }
 
-// mbar_wait for threads that are not on the critical path: each poll may
-// suspend the thread for up to `hint_ns` before it gives up (fewer issue
-// slots taken from the warps that do the work); gives up after `limit`
-// polls and returns false.
-__device__ __forceinline__ bool mbar_wait_sleep(void* bar, uint32_t parity, uint32_t limit, uint32_t hint_ns) {
+// mbar_wait for threads that are not on the critical path: after a poll that
+// finds the phase open the thread sleeps ~`nap_ns` before the next one (its
+// warp stops taking issue slots from the warps that do the work); gives up
+// after `limit` polls and returns false.
+__device__ __forceinline__ bool mbar_wait_backoff(void* bar, uint32_t parity, uint32_t limit, uint32_t nap_ns) {
   const uint32_t a = smem_u32(bar);
   for (uint32_t it = 0; it < limit; ++it) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(a), "r"(parity), "r"(hint_ns)
+        : "r"(a), "r"(parity)
         : "memory");
     if (done) return true;
+    __nanosleep(nap_ns);
   }
   return false;
 }
