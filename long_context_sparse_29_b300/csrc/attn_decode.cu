@@ -72,6 +72,7 @@ struct Misc {
   uint64_t kv_full[2], kv_empty[2], s_full[2], p_full[2];
   uint64_t q_full, q_ready, o_full, drain[2], recv, merge_in;
   int go;                           // the row counter reached every split (global merge)
+  uint32_t kmask[2][2];             // per KV slot: which of its 64 keys are valid (bits)
   uint32_t tmem;
   int abort;
   alignas(16) float alpha[2][kH];   // per-head rescale factors of a tile, double-buffered
@@ -105,6 +106,7 @@ struct DParams {
   float* lse;               // [rows, 64] or NULL
   void* ws;                 // status flags
   int nsplit;               // items per row (the cluster size when they merge through shared memory)
+  int expand;               // the producers expand the cache rows themselves (no gathered rows)
   __nv_bfloat16* part_o;    // global merge: [items, 512 dims, 64 heads] normalised partial outputs
   float* part_ml;           // global merge: [items, 64, 2] running max (log2 units), sum
   int* arrive;              // global merge: [rows] items that finished their partial (zero at launch)
@@ -320,7 +322,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   if (tid == 0) {
     ms->abort = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms->kv_full[i], 1);    // the tile's TMA boxes (one arrive with their byte count)
+      mbar_init(&ms->kv_full[i], p.expand ? 4 : 1);   // expanding: one arrival per producer warp; else the TMA boxes
       mbar_init(&ms->kv_empty[i], 1);
       mbar_init(&ms->s_full[i], 1);
       mbar_init(&ms->p_full[i], 4);
@@ -352,13 +354,16 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   // preceding launches
   pdl_wait();
   // ---- this item's keys: entries first, then the window tokens ----
+  // key slots: the visible entries (dense) or the row's valid selected
+  // entries (gathered) or all k selected positions (expanded here: an
+  // invalid index is a masked slot), then the window tokens
   int ne = 0;
   if (t_ok) {
     if (dense) {
       const int64_t nv = (t + 1) / p.m;
       ne = (int)(nv < p.N ? nv : p.N);
     } else {
-      ne = p.ecount[row];
+      ne = p.expand ? p.k : p.ecount[row];
     }
   }
   const int64_t u_lo = t - p.W + 1 < 0 ? 0 : t - p.W + 1;
@@ -379,33 +384,127 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   bool fail = false;
 
   if (warp >= 4 && warp < 8) {
-    // ================================ producers ================================
-    // the row's keys are contiguous bf16 rows of xg: 8 TMA boxes of 64 rows x
-    // 64 columns per tile, from producer warp 0 (the tile's other warps idle)
-    const int pw = warp - 4;
-    uint32_t g = 0;
-    bool ok = true;
-    if (pw == 0) {
+    if (p.expand) {
+      // ================================ producers ================================
+      // Warp pw expands rows 16 pw .. 16 pw + 15 of each 64-key tile from the
+      // 592-byte cache rows straight into the tile's shared-memory slot (bf16,
+      // 128-byte swizzle, 8 column boxes of 64 dims): lane l takes the FP8 16-byte
+      // chunks l + 32 m (m < 14) of the warp's 16 x 28 and the bf16 RoPE chunks
+      // l + 32 m (m < 4) of its 16 x 8.  All of a tile's loads are issued into
+      // registers before the slot is free (they fly while earlier tiles compute).
+      const int pw = warp - 4;
+      uint32_t g = 0;
+      bool ok = true;
       for (int tl = tlo; tl < thi && ok && !vabort(ms); ++tl, ++g) {
         const int buf = g & 1;
+        // this warp's 16 rows: lane i < 16 resolves key slot 64 tl + 16 pw + i
+        const uint8_t* myrow = nullptr;
+        bool myok = false;
+        if (lane < 16) {
+          const int key = tl * kTile + 16 * pw + lane;
+          if (key < ne) {
+            int64_t j = key;
+            bool v = true;
+            if (!dense) {
+              j = __ldg(p.idx + row * (int64_t)p.k + key);
+              v = j >= 0 && j < p.N && (j + 1) * p.m - 1 <= t;
+              if (!v && j >= 0) flag_device_check(p.ws, (unsigned)j);
+            }
+            if (v) myrow = p.cache + (b * p.N + j) * kMixRow;
+          } else if (key < nkeys) {
+            myrow = p.swa + (b * p.Ts + (w_lo - p0 + (key - ne))) * kMixRow;
+          }
+          myok = myrow != nullptr;
+        }
+        const uint32_t vbits = __ballot_sync(0xffffffffu, myok) & 0xffffu;
+        uint4 c[14];
+        float sc[14];
+        uint4 rp[4];
+#pragma unroll
+        for (int m = 0; m < 14; ++m) {
+          const int f = lane + 32 * m, rr = f / 28, ch = f - 28 * rr;
+          const uint64_t rw = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(myrow), rr);
+          const uint8_t* r = reinterpret_cast<const uint8_t*>(rw);
+          c[m] = make_uint4(0, 0, 0, 0);
+          sc[m] = 0.0f;
+          if (r) {
+            c[m] = __ldg(reinterpret_cast<const uint4*>(r) + ch);
+            sc[m] = __ldg(reinterpret_cast<const float*>(r + kMixScaleOff) + (ch >> 3));
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int f = lane + 32 * m, rr = f >> 3, ch = f & 7;
+          const uint64_t rw = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(myrow), rr);
+          const uint8_t* r = reinterpret_cast<const uint8_t*>(rw);
+          rp[m] = r ? __ldg(reinterpret_cast<const uint4*>(r + kMixRopeOff) + ch) : make_uint4(0, 0, 0, 0);
+        }
         if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
           ok = false;
           break;
         }
-        const uint32_t tb = smem_u32(sKV + buf * 65536);
-        if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], kTile * kD * 2);
+        uint8_t* kv = sKV + buf * 65536;
+#pragma unroll
+        for (int m = 0; m < 14; ++m) {
+          const int f = lane + 32 * m, rr = f / 28, ch = f - 28 * rr;
+          const uint32_t r = (uint32_t)(16 * pw + rr);
+          uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+          if ((vbits >> rr) & 1u) dequant16(c[m], sc[m], o0, o1);
+          uint8_t* box = kv + (ch >> 2) * 8192;
+          *reinterpret_cast<uint4*>(box + sw128(r, 2u * (ch & 3))) = o0;
+          *reinterpret_cast<uint4*>(box + sw128(r, 2u * (ch & 3) + 1)) = o1;
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int f = lane + 32 * m, rr = f >> 3, ch = f & 7;
+          *reinterpret_cast<uint4*>(kv + 7 * 8192 + sw128((uint32_t)(16 * pw + rr), (uint32_t)ch)) = rp[m];
+        }
+        if (lane == 0) reinterpret_cast<uint16_t*>(&ms->kmask[buf][0])[pw] = (uint16_t)vbits;
+        fence_proxy_async();   // the rows were written through the generic proxy; the MMAs read them
         __syncwarp();
-        if (lane < 8)
-          tma_load_2d(tb + lane * 8192, &tm_xg, 64 * lane, (int)(row * p.kp + (int64_t)tl * kTile), &ms->kv_full[buf]);
-        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->kv_full[buf]);
       }
       if (!ok) {
         ms->abort = 1;
         if (lane == 0) flag_timeout(p.ws);
         fail = true;
       }
-      // the copies of this warp land before the CTA can exit
-      if (g > 0) mbar_wait(&ms->kv_full[(g - 1) & 1], ((g - 1) >> 1) & 1, kWaitLimit);
+    } else {
+      // ================================ producers ================================
+      // the row's keys are contiguous bf16 rows of xg: 8 TMA boxes of 64 rows x
+      // 64 columns per tile, from producer warp 0 (the tile's other warps idle)
+      const int pw = warp - 4;
+      uint32_t g = 0;
+      bool ok = true;
+      if (pw == 0) {
+        for (int tl = tlo; tl < thi && ok && !vabort(ms); ++tl, ++g) {
+          const int buf = g & 1;
+          if (g >= 2 && !mbar_wait(&ms->kv_empty[buf], ((g >> 1) - 1) & 1, kWaitLimit)) {
+            ok = false;
+            break;
+          }
+          const uint32_t tb = smem_u32(sKV + buf * 65536);
+          if (lane == 0) {
+            // the tile's valid keys: those below the item's end
+            const int nvalid = min(kTile, key_hi - tl * kTile);
+            const uint64_t mk = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+            ms->kmask[buf][0] = (uint32_t)mk;
+            ms->kmask[buf][1] = (uint32_t)(mk >> 32);
+            mbar_arrive_expect_tx(&ms->kv_full[buf], kTile * kD * 2);
+          }
+          __syncwarp();
+          if (lane < 8)
+            tma_load_2d(tb + lane * 8192, &tm_xg, 64 * lane, (int)(row * p.kp + (int64_t)tl * kTile), &ms->kv_full[buf]);
+          __syncwarp();
+        }
+        if (!ok) {
+          ms->abort = 1;
+          if (lane == 0) flag_timeout(p.ws);
+          fail = true;
+        }
+        // the copies of this warp land before the CTA can exit
+        if (g > 0) mbar_wait(&ms->kv_full[(g - 1) & 1], ((g - 1) >> 1) & 1, kWaitLimit);
+      }
     }
   } else if (warp == kMmaWarp) {
     // ============================== QK^T issue ==============================
@@ -526,8 +625,11 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     bool stop = false;
     for (int tl = tlo; tl < thi; ++tl, ++g) {
       if (!fail && !mbar_wait(&ms->s_full[g & 1], (g >> 1) & 1, kWaitLimit)) fail = true;
+      // the producers' mask of this tile's valid keys (published with kv_full;
+      // S being ready implies it)
+      if (!fail && !mbar_wait(&ms->kv_full[g & 1], (g >> 1) & 1, kWaitLimit)) fail = true;
       fence_after_sync();
-      const int nvalid = min(kTile, key_hi - tl * kTile);
+      const uint64_t kmask = (uint64_t)ms->kmask[g & 1][0] | ((uint64_t)ms->kmask[g & 1][1] << 32);
       uint32_t v[32];
       tmem_ld16x256b_x8(tmem + tq_lane + kTmemS + 64u * (g & 1), v);
       tmem_wait_ld();
@@ -537,7 +639,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
       for (int j = 0; j < 8; ++j) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const bool valid = 8 * j + cq + e < nvalid;
+          const bool valid = (kmask >> (8 * j + cq + e)) & 1ull;
           xa[2 * j + e] = valid ? __uint_as_float(v[4 * j + e]) * p.scale_log2 : -INFINITY;
           xb[2 * j + e] = valid ? __uint_as_float(v[4 * j + 2 + e]) * p.scale_log2 : -INFINITY;
           ta = fmaxf(ta, xa[2 * j + e]);
@@ -592,10 +694,12 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
       if (g >= 2 && !fail && !mbar_wait(&ms->kv_empty[g & 1], ((g >> 1) - 1) & 1, kWaitLimit)) fail = true;
       float sa = 0.0f, sb2 = 0.0f;
       uint8_t* dst = sP + (g & 1) * 8192;
+      // a head whose keys so far are all masked keeps m = -inf: its P is 0
+      const float mea = ma == -INFINITY ? 0.0f : ma, meb = mb == -INFINITY ? 0.0f : mb;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float pa0 = ex2(xa[2 * j] - ma), pa1 = ex2(xa[2 * j + 1] - ma);
-        const float pb0 = ex2(xb[2 * j] - mb), pb1 = ex2(xb[2 * j + 1] - mb);
+        const float pa0 = ex2(xa[2 * j] - mea), pa1 = ex2(xa[2 * j + 1] - mea);
+        const float pb0 = ex2(xb[2 * j] - meb), pb1 = ex2(xb[2 * j + 1] - meb);
         sa += pa0 + pa1;
         sb2 += pb0 + pb1;
         const __nv_bfloat162 qa = __floats2bfloat162_rn(pa0, pa1);
@@ -935,11 +1039,25 @@ bool attn_decode_applies(int H, int D, int R, int64_t rows, int k, bool sparse) 
 
 int64_t attn_decode_kp(int64_t max_keys) { return (max_keys + kTile - 1) / kTile * kTile; }
 
+// Items of at most kExpandTiles key tiles expand the cache rows themselves
+// (each tile's row loads are one exposed round trip, cheaper than a gather
+// launch); longer items read rows gathered ahead of them (their loads ride
+// TMA boxes of gathered rows, two tiles deep).
+constexpr int kExpandTiles = 4;
+static bool decode_expand(int64_t rows, int64_t max_keys) {
+  const int64_t tiles = (max_keys + kTile - 1) / kTile;
+  const int64_t s = attn_decode_splits(rows, max_keys);
+  return (tiles + s - 1) / s <= kExpandTiles;
+}
 size_t attn_decode_workspace(int64_t rows, int64_t max_keys) {
-  const size_t base = al256((size_t)rows * 4) + al256((size_t)rows * attn_decode_kp(max_keys) * kD * 2);
-  if (decode_cluster_merge(rows, max_keys)) return base;
-  const int64_t items = rows * attn_decode_splits(rows, max_keys);
-  return base + al256((size_t)items * kH * kD * 2) + al256((size_t)items * kH * 2 * 4) + al256((size_t)rows * 4);
+  size_t bytes = decode_expand(rows, max_keys)
+                     ? 0
+                     : al256((size_t)rows * 4) + al256((size_t)rows * attn_decode_kp(max_keys) * kD * 2);
+  if (!decode_cluster_merge(rows, max_keys)) {
+    const int64_t items = rows * attn_decode_splits(rows, max_keys);
+    bytes += al256((size_t)items * kH * kD * 2) + al256((size_t)items * kH * 2 * 4) + al256((size_t)rows * 4);
+  }
+  return bytes;
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
@@ -967,12 +1085,17 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   p.nsplit = attn_decode_splits(rows, a.max_keys);
   const int64_t items = rows * p.nsplit;
   const bool cl = decode_cluster_merge(rows, a.max_keys);
+  p.expand = decode_expand(rows, a.max_keys) ? 1 : 0;
   uint8_t* base = reinterpret_cast<uint8_t*>(a.ws) + kWsHeader;
-  p.ecount = reinterpret_cast<int*>(base);
-  base += al256((size_t)rows * 4);
+  p.ecount = nullptr;
+  p.xg = nullptr;
   p.kp = attn_decode_kp(a.max_keys);
-  p.xg = reinterpret_cast<__nv_bfloat16*>(base);
-  base += al256((size_t)rows * p.kp * kD * 2);
+  if (!p.expand) {
+    p.ecount = reinterpret_cast<int*>(base);
+    base += al256((size_t)rows * 4);
+    p.xg = reinterpret_cast<__nv_bfloat16*>(base);
+    base += al256((size_t)rows * p.kp * kD * 2);
+  }
   p.part_o = nullptr;
   p.part_ml = nullptr;
   p.arrive = nullptr;
@@ -985,6 +1108,7 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   }
   CUtensorMap tm_q, tm_xg, tm_po;
   memset(&tm_po, 0, sizeof(tm_po));
+  memset(&tm_xg, 0, sizeof(tm_xg));
   {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorInvalidValue;
@@ -1005,19 +1129,24 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     }
-    const cuuint64_t gdims[2] = {(cuuint64_t)kD, (cuuint64_t)(rows * p.kp)};
-    if (fn(&tm_xg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.xg, gdims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-        CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    if (!p.expand) {
+      const cuuint64_t gdims[2] = {(cuuint64_t)kD, (cuuint64_t)(rows * p.kp)};
+      if (fn(&tm_xg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.xg, gdims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
   }
   cudaError_t e = cudaSuccess;
   if (!cl) {
     e = cudaMemsetAsync(p.arrive, 0, (size_t)rows * 4, st);
     if (e != cudaSuccess) return e;
   }
-  e = launch_pdl(decode_gather_kernel, dim3((unsigned)(p.kp / kTile), (unsigned)rows), dim3(kGatherThreads), 0, st, p);
-  if (e != cudaSuccess) return e;
+  if (!p.expand) {
+    e = launch_pdl(decode_gather_kernel, dim3((unsigned)(p.kp / kTile), (unsigned)rows), dim3(kGatherThreads), 0, st,
+                   p);
+    if (e != cudaSuccess) return e;
+  }
   decode_clusters_resident(1);   // the kernels' shared-memory and cluster-size attributes, set once per device
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)items);
