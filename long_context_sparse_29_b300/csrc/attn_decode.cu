@@ -293,7 +293,9 @@ __device__ __forceinline__ void merge_slice(const uint8_t* rows, uint32_t stride
 // kCluster: the items of a row are one thread-block cluster and merge through
 // each other's shared memory; otherwise they write their partials to global
 // memory, meet at a per-row counter (cooperative launch) and merge from there.
-template <bool kCluster>
+// kExpand: the producers expand the cache rows themselves (a mask marks the
+// valid keys of each tile); otherwise they load rows gathered ahead.
+template <bool kCluster, bool kExpand>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_xg, const __grid_constant__ CUtensorMap tm_po) {
@@ -322,7 +324,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   if (tid == 0) {
     ms->abort = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms->kv_full[i], p.expand ? 4 : 1);   // expanding: one arrival per producer warp; else the TMA boxes
+      mbar_init(&ms->kv_full[i], kExpand ? 4 : 1);   // expanding: one arrival per producer warp; else the TMA boxes
       mbar_init(&ms->kv_empty[i], 1);
       mbar_init(&ms->s_full[i], 1);
       mbar_init(&ms->p_full[i], 4);
@@ -363,7 +365,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
       const int64_t nv = (t + 1) / p.m;
       ne = (int)(nv < p.N ? nv : p.N);
     } else {
-      ne = p.expand ? p.k : p.ecount[row];
+      ne = kExpand ? p.k : p.ecount[row];
     }
   }
   const int64_t u_lo = t - p.W + 1 < 0 ? 0 : t - p.W + 1;
@@ -384,7 +386,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   bool fail = false;
 
   if (warp >= 4 && warp < 8) {
-    if (p.expand) {
+    if constexpr (kExpand) {
       // ================================ producers ================================
       // Warp pw expands rows 16 pw .. 16 pw + 15 of each 64-key tile from the
       // 592-byte cache rows straight into the tile's shared-memory slot (bf16,
@@ -484,14 +486,7 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
             break;
           }
           const uint32_t tb = smem_u32(sKV + buf * 65536);
-          if (lane == 0) {
-            // the tile's valid keys: those below the item's end
-            const int nvalid = min(kTile, key_hi - tl * kTile);
-            const uint64_t mk = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
-            ms->kmask[buf][0] = (uint32_t)mk;
-            ms->kmask[buf][1] = (uint32_t)(mk >> 32);
-            mbar_arrive_expect_tx(&ms->kv_full[buf], kTile * kD * 2);
-          }
+          if (lane == 0) mbar_arrive_expect_tx(&ms->kv_full[buf], kTile * kD * 2);
           __syncwarp();
           if (lane < 8)
             tma_load_2d(tb + lane * 8192, &tm_xg, 64 * lane, (int)(row * p.kp + (int64_t)tl * kTile), &ms->kv_full[buf]);
@@ -625,11 +620,18 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
     bool stop = false;
     for (int tl = tlo; tl < thi; ++tl, ++g) {
       if (!fail && !mbar_wait(&ms->s_full[g & 1], (g >> 1) & 1, kWaitLimit)) fail = true;
-      // the producers' mask of this tile's valid keys (published with kv_full;
-      // S being ready implies it)
-      if (!fail && !mbar_wait(&ms->kv_full[g & 1], (g >> 1) & 1, kWaitLimit)) fail = true;
-      fence_after_sync();
-      const uint64_t kmask = (uint64_t)ms->kmask[g & 1][0] | ((uint64_t)ms->kmask[g & 1][1] << 32);
+      // the tile's valid keys: the expanding producers' mask (published with
+      // kv_full; S being ready implies it), or those below the item's end
+      uint64_t kmask;
+      if constexpr (kExpand) {
+        if (!fail && !mbar_wait(&ms->kv_full[g & 1], (g >> 1) & 1, kWaitLimit)) fail = true;
+        fence_after_sync();
+        kmask = (uint64_t)ms->kmask[g & 1][0] | ((uint64_t)ms->kmask[g & 1][1] << 32);
+      } else {
+        fence_after_sync();
+        const int nvalid = min(kTile, key_hi - tl * kTile);
+        kmask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+      }
       uint32_t v[32];
       tmem_ld16x256b_x8(tmem + tq_lane + kTmemS + 64u * (g & 1), v);
       tmem_wait_ld();
@@ -695,7 +697,8 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
       float sa = 0.0f, sb2 = 0.0f;
       uint8_t* dst = sP + (g & 1) * 8192;
       // a head whose keys so far are all masked keeps m = -inf: its P is 0
-      const float mea = ma == -INFINITY ? 0.0f : ma, meb = mb == -INFINITY ? 0.0f : mb;
+      // (only with expanded rows: a gathered item's first tile has a key)
+      const float mea = (kExpand && ma == -INFINITY) ? 0.0f : ma, meb = (kExpand && mb == -INFINITY) ? 0.0f : mb;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float pa0 = ex2(xa[2 * j] - mea), pa1 = ex2(xa[2 * j + 1] - mea);
@@ -975,12 +978,14 @@ int decode_clusters_resident(int s) {
   static PerDevice attrs;
   static PerDevice count[kMaxSplits + 1];
   attrs.get([] {
-    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel<true>),
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel<false>),
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    cudaFuncSetAttribute(reinterpret_cast<const void*>(attn_decode_kernel<true>),
-                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    const void* ks[4] = {reinterpret_cast<const void*>(attn_decode_kernel<true, false>),
+                         reinterpret_cast<const void*>(attn_decode_kernel<true, true>),
+                         reinterpret_cast<const void*>(attn_decode_kernel<false, false>),
+                         reinterpret_cast<const void*>(attn_decode_kernel<false, true>)};
+    for (int i = 0; i < 4; ++i) {
+      cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      if (i < 2) cudaFuncSetAttribute(ks[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
     cudaGetLastError();
     return 1;
   });
@@ -998,7 +1003,7 @@ int decode_clusters_resident(int s) {
            cfg.attrs = at;
            cfg.numAttrs = 1;
            int n = 0;
-           if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(attn_decode_kernel<true>), &cfg) !=
+           if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(attn_decode_kernel<true, false>), &cfg) !=
                cudaSuccess) {
              cudaGetLastError();
              n = 0;
@@ -1165,14 +1170,16 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
     attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<true>, p, tm_q, tm_xg, tm_po);
+    return p.expand ? cudaLaunchKernelEx(&cfg, attn_decode_kernel<true, true>, p, tm_q, tm_xg, tm_po)
+                    : cudaLaunchKernelEx(&cfg, attn_decode_kernel<true, false>, p, tm_q, tm_xg, tm_po);
   }
   // every item resident at once (an item waits on its row's counter)
   attrs[0].id = cudaLaunchAttributeCooperative;
   attrs[0].val.cooperative = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<false>, p, tm_q, tm_xg, tm_po);
+  return p.expand ? cudaLaunchKernelEx(&cfg, attn_decode_kernel<false, true>, p, tm_q, tm_xg, tm_po)
+                  : cudaLaunchKernelEx(&cfg, attn_decode_kernel<false, false>, p, tm_q, tm_xg, tm_po);
 }
 
 }  // namespace csa
