@@ -10,21 +10,24 @@
 // The same arithmetic as attn_tc.cu (QK^T and PV on the tensor cores with
 // bf16 operands, fp32 accumulation in TMEM, online softmax in the exp2
 // domain with a lazy rescale), organised for a handful of rows: a row's
-// keys are split over many CTAs (one work item = one row and one split, at
-// most one item per SM, every item resident at once: cooperative launch).
-// Two launches:
-//  * decode_gather_kernel writes every row's keys -- its valid selected
-//    entries in idx order (invalid ones set the device-check flag), or every
-//    visible entry, then its window tokens -- as contiguous bf16 rows
-//    (exact expansion of the 592-byte rows), with many CTAs per row;
-//  * attn_decode_kernel: the query is loaded by TMA and its RoPE dims
-//    rotated to its position in shared memory by the softmax warps; each
-//    64-key tile of the item's split is one set of TMA boxes from the
-//    gathered rows; each item writes its normalised partial output (bf16)
-//    and its softmax statistics, the items of a row meet at a bounded grid
-//    barrier (a counter per row), and each item then merges one slice of
-//    the row's dims over all splits in split order (inputs staged by bulk
-//    copies), rotates the RoPE dims back and stores the output.
+// keys are split over several CTAs (one work item = one row and one split of
+// its 64-key tiles).  The keys of a tile reach shared memory one of two ways:
+//  * gathered: decode_gather_kernel first writes every row's keys -- its
+//    valid selected entries in idx order (invalid ones set the device-check
+//    flag), or every visible entry, then its window tokens -- as contiguous
+//    bf16 rows (exact expansion of the 592-byte rows), with many CTAs per
+//    row, and each tile is one set of TMA boxes from them;
+//  * expanded (items of few tiles): four producer warps load the tile's
+//    592-byte rows into registers before its slot is free and write their
+//    exact bf16 expansion into the slot, with a mask of the valid keys (an
+//    invalid selected index is a masked slot).
+// The query is loaded by TMA and its RoPE dims rotated to its position in
+// shared memory by the softmax warps.  Each item normalises its partial
+// output (bf16) and keeps its softmax statistics; the items of a row merge
+// -- through one thread-block cluster's shared memory (many rows) or through
+// global memory after a bounded per-row counter (few rows, many splits) --
+// each item one slice of the row's dims over all splits in split order, with
+// the RoPE dims rotated back.
 // Every wait is bounded; on expiry the CTA records the timeout flag in the
 // workspace, waits (bounded) for its own copies and MMAs and frees TMEM.
 #include <cuda.h>
