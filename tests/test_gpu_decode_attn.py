@@ -142,3 +142,39 @@ def test_decode_in_item_rescale(csa, oracle_mod):
     assert bad == 0
     for b in (0, 57, 99):
         assert max_rel_err(got[b:b + 1], ref) <= 1e-2
+
+
+@pytest.mark.parametrize("B,k", [
+    (2, 300),     # a few tiles per item: the items expand the cache rows themselves (masked slots)
+    (40, 2000),   # many tiles per item: rows gathered ahead (invalid entries compacted away)
+])
+def test_decode_invalid_indices_scattered(csa, oracle_mod, B, k):
+    """Selected lists with invalid indices (-1, past the cache, not yet
+    visible) scattered through them, not only at the end: the oracle skips
+    them; the kernels mask or compact them and set the device-check flag."""
+    rng = np.random.default_rng(5000 + B)
+    N, m, W, Ts = 4096, 4, 64, 128
+    T = N * m
+    rope_np, rope_dev = oracle_mod.rope_table(T + 1, 64), csa.rope_table(T + 1, 64)
+    cache, swa = _caches(oracle_mod, rng, B, N, Ts)
+    q = wl.f32_to_bf16_bits(rng.standard_normal((B, 1, 64, 512)).astype(np.float32))
+    q_pos = np.full((B, 1), T - 1 - 4 * 100, np.int64)          # entries >= 3996 not yet visible
+    pos0 = (q_pos[:, 0] - Ts + 1).astype(np.int64)
+    idx = np.stack([rng.permutation(N)[:k].astype(np.int32) for _ in range(B)])[:, None, :]
+    bad = rng.random(idx.shape) < 0.1
+    kinds = rng.integers(0, 3, size=idx.shape)
+    idx = np.where(bad & (kinds == 0), -1, idx)
+    idx = np.where(bad & (kinds == 1), N + 7, idx)                # past the cache
+    idx = np.where(bad & (kinds == 2), N - 1, idx)                # not visible at q_pos
+    idx = idx.astype(np.int32)
+    ws = csa.Workspace()
+    out, lse = csa.sparse_mqa(dev_bf16(q), dev(q_pos), dev(cache), m, dev(idx), dev(swa), dev(pos0), W,
+                              1 / math.sqrt(512), rope_dev, lse=True, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.flags() & csa.FLAG_DEVICE_CHECK
+    ref, rlse, nbad = oracle_mod.attention(wl.bf16_bits_to_f32(q), q_pos, cache, N, m, idx, swa, pos0, W,
+                                           1 / math.sqrt(512), rope_np, 64)
+    assert nbad > 0
+    got = out.float().cpu().numpy()
+    assert max_rel_err(got, ref) <= 1e-2, max_rel_err(got, ref)
+    np.testing.assert_allclose(lse.cpu().numpy(), rlse, rtol=0, atol=2e-2)
