@@ -463,6 +463,18 @@ def decode_bytes(cfg) -> float:
     return float(cfg.B * (per_q + append))
 
 
+def decode_layer_kernels(cfg, sms):
+    """Kernels one decode layer launches per step, by the library's rule: a
+    row's 64-key tiles are split over min(SMs // rows, tiles) items (for at
+    most 8 items the device must also hold every row's cluster at once, true
+    for these configurations); items of at most 4 tiles expand the cache rows
+    themselves, longer ones read rows gathered by one more kernel."""
+    tiles = -(-((cfg.k if cfg.k else cfg.N) + cfg.W) // 64)
+    splits = max(1, min(sms // cfg.B, tiles))
+    gather = -(-tiles // splits) > 4
+    return 1 + (2 if cfg.k else 0) + 1 + (1 if gather else 0)
+
+
 def run_config(args, name):
     import torch
     import long_context_sparse_29_b300 as csa
@@ -513,10 +525,11 @@ def run_config(args, name):
         l2 = "caches resident; each step reads them once (larger than L2 except the HCA-only step)"
         step_desc = "decode_append + indexer_topk + sparse_mqa (CSA) / decode_append + hca_dense_attn (HCA), " \
                     "one CUDA graph per step"
-        # kernels per step: CSA layer 5 (append; scores with the score
-        # histogram, histogram top-k; row gather, attention with the split
-        # merge), HCA layer 3 (append; row gather, attention)
-        launches = sum(5 if c.k else 3 for c in layers)
+        # kernels per step: per layer the append; for CSA the scores (with
+        # the score histogram) and the histogram top-k; the attention, and
+        # before it the row gather when the attention's items are long
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        launches = sum(decode_layer_kernels(c, sms) for c in layers)
     elif name == "c2_csa_prefill_128k":
         cfg = wl.CONFIGS[name]
         T, W, m, Tc = cfg.T, cfg.W, cfg.m, 8192
