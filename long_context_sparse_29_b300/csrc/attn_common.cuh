@@ -102,34 +102,5 @@ __device__ __forceinline__ void dequant16(const uint4 c, float sc, uint4& o0, ui
   o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
-// 8 E4M3 codes (c.x: codes 0-3, c.y: codes 4-7) times sc -> 8 bf16, exact
-// (the expansion of dequant16 on half the codes).
-__device__ __forceinline__ uint4 dequant8(const uint2 c, float sc) {
-  const uint32_t w[2] = {c.x, c.y};
-  uint32_t r[4];
-  if (sc <= 128.0f) {
-    const float s120 = __fmul_rn(sc, 0x1p120f);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float f0 = __fmul_rn(__uint_as_float(e4m3_bits(w[i], 0)), s120);
-      const float f1 = __fmul_rn(__uint_as_float(e4m3_bits(w[i], 1)), s120);
-      const float f2 = __fmul_rn(__uint_as_float(e4m3_bits(w[i], 2)), s120);
-      const float f3 = __fmul_rn(__uint_as_float(e4m3_bits(w[i], 3)), s120);
-      r[2 * i] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-      r[2 * i + 1] = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      float f[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) f[j] = __fmul_rn(__fmul_rn(__uint_as_float(e4m3_bits(w[i], j)), 0x1p120f), sc);
-      r[2 * i] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632);
-      r[2 * i + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632);
-    }
-  }
-  return make_uint4(r[0], r[1], r[2], r[3]);
-}
-
 }  // namespace attn
 }  // namespace csa
