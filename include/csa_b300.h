@@ -107,9 +107,12 @@ int csa_rope_table(int64_t P, int R, double base, float *cos_out, float *sin_out
  * dim D, the largest key count per query max_keys (attention: k + W for CSA,
  * entries + W for HCA) and Ts window-cache rows per sequence.  Never less
  * than 256 (the status block).  Returns -1 for an unknown op.  The attention
- * calls use the space for split-softmax partial states (few queries) and
- * for a bf16 copy of the cache rows when every row serves many queries
- * (prefill); with less workspace they fall back to slower plans.
+ * calls use the space for a bf16 copy of the cache rows when every row serves
+ * many queries (prefill), and for few queries (decode) for the bf16 rows each
+ * query's keys are gathered into when a query's keys span many tiles and for
+ * the split-softmax partial states when a query's keys are split over more
+ * CTAs than one thread-block cluster holds; with less workspace they fall
+ * back to slower plans.
  */
 int64_t csa_workspace_size(int op, int B, int64_t Tq, int64_t N, int k, int H, int D,
                            int64_t max_keys, int64_t Ts);
