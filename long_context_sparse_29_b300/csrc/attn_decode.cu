@@ -886,9 +886,9 @@ attn_decode_kernel(const DParams p, const __grid_constant__ CUtensorMap tm_q,
   const int d0 = min(kD, split * dp), d1 = min(kD, d0 + dp);
   const int nd = d1 - d0;
   // shared memory is free now: the row's statistics [ns][64] (m, l) at 0,
-  // this slice's partial rows [ns][nd] of 128 bytes after them (16-byte chunk
-  // c of dim d's row at chunk c ^ (d mod 8), as written), staged by bulk
-  // copies (all in flight together)
+  // this slice's partial rows [ns][nd] of 128 bytes after them (plain rows:
+  // the tensor map of the partials' store undid the staging swizzle), staged
+  // by bulk copies (all in flight together)
   const uint32_t ml_bytes = (uint32_t)ns * kH * 8;
   const uint32_t sl_off = (ml_bytes + 1023) & ~1023u;
   const float2* ml_s = reinterpret_cast<const float2*>(sm);
