@@ -276,6 +276,7 @@ def run_ours(args, rank, world, local_rank):
                             "unit": dec["unit"], "ms_per_step": dec["ms_per_step"], "steps": dec["steps"],
                             "algorithmic_bytes_per_step": r["algorithmic_bytes_per_step"],
                             "achieved_gbs": r["achieved"], "peak_gbs": r["peak"], "hbm_frac": r["frac"],
+                            "traffic_per_step": r["traffic"],
                             "peak_src": r["peak_src"], "gpu_launches": dec["gpu_launches"],
                             "clocks": dec["clocks"], "step": dec["config"]["step"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -296,6 +297,13 @@ LAUNCHES_PER_STEP = 11
 # one ncu capture of it (dram__bytes_read.sum + dram__bytes_write.sum); to be
 # set to None when the kernel changes, until it is captured again
 ATTN_TRAFFIC = 631751936 + 493387520
+
+# DRAM bytes (read + write) of one decode step of the 4 x 1M hybrid workload:
+# the sum over the step's six kernels (CSA append, scores, top-k, attention;
+# HCA append, attention), from ncu captures of this build (cold cache:
+# dram__bytes_read.sum + dram__bytes_write.sum; nothing is written back
+# within a launch); None where no capture covers every kernel of the step
+DECODE_STEP_TRAFFIC = {"c5_hybrid_csa_decode_1m": 69888 + 35717120 + 4297728 + 3613696 + 575488 + 20105216}
 
 
 # --------------------------------------------------------------------------
@@ -640,7 +648,7 @@ def run_config(args, name):
         ach = roof["algorithmic_bytes_per_step"] / (ms * 1e-3) / 1e9
     else:
         ach = roof["algorithmic_flops_per_step"] / (ms * 1e-3) / 1e12
-    roof.update({"achieved": ach, "frac": ach / roof["peak"], "traffic": None,
+    roof.update({"achieved": ach, "frac": ach / roof["peak"], "traffic": DECODE_STEP_TRAFFIC.get(name),
                  "peak_src": f"{pk['src']} ({'HBM copy' if roof['bound'] == 'hbm' else 'bf16 dense, burst'})",
                  "note": "the whole step (all its launches) timed with CUDA events"})
     cfg0 = layers[0]
