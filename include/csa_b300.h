@@ -325,7 +325,7 @@ int hca_dense_attn(const void *q, int q_dtype, const int64_t *q_pos, int B, int6
 
 /*
  * csa_indexer_topk_noalloc: csa_indexer_topk without a caller workspace.
- * The paper has no counterpart to this call; it exists for callers that
+ * The method has no counterpart to this call; it exists for callers that
  * cannot allocate device memory.  Serving runtimes that plan every device
  * buffer before they start and refuse allocation afterwards, and plugins
  * that such a runtime hands the tensors of one call but no allocator,
