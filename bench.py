@@ -300,7 +300,7 @@ ATTN_TRAFFIC = 631751936 + 493387520
 
 # DRAM bytes (read + write) of one decode step of the 4 x 1M hybrid workload:
 # the sum over the step's six kernels (CSA append, scores, top-k, attention;
-# HCA append, attention), from ncu captures of this build (cold cache:
+# HCA append, attention), from ncu captures of the current kernels (cold cache:
 # dram__bytes_read.sum + dram__bytes_write.sum; nothing is written back
 # within a launch); None where no capture covers every kernel of the step
 DECODE_STEP_TRAFFIC = {"c5_hybrid_csa_decode_1m": 69888 + 35717120 + 4297728 + 3613696 + 575488 + 20105216}
